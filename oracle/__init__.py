@@ -1,0 +1,158 @@
+"""Python access to the CPU oracle (oracle.c) for the tests, the smoke check and
+the bench's CPU-baseline leg.
+
+TEST INFRASTRUCTURE ONLY: the product package never imports this module.  It
+shares no code with the CUDA library; the only code the two sides share is the
+seeded input generator module ``synth``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+CFLAGS = ["-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off", "-Wall", "-shared",
+          "-fPIC"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_double.restype = ctypes.c_double
+        L.oracle_q4_k_scale_min.argtypes = [_P, ctypes.c_int, _P, _P]
+        L.oracle_q4_k_scale_min.restype = None
+        L.oracle_dequant_row.argtypes = [ctypes.c_int, _P, _I64, _P]
+        L.oracle_int_weights_row.argtypes = [ctypes.c_int, _P, _I64, _P]
+        L.oracle_matvec.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, ctypes.c_int, _I64, _I64,
+                                    _P, _P]
+        L.oracle_quantize_act.argtypes = [_P, _I64, _I64, _P, _P, _P]
+        L.oracle_blockdots.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _I64, _P, _I64, _I64,
+                                       _I64, _P]
+        L.oracle_mmq.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _P, _I64, _P, _I64, _I64,
+                                 _I64, _P, _P]
+        for f in ("oracle_dequant_row", "oracle_int_weights_row", "oracle_matvec",
+                  "oracle_quantize_act", "oracle_blockdots", "oracle_mmq"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed (rc={rc})")
+
+
+def f16_to_double(bits: int) -> float:
+    return lib().oracle_f16_to_double(bits)
+
+
+def q4_k_scale_min(s12: bytes, j: int):
+    buf = np.frombuffer(bytes(s12), dtype=np.uint8).copy()
+    sc, mn = ctypes.c_int(), ctypes.c_int()
+    lib().oracle_q4_k_scale_min(_ptr(buf), j, ctypes.byref(sc), ctypes.byref(mn))
+    return sc.value, mn.value
+
+
+def dequant_row(qtype: int, row: np.ndarray, K: int) -> np.ndarray:
+    row = np.ascontiguousarray(row, dtype=np.uint8)
+    out = np.empty(K, dtype=np.float64)
+    _check(lib().oracle_dequant_row(qtype, _ptr(row), K, _ptr(out)), "dequant_row")
+    return out
+
+
+def dequant(qtype: int, W: np.ndarray, N: int, K: int) -> np.ndarray:
+    W = np.ascontiguousarray(W, dtype=np.uint8).reshape(N, -1)
+    return np.stack([dequant_row(qtype, W[n], K) for n in range(N)]) if N else \
+        np.zeros((0, K))
+
+
+def int_weights_row(qtype: int, row: np.ndarray, K: int) -> np.ndarray:
+    row = np.ascontiguousarray(row, dtype=np.uint8)
+    out = np.empty(K, dtype=np.int64)
+    _check(lib().oracle_int_weights_row(qtype, _ptr(row), K, _ptr(out)), "int_weights_row")
+    return out
+
+
+def matvec(qtype: int, W: np.ndarray, N: int, K: int, x: np.ndarray, n0: int = 0,
+           n1: int | None = None):
+    """Returns (y, bound), each float64 [B][n1-n0]."""
+    n1 = N if n1 is None else n1
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
+    B = x.shape[0]
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    y = np.empty((B, n1 - n0), dtype=np.float64)
+    bnd = np.empty_like(y)
+    _check(lib().oracle_matvec(qtype, _ptr(W), N, K, _ptr(x), B, n0, n1, _ptr(y), _ptr(bnd)),
+           "matvec")
+    return y, bnd
+
+
+def quantize_act(x: np.ndarray):
+    """Returns (qs int8 [M][K], scale f32 [M][K/32], bsum int32 [M][K/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, K = x.shape
+    qs = np.empty((M, K), dtype=np.int8)
+    sc = np.empty((M, K // 32), dtype=np.float32)
+    bs = np.empty((M, K // 32), dtype=np.int32)
+    _check(lib().oracle_quantize_act(_ptr(x), M, K, _ptr(qs), _ptr(sc), _ptr(bs)),
+           "quantize_act")
+    return qs, sc, bs
+
+
+def blockdots(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, mrows=None,
+              n0: int = 0, n1: int | None = None) -> np.ndarray:
+    """Returns int64 D [len(mrows)][n1-n0][K/32]."""
+    n1 = N if n1 is None else n1
+    qs = np.ascontiguousarray(qs, dtype=np.int8)
+    M = qs.shape[0]
+    mrows = np.arange(M, dtype=np.int64) if mrows is None else \
+        np.ascontiguousarray(mrows, dtype=np.int64)
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    D = np.empty((len(mrows), n1 - n0, K // 32), dtype=np.int64)
+    _check(lib().oracle_blockdots(qtype, _ptr(W), N, K, _ptr(qs), M, _ptr(mrows), len(mrows),
+                                  n0, n1, _ptr(D)), "blockdots")
+    return D
+
+
+def mmq(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, scale: np.ndarray,
+        mrows=None, n0: int = 0, n1: int | None = None):
+    """Returns (y, bound), float64 [len(mrows)][n1-n0]."""
+    n1 = N if n1 is None else n1
+    qs = np.ascontiguousarray(qs, dtype=np.int8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M = qs.shape[0]
+    mrows = np.arange(M, dtype=np.int64) if mrows is None else \
+        np.ascontiguousarray(mrows, dtype=np.int64)
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    y = np.empty((len(mrows), n1 - n0), dtype=np.float64)
+    bnd = np.empty_like(y)
+    _check(lib().oracle_mmq(qtype, _ptr(W), N, K, _ptr(qs), _ptr(scale), M, _ptr(mrows),
+                            len(mrows), n0, n1, _ptr(y), _ptr(bnd)), "mmq")
+    return y, bnd

@@ -1,0 +1,363 @@
+"""Pins for the CPU oracle, against facts that do not come from the oracle itself:
+hand-worked golden blocks (tests/golden/), IEEE binary16 as numpy decodes it,
+invariants of the block formats and of the activation quantiser, special cases
+that reduce to a plain float64 matrix product, Python big-integer brute force, and
+a second, vectorised decoder.  CPU only."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gguf_pack as gp
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read(name):
+    kv, flips = {}, []
+    for line in open(os.path.join(GOLD, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = line.split(":", 1)
+        if k == "flip":
+            flips.append(v.split())
+        else:
+            kv[k] = v.strip()
+    return kv, flips
+
+
+def _ints(s):
+    return [int(t) for t in s.split()]
+
+
+# ---- IEEE binary16 ---------------------------------------------------------
+
+def test_f16_all_bit_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_f16_golden_values():
+    for line in open(os.path.join(GOLD, "f16_values.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        b, v = line.split()
+        got = oracle.f16_to_double(int(b, 16))
+        assert got == float(v) and np.signbit(got) == np.signbit(float(v)), (b, v, got)
+
+
+# ---- hand-worked blocks ----------------------------------------------------
+
+def test_q8_0_ramp_block():
+    kv, _ = _read("q8_0_ramp.txt")
+    blk = np.frombuffer(bytes.fromhex(kv["hex"]), dtype=np.uint8)
+    w = oracle.dequant_row(8, blk, 32)
+    assert w.tolist() == [float(v) for v in _ints(kv["w"])]
+    y, _ = oracle.matvec(8, blk, 1, 32, np.ones(32, np.float32))
+    assert y[0, 0] == int(kv["dot_ones"])
+
+
+def test_q8_0_negative_subnormal_scale():
+    kv, _ = _read("q8_0_neg_subnormal.txt")
+    blk = np.frombuffer(bytes.fromhex(kv["hex"]), dtype=np.uint8)
+    w = oracle.dequant_row(8, blk, 32)
+    assert (w * 2.0 ** 24).tolist() == [float(v) for v in _ints(kv["w_times_2p24"])]
+    y, _ = oracle.matvec(8, blk, 1, 32, np.ones(32, np.float32))
+    assert y[0, 0] * 2.0 ** 24 == int(kv["dot_ones_times_2p24"])
+
+
+def test_q4_k_ones_twos_block():
+    kv, _ = _read("q4_k_ones_twos.txt")
+    blk = np.frombuffer(bytes.fromhex(kv["hex"]), dtype=np.uint8)
+    expect = []
+    for run in kv["w_runs"].split():
+        v, n = run.split("x")
+        expect += [float(v)] * int(n)
+    assert oracle.dequant_row(12, blk, 256).tolist() == expect
+    y, _ = oracle.matvec(12, blk, 1, 256, np.ones(256, np.float32))
+    assert y[0, 0] == int(kv["dot_ones"])
+
+
+def test_q4_k_scale_packing_all_fields():
+    kv, _ = _read("q4_k_scales_distinct.txt")
+    raw = bytes.fromhex(kv["hex"])
+    sc, mn = _ints(kv["sc"]), _ints(kv["mn"])
+    for j in range(8):
+        assert oracle.q4_k_scale_min(raw[4:16], j) == (sc[j], mn[j])
+    blk = np.frombuffer(raw, dtype=np.uint8)
+    w = oracle.dequant_row(12, blk, 256)
+    per = [float(v) for v in kv["w_per_subblock"].split()]
+    for j in range(8):
+        assert w[32 * j:32 * j + 32].tolist() == [per[j]] * 32
+    y, _ = oracle.matvec(12, blk, 1, 256, np.ones(256, np.float32))
+    assert y[0, 0] == int(kv["dot_ones"])
+
+
+def test_q4_k_nibble_order():
+    kv, _ = _read("q4_k_nibble_order.txt")
+    raw = (bytes([0x00, 0x3C, 0x00, 0x00]) + bytes.fromhex(kv["scale_bytes"]) +
+           bytes(range(128)))
+    w = oracle.dequant_row(12, np.frombuffer(raw, dtype=np.uint8), 256)
+    for c in range(4):
+        for l in range(32):
+            assert w[64 * c + l] == (l & 15)
+            assert w[64 * c + 32 + l] == 2 * c + (l >> 4)
+    assert w.sum() == int(kv["dot_ones"])
+
+
+def test_q6_k_constant_blocks():
+    kv, _ = _read("q6_k_constant.txt")
+    d = bytes([0x00, 0x3C])
+    ones = bytes([1] * 16)
+    a = bytes(128) + bytes(64) + ones + d
+    b = bytes(128) + bytes([0xAA] * 64) + ones + d
+    c = bytes([0x11] * 128) + bytes([0xAA] * 64) + bytes(range(1, 17)) + d
+    x1 = np.ones(256, np.float32)
+    for raw, key in ((a, "caseA_dot_ones"), (b, "caseB_dot_ones"), (c, "caseC_dot_ones")):
+        y, _ = oracle.matvec(14, np.frombuffer(raw, dtype=np.uint8), 1, 256, x1)
+        assert y[0, 0] == int(kv[key])
+    wc = oracle.dequant_row(14, np.frombuffer(c, dtype=np.uint8), 256)
+    assert wc.tolist() == [float(e // 16 + 1) for e in range(256)]
+    assert np.all(oracle.dequant_row(14, np.frombuffer(a, dtype=np.uint8), 256) == -32.0)
+
+
+def test_q6_k_single_bit_flips():
+    _, flips = _read("q6_k_bitflips.txt")
+    assert flips
+    base = bytearray(bytes(128) + bytes([0xAA] * 64) + bytes([1] * 16) + bytes([0x00, 0x3C]))
+    for plane, byte, bit, _arrow, elem, delta in flips:
+        raw = bytearray(base)
+        off = (0 if plane == "ql" else 128) + int(byte)
+        raw[off] ^= 1 << int(bit)
+        w = oracle.dequant_row(14, np.frombuffer(bytes(raw), dtype=np.uint8), 256)
+        expect = np.zeros(256)
+        expect[int(elem)] = float(delta)
+        assert np.array_equal(w, expect), (plane, byte, bit)
+
+
+# ---- format invariants -----------------------------------------------------
+
+def test_q4_k_scale_pack_unpack_roundtrip():
+    rng = np.random.default_rng(7)
+    cases = [([0] * 8, [0] * 8), ([63] * 8, [63] * 8), (list(range(8)), list(range(56, 64)))]
+    cases += [(list(rng.integers(0, 64, 8)), list(rng.integers(0, 64, 8))) for _ in range(200)]
+    for sc, mn in cases:
+        s12 = gp.pack_q4_k_scales(sc, mn)
+        assert [oracle.q4_k_scale_min(s12, j) for j in range(8)] == list(zip(sc, mn))
+    # every byte with its top bits set decodes to fields in range
+    for j in range(8):
+        s, m = oracle.q4_k_scale_min(bytes([0xFF] * 12), j)
+        assert s == 63 and m == 63
+
+
+def test_q4_k_zero_quants_give_minus_min():
+    rng = np.random.default_rng(1)
+    sc = rng.integers(0, 64, 8)
+    mn = rng.integers(0, 64, 8)
+    raw = gp.pack_q4_k(gp.f16_bits(0.75), gp.f16_bits(0.125), sc, mn, np.zeros(256, int))
+    w = oracle.dequant_row(12, np.frombuffer(raw, dtype=np.uint8), 256)
+    for j in range(8):
+        assert np.all(w[32 * j:32 * j + 32] == -0.125 * mn[j])
+
+
+def test_zero_scales_give_zero_weights():
+    rng = np.random.default_rng(2)
+    r4 = gp.pack_q4_k(gp.f16_bits(1.0), gp.f16_bits(1.0), [0] * 8, [0] * 8,
+                      rng.integers(0, 16, 256))
+    r6 = gp.pack_q6_k(gp.f16_bits(1.0), [0] * 16, rng.integers(0, 64, 256))
+    r8 = gp.pack_q8_0(0, rng.integers(-128, 128, 32))
+    for t, raw, K in ((12, r4, 256), (14, r6, 256), (8, r8, 32)):
+        assert np.all(oracle.dequant_row(t, np.frombuffer(raw, dtype=np.uint8), K) == 0.0)
+
+
+def test_linearity_in_d_and_dmin():
+    rng = np.random.default_rng(3)
+    nib, sc, mn = rng.integers(0, 16, 256), rng.integers(0, 64, 8), rng.integers(0, 64, 8)
+    w1 = oracle.dequant_row(12, np.frombuffer(
+        gp.pack_q4_k(gp.f16_bits(0.5), gp.f16_bits(0.25), sc, mn, nib), np.uint8), 256)
+    w2 = oracle.dequant_row(12, np.frombuffer(
+        gp.pack_q4_k(gp.f16_bits(1.0), gp.f16_bits(0.5), sc, mn, nib), np.uint8), 256)
+    assert np.array_equal(2 * w1, w2)
+    q6, s6 = rng.integers(0, 64, 256), rng.integers(-128, 128, 16)
+    a = oracle.dequant_row(14, np.frombuffer(gp.pack_q6_k(gp.f16_bits(0.25), s6, q6), np.uint8),
+                           256)
+    b = oracle.dequant_row(14, np.frombuffer(gp.pack_q6_k(gp.f16_bits(-1.0), s6, q6), np.uint8),
+                           256)
+    assert np.array_equal(-4 * a, b)
+
+
+# ---- special cases that reduce to a plain float64 product --------------------
+
+@pytest.mark.parametrize("qtype", [8, 12, 14])
+def test_unit_scales_reduce_to_integer_matrix_product(qtype):
+    rng = np.random.default_rng(4 + qtype)
+    N, K, B = 5, 512, 3
+    rows, ints = [], np.zeros((N, K), dtype=np.int64)
+    one = gp.f16_bits(1.0)
+    for n in range(N):
+        row = b""
+        for blk in range(K // (32 if qtype == 8 else 256)):
+            if qtype == 8:
+                q = rng.integers(-128, 128, 32)
+                row += gp.pack_q8_0(one, q)
+                ints[n, 32 * blk:32 * blk + 32] = q
+            elif qtype == 12:
+                q = rng.integers(0, 16, 256)
+                row += gp.pack_q4_k(one, 0, [1] * 8, [0] * 8, q)
+                ints[n, 256 * blk:256 * blk + 256] = q
+            else:
+                q = rng.integers(0, 64, 256)
+                row += gp.pack_q6_k(one, [1] * 16, q)
+                ints[n, 256 * blk:256 * blk + 256] = q - 32
+        rows.append(row)
+    W = np.frombuffer(b"".join(rows), dtype=np.uint8)
+    x = rng.standard_normal((B, K)).astype(np.float32)
+    y, bnd = oracle.matvec(qtype, W, N, K, x)
+    ref = x.astype(np.float64) @ ints.T.astype(np.float64)
+    assert np.allclose(y, ref.reshape(B, N), rtol=1e-13, atol=1e-12)
+    assert np.allclose(bnd, np.abs(x.astype(np.float64)) @ np.abs(ints.T), rtol=1e-13)
+
+
+# ---- second formulation (vectorised numpy) and brute force ----------------
+
+@pytest.mark.parametrize("qtype", [8, 12, 14])
+def test_dequant_matches_vectorised_numpy_decoder(qtype):
+    N, K = 7, 512
+    W = synth.weights(qtype, N, K, seed=11)
+    assert np.array_equal(oracle.dequant(qtype, W, N, K), gp.np_dequant(qtype, W, N, K))
+
+
+@pytest.mark.parametrize("qtype", [8, 12, 14])
+@pytest.mark.parametrize("N,K,B", [(1, 256, 1), (2, 256, 8), (3, 512, 4), (3, 512, 2)])
+def test_brute_force_tiny_matvec(qtype, N, K, B):
+    W = synth.weights(qtype, N, K, seed=N * 100 + K + B)
+    x = synth.activations(B, K, seed=B)
+    y, bnd = oracle.matvec(qtype, W, N, K, x)
+    w = gp.np_dequant(qtype, W, N, K)
+    for b in range(B):
+        for n in range(N):
+            exact = sum(float(w[n, k]) * float(x[b, k]) for k in range(K))
+            assert abs(y[b, n] - exact) <= 1e-12 * bnd[b, n] + 1e-300
+
+
+@pytest.mark.parametrize("qtype", [8, 12, 14])
+def test_blockdots_python_big_integers(qtype):
+    N, K, M = 3, 512, 4
+    W = synth.weights(qtype, N, K, seed=21)
+    x = synth.activations(M, K, seed=22)
+    qs, sc, bs = oracle.quantize_act(x)
+    D = oracle.blockdots(qtype, W, N, K, qs)
+    wf = gp.np_dequant(qtype, W, N, K)
+    rowbytes = len(W) // N
+    for n in range(N):
+        wi = oracle.int_weights_row(qtype, W[n * rowbytes:(n + 1) * rowbytes], K)
+        # the integer weight times the block scale (minus the q4_K min term) is the weight
+        blk = W[n * rowbytes:(n + 1) * rowbytes].reshape(-1, rowbytes // (K // (
+            32 if qtype == 8 else 256)))
+        for k in range(K):
+            b = blk[k // (32 if qtype == 8 else 256)]
+            if qtype == 14:
+                d = np.frombuffer(bytes(b[208:210]), np.float16)[0].astype(np.float64)
+                assert wf[n, k] == d * wi[k]
+            elif qtype == 8:
+                d = np.frombuffer(bytes(b[0:2]), np.float16)[0].astype(np.float64)
+                assert wf[n, k] == d * wi[k]
+        for m in range(M):
+            for blk_i in range(K // 32):
+                ref = sum(int(wi[k]) * int(qs[m, k]) for k in range(32 * blk_i, 32 * blk_i + 32))
+                assert D[m, n, blk_i] == ref
+    assert np.abs(D).max() < 2 ** 24  # exact in f32 partial sums
+
+
+@pytest.mark.parametrize("qtype", [8, 12, 14])
+def test_mmq_reference_equals_block_structured_sum(qtype):
+    """The plain definition sum_k w * (s q) equals the block-structured form
+    sum_b s_b * (d * D_b - dmin * m_j * S_b) built from the block dots."""
+    N, K, M = 3, 512, 3
+    W = synth.weights(qtype, N, K, seed=31)
+    x = synth.activations(M, K, seed=32)
+    qs, sc, bs = oracle.quantize_act(x)
+    y, bnd = oracle.mmq(qtype, W, N, K, qs, sc)
+    D = oracle.blockdots(qtype, W, N, K, qs)
+    be = 32 if qtype == 8 else 256
+    rowbytes = len(W) // N
+    for n in range(N):
+        blocks = W[n * rowbytes:(n + 1) * rowbytes].reshape(K // be, -1)
+        for m in range(M):
+            acc = 0.0
+            for b in range(K // 32):
+                blk = blocks[b * 32 // be]
+                if qtype == 8:
+                    d = float(np.frombuffer(bytes(blk[0:2]), np.float16)[0])
+                    acc += float(sc[m, b]) * d * float(D[m, n, b])
+                elif qtype == 12:
+                    d = float(np.frombuffer(bytes(blk[0:2]), np.float16)[0])
+                    dmin = float(np.frombuffer(bytes(blk[2:4]), np.float16)[0])
+                    _, mj = oracle.q4_k_scale_min(bytes(blk[4:16]), b % 8)
+                    acc += float(sc[m, b]) * (d * float(D[m, n, b]) - dmin * mj * float(bs[m, b]))
+                else:
+                    d = float(np.frombuffer(bytes(blk[208:210]), np.float16)[0])
+                    acc += float(sc[m, b]) * d * float(D[m, n, b])
+            assert abs(acc - y[m, n]) <= 1e-12 * bnd[m, n]
+
+
+# ---- activation quantiser --------------------------------------------------
+
+def test_activation_quantiser_ties_golden():
+    kv, _ = _read("act_quant_ties.txt")
+    s = float(kv["scale"])
+    x = (np.array([float(v) for v in kv["x_over_scale"].split()]) * s).astype(np.float32)
+    qs, sc, bs = oracle.quantize_act(x.reshape(1, 32))
+    assert sc[0, 0] == np.float32(s)
+    assert qs[0].tolist() == _ints(kv["q"])
+    assert bs[0, 0] == int(kv["bsum"])
+
+
+def test_activation_quantiser_zero_block_and_invariants():
+    x = synth.activations(6, 256, seed=5) * np.float32(3.0)
+    x[2, 32:64] = 0.0
+    x[3, :32] = np.float32(1e-30)
+    qs, sc, bs = oracle.quantize_act(x)
+    assert sc[2, 1] == 0 and np.all(qs[2, 32:64] == 0) and bs[2, 1] == 0
+    assert np.array_equal(bs, qs.reshape(6, 8, 32).astype(np.int64).sum(-1))
+    nz = sc > 0
+    assert np.all(np.abs(qs.reshape(6, 8, 32)).max(-1)[nz] == 127)
+    assert np.abs(qs).max() <= 127
+    # |x - s q| <= s/2 (plus f32 rounding of s)
+    err = np.abs(x.reshape(6, 8, 32) - sc[..., None].astype(np.float64) * qs.reshape(6, 8, 32))
+    assert np.all(err <= sc[..., None] * (0.5 + 1e-6))
+
+
+def test_requantising_a_dequantised_q8_0_block_is_the_identity():
+    """A q8_0 block with max |q| = 127 dequantises to x = d*q exactly in f32, and the
+    activation quantiser maps it back to scale d and the same q."""
+    rng = np.random.default_rng(9)
+    for trial in range(200):
+        q = rng.integers(-127, 128, 32)
+        q[rng.integers(0, 32)] = 127 if trial % 2 else -127
+        d = np.float16(abs(rng.standard_normal()) * 0.05 + 1e-3)
+        raw = gp.pack_q8_0(int(np.array([d]).view(np.uint16)[0]), q)
+        x = oracle.dequant_row(8, np.frombuffer(raw, np.uint8), 32).astype(np.float32)
+        qs, sc, bs = oracle.quantize_act(x.reshape(1, 32))
+        assert sc[0, 0] == np.float32(d)
+        assert qs[0].tolist() == q.tolist()
+        assert bs[0, 0] == q.sum()
+
+
+def test_power_of_two_scaled_blocks_roundtrip():
+    rng = np.random.default_rng(10)
+    for e in range(-20, 21, 5):
+        q = rng.integers(-127, 128, (4, 32))
+        q[:, 0] = 127
+        x = (q * 2.0 ** e).astype(np.float32)
+        qs, sc, bs = oracle.quantize_act(x.reshape(1, 128))
+        assert np.all(sc == np.float32(2.0 ** e))
+        assert np.array_equal(qs.reshape(4, 32), q)
