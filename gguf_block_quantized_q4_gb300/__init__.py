@@ -1,0 +1,204 @@
+"""Python binding of libmq, the GB300 GGUF block-quantised matmul library.
+
+Argument marshalling only: every step of the computation runs in libmq's CUDA
+kernels.  PyTorch provides device memory and streams.  The C ABI
+(include/mq.h) is exposed twice:
+
+* ``lib()``: the raw ctypes library with the exact C names and signatures
+  (``mq_matvec`` etc.), taking plain pointers and sizes;
+* thin wrappers with the same names minus the ``mq_`` prefix that take torch
+  tensors, read their data pointers and the current CUDA stream, and raise
+  :class:`MQError` on a non-OK status.
+
+There is no fallback: if libmq.so is missing or fails to load, importing the
+wrappers raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmq.so")
+
+Q8_0, Q4_K, Q6_K = 8, 12, 14
+REG_DEFAULT, REG_NO_MMQ_PLANE = 0, 1
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+
+STATUS = ["MQ_OK", "MQ_ERR_ARG", "MQ_ERR_TYPE", "MQ_ERR_SHAPE", "MQ_ERR_PAYLOAD",
+          "MQ_ERR_ALIGN", "MQ_ERR_CUDA", "MQ_ERR_OOM", "MQ_ERR_LAUNCH", "MQ_ERR_TIMEOUT",
+          "MQ_ERR_STATE"]
+
+# The C ABI: name -> (restype, argtypes)
+_P, _I64, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+_ST = ctypes.c_int
+ABI = {
+    "mq_init": (_ST, [ctypes.c_int]),
+    "mq_register_weight": (_ST, [ctypes.c_int, _P, _SZ, _I64, _I64, ctypes.c_uint32,
+                                 ctypes.POINTER(_P)]),
+    "mq_weight_free": (_ST, [_P]),
+    "mq_weight_info": (_ST, [_P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_I64),
+                             ctypes.POINTER(_I64), ctypes.POINTER(_SZ)]),
+    "mq_weight_unpack": (_ST, [_P, _P, _SZ]),
+    "mq_matvec": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "mq_act_bytes": (_SZ, [_I64, _I64]),
+    "mq_quantize_act": (_ST, [_P, _P, _I64, _I64, _P]),
+    "mq_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_mmq_blockdots": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_stream_status": (_ST, [_P]),
+    "mq_last_error": (ctypes.c_char_p, []),
+    "mq_status_name": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+class MQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = STATUS[status] if 0 <= status < len(STATUS) else f"status {status}"
+        super().__init__(f"{self.name}: {message}")
+
+
+def lib():
+    """Load libmq.so (built in-tree by build.py) and declare the C ABI."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m gguf_block_quantized_q4_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in ABI.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise MQError(status, lib().mq_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def init(device: int = 0):
+    _check(lib().mq_init(device))
+
+
+class Weight:
+    """A registered weight (library-owned device planes)."""
+
+    def __init__(self, qtype: int, data, N: int, K: int, flags: int = REG_DEFAULT):
+        import numpy as np
+        buf = np.ascontiguousarray(np.frombuffer(memoryview(data), dtype=np.uint8)
+                                   if not isinstance(data, np.ndarray) else data.view(np.uint8))
+        h = ctypes.c_void_p()
+        _check(lib().mq_register_weight(qtype, buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes,
+                                        N, K, flags, ctypes.byref(h)))
+        self.handle = h
+        self.qtype, self.N, self.K = qtype, N, K
+        self.nbytes = buf.nbytes
+
+    def info(self):
+        t, n, k, b = ctypes.c_int(), _I64(), _I64(), _SZ()
+        _check(lib().mq_weight_info(self.handle, ctypes.byref(t), ctypes.byref(n),
+                                    ctypes.byref(k), ctypes.byref(b)))
+        return t.value, n.value, k.value, b.value
+
+    def unpack(self):
+        import numpy as np
+        out = np.empty(self.nbytes, dtype=np.uint8)
+        _check(lib().mq_weight_unpack(self.handle, out.ctypes.data_as(ctypes.c_void_p),
+                                      out.nbytes))
+        return out
+
+    def free(self):
+        if self.handle:
+            _check(lib().mq_weight_free(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None) and _lib is not None:
+                _lib.mq_weight_free(self.handle)
+        except Exception:
+            pass
+
+
+def register_weight(qtype, data, N, K, flags=REG_DEFAULT) -> Weight:
+    return Weight(qtype, data, N, K, flags)
+
+
+def matvec(W: Weight, x, y=None, stream=None):
+    """y[B][N] = dequant(W) @ x[B][K]^T (x: CUDA f32 [B][K] or [K])."""
+    import torch
+    x2 = x.reshape(-1, W.K)
+    B = x2.shape[0]
+    if y is None:
+        y = torch.empty((B, W.N), dtype=torch.float32, device=x.device)
+    _check(lib().mq_matvec(W.qtype, W.handle, _ptr(x2), _ptr(y), W.N, W.K, B, _stream(stream)))
+    return y
+
+
+def act_bytes(M: int, K: int) -> int:
+    return lib().mq_act_bytes(M, K)
+
+
+def act_views(xq, M: int, K: int):
+    """Views (qs int8 [M][K], scale f32 [M][K/32], bsum int32 [M][K/32], op f16 [M][K])
+    of an xq buffer, following the layout documented in mq.h."""
+    import torch
+
+    def al(v):
+        return (v + 255) & ~255
+    o_qs = 0
+    o_sc = al(o_qs + M * K)
+    o_bs = al(o_sc + M * (K // 32) * 4)
+    o_op = al(o_bs + M * (K // 32) * 4)
+    qs = xq[o_qs:o_qs + M * K].view(torch.int8).view(M, K)
+    sc = xq[o_sc:o_sc + M * (K // 32) * 4].view(torch.float32).view(M, K // 32)
+    bs = xq[o_bs:o_bs + M * (K // 32) * 4].view(torch.int32).view(M, K // 32)
+    op = xq[o_op:o_op + M * K * 2].view(torch.float16).view(M, K)
+    return qs, sc, bs, op
+
+
+def quantize_act(x, xq=None, stream=None):
+    """Quantise CUDA f32 x[M][K]; returns the uint8 xq buffer."""
+    import torch
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty(act_bytes(M, K), dtype=torch.uint8, device=x.device)
+    _check(lib().mq_quantize_act(_ptr(x), _ptr(xq), M, K, _stream(stream)))
+    return xq
+
+
+def mmq(W: Weight, xq, M: int, y=None, stream=None):
+    import torch
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.float32, device=xq.device)
+    _check(lib().mq_mmq(W.qtype, W.handle, _ptr(xq), _ptr(y), M, W.N, W.K, _stream(stream)))
+    return y
+
+
+def mmq_blockdots(W: Weight, xq, M: int, D=None, stream=None):
+    import torch
+    if D is None:
+        D = torch.empty((M, W.N, W.K // 32), dtype=torch.int32, device=xq.device)
+    _check(lib().mq_mmq_blockdots(W.qtype, W.handle, _ptr(xq), _ptr(D), M, W.N, W.K,
+                                  _stream(stream)))
+    return D
+
+
+def stream_status(stream=None):
+    _check(lib().mq_stream_status(_stream(stream)))

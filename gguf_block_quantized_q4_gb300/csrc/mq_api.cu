@@ -1,0 +1,409 @@
+// mq_api.cu -- the C ABI entry points of libmq: argument validation, error
+// reporting, per-device state, weight registration.  Compute happens in the
+// kernels of repack.cu, matvec.cu, quantize.cu and mmq.cu.
+//
+// Error model ("minfer CUDA Backend Design" §4.9 rules 1, 4, 5; "GPU Safety"
+// CUDA rules): every invariant violation returns an mq_status and a message
+// naming the call, the invariant and the values; there is no fallback path.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "mq_common.cuh"
+
+namespace mq {
+
+static thread_local char g_msg[1024] = "no error";
+
+mq_status fail(mq_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+mq_status cuda_fail(cudaError_t e, const char *call, const char *site) {
+  return fail(e == cudaErrorMemoryAllocation ? MQ_ERR_OOM : MQ_ERR_CUDA, "%s: %s failed: %s (%s)",
+              site, call, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+static std::mutex g_dev_mu;
+static std::vector<DeviceState *> g_devs;
+
+DeviceState *device_state(int dev) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (dev < 0 || dev >= (int)g_devs.size()) return nullptr;
+  DeviceState *st = g_devs[dev];
+  return (st && st->ready) ? st : nullptr;
+}
+
+mq_status current_state(DeviceState **st, const char *site) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice", site);
+  *st = device_state(dev);
+  if (!*st) return fail(MQ_ERR_STATE, "%s: mq_init(%d) was not called for the current device",
+                        site, dev);
+  return MQ_OK;
+}
+
+}  // namespace mq
+
+using namespace mq;
+
+#define CK(call, site)                                              \
+  do {                                                              \
+    cudaError_t e_ = (call);                                        \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call, site);       \
+  } while (0)
+
+extern "C" const char *mq_last_error(void) { return g_msg; }
+
+extern "C" const char *mq_status_name(mq_status s) {
+  switch (s) {
+    case MQ_OK: return "MQ_OK";
+    case MQ_ERR_ARG: return "MQ_ERR_ARG";
+    case MQ_ERR_TYPE: return "MQ_ERR_TYPE";
+    case MQ_ERR_SHAPE: return "MQ_ERR_SHAPE";
+    case MQ_ERR_PAYLOAD: return "MQ_ERR_PAYLOAD";
+    case MQ_ERR_ALIGN: return "MQ_ERR_ALIGN";
+    case MQ_ERR_CUDA: return "MQ_ERR_CUDA";
+    case MQ_ERR_OOM: return "MQ_ERR_OOM";
+    case MQ_ERR_LAUNCH: return "MQ_ERR_LAUNCH";
+    case MQ_ERR_TIMEOUT: return "MQ_ERR_TIMEOUT";
+    case MQ_ERR_STATE: return "MQ_ERR_STATE";
+  }
+  return "MQ_ERR_UNKNOWN";
+}
+
+extern "C" mq_status mq_init(int device) {
+  const char *site = "mq_init";
+  int ndev = 0;
+  CK(cudaGetDeviceCount(&ndev), site);
+  if (device < 0 || device >= ndev)
+    return fail(MQ_ERR_ARG, "mq_init: device %d out of range [0, %d)", device, ndev);
+  CK(cudaSetDevice(device), site);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if ((int)g_devs.size() < ndev) g_devs.resize(ndev, nullptr);
+    if (g_devs[device] && g_devs[device]->ready) return MQ_OK;
+  }
+  DeviceState *st = new DeviceState();
+  cudaDeviceProp pr;
+  CK(cudaGetDeviceProperties(&pr, device), site);
+  if (pr.major < 10)
+    return fail(MQ_ERR_ARG, "mq_init: device %d is sm_%d%d; libmq is built for sm_103a", device,
+                pr.major, pr.minor);
+  st->sms = pr.multiProcessorCount;
+  CK(cudaDeviceGetAttribute(&st->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device),
+     site);
+  CK(cudaMalloc(&st->status, 64), site);
+  CK(cudaMemset(st->status, 0, 64), site);
+  CK(cudaStreamCreateWithFlags(&st->reg_stream, cudaStreamNonBlocking), site);
+  mq_status s = init_kernels(st);
+  if (s != MQ_OK) return s;
+  CK(cudaDeviceSynchronize(), site);
+  st->ready = true;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_devs[device] && g_devs[device]->ready) {
+    // another thread finished first; keep its state
+    cudaFree(st->status);
+    cudaStreamDestroy(st->reg_stream);
+    delete st;
+  } else {
+    g_devs[device] = st;
+  }
+  return MQ_OK;
+}
+
+static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t K) {
+  if (type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q6_K)
+    return fail(MQ_ERR_TYPE, "%s: unsupported GGUF type %d (supported: 8 Q8_0, 12 Q4_K, 14 Q6_K)",
+                site, type);
+  if (N < 1 || K < 1)
+    return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld must both be >= 1", site, (long long)N,
+                (long long)K);
+  int be = block_elems(type);
+  if (K % be)
+    return fail(MQ_ERR_SHAPE, "%s: K=%lld is not a multiple of the type-%d block size %d", site,
+                (long long)K, type, be);
+  if (N > (int64_t(1) << 31) || K > (int64_t(1) << 24))
+    return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld beyond the supported range (N <= 2^31, K <= 2^24)",
+                site, (long long)N, (long long)K);
+  return MQ_OK;
+}
+
+static mq_status free_planes(mq_weight *w) {
+  void *ps[] = {w->q, w->sc, w->d, w->mw, w->mbd, w->mbm, w->mbs};
+  for (void *p : ps)
+    if (p) cudaFree(p);
+  w->q = nullptr; w->sc = nullptr; w->d = nullptr; w->mw = nullptr;
+  w->mbd = nullptr; w->mbm = nullptr; w->mbs = nullptr;
+  return MQ_OK;
+}
+
+template <class T>
+static mq_status alloc_plane(T **p, size_t bytes, size_t *total, const char *what) {
+  cudaError_t e = cudaMalloc((void **)p, bytes);
+  if (e != cudaSuccess)
+    return fail(e == cudaErrorMemoryAllocation ? MQ_ERR_OOM : MQ_ERR_CUDA,
+                "mq_register_weight: cudaMalloc(%zu) for the %s plane failed: %s", bytes, what,
+                cudaGetErrorName(e));
+  *total += bytes;
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, size_t nbytes,
+                                        int64_t N, int64_t K, uint32_t flags, mq_weight **out) {
+  const char *site = "mq_register_weight";
+  if (!out) return fail(MQ_ERR_ARG, "%s: out is NULL", site);
+  *out = nullptr;
+  mq_status s = check_type_shape(site, type, N, K);
+  if (s != MQ_OK) return s;
+  if (flags & ~MQ_REG_NO_MMQ_PLANE)
+    return fail(MQ_ERR_ARG, "%s: unknown flag bits 0x%x", site, flags & ~MQ_REG_NO_MMQ_PLANE);
+  size_t expect = size_t(N) * size_t(K / block_elems(type)) * size_t(block_bytes(type));
+  if (nbytes != expect)
+    return fail(MQ_ERR_PAYLOAD,
+                "%s: payload is %zu bytes but a type-%d %lld x %lld tensor is exactly %zu bytes "
+                "(N * K/%d * %d)",
+                site, nbytes, type, (long long)N, (long long)K, expect, block_elems(type),
+                block_bytes(type));
+  if (!host_bytes) return fail(MQ_ERR_ARG, "%s: host_bytes is NULL", site);
+  DeviceState *st = nullptr;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+
+  mq_weight *w = new mq_weight();
+  w->type = type;
+  w->N = N;
+  w->K = K;
+  CK(cudaGetDevice(&w->device), site);
+  w->payload = nbytes;
+  size_t total = 0;
+  const int64_t nsb = K / 256;
+  auto cleanup = [&](mq_status r) {
+    free_planes(w);
+    delete w;
+    return r;
+  };
+  if (type == MQ_Q8_0) {
+    if ((s = alloc_plane(&w->q, size_t(N) * K, &total, "q8_0 qs")) != MQ_OK) return cleanup(s);
+    if ((s = alloc_plane(&w->d, size_t(N) * (K / 32) * 2, &total, "q8_0 d")) != MQ_OK)
+      return cleanup(s);
+  } else if (type == MQ_Q4_K) {
+    if ((s = alloc_plane(&w->q, size_t(N) * nsb * 144, &total, "q4_K")) != MQ_OK)
+      return cleanup(s);
+  } else {
+    if ((s = alloc_plane(&w->q, size_t(N) * nsb * 192, &total, "q6_K quants")) != MQ_OK)
+      return cleanup(s);
+    if ((s = alloc_plane(&w->sc, size_t(N) * nsb * 16, &total, "q6_K scales")) != MQ_OK)
+      return cleanup(s);
+    if ((s = alloc_plane(&w->d, size_t(N) * nsb * 2, &total, "q6_K d")) != MQ_OK)
+      return cleanup(s);
+  }
+  const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE);
+  if (mmq) {
+    if ((s = alloc_plane(&w->mw, size_t(N) * K * 2, &total, "prefill operand")) != MQ_OK)
+      return cleanup(s);
+    if ((s = alloc_plane(&w->mbd, size_t(N) * (K / 32) * 4, &total, "prefill d")) != MQ_OK)
+      return cleanup(s);
+    if (type == MQ_Q4_K &&
+        (s = alloc_plane(&w->mbm, size_t(N) * (K / 32) * 4, &total, "prefill min")) != MQ_OK)
+      return cleanup(s);
+    if (type == MQ_Q6_K &&
+        (s = alloc_plane(&w->mbs, size_t(N) * (K / 16) * 4, &total, "prefill sub-scale")) != MQ_OK)
+      return cleanup(s);
+  }
+  w->device_bytes = total;
+
+  // Upload the GGUF bytes to a staging buffer, repack on the device.
+  uint8_t *raw = nullptr;
+  cudaError_t e = cudaMalloc(&raw, nbytes);
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(staging)", site));
+  e = cudaMemcpyAsync(raw, host_bytes, nbytes, cudaMemcpyHostToDevice, st->reg_stream);
+  if (e == cudaSuccess) {
+    s = repack_weight(w, raw, mmq, st->reg_stream);
+    e = cudaStreamSynchronize(st->reg_stream);
+  }
+  cudaFree(raw);
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "upload/repack", site));
+  if (s != MQ_OK) return cleanup(s);
+  *out = w;
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_weight_free(mq_weight *w) {
+  if (!w) return MQ_OK;
+  int cur = 0;
+  const int dev = w->device;
+  cudaGetDevice(&cur);
+  if (cur != dev) cudaSetDevice(dev);
+  cudaError_t e = cudaDeviceSynchronize();
+  free_planes(w);
+  delete w;
+  if (cur != dev) cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize", "mq_weight_free");
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_weight_info(const mq_weight *w, int *type, int64_t *N, int64_t *K,
+                                    size_t *device_bytes) {
+  if (!w) return fail(MQ_ERR_ARG, "mq_weight_info: w is NULL");
+  if (type) *type = w->type;
+  if (N) *N = w->N;
+  if (K) *K = w->K;
+  if (device_bytes) *device_bytes = w->device_bytes;
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_weight_unpack(const mq_weight *w, void *host_bytes, size_t nbytes) {
+  const char *site = "mq_weight_unpack";
+  if (!w) return fail(MQ_ERR_ARG, "%s: w is NULL", site);
+  if (!host_bytes) return fail(MQ_ERR_ARG, "%s: host_bytes is NULL", site);
+  if (nbytes != w->payload)
+    return fail(MQ_ERR_PAYLOAD, "%s: nbytes=%zu but the weight's payload is %zu bytes", site,
+                nbytes, w->payload);
+  DeviceState *st = nullptr;
+  mq_status s;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  uint8_t *raw = nullptr;
+  CK(cudaMalloc(&raw, nbytes), site);
+  s = unpack_weight(w, raw, st->reg_stream);
+  cudaError_t e = cudaSuccess;
+  if (s == MQ_OK) e = cudaMemcpyAsync(host_bytes, raw, nbytes, cudaMemcpyDeviceToHost, st->reg_stream);
+  cudaError_t e2 = cudaStreamSynchronize(st->reg_stream);
+  cudaFree(raw);
+  if (s != MQ_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync", site);
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamSynchronize", site);
+  return MQ_OK;
+}
+
+// A pointer the device can read/write as global memory.
+static mq_status check_dev_ptr(const char *site, const char *name, const void *p, int dev,
+                               size_t align) {
+  if (!p) return fail(MQ_ERR_ARG, "%s: %s is NULL", site, name);
+  if (reinterpret_cast<uintptr_t>(p) % align)
+    return fail(MQ_ERR_ALIGN, "%s: %s=%p is not %zu-byte aligned", site, name, p, align);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MQ_ERR_ARG, "%s: %s=%p is not a CUDA pointer (%s)", site, name, p,
+                cudaGetErrorName(e));
+  }
+  if (a.type == cudaMemoryTypeDevice && a.device != dev)
+    return fail(MQ_ERR_ARG, "%s: %s=%p lives on device %d, the weight on device %d", site, name,
+                p, a.device, dev);
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(MQ_ERR_ARG, "%s: %s=%p is host memory (type %d); a device pointer is required",
+                site, name, p, (int)a.type);
+  return MQ_OK;
+}
+
+static mq_status check_weight(const char *site, int type, const mq_weight *W, int64_t N,
+                              int64_t K) {
+  if (!W) return fail(MQ_ERR_ARG, "%s: W is NULL", site);
+  mq_status s = check_type_shape(site, type, N, K);
+  if (s != MQ_OK) return s;
+  if (W->type != type)
+    return fail(MQ_ERR_TYPE, "%s: type %d but the weight was registered as type %d", site, type,
+                W->type);
+  if (W->N != N || W->K != K)
+    return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld but the weight is %lld x %lld", site,
+                (long long)N, (long long)K, (long long)W->N, (long long)W->K);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != W->device)
+    return fail(MQ_ERR_ARG, "%s: current device %d but the weight lives on device %d", site, dev,
+                W->device);
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y,
+                               int64_t N, int64_t K, int B, mq_stream stream) {
+  const char *site = "mq_matvec";
+  mq_status s = check_weight(site, type, W, N, K);
+  if (s != MQ_OK) return s;
+  if (B < 1 || B > kMaxB)
+    return fail(MQ_ERR_ARG, "%s: B=%d outside [1, %d]", site, B, kMaxB);
+  DeviceState *st = nullptr;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "x", x, W->device, 16)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "y", y, W->device, 16)) != MQ_OK) return s;
+  return launch_matvec(W, x, y, B, (cudaStream_t)stream, st);
+}
+
+extern "C" size_t mq_act_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 32 || K % 32) return 0;
+  return act_layout(M, K).total;
+}
+
+extern "C" mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_t K,
+                                     mq_stream stream) {
+  const char *site = "mq_quantize_act";
+  if (M < 1) return fail(MQ_ERR_ARG, "%s: M=%lld must be >= 1", site, (long long)M);
+  if (K < 32 || K % 32)
+    return fail(MQ_ERR_SHAPE, "%s: K=%lld must be a positive multiple of 32", site, (long long)K);
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 24))
+    return fail(MQ_ERR_SHAPE, "%s: M=%lld K=%lld beyond the supported range", site, (long long)M,
+                (long long)K);
+  DeviceState *st = nullptr;
+  mq_status s;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if ((s = check_dev_ptr(site, "x", x, dev, 16)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "xq", xq, dev, 256)) != MQ_OK) return s;
+  return launch_quantize(x, xq, M, K, (cudaStream_t)stream);
+}
+
+static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, const void *xq,
+                            const void *out, int64_t M, int64_t N, int64_t K, DeviceState **st) {
+  mq_status s = check_weight(site, type, W, N, K);
+  if (s != MQ_OK) return s;
+  if (!W->mw)
+    return fail(MQ_ERR_ARG, "%s: the weight was registered with MQ_REG_NO_MMQ_PLANE", site);
+  if (M < 1 || M > (int64_t(1) << 31))
+    return fail(MQ_ERR_ARG, "%s: M=%lld outside [1, 2^31]", site, (long long)M);
+  if ((s = current_state(st, site)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "xq", xq, W->device, 256)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "out", out, W->device, 16)) != MQ_OK) return s;
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int64_t M,
+                            int64_t N, int64_t K, mq_stream stream) {
+  DeviceState *st = nullptr;
+  mq_status s = mmq_common("mq_mmq", type, W, xq, y, M, N, K, &st);
+  if (s != MQ_OK) return s;
+  return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st);
+}
+
+extern "C" mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const void *xq,
+                                      int32_t *D, int64_t M, int64_t N, int64_t K,
+                                      mq_stream stream) {
+  DeviceState *st = nullptr;
+  mq_status s = mmq_common("mq_mmq_blockdots", type, W, xq, D, M, N, K, &st);
+  if (s != MQ_OK) return s;
+  return launch_mmq(W, xq, nullptr, D, M, (cudaStream_t)stream, st);
+}
+
+extern "C" mq_status mq_stream_status(mq_stream stream) {
+  const char *site = "mq_stream_status";
+  DeviceState *st = nullptr;
+  mq_status s;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  CK(cudaStreamSynchronize((cudaStream_t)stream), site);
+  int h[2] = {0, 0};
+  CK(cudaMemcpy(h, st->status, sizeof(h), cudaMemcpyDeviceToHost), site);
+  if (h[0] != 0) {
+    CK(cudaMemset(st->status, 0, 64), site);
+    return fail(MQ_ERR_TIMEOUT, "%s: a bounded device-side wait expired (code %d, kernel id %d)",
+                site, h[0], h[1]);
+  }
+  return MQ_OK;
+}

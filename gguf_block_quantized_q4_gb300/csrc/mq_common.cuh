@@ -1,0 +1,113 @@
+// mq_common.cuh -- internal declarations shared by the libmq translation units.
+//
+// Device planes of a registered weight ("minfer CUDA Backend Design" §2.3:
+// weights are uploaded once and repacked per quant type; §4.7: the planes trade
+// device memory for speed).  All planes are lossless regroupings of the GGUF
+// bytes except the prefill operand planes, which hold exact integer values.
+//
+// Decode planes (read by the matvec; every 16-byte word a fragment thread reads
+// is contiguous and 16-byte aligned):
+//   Q8_0  qs   int8 [N][K]      each 32-element block regrouped: stored byte
+//                                8t + 4u + i  <-  block byte 16u + 4t + i
+//                                (t = fragment thread 0..3, u = 16-element half)
+//         d    u16  [N][K/32]   the f16 block scales
+//   Q4_K  q    [N][K/256][144]  bytes 0..15 the GGUF header (d, dmin, 12 scale
+//                                bytes); byte 16 + 32t + 4(2c+u) + i  <-  qs byte
+//                                32c + 16u + 4t + i
+//   Q6_K  q    [N][K/256][192]  byte 48t + 4(3(2h+v) + w) + i  <-  word w of
+//                                (h, v): w=0 ql[64h + 16v + 4t + i],
+//                                w=1 ql[64h + 32 + 16v + 4t + i], w=2 qh[32h + 16v + 4t + i]
+//         sc   int8 [N][K/256][16] the sub-scales
+//         d    u16  [N][K/256]  the f16 super-block scales
+// Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them):
+//   w      f16  [N][K]   integer weight W_int (Q8_0 q; Q4_K sc_j*nib; Q6_K q-32)
+//   bd     f32  [N][K/32] block scale d of the element's (super-)block
+//   bm     f32  [N][K/32] Q4_K only: dmin*m_j (the min term)
+//   bs     f32  [N][K/16] Q6_K only: the 16-element sub-scale
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mq.h"
+
+struct mq_weight {
+  int type;
+  int64_t N, K;
+  int device;
+  size_t payload;        // GGUF bytes
+  size_t device_bytes;   // all planes
+  // decode planes
+  uint8_t *q = nullptr;  // Q8_0 qs / Q4_K 144-byte blocks / Q6_K 192-byte quant blocks
+  int8_t *sc = nullptr;  // Q6_K sub-scales
+  uint16_t *d = nullptr; // Q8_0 block d / Q6_K super-block d
+  // prefill operand planes
+  __half *mw = nullptr;
+  float *mbd = nullptr;
+  float *mbm = nullptr;
+  float *mbs = nullptr;
+};
+
+namespace mq {
+
+constexpr int kMaxB = 8;
+constexpr int kStatusTimeout = 1;
+
+// ---- per-thread error reporting ------------------------------------------
+mq_status fail(mq_status s, const char *fmt, ...);
+mq_status cuda_fail(cudaError_t e, const char *call, const char *site);
+
+// Per-device state set up by mq_init.
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int *status = nullptr;  // device status word for bounded waits
+  cudaStream_t reg_stream = nullptr;
+};
+DeviceState *device_state(int dev);  // nullptr if mq_init(dev) was not called
+mq_status current_state(DeviceState **st, const char *site);
+
+// ---- kernel launchers (defined per translation unit) ----------------------
+mq_status repack_weight(mq_weight *w, const uint8_t *raw_dev, bool mmq, cudaStream_t s);
+mq_status unpack_weight(const mq_weight *w, uint8_t *raw_dev, cudaStream_t s);
+mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
+                        const DeviceState *st);
+mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
+mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
+                     cudaStream_t s, const DeviceState *st);
+mq_status init_kernels(DeviceState *st);  // smem opt-ins
+
+// xq buffer layout (mq_act_bytes)
+struct ActLayout {
+  size_t qs, scale, bsum, op, total;
+};
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline ActLayout act_layout(int64_t M, int64_t K) {
+  ActLayout L;
+  L.qs = 0;
+  L.scale = align256(L.qs + size_t(M) * K);
+  L.bsum = align256(L.scale + size_t(M) * (K / 32) * 4);
+  L.op = align256(L.bsum + size_t(M) * (K / 32) * 4);
+  L.total = align256(L.op + size_t(M) * K * 2);
+  return L;
+}
+
+inline int block_elems(int type) { return type == MQ_Q8_0 ? 32 : 256; }
+inline int block_bytes(int type) {
+  return type == MQ_Q8_0 ? 34 : (type == MQ_Q4_K ? 144 : 210);
+}
+
+// Checked launch: reads the launch's own error at the site ("CUDA Backend
+// Design" §4.9 rule 5).
+#define MQ_LAUNCH_CHECK(name)                                                      \
+  do {                                                                             \
+    cudaError_t e_ = cudaGetLastError();                                           \
+    if (e_ != cudaSuccess)                                                         \
+      return ::mq::fail(MQ_ERR_LAUNCH, "launch of %s failed: %s (%s)", name,       \
+                        cudaGetErrorName(e_), cudaGetErrorString(e_));             \
+  } while (0)
+
+}  // namespace mq

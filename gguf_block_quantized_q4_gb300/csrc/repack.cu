@@ -1,0 +1,222 @@
+// repack.cu -- registration-time repack of GGUF blocks into the device planes
+// described in mq_common.cuh, and the inverse (unpack) used to verify that the
+// decode planes are a lossless regrouping.
+//
+// Block formats (GGUF; byte ratios per "minfer CUDA Backend Design" §2.3):
+//   Q8_0  34 B / 32 el : f16 d, int8 q[32];                 w = d*q
+//   Q4_K 144 B / 256 el: f16 d, f16 dmin, u8 scales[12], u8 qs[128]
+//         sub-block j (elements 32j..32j+31) has a 6-bit scale sc_j and min m_j:
+//           j<4 : sc = s[j]&63,                    m = s[j+4]&63
+//           j>=4: sc = (s[j+4]&15) | (s[j-4]>>6)<<4, m = (s[j+4]>>4) | (s[j]>>6)<<4
+//         element 64c + 32h + l is nibble h of qs[32c + l];  w = d*sc_j*nib - dmin*m_j
+//   Q6_K 210 B / 256 el: u8 ql[128], u8 qh[64], int8 sc[16], f16 d
+//         element 128h + 32r + l: low 4 bits from ql[64h + 32(r%2) + l] (low nibble
+//         for r<2, high for r>=2), high 2 bits = (qh[32h + l] >> 2r) & 3;
+//         w = d * sc[e/16] * (q - 32)
+// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_K sc_j*nib,
+// at most 945, exact in f16; Q6_K q - 32) and f32 block scales.
+#include "mq_common.cuh"
+
+namespace mq {
+namespace {
+
+__device__ __forceinline__ float f16bits(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t rd16(const uint8_t *p) {
+  return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+__device__ __forceinline__ void q4k_scale_min(const uint8_t *s, int j, int &sc, int &m) {
+  if (j < 4) {
+    sc = s[j] & 63;
+    m = s[j + 4] & 63;
+  } else {
+    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+  }
+}
+
+// One thread per GGUF block.
+__global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+                            uint8_t *__restrict__ q, uint16_t *__restrict__ d,
+                            __half *__restrict__ mw, float *__restrict__ mbd) {
+  const int64_t nb = K / 32;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nb) return;
+  const int64_t n = i / nb, b = i % nb;
+  const uint8_t *src = raw + i * 34;
+  const uint16_t dbits = rd16(src);
+  d[i] = dbits;
+  uint8_t *dst = q + n * K + b * 32;
+  for (int t = 0; t < 4; ++t)
+    for (int u = 0; u < 2; ++u)
+      for (int e = 0; e < 4; ++e) dst[8 * t + 4 * u + e] = src[2 + 16 * u + 4 * t + e];
+  if (mw) {
+    for (int e = 0; e < 32; ++e) mw[n * K + b * 32 + e] = __int2half_rn((int8_t)src[2 + e]);
+    mbd[i] = f16bits(dbits);
+  }
+}
+
+__global__ void unpack_q8_0(const uint8_t *__restrict__ q, const uint16_t *__restrict__ d,
+                            int64_t N, int64_t K, uint8_t *__restrict__ raw) {
+  const int64_t nb = K / 32;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nb) return;
+  const int64_t n = i / nb, b = i % nb;
+  uint8_t *dst = raw + i * 34;
+  dst[0] = d[i] & 255;
+  dst[1] = d[i] >> 8;
+  const uint8_t *src = q + n * K + b * 32;
+  for (int t = 0; t < 4; ++t)
+    for (int u = 0; u < 2; ++u)
+      for (int e = 0; e < 4; ++e) dst[2 + 16 * u + 4 * t + e] = src[8 * t + 4 * u + e];
+}
+
+// One thread per super-block.
+__global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+                            uint8_t *__restrict__ q, __half *__restrict__ mw,
+                            float *__restrict__ mbd, float *__restrict__ mbm) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = raw + i * 144;
+  uint8_t *dst = q + i * 144;
+  for (int e = 0; e < 16; ++e) dst[e] = src[e];
+  for (int t = 0; t < 4; ++t)
+    for (int c = 0; c < 4; ++c)
+      for (int u = 0; u < 2; ++u)
+        for (int e = 0; e < 4; ++e)
+          dst[16 + 32 * t + 4 * (2 * c + u) + e] = src[16 + 32 * c + 16 * u + 4 * t + e];
+  if (mw) {
+    const int64_t n = i / nsb, s = i % nsb;
+    const float dd = f16bits(rd16(src)), dmin = f16bits(rd16(src + 2));
+    for (int j = 0; j < 8; ++j) {
+      int sc, m;
+      q4k_scale_min(src + 4, j, sc, m);
+      const int c = j / 2, h = j % 2;
+      for (int l = 0; l < 32; ++l) {
+        const int nib = (src[16 + 32 * c + l] >> (4 * h)) & 15;
+        mw[n * K + s * 256 + 32 * j + l] = __int2half_rn(sc * nib);
+      }
+      mbd[n * (K / 32) + s * 8 + j] = dd;
+      mbm[n * (K / 32) + s * 8 + j] = dmin * (float)m;
+    }
+  }
+}
+
+__global__ void unpack_q4_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
+                            uint8_t *__restrict__ raw) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = q + i * 144;
+  uint8_t *dst = raw + i * 144;
+  for (int e = 0; e < 16; ++e) dst[e] = src[e];
+  for (int t = 0; t < 4; ++t)
+    for (int c = 0; c < 4; ++c)
+      for (int u = 0; u < 2; ++u)
+        for (int e = 0; e < 4; ++e)
+          dst[16 + 32 * c + 16 * u + 4 * t + e] = src[16 + 32 * t + 4 * (2 * c + u) + e];
+}
+
+// Byte offset in the raw Q6_K block of word w (0: ql low pair, 1: ql high pair,
+// 2: qh) of fragment thread t for half h and 16-element half v.
+__device__ __forceinline__ int q6k_src(int t, int h, int v, int w) {
+  return w == 0 ? 64 * h + 16 * v + 4 * t
+                : (w == 1 ? 64 * h + 32 + 16 * v + 4 * t : 128 + 32 * h + 16 * v + 4 * t);
+}
+
+__global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+                            uint8_t *__restrict__ q, int8_t *__restrict__ sc,
+                            uint16_t *__restrict__ d, __half *__restrict__ mw,
+                            float *__restrict__ mbd, float *__restrict__ mbs) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = raw + i * 210;
+  uint8_t *dst = q + i * 192;
+  for (int t = 0; t < 4; ++t)
+    for (int h = 0; h < 2; ++h)
+      for (int v = 0; v < 2; ++v)
+        for (int w = 0; w < 3; ++w)
+          for (int e = 0; e < 4; ++e)
+            dst[48 * t + 4 * (3 * (2 * h + v) + w) + e] = src[q6k_src(t, h, v, w) + e];
+  for (int e = 0; e < 16; ++e) sc[i * 16 + e] = (int8_t)src[192 + e];
+  const uint16_t dbits = rd16(src + 208);
+  d[i] = dbits;
+  if (mw) {
+    const int64_t n = i / nsb, s = i % nsb;
+    const float dd = f16bits(dbits);
+    for (int e = 0; e < 256; ++e) {
+      const int h = e / 128, r = (e / 32) % 4, l = e % 32;
+      const int qlb = src[64 * h + 32 * (r % 2) + l];
+      const int lo4 = r < 2 ? (qlb & 15) : (qlb >> 4);
+      const int hi2 = (src[128 + 32 * h + l] >> (2 * r)) & 3;
+      mw[n * K + s * 256 + e] = __int2half_rn((lo4 | (hi2 << 4)) - 32);
+    }
+    for (int b = 0; b < 8; ++b) mbd[n * (K / 32) + s * 8 + b] = dd;
+    for (int g = 0; g < 16; ++g) mbs[n * (K / 16) + s * 16 + g] = (float)(int8_t)src[192 + g];
+  }
+}
+
+__global__ void unpack_q6_k(const uint8_t *__restrict__ q, const int8_t *__restrict__ sc,
+                            const uint16_t *__restrict__ d, int64_t N, int64_t K,
+                            uint8_t *__restrict__ raw) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = q + i * 192;
+  uint8_t *dst = raw + i * 210;
+  for (int t = 0; t < 4; ++t)
+    for (int h = 0; h < 2; ++h)
+      for (int v = 0; v < 2; ++v)
+        for (int w = 0; w < 3; ++w)
+          for (int e = 0; e < 4; ++e)
+            dst[q6k_src(t, h, v, w) + e] = src[48 * t + 4 * (3 * (2 * h + v) + w) + e];
+  for (int e = 0; e < 16; ++e) dst[192 + e] = (uint8_t)sc[i * 16 + e];
+  dst[208] = d[i] & 255;
+  dst[209] = d[i] >> 8;
+}
+
+inline unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t s) {
+  const int T = 128;
+  const int64_t N = w->N, K = w->K;
+  if (w->type == MQ_Q8_0) {
+    const int64_t n = N * (K / 32);
+    repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, w->d, mmq ? w->mw : nullptr,
+                                              w->mbd);
+    MQ_LAUNCH_CHECK("repack_q8_0");
+  } else if (w->type == MQ_Q4_K) {
+    const int64_t n = N * (K / 256);
+    repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, mmq ? w->mw : nullptr, w->mbd,
+                                              w->mbm);
+    MQ_LAUNCH_CHECK("repack_q4_k");
+  } else {
+    const int64_t n = N * (K / 256);
+    repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, w->sc, w->d,
+                                              mmq ? w->mw : nullptr, w->mbd, w->mbs);
+    MQ_LAUNCH_CHECK("repack_q6_k");
+  }
+  return MQ_OK;
+}
+
+mq_status unpack_weight(const mq_weight *w, uint8_t *raw, cudaStream_t s) {
+  const int T = 128;
+  const int64_t N = w->N, K = w->K;
+  if (w->type == MQ_Q8_0) {
+    unpack_q8_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_q8_0");
+  } else if (w->type == MQ_Q4_K) {
+    unpack_q4_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_q4_k");
+  } else {
+    unpack_q6_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, w->sc, w->d, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_q6_k");
+  }
+  return MQ_OK;
+}
+
+}  // namespace mq

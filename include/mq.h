@@ -1,0 +1,185 @@
+/*
+ * mq.h -- C ABI of libmq: GGUF block-quantised weight x f32 activation matmul
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the quantised MatMul of the minfer engine ("minfer CUDA
+ * Backend Design", §4.4 Execution dispatch): weights stay in their GGUF block
+ * encoding (Q8_0 / Q4_K / Q6_K), activations and outputs are f32 ("CUDA
+ * Backend Design" §1.3: activations stay f32).  Two forms:
+ *
+ *   decode matvec   y[b][n] = sum_k w[n][k] * x[b][k],  b < B <= 8
+ *                   ("CUDA Backend Design" §4.4: nt == 1 and the _multi
+ *                   variants for nt 2..8), weights dequantised in registers.
+ *   prefill MMQ     activations quantised per 32-element block to int8 with an
+ *                   f32 scale (mq_quantize_act), then an exact integer
+ *                   contraction per block and a per-block scale epilogue
+ *                   (mq_mmq) ("CUDA Backend Design" §4.4: the int8 MMQ path).
+ *
+ * Conventions ("CUDA Backend Design" §4.9 GPU safety; "GPU Safety" CUDA
+ * rules): every invariant violation returns an error status and never falls
+ * back to another kernel or to the CPU; every launch is checked at its site;
+ * device limits are queried at run time; waits inside kernels are bounded.
+ *
+ * Threading: calls may come from several host threads.  mq_last_error() is
+ * per thread.  A weight handle may be used concurrently from several streams
+ * (kernels only read it).  mq_weight_free must not race with calls using the
+ * handle.
+ *
+ * Pointers: "device pointer" means memory the current CUDA device can access
+ * as global memory (cudaMalloc, torch CUDA tensors, managed memory).  Host
+ * pointers passed where a device pointer is required are rejected with
+ * MQ_ERR_ARG (checked with cudaPointerGetAttributes).  All hot-path calls are
+ * asynchronous on the given stream and allocate nothing.
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GGUF tensor type ids of the supported block formats.
+ *   MQ_Q8_0: 32-element blocks of 34 bytes: f16 d, 32 x int8 q;  w = d*q.
+ *   MQ_Q4_K: 256-element super-blocks of 144 bytes: f16 d, f16 dmin, 12 bytes
+ *            of packed 6-bit sub-block scales/mins, 128 bytes of 4-bit quants;
+ *            w = d*sc_j*q - dmin*m_j.
+ *   MQ_Q6_K: 256-element super-blocks of 210 bytes: 128 bytes low 4 bits,
+ *            64 bytes high 2 bits, 16 int8 sub-scales, f16 d;
+ *            w = d*sc*(q - 32).
+ * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256). */
+typedef enum { MQ_Q8_0 = 8, MQ_Q4_K = 12, MQ_Q6_K = 14 } mq_type;
+
+typedef enum {
+    MQ_OK = 0,
+    MQ_ERR_ARG = 1,      /* null / host / misaligned pointer, bad flag, B or M out of range */
+    MQ_ERR_TYPE = 2,     /* unsupported type, or type differs from the weight's */
+    MQ_ERR_SHAPE = 3,    /* N, K invalid, K not a multiple of the block, or N/K differ from W */
+    MQ_ERR_PAYLOAD = 4,  /* nbytes != N*(K/blk)*blkbytes (equality, "CUDA Backend Design" §2.3) */
+    MQ_ERR_ALIGN = 5,    /* a buffer is not 16-byte aligned */
+    MQ_ERR_CUDA = 6,     /* a CUDA runtime call failed (message names it) */
+    MQ_ERR_OOM = 7,      /* device allocation failed at registration */
+    MQ_ERR_LAUNCH = 8,   /* a kernel launch or smem opt-in was refused (message names the kernel) */
+    MQ_ERR_TIMEOUT = 9,  /* a bounded device-side wait expired (reported by mq_stream_status) */
+    MQ_ERR_STATE = 10    /* mq_init was not called for the current device */
+} mq_status;
+
+/* Opaque weight handle: library-owned device planes built at registration. */
+typedef struct mq_weight mq_weight;
+
+/* Stream handle: a cudaStream_t (NULL = the legacy default stream). */
+typedef void *mq_stream;
+
+/* Registration flags. */
+#define MQ_REG_DEFAULT 0u
+/* Skip the prefill operand planes; mq_mmq then returns MQ_ERR_ARG for this weight. */
+#define MQ_REG_NO_MMQ_PLANE 1u
+
+/* mq_init -- prepare the library for CUDA device `device` (makes it current on
+ * the calling thread).  Queries the SM count and the shared-memory opt-in
+ * limit, opts every kernel that needs more than 48 KiB of dynamic shared
+ * memory in (once per device, outside any stream capture: "CUDA Backend
+ * Design" §2.4, the eager pre-warm), and allocates the per-device status word
+ * used by bounded waits.  Idempotent.  Must precede every other call for that
+ * device.  Errors: MQ_ERR_CUDA, MQ_ERR_LAUNCH (an opt-in refused). */
+mq_status mq_init(int device);
+
+/* mq_register_weight -- copy an N x K GGUF tensor (rows contiguous, blocks
+ * along K, exactly as stored in a GGUF file) to the current device and build
+ * the device planes ("CUDA Backend Design" §2.3 weight residency and
+ * registry: uploaded once at load, quant-specific repacks):
+ *   - the decode plane: the same bytes, regrouped so that each thread of a
+ *     tensor-core fragment reads 16-byte words (lossless: mq_weight_unpack
+ *     restores the original bytes);
+ *   - unless MQ_REG_NO_MMQ_PLANE: the prefill operand planes (integer-valued
+ *     f16 weights [N][K] plus f32 block-scale planes).
+ * host_bytes: host pointer to nbytes bytes (read only during the call).
+ * Validation before any device work: type supported (MQ_ERR_TYPE); N >= 1,
+ * K >= 1, K a multiple of the block size (MQ_ERR_SHAPE); nbytes ==
+ * N*(K/blk)*blkbytes (MQ_ERR_PAYLOAD).  Synchronous: uses the library's own
+ * stream and synchronises it before returning, so it never enters a caller's
+ * stream-capture window ("CUDA Backend Design" §2.4).  *out receives the
+ * handle (owned by the caller, released with mq_weight_free).
+ * Errors also: MQ_ERR_OOM, MQ_ERR_CUDA, MQ_ERR_STATE. */
+mq_status mq_register_weight(mq_type type, const void *host_bytes, size_t nbytes, int64_t N,
+                             int64_t K, uint32_t flags, mq_weight **out);
+
+/* mq_weight_free -- release the weight's device planes (synchronises the
+ * device first so no queued kernel still reads them).  NULL is a no-op. */
+mq_status mq_weight_free(mq_weight *w);
+
+/* mq_weight_info -- type, N, K and total device bytes of a weight. */
+mq_status mq_weight_info(const mq_weight *w, int *type, int64_t *N, int64_t *K,
+                         size_t *device_bytes);
+
+/* mq_weight_unpack -- write the original GGUF bytes of W back to host memory
+ * (nbytes must equal the registered payload size).  Test/diagnostic call:
+ * rebuilds the bytes from the decode plane on the device.  Synchronous. */
+mq_status mq_weight_unpack(const mq_weight *w, void *host_bytes, size_t nbytes);
+
+/* mq_matvec -- decode matvec.  x: device f32 [B][K] row-major; y: device f32
+ * [B][N] row-major (written, never read); 1 <= B <= 8.  type, N, K must match
+ * W.  x and y 16-byte aligned.  Every column b of a batched call is computed
+ * exactly as the B = 1 call on x[b] (bitwise; "Architecture Execution Plan"
+ * ADR-0010, the bitwise-by-default identity rule).  Float result within
+ * 1e-4 * sum_k |w[n][k]| |x[b][k]| of the exact product. */
+mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, int64_t N,
+                    int64_t K, int B, mq_stream stream);
+
+/* mq_act_bytes -- size of the quantised-activation buffer xq for M x K.
+ * Layout (each section starts on a 256-byte boundary, in this order):
+ *   qs      int8  [M][K]       the quantised values q
+ *   scale   f32   [M][K/32]    the block scales s = max|x| / 127
+ *   bsum    int32 [M][K/32]    the block sums S = sum q
+ *   operand f16   [M][K]       q as f16 (exact), the tensor-core operand
+ * Returns 0 if K is not a positive multiple of 32 or M < 1. */
+size_t mq_act_bytes(int64_t M, int64_t K);
+
+/* mq_quantize_act -- quantise f32 activations per 32-element block ("CUDA
+ * Backend Design" §4.4: prefill quantises A into per-32 int8 blocks;
+ * "Architecture Execution Plan" C4 S2b design decision 4: amax/127,
+ * round half to even).  In IEEE binary32: amax = max|x|, s = amax/127
+ * (correctly rounded), q = round_half_even(x/s) clamped to [-127, 127],
+ * S = sum q; a block whose s is 0 gets q = 0.  x: device f32 [M][K];
+ * xq: device buffer of mq_act_bytes(M, K) bytes (256-byte aligned).
+ * K % 32 == 0, M >= 1. */
+mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_t K, mq_stream stream);
+
+/* mq_mmq -- prefill matmul y[m][n] = sum_b s[m][b] * (d[n][b]*D[m][n][b] -
+ * dmin_term[n][b]*S[m][b]) where D is the exact integer block dot of the
+ * weight's integer values with q (see mq_mmq_blockdots).  xq from
+ * mq_quantize_act(M, K); y: device f32 [M][N] row-major.  W must have its
+ * MMQ planes.  Float result within 1e-4 * sum_k |w| |s*q| of the exact
+ * product of W with the dequantised activations. */
+mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int64_t M,
+                 int64_t N, int64_t K, mq_stream stream);
+
+/* mq_mmq_blockdots -- test export of the contraction's integer part:
+ * D[(m*N + n)*(K/32) + b] = sum_{k in block b} W_int[n][k] * q[m][k], int32,
+ * where W_int is the weight's integer value: Q8_0 the int8 quant; Q4_K the
+ * 6-bit sub-block scale times the 4-bit quant; Q6_K the int8 16-element
+ * sub-scale times (6-bit quant - 32).  Same tensor-core code path as mq_mmq.
+ * D: device int32 buffer of M*N*(K/32) elements. */
+mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const void *xq, int32_t *D,
+                           int64_t M, int64_t N, int64_t K, mq_stream stream);
+
+/* mq_stream_status -- synchronise `stream`, then read and clear the current
+ * device's status word written by bounded device-side waits.  Returns MQ_OK,
+ * or MQ_ERR_TIMEOUT if a wait expired since the last call (the message names
+ * the kernel), or MQ_ERR_CUDA if the synchronisation failed. */
+mq_status mq_stream_status(mq_stream stream);
+
+/* mq_last_error -- message of the last failing call on this thread: the call,
+ * the violated invariant and the values involved.  Never NULL. */
+const char *mq_last_error(void);
+
+/* mq_status_name -- "MQ_OK", "MQ_ERR_ARG", ... */
+const char *mq_status_name(mq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQ_H */

@@ -1,0 +1,140 @@
+"""CPU-only checks of the C-ABI boundary: libmq.so builds, loads, exports every
+function include/mq.h declares, and rejects invalid arguments on the host before
+any device work.  No compute call runs here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gguf_block_quantized_q4_gb300 as mq
+from gguf_block_quantized_q4_gb300 import build as mqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    mqbuild.build()
+    return mq.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mq_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("mq_init", "mq_register_weight", "mq_matvec", "mq_quantize_act", "mq_mmq",
+                 "mq_mmq_blockdots", "mq_weight_unpack", "mq_stream_status", "mq_last_error"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in mq.ABI, f"binding lacks {name}"
+
+
+def test_exported_symbols_are_unmangled_c(L):
+    out = os.popen(f"nm -D --defined-only {mq.LIB_PATH}").read()
+    exported = set(re.findall(r"\b(mq_[a-z_]+)\b", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_names(L):
+    for i, n in enumerate(mq.STATUS):
+        assert L.mq_status_name(i).decode() == n
+
+
+def test_act_bytes_layout(L):
+    assert L.mq_act_bytes(0, 64) == 0
+    assert L.mq_act_bytes(4, 48) == 0
+    M, K = 3, 96
+    al = lambda v: (v + 255) & ~255
+    expect = al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2)
+    assert L.mq_act_bytes(M, K) == expect
+    assert L.mq_act_bytes(512, 3584) % 256 == 0
+
+
+def _reg(L, qtype, data, N, K, flags=0):
+    h = ctypes.c_void_p()
+    buf = np.ascontiguousarray(data, dtype=np.uint8)
+    st = L.mq_register_weight(qtype, buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes, N, K,
+                              flags, ctypes.byref(h))
+    return st, L.mq_last_error().decode()
+
+
+def test_register_rejects_bad_type(L):
+    st, msg = _reg(L, 2, np.zeros(18 * 8, np.uint8), 1, 256)
+    assert mq.STATUS[st] == "MQ_ERR_TYPE" and "unsupported GGUF type 2" in msg
+
+
+def test_register_rejects_bad_shape(L):
+    st, msg = _reg(L, mq.Q4_K, np.zeros(144, np.uint8), 1, 128)
+    assert mq.STATUS[st] == "MQ_ERR_SHAPE" and "multiple" in msg
+    st, _ = _reg(L, mq.Q8_0, np.zeros(34, np.uint8), 0, 32)
+    assert mq.STATUS[st] == "MQ_ERR_SHAPE"
+
+
+@pytest.mark.parametrize("qtype,K,wrong", [
+    (mq.Q4_K, 512, 18 * 16),      # a q4_0 payload has q4_K's byte ratio 18/32 == 144/256
+    (mq.Q4_K, 512, 34 * 16),      # a q8_0 payload is longer
+    (mq.Q4_K, 512, 84 * 2),       # a 2-bit K-quant payload is shorter
+    (mq.Q6_K, 256, 224),          # the 224-byte padded Q6_K row is not a GGUF payload
+    (mq.Q8_0, 64, 67),
+])
+def test_register_payload_is_an_equality(L, qtype, K, wrong):
+    N = 1 if qtype != mq.Q4_K or wrong != 18 * 16 else 1
+    expect = N * (K // mq.BLOCK[qtype][0]) * mq.BLOCK[qtype][1]
+    if wrong == expect:
+        pytest.skip("same size")
+    st, msg = _reg(L, qtype, np.zeros(wrong, np.uint8), N, K)
+    assert mq.STATUS[st] == "MQ_ERR_PAYLOAD", msg
+    assert str(expect) in msg
+
+
+def test_q4_0_payload_with_q4_k_ratio_is_refused(L):
+    # 2 rows x 512: q4_K expects 2*2*144 = 576 bytes; a q4_0 tensor of 1 row x 1024 has
+    # 32 blocks of 18 = 576 bytes, but N=2, K=512 as q4_K would accept 576 -- so the
+    # type gate, not the size, is what must separate them.  Here the caller claims
+    # q4_K with the wrong N: 1 x 1024 q4_K needs 4*144 = 576 too.  Equal sizes pass
+    # validation; a different N must change the expected size.
+    st, _ = _reg(L, mq.Q4_K, np.zeros(576, np.uint8), 3, 512)
+    assert mq.STATUS[st] == "MQ_ERR_PAYLOAD"
+
+
+def test_register_rejects_unknown_flags_and_null(L):
+    st, msg = _reg(L, mq.Q8_0, np.zeros(34, np.uint8), 1, 32, flags=0x80)
+    assert mq.STATUS[st] == "MQ_ERR_ARG" and "flag" in msg
+    h = ctypes.c_void_p()
+    st = L.mq_register_weight(mq.Q8_0, None, 34, 1, 32, 0, ctypes.byref(h))
+    assert mq.STATUS[st] == "MQ_ERR_ARG"
+
+
+def test_quantize_rejects_bad_shape_before_device_work(L):
+    assert mq.STATUS[L.mq_quantize_act(None, None, 4, 48, None)] == "MQ_ERR_SHAPE"
+    assert mq.STATUS[L.mq_quantize_act(None, None, 0, 64, None)] == "MQ_ERR_ARG"
+
+
+def test_matvec_rejects_null_weight(L):
+    st = L.mq_matvec(mq.Q8_0, None, None, None, 1, 32, 1, None)
+    assert mq.STATUS[st] == "MQ_ERR_ARG"
+    assert "W is NULL" in L.mq_last_error().decode()
+
+
+def test_last_error_is_per_thread(L):
+    import threading
+    L.mq_matvec(mq.Q8_0, None, None, None, 1, 32, 1, None)
+    seen = {}
+
+    def other():
+        seen["msg"] = L.mq_last_error().decode()
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["msg"] == "no error"
+    assert "W is NULL" in L.mq_last_error().decode()

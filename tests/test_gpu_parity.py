@@ -1,0 +1,274 @@
+"""GPU parity of libmq's CUDA path against the CPU oracle, through the C ABI.
+
+Integer work (decode-plane round trip, quantised activations, per-block integer
+dots) must match bit for bit; float outputs must satisfy
+|y - y_ref| <= 1e-4 * sum_k |w||x| per element (the decode matvec and the MMQ,
+the latter against the dequantised activations s*q).  Sizes: small shapes that
+span several tiles with ragged tails, and the five hot-path workloads at full
+size in the launch configuration the bench uses (outputs compared in full where
+the oracle is fast enough, else on sampled rows)."""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import gguf_block_quantized_q4_gb300 as mq  # noqa: E402
+from gguf_block_quantized_q4_gb300 import build as mqbuild  # noqa: E402
+
+REL = 1e-4  # the per-element bound: |y - y_ref| <= REL * sum |w||x|
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mqbuild.build()
+    mq.init(0)
+    yield
+
+
+@functools.lru_cache(maxsize=None)
+def weights(qtype, N, K, seed):
+    return synth.weights(qtype, N, K, seed)
+
+
+@functools.lru_cache(maxsize=8)
+def registered(qtype, N, K, seed, flags=0):
+    return mq.register_weight(qtype, weights(qtype, N, K, seed), N, K, flags)
+
+
+def assert_bound(y, yref, bnd, what):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - yref)
+    lim = REL * bnd
+    bad = err > lim + 1e-37
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside the bound; worst "
+                           f"err/bound {np.max(err / np.maximum(bnd, 1e-300)):.3e}")
+
+
+def gpu_matvec(W, x):
+    xt = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    y = mq.matvec(W, xt)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+# ---- decode planes -----------------------------------------------------------
+
+@pytest.mark.parametrize("qtype,N,K", [(8, 37, 96), (8, 896, 896), (12, 19, 512),
+                                       (12, 18944, 3584), (14, 21, 768), (14, 3584, 18944)])
+def test_decode_plane_roundtrip_is_byte_exact(qtype, N, K):
+    W = registered(qtype, N, K, 7)
+    assert np.array_equal(W.unpack(), weights(qtype, N, K, 7))
+    t, n, k, nbytes = W.info()
+    assert (t, n, k) == (qtype, N, K) and nbytes > 0
+
+
+# ---- decode matvec -----------------------------------------------------------
+
+SMALL = [(8, 1, 32), (8, 37, 96), (8, 130, 288), (8, 64, 896),
+         (12, 1, 256), (12, 19, 512), (12, 100, 768), (12, 257, 2560),
+         (14, 1, 256), (14, 21, 768), (14, 130, 512), (14, 64, 4608)]
+
+
+@pytest.mark.parametrize("qtype,N,K", SMALL)
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_matvec_small_shapes(qtype, N, K, B):
+    W = registered(qtype, N, K, 11)
+    x = synth.activations(B, K, seed=100 + B)
+    y = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 11), N, K, x)
+    assert_bound(y, yref, bnd, f"type {qtype} {N}x{K} B={B}")
+
+
+@pytest.mark.parametrize("name,B", [("q8_0_matvec_896x896", 1), ("q4_k_matvec_18944x3584", 1),
+                                    ("q6_k_matvec_3584x18944", 1), ("q6_k_matvec_3584x18944", 2),
+                                    ("q6_k_matvec_3584x18944", 4), ("q6_k_matvec_3584x18944", 8),
+                                    ("q6_k_lm_head_151936x3584", 1)])
+def test_matvec_workloads_full(name, B):
+    c = synth.WORKLOADS[name]
+    qtype, N, K = c["qtype"], c["N"], c["K"]
+    W = registered(qtype, N, K, c["w_seed"])
+    x = synth.activations(B, K, c["x_seed"], c["x_scale"])
+    y = gpu_matvec(W, x)
+    if N > 20000:  # the LM head: every row would take the oracle ~10 s; check 3 row ranges
+        for n0, n1 in ((0, 4096), (N // 2 - 2048, N // 2 + 2048), (N - 4096, N)):
+            yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, c["w_seed"]), N, K, x, n0, n1)
+            assert_bound(y[:, n0:n1], yref, bnd, f"{name} rows {n0}:{n1}")
+    else:
+        yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, c["w_seed"]), N, K, x)
+        assert_bound(y, yref, bnd, name)
+
+
+def test_matvec_batch_columns_equal_single_calls_bitwise():
+    c = synth.WORKLOADS["q6_k_matvec_3584x18944"]
+    W = registered(c["qtype"], c["N"], c["K"], c["w_seed"])
+    x = synth.activations(8, c["K"], c["x_seed"], 1.0)
+    y8 = gpu_matvec(W, x)
+    for b in range(8):
+        y1 = gpu_matvec(W, x[b:b + 1])
+        assert np.array_equal(y1[0].view(np.uint32), y8[b].view(np.uint32)), b
+    y3 = gpu_matvec(W, x[2:5])
+    assert np.array_equal(y3.view(np.uint32), y8[2:5].view(np.uint32))
+
+
+@pytest.mark.parametrize("qtype,N,K", [(8, 70, 288), (12, 70, 768), (14, 70, 768)])
+def test_matvec_extreme_magnitudes(qtype, N, K):
+    W = registered(qtype, N, K, 13)
+    rng = np.random.default_rng(5)
+    x = synth.activations(4, K, seed=6)
+    x[0] *= np.float32(1e30)       # f16 would overflow without the per-chunk exponent
+    x[1] *= np.float32(1e-30)      # and underflow
+    x[2, : K // 2] *= np.float32(1e20)
+    x[2, K // 2:] *= np.float32(1e-10)  # chunks of very different range
+    x[3] = 0.0
+    x[3, rng.integers(0, K, 5)] = np.float32(3.0)
+    y = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 13), N, K, x)
+    assert_bound(y, yref, bnd, f"extreme type {qtype}")
+    y0 = gpu_matvec(W, np.zeros((2, K), np.float32))
+    assert np.all(y0 == 0.0)
+
+
+# ---- activation quantiser ----------------------------------------------------
+
+def gpu_quantize(x):
+    xt = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    M, K = x.shape
+    xq = mq.quantize_act(xt)
+    torch.cuda.synchronize()
+    qs, sc, bs, op = (v.cpu().numpy() for v in mq.act_views(xq, M, K))
+    return xq, qs, sc, bs, op
+
+
+def assert_quant_exact(x):
+    _, qs, sc, bs, op = gpu_quantize(x)
+    rq, rs, rb = oracle.quantize_act(x)
+    assert np.array_equal(qs, rq)
+    assert np.array_equal(sc.view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(bs, rb)
+    assert np.array_equal(op.astype(np.float32), rq.astype(np.float32))
+
+
+@pytest.mark.parametrize("name,M", [("q4_k_mmq_512x18944x3584", 512),
+                                    ("q6_k_lm_head_151936x3584", 2048)])
+def test_quantize_workloads_bit_exact(name, M):
+    c = synth.WORKLOADS[name]
+    assert_quant_exact(synth.activations(M, c["K"], c["x_seed"], c["x_scale"]))
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (7, 96), (65, 288), (3, 4096)])
+def test_quantize_small_and_edge_blocks(M, K):
+    x = synth.activations(M, K, seed=M * 7 + K)
+    x[0, :32] = 0.0                                   # s = 0 block
+    if K >= 64:
+        x[0, 32:64] = np.float32(1e-41)               # subnormal block
+    if M > 1:
+        s = np.float32(0.125)
+        x[1, :32] = s * np.array([127, 2.5, -2.5, 3.5, 0.5, -0.5, 1.5, -1.5] * 4, np.float32)
+    if M > 2:
+        x[2, :32] = np.float32(3e38) * np.sign(x[2, :32])  # near the f32 maximum
+    assert_quant_exact(x)
+
+
+# ---- MMQ -------------------------------------------------------------------
+
+SMALL_MMQ = [(8, 37, 96, 5), (8, 130, 288, 70), (12, 19, 512, 9), (12, 200, 768, 65),
+             (14, 21, 768, 3), (14, 130, 512, 129)]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
+def test_blockdots_bit_exact_small(qtype, N, K, M):
+    W = registered(qtype, N, K, 17)
+    x = synth.activations(M, K, seed=M + K)
+    xq, qs, _, _, _ = gpu_quantize(x)
+    D = mq.mmq_blockdots(W, xq, M)
+    torch.cuda.synchronize()
+    ref = oracle.blockdots(qtype, weights(qtype, N, K, 17), N, K, qs)
+    assert np.array_equal(D.cpu().numpy(), ref.astype(np.int32))
+
+
+@pytest.mark.parametrize("name", ["q4_k_mmq_512x18944x3584", "q6_k_lm_head_151936x3584"])
+def test_blockdots_bit_exact_workload_tiles(name):
+    """A 128 x 256 x (all blocks) tile of each prefill workload: the first 256 weight rows
+    and 128 activation rows, with the workload's distributions and seeds."""
+    c = synth.WORKLOADS[name]
+    qtype, K = c["qtype"], c["K"]
+    rowbytes = K // 256 * synth.BLOCK[qtype][1]
+    Wfull = weights(qtype, c["N"], K, c["w_seed"])
+    Wt = np.ascontiguousarray(Wfull[:256 * rowbytes])
+    W = mq.register_weight(qtype, Wt, 256, K)
+    x = synth.activations(128, K, c["x_seed"], c["x_scale"])
+    xq, qs, _, _, _ = gpu_quantize(x)
+    D = mq.mmq_blockdots(W, xq, 128)
+    torch.cuda.synchronize()
+    ref = oracle.blockdots(qtype, Wt, 256, K, qs)
+    assert np.array_equal(D.cpu().numpy(), ref.astype(np.int32))
+    W.free()
+
+
+@pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
+def test_mmq_small_shapes(qtype, N, K, M):
+    W = registered(qtype, N, K, 17)
+    x = synth.activations(M, K, seed=M + K)
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    y = mq.mmq(W, xq, M)
+    torch.cuda.synchronize()
+    yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 17), N, K, qs, sc)
+    assert_bound(y.cpu().numpy(), yref, bnd, f"mmq type {qtype} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("name", ["q4_k_mmq_512x18944x3584", "q6_k_lm_head_151936x3584"])
+def test_mmq_workloads_sampled(name):
+    c = synth.WORKLOADS[name]
+    qtype, N, K, M = c["qtype"], c["N"], c["K"], c["M"][0]
+    W = registered(qtype, N, K, c["w_seed"])
+    x = synth.activations(M, K, c["x_seed"], c["x_scale"])
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    y = mq.mmq(W, xq, M)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    rng = np.random.default_rng(1)
+    rows = sorted(set([0, 1, M // 4 - 1, M // 2, M - 1] + list(rng.integers(0, M, 11))))
+    ranges = [(0, N)] if N <= 20000 else [(0, 2048), (N // 2, N // 2 + 2048), (N - 2048, N)]
+    for n0, n1 in ranges:
+        yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, c["w_seed"]), N, K, qs, sc,
+                               mrows=rows, n0=n0, n1=n1)
+        assert_bound(y[rows, n0:n1], yref, bnd, f"{name} cols {n0}:{n1}")
+    assert np.isfinite(y).all()
+
+
+# ---- errors on the device path -----------------------------------------------
+
+def test_errors_are_reported_not_fallen_back():
+    W = registered(12, 19, 512, 17)
+    x = torch.zeros((1, 512), device="cuda")
+    y = torch.zeros((1, 19), device="cuda")
+    L = mq.lib()
+    P = lambda t: t.data_ptr()
+    st = L.mq_matvec(14, W.handle, P(x), P(y), 19, 512, 1, None)
+    assert mq.STATUS[st] == "MQ_ERR_TYPE"
+    st = L.mq_matvec(12, W.handle, P(x), P(y), 20, 512, 1, None)
+    assert mq.STATUS[st] == "MQ_ERR_SHAPE"
+    for B in (0, 9):
+        assert mq.STATUS[L.mq_matvec(12, W.handle, P(x), P(y), 19, 512, B, None)] == "MQ_ERR_ARG"
+    xh = np.zeros(512, np.float32)
+    st = L.mq_matvec(12, W.handle, xh.ctypes.data, P(y), 19, 512, 1, None)
+    assert mq.STATUS[st] == "MQ_ERR_ARG" and "host memory" in L.mq_last_error().decode() or \
+        "not a CUDA pointer" in L.mq_last_error().decode()
+    yb = torch.zeros(64, device="cuda")
+    st = L.mq_matvec(12, W.handle, P(x), P(yb) + 4, 19, 512, 1, None)
+    assert mq.STATUS[st] == "MQ_ERR_ALIGN"
+    Wn = mq.register_weight(12, weights(12, 19, 512, 17), 19, 512, mq.REG_NO_MMQ_PLANE)
+    xq = mq.quantize_act(torch.zeros((4, 512), device="cuda"))
+    with pytest.raises(mq.MQError) as e:
+        mq.mmq(Wn, xq, 4)
+    assert e.value.name == "MQ_ERR_ARG"
+    Wn.free()
+    mq.stream_status()
