@@ -118,15 +118,17 @@ def src_sha(path):
 
 
 def traffic_for(kernel_key, src):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
-    unchanged since it was captured."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.txt: lines of
+    `key dram_bytes_per_launch source_sha`), if the kernel source is unchanged since the
+    counters were taken; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel_key)
-    if not d or d.get("src_sha") != src_sha(src):
-        return None
-    return d.get("dram_bytes_per_launch")
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel_key:
+            return float(f[1]) if f[2] == src_sha(src) else None
+    return None
 
 
 def cpu_baseline(budget_s: float = 12.0):
