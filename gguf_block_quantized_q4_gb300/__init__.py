@@ -155,22 +155,44 @@ def act_bytes(M: int, K: int) -> int:
     return lib().mq_act_bytes(M, K)
 
 
+def act_layout(M: int, K: int):
+    """Byte offsets of the xq sections (see mq_act_bytes in mq.h)."""
+    def al(v):
+        return (v + 255) & ~255
+    mt = (M + 127) // 128 * 128
+    nb = K // 32
+    o = {"qs": 0}
+    o["scale"] = al(o["qs"] + M * K)
+    o["bsum"] = al(o["scale"] + M * nb * 4)
+    o["op"] = al(o["bsum"] + M * nb * 4)
+    o["scaleT"] = al(o["op"] + M * K * 2)
+    o["minT"] = al(o["scaleT"] + mt * nb * 4)
+    o["total"] = al(o["minT"] + mt * nb * 4)
+    o["mt"] = mt
+    return o
+
+
 def act_views(xq, M: int, K: int):
     """Views (qs int8 [M][K], scale f32 [M][K/32], bsum int32 [M][K/32], op f16 [M][K])
     of an xq buffer, following the layout documented in mq.h."""
     import torch
-
-    def al(v):
-        return (v + 255) & ~255
-    o_qs = 0
-    o_sc = al(o_qs + M * K)
-    o_bs = al(o_sc + M * (K // 32) * 4)
-    o_op = al(o_bs + M * (K // 32) * 4)
-    qs = xq[o_qs:o_qs + M * K].view(torch.int8).view(M, K)
-    sc = xq[o_sc:o_sc + M * (K // 32) * 4].view(torch.float32).view(M, K // 32)
-    bs = xq[o_bs:o_bs + M * (K // 32) * 4].view(torch.int32).view(M, K // 32)
-    op = xq[o_op:o_op + M * K * 2].view(torch.float16).view(M, K)
+    o = act_layout(M, K)
+    nb = K // 32
+    qs = xq[o["qs"]:o["qs"] + M * K].view(torch.int8).view(M, K)
+    sc = xq[o["scale"]:o["scale"] + M * nb * 4].view(torch.float32).view(M, nb)
+    bs = xq[o["bsum"]:o["bsum"] + M * nb * 4].view(torch.int32).view(M, nb)
+    op = xq[o["op"]:o["op"] + M * K * 2].view(torch.float16).view(M, K)
     return qs, sc, bs, op
+
+
+def act_views_transposed(xq, M: int, K: int):
+    """Views (scaleT f32 [K/32][M], minT f32 [K/32][M]) of the transposed sections."""
+    import torch
+    o = act_layout(M, K)
+    nb, mt = K // 32, o["mt"]
+    st = xq[o["scaleT"]:o["scaleT"] + mt * nb * 4].view(torch.float32).view(nb, mt)[:, :M]
+    tt = xq[o["minT"]:o["minT"] + mt * nb * 4].view(torch.float32).view(nb, mt)[:, :M]
+    return st, tt
 
 
 def quantize_act(x, xq=None, stream=None):

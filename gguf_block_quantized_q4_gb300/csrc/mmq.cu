@@ -1,266 +1,487 @@
-// mmq.cu -- prefill MMQ: y[m][n] = sum_b s[m][b] * (d[n][b] * D[m][n][b] -
-// dmin_term[n][b] * S[m][b]) with D the exact integer dot of block b
-// ("minfer CUDA Backend Design" §4.4: the int8 MMQ path for prefill; the
-// per-block scale epilogue uses decoded f32 scale planes, §4.7 W_dsc).
+// mmq.cu -- prefill MMQ on the 5th-generation tensor cores (tcgen05):
+//   y[m][n] = sum_b s[m][b] * (d[n][b] * D[m][n][b] - dmin_term[n][b] * S[m][b])
+// with D the exact integer dot of 32-element block b ("minfer CUDA Backend
+// Design" §4.4: the int8 MMQ path for prefill; §4.7: decoded f32 scale planes
+// for the per-block epilogue).
 //
-// The contraction is exact: both operands are integers held in f16 (q in
-// [-127, 127]; W_int = Q8_0 q, Q4_K sc_j*nib <= 945, Q6_K q-32 in [-32, 31]),
-// every product is exact and every partial sum of one 32-element block stays
-// below 2^24, so the f32 tensor-core accumulation of a block equals the
-// integer dot.  (sm_103a has no integer tcgen05 kind and its legacy int8
-// mma.sync runs at a quarter of the f16 rate, so f16 with integer values is the
-// exact and fast encoding here.)
+// Exactness.  Both operands are integers carried in f16 (q in [-127, 127];
+// W_int = Q8_0 q, Q4_K sc_j*nib <= 945, Q6_K v = sc*(q-32) as even part +
+// odd part, each exact).  Every product is exact and every partial sum of a
+// block stays below 2^24 (|D| <= 32*127*4097 < 16.7M), so tcgen05.mma kind::f16
+// accumulating one block in f32 yields the integer dot exactly.  sm_103a has
+// no integer tcgen05 kind, and f16 integers are exact, so this is the int8
+// contraction on the tensor pipe.
 //
-// This kernel: CTA tile 64 (m) x 128 (n), 8 warps of 32 x 32, one 32-K block
-// per pipeline stage, a 4-stage cp.async ring, mma.sync m16n8k16 with
-// ldmatrix fragments from an XOR-swizzled tile.  Per block and element the
-// epilogue is
-//   Q8_0: y += (s_m * d_n) * D
-//   Q4_K: a += s_m * D,  y -= (s_m * S_m) * (dmin*m_j)_n,  per super-block y += d_n * a
-//   Q6_K: D = sc_lo_n * D_lo + sc_hi_n * D_hi (exact), a += s_m * D, per super-block y += d_n * a
-// In blockdots mode the per-block D is written out instead (test export).
-// Grid: m-tiles fastest, so the CTAs in flight share each weight tile through L2
-// and the weights stream from HBM about once.
+// Structure (one 128 x 128 output tile per CTA, 12 warps = 3 warpgroups).  The
+// K loop runs over pairs of 32-element blocks (64 K per pipeline stage):
+//   warpgroup 0 (registers lowered to 24 with setmaxnreg):
+//     warp 0    TMA producer: per pair, the activation tile (128 x 64 f16) and the
+//               weight tile(s) (128 x 64 f16; Q6_K also the odd part) into a
+//               shared-memory ring (128-byte swizzle), mbarrier tx-count; per 8
+//               blocks, 1-D bulk copies of the tile's row scales s and s*S and
+//               column scales d and dmin*m_j into a 2-slot ring.
+//     warps 1,2 MMA issuers (warp 1 also owns TMEM: 512 columns = two pairs of
+//               128-column f32 accumulators).  Issuer i takes the pairs p with
+//               p % 2 == i and accumulator pair i: 4 (Q6_K: 8) tcgen05.mma M=128
+//               N=128 K=16, one block per accumulator, then tcgen05.commit to the
+//               stage's "empty" and the accumulator pair's "full" barrier.  Two
+//               issuers keep the tensor pipe fed while the other one waits.
+//   warpgroups 1-2 (registers raised to 240): 8 epilogue warps.  Warp w reads
+//               TMEM lanes 32*(w%4).. (its 32 rows) and 64 of the 128 columns;
+//               per block it loads the accumulator (tcgen05.ld, both halves in
+//               flight, one wait) and promotes it in registers:
+//                 Q8_0: y += (s_m * d_n) * D
+//                 Q4_K: a += s_m * D;  y -= (s_m * S_m) * (dmin*m_j)_n; per super-block y += d_n * a
+//                 Q6_K: a += s_m * D;  per super-block y += d_n * a
+//               and frees the accumulator pair after its second block.
+// All mbarrier waits are bounded (2 s by %globaltimer); an expired wait writes
+// MQ_ERR_TIMEOUT into the device status word read by mq_stream_status.
+// Grid: m-tiles fastest, so concurrently running CTAs share each weight tile
+// through L2 and the weights stream from HBM about once.
+#include <cstddef>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "mq_common.cuh"
 
 namespace mq {
 namespace {
 
-constexpr int BM = 64, BN = 128, BK = 32, STAGES = 4, THREADS = 256;
-
-struct MmqArgs {
-  const __half *A;       // activation operand f16 [M][K]
-  const float *sx;       // [M][K/32]
-  const int32_t *ssum;   // [M][K/32]
-  const __half *W;       // weight operand f16 [N][K]
-  const float *bd;       // [N][K/32]
-  const float *bm;       // [N][K/32] (Q4_K)
-  const float *bs;       // [N][K/16] (Q6_K)
-  float *y;              // [M][N]
-  int32_t *D;            // [M][N][K/32] (blockdots mode)
-  int64_t M, N, K;
-};
-
-struct Stage {
-  __half a[BM * BK];
-  __half b[BN * BK];
-  float sx[BM];
-  int32_t ss[BM];
-  float bd[BN];
-  float bx[2 * BN];  // Q4_K: bm[n]; Q6_K: bs lo [n], bs hi [BN + n]
-};
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void cp16(void *s, const void *g, bool ok) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(s)), "l"(g),
-               "r"(ok ? 16 : 0));
-}
-__device__ __forceinline__ void cp4(void *s, const void *g, bool ok) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(s)), "l"(g),
-               "r"(ok ? 4 : 0));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Row r of a 32-K tile is 64 bytes = 4 chunks of 16; chunk c lives at c ^ ((r>>1)&3).
-__device__ __forceinline__ int swz(int r, int c) { return r * BK + 8 * (c ^ ((r >> 1) & 3)); }
+constexpr int TM = 128, TN = 128, TK = 32;
+constexpr int PK = 2 * TK;              // K per pipeline stage (a pair of blocks)
+constexpr int NEPI = 8;                 // epilogue warps
+constexpr int NTHR = 32 * (4 + NEPI);   // 384 threads
+constexpr uint32_t TMEM_COLS = 512;     // accumulator pair i at columns 256*i .. +256
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kTestWaitNs = 1000000ull;
+constexpr int kTileBytes = TM * PK * 2;  // 16 KB per operand tile and stage
+// launch: 384 threads x 168 registers = 64512; after setmaxnreg the control
+// warpgroup holds 128 x 24 and the epilogue warpgroups 256 x 240 = 64512.
+constexpr int kRegCtl = 24, kRegEpi = 240;
+static_assert(128 * kRegCtl + 256 * kRegEpi <= 384 * 168, "register split exceeds the launch");
 
 template <int TYPE>
-__device__ __forceinline__ void load_stage(const MmqArgs &p, Stage &st, int64_t m0, int64_t n0,
-                                           int64_t kb) {
-  const int tid = threadIdx.x;
-  const int64_t nb = p.K / 32;
-  {  // A: 64 rows x 4 chunks
-    const int r = tid >> 2, c = tid & 3;
-    const int64_t m = m0 + r;
-    const bool ok = m < p.M;
-    cp16(&st.a[swz(r, c)], p.A + (ok ? m : 0) * p.K + kb * BK + 8 * c, ok);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // B: 128 rows x 4 chunks
-    const int idx = tid + i * THREADS, r = idx >> 2, c = idx & 3;
-    const int64_t n = n0 + r;
-    const bool ok = n < p.N;
-    cp16(&st.b[swz(r, c)], p.W + (ok ? n : 0) * p.K + kb * BK + 8 * c, ok);
-  }
-  if (tid < BM) {
-    const int64_t m = m0 + tid;
-    const bool ok = m < p.M;
-    cp4(&st.sx[tid], p.sx + (ok ? m : 0) * nb + kb, ok);
-    cp4(&st.ss[tid], p.ssum + (ok ? m : 0) * nb + kb, ok);
-  } else if (tid < BM + BN) {
-    const int r = tid - BM;
-    const int64_t n = n0 + r;
-    const bool ok = n < p.N;
-    cp4(&st.bd[r], p.bd + (ok ? n : 0) * nb + kb, ok);
-    if constexpr (TYPE == MQ_Q4_K) cp4(&st.bx[r], p.bm + (ok ? n : 0) * nb + kb, ok);
-    if constexpr (TYPE == MQ_Q6_K) {
-      cp4(&st.bx[r], p.bs + (ok ? n : 0) * (2 * nb) + 2 * kb, ok);
-      cp4(&st.bx[BN + r], p.bs + (ok ? n : 0) * (2 * nb) + 2 * kb + 1, ok);
+constexpr int stages() {  // 192 KB of operand ring
+  return TYPE == MQ_Q6_K ? 4 : 6;
+}
+
+struct TcArgs {
+  const float *st;      // [nb][mt] activation block scales, transposed
+  const float *tt;      // [nb][mt] s*S, transposed
+  const float *td;      // [nb][np] weight block scale d, transposed
+  const float *tm;      // [nb][np] Q4_K dmin*m_j, transposed
+  float *y;             // [M][N]
+  int32_t *D;           // [M][N][nb] (block-dot mode)
+  int64_t M, N, mt, np;
+  int nb;
+  int *status;
+  int debug_expire;
+};
+
+// Arrays that some block types do not need take (almost) no space; every slot
+// array starts on a 128-byte boundary (bulk-copy destinations and float4 reads).
+template <class T, int N, int W>
+struct __align__(128) Slots {
+  T v[N][W];
+};
+template <class T, int W>
+struct __align__(128) Slots<T, 0, W> {
+  T v[1][1];  // never indexed
+};
+
+template <int TYPE>
+struct __align__(1024) TcSmem {
+  static constexpr int NST = stages<TYPE>();
+  static constexpr bool ODD = TYPE == MQ_Q6_K;
+  static constexpr bool MIN = TYPE == MQ_Q4_K;
+  __half a[NST][TM * PK];
+  __half b[NST][TN * PK];
+  Slots<__half, ODD ? NST : 0, TN * PK> b2;
+  alignas(128) float gsx[2][8][TM];     // per group slot: row scales s
+  alignas(128) float gd[2][8][TN];      // column scales d
+  Slots<float, MIN ? 16 : 0, TM> gt;    // row factors s*S (Q4_K), [slot*8 + block]
+  Slots<float, MIN ? 16 : 0, TN> gm;    // column dmin*m_j (Q4_K), [slot*8 + block]
+  uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], never;
+  uint32_t tmem;
+};
+
+template <int TYPE>
+constexpr bool smem_layout_ok() {
+  using S = TcSmem<TYPE>;
+  return offsetof(S, a) % 1024 == 0 && offsetof(S, b) % 1024 == 0 &&
+         offsetof(S, b2) % 1024 == 0 && offsetof(S, gsx) % 128 == 0 &&
+         offsetof(S, gd) % 128 == 0 && offsetof(S, gt) % 128 == 0 &&
+         offsetof(S, gm) % 128 == 0 && offsetof(S, full) % 8 == 0;
+}
+static_assert(smem_layout_ok<MQ_Q8_0>() && smem_layout_ok<MQ_Q4_K>() &&
+                  smem_layout_ok<MQ_Q6_K>(),
+              "TMA tiles need 1024-byte, bulk copies and float4 reads 16-byte alignment");
+
+__device__ __forceinline__ uint32_t sa(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// One non-suspending probe of an mbarrier phase (cheap when it has completed).
+__device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity), "r"(0)
+      : "memory");
+  return ok != 0;
+}
+// A probe that may suspend the thread until the phase completes (or a hardware
+// time limit passes), so a waiting warp does not take issue slots from others.
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase.  On expiry: record (timeout, site) in the
+// status word and return false; the caller carries on so the kernel ends.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *status, int site,
+                                          uint64_t limit_ns, unsigned sleep_ns = 0) {
+  if (mbar_probe(a, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      if (mbar_try(a, parity)) return true;
+      if (sleep_ns) __nanosleep(sleep_ns);
+    }
+    if (gtime() - t0 > limit_ns) {
+      if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
+      return false;
     }
   }
 }
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
+                                        uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// K-major operand in the 128-byte swizzle layout TMA writes: 8-row groups of
+// 1024 bytes (SBO), leading offset unused (16), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3fff) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+#define TC_LD32(taddr, r)                                                                     \
+  asm volatile(                                                                               \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"     \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),         \
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),         \
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),         \
+        "=r"(r[31])                                                                           \
+      : "r"(taddr))
 
 template <int TYPE, bool DOTS>
-__global__ void __launch_bounds__(THREADS, 1) mmq_kernel(const MmqArgs p) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Stage *stages = reinterpret_cast<Stage *>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wm = warp >> 2, wn = warp & 3;  // warp tile (32 m) x (32 n)
-  const int g = lane >> 2, t = lane & 3;
-  const int64_t m0 = int64_t(blockIdx.x) * BM, n0 = int64_t(blockIdx.y) * BN;
-  const int64_t nb = p.K / 32;
+__global__ void __launch_bounds__(NTHR, 1)
+    mmq_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
+                  const __grid_constant__ CUtensorMap tW2, const TcArgs p) {
+  using Sm = TcSmem<TYPE>;
+  constexpr int NST = Sm::NST;
+  constexpr bool ODD = Sm::ODD, MIN = Sm::MIN;
+  extern __shared__ uint8_t smem_raw[];
+  Sm &sm = *reinterpret_cast<Sm *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                   ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = int64_t(blockIdx.x) * TM, n0 = int64_t(blockIdx.y) * TN;
+  const int nb = p.nb, npairs = (nb + 1) / 2;
 
-  // fragment-owned rows/cols: rows wm*32 + mi*16 + g (+8), cols wn*32 + ni*8 + 2t (+1)
-  float y[2][4][4], a[2][4][4];
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-      for (int v = 0; v < 4; ++v) y[mi][ni][v] = a[mi][ni][v] = 0.f;
-
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nb) load_stage<TYPE>(p, stages[s], m0, n0, s);
-    cp_commit();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(sa(&sm.full[s]), 1);
+      mbar_init(sa(&sm.empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sa(&sm.tfull[t]), 1);
+      mbar_init(sa(&sm.tempty[t]), NEPI);
+      mbar_init(sa(&sm.gfull[t]), 1);
+      mbar_init(sa(&sm.gempty[t]), NEPI);
+    }
+    mbar_init(sa(&sm.never), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     sa(&sm.tmem)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
 
-  for (int64_t kb = 0; kb < nb; ++kb) {
-    cp_wait<STAGES - 2>();
-    __syncthreads();
-    {
-      const int64_t nk = kb + STAGES - 1;
-      if (nk < nb) load_stage<TYPE>(p, stages[nk % STAGES], m0, n0, nk);
-      cp_commit();
-    }
-    const Stage &st = stages[kb % STAGES];
-    float c0[2][4][4], c1[2][4][4];
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-      for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) c0[mi][ni][v] = c1[mi][ni][v] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {  // two k16 halves of the block
-      uint32_t af[2][4], bf[2][4];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int r = wm * 32 + mi * 16 + (lane & 15);
-        ldsm_x4(af[mi], &st.a[swz(r, 2 * ks + (lane >> 4))]);
-      }
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int r = wn * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        ldsm_x4(bf[np], &st.b[swz(r, 2 * ks + ((lane >> 3) & 1))]);
-      }
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-          const uint32_t b0 = bf[ni >> 1][2 * (ni & 1)], b1 = bf[ni >> 1][2 * (ni & 1) + 1];
-          if (TYPE == MQ_Q6_K && ks == 1)
-            mma16816(c1[mi][ni], af[mi], b0, b1);
-          else
-            mma16816(c0[mi][ni], af[mi], b0, b1);
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+    if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
+      const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
+      for (int pr = 0; pr < npairs; ++pr) {
+        if (!DOTS && (pr & 3) == 0) {  // group g = pr/4 of 8 blocks
+          const int g = pr >> 2, slot = g & 1, nbl = min(8, nb - 8 * g);
+          if (g >= 2)
+            mbar_wait(sa(&sm.gempty[slot]), ((g >> 1) - 1) & 1, p.status, 5, kWaitNs, 64);
+          mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * (MIN ? 4u : 2u));
+          for (int bi = 0; bi < nbl; ++bi) {
+            const int64_t b = 8 * g + bi;
+            bulk_1d(sa(sm.gsx[slot][bi]), p.st + b * p.mt + m0, 512, sa(&sm.gfull[slot]));
+            bulk_1d(sa(sm.gd[slot][bi]), p.td + b * p.np + n0, 512, sa(&sm.gfull[slot]));
+            if constexpr (MIN) {
+              bulk_1d(sa(sm.gt.v[MIN ? 8 * slot + bi : 0]), p.tt + b * p.mt + m0, 512,
+                      sa(&sm.gfull[slot]));
+              bulk_1d(sa(sm.gm.v[MIN ? 8 * slot + bi : 0]), p.tm + b * p.np + n0, 512,
+                      sa(&sm.gfull[slot]));
+            }
+          }
         }
+        const int s = pr % NST;
+        if (pr >= NST) mbar_wait(sa(&sm.empty[s]), ((pr / NST) - 1) & 1, p.status, 1, kWaitNs, 64);
+        mbar_expect_tx(sa(&sm.full[s]), bytes);
+        tma_2d(sa(sm.a[s]), &tA, pr * PK, (int)m0, sa(&sm.full[s]));
+        tma_2d(sa(sm.b[s]), &tW, pr * PK, (int)n0, sa(&sm.full[s]));
+        if constexpr (ODD) tma_2d(sa(sm.b2.v[ODD ? s : 0]), &tW2, pr * PK, (int)n0, sa(&sm.full[s]));
+      }
+    } else if ((warp == 1 || warp == 2) && lane == 0) {  // ---- MMA issuers
+      const int i = warp - 1;
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
+      const uint32_t acc0 = tmem + (uint32_t)(256 * i);
+      for (int pr = i; pr < npairs; pr += 2) {
+        const int s = pr % NST, use = pr >> 1;  // use: this issuer's pair count
+        mbar_wait(sa(&sm.full[s]), (pr / NST) & 1, p.status, 2, kWaitNs);
+        if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs, 32);
+        tc_fence_after();
+        const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // block 2*pr + h -> columns acc0 + 128*h
+          const uint32_t dt = acc0 + (uint32_t)(128 * h);
+          // +2 in the descriptor = +32 bytes = the next 16-element K slice
+          mma_f16(dt, ad + 4 * h, bd + 4 * h, idesc, 0u);
+          mma_f16(dt, ad + 4 * h + 2, bd + 4 * h + 2, idesc, 1u);
+          if constexpr (ODD) {
+            const uint64_t od = sdesc(sa(sm.b2.v[ODD ? s : 0]));
+            mma_f16(dt, ad + 4 * h, od + 4 * h, idesc, 1u);
+            mma_f16(dt, ad + 4 * h + 2, od + 4 * h + 2, idesc, 1u);
+          }
+        }
+        mma_commit(sa(&sm.empty[s]));
+        mma_commit(sa(&sm.tfull[i]));
+      }
     }
-    // epilogue of block kb
+  } else {  // ---- epilogue warps
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
+    const int e = warp - 4, q = warp & 3, hcol = e >> 2;
+    const int rl = 32 * q + lane;
+    const int64_t m = m0 + rl;
+    const bool mok = m < p.M;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * hcol);
+    float acc[64], y[64];
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
+    for (int j = 0; j < 64; ++j) acc[j] = y[j] = 0.f;
+    for (int pr = 0; pr < npairs; ++pr) {
+      const int i = pr & 1, use = pr >> 1;
+      const int g = pr >> 2, slot = g & 1;
+      if (!DOTS && (pr & 3) == 0)
+        mbar_wait(sa(&sm.gfull[slot]), (g >> 1) & 1, p.status, 6, kWaitNs);
+      if (pr == 0 && p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
+      mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
+      tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int b = 2 * pr + h;
+        if (b >= nb) break;
+        const int bi = b & 7;
+        uint32_t r[64];
+        TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
+        TC_LD32(trow + (uint32_t)(256 * i + 128 * h + 32), (r + 32));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if constexpr (DOTS) {
+          if (mok) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // rows g, g+8
-        const int rl = wm * 32 + mi * 16 + g + 8 * h;
-        const float sxm = st.sx[rl];
-        const float tm = sxm * (float)st.ss[rl];
+            for (int j = 0; j < 64; ++j) {
+              const int64_t n = n0 + 64 * hcol + j;
+              if (n < p.N) p.D[(m * p.N + n) * nb + b] = __float2int_rn(__uint_as_float(r[j]));
+            }
+          }
+        } else {
+          const float sxv = sm.gsx[slot][bi][rl];
+          const float4 *cd4 = reinterpret_cast<const float4 *>(&sm.gd[slot][bi][64 * hcol]);
+          if constexpr (TYPE == MQ_Q8_0) {
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
+            for (int j4 = 0; j4 < 16; ++j4) {
+              const float4 c = cd4[j4];
+              y[4 * j4 + 0] = fmaf(sxv * c.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
+              y[4 * j4 + 1] = fmaf(sxv * c.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
+              y[4 * j4 + 2] = fmaf(sxv * c.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
+              y[4 * j4 + 3] = fmaf(sxv * c.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
+            }
+          } else {
+            const float tv = MIN ? -sm.gt.v[MIN ? 8 * slot + bi : 0][MIN ? rl : 0] : 0.f;
+            const float4 *cm4 = reinterpret_cast<const float4 *>(
+                &sm.gm.v[MIN ? 8 * slot + bi : 0][MIN ? 64 * hcol : 0]);
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = wn * 32 + ni * 8 + 2 * t + e;
-            const int v = 2 * h + e;
-            float dv = c0[mi][ni][v];
-            if constexpr (TYPE == MQ_Q6_K) dv = fmaf(st.bx[BN + cl], c1[mi][ni][v], st.bx[cl] * dv);
-            if constexpr (DOTS) {
-              const int64_t m = m0 + rl, n = n0 + cl;
-              if (m < p.M && n < p.N) p.D[(m * p.N + n) * nb + kb] = __float2int_rn(dv);
-            } else if constexpr (TYPE == MQ_Q8_0) {
-              y[mi][ni][v] = fmaf(sxm * st.bd[cl], dv, y[mi][ni][v]);
-            } else {
-              a[mi][ni][v] = fmaf(sxm, dv, a[mi][ni][v]);
-              if constexpr (TYPE == MQ_Q4_K) y[mi][ni][v] = fmaf(-tm, st.bx[cl], y[mi][ni][v]);
-              if ((kb & 7) == 7) {
-                y[mi][ni][v] = fmaf(st.bd[cl], a[mi][ni][v], y[mi][ni][v]);
-                a[mi][ni][v] = 0.f;
+            for (int j4 = 0; j4 < 16; ++j4) {  // columns 4*j4 .. 4*j4+3
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                acc[4 * j4 + u] = fmaf(sxv, __uint_as_float(r[4 * j4 + u]), acc[4 * j4 + u]);
+              if constexpr (MIN) {
+                const float4 c = cm4[j4];
+                y[4 * j4 + 0] = fmaf(tv, c.x, y[4 * j4 + 0]);
+                y[4 * j4 + 1] = fmaf(tv, c.y, y[4 * j4 + 1]);
+                y[4 * j4 + 2] = fmaf(tv, c.z, y[4 * j4 + 2]);
+                y[4 * j4 + 3] = fmaf(tv, c.w, y[4 * j4 + 3]);
               }
+            }
+            if (bi == 7 || b == nb - 1) {  // end of a super-block: y += d * a
+#pragma unroll
+              for (int j4 = 0; j4 < 16; ++j4) {
+                const float4 c = cd4[j4];
+                y[4 * j4 + 0] = fmaf(c.x, acc[4 * j4 + 0], y[4 * j4 + 0]);
+                y[4 * j4 + 1] = fmaf(c.y, acc[4 * j4 + 1], y[4 * j4 + 1]);
+                y[4 * j4 + 2] = fmaf(c.z, acc[4 * j4 + 2], y[4 * j4 + 2]);
+                y[4 * j4 + 3] = fmaf(c.w, acc[4 * j4 + 3], y[4 * j4 + 3]);
+              }
+#pragma unroll
+              for (int j = 0; j < 64; ++j) acc[j] = 0.f;
             }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
+      if (!DOTS && ((pr & 3) == 3 || pr == npairs - 1)) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sa(&sm.gempty[slot]));
+      }
     }
-  }
-  cp_wait<0>();
-  if constexpr (!DOTS) {
+    if constexpr (!DOTS) {
+      if (mok) {
+        float *dst = p.y + m * p.N + n0 + 64 * hcol;
+        const int64_t left = p.N - (n0 + 64 * hcol);
+        if (left >= 64 && (p.N & 3) == 0) {
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+          for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+        } else {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t m = m0 + wm * 32 + mi * 16 + g + 8 * h;
-        if (m >= p.M) continue;
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-          const int64_t n = n0 + wn * 32 + ni * 8 + 2 * t;
-          float *dst = p.y + m * p.N + n;
-          const float v0 = y[mi][ni][2 * h], v1 = y[mi][ni][2 * h + 1];
-          if (n + 1 < p.N && ((p.N & 1) == 0)) {
-            *reinterpret_cast<float2 *>(dst) = make_float2(v0, v1);
-          } else {
-            if (n < p.N) dst[0] = v0;
-            if (n + 1 < p.N) dst[1] = v1;
-          }
+          for (int j = 0; j < 64; ++j)
+            if (j < left) dst[j] = y[j];
         }
       }
+    }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS));
 }
 
-template <int TYPE, bool DOTS>
-mq_status launch_t(const MmqArgs &a, cudaStream_t s, const char *name) {
-  const size_t smem = sizeof(Stage) * STAGES;
-  dim3 grid((unsigned)((a.M + BM - 1) / BM), (unsigned)((a.N + BN - 1) / BN));
-  if (grid.y > 65535)
-    return fail(MQ_ERR_SHAPE, "%s: N=%lld needs more than 65535 column tiles", name,
-                (long long)a.N);
-  mmq_kernel<TYPE, DOTS><<<grid, THREADS, smem, s>>>(a);
-  MQ_LAUNCH_CHECK(name);
+// ---- host side -------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+mq_status get_encode() {
+  if (g_encode) return MQ_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e =
+      cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(MQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver (%s)",
+                cudaGetErrorName(e));
+  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
   return MQ_OK;
+}
+
+// f16 [rows][K] K-major, box 64 x 128, 128-byte swizzle (rows beyond the tensor and
+// columns beyond K read as 0).
+mq_status encode_f16_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K,
+                         const char *what) {
+  mq_status s = get_encode();
+  if (s != MQ_OK) return s;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {PK, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MQ_ERR_CUDA, "TMA descriptor for the %s operand (%lld x %lld f16 at %p) refused: %d",
+                what, (long long)rows, (long long)K, ptr, (int)r);
+  return MQ_OK;
+}
+
+template <int TYPE>
+constexpr size_t smem_bytes() {
+  return sizeof(TcSmem<TYPE>) + 1024;
 }
 
 template <int TYPE, bool DOTS>
 mq_status optin_t(const DeviceState *st, const char *name) {
-  const size_t smem = sizeof(Stage) * STAGES;
+  const size_t smem = smem_bytes<TYPE>();
   if ((int)smem > st->smem_optin)
     return fail(MQ_ERR_LAUNCH, "%s needs %zu bytes of shared memory; the device allows %d", name,
                 smem, st->smem_optin);
-  cudaError_t e = cudaFuncSetAttribute(mmq_kernel<TYPE, DOTS>,
+  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<TYPE, DOTS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
@@ -268,47 +489,78 @@ mq_status optin_t(const DeviceState *st, const char *name) {
   return MQ_OK;
 }
 
+template <int TYPE, bool DOTS>
+mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const TcArgs &a, cudaStream_t s,
+                   const char *name) {
+  dim3 grid((unsigned)((a.M + TM - 1) / TM), (unsigned)((a.N + TN - 1) / TN));
+  if (grid.y > 65535)
+    return fail(MQ_ERR_SHAPE, "%s: N=%lld needs more than 65535 column tiles", name,
+                (long long)a.N);
+  const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
+  const CUtensorMap &tW2 = *reinterpret_cast<const CUtensorMap *>(
+      TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);
+  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, a);
+  MQ_LAUNCH_CHECK(name);
+  return MQ_OK;
+}
+
 }  // namespace
+
+mq_status encode_weight_maps(mq_weight *w) {
+  static_assert(sizeof(CUtensorMap) <= sizeof(w->tmap_w), "tensor map storage");
+  mq_status s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w), w->mw, w->N, w->K,
+                               "weight");
+  if (s != MQ_OK) return s;
+  if (w->mw2)
+    s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w2), w->mw2, w->N, w->K,
+                       "weight odd-part");
+  return s;
+}
 
 mq_status init_kernels(DeviceState *st) {
   mq_status s;
-  if ((s = optin_t<MQ_Q8_0, false>(st, "mmq_kernel<Q8_0>")) != MQ_OK) return s;
-  if ((s = optin_t<MQ_Q4_K, false>(st, "mmq_kernel<Q4_K>")) != MQ_OK) return s;
-  if ((s = optin_t<MQ_Q6_K, false>(st, "mmq_kernel<Q6_K>")) != MQ_OK) return s;
-  if ((s = optin_t<MQ_Q8_0, true>(st, "mmq_kernel<Q8_0,dots>")) != MQ_OK) return s;
-  if ((s = optin_t<MQ_Q4_K, true>(st, "mmq_kernel<Q4_K,dots>")) != MQ_OK) return s;
-  if ((s = optin_t<MQ_Q6_K, true>(st, "mmq_kernel<Q6_K,dots>")) != MQ_OK) return s;
+  if ((s = get_encode()) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q8_0, false>(st, "mmq_tc_kernel<Q8_0>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_K, false>(st, "mmq_tc_kernel<Q4_K>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q6_K, false>(st, "mmq_tc_kernel<Q6_K>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q8_0, true>(st, "mmq_tc_kernel<Q8_0,dots>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_K, true>(st, "mmq_tc_kernel<Q4_K,dots>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q6_K, true>(st, "mmq_tc_kernel<Q6_K,dots>")) != MQ_OK) return s;
   return MQ_OK;
 }
 
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
-                     cudaStream_t s, const DeviceState *) {
+                     cudaStream_t s, const DeviceState *st, int debug_expire) {
   const ActLayout L = act_layout(M, W->K);
   const uint8_t *base = reinterpret_cast<const uint8_t *>(xq);
-  MmqArgs a;
-  a.A = reinterpret_cast<const __half *>(base + L.op);
-  a.sx = reinterpret_cast<const float *>(base + L.scale);
-  a.ssum = reinterpret_cast<const int32_t *>(base + L.bsum);
-  a.W = W->mw;
-  a.bd = W->mbd;
-  a.bm = W->mbm;
-  a.bs = W->mbs;
+  alignas(64) CUtensorMap tA;
+  mq_status r = encode_f16_map(&tA, base + L.op, M, W->K, "activation");
+  if (r != MQ_OK) return r;
+  TcArgs a;
+  a.st = reinterpret_cast<const float *>(base + L.st);
+  a.tt = reinterpret_cast<const float *>(base + L.tt);
+  a.td = W->td;
+  a.tm = W->tm;
   a.y = y;
   a.D = D;
   a.M = M;
   a.N = W->N;
-  a.K = W->K;
+  a.mt = L.mt;
+  a.np = W->np;
+  a.nb = (int)(W->K / 32);
+  a.status = st->status;
+  a.debug_expire = debug_expire;
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
-      return dots ? launch_t<MQ_Q4_K, true>(a, s, "mmq_kernel<Q4_K,dots>")
-                  : launch_t<MQ_Q4_K, false>(a, s, "mmq_kernel<Q4_K>");
+      return dots ? launch_t<MQ_Q4_K, true>(W, tA, a, s, "mmq_tc_kernel<Q4_K,dots>")
+                  : launch_t<MQ_Q4_K, false>(W, tA, a, s, "mmq_tc_kernel<Q4_K>");
     case MQ_Q6_K:
-      return dots ? launch_t<MQ_Q6_K, true>(a, s, "mmq_kernel<Q6_K,dots>")
-                  : launch_t<MQ_Q6_K, false>(a, s, "mmq_kernel<Q6_K>");
+      return dots ? launch_t<MQ_Q6_K, true>(W, tA, a, s, "mmq_tc_kernel<Q6_K,dots>")
+                  : launch_t<MQ_Q6_K, false>(W, tA, a, s, "mmq_tc_kernel<Q6_K>");
     default:
-      return dots ? launch_t<MQ_Q8_0, true>(a, s, "mmq_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q8_0, false>(a, s, "mmq_kernel<Q8_0>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, a, s, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q8_0, false>(W, tA, a, s, "mmq_tc_kernel<Q8_0>");
   }
 }
 

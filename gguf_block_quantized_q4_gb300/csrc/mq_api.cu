@@ -7,6 +7,7 @@
 // naming the call, the invariant and the values; there is no fallback path.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -137,11 +138,11 @@ static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t
 }
 
 static mq_status free_planes(mq_weight *w) {
-  void *ps[] = {w->q, w->sc, w->d, w->mw, w->mbd, w->mbm, w->mbs};
+  void *ps[] = {w->q, w->sc, w->d, w->mw, w->mw2, w->td, w->tm};
   for (void *p : ps)
     if (p) cudaFree(p);
   w->q = nullptr; w->sc = nullptr; w->d = nullptr; w->mw = nullptr;
-  w->mbd = nullptr; w->mbm = nullptr; w->mbs = nullptr;
+  w->mw2 = nullptr; w->td = nullptr; w->tm = nullptr;
   return MQ_OK;
 }
 
@@ -180,6 +181,7 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
   w->type = type;
   w->N = N;
   w->K = K;
+  w->np = round_up(N, 128);
   CK(cudaGetDevice(&w->device), site);
   w->payload = nbytes;
   size_t total = 0;
@@ -208,14 +210,17 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
   if (mmq) {
     if ((s = alloc_plane(&w->mw, size_t(N) * K * 2, &total, "prefill operand")) != MQ_OK)
       return cleanup(s);
-    if ((s = alloc_plane(&w->mbd, size_t(N) * (K / 32) * 4, &total, "prefill d")) != MQ_OK)
+    if (type == MQ_Q6_K &&
+        (s = alloc_plane(&w->mw2, size_t(N) * K * 2, &total, "prefill odd part")) != MQ_OK)
+      return cleanup(s);
+    if ((s = alloc_plane(&w->td, size_t(w->np) * (K / 32) * 4, &total, "prefill d")) != MQ_OK)
       return cleanup(s);
     if (type == MQ_Q4_K &&
-        (s = alloc_plane(&w->mbm, size_t(N) * (K / 32) * 4, &total, "prefill min")) != MQ_OK)
+        (s = alloc_plane(&w->tm, size_t(w->np) * (K / 32) * 4, &total, "prefill min")) != MQ_OK)
       return cleanup(s);
-    if (type == MQ_Q6_K &&
-        (s = alloc_plane(&w->mbs, size_t(N) * (K / 16) * 4, &total, "prefill sub-scale")) != MQ_OK)
-      return cleanup(s);
+    // the padding columns of the transposed planes must read as zero
+    cudaMemsetAsync(w->td, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
+    if (w->tm) cudaMemsetAsync(w->tm, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
   }
   w->device_bytes = total;
 
@@ -231,6 +236,7 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
   cudaFree(raw);
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "upload/repack", site));
   if (s != MQ_OK) return cleanup(s);
+  if (mmq && (s = encode_weight_maps(w)) != MQ_OK) return cleanup(s);
   *out = w;
   return MQ_OK;
 }
@@ -361,6 +367,15 @@ extern "C" mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_
   return launch_quantize(x, xq, M, K, (cudaStream_t)stream);
 }
 
+// Failure-injection seam for the bounded-wait test: with MQ_TEST_EXPIRE_WAIT=1 the
+// MMQ epilogue first waits on a barrier nothing arrives on; the wait expires
+// after about a millisecond, records MQ_ERR_TIMEOUT in the status word and the
+// kernel carries on (results stay correct).  Read at every call.
+static int test_expire_wait() {
+  const char *v = getenv("MQ_TEST_EXPIRE_WAIT");
+  return (v && v[0] == '1') ? 1 : 0;
+}
+
 static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, const void *xq,
                             const void *out, int64_t M, int64_t N, int64_t K, DeviceState **st) {
   mq_status s = check_weight(site, type, W, N, K);
@@ -380,7 +395,7 @@ extern "C" mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, fl
   DeviceState *st = nullptr;
   mq_status s = mmq_common("mq_mmq", type, W, xq, y, M, N, K, &st);
   if (s != MQ_OK) return s;
-  return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st);
+  return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait());
 }
 
 extern "C" mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const void *xq,
@@ -389,7 +404,7 @@ extern "C" mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const vo
   DeviceState *st = nullptr;
   mq_status s = mmq_common("mq_mmq_blockdots", type, W, xq, D, M, N, K, &st);
   if (s != MQ_OK) return s;
-  return launch_mmq(W, xq, nullptr, D, M, (cudaStream_t)stream, st);
+  return launch_mmq(W, xq, nullptr, D, M, (cudaStream_t)stream, st, test_expire_wait());
 }
 
 extern "C" mq_status mq_stream_status(mq_stream stream) {

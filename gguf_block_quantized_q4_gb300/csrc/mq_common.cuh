@@ -19,11 +19,14 @@
 //                                w=1 ql[64h + 32 + 16v + 4t + i], w=2 qh[32h + 16v + 4t + i]
 //         sc   int8 [N][K/256][16] the sub-scales
 //         d    u16  [N][K/256]  the f16 super-block scales
-// Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them):
-//   w      f16  [N][K]   integer weight W_int (Q8_0 q; Q4_K sc_j*nib; Q6_K q-32)
-//   bd     f32  [N][K/32] block scale d of the element's (super-)block
-//   bm     f32  [N][K/32] Q4_K only: dmin*m_j (the min term)
-//   bs     f32  [N][K/16] Q6_K only: the 16-element sub-scale
+// Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them), K-major for TMA:
+//   w      f16  [N][K]    integer weight W_int: Q8_0 q; Q4_K sc_j*nib (<= 945);
+//                         Q6_K the even part 2*floor(v/2) of v = sc*(q-32) (|v| <= 4096)
+//   w2     f16  [N][K]    Q6_K only: the odd part v - 2*floor(v/2) in {0, 1}
+//                         (every value exact in f16; w + w2 = v)
+//   td     f32  [K/32][Np] block scale d of each 32-element block (transposed;
+//                          Np = N rounded up to 128, the padding is zero)
+//   tm     f32  [K/32][Np] Q4_K only: dmin*m_j of each block (transposed)
 #pragma once
 
 #include <cstddef>
@@ -31,11 +34,12 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/mq.h"
+#include "mq.h"
 
 struct mq_weight {
   int type;
   int64_t N, K;
+  int64_t np;            // N rounded up to 128: row stride of the transposed planes
   int device;
   size_t payload;        // GGUF bytes
   size_t device_bytes;   // all planes
@@ -45,9 +49,11 @@ struct mq_weight {
   uint16_t *d = nullptr; // Q8_0 block d / Q6_K super-block d
   // prefill operand planes
   __half *mw = nullptr;
-  float *mbd = nullptr;
-  float *mbm = nullptr;
-  float *mbs = nullptr;
+  __half *mw2 = nullptr;
+  float *td = nullptr;
+  float *tm = nullptr;
+  alignas(64) unsigned char tmap_w[128];   // TMA descriptors of w and w2 (CUtensorMap)
+  alignas(64) unsigned char tmap_w2[128];
 };
 
 namespace mq {
@@ -64,7 +70,7 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
-  int *status = nullptr;  // device status word for bounded waits
+  int *status = nullptr;  // device status word for bounded waits (code, kernel id)
   cudaStream_t reg_stream = nullptr;
 };
 DeviceState *device_state(int dev);  // nullptr if mq_init(dev) was not called
@@ -77,21 +83,30 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
                         const DeviceState *st);
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
-                     cudaStream_t s, const DeviceState *st);
+                     cudaStream_t s, const DeviceState *st, int debug_expire);
+mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
 mq_status init_kernels(DeviceState *st);  // smem opt-ins
 
-// xq buffer layout (mq_act_bytes)
+// xq buffer layout (mq_act_bytes): q int8 [M][K], s f32 [M][K/32], S int32
+// [M][K/32], q as f16 [M][K], then the transposed block scales sT f32
+// [K/32][Mt] and the min-term factors tT = s*S f32 [K/32][Mt], Mt = M rounded up
+// to 128 (the epilogue's tile rows are one contiguous 512-byte run per block).
 struct ActLayout {
-  size_t qs, scale, bsum, op, total;
+  size_t qs, scale, bsum, op, st, tt, total;
+  int64_t mt;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 inline ActLayout act_layout(int64_t M, int64_t K) {
   ActLayout L;
+  L.mt = round_up(M, 128);
   L.qs = 0;
   L.scale = align256(L.qs + size_t(M) * K);
   L.bsum = align256(L.scale + size_t(M) * (K / 32) * 4);
   L.op = align256(L.bsum + size_t(M) * (K / 32) * 4);
-  L.total = align256(L.op + size_t(M) * K * 2);
+  L.st = align256(L.op + size_t(M) * K * 2);
+  L.tt = align256(L.st + size_t(L.mt) * (K / 32) * 4);
+  L.total = align256(L.tt + size_t(L.mt) * (K / 32) * 4);
   return L;
 }
 

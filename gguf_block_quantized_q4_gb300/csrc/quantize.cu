@@ -7,8 +7,9 @@
 //   amax = max |x|;  s = amax / 127 (correctly rounded division);
 //   q = round_half_even(x / s) clamped to [-127, 127], or 0 when s == 0;
 //   S = sum q.
-// Writes the four sections of the xq buffer (mq_act_bytes): q as int8, s as
-// f32, S as int32, and q as f16 (the tensor-core operand of mq_mmq).
+// Writes every section of the xq buffer (mq_act_bytes): q as int8, s as f32,
+// S as int32, q as f16 (the tensor-core operand of mq_mmq), and the transposed
+// s and s*S planes the MMQ epilogue stages per 128-row tile.
 //
 // Memory-bound: 8 threads per block, 4 elements (one float4) per thread; the
 // block's max and sum reduce over the 8 lanes with shuffles.
@@ -57,6 +58,9 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
   if (sub == 0) {
     reinterpret_cast<float *>(xq + L.scale)[blk] = s;
     reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
+    const int64_t nb = K / 32, m = blk / nb, b = blk - m * nb;
+    reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
+    reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = s * (float)S;
   }
 }
 

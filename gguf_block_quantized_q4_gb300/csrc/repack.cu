@@ -13,8 +13,10 @@
 //         element 128h + 32r + l: low 4 bits from ql[64h + 32(r%2) + l] (low nibble
 //         for r<2, high for r>=2), high 2 bits = (qh[32h + l] >> 2r) & 3;
 //         w = d * sc[e/16] * (q - 32)
-// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_K sc_j*nib,
-// at most 945, exact in f16; Q6_K q - 32) and f32 block scales.
+// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_K sc_j*nib, at
+// most 945, exact in f16; Q6_K v = sc*(q-32), |v| <= 4096, stored as its even
+// part 2*floor(v/2) plus its odd part in {0,1}, both exact in f16) and the
+// transposed f32 block-scale planes td (d) and tm (Q4_K dmin*m_j).
 #include "mq_common.cuh"
 
 namespace mq {
@@ -36,9 +38,9 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *s, int j, int &sc, 
 }
 
 // One thread per GGUF block.
-__global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+__global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
                             uint8_t *__restrict__ q, uint16_t *__restrict__ d,
-                            __half *__restrict__ mw, float *__restrict__ mbd) {
+                            __half *__restrict__ mw, float *__restrict__ td) {
   const int64_t nb = K / 32;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nb) return;
@@ -52,7 +54,7 @@ __global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t 
       for (int e = 0; e < 4; ++e) dst[8 * t + 4 * u + e] = src[2 + 16 * u + 4 * t + e];
   if (mw) {
     for (int e = 0; e < 32; ++e) mw[n * K + b * 32 + e] = __int2half_rn((int8_t)src[2 + e]);
-    mbd[i] = f16bits(dbits);
+    td[b * NP + n] = f16bits(dbits);
   }
 }
 
@@ -72,9 +74,9 @@ __global__ void unpack_q8_0(const uint8_t *__restrict__ q, const uint16_t *__res
 }
 
 // One thread per super-block.
-__global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+__global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
                             uint8_t *__restrict__ q, __half *__restrict__ mw,
-                            float *__restrict__ mbd, float *__restrict__ mbm) {
+                            float *__restrict__ td, float *__restrict__ tm) {
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
@@ -97,8 +99,8 @@ __global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
         const int nib = (src[16 + 32 * c + l] >> (4 * h)) & 15;
         mw[n * K + s * 256 + 32 * j + l] = __int2half_rn(sc * nib);
       }
-      mbd[n * (K / 32) + s * 8 + j] = dd;
-      mbm[n * (K / 32) + s * 8 + j] = dmin * (float)m;
+      td[(s * 8 + j) * NP + n] = dd;
+      tm[(s * 8 + j) * NP + n] = dmin * (float)m;
     }
   }
 }
@@ -125,10 +127,10 @@ __device__ __forceinline__ int q6k_src(int t, int h, int v, int w) {
                 : (w == 1 ? 64 * h + 32 + 16 * v + 4 * t : 128 + 32 * h + 16 * v + 4 * t);
 }
 
-__global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+__global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
                             uint8_t *__restrict__ q, int8_t *__restrict__ sc,
                             uint16_t *__restrict__ d, __half *__restrict__ mw,
-                            float *__restrict__ mbd, float *__restrict__ mbs) {
+                            __half *__restrict__ mw2, float *__restrict__ td) {
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
@@ -151,10 +153,12 @@ __global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
       const int qlb = src[64 * h + 32 * (r % 2) + l];
       const int lo4 = r < 2 ? (qlb & 15) : (qlb >> 4);
       const int hi2 = (src[128 + 32 * h + l] >> (2 * r)) & 3;
-      mw[n * K + s * 256 + e] = __int2half_rn((lo4 | (hi2 << 4)) - 32);
+      const int v = (int)(int8_t)src[192 + e / 16] * ((lo4 | (hi2 << 4)) - 32);
+      const int odd = v & 1;  // v - 2*floor(v/2), two's complement
+      mw[n * K + s * 256 + e] = __int2half_rn(v - odd);
+      mw2[n * K + s * 256 + e] = __int2half_rn(odd);
     }
-    for (int b = 0; b < 8; ++b) mbd[n * (K / 32) + s * 8 + b] = dd;
-    for (int g = 0; g < 16; ++g) mbs[n * (K / 16) + s * 16 + g] = (float)(int8_t)src[192 + g];
+    for (int b = 0; b < 8; ++b) td[(s * 8 + b) * NP + n] = dd;
   }
 }
 
@@ -186,18 +190,18 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
   const int64_t N = w->N, K = w->K;
   if (w->type == MQ_Q8_0) {
     const int64_t n = N * (K / 32);
-    repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, w->d, mmq ? w->mw : nullptr,
-                                              w->mbd);
+    repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
+                                              w->td);
     MQ_LAUNCH_CHECK("repack_q8_0");
   } else if (w->type == MQ_Q4_K) {
     const int64_t n = N * (K / 256);
-    repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, mmq ? w->mw : nullptr, w->mbd,
-                                              w->mbm);
+    repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr, w->td,
+                                              w->tm);
     MQ_LAUNCH_CHECK("repack_q4_k");
   } else {
     const int64_t n = N * (K / 256);
-    repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->q, w->sc, w->d,
-                                              mmq ? w->mw : nullptr, w->mbd, w->mbs);
+    repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->sc, w->d,
+                                              mmq ? w->mw : nullptr, w->mw2, w->td);
     MQ_LAUNCH_CHECK("repack_q6_k");
   }
   return MQ_OK;

@@ -129,11 +129,14 @@ mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, 
                     int64_t K, int B, mq_stream stream);
 
 /* mq_act_bytes -- size of the quantised-activation buffer xq for M x K.
- * Layout (each section starts on a 256-byte boundary, in this order):
+ * Layout (each section starts on a 256-byte boundary, in this order;
+ * Mt = M rounded up to a multiple of 128):
  *   qs      int8  [M][K]       the quantised values q
  *   scale   f32   [M][K/32]    the block scales s = max|x| / 127
  *   bsum    int32 [M][K/32]    the block sums S = sum q
  *   operand f16   [M][K]       q as f16 (exact), the tensor-core operand
+ *   scaleT  f32   [K/32][Mt]   s transposed (rows >= M unspecified)
+ *   minT    f32   [K/32][Mt]   s * S transposed, the min-term factor (rows >= M unspecified)
  * Returns 0 if K is not a positive multiple of 32 or M < 1. */
 size_t mq_act_bytes(int64_t M, int64_t K);
 

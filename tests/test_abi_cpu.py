@@ -55,8 +55,10 @@ def test_act_bytes_layout(L):
     assert L.mq_act_bytes(4, 48) == 0
     M, K = 3, 96
     al = lambda v: (v + 255) & ~255
-    expect = al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2)
-    assert L.mq_act_bytes(M, K) == expect
+    mt = 128
+    expect = al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2) + mt * 3 * 4)
+                + mt * 3 * 4)
+    assert L.mq_act_bytes(M, K) == expect == mq.act_layout(M, K)["total"]
     assert L.mq_act_bytes(512, 3584) % 256 == 0
 
 

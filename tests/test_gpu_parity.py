@@ -148,12 +148,15 @@ def gpu_quantize(x):
 
 
 def assert_quant_exact(x):
-    _, qs, sc, bs, op = gpu_quantize(x)
+    xq, qs, sc, bs, op = gpu_quantize(x)
     rq, rs, rb = oracle.quantize_act(x)
     assert np.array_equal(qs, rq)
     assert np.array_equal(sc.view(np.uint32), rs.view(np.uint32))
     assert np.array_equal(bs, rb)
     assert np.array_equal(op.astype(np.float32), rq.astype(np.float32))
+    st, tt = (v.cpu().numpy() for v in mq.act_views_transposed(xq, *x.shape))
+    assert np.array_equal(st.T.view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(tt.T, rs * rb.astype(np.float32))
 
 
 @pytest.mark.parametrize("name,M", [("q4_k_mmq_512x18944x3584", 512),
@@ -242,6 +245,29 @@ def test_mmq_workloads_sampled(name):
                                mrows=rows, n0=n0, n1=n1)
         assert_bound(y[rows, n0:n1], yref, bnd, f"{name} cols {n0}:{n1}")
     assert np.isfinite(y).all()
+
+
+def test_bounded_wait_expiry_is_reported_and_the_result_stays_correct(monkeypatch):
+    """With the failure-injection seam, the MMQ epilogue waits on a barrier nothing
+    arrives on; the bounded wait expires, the status word reports MQ_ERR_TIMEOUT,
+    and the kernel finishes with the correct result (the context stays usable)."""
+    qtype, N, K, M = 12, 200, 768, 65
+    W = registered(qtype, N, K, 17)
+    x = synth.activations(M, K, seed=M + K)
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    mq.stream_status()
+    monkeypatch.setenv("MQ_TEST_EXPIRE_WAIT", "1")
+    y = mq.mmq(W, xq, M)
+    with pytest.raises(mq.MQError) as e:
+        mq.stream_status()
+    assert e.value.name == "MQ_ERR_TIMEOUT"
+    monkeypatch.delenv("MQ_TEST_EXPIRE_WAIT")
+    mq.stream_status()  # cleared
+    yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 17), N, K, qs, sc)
+    assert_bound(y.cpu().numpy(), yref, bnd, "after an expired wait")
+    y2 = mq.mmq(W, xq, M)
+    mq.stream_status()
+    assert np.array_equal(y.cpu().numpy(), y2.cpu().numpy())
 
 
 # ---- errors on the device path -----------------------------------------------
