@@ -29,11 +29,16 @@
 // by B pairs (x[4t], x[4t+1]) and (x[4t+2], x[4t+3]).  The decode planes
 // (repack.cu) store each thread's words contiguously.
 //
-// Work split: a CTA of WARPS warps owns 16*WARPS consecutive rows and one
-// K-slice; when one wave would be short of CTAs, K is split over a thread-block
-// cluster of S CTAs whose partial sums are reduced through distributed shared
-// memory in rank order (deterministic, and independent of B, so every column of
-// a batched call equals the B = 1 call bitwise).
+// Data movement: a CTA owns one 64-row group of the decode plane and a K-slice.
+// A producer warp streams, per 256-element chunk, the group's weight tile (one
+// contiguous run of the tiled decode plane) and the x chunk of every batch row
+// into a 4-stage shared-memory ring with 1-D bulk copies (cp.async.bulk,
+// mbarrier transaction counts); four compute warps, 16 rows each, read their
+// fragment words from shared memory.  When one wave would be short of CTAs, K
+// is split over a thread-block cluster of S CTAs whose partial sums are reduced
+// through distributed shared memory in rank order (deterministic, and
+// independent of B, so every column of a batched call equals the B = 1 call
+// bitwise).  All mbarrier waits are bounded.
 #include <cooperative_groups.h>
 
 #include "mq_common.cuh"
@@ -43,7 +48,9 @@ namespace cg = cooperative_groups;
 namespace mq {
 namespace {
 
-constexpr int kChunk = 256;  // K elements staged per step (16 groups of 16)
+constexpr int kNS = 4;          // shared-memory ring stages
+constexpr int kThreads = 160;   // 4 compute warps + 1 producer warp
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct MvArgs {
   const uint8_t *q;
@@ -55,7 +62,17 @@ struct MvArgs {
   int B;
   int nchunk;  // ceil(K / 256)
   int S;       // K slices (cluster size)
+  int *status;
 };
+
+// Bytes of one (64-row group, chunk) tile of the decode planes, as laid out in
+// shared memory: Q4_K 64 x 144; Q6_K 64 x 192 quants, then 64 x 16 sub-scales,
+// then 64 f16 d; Q8_0 64 x 256 quants (64 x chunk width used), then 64 x 8 f16 d.
+template <int TYPE>
+constexpr int tile_bytes() {
+  return TYPE == MQ_Q4_K ? 64 * 144 : (TYPE == MQ_Q6_K ? 64 * 192 + 64 * 16 + 64 * 2
+                                                       : 64 * 256 + 64 * 16);
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -118,112 +135,138 @@ struct WRegs<MQ_Q8_0> {  // 2 words per row per block, 8 blocks
   uint16_t da[8], db[8];
 };
 
-template <int WARPS, int NT>
-struct Smem {
+template <int TYPE, int NT>
+struct MvSmem {
+  alignas(128) uint8_t w[kNS][tile_bytes<TYPE>()];  // weight tiles
+  alignas(128) float x[kNS][4 * NT][kChunk];        // x chunks of the batch rows
   uint2 frag[16][NT][32];      // B fragments of the staged chunk
   float xsum[8][8];            // Q4_K: per sub-block, per batch row sum of scaled x
   unsigned wmax[8 * NT];       // per 32-item slice max |x| bits
   float unscale[8];            // 2^-e per batch row of the chunk
-  float tab[WARPS][16][16];    // per-warp decoded scales of the tile's 16 rows
-  float part[WARPS * 16][8];   // split-K partial sums
+  float tab[4][16][16];        // per-warp decoded scales of the tile's 16 rows
+  float part[64][8];           // split-K partial sums
+  uint64_t full[kNS], empty[kNS];
 };
 
-// Load the weight words of chunk c for rows rA (g) and rB (g+8).
+__device__ __forceinline__ int chunk_width(int64_t K, int c) {
+  const int64_t left = K - int64_t(c) * kChunk;
+  return left < kChunk ? (int)left : kChunk;
+}
+__device__ __forceinline__ uint32_t sa(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; on expiry records (timeout, site) in the status word and returns.
+__device__ __forceinline__ void mbar_wait(uint32_t a, uint32_t parity, int *status, int site) {
+  if (mbar_try(a, parity)) return;
+  const uint64_t t0 = gtime();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try(a, parity)) return;
+    if (gtime() - t0 > kWaitNs) {
+      if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
+                                        uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// The fragment words of one chunk for tile rows ra (g) and ra + 8, from the
+// shared-memory tile (nblk = blocks in the chunk, Q8_0 only).
 template <int TYPE>
-__device__ __forceinline__ void load_chunk(const MvArgs &p, WRegs<TYPE> &w, int64_t rA,
-                                           int64_t rB, bool okA, bool okB, int c, int t) {
+__device__ __forceinline__ void load_words(const uint8_t *tile, WRegs<TYPE> &w, int ra, int t,
+                                           int nblk) {
+  const int rb = ra + 8;
   if constexpr (TYPE == MQ_Q4_K) {
-    const int64_t nsb = p.K / 256;
-    const uint8_t *ba = p.q + (rA * nsb + c) * 144;
-    const uint8_t *bb = p.q + (rB * nsb + c) * 144;
-    uint4 z = make_uint4(0, 0, 0, 0);
-    uint4 a0 = okA ? ldg16(ba + 16 + 32 * t) : z, a1 = okA ? ldg16(ba + 32 + 32 * t) : z;
-    uint4 b0 = okB ? ldg16(bb + 16 + 32 * t) : z, b1 = okB ? ldg16(bb + 32 + 32 * t) : z;
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 16 + 32 * t);
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 32 + 32 * t);
+    const uint4 b0 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 16 + 32 * t);
+    const uint4 b1 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 32 + 32 * t);
     w.a[0] = a0.x; w.a[1] = a0.y; w.a[2] = a0.z; w.a[3] = a0.w;
     w.a[4] = a1.x; w.a[5] = a1.y; w.a[6] = a1.z; w.a[7] = a1.w;
     w.b[0] = b0.x; w.b[1] = b0.y; w.b[2] = b0.z; w.b[3] = b0.w;
     w.b[4] = b1.x; w.b[5] = b1.y; w.b[6] = b1.z; w.b[7] = b1.w;
-    const bool own = (t & 1) ? okB : okA;
-    w.hdr = own ? ldg16((t & 1) ? bb : ba) : z;
+    w.hdr = *reinterpret_cast<const uint4 *>(tile + ((t & 1) ? rb : ra) * 144);
   } else if constexpr (TYPE == MQ_Q6_K) {
-    const int64_t nsb = p.K / 256;
-    const uint8_t *ba = p.q + (rA * nsb + c) * 192 + 48 * t;
-    const uint8_t *bb = p.q + (rB * nsb + c) * 192 + 48 * t;
-    uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-      uint4 va = okA ? ldg16(ba + 16 * i) : z, vb = okB ? ldg16(bb + 16 * i) : z;
+      const uint4 va = *reinterpret_cast<const uint4 *>(tile + ra * 192 + 48 * t + 16 * i);
+      const uint4 vb = *reinterpret_cast<const uint4 *>(tile + rb * 192 + 48 * t + 16 * i);
       w.a[4 * i] = va.x; w.a[4 * i + 1] = va.y; w.a[4 * i + 2] = va.z; w.a[4 * i + 3] = va.w;
       w.b[4 * i] = vb.x; w.b[4 * i + 1] = vb.y; w.b[4 * i + 2] = vb.z; w.b[4 * i + 3] = vb.w;
     }
-    const bool own = (t & 1) ? okB : okA;
-    const int64_t row = (t & 1) ? rB : rA;
-    w.sc8 = own ? ldg8(p.sc + (row * nsb + c) * 16 + 8 * (t >> 1)) : make_uint2(0, 0);
-    w.dbits = own ? p.d[row * nsb + c] : (uint16_t)0;
-  } else {  // Q8_0: blocks 8c .. 8c+7 (fewer in the last chunk)
-    const int64_t nb = p.K / 32;
-    const int64_t left = nb - int64_t(c) * 8;
-    const int nblk = left < 8 ? (int)left : 8;
+    const int row = (t & 1) ? rb : ra;
+    w.sc8 = *reinterpret_cast<const uint2 *>(tile + 64 * 192 + row * 16 + 8 * (t >> 1));
+    w.dbits = *reinterpret_cast<const uint16_t *>(tile + 64 * 192 + 64 * 16 + row * 2);
+  } else {  // Q8_0: [block j][row][32 bytes], then d [row][8]
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const bool in = i < nblk;
-      const int64_t blk = int64_t(c) * 8 + i;
-      uint2 va = (okA && in) ? ldg8(p.q + rA * p.K + blk * 32 + 8 * t) : make_uint2(0, 0);
-      uint2 vb = (okB && in) ? ldg8(p.q + rB * p.K + blk * 32 + 8 * t) : make_uint2(0, 0);
-      w.a[2 * i] = va.x; w.a[2 * i + 1] = va.y;
-      w.b[2 * i] = vb.x; w.b[2 * i + 1] = vb.y;
-      w.da[i] = (okA && in) ? p.d[rA * nb + blk] : (uint16_t)0;
-      w.db[i] = (okB && in) ? p.d[rB * nb + blk] : (uint16_t)0;
+    for (int j = 0; j < 8; ++j) {
+      const bool in = j < nblk;
+      const uint2 va = in ? *reinterpret_cast<const uint2 *>(tile + (j * 64 + ra) * 32 + 8 * t)
+                          : make_uint2(0, 0);
+      const uint2 vb = in ? *reinterpret_cast<const uint2 *>(tile + (j * 64 + rb) * 32 + 8 * t)
+                          : make_uint2(0, 0);
+      w.a[2 * j] = va.x; w.a[2 * j + 1] = va.y;
+      w.b[2 * j] = vb.x; w.b[2 * j + 1] = vb.y;
+      const uint16_t *dd = reinterpret_cast<const uint16_t *>(tile + 64 * 256);
+      w.da[j] = in ? dd[ra * 8 + j] : (uint16_t)0;
+      w.db[j] = in ? dd[rb * 8 + j] : (uint16_t)0;
     }
   }
 }
 
-// x items of one chunk held in registers between prefetch and staging.
-template <int WARPS, int NT>
-struct XRegs {
-  static constexpr int kItems = (256 * NT) / (32 * WARPS);
-  float4 v[kItems];
-};
-
-template <int WARPS, int NT>
-__device__ __forceinline__ void load_x(const MvArgs &p, XRegs<WARPS, NT> &xr, int c) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int k = 0; k < XRegs<WARPS, NT>::kItems; ++k) {
-    const int it = tid + k * 32 * WARPS;
-    const int b = it >> 6, g = (it >> 2) & 15, t = it & 3;
-    const int64_t k0 = int64_t(c) * kChunk + 16 * g + 4 * t;
-    if (b < p.B && k0 < p.K)
-      xr.v[k] = __ldg(reinterpret_cast<const float4 *>(p.x + int64_t(b) * p.K + k0));
-    else
-      xr.v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-// Split the chunk's x into f16 hi/lo fragments (see the file header).
-template <int TYPE, int WARPS, int NT>
-__device__ __forceinline__ void stage_x(Smem<WARPS, NT> &sm, const XRegs<WARPS, NT> &xr) {
+// Split the staged x chunk (shared memory, raw f32) into f16 hi/lo fragments
+// (see the file header).  Called by the 128 compute threads together.
+template <int TYPE, int NT>
+__device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, int s, int B, int cw) {
   const int tid = threadIdx.x, lane = tid & 31;
-  constexpr int kItems = XRegs<WARPS, NT>::kItems;
+  constexpr int kItems = (256 * NT) / 128;
+  float4 xv[kItems];
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
-    const float4 v = xr.v[k];
+    const int it = tid + k * 128;
+    const int b = it >> 6, g = (it >> 2) & 15, t = it & 3;
+    xv[k] = (b < B && 16 * g < cw) ? *reinterpret_cast<const float4 *>(&sm.x[s][b][16 * g + 4 * t])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 v = xv[k];
     float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if (lane == 0) sm.wmax[(tid + k * 32 * WARPS) >> 5] = mb;
+    if (lane == 0) sm.wmax[it >> 5] = mb;
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
-    const int it = tid + k * 32 * WARPS;
+    const int it = tid + k * 128;
     const int b = it >> 6, g = (it >> 2) & 15, t = it & 3;
     const unsigned mb = max(sm.wmax[2 * b], sm.wmax[2 * b + 1]);
     const int E = (int)((mb >> 23) & 255);
     int e = mb == 0 ? 0 : 141 - max(E, 1);
     e = min(max(e, -100), 126);
-    const float s = __int_as_float((e + 127) << 23);
-    const float4 v = xr.v[k];
-    const float v0 = v.x * s, v1 = v.y * s, v2 = v.z * s, v3 = v.w * s;
+    const float sc = __int_as_float((e + 127) << 23);
+    const float4 v = xv[k];
+    const float v0 = v.x * sc, v1 = v.y * sc, v2 = v.z * sc, v3 = v.w * sc;
     const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1), h2 = __float2half_rn(v2),
                  h3 = __float2half_rn(v3);
     const uint32_t hi01 = pack_f16x2(__half2float(h0), __half2float(h1));
@@ -243,41 +286,78 @@ __device__ __forceinline__ void stage_x(Smem<WARPS, NT> &sm, const XRegs<WARPS, 
     }
     if ((it & 63) == 0) sm.unscale[b] = __int_as_float((127 - e) << 23);
   }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-template <int TYPE, int WARPS, int NT>
-__global__ void __launch_bounds__(WARPS * 32) matvec_kernel(const MvArgs p) {
-  __shared__ __align__(16) Smem<WARPS, NT> sm;
+template <int TYPE, int NT>
+__global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  MvSmem<TYPE, NT> &sm = *reinterpret_cast<MvSmem<TYPE, NT> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int rank = blockIdx.x % p.S;
   const int64_t group = blockIdx.x / p.S;
-  const int64_t row0 = group * (16 * WARPS) + 16 * warp;
-  const int64_t rA = row0 + g, rB = row0 + g + 8;
-  const bool okA = rA < p.N, okB = rB < p.N;
   const int c_begin = (int)((int64_t)rank * p.nchunk / p.S);
   const int c_end = (int)((int64_t)(rank + 1) * p.nchunk / p.S);
+  const int nch = c_end - c_begin;
+
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.full[s])), "r"(1));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.empty[s])), "r"(4));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
   float tot[2][NT];
 #pragma unroll
   for (int i = 0; i < NT; ++i) tot[0][i] = tot[1][i] = 0.f;
+  const int ra = 16 * warp + g;  // tile row of fragment row g (the other is ra + 8)
+  const int64_t rA = group * 64 + ra, rB = rA + 8;
+  const bool okA = rA < p.N, okB = rB < p.N;
 
-  WRegs<TYPE> cur, nxt;
-  XRegs<WARPS, NT> xr;
-  if (c_begin < c_end) {
-    load_chunk<TYPE>(p, cur, rA, rB, okA, okB, c_begin, t);
-    load_x<WARPS, NT>(p, xr, c_begin);
-  }
-  float(*tab)[16] = sm.tab[warp];
-
-  for (int c = c_begin; c < c_end; ++c) {
-    __syncthreads();  // previous chunk's fragments fully consumed
-    stage_x<TYPE, WARPS, NT>(sm, xr);
-    __syncthreads();
-    if (c + 1 < c_end) {
-      load_chunk<TYPE>(p, nxt, rA, rB, okA, okB, c + 1, t);
-      load_x<WARPS, NT>(p, xr, c + 1);
+  if (warp == 4) {  // ---- producer: weight tiles and x chunks into the ring
+    if (lane == 0) {
+      for (int i = 0; i < nch; ++i) {
+        const int c = c_begin + i, s = i % kNS;
+        const int cw = chunk_width(p.K, c);
+        if (i >= kNS) mbar_wait(sa(&sm.empty[s]), ((i / kNS) - 1) & 1, p.status, 21);
+        const int64_t tile = group * p.nchunk + c;
+        uint32_t bytes = (uint32_t)(p.B * cw * 4);
+        if constexpr (TYPE == MQ_Q4_K) bytes += 64 * 144;
+        if constexpr (TYPE == MQ_Q6_K) bytes += 64 * 192 + 64 * 16 + 64 * 2;
+        if constexpr (TYPE == MQ_Q8_0) bytes += 64 * cw + 64 * 16;
+        const uint32_t bar = sa(&sm.full[s]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(bytes)
+                     : "memory");
+        uint8_t *w = sm.w[s];
+        if constexpr (TYPE == MQ_Q4_K) {
+          bulk_1d(sa(w), p.q + tile * 64 * 144, 64 * 144, bar);
+        } else if constexpr (TYPE == MQ_Q6_K) {
+          bulk_1d(sa(w), p.q + tile * 64 * 192, 64 * 192, bar);
+          bulk_1d(sa(w + 64 * 192), p.sc + tile * 64 * 16, 64 * 16, bar);
+          bulk_1d(sa(w + 64 * 192 + 64 * 16), p.d + tile * 64, 64 * 2, bar);
+        } else {
+          bulk_1d(sa(w), p.q + (group * p.K + int64_t(c) * kChunk) * 64, (uint32_t)(64 * cw), bar);
+          bulk_1d(sa(w + 64 * 256), p.d + tile * 64 * 8, 64 * 16, bar);
+        }
+        for (int b = 0; b < p.B; ++b)
+          bulk_1d(sa(sm.x[s][b]), p.x + int64_t(b) * p.K + int64_t(c) * kChunk,
+                  (uint32_t)(cw * 4), bar);
+      }
     }
+  } else {  // ---- compute warps
+    float(*tab)[16] = sm.tab[warp];
+    for (int i = 0; i < nch; ++i) {
+      const int c = c_begin + i, s = i % kNS;
+      const int cw = chunk_width(p.K, c);
+      mbar_wait(sa(&sm.full[s]), (i / kNS) & 1, p.status, 22);
+      stage_x<TYPE, NT>(sm, s, p.B, cw);
+      WRegs<TYPE> cur;
+      load_words<TYPE>(sm.w[s], cur, ra, t, cw / 32);
     float acc[2][NT];
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc[0][i] = acc[1][i] = 0.f;
@@ -427,30 +507,36 @@ __global__ void __launch_bounds__(WARPS * 32) matvec_kernel(const MvArgs p) {
       tot[0][i] = fmaf(us, acc[0][i], tot[0][i]);
       tot[1][i] = fmaf(us, acc[1][i], tot[1][i]);
     }
-    if (c + 1 < c_end) cur = nxt;
-    __syncwarp();
+      __syncwarp();
+      if (lane == 0)  // this warp is done with stage s
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[s])) : "memory");
+    }
   }
 
   if (p.S == 1) {
+    if (warp < 4) {
 #pragma unroll
-    for (int i = 0; i < NT; ++i) {
-      const int b = t + 4 * i;
-      if (b < p.B) {
-        if (okA) p.y[int64_t(b) * p.N + rA] = tot[0][i];
-        if (okB) p.y[int64_t(b) * p.N + rB] = tot[1][i];
+      for (int i = 0; i < NT; ++i) {
+        const int b = t + 4 * i;
+        if (b < p.B) {
+          if (okA) p.y[int64_t(b) * p.N + rA] = tot[0][i];
+          if (okB) p.y[int64_t(b) * p.N + rB] = tot[1][i];
+        }
       }
     }
     return;
   }
   // split-K over the cluster: rank 0 sums the ranks' partials in rank order
+  if (warp < 4) {
 #pragma unroll
-  for (int i = 0; i < NT; ++i) {
-    sm.part[16 * warp + g][t + 4 * i] = tot[0][i];
-    sm.part[16 * warp + g + 8][t + 4 * i] = tot[1][i];
+    for (int i = 0; i < NT; ++i) {
+      sm.part[16 * warp + g][t + 4 * i] = tot[0][i];
+      sm.part[16 * warp + g + 8][t + 4 * i] = tot[1][i];
+    }
   }
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  if (rank == 0) {
+  if (rank == 0 && warp < 4) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const int b = t + 4 * i;
@@ -469,13 +555,18 @@ __global__ void __launch_bounds__(WARPS * 32) matvec_kernel(const MvArgs p) {
   cluster.sync();
 }
 
-template <int TYPE, int WARPS, int NT>
+template <int TYPE, int NT>
+constexpr size_t mv_smem_bytes() {
+  return sizeof(MvSmem<TYPE, NT>) + 128;
+}
+
+template <int TYPE, int NT>
 mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
-  const int64_t groups = (a.N + 16 * WARPS - 1) / (16 * WARPS);
+  const int64_t groups = (a.N + 63) / 64;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(groups * a.S), 1, 1);
-  cfg.blockDim = dim3(WARPS * 32, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = mv_smem_bytes<TYPE, NT>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -484,14 +575,39 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.S > 1 ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, WARPS, NT>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, NT>, a);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u, cluster %d) failed: %s", name,
                 cfg.gridDim.x, a.S, cudaGetErrorName(e));
   return MQ_OK;
 }
 
+template <int TYPE, int NT>
+mq_status optin_mv(const DeviceState *st, const char *name) {
+  const size_t smem = mv_smem_bytes<TYPE, NT>();
+  if ((int)smem > st->smem_optin)
+    return fail(MQ_ERR_LAUNCH, "%s needs %zu bytes of shared memory; the device allows %d", name,
+                smem, st->smem_optin);
+  cudaError_t e = cudaFuncSetAttribute(matvec_kernel<TYPE, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess)
+    return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
+                cudaGetErrorName(e));
+  return MQ_OK;
+}
+
 }  // namespace
+
+mq_status init_matvec(DeviceState *st) {
+  mq_status s;
+  if ((s = optin_mv<MQ_Q8_0, 1>(st, "matvec_kernel<Q8_0,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q8_0, 2>(st, "matvec_kernel<Q8_0,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_K, 1>(st, "matvec_kernel<Q4_K,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_K, 2>(st, "matvec_kernel<Q4_K,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q6_K, 1>(st, "matvec_kernel<Q6_K,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q6_K, 2>(st, "matvec_kernel<Q6_K,NT=2>")) != MQ_OK) return s;
+  return MQ_OK;
+}
 
 // K-split heuristic: enough CTAs for two per SM.  Depends only on (N, K, type),
 // never on B, so batched columns reproduce the B = 1 result bitwise.
@@ -506,7 +622,6 @@ static int choose_split(int64_t N, int64_t K, int sms, int rows_per_cta) {
 
 mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
                         const DeviceState *st) {
-  constexpr int kWarps = 4;
   MvArgs a;
   a.q = W->q;
   a.sc = W->sc;
@@ -517,18 +632,19 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.K = W->K;
   a.B = B;
   a.nchunk = (int)((W->K + kChunk - 1) / kChunk);
-  a.S = choose_split(W->N, W->K, st->sms, 16 * kWarps);
+  a.S = choose_split(W->N, W->K, st->sms, 64);
+  a.status = st->status;
   const bool two = B > 4;
   switch (W->type) {
     case MQ_Q4_K:
-      return two ? launch_one<MQ_Q4_K, kWarps, 2>(a, s, "matvec_kernel<Q4_K,NT=2>")
-                 : launch_one<MQ_Q4_K, kWarps, 1>(a, s, "matvec_kernel<Q4_K,NT=1>");
+      return two ? launch_one<MQ_Q4_K, 2>(a, s, "matvec_kernel<Q4_K,NT=2>")
+                 : launch_one<MQ_Q4_K, 1>(a, s, "matvec_kernel<Q4_K,NT=1>");
     case MQ_Q6_K:
-      return two ? launch_one<MQ_Q6_K, kWarps, 2>(a, s, "matvec_kernel<Q6_K,NT=2>")
-                 : launch_one<MQ_Q6_K, kWarps, 1>(a, s, "matvec_kernel<Q6_K,NT=1>");
+      return two ? launch_one<MQ_Q6_K, 2>(a, s, "matvec_kernel<Q6_K,NT=2>")
+                 : launch_one<MQ_Q6_K, 1>(a, s, "matvec_kernel<Q6_K,NT=1>");
     default:
-      return two ? launch_one<MQ_Q8_0, kWarps, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
-                 : launch_one<MQ_Q8_0, kWarps, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");
+      return two ? launch_one<MQ_Q8_0, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
+                 : launch_one<MQ_Q8_0, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");
   }
 }
 

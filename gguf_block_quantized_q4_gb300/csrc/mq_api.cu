@@ -105,6 +105,7 @@ extern "C" mq_status mq_init(int device) {
   CK(cudaMemset(st->status, 0, 64), site);
   CK(cudaStreamCreateWithFlags(&st->reg_stream, cudaStreamNonBlocking), site);
   mq_status s = init_kernels(st);
+  if (s == MQ_OK) s = init_matvec(st);
   if (s != MQ_OK) return s;
   CK(cudaDeviceSynchronize(), site);
   st->ready = true;
@@ -191,20 +192,24 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
     delete w;
     return r;
   };
+  // decode planes: padded to whole 64-row groups, padding rows zero
+  w->ngroup = (N + kRowGroup - 1) / kRowGroup;
+  w->nchunk = (int)((K + kChunk - 1) / kChunk);
+  const size_t npad = size_t(w->ngroup) * kRowGroup;
+  auto zalloc = [&](auto **pp, size_t bytes, const char *what) {
+    mq_status r = alloc_plane(pp, bytes, &total, what);
+    if (r == MQ_OK) cudaMemsetAsync(*pp, 0, bytes, st->reg_stream);
+    return r;
+  };
   if (type == MQ_Q8_0) {
-    if ((s = alloc_plane(&w->q, size_t(N) * K, &total, "q8_0 qs")) != MQ_OK) return cleanup(s);
-    if ((s = alloc_plane(&w->d, size_t(N) * (K / 32) * 2, &total, "q8_0 d")) != MQ_OK)
-      return cleanup(s);
+    if ((s = zalloc(&w->q, npad * K, "q8_0 qs")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q8_0 d")) != MQ_OK) return cleanup(s);
   } else if (type == MQ_Q4_K) {
-    if ((s = alloc_plane(&w->q, size_t(N) * nsb * 144, &total, "q4_K")) != MQ_OK)
-      return cleanup(s);
+    if ((s = zalloc(&w->q, npad * nsb * 144, "q4_K")) != MQ_OK) return cleanup(s);
   } else {
-    if ((s = alloc_plane(&w->q, size_t(N) * nsb * 192, &total, "q6_K quants")) != MQ_OK)
-      return cleanup(s);
-    if ((s = alloc_plane(&w->sc, size_t(N) * nsb * 16, &total, "q6_K scales")) != MQ_OK)
-      return cleanup(s);
-    if ((s = alloc_plane(&w->d, size_t(N) * nsb * 2, &total, "q6_K d")) != MQ_OK)
-      return cleanup(s);
+    if ((s = zalloc(&w->q, npad * nsb * 192, "q6_K quants")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->sc, npad * nsb * 16, "q6_K scales")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->d, npad * nsb * 2, "q6_K d")) != MQ_OK) return cleanup(s);
   }
   const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE);
   if (mmq) {

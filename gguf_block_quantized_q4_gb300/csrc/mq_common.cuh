@@ -5,20 +5,22 @@
 // device memory for speed).  All planes are lossless regroupings of the GGUF
 // bytes except the prefill operand planes, which hold exact integer values.
 //
-// Decode planes (read by the matvec; every 16-byte word a fragment thread reads
-// is contiguous and 16-byte aligned):
-//   Q8_0  qs   int8 [N][K]      each 32-element block regrouped: stored byte
-//                                8t + 4u + i  <-  block byte 16u + 4t + i
-//                                (t = fragment thread 0..3, u = 16-element half)
-//         d    u16  [N][K/32]   the f16 block scales
-//   Q4_K  q    [N][K/256][144]  bytes 0..15 the GGUF header (d, dmin, 12 scale
-//                                bytes); byte 16 + 32t + 4(2c+u) + i  <-  qs byte
-//                                32c + 16u + 4t + i
-//   Q6_K  q    [N][K/256][192]  byte 48t + 4(3(2h+v) + w) + i  <-  word w of
-//                                (h, v): w=0 ql[64h + 16v + 4t + i],
-//                                w=1 ql[64h + 32 + 16v + 4t + i], w=2 qh[32h + 16v + 4t + i]
-//         sc   int8 [N][K/256][16] the sub-scales
-//         d    u16  [N][K/256]  the f16 super-block scales
+// Decode planes (read by the matvec).  Rows are grouped by 64 (N padded with
+// zero rows to a multiple of 64) and K is cut into 256-element chunks; the tile
+// of one (row group g, chunk c) is contiguous, so one bulk copy moves it into
+// shared memory.  Inside a row, each fragment thread's words are contiguous and
+// 16-byte aligned (t = fragment thread 0..3, r = row in the group):
+//   Q4_K  q   tile (g,c) at ((g*nchunk + c)*64 + r)*144: bytes 0..15 the GGUF
+//             header (d, dmin, 12 scale bytes); byte 16 + 32t + 4(2c'+u) + i  <-
+//             qs byte 32c' + 16u + 4t + i
+//   Q6_K  q   at ((g*nchunk + c)*64 + r)*192: byte 48t + 4(3(2h+v) + w) + i  <-
+//             word w of (h, v): w=0 ql[64h + 16v + 4t + i],
+//             w=1 ql[64h + 32 + 16v + 4t + i], w=2 qh[32h + 16v + 4t + i]
+//         sc  int8 at ((g*nchunk + c)*64 + r)*16: the 16 sub-scales
+//         d   u16 at (g*nchunk + c)*64 + r: the f16 super-block scale
+//   Q8_0  qs  tile (g,c) at (g*K + 256c)*64 bytes, [block j][row r][32 bytes]:
+//             stored byte 8t + 4u + i  <-  block byte 16u + 4t + i (u = 16-element half)
+//         d   u16 at ((g*nchunk + c)*64 + r)*8 + j (8 slots per chunk; unused ones 0)
 // Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them), K-major for TMA:
 //   w      f16  [N][K]    integer weight W_int: Q8_0 q; Q4_K sc_j*nib (<= 945);
 //                         Q6_K the even part 2*floor(v/2) of v = sc*(q-32) (|v| <= 4096)
@@ -40,6 +42,8 @@ struct mq_weight {
   int type;
   int64_t N, K;
   int64_t np;            // N rounded up to 128: row stride of the transposed planes
+  int64_t ngroup;        // decode-plane row groups (N rounded up to 64, / 64)
+  int nchunk;            // decode-plane K chunks (K / 256 rounded up)
   int device;
   size_t payload;        // GGUF bytes
   size_t device_bytes;   // all planes
@@ -59,6 +63,8 @@ struct mq_weight {
 namespace mq {
 
 constexpr int kMaxB = 8;
+constexpr int kRowGroup = 64;  // decode-plane row group
+constexpr int kChunk = 256;    // decode-plane K chunk
 constexpr int kStatusTimeout = 1;
 
 // ---- per-thread error reporting ------------------------------------------
@@ -85,7 +91,8 @@ mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaSt
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
                      cudaStream_t s, const DeviceState *st, int debug_expire);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
-mq_status init_kernels(DeviceState *st);  // smem opt-ins
+mq_status init_kernels(DeviceState *st);  // smem opt-ins of the MMQ kernels
+mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 
 // xq buffer layout (mq_act_bytes): q int8 [M][K], s f32 [M][K/32], S int32
 // [M][K/32], q as f16 [M][K], then the transposed block scales sT f32

@@ -38,17 +38,31 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *s, int j, int &sc, 
 }
 
 // One thread per GGUF block.
+// Byte offset of block b of row n in the Q8_0 decode plane, and index of its d.
+__device__ __forceinline__ int64_t q8_0_off(int64_t n, int64_t b, int64_t K) {
+  const int64_t g = n / kRowGroup, r = n % kRowGroup, c = b / 8, j = b % 8;
+  return (g * K + int64_t(kChunk) * c) * kRowGroup + (j * kRowGroup + r) * 32;
+}
+__device__ __forceinline__ int64_t q8_0_doff(int64_t n, int64_t b, int nchunk) {
+  const int64_t g = n / kRowGroup, r = n % kRowGroup, c = b / 8, j = b % 8;
+  return ((g * nchunk + c) * kRowGroup + r) * 8 + j;
+}
+__device__ __forceinline__ int64_t tile_row(int64_t n, int64_t c, int nchunk) {
+  return (n / kRowGroup * nchunk + c) * kRowGroup + n % kRowGroup;
+}
+
 __global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
                             uint8_t *__restrict__ q, uint16_t *__restrict__ d,
                             __half *__restrict__ mw, float *__restrict__ td) {
   const int64_t nb = K / 32;
+  const int nchunk = (int)((K + kChunk - 1) / kChunk);
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nb) return;
   const int64_t n = i / nb, b = i % nb;
   const uint8_t *src = raw + i * 34;
   const uint16_t dbits = rd16(src);
-  d[i] = dbits;
-  uint8_t *dst = q + n * K + b * 32;
+  d[q8_0_doff(n, b, nchunk)] = dbits;
+  uint8_t *dst = q + q8_0_off(n, b, K);
   for (int t = 0; t < 4; ++t)
     for (int u = 0; u < 2; ++u)
       for (int e = 0; e < 4; ++e) dst[8 * t + 4 * u + e] = src[2 + 16 * u + 4 * t + e];
@@ -61,13 +75,15 @@ __global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t 
 __global__ void unpack_q8_0(const uint8_t *__restrict__ q, const uint16_t *__restrict__ d,
                             int64_t N, int64_t K, uint8_t *__restrict__ raw) {
   const int64_t nb = K / 32;
+  const int nchunk = (int)((K + kChunk - 1) / kChunk);
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nb) return;
   const int64_t n = i / nb, b = i % nb;
   uint8_t *dst = raw + i * 34;
-  dst[0] = d[i] & 255;
-  dst[1] = d[i] >> 8;
-  const uint8_t *src = q + n * K + b * 32;
+  const uint16_t dv = d[q8_0_doff(n, b, nchunk)];
+  dst[0] = dv & 255;
+  dst[1] = dv >> 8;
+  const uint8_t *src = q + q8_0_off(n, b, K);
   for (int t = 0; t < 4; ++t)
     for (int u = 0; u < 2; ++u)
       for (int e = 0; e < 4; ++e) dst[2 + 16 * u + 4 * t + e] = src[8 * t + 4 * u + e];
@@ -81,7 +97,7 @@ __global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
   const uint8_t *src = raw + i * 144;
-  uint8_t *dst = q + i * 144;
+  uint8_t *dst = q + tile_row(i / nsb, i % nsb, (int)nsb) * 144;
   for (int e = 0; e < 16; ++e) dst[e] = src[e];
   for (int t = 0; t < 4; ++t)
     for (int c = 0; c < 4; ++c)
@@ -110,7 +126,7 @@ __global__ void unpack_q4_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
-  const uint8_t *src = q + i * 144;
+  const uint8_t *src = q + tile_row(i / nsb, i % nsb, (int)nsb) * 144;
   uint8_t *dst = raw + i * 144;
   for (int e = 0; e < 16; ++e) dst[e] = src[e];
   for (int t = 0; t < 4; ++t)
@@ -135,16 +151,17 @@ __global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
   const uint8_t *src = raw + i * 210;
-  uint8_t *dst = q + i * 192;
+  const int64_t tr = tile_row(i / nsb, i % nsb, (int)nsb);
+  uint8_t *dst = q + tr * 192;
   for (int t = 0; t < 4; ++t)
     for (int h = 0; h < 2; ++h)
       for (int v = 0; v < 2; ++v)
         for (int w = 0; w < 3; ++w)
           for (int e = 0; e < 4; ++e)
             dst[48 * t + 4 * (3 * (2 * h + v) + w) + e] = src[q6k_src(t, h, v, w) + e];
-  for (int e = 0; e < 16; ++e) sc[i * 16 + e] = (int8_t)src[192 + e];
+  for (int e = 0; e < 16; ++e) sc[tr * 16 + e] = (int8_t)src[192 + e];
   const uint16_t dbits = rd16(src + 208);
-  d[i] = dbits;
+  d[tr] = dbits;
   if (mw) {
     const int64_t n = i / nsb, s = i % nsb;
     const float dd = f16bits(dbits);
@@ -168,7 +185,8 @@ __global__ void unpack_q6_k(const uint8_t *__restrict__ q, const int8_t *__restr
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
-  const uint8_t *src = q + i * 192;
+  const int64_t tr = tile_row(i / nsb, i % nsb, (int)nsb);
+  const uint8_t *src = q + tr * 192;
   uint8_t *dst = raw + i * 210;
   for (int t = 0; t < 4; ++t)
     for (int h = 0; h < 2; ++h)
@@ -176,9 +194,9 @@ __global__ void unpack_q6_k(const uint8_t *__restrict__ q, const int8_t *__restr
         for (int w = 0; w < 3; ++w)
           for (int e = 0; e < 4; ++e)
             dst[q6k_src(t, h, v, w) + e] = src[48 * t + 4 * (3 * (2 * h + v) + w) + e];
-  for (int e = 0; e < 16; ++e) dst[192 + e] = (uint8_t)sc[i * 16 + e];
-  dst[208] = d[i] & 255;
-  dst[209] = d[i] >> 8;
+  for (int e = 0; e < 16; ++e) dst[192 + e] = (uint8_t)sc[tr * 16 + e];
+  dst[208] = d[tr] & 255;
+  dst[209] = d[tr] >> 8;
 }
 
 inline unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
