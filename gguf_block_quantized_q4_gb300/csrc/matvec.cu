@@ -2,43 +2,53 @@
 // Q4_K / Q6_K weights and f32 activations, B <= 8 ("minfer CUDA Backend Design"
 // §4.4: the nt == 1 matvec and the _multi variants for nt 2..8).
 //
-// GB300 design.  The weights are streamed once from HBM with 16-byte loads
-// and dequantised in registers straight into tensor-core fragments; the dot
-// products run on the legacy warp-level tensor path (mma.sync m16n8k16, f16
-// inputs, f32 accumulate).  This keeps the CUDA-core work per weight element
-// to a few integer/f16x2 operations, independent of the batch size B:
+// GB300 design.  The weights are streamed once from HBM and dequantised in
+// registers straight into tensor-core fragments; the dot products run on the
+// warp-level tensor path (mma.sync m16n8k16, f16 inputs, f32 accumulate), so the
+// CUDA-core work per weight element is a fraction of an instruction and does
+// not grow with the batch size B:
 //
-//  * weight side (A operand, 16 rows x 16 K per MMA): the quants of one
-//    16-element scale group become exact f16 integers -- Q4_K nibbles through
-//    cvt.rn.f16x2.e4m3x2 (a byte n < 16 read as e4m3 is n * 2^-9 exactly),
-//    Q6_K and Q8_0 through a byte permute into an f16 whose exponent makes the
-//    low mantissa byte the integer, then one f16x2 subtraction.
+//  * weight side (A operand, 16 rows x 16 K per MMA): quants become exact f16
+//    integers.  Q4_K: a nibble masked into the mantissa of 1024 (bits 0-3) or
+//    1024/16-scaled (bits 4-7) is turned by one f16x2 fma into sc_j * nib, the
+//    6-bit sub-block scale folded in exactly (sc_j * nib <= 945), so a whole
+//    256-element super-block accumulates in the MMA and d is applied once.
+//    Q6_K and Q8_0: a byte permute into an f16 whose exponent makes the low
+//    mantissa byte the integer, then one f16x2 subtraction; the 16-element
+//    (Q6_K) or 32-element (Q8_0) scale is applied to the f32 MMA result.
+//  * Q4_K min term -dmin * sum_j m_j * sum(x over sub-block j): one more MMA per
+//    super-block whose A operand holds the eight 6-bit mins m_j and whose B
+//    operand holds the sub-block sums of x.
 //  * activation side (B operand, 16 K x 8 columns): x is staged per 256-element
-//    chunk in shared memory as two f16 parts per batch row, hi = f16(x*2^e) and
-//    lo = f16(x*2^e - hi), with 2^e a per-(row, chunk) power of two that puts
-//    max|x| in [2^14, 2^15).  hi + lo carries 22 significant bits, so the
-//    product error is ~2^-22 relative, far inside the 1e-4 * sum|w||x| bound.
-//    Columns 2b and 2b+1 of an n8 tile hold hi and lo of batch row b, so one
-//    thread's two accumulator columns are the two parts of the same row.
-//  * per scale group the f32 MMA result is scaled by the group's weight scale
-//    (and, for Q4_K, the min term -dmin*m_j*sum(x) is subtracted), then per
-//    chunk by 2^-e.
+//    chunk as two f16 parts per batch row, hi = f16(x*2^e) and lo =
+//    f16(x*2^e - hi), with 2^e a per-(row, chunk) power of two that puts max|x|
+//    in [2^14, 2^15).  hi + lo carries 22 significant bits, so the product error
+//    is ~2^-22 relative, far inside the 1e-4 * sum|w||x| bound.  Columns 2b and
+//    2b+1 of an n8 tile hold hi and lo of batch row b, so one thread's two
+//    accumulator columns are the two parts of the same row.
 //
 // The fragment rule: thread t (of a quad) holds the elements 4t..4t+3 of each
 // 16-element group; A register pairs are (4t, 4t+1) and (4t+2, 4t+3), matched
 // by B pairs (x[4t], x[4t+1]) and (x[4t+2], x[4t+3]).  The decode planes
 // (repack.cu) store each thread's words contiguously.
 //
-// Data movement: a CTA owns one 64-row group of the decode plane and a K-slice.
-// A producer warp streams, per 256-element chunk, the group's weight tile (one
-// contiguous run of the tiled decode plane) and the x chunk of every batch row
-// into a 4-stage shared-memory ring with 1-D bulk copies (cp.async.bulk,
-// mbarrier transaction counts); four compute warps, 16 rows each, read their
-// fragment words from shared memory.  When one wave would be short of CTAs, K
-// is split over a thread-block cluster of S CTAs whose partial sums are reduced
-// through distributed shared memory in rank order (deterministic, and
-// independent of B, so every column of a batched call equals the B = 1 call
-// bitwise).  All mbarrier waits are bounded.
+// Data movement and roles.  A CTA owns one 128-row group of the decode plane
+// and a K-slice, and runs 10 warps around a shared-memory ring of chunk stages:
+//  * the copy warp (one lane) streams, per 256-element chunk, the group's weight
+//    tile (one contiguous run of the tiled decode plane) and the x chunk of every
+//    batch row into the stage with 1-D bulk copies (cp.async.bulk, counted by the
+//    stage's transaction barrier);
+//  * the x warp turns the staged x chunk into B fragments (and the sub-block
+//    sums for Q4_K) in a second, smaller ring of fragment slots;
+//  * eight compute warps, 16 rows each, wait for a weight stage, decode their
+//    rows' scales into a warp-private table and copy their quant words into
+//    registers, release the weight stage at once (so the next chunk's copy is
+//    in flight during the MMAs), then wait for the fragment slot, run the MMAs
+//    and release the slot.  They never wait for one another.
+// When one wave would be short of CTAs, K is split over a thread-block cluster
+// of S CTAs whose partial sums are reduced through distributed shared memory in
+// rank order (deterministic, and independent of B, so every column of a batched
+// call equals the B = 1 call bitwise).  All mbarrier waits are bounded.
 #include <cooperative_groups.h>
 
 #include "mq_common.cuh"
@@ -48,13 +58,15 @@ namespace cg = cooperative_groups;
 namespace mq {
 namespace {
 
-constexpr int kNS = 4;          // shared-memory ring stages
-constexpr int kThreads = 160;   // 4 compute warps + 1 producer warp
+constexpr int kRows = kRowGroup;               // rows per CTA
+constexpr int kCompute = kRows / 16;           // compute warps, 16 rows each
+constexpr int kXWarp = kCompute;               // x-fragment warp
+constexpr int kCopyWarp = kCompute + 1;        // bulk-copy warp
+constexpr int kThreads = 32 * (kCompute + 2);
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct MvArgs {
   const uint8_t *q;
-  const int8_t *sc;
   const uint16_t *d;
   const float *x;
   float *y;
@@ -65,14 +77,54 @@ struct MvArgs {
   int *status;
 };
 
-// Bytes of one (64-row group, chunk) tile of the decode planes, as laid out in
-// shared memory: Q4_K 64 x 144; Q6_K 64 x 192 quants, then 64 x 16 sub-scales,
-// then 64 f16 d; Q8_0 64 x 256 quants (64 x chunk width used), then 64 x 8 f16 d.
+// Bytes of one (128-row group, chunk) tile of the decode plane.
 template <int TYPE>
-constexpr int tile_bytes() {
-  return TYPE == MQ_Q4_K ? 64 * 144 : (TYPE == MQ_Q6_K ? 64 * 192 + 64 * 16 + 64 * 2
-                                                       : 64 * 256 + 64 * 16);
+__host__ __device__ constexpr int tile_bytes() {
+  return kRows * (TYPE == MQ_Q4_K ? 144 : (TYPE == MQ_Q6_K ? 210 : 256 + 16));
 }
+// Weight-ring depth: two CTAs per SM must fit in shared memory.
+template <int TYPE, int NT>
+__host__ __device__ constexpr int ring_stages() {
+  return TYPE == MQ_Q4_K ? (NT == 1 ? 4 : 3) : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
+}
+constexpr int kFragSlots = 2;  // fragment-ring depth
+
+// Per-warp tables decoded from the tile headers of the warp's 16 rows.
+template <int TYPE>
+struct WarpTab;
+template <>
+struct WarpTab<MQ_Q4_K> {
+  uint4 sc[4][8][2];  // [pair c'][g][lo, hi sub-block]: f16x2 (mul A, add A, mul B, add B)
+  uint2 mf[8][4];     // [g][t]: min-term A fragment words of rows g, g+8
+  float4 dd[8];       // [g]: d_A, 32*dmin_A, d_B, 32*dmin_B
+};
+template <>
+struct WarpTab<MQ_Q6_K> {
+  float2 s[16][8];  // [16-element group][g]: d*sc of rows g, g+8
+};
+template <>
+struct WarpTab<MQ_Q8_0> {
+  float2 s[8][8];  // [32-element block][g]: d of rows g, g+8
+};
+
+template <int TYPE, int NT>
+struct MvSmem {
+  static constexpr int NS = ring_stages<TYPE, NT>();
+  static constexpr int FS = kFragSlots;
+  static constexpr int FG = TYPE == MQ_Q4_K ? 17 : 16;  // 16 groups (+ the Q4_K min group)
+  union {
+    alignas(128) uint8_t w[NS][tile_bytes<TYPE>()];  // weight tiles
+    float part[kRows][8];  // split-K partial sums (after the ring has drained)
+  };
+  alignas(128) float xr[NS][4 * NT][kChunk];  // staged x chunks of the batch rows
+  alignas(16) uint2 frag[FS][FG][NT][32];     // B fragments
+  float unscale[FS][8];                       // 2^-e per batch row of the slot's chunk
+  WarpTab<TYPE> tab[kCompute];
+  float xs[8];  // x-warp scratch: sub-block sums of one batch row
+  // weight stage: copied (wfull) / read into registers by all warps (wempty);
+  // fragment slot: written (ffull) / used by the compute warps (fempty)
+  uint64_t wfull[NS], wempty[NS], ffull[FS], fempty[FS];
+};
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -83,16 +135,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two bytes < 16 -> f16x2 (n0 * 2^-9, n1 * 2^-9), exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)v16));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
 
@@ -100,53 +155,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-
-__device__ __forceinline__ uint4 ldg16(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
 }
-
-__device__ __forceinline__ uint2 ldg8(const void *p) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
-
-// Per-thread weight words of one chunk for the two rows (g, g+8) of the tile.
-template <int TYPE>
-struct WRegs;
-template <>
-struct WRegs<MQ_Q4_K> {  // 8 quant words per row + the decoded row's header
-  uint32_t a[8], b[8];
-  uint4 hdr;
-};
-template <>
-struct WRegs<MQ_Q6_K> {  // 12 words per row
-  uint32_t a[12], b[12];
-  uint2 sc8;             // 8 sub-scales of the decoded row
-  uint16_t dbits;
-};
-template <>
-struct WRegs<MQ_Q8_0> {  // 2 words per row per block, 8 blocks
-  uint32_t a[16], b[16];
-  uint16_t da[8], db[8];
-};
-
-template <int TYPE, int NT>
-struct MvSmem {
-  alignas(128) uint8_t w[kNS][tile_bytes<TYPE>()];  // weight tiles
-  alignas(128) float x[kNS][4 * NT][kChunk];        // x chunks of the batch rows
-  uint2 frag[16][NT][32];      // B fragments of the staged chunk
-  float xsum[8][8];            // Q4_K: per sub-block, per batch row sum of scaled x
-  unsigned wmax[8 * NT];       // per 32-item slice max |x| bits
-  float unscale[8];            // 2^-e per batch row of the chunk
-  float tab[4][16][16];        // per-warp decoded scales of the tile's 16 rows
-  float part[64][8];           // split-K partial sums
-  uint64_t full[kNS], empty[kNS];
-};
 
 __device__ __forceinline__ int chunk_width(int64_t K, int c) {
   const int64_t left = K - int64_t(c) * kChunk;
@@ -184,6 +198,9 @@ __device__ __forceinline__ void mbar_wait(uint32_t a, uint32_t parity, int *stat
     }
   }
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
 __device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
                                         uint32_t bar) {
   asm volatile(
@@ -192,108 +209,362 @@ __device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t 
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-
-// The fragment words of one chunk for tile rows ra (g) and ra + 8, from the
-// shared-memory tile (nblk = blocks in the chunk, Q8_0 only).
-template <int TYPE>
-__device__ __forceinline__ void load_words(const uint8_t *tile, WRegs<TYPE> &w, int ra, int t,
-                                           int nblk) {
-  const int rb = ra + 8;
-  if constexpr (TYPE == MQ_Q4_K) {
-    const uint4 a0 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 16 + 32 * t);
-    const uint4 a1 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 32 + 32 * t);
-    const uint4 b0 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 16 + 32 * t);
-    const uint4 b1 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 32 + 32 * t);
-    w.a[0] = a0.x; w.a[1] = a0.y; w.a[2] = a0.z; w.a[3] = a0.w;
-    w.a[4] = a1.x; w.a[5] = a1.y; w.a[6] = a1.z; w.a[7] = a1.w;
-    w.b[0] = b0.x; w.b[1] = b0.y; w.b[2] = b0.z; w.b[3] = b0.w;
-    w.b[4] = b1.x; w.b[5] = b1.y; w.b[6] = b1.z; w.b[7] = b1.w;
-    w.hdr = *reinterpret_cast<const uint4 *>(tile + ((t & 1) ? rb : ra) * 144);
-  } else if constexpr (TYPE == MQ_Q6_K) {
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const uint4 va = *reinterpret_cast<const uint4 *>(tile + ra * 192 + 48 * t + 16 * i);
-      const uint4 vb = *reinterpret_cast<const uint4 *>(tile + rb * 192 + 48 * t + 16 * i);
-      w.a[4 * i] = va.x; w.a[4 * i + 1] = va.y; w.a[4 * i + 2] = va.z; w.a[4 * i + 3] = va.w;
-      w.b[4 * i] = vb.x; w.b[4 * i + 1] = vb.y; w.b[4 * i + 2] = vb.z; w.b[4 * i + 3] = vb.w;
+// ---------------------------------------------------------------------------
+// Copy warp (one lane): weight tile and x rows of each chunk into its stage.
+template <int TYPE, int NT>
+__device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs &p,
+                                             int64_t group, int c_begin, int nch) {
+  constexpr int NS = MvSmem<TYPE, NT>::NS;
+  for (int i = 0; i < nch; ++i) {
+    const int c = c_begin + i, s = i % NS;
+    const int cw = chunk_width(p.K, c);
+    if (i >= NS) mbar_wait(sa(&sm.wempty[s]), ((i / NS) - 1) & 1, p.status, 21);
+    const uint32_t bar = sa(&sm.wfull[s]);
+    const uint32_t wbytes =
+        TYPE == MQ_Q8_0 ? (uint32_t)(kRows * cw + kRows * 16) : (uint32_t)tile_bytes<TYPE>();
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(wbytes + (uint32_t)(p.B * cw * 4))
+                 : "memory");
+    uint8_t *w = sm.w[s];
+    if constexpr (TYPE == MQ_Q8_0) {
+      bulk_1d(sa(w), p.q + (group * p.K + int64_t(c) * kChunk) * kRows, (uint32_t)(kRows * cw),
+              bar);
+      bulk_1d(sa(w + kRows * 256), p.d + (group * p.nchunk + c) * kRows * 8, kRows * 16, bar);
+    } else {
+      bulk_1d(sa(w), p.q + (group * p.nchunk + c) * int64_t(tile_bytes<TYPE>()),
+              (uint32_t)tile_bytes<TYPE>(), bar);
     }
-    const int row = (t & 1) ? rb : ra;
-    w.sc8 = *reinterpret_cast<const uint2 *>(tile + 64 * 192 + row * 16 + 8 * (t >> 1));
-    w.dbits = *reinterpret_cast<const uint16_t *>(tile + 64 * 192 + 64 * 16 + row * 2);
-  } else {  // Q8_0: [block j][row][32 bytes], then d [row][8]
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = j < nblk;
-      const uint2 va = in ? *reinterpret_cast<const uint2 *>(tile + (j * 64 + ra) * 32 + 8 * t)
-                          : make_uint2(0, 0);
-      const uint2 vb = in ? *reinterpret_cast<const uint2 *>(tile + (j * 64 + rb) * 32 + 8 * t)
-                          : make_uint2(0, 0);
-      w.a[2 * j] = va.x; w.a[2 * j + 1] = va.y;
-      w.b[2 * j] = vb.x; w.b[2 * j + 1] = vb.y;
-      const uint16_t *dd = reinterpret_cast<const uint16_t *>(tile + 64 * 256);
-      w.da[j] = in ? dd[ra * 8 + j] : (uint16_t)0;
-      w.db[j] = in ? dd[rb * 8 + j] : (uint16_t)0;
-    }
+    for (int b = 0; b < p.B; ++b)
+      bulk_1d(sa(sm.xr[s][b]), p.x + int64_t(b) * p.K + int64_t(c) * kChunk, (uint32_t)(cw * 4),
+              bar);
   }
 }
 
-// Split the staged x chunk (shared memory, raw f32) into f16 hi/lo fragments
-// (see the file header).  Called by the 128 compute threads together.
+// x warp: staged x chunk -> hi/lo B fragments (+ Q4_K sub-block sums).
 template <int TYPE, int NT>
-__device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, int s, int B, int cw) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  constexpr int kItems = (256 * NT) / 128;
-  float4 xv[kItems];
+__device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, int c_begin,
+                                        int nch, int lane) {
+  constexpr int NS = MvSmem<TYPE, NT>::NS, FS = MvSmem<TYPE, NT>::FS;
+  for (int i = 0; i < nch; ++i) {
+    const int c = c_begin + i, s = i % NS, fs = i % FS;
+    const int cw = chunk_width(p.K, c);
+    mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 23);
+    if (i >= FS) mbar_wait(sa(&sm.fempty[fs]), ((i / FS) - 1) & 1, p.status, 25);
+    // lane handles float4 items f = lane and lane + 32 of each batch row
+    for (int b = 0; b < p.B; ++b) {
+      float4 v[2];
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const int it = tid + k * 128;
-    const int b = it >> 6, g = (it >> 2) & 15, t = it & 3;
-    xv[k] = (b < B && 16 * g < cw) ? *reinterpret_cast<const float4 *>(&sm.x[s][b][16 * g + 4 * t])
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 v = xv[k];
-    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if (lane == 0) sm.wmax[it >> 5] = mb;
-  }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int k = 0; k < 2; ++k) {
+        const int f = lane + 32 * k;
+        v[k] = 4 * f < cw ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float m = 0.f;
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const int it = tid + k * 128;
-    const int b = it >> 6, g = (it >> 2) & 15, t = it & 3;
-    const unsigned mb = max(sm.wmax[2 * b], sm.wmax[2 * b + 1]);
-    const int E = (int)((mb >> 23) & 255);
-    int e = mb == 0 ? 0 : 141 - max(E, 1);
-    e = min(max(e, -100), 126);
-    const float sc = __int_as_float((e + 127) << 23);
-    const float4 v = xv[k];
-    const float v0 = v.x * sc, v1 = v.y * sc, v2 = v.z * sc, v3 = v.w * sc;
-    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1), h2 = __float2half_rn(v2),
-                 h3 = __float2half_rn(v3);
-    const uint32_t hi01 = pack_f16x2(__half2float(h0), __half2float(h1));
-    const uint32_t hi23 = pack_f16x2(__half2float(h2), __half2float(h3));
-    const uint32_t lo01 = pack_f16x2(v0 - __half2float(h0), v1 - __half2float(h1));
-    const uint32_t lo23 = pack_f16x2(v2 - __half2float(h2), v3 - __half2float(h3));
-    const int col = 2 * (b & 3);
-    sm.frag[g][b >> 2][col * 4 + t] = make_uint2(hi01, hi23);
-    sm.frag[g][b >> 2][(col + 1) * 4 + t] = make_uint2(lo01, lo23);
-    if constexpr (TYPE == MQ_Q4_K) {
-      // sum over the 8 consecutive items (32 elements) of sub-block g/2
-      float ps = (v0 + v1) + (v2 + v3);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-      if ((it & 7) == 0) sm.xsum[g >> 1][b] = ps;
+      for (int k = 0; k < 2; ++k)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+      const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      const int E = (int)((mb >> 23) & 255);
+      int e = mb == 0 ? 0 : 141 - max(E, 1);
+      e = min(max(e, -100), 126);
+      const float scale = __int_as_float((e + 127) << 23);
+      if (lane == 0) sm.unscale[fs][b] = __int_as_float((127 - e) << 23);
+      const int col = 2 * (b & 3);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int f = lane + 32 * k, g16 = f >> 2, t = f & 3;
+        const float v0 = v[k].x * scale, v1 = v[k].y * scale, v2 = v[k].z * scale,
+                    v3 = v[k].w * scale;
+        const uint32_t hi01 = pack_f16x2(v0, v1), hi23 = pack_f16x2(v2, v3);
+        const uint32_t lo01 = pack_f16x2(v0 - f16_lo(hi01), v1 - f16_hi(hi01));
+        const uint32_t lo23 = pack_f16x2(v2 - f16_lo(hi23), v3 - f16_hi(hi23));
+        sm.frag[fs][g16][b >> 2][col * 4 + t] = make_uint2(hi01, hi23);
+        sm.frag[fs][g16][b >> 2][(col + 1) * 4 + t] = make_uint2(lo01, lo23);
+        if constexpr (TYPE == MQ_Q4_K) {
+          // sum of sub-block j = f >> 3 (8 consecutive items), scaled by 1/32 so
+          // that |sum| < 2^15 fits f16
+          float ps = (v0 + v1) + (v2 + v3);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+          if ((lane & 7) == 0) sm.xs[f >> 3] = ps * 0.03125f;
+        }
+      }
+      if constexpr (TYPE == MQ_Q4_K) {
+        // min-term B fragment: lane (col', t') holds sums 2t', 2t'+1 (hi or lo part)
+        __syncwarp();
+        if (lane < 8) {
+          const int part = lane >> 2, t = lane & 3;
+          const float s0 = sm.xs[2 * t], s1 = sm.xs[2 * t + 1];
+          const uint32_t h = pack_f16x2(s0, s1);
+          const uint32_t word = part == 0 ? h : pack_f16x2(s0 - f16_lo(h), s1 - f16_hi(h));
+          sm.frag[fs][16][b >> 2][(col + part) * 4 + t] = make_uint2(word, 0u);
+        }
+        __syncwarp();
+      }
     }
-    if ((it & 63) == 0) sm.unscale[b] = __int_as_float((127 - e) << 23);
+    mbar_arrive(sa(&sm.ffull[fs]));  // each lane, after its own fragment stores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
   }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Compute warps.  After a warp has read its scales and quant words out of a
+// weight stage it releases the stage, then waits for the fragment slot.
+__device__ __forceinline__ void release_and_wait(uint64_t &wempty, uint64_t &ffull,
+                                                 uint32_t fpar, int lane, int *status) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sa(&wempty));
+  mbar_wait(sa(&ffull), fpar, status, 24);
+}
+
+// ---------------------------------------------------------------------------
+// Compute warps.  Thread (g, t) of warp w covers tile rows ra = 16w + g and
+// rb = ra + 8; tot[0/1][i] accumulates rows ra/rb for batch row 4i + t.
+template <int NT>
+__device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s, int fs,
+                                                  uint32_t fpar, int warp, int lane, int *status,
+                                                  float (&tot)[2][NT]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t *tile = sm.w[s];
+  WarpTab<MQ_Q4_K> &tb = sm.tab[warp];
+  {  // decode the 16 rows' scales: lane (r, h) takes sub-blocks 4h..4h+3 of row r
+    const int r = lane & 15, h = lane >> 4;
+    const uint4 hd = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r) * 144);
+    uint32_t scw, mnw;
+    if (h == 0) {
+      scw = hd.y & 0x3f3f3f3fu;
+      mnw = hd.z & 0x3f3f3f3fu;
+    } else {
+      scw = (hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u);
+      mnw = ((hd.w >> 4) & 0x0f0f0f0fu) | ((hd.z >> 2) & 0x30303030u);
+    }
+    // bytes -> f16x2 integers (1024 + v) - 1024
+    const uint32_t k1024 = 0x64006400u;
+    const uint32_t s01 = hsub2(__byte_perm(scw, 0x64646464u, 0x5140), k1024);
+    const uint32_t s23 = hsub2(__byte_perm(scw, 0x64646464u, 0x5342), k1024);
+    const uint32_t m01 = hsub2(__byte_perm(mnw, 0x64646464u, 0x5140), k1024);
+    const uint32_t m23 = hsub2(__byte_perm(mnw, 0x64646464u, 0x5342), k1024);
+    const int gg = r & 7, ab = r >> 3;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {  // pair c' = 2h + q: sub-blocks 4h+2q (lo), 4h+2q+1 (hi)
+      const uint32_t sp = q ? s23 : s01;
+      const uint32_t slo = __byte_perm(sp, sp, 0x1010), shi = __byte_perm(sp, sp, 0x3232);
+      // lo nibble n read as 1024 + n:   (1024 + n) * sc - 1024 sc
+      // hi nibble n read as 1024 + 16n: (1024 + 16n) * sc/16 - 64 sc
+      reinterpret_cast<uint2 *>(&tb.sc[2 * h + q][gg][0])[ab] =
+          make_uint2(slo, hmul2(slo, 0xE400E400u));
+      reinterpret_cast<uint2 *>(&tb.sc[2 * h + q][gg][1])[ab] =
+          make_uint2(hmul2(shi, 0x2C002C00u), hmul2(shi, 0xD400D400u));
+    }
+    reinterpret_cast<uint32_t *>(&tb.mf[gg][2 * h])[ab] = m01;
+    reinterpret_cast<uint32_t *>(&tb.mf[gg][2 * h + 1])[ab] = m23;
+    const float dv = h == 0 ? f16_lo(hd.x) : 32.f * f16_hi(hd.x);
+    reinterpret_cast<float *>(&tb.dd[gg])[2 * ab + h] = dv;
+  }
+  __syncwarp();
+  const int ra = 16 * warp + g, rb = ra + 8;
+  const uint4 a0 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 16 + 32 * t);
+  const uint4 a1 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 32 + 32 * t);
+  const uint4 b0 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 16 + 32 * t);
+  const uint4 b1 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 32 + 32 * t);
+  const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
+  float acc[2][NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[0][i][r] = acc[1][i][r] = 0.f;
+  constexpr uint32_t kMagic = 0x64006400u;
+#pragma unroll
+  for (int cp = 0; cp < 4; ++cp) {
+    const uint4 slo = tb.sc[cp][g][0], shi = tb.sc[cp][g][1];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t xa = wa[2 * cp + u], xb = wb[2 * cp + u];
+      const uint32_t xa8 = xa >> 8, xb8 = xb >> 8;
+      const uint32_t l0 = hfma2((xa & 0x000f000fu) | kMagic, slo.x, slo.y);
+      const uint32_t l1 = hfma2((xb & 0x000f000fu) | kMagic, slo.z, slo.w);
+      const uint32_t l2 = hfma2((xa8 & 0x000f000fu) | kMagic, slo.x, slo.y);
+      const uint32_t l3 = hfma2((xb8 & 0x000f000fu) | kMagic, slo.z, slo.w);
+      const uint32_t h0 = hfma2((xa & 0x00f000f0u) | kMagic, shi.x, shi.y);
+      const uint32_t h1 = hfma2((xb & 0x00f000f0u) | kMagic, shi.z, shi.w);
+      const uint32_t h2 = hfma2((xa8 & 0x00f000f0u) | kMagic, shi.x, shi.y);
+      const uint32_t h3 = hfma2((xb8 & 0x00f000f0u) | kMagic, shi.z, shi.w);
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const uint2 bl = sm.frag[fs][4 * cp + u][i][lane];      // sub-block 2c', K half u
+        const uint2 bh = sm.frag[fs][4 * cp + 2 + u][i][lane];  // sub-block 2c'+1
+        mma16816(acc[0][i], l0, l1, l2, l3, bl.x, bl.y);
+        mma16816(acc[1][i], h0, h1, h2, h3, bh.x, bh.y);
+      }
+    }
+  }
+  const uint2 mf = tb.mf[g][t];
+  const float4 dd = tb.dd[g];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const uint2 bm = sm.frag[fs][16][i][lane];
+    float cm[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16816(cm, mf.x, mf.y, 0u, 0u, bm.x, bm.y);
+    const float us = sm.unscale[fs][4 * i + t];
+    const float yA = dd.x * ((acc[0][i][0] + acc[0][i][1]) + (acc[1][i][0] + acc[1][i][1])) -
+                     dd.y * (cm[0] + cm[1]);
+    const float yB = dd.z * ((acc[0][i][2] + acc[0][i][3]) + (acc[1][i][2] + acc[1][i][3])) -
+                     dd.w * (cm[2] + cm[3]);
+    tot[0][i] = fmaf(us, yA, tot[0][i]);
+    tot[1][i] = fmaf(us, yB, tot[1][i]);
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s, int fs,
+                                                  uint32_t fpar, int warp, int lane, int *status,
+                                                  float (&tot)[2][NT]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t *tile = sm.w[s];
+  WarpTab<MQ_Q6_K> &tb = sm.tab[warp];
+  {  // lane (r, h): groups 8h..8h+7 of row r
+    const int r = lane & 15, h = lane >> 4, row = 16 * warp + r;
+    const uint2 scv = *reinterpret_cast<const uint2 *>(tile + kRows * 192 + row * 16 + 8 * h);
+    const float dv =
+        __half2float(*reinterpret_cast<const __half *>(tile + kRows * 208 + row * 2));
+    float *dst = reinterpret_cast<float *>(&tb.s[8 * h][r & 7]) + (r >> 3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      dst[k * 16] = dv * (float)(int8_t)((scv.x >> (8 * k)) & 255u);
+      dst[(4 + k) * 16] = dv * (float)(int8_t)((scv.y >> (8 * k)) & 255u);
+    }
+  }
+  __syncwarp();
+  const int ra = 16 * warp + g, rb = ra + 8;
+  uint32_t wa[12], wb[12];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const uint4 va = *reinterpret_cast<const uint4 *>(tile + ra * 192 + 48 * t + 16 * i);
+    const uint4 vb = *reinterpret_cast<const uint4 *>(tile + rb * 192 + 48 * t + 16 * i);
+    wa[4 * i] = va.x; wa[4 * i + 1] = va.y; wa[4 * i + 2] = va.z; wa[4 * i + 3] = va.w;
+    wb[4 * i] = vb.x; wb[4 * i + 1] = vb.y; wb[4 * i + 2] = vb.z; wb[4 * i + 3] = vb.w;
+  }
+  release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
+  float acc[2][NT];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[0][i] = acc[1][i] = 0.f;
+  const uint32_t magic = 0x64646464u;
+  const uint32_t bias = 0x64206420u;  // f16x2 (1056, 1056): 1024 + 32
+#pragma unroll
+  for (int hv = 0; hv < 4; ++hv) {  // (h, v) = (hv >> 1, hv & 1)
+    const uint32_t qaA = wa[3 * hv], qbA = wa[3 * hv + 1], qhA = wa[3 * hv + 2];
+    const uint32_t qaB = wb[3 * hv], qbB = wb[3 * hv + 1], qhB = wb[3 * hv + 2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t loA, loB, hA, hB;
+      if (r == 0) { loA = qaA & 0x0f0f0f0fu; loB = qaB & 0x0f0f0f0fu; hA = qhA << 4; hB = qhB << 4; }
+      else if (r == 1) { loA = qbA & 0x0f0f0f0fu; loB = qbB & 0x0f0f0f0fu; hA = qhA << 2; hB = qhB << 2; }
+      else if (r == 2) { loA = (qaA >> 4) & 0x0f0f0f0fu; loB = (qaB >> 4) & 0x0f0f0f0fu; hA = qhA; hB = qhB; }
+      else { loA = (qbA >> 4) & 0x0f0f0f0fu; loB = (qbB >> 4) & 0x0f0f0f0fu; hA = qhA >> 2; hB = qhB >> 2; }
+      const uint32_t qA = loA | (hA & 0x30303030u), qB = loB | (hB & 0x30303030u);
+      const uint32_t a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
+      const uint32_t a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
+      const uint32_t a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
+      const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
+      const int sidx = 8 * (hv >> 1) + 2 * r + (hv & 1);
+      const float2 sc = tb.s[sidx][g];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        float c4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint2 bf = sm.frag[fs][sidx][i][lane];
+        mma16816(c4, a0, a1, a2, a3, bf.x, bf.y);
+        acc[0][i] = fmaf(sc.x, c4[0] + c4[1], acc[0][i]);
+        acc[1][i] = fmaf(sc.y, c4[2] + c4[3], acc[1][i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const float us = sm.unscale[fs][4 * i + t];
+    tot[0][i] = fmaf(us, acc[0][i], tot[0][i]);
+    tot[1][i] = fmaf(us, acc[1][i], tot[1][i]);
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int s, int fs,
+                                                   uint32_t fpar, int warp, int lane,
+                                                   int *status, int nblk, float (&tot)[2][NT]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t *tile = sm.w[s];
+  WarpTab<MQ_Q8_0> &tb = sm.tab[warp];
+  {  // lane (r, h): blocks 4h..4h+3 of row r (slots past the chunk's blocks hold 0)
+    const int r = lane & 15, h = lane >> 4, row = 16 * warp + r;
+    const uint2 dv = *reinterpret_cast<const uint2 *>(tile + kRows * 256 + row * 16 + 8 * h);
+    float *dst = reinterpret_cast<float *>(&tb.s[4 * h][r & 7]) + (r >> 3);
+    dst[0] = f16_lo(dv.x);
+    dst[16] = f16_hi(dv.x);
+    dst[32] = f16_lo(dv.y);
+    dst[48] = f16_hi(dv.y);
+  }
+  __syncwarp();
+  const int ra = 16 * warp + g, rb = ra + 8;
+  uint2 va[8], vb[8];  // blocks past the chunk's end hold stale but finite bytes
+#pragma unroll
+  for (int blk = 0; blk < 8; ++blk) {
+    va[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + ra) * 32 + 8 * t);
+    vb[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + rb) * 32 + 8 * t);
+  }
+  release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
+  float acc[2][NT];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[0][i] = acc[1][i] = 0.f;
+  const uint32_t magic = 0x64646464u;
+  const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152): 1024 + 128
+#pragma unroll
+  for (int blk = 0; blk < 8; ++blk) {
+    if (blk < nblk) {
+      const uint32_t wa[2] = {va[blk].x, va[blk].y}, wb[2] = {vb[blk].x, vb[blk].y};
+      float c4[NT][4];
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) c4[i][r] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t qA = wa[u] ^ 0x80808080u, qB = wb[u] ^ 0x80808080u;
+        const uint32_t a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
+        const uint32_t a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
+        const uint32_t a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
+        const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const uint2 bf = sm.frag[fs][2 * blk + u][i][lane];
+          mma16816(c4[i], a0, a1, a2, a3, bf.x, bf.y);
+        }
+      }
+      const float2 dv = tb.s[blk][g];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        acc[0][i] = fmaf(dv.x, c4[i][0] + c4[i][1], acc[0][i]);
+        acc[1][i] = fmaf(dv.y, c4[i][2] + c4[i][3], acc[1][i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const float us = sm.unscale[fs][4 * i + t];
+    tot[0][i] = fmaf(us, acc[0][i], tot[0][i]);
+    tot[1][i] = fmaf(us, acc[1][i], tot[1][i]);
+  }
 }
 
 template <int TYPE, int NT>
-__global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
+__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  MvSmem<TYPE, NT> &sm = *reinterpret_cast<MvSmem<TYPE, NT> *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  using Smem = MvSmem<TYPE, NT>;
+  constexpr int NS = Smem::NS;
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                       ~uintptr_t(127));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int rank = blockIdx.x % p.S;
@@ -302,10 +573,23 @@ __global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
   const int c_end = (int)((int64_t)(rank + 1) * p.nchunk / p.S);
   const int nch = c_end - c_begin;
 
+  // B-fragment columns of absent batch rows stay zero for the whole call
+  {
+    uint4 *f = reinterpret_cast<uint4 *>(&sm.frag[0][0][0][0]);
+    constexpr int n16 = (int)(sizeof(sm.frag) / 16);
+    for (int i = tid; i < n16; i += kThreads) f[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < Smem::FS * 8) (&sm.unscale[0][0])[tid] = 0.f;
+  }
   if (tid == 0) {
-    for (int s = 0; s < kNS; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.full[s])), "r"(1));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.empty[s])), "r"(4));
+    for (int s = 0; s < NS; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.wfull[s])), "r"(1));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.wempty[s])),
+                   "r"(kCompute + 1));
+    }
+    for (int f = 0; f < Smem::FS; ++f) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.ffull[f])), "r"(32));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.fempty[f])),
+                   "r"(kCompute));
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -314,207 +598,32 @@ __global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
   float tot[2][NT];
 #pragma unroll
   for (int i = 0; i < NT; ++i) tot[0][i] = tot[1][i] = 0.f;
-  const int ra = 16 * warp + g;  // tile row of fragment row g (the other is ra + 8)
-  const int64_t rA = group * 64 + ra, rB = rA + 8;
-  const bool okA = rA < p.N, okB = rB < p.N;
 
-  if (warp == 4) {  // ---- producer: weight tiles and x chunks into the ring
-    if (lane == 0) {
-      for (int i = 0; i < nch; ++i) {
-        const int c = c_begin + i, s = i % kNS;
-        const int cw = chunk_width(p.K, c);
-        if (i >= kNS) mbar_wait(sa(&sm.empty[s]), ((i / kNS) - 1) & 1, p.status, 21);
-        const int64_t tile = group * p.nchunk + c;
-        uint32_t bytes = (uint32_t)(p.B * cw * 4);
-        if constexpr (TYPE == MQ_Q4_K) bytes += 64 * 144;
-        if constexpr (TYPE == MQ_Q6_K) bytes += 64 * 192 + 64 * 16 + 64 * 2;
-        if constexpr (TYPE == MQ_Q8_0) bytes += 64 * cw + 64 * 16;
-        const uint32_t bar = sa(&sm.full[s]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"(bytes)
-                     : "memory");
-        uint8_t *w = sm.w[s];
-        if constexpr (TYPE == MQ_Q4_K) {
-          bulk_1d(sa(w), p.q + tile * 64 * 144, 64 * 144, bar);
-        } else if constexpr (TYPE == MQ_Q6_K) {
-          bulk_1d(sa(w), p.q + tile * 64 * 192, 64 * 192, bar);
-          bulk_1d(sa(w + 64 * 192), p.sc + tile * 64 * 16, 64 * 16, bar);
-          bulk_1d(sa(w + 64 * 192 + 64 * 16), p.d + tile * 64, 64 * 2, bar);
-        } else {
-          bulk_1d(sa(w), p.q + (group * p.K + int64_t(c) * kChunk) * 64, (uint32_t)(64 * cw), bar);
-          bulk_1d(sa(w + 64 * 256), p.d + tile * 64 * 8, 64 * 16, bar);
-        }
-        for (int b = 0; b < p.B; ++b)
-          bulk_1d(sa(sm.x[s][b]), p.x + int64_t(b) * p.K + int64_t(c) * kChunk,
-                  (uint32_t)(cw * 4), bar);
-      }
-    }
-  } else {  // ---- compute warps
-    float(*tab)[16] = sm.tab[warp];
+  if (warp == kCopyWarp) {
+    if (lane == 0) issue_copies<TYPE, NT>(sm, p, group, c_begin, nch);
+  } else if (warp == kXWarp) {
+    stage_x<TYPE, NT>(sm, p, c_begin, nch, lane);
+  } else {
     for (int i = 0; i < nch; ++i) {
-      const int c = c_begin + i, s = i % kNS;
-      const int cw = chunk_width(p.K, c);
-      mbar_wait(sa(&sm.full[s]), (i / kNS) & 1, p.status, 22);
-      stage_x<TYPE, NT>(sm, s, p.B, cw);
-      WRegs<TYPE> cur;
-      load_words<TYPE>(sm.w[s], cur, ra, t, cw / 32);
-    float acc[2][NT];
-#pragma unroll
-    for (int i = 0; i < NT; ++i) acc[0][i] = acc[1][i] = 0.f;
-
-    if constexpr (TYPE == MQ_Q4_K) {
-      // decode 4 scales + 4 mins of row (t&1 ? g+8 : g), sub-blocks 4*(t>>1) .. +3
-      {
-        const uint4 h = cur.hdr;
-        const float dd = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffff)));
-        const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-        uint32_t scw, mw;
-        if (t >> 1) {
-          scw = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
-          mw = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
-        } else {
-          scw = h.y & 0x3f3f3f3fu;
-          mw = h.z & 0x3f3f3f3fu;
-        }
-        const int rl = g + 8 * (t & 1), j0 = 4 * (t >> 1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tab[rl][2 * (j0 + i)] = dd * 512.f * (float)((scw >> (8 * i)) & 255u);
-          tab[rl][2 * (j0 + i) + 1] = dm * (float)((mw >> (8 * i)) & 255u);
-        }
-      }
+      const int s = i % NS, fs = i % Smem::FS;
+      const uint32_t fpar = (i / Smem::FS) & 1;
+      mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 22);
+      if constexpr (TYPE == MQ_Q4_K)
+        compute_chunk_q4k<NT>(sm, s, fs, fpar, warp, lane, p.status, tot);
+      else if constexpr (TYPE == MQ_Q6_K)
+        compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, tot);
+      else
+        compute_chunk_q8_0<NT>(sm, s, fs, fpar, warp, lane, p.status,
+                               chunk_width(p.K, c_begin + i) / 32, tot);
       __syncwarp();
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {  // sub-blocks 2cc (low nibbles), 2cc+1 (high)
-        float clo[NT][4], chi[NT][4];
-#pragma unroll
-        for (int i = 0; i < NT; ++i)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) clo[i][r] = chi[i][r] = 0.f;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t wa = cur.a[2 * cc + u], wb = cur.b[2 * cc + u];
-          const uint32_t la = wa & 0x0f0f0f0fu, ha = (wa >> 4) & 0x0f0f0f0fu;
-          const uint32_t lb = wb & 0x0f0f0f0fu, hb = (wb >> 4) & 0x0f0f0f0fu;
-          const uint32_t la0 = e4m3x2_to_f16x2(la & 0xffff), la2 = e4m3x2_to_f16x2(la >> 16);
-          const uint32_t lb0 = e4m3x2_to_f16x2(lb & 0xffff), lb2 = e4m3x2_to_f16x2(lb >> 16);
-          const uint32_t ha0 = e4m3x2_to_f16x2(ha & 0xffff), ha2 = e4m3x2_to_f16x2(ha >> 16);
-          const uint32_t hb0 = e4m3x2_to_f16x2(hb & 0xffff), hb2 = e4m3x2_to_f16x2(hb >> 16);
-#pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            const uint2 bl = sm.frag[4 * cc + u][i][lane];      // group 2*(2cc) + u
-            const uint2 bh = sm.frag[4 * cc + 2 + u][i][lane];  // group 2*(2cc+1) + u
-            mma16816(clo[i], la0, lb0, la2, lb2, bl.x, bl.y);
-            mma16816(chi[i], ha0, hb0, ha2, hb2, bh.x, bh.y);
-          }
-        }
-        const int jl = 2 * cc, jh = 2 * cc + 1;
-        const float sAl = tab[g][2 * jl], mAl = tab[g][2 * jl + 1];
-        const float sBl = tab[g + 8][2 * jl], mBl = tab[g + 8][2 * jl + 1];
-        const float sAh = tab[g][2 * jh], mAh = tab[g][2 * jh + 1];
-        const float sBh = tab[g + 8][2 * jh], mBh = tab[g + 8][2 * jh + 1];
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-          const float xl = sm.xsum[jl][t + 4 * i], xh = sm.xsum[jh][t + 4 * i];
-          acc[0][i] = fmaf(sAl, clo[i][0] + clo[i][1], acc[0][i]);
-          acc[1][i] = fmaf(sBl, clo[i][2] + clo[i][3], acc[1][i]);
-          acc[0][i] = fmaf(-mAl, xl, acc[0][i]);
-          acc[1][i] = fmaf(-mBl, xl, acc[1][i]);
-          acc[0][i] = fmaf(sAh, chi[i][0] + chi[i][1], acc[0][i]);
-          acc[1][i] = fmaf(sBh, chi[i][2] + chi[i][3], acc[1][i]);
-          acc[0][i] = fmaf(-mAh, xh, acc[0][i]);
-          acc[1][i] = fmaf(-mBh, xh, acc[1][i]);
-        }
-      }
-    } else if constexpr (TYPE == MQ_Q6_K) {
-      {
-        const float dd = __half2float(__ushort_as_half(cur.dbits));
-        const int rl = g + 8 * (t & 1), s0 = 8 * (t >> 1);
-        const uint32_t w0 = cur.sc8.x, w1 = cur.sc8.y;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tab[rl][s0 + i] = dd * (float)(int8_t)((w0 >> (8 * i)) & 255u);
-          tab[rl][s0 + 4 + i] = dd * (float)(int8_t)((w1 >> (8 * i)) & 255u);
-        }
-      }
-      __syncwarp();
-      const uint32_t magic = 0x64646464u;
-      const uint32_t bias = 0x64206420u;  // f16x2 (1056, 1056)
-#pragma unroll
-      for (int hv = 0; hv < 4; ++hv) {  // (h, v) = (hv >> 1, hv & 1)
-        const uint32_t qaA = cur.a[3 * hv], qbA = cur.a[3 * hv + 1], qhA = cur.a[3 * hv + 2];
-        const uint32_t qaB = cur.b[3 * hv], qbB = cur.b[3 * hv + 1], qhB = cur.b[3 * hv + 2];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          uint32_t loA, loB, hA, hB;
-          if (r == 0) { loA = qaA & 0x0f0f0f0fu; loB = qaB & 0x0f0f0f0fu; hA = qhA << 4; hB = qhB << 4; }
-          else if (r == 1) { loA = qbA & 0x0f0f0f0fu; loB = qbB & 0x0f0f0f0fu; hA = qhA << 2; hB = qhB << 2; }
-          else if (r == 2) { loA = (qaA >> 4) & 0x0f0f0f0fu; loB = (qaB >> 4) & 0x0f0f0f0fu; hA = qhA; hB = qhB; }
-          else { loA = (qbA >> 4) & 0x0f0f0f0fu; loB = (qbB >> 4) & 0x0f0f0f0fu; hA = qhA >> 2; hB = qhB >> 2; }
-          const uint32_t qA = loA | (hA & 0x30303030u), qB = loB | (hB & 0x30303030u);
-          const uint32_t a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
-          const uint32_t a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
-          const uint32_t a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
-          const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
-          const int sidx = 8 * (hv >> 1) + 2 * r + (hv & 1);
-          const float sA = tab[g][sidx], sB = tab[g + 8][sidx];
-#pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint2 bf = sm.frag[sidx][i][lane];
-            mma16816(cacc, a0, a1, a2, a3, bf.x, bf.y);
-            acc[0][i] = fmaf(sA, cacc[0] + cacc[1], acc[0][i]);
-            acc[1][i] = fmaf(sB, cacc[2] + cacc[3], acc[1][i]);
-          }
-        }
-      }
-    } else {  // Q8_0
-      const uint32_t magic = 0x64646464u;
-      const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
-#pragma unroll
-      for (int blk = 0; blk < 8; ++blk) {
-        float cacc[NT][4];
-#pragma unroll
-        for (int i = 0; i < NT; ++i)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) cacc[i][r] = 0.f;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t qA = cur.a[2 * blk + u] ^ 0x80808080u;
-          const uint32_t qB = cur.b[2 * blk + u] ^ 0x80808080u;
-          const uint32_t a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
-          const uint32_t a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
-          const uint32_t a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
-          const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
-#pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            const uint2 bf = sm.frag[2 * blk + u][i][lane];
-            mma16816(cacc[i], a0, a1, a2, a3, bf.x, bf.y);
-          }
-        }
-        const float dA = __half2float(__ushort_as_half(cur.da[blk]));
-        const float dB = __half2float(__ushort_as_half(cur.db[blk]));
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-          acc[0][i] = fmaf(dA, cacc[i][0] + cacc[i][1], acc[0][i]);
-          acc[1][i] = fmaf(dB, cacc[i][2] + cacc[i][3], acc[1][i]);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < NT; ++i) {
-      const float us = sm.unscale[t + 4 * i];
-      tot[0][i] = fmaf(us, acc[0][i], tot[0][i]);
-      tot[1][i] = fmaf(us, acc[1][i], tot[1][i]);
-    }
-      __syncwarp();
-      if (lane == 0)  // this warp is done with stage s
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[s])) : "memory");
+      if (lane == 0) mbar_arrive(sa(&sm.fempty[fs]));  // this warp is done with the slot
     }
   }
 
+  const int64_t rA = group * kRows + 16 * warp + g, rB = rA + 8;
+  const bool okA = rA < p.N, okB = rB < p.N;
   if (p.S == 1) {
-    if (warp < 4) {
+    if (warp < kCompute) {
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         const int b = t + 4 * i;
@@ -526,8 +635,10 @@ __global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
     }
     return;
   }
-  // split-K over the cluster: rank 0 sums the ranks' partials in rank order
-  if (warp < 4) {
+  // split-K over the cluster: rank 0 sums the ranks' partials in rank order.
+  // part overlays the ring, so every warp must be past its last ring access.
+  __syncthreads();
+  if (warp < kCompute) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       sm.part[16 * warp + g][t + 4 * i] = tot[0][i];
@@ -536,7 +647,7 @@ __global__ void __launch_bounds__(kThreads) matvec_kernel(const MvArgs p) {
   }
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  if (rank == 0 && warp < 4) {
+  if (rank == 0 && warp < kCompute) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const int b = t + 4 * i;
@@ -562,7 +673,7 @@ constexpr size_t mv_smem_bytes() {
 
 template <int TYPE, int NT>
 mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
-  const int64_t groups = (a.N + 63) / 64;
+  const int64_t groups = (a.N + kRows - 1) / kRows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(groups * a.S), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -609,13 +720,14 @@ mq_status init_matvec(DeviceState *st) {
   return MQ_OK;
 }
 
-// K-split heuristic: enough CTAs for two per SM.  Depends only on (N, K, type),
+// K-split: as many slices as keep every CTA of the grid resident in one wave
+// of two CTAs per SM (at most 8, a portable cluster).  Depends only on (N, K),
 // never on B, so batched columns reproduce the B = 1 result bitwise.
-static int choose_split(int64_t N, int64_t K, int sms, int rows_per_cta) {
-  const int64_t groups = (N + rows_per_cta - 1) / rows_per_cta;
+static int choose_split(int64_t N, int64_t K, int sms) {
+  const int64_t groups = (N + kRows - 1) / kRows;
   const int nchunk = (int)((K + kChunk - 1) / kChunk);
-  int64_t want = (2 * int64_t(sms) + groups - 1) / groups;
-  int S = (int)(want < 8 ? want : 8);
+  const int64_t fit = 2 * int64_t(sms) / groups;
+  int S = (int)(fit < 8 ? fit : 8);
   S = min(S, nchunk);
   return max(S, 1);
 }
@@ -624,7 +736,6 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
                         const DeviceState *st) {
   MvArgs a;
   a.q = W->q;
-  a.sc = W->sc;
   a.d = W->d;
   a.x = x;
   a.y = y;
@@ -632,7 +743,7 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.K = W->K;
   a.B = B;
   a.nchunk = (int)((W->K + kChunk - 1) / kChunk);
-  a.S = choose_split(W->N, W->K, st->sms, 64);
+  a.S = choose_split(W->N, W->K, st->sms);
   a.status = st->status;
   const bool two = B > 4;
   switch (W->type) {

@@ -139,10 +139,10 @@ static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t
 }
 
 static mq_status free_planes(mq_weight *w) {
-  void *ps[] = {w->q, w->sc, w->d, w->mw, w->mw2, w->td, w->tm};
+  void *ps[] = {w->q, w->d, w->mw, w->mw2, w->td, w->tm};
   for (void *p : ps)
     if (p) cudaFree(p);
-  w->q = nullptr; w->sc = nullptr; w->d = nullptr; w->mw = nullptr;
+  w->q = nullptr; w->d = nullptr; w->mw = nullptr;
   w->mw2 = nullptr; w->td = nullptr; w->tm = nullptr;
   return MQ_OK;
 }
@@ -192,7 +192,7 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
     delete w;
     return r;
   };
-  // decode planes: padded to whole 64-row groups, padding rows zero
+  // decode planes: padded to whole row groups, padding rows zero
   w->ngroup = (N + kRowGroup - 1) / kRowGroup;
   w->nchunk = (int)((K + kChunk - 1) / kChunk);
   const size_t npad = size_t(w->ngroup) * kRowGroup;
@@ -207,9 +207,7 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
   } else if (type == MQ_Q4_K) {
     if ((s = zalloc(&w->q, npad * nsb * 144, "q4_K")) != MQ_OK) return cleanup(s);
   } else {
-    if ((s = zalloc(&w->q, npad * nsb * 192, "q6_K quants")) != MQ_OK) return cleanup(s);
-    if ((s = zalloc(&w->sc, npad * nsb * 16, "q6_K scales")) != MQ_OK) return cleanup(s);
-    if ((s = zalloc(&w->d, npad * nsb * 2, "q6_K d")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->q, npad * nsb * 210, "q6_K")) != MQ_OK) return cleanup(s);
   }
   const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE);
   if (mmq) {

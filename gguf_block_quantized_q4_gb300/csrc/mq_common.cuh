@@ -5,22 +5,25 @@
 // device memory for speed).  All planes are lossless regroupings of the GGUF
 // bytes except the prefill operand planes, which hold exact integer values.
 //
-// Decode planes (read by the matvec).  Rows are grouped by 64 (N padded with
-// zero rows to a multiple of 64) and K is cut into 256-element chunks; the tile
+// Decode planes (read by the matvec).  Rows are grouped by 128 (N padded with
+// zero rows to a multiple of 128) and K is cut into 256-element chunks; the tile
 // of one (row group g, chunk c) is contiguous, so one bulk copy moves it into
 // shared memory.  Inside a row, each fragment thread's words are contiguous and
 // 16-byte aligned (t = fragment thread 0..3, r = row in the group):
-//   Q4_K  q   tile (g,c) at ((g*nchunk + c)*64 + r)*144: bytes 0..15 the GGUF
-//             header (d, dmin, 12 scale bytes); byte 16 + 32t + 4(2c'+u) + i  <-
-//             qs byte 32c' + 16u + 4t + i
-//   Q6_K  q   at ((g*nchunk + c)*64 + r)*192: byte 48t + 4(3(2h+v) + w) + i  <-
-//             word w of (h, v): w=0 ql[64h + 16v + 4t + i],
-//             w=1 ql[64h + 32 + 16v + 4t + i], w=2 qh[32h + 16v + 4t + i]
-//         sc  int8 at ((g*nchunk + c)*64 + r)*16: the 16 sub-scales
-//         d   u16 at (g*nchunk + c)*64 + r: the f16 super-block scale
-//   Q8_0  qs  tile (g,c) at (g*K + 256c)*64 bytes, [block j][row r][32 bytes]:
+//   Q4_K  q   tile (g,c) at ((g*nchunk + c)*128 + r)*144: bytes 0..15 the GGUF
+//             header (d, dmin, 12 scale bytes); word 2c'+u of thread t (bytes
+//             16 + 32t + 4(2c'+u) + i) holds qs bytes 32c' + 16u + 4t + {0,2,1,3}[i],
+//             so that masking nibbles 0-3 / 4-7 of bytes 0 and 2 (then, after a
+//             shift by 8, of bytes 1 and 3) yields the element pairs of one
+//             fragment register
+//   Q6_K  q   tile (g,c) at (g*nchunk + c)*128*210, three parts:
+//             quants at r*192: byte 48t + 4(3(2h+v) + w) + i  <-  word w of (h, v):
+//               w=0 ql[64h + 16v + 4t + i], w=1 ql[64h + 32 + 16v + 4t + i],
+//               w=2 qh[32h + 16v + 4t + i];
+//             int8 sub-scales at 128*192 + r*16; f16 d at 128*208 + r*2
+//   Q8_0  qs  tile (g,c) at (g*K + 256c)*128 bytes, [block j][row r][32 bytes]:
 //             stored byte 8t + 4u + i  <-  block byte 16u + 4t + i (u = 16-element half)
-//         d   u16 at ((g*nchunk + c)*64 + r)*8 + j (8 slots per chunk; unused ones 0)
+//         d   u16 at ((g*nchunk + c)*128 + r)*8 + j (8 slots per chunk; unused ones 0)
 // Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them), K-major for TMA:
 //   w      f16  [N][K]    integer weight W_int: Q8_0 q; Q4_K sc_j*nib (<= 945);
 //                         Q6_K the even part 2*floor(v/2) of v = sc*(q-32) (|v| <= 4096)
@@ -42,15 +45,14 @@ struct mq_weight {
   int type;
   int64_t N, K;
   int64_t np;            // N rounded up to 128: row stride of the transposed planes
-  int64_t ngroup;        // decode-plane row groups (N rounded up to 64, / 64)
+  int64_t ngroup;        // decode-plane row groups (N rounded up to 128, / 128)
   int nchunk;            // decode-plane K chunks (K / 256 rounded up)
   int device;
   size_t payload;        // GGUF bytes
   size_t device_bytes;   // all planes
   // decode planes
-  uint8_t *q = nullptr;  // Q8_0 qs / Q4_K 144-byte blocks / Q6_K 192-byte quant blocks
-  int8_t *sc = nullptr;  // Q6_K sub-scales
-  uint16_t *d = nullptr; // Q8_0 block d / Q6_K super-block d
+  uint8_t *q = nullptr;  // Q8_0 qs / Q4_K and Q6_K tiles
+  uint16_t *d = nullptr; // Q8_0 block d
   // prefill operand planes
   __half *mw = nullptr;
   __half *mw2 = nullptr;
@@ -63,7 +65,7 @@ struct mq_weight {
 namespace mq {
 
 constexpr int kMaxB = 8;
-constexpr int kRowGroup = 64;  // decode-plane row group
+constexpr int kRowGroup = 128; // decode-plane row group (rows per matvec CTA)
 constexpr int kChunk = 256;    // decode-plane K chunk
 constexpr int kStatusTimeout = 1;
 

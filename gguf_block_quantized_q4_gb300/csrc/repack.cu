@@ -50,6 +50,15 @@ __device__ __forceinline__ int64_t q8_0_doff(int64_t n, int64_t b, int nchunk) {
 __device__ __forceinline__ int64_t tile_row(int64_t n, int64_t c, int nchunk) {
   return (n / kRowGroup * nchunk + c) * kRowGroup + n % kRowGroup;
 }
+// Q4_K: byte i of a stored quant word comes from element offset kQ4kPerm[i] of the
+// thread's 4 consecutive qs bytes (elements 4t, 4t+1 land in bytes 0 and 2).
+__constant__ int kQ4kPerm[4] = {0, 2, 1, 3};
+// Q6_K: byte offset of the tile holding (row n, super-block c); the tile is
+// [128 rows][192 quant bytes], then [128][16] sub-scales, then [128] f16 d.
+constexpr int64_t kQ6kTile = int64_t(kRowGroup) * 210;
+__device__ __forceinline__ int64_t q6k_tile(int64_t n, int64_t c, int nchunk) {
+  return (n / kRowGroup * nchunk + c) * kQ6kTile;
+}
 
 __global__ void repack_q8_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
                             uint8_t *__restrict__ q, uint16_t *__restrict__ d,
@@ -103,7 +112,7 @@ __global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
     for (int c = 0; c < 4; ++c)
       for (int u = 0; u < 2; ++u)
         for (int e = 0; e < 4; ++e)
-          dst[16 + 32 * t + 4 * (2 * c + u) + e] = src[16 + 32 * c + 16 * u + 4 * t + e];
+          dst[16 + 32 * t + 4 * (2 * c + u) + e] = src[16 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]];
   if (mw) {
     const int64_t n = i / nsb, s = i % nsb;
     const float dd = f16bits(rd16(src)), dmin = f16bits(rd16(src + 2));
@@ -133,7 +142,7 @@ __global__ void unpack_q4_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
     for (int c = 0; c < 4; ++c)
       for (int u = 0; u < 2; ++u)
         for (int e = 0; e < 4; ++e)
-          dst[16 + 32 * c + 16 * u + 4 * t + e] = src[16 + 32 * t + 4 * (2 * c + u) + e];
+          dst[16 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]] = src[16 + 32 * t + 4 * (2 * c + u) + e];
 }
 
 // Byte offset in the raw Q6_K block of word w (0: ql low pair, 1: ql high pair,
@@ -144,24 +153,25 @@ __device__ __forceinline__ int q6k_src(int t, int h, int v, int w) {
 }
 
 __global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
-                            uint8_t *__restrict__ q, int8_t *__restrict__ sc,
-                            uint16_t *__restrict__ d, __half *__restrict__ mw,
+                            uint8_t *__restrict__ q, __half *__restrict__ mw,
                             __half *__restrict__ mw2, float *__restrict__ td) {
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
   const uint8_t *src = raw + i * 210;
-  const int64_t tr = tile_row(i / nsb, i % nsb, (int)nsb);
-  uint8_t *dst = q + tr * 192;
+  const int64_t r = (i / nsb) % kRowGroup;
+  uint8_t *tile = q + q6k_tile(i / nsb, i % nsb, (int)nsb);
+  uint8_t *dst = tile + r * 192;
   for (int t = 0; t < 4; ++t)
     for (int h = 0; h < 2; ++h)
       for (int v = 0; v < 2; ++v)
         for (int w = 0; w < 3; ++w)
           for (int e = 0; e < 4; ++e)
             dst[48 * t + 4 * (3 * (2 * h + v) + w) + e] = src[q6k_src(t, h, v, w) + e];
-  for (int e = 0; e < 16; ++e) sc[tr * 16 + e] = (int8_t)src[192 + e];
+  for (int e = 0; e < 16; ++e) tile[kRowGroup * 192 + r * 16 + e] = src[192 + e];
   const uint16_t dbits = rd16(src + 208);
-  d[tr] = dbits;
+  tile[kRowGroup * 208 + 2 * r] = src[208];
+  tile[kRowGroup * 208 + 2 * r + 1] = src[209];
   if (mw) {
     const int64_t n = i / nsb, s = i % nsb;
     const float dd = f16bits(dbits);
@@ -179,14 +189,14 @@ __global__ void repack_q6_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
   }
 }
 
-__global__ void unpack_q6_k(const uint8_t *__restrict__ q, const int8_t *__restrict__ sc,
-                            const uint16_t *__restrict__ d, int64_t N, int64_t K,
+__global__ void unpack_q6_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
                             uint8_t *__restrict__ raw) {
   const int64_t nsb = K / 256;
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nsb) return;
-  const int64_t tr = tile_row(i / nsb, i % nsb, (int)nsb);
-  const uint8_t *src = q + tr * 192;
+  const int64_t r = (i / nsb) % kRowGroup;
+  const uint8_t *tile = q + q6k_tile(i / nsb, i % nsb, (int)nsb);
+  const uint8_t *src = tile + r * 192;
   uint8_t *dst = raw + i * 210;
   for (int t = 0; t < 4; ++t)
     for (int h = 0; h < 2; ++h)
@@ -194,9 +204,9 @@ __global__ void unpack_q6_k(const uint8_t *__restrict__ q, const int8_t *__restr
         for (int w = 0; w < 3; ++w)
           for (int e = 0; e < 4; ++e)
             dst[q6k_src(t, h, v, w) + e] = src[48 * t + 4 * (3 * (2 * h + v) + w) + e];
-  for (int e = 0; e < 16; ++e) dst[192 + e] = (uint8_t)sc[tr * 16 + e];
-  dst[208] = d[tr] & 255;
-  dst[209] = d[tr] >> 8;
+  for (int e = 0; e < 16; ++e) dst[192 + e] = tile[kRowGroup * 192 + r * 16 + e];
+  dst[208] = tile[kRowGroup * 208 + 2 * r];
+  dst[209] = tile[kRowGroup * 208 + 2 * r + 1];
 }
 
 inline unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
@@ -218,8 +228,8 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
     MQ_LAUNCH_CHECK("repack_q4_k");
   } else {
     const int64_t n = N * (K / 256);
-    repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->sc, w->d,
-                                              mmq ? w->mw : nullptr, w->mw2, w->td);
+    repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,
+                                              w->mw2, w->td);
     MQ_LAUNCH_CHECK("repack_q6_k");
   }
   return MQ_OK;
@@ -235,7 +245,7 @@ mq_status unpack_weight(const mq_weight *w, uint8_t *raw, cudaStream_t s) {
     unpack_q4_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q4_k");
   } else {
-    unpack_q6_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, w->sc, w->d, N, K, raw);
+    unpack_q6_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q6_k");
   }
   return MQ_OK;
