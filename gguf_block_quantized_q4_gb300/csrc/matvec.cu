@@ -87,15 +87,19 @@ template <int TYPE, int NT>
 __host__ __device__ constexpr int ring_stages() {
   return TYPE == MQ_Q4_K ? (NT == 1 ? 4 : 3) : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
 }
-constexpr int kFragSlots = 2;  // fragment-ring depth
+// Fragment-ring depth.
+template <int TYPE>
+__host__ __device__ constexpr int frag_slots() {
+  return TYPE == MQ_Q4_K ? 3 : 2;
+}
 
 // Per-warp tables decoded from the tile headers of the warp's 16 rows.
 template <int TYPE>
 struct WarpTab;
 template <>
 struct WarpTab<MQ_Q4_K> {
-  uint4 sc[4][8][2];  // [pair c'][g][lo, hi sub-block]: f16x2 (mul A, add A, mul B, add B)
-  uint2 mf[8][4];     // [g][t]: min-term A fragment words of rows g, g+8
+  uint4 sc[4][2][8];  // [pair c'][lo, hi sub-block][g]: f16x2 (mul A, add A, mul B, add B)
+  uint2 mf[4][8];     // [t][g]: min-term A fragment words of rows g, g+8
   float4 dd[8];       // [g]: d_A, 32*dmin_A, d_B, 32*dmin_B
 };
 template <>
@@ -110,7 +114,7 @@ struct WarpTab<MQ_Q8_0> {
 template <int TYPE, int NT>
 struct MvSmem {
   static constexpr int NS = ring_stages<TYPE, NT>();
-  static constexpr int FS = kFragSlots;
+  static constexpr int FS = frag_slots<TYPE>();
   static constexpr int FG = TYPE == MQ_Q4_K ? 17 : 16;  // 16 groups (+ the Q4_K min group)
   union {
     alignas(128) uint8_t w[NS][tile_bytes<TYPE>()];  // weight tiles
@@ -151,6 +155,13 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   return r;
 }
 
+// (a & b) | c as one three-input logic instruction (written out so that two
+// constant operands do not turn it into two instructions)
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -325,43 +336,43 @@ __device__ __forceinline__ void release_and_wait(uint64_t &wempty, uint64_t &ffu
 template <int NT>
 __device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s, int fs,
                                                   uint32_t fpar, int warp, int lane, int *status,
-                                                  float (&tot)[2][NT]) {
+                                                  const int (&fl)[NT], float (&tot)[2][NT]) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
   WarpTab<MQ_Q4_K> &tb = sm.tab[warp];
-  {  // decode the 16 rows' scales: lane (r, h) takes sub-blocks 4h..4h+3 of row r
-    const int r = lane & 15, h = lane >> 4;
-    const uint4 hd = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r) * 144);
-    uint32_t scw, mnw;
-    if (h == 0) {
-      scw = hd.y & 0x3f3f3f3fu;
-      mnw = hd.z & 0x3f3f3f3fu;
+  {  // lane c'*8 + r decodes sub-blocks 2c', 2c'+1 of rows r and r+8 (entry = lane)
+    const int cp = lane >> 3, r = lane & 7;
+    const uint4 ha = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r) * 144);
+    const uint4 hb = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r + 8) * 144);
+    // 6-bit scales / mins of sub-blocks 4q..4q+3 as bytes (q = cp >> 1)
+    uint32_t sa4, sb4, ma4, mb4;
+    if (cp < 2) {
+      sa4 = ha.y & 0x3f3f3f3fu;
+      sb4 = hb.y & 0x3f3f3f3fu;
+      ma4 = ha.z & 0x3f3f3f3fu;
+      mb4 = hb.z & 0x3f3f3f3fu;
     } else {
-      scw = (hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u);
-      mnw = ((hd.w >> 4) & 0x0f0f0f0fu) | ((hd.z >> 2) & 0x30303030u);
+      sa4 = (ha.w & 0x0f0f0f0fu) | ((ha.y >> 2) & 0x30303030u);
+      sb4 = (hb.w & 0x0f0f0f0fu) | ((hb.y >> 2) & 0x30303030u);
+      ma4 = ((ha.w >> 4) & 0x0f0f0f0fu) | ((ha.z >> 2) & 0x30303030u);
+      mb4 = ((hb.w >> 4) & 0x0f0f0f0fu) | ((hb.z >> 2) & 0x30303030u);
     }
-    // bytes -> f16x2 integers (1024 + v) - 1024
-    const uint32_t k1024 = 0x64006400u;
-    const uint32_t s01 = hsub2(__byte_perm(scw, 0x64646464u, 0x5140), k1024);
-    const uint32_t s23 = hsub2(__byte_perm(scw, 0x64646464u, 0x5342), k1024);
-    const uint32_t m01 = hsub2(__byte_perm(mnw, 0x64646464u, 0x5140), k1024);
-    const uint32_t m23 = hsub2(__byte_perm(mnw, 0x64646464u, 0x5342), k1024);
-    const int gg = r & 7, ab = r >> 3;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {  // pair c' = 2h + q: sub-blocks 4h+2q (lo), 4h+2q+1 (hi)
-      const uint32_t sp = q ? s23 : s01;
-      const uint32_t slo = __byte_perm(sp, sp, 0x1010), shi = __byte_perm(sp, sp, 0x3232);
-      // lo nibble n read as 1024 + n:   (1024 + n) * sc - 1024 sc
-      // hi nibble n read as 1024 + 16n: (1024 + 16n) * sc/16 - 64 sc
-      reinterpret_cast<uint2 *>(&tb.sc[2 * h + q][gg][0])[ab] =
-          make_uint2(slo, hmul2(slo, 0xE400E400u));
-      reinterpret_cast<uint2 *>(&tb.sc[2 * h + q][gg][1])[ab] =
-          make_uint2(hmul2(shi, 0x2C002C00u), hmul2(shi, 0xD400D400u));
-    }
-    reinterpret_cast<uint32_t *>(&tb.mf[gg][2 * h])[ab] = m01;
-    reinterpret_cast<uint32_t *>(&tb.mf[gg][2 * h + 1])[ab] = m23;
-    const float dv = h == 0 ? f16_lo(hd.x) : 32.f * f16_hi(hd.x);
-    reinterpret_cast<float *>(&tb.dd[gg])[2 * ab + h] = dv;
+    // bytes 2(cp&1), 2(cp&1)+1 of each -> f16x2 integers (1024 + v) - 1024
+    const uint32_t sel = (cp & 1) ? 0x5342u : 0x5140u, k1024 = 0x64006400u;
+    const uint32_t scA = hsub2(__byte_perm(sa4, 0x64646464u, sel), k1024);
+    const uint32_t scB = hsub2(__byte_perm(sb4, 0x64646464u, sel), k1024);
+    // lo sub-block 2c' multiplies (1024 + n) by sc; hi sub-block 2c'+1 multiplies
+    // (1024 + 16n) by sc/16; the addend is -1024 times the multiplier in both
+    const uint32_t loA = __byte_perm(scA, scA, 0x1010), loB = __byte_perm(scB, scB, 0x1010);
+    const uint32_t hiA = hmul2(__byte_perm(scA, scA, 0x3232), 0x2C002C00u);
+    const uint32_t hiB = hmul2(__byte_perm(scB, scB, 0x3232), 0x2C002C00u);
+    constexpr uint32_t kNeg1024 = 0xE400E400u;
+    tb.sc[cp][0][r] = make_uint4(loA, hmul2(loA, kNeg1024), loB, hmul2(loB, kNeg1024));
+    tb.sc[cp][1][r] = make_uint4(hiA, hmul2(hiA, kNeg1024), hiB, hmul2(hiB, kNeg1024));
+    tb.mf[cp][r] = make_uint2(hsub2(__byte_perm(ma4, 0x64646464u, sel), k1024),
+                              hsub2(__byte_perm(mb4, 0x64646464u, sel), k1024));
+    if (cp == 0)
+      tb.dd[r] = make_float4(f16_lo(ha.x), 32.f * f16_hi(ha.x), f16_lo(hb.x), 32.f * f16_hi(hb.x));
   }
   __syncwarp();
   const int ra = 16 * warp + g, rb = ra + 8;
@@ -372,48 +383,56 @@ __device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s
   const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
   const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
   release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
+  // min term first: its MMA latency hides under the main loop
+  float cm[NT][4];
+  {
+    const uint2 mf = tb.mf[t][g];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const uint2 bm = sm.frag[fs][16][i][fl[i]];
+      cm[i][0] = cm[i][1] = cm[i][2] = cm[i][3] = 0.f;
+      mma16816(cm[i], mf.x, mf.y, 0u, 0u, bm.x, bm.y);
+    }
+  }
   float acc[2][NT][4];
 #pragma unroll
   for (int i = 0; i < NT; ++i)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[0][i][r] = acc[1][i][r] = 0.f;
-  constexpr uint32_t kMagic = 0x64006400u;
+  // nibble n of bits 0-3 (kLo) or 4-7 (kHi) of each half -> f16 1024 + n or 1024 + 16n
+  constexpr uint32_t kMagic = 0x64006400u, kLo = 0x000f000fu, kHi = 0x00f000f0u;
 #pragma unroll
   for (int cp = 0; cp < 4; ++cp) {
-    const uint4 slo = tb.sc[cp][g][0], shi = tb.sc[cp][g][1];
+    const uint4 slo = tb.sc[cp][0][g], shi = tb.sc[cp][1][g];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const uint32_t xa = wa[2 * cp + u], xb = wb[2 * cp + u];
       const uint32_t xa8 = xa >> 8, xb8 = xb >> 8;
-      const uint32_t l0 = hfma2((xa & 0x000f000fu) | kMagic, slo.x, slo.y);
-      const uint32_t l1 = hfma2((xb & 0x000f000fu) | kMagic, slo.z, slo.w);
-      const uint32_t l2 = hfma2((xa8 & 0x000f000fu) | kMagic, slo.x, slo.y);
-      const uint32_t l3 = hfma2((xb8 & 0x000f000fu) | kMagic, slo.z, slo.w);
-      const uint32_t h0 = hfma2((xa & 0x00f000f0u) | kMagic, shi.x, shi.y);
-      const uint32_t h1 = hfma2((xb & 0x00f000f0u) | kMagic, shi.z, shi.w);
-      const uint32_t h2 = hfma2((xa8 & 0x00f000f0u) | kMagic, shi.x, shi.y);
-      const uint32_t h3 = hfma2((xb8 & 0x00f000f0u) | kMagic, shi.z, shi.w);
+      const uint32_t l0 = hfma2(and_or(xa, kLo, kMagic), slo.x, slo.y);
+      const uint32_t l1 = hfma2(and_or(xb, kLo, kMagic), slo.z, slo.w);
+      const uint32_t l2 = hfma2(and_or(xa8, kLo, kMagic), slo.x, slo.y);
+      const uint32_t l3 = hfma2(and_or(xb8, kLo, kMagic), slo.z, slo.w);
+      const uint32_t h0 = hfma2(and_or(xa, kHi, kMagic), shi.x, shi.y);
+      const uint32_t h1 = hfma2(and_or(xb, kHi, kMagic), shi.z, shi.w);
+      const uint32_t h2 = hfma2(and_or(xa8, kHi, kMagic), shi.x, shi.y);
+      const uint32_t h3 = hfma2(and_or(xb8, kHi, kMagic), shi.z, shi.w);
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        const uint2 bl = sm.frag[fs][4 * cp + u][i][lane];      // sub-block 2c', K half u
-        const uint2 bh = sm.frag[fs][4 * cp + 2 + u][i][lane];  // sub-block 2c'+1
+        const uint2 bl = sm.frag[fs][4 * cp + u][i][fl[i]];      // sub-block 2c', K half u
+        const uint2 bh = sm.frag[fs][4 * cp + 2 + u][i][fl[i]];  // sub-block 2c'+1
         mma16816(acc[0][i], l0, l1, l2, l3, bl.x, bl.y);
         mma16816(acc[1][i], h0, h1, h2, h3, bh.x, bh.y);
       }
     }
   }
-  const uint2 mf = tb.mf[g][t];
   const float4 dd = tb.dd[g];
 #pragma unroll
   for (int i = 0; i < NT; ++i) {
-    const uint2 bm = sm.frag[fs][16][i][lane];
-    float cm[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16816(cm, mf.x, mf.y, 0u, 0u, bm.x, bm.y);
     const float us = sm.unscale[fs][4 * i + t];
     const float yA = dd.x * ((acc[0][i][0] + acc[0][i][1]) + (acc[1][i][0] + acc[1][i][1])) -
-                     dd.y * (cm[0] + cm[1]);
+                     dd.y * (cm[i][0] + cm[i][1]);
     const float yB = dd.z * ((acc[0][i][2] + acc[0][i][3]) + (acc[1][i][2] + acc[1][i][3])) -
-                     dd.w * (cm[2] + cm[3]);
+                     dd.w * (cm[i][2] + cm[i][3]);
     tot[0][i] = fmaf(us, yA, tot[0][i]);
     tot[1][i] = fmaf(us, yB, tot[1][i]);
   }
@@ -422,7 +441,7 @@ __device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s
 template <int NT>
 __device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s, int fs,
                                                   uint32_t fpar, int warp, int lane, int *status,
-                                                  float (&tot)[2][NT]) {
+                                                  const int (&fl)[NT], float (&tot)[2][NT]) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
   WarpTab<MQ_Q6_K> &tb = sm.tab[warp];
@@ -475,7 +494,7 @@ __device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         float c4[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint2 bf = sm.frag[fs][sidx][i][lane];
+        const uint2 bf = sm.frag[fs][sidx][i][fl[i]];
         mma16816(c4, a0, a1, a2, a3, bf.x, bf.y);
         acc[0][i] = fmaf(sc.x, c4[0] + c4[1], acc[0][i]);
         acc[1][i] = fmaf(sc.y, c4[2] + c4[3], acc[1][i]);
@@ -493,7 +512,8 @@ __device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s
 template <int NT>
 __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int s, int fs,
                                                    uint32_t fpar, int warp, int lane,
-                                                   int *status, int nblk, float (&tot)[2][NT]) {
+                                                   int *status, int nblk, const int (&fl)[NT],
+                                                   float (&tot)[2][NT]) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
   WarpTab<MQ_Q8_0> &tb = sm.tab[warp];
@@ -538,7 +558,7 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int 
         const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          const uint2 bf = sm.frag[fs][2 * blk + u][i][lane];
+          const uint2 bf = sm.frag[fs][2 * blk + u][i][fl[i]];
           mma16816(c4[i], a0, a1, a2, a3, bf.x, bf.y);
         }
       }
@@ -573,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   const int c_end = (int)((int64_t)(rank + 1) * p.nchunk / p.S);
   const int nch = c_end - c_begin;
 
-  // B-fragment columns of absent batch rows stay zero for the whole call
+  // fragment columns of absent batch rows stay zero (never read for stored outputs)
   {
     uint4 *f = reinterpret_cast<uint4 *>(&sm.frag[0][0][0][0]);
     constexpr int n16 = (int)(sizeof(sm.frag) / 16);
@@ -604,17 +624,24 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   } else if (warp == kXWarp) {
     stage_x<TYPE, NT>(sm, p, c_begin, nch, lane);
   } else {
+    // Lane (g, t) feeds column g of each n8 tile, i.e. batch row 4i + g/2.  Lanes
+    // of absent batch rows read lane (g mod 2, t)'s fragment instead: the copy
+    // only feeds accumulator columns that are never stored, and the shared
+    // reads then touch fewer distinct words.
+    int fl[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) fl[i] = 4 * i + (g >> 1) < p.B ? lane : (lane & 7);
     for (int i = 0; i < nch; ++i) {
       const int s = i % NS, fs = i % Smem::FS;
       const uint32_t fpar = (i / Smem::FS) & 1;
       mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 22);
       if constexpr (TYPE == MQ_Q4_K)
-        compute_chunk_q4k<NT>(sm, s, fs, fpar, warp, lane, p.status, tot);
+        compute_chunk_q4k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else if constexpr (TYPE == MQ_Q6_K)
-        compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, tot);
+        compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else
         compute_chunk_q8_0<NT>(sm, s, fs, fpar, warp, lane, p.status,
-                               chunk_width(p.K, c_begin + i) / 32, tot);
+                               chunk_width(p.K, c_begin + i) / 32, fl, tot);
       __syncwarp();
       if (lane == 0) mbar_arrive(sa(&sm.fempty[fs]));  // this warp is done with the slot
     }
