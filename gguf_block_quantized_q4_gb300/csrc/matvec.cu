@@ -45,6 +45,12 @@
 //    registers, release the weight stage at once (so the next chunk's copy is
 //    in flight during the MMAs), then wait for the fragment slot, run the MMAs
 //    and release the slot.  They never wait for one another.
+// Launches overlap: the kernel is launched with programmatic stream
+// serialization and lets the next kernel in the stream launch as soon as all of
+// its CTAs are running.  The weight tiles of the first ring stages are
+// requested before griddepcontrol.wait (registered weights are never written
+// by a kernel), x only after it, and y is written only after x has been read,
+// so the tail of the previous kernel overlaps this kernel's first HBM traffic.
 // When one wave would be short of CTAs, K is split over a thread-block cluster
 // of S CTAs whose partial sums are reduced through distributed shared memory in
 // rank order (deterministic, and independent of B, so every column of a batched
@@ -226,10 +232,9 @@ template <int TYPE, int NT>
 __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs &p,
                                              int64_t group, int c_begin, int nch) {
   constexpr int NS = MvSmem<TYPE, NT>::NS;
-  for (int i = 0; i < nch; ++i) {
+  auto weights = [&](int i) {
     const int c = c_begin + i, s = i % NS;
     const int cw = chunk_width(p.K, c);
-    if (i >= NS) mbar_wait(sa(&sm.wempty[s]), ((i / NS) - 1) & 1, p.status, 21);
     const uint32_t bar = sa(&sm.wfull[s]);
     const uint32_t wbytes =
         TYPE == MQ_Q8_0 ? (uint32_t)(kRows * cw + kRows * 16) : (uint32_t)tile_bytes<TYPE>();
@@ -245,9 +250,22 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
       bulk_1d(sa(w), p.q + (group * p.nchunk + c) * int64_t(tile_bytes<TYPE>()),
               (uint32_t)tile_bytes<TYPE>(), bar);
     }
+  };
+  auto xrows = [&](int i) {
+    const int c = c_begin + i, s = i % NS;
+    const int cw = chunk_width(p.K, c);
     for (int b = 0; b < p.B; ++b)
       bulk_1d(sa(sm.xr[s][b]), p.x + int64_t(b) * p.K + int64_t(c) * kChunk, (uint32_t)(cw * 4),
-              bar);
+              sa(&sm.wfull[s]));
+  };
+  const int pre = nch < NS ? nch : NS;
+  for (int i = 0; i < pre; ++i) weights(i);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+  for (int i = 0; i < pre; ++i) xrows(i);
+  for (int i = pre; i < nch; ++i) {
+    mbar_wait(sa(&sm.wempty[i % NS]), ((i / NS) - 1) & 1, p.status, 21);
+    weights(i);
+    xrows(i);
   }
 }
 
@@ -614,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   float tot[2][NT];
 #pragma unroll
@@ -706,13 +725,15 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = mv_smem_bytes<TYPE, NT>();
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = a.S > 1 ? 1 : 0;
+  cfg.numAttrs = a.S > 1 ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, NT>, a);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u, cluster %d) failed: %s", name,
