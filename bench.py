@@ -6,9 +6,10 @@ Q4_K 18944 x 3584 weight (a Qwen2.5-7B FFN up/gate projection, synthetic):
   3. prefill MMQ, M = 512           (the prefill MMQ TOPS metric)
 
 Prints one JSON line.  `value` is the decode matvec's HBM throughput (algorithmic
-bytes / kernel time, whole job = all ranks); the MMQ's int-op rate and the
-per-kernel rooflines are in the same line.  L2 is defeated by rotating over R
-independent copies of every buffer (weights and activations), > 3x the 135 MB L2.
+bytes / kernel time, whole job = all ranks), timed over back-to-back calls on
+rotating weight copies (> 3x the 135 MB L2) replayed from a CUDA graph; the
+MMQ's int-op rate and the per-kernel rooflines are in the same line.  The K
+timed steps (matvec + quantise + MMQ each) are one captured CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mq|reference]
 """
@@ -31,7 +32,8 @@ WORKLOAD = "q4_k_18944x3584: decode matvec B=1 + quantise + MMQ M=512"
 METRIC = "Q-matvec HBM GB/s (% of peak); prefill MMQ int8 TOPS (% of tensor peak)"
 QTYPE, N, K, B, M = 12, 18944, 3584, 1, 512
 W_SEED, XD_SEED, XA_SEED = 102, 202, 204
-ROT = 4  # buffer sets rotated between steps (4 x ~245 MB >> L2)
+ROT = 4  # prefill buffer sets rotated between steps (4 x ~220 MB >> L2)
+L2_BYTES = 135e6
 
 # algorithmic bytes / ops per launch (what the method must move or compute)
 MV_BYTES = N * (K // 256) * 144 + B * K * 4 + B * N * 4
@@ -197,6 +199,28 @@ def run_reference(args):
     return 0
 
 
+def graph_time_ms(fn, calls, trials=5):
+    """Median over `trials` of the device time of one replay of a CUDA graph holding
+    `fn(j)` for j < calls, divided by calls (events on the replay stream)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for j in range(calls):
+            fn(j)
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(trials):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / calls)
+    del g
+    return statistics.median(out)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -226,59 +250,65 @@ def main():
     dev = torch.device("cuda", local)
 
     Wb = synth.weights(QTYPE, N, K, W_SEED)
-    Ws = [mq.register_weight(QTYPE, Wb, N, K) for _ in range(ROT)]
+    # decode: RMV weight copies, > 3x L2 together, so back-to-back calls read HBM
+    rmv = int(np.ceil(3 * L2_BYTES / len(Wb)))
+    Wd = [mq.register_weight(QTYPE, Wb, N, K, mq.REG_NO_MMQ_PLANE) for _ in range(rmv)]
+    Wp = [mq.register_weight(QTYPE, Wb, N, K) for _ in range(ROT)]
     xd_h = synth.activations(B, K, XD_SEED)
     xa_h = synth.activations(M, K, XA_SEED)
     xd = [torch.from_numpy(xd_h).to(dev) for _ in range(ROT)]
     xa = [torch.from_numpy(xa_h).to(dev) for _ in range(ROT)]
-    yd = [torch.empty((B, N), device=dev) for _ in range(ROT)]
+    yd = [torch.empty((B, N), device=dev) for _ in range(rmv)]
     xq = [torch.empty(mq.act_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(ROT)]
     ym = [torch.empty((M, N), device=dev) for _ in range(ROT)]
-    stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    def step(i):
+        # one pass of the hot path: a decode matvec, then a prefill (quantise + MMQ); the
+        # prefill's ~180 MB of traffic evicts the next decode weight from L2
         r = i % ROT
-        if ev is not None:
-            ev[0].record(stream)
-        mq.matvec(Ws[r], xd[r], yd[r], stream)
-        if ev is not None:
-            ev[1].record(stream)
-        mq.quantize_act(xa[r], xq[r], stream)
-        if ev is not None:
-            ev[2].record(stream)
-        mq.mmq(Ws[r], xq[r], M, ym[r], stream)
-        if ev is not None:
-            ev[3].record(stream)
+        mq.matvec(Wd[i % rmv], xd[r], yd[i % rmv])
+        mq.quantize_act(xa[r], xq[r])
+        mq.mmq(Wp[r], xq[r], M, ym[r])
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    mq.stream_status(stream)
+    mq.stream_status()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # the K timed steps, captured once as a CUDA graph (no host launch gaps)
+    g_steps = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_steps):
+        for i in range(args.steps):
+            step(i)
+    g_steps.replay()  # untimed warm replay
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i, evs[i])
-        e1.record(stream)
+        e0.record()
+        g_steps.replay()
+        e1.record()
         torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    mq.stream_status(stream)
+    mq.stream_status()
     total_ms = e0.elapsed_time(e1)
-    t_mv = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    t_q = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    t_mm = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    del g_steps
+
+    # per-kernel device times: back-to-back calls on rotating buffers, graph replays
+    t_mv = graph_time_ms(lambda j: mq.matvec(Wd[j % rmv], xd[j % ROT], yd[j % rmv]), 5 * rmv)
+    t_q = graph_time_ms(lambda j: mq.quantize_act(xa[j % ROT], xq[j % ROT]), 4 * ROT)
+    t_mm = graph_time_ms(lambda j: mq.mmq(Wp[j % ROT], xq[j % ROT], M, ym[j % ROT]), 2 * ROT)
+    mq.stream_status()
     times = torch.tensor([total_ms, t_mv, t_q, t_mm], dtype=torch.float64, device=dev)
     if ws > 1:
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     total_ms, t_mv, t_q, t_mm = times.tolist()
 
-    # end to end through the public API: pinned host inputs in, results back out
+    # end to end through the public API, eager: pinned host inputs in, results back out
+    stream = torch.cuda.current_stream()
     xd_p = torch.from_numpy(xd_h).pin_memory()
     xa_p = torch.from_numpy(xa_h).pin_memory()
     yd_p = torch.empty((B, N), dtype=torch.float32).pin_memory()
@@ -288,12 +318,12 @@ def main():
         r = i % ROT
         ev[0].record(stream)
         xd[r].copy_(xd_p, non_blocking=True)
-        mq.matvec(Ws[r], xd[r], yd[r], stream)
-        yd_p.copy_(yd[r], non_blocking=True)
+        mq.matvec(Wd[i % rmv], xd[r], yd[i % rmv], stream)
+        yd_p.copy_(yd[i % rmv], non_blocking=True)
         ev[1].record(stream)
         xa[r].copy_(xa_p, non_blocking=True)
         mq.quantize_act(xa[r], xq[r], stream)
-        mq.mmq(Ws[r], xq[r], M, ym[r], stream)
+        mq.mmq(Wp[r], xq[r], M, ym[r], stream)
         ym_p.copy_(ym[r], non_blocking=True)
         ev[2].record(stream)
 
@@ -304,13 +334,12 @@ def main():
     for i in range(args.steps):
         e2e_step(i, eev[i])
     torch.cuda.synchronize()
-    te_mv = sum(e[0].elapsed_time(e[1]) for e in eev) / args.steps
-    te_mm = sum(e[1].elapsed_time(e[2]) for e in eev) / args.steps
+    te_mv = statistics.median(e[0].elapsed_time(e[1]) for e in eev)
+    te_mm = statistics.median(e[1].elapsed_time(e[2]) for e in eev)
     te = torch.tensor([te_mv, te_mm], dtype=torch.float64, device=dev)
     if ws > 1:
         torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
     te_mv, te_mm = te.tolist()
-    # results of the last e2e step must match the device-only path's buffers
     assert np.isfinite(yd_p.numpy()).all() and np.isfinite(ym_p.numpy()).all()
 
     hbm, bf16, peak_src = peaks()
@@ -327,7 +356,7 @@ def main():
                      "peak": hbm, "unit": "GB/s", "frac": q_gbs / hbm,
                      "traffic": traffic_for("quantize_m512", os.path.join(csrc, "quantize.cu")),
                      "ms": t_q, "algorithmic_bytes": Q_BYTES},
-        "mmq": {"kernel": "mmq_kernel<Q4_K>", "bound": "tensor", "achieved": mm_tops,
+        "mmq": {"kernel": "mmq_tc_kernel<Q4_K>", "bound": "tensor", "achieved": mm_tops,
                 "peak": bf16, "unit": "TFLOP/s", "frac": mm_tops / bf16,
                 "traffic": traffic_for("mmq_q4_k_m512", os.path.join(csrc, "mmq.cu")),
                 "ms": t_mm, "algorithmic_ops": MMQ_OPS},
@@ -345,7 +374,10 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
         "data": "synthetic (seeded, Qwen2.5-7B FFN-shaped Q4_K weights, N(0,1) activations)",
         "config": {"workload": WORKLOAD, "N": N, "K": K, "decode_B": B, "prefill_M": M,
-                   "l2": f"rotating {ROT} buffer sets (weights + activations, > 3x L2)",
+                   "l2": (f"inputs larger than L2: {rmv} decode weight copies rotated; each timed "
+                          f"step's prefill moves ~180 MB between decode calls"),
+                   "timing": ("steps: one CUDA graph of K steps; per-kernel: graph replays of "
+                              "back-to-back calls on rotating buffers, median of 5"),
                    "parallelism": f"replicas x{ws}"},
         "matvec_gbs": mv_gbs * ws, "matvec_frac_of_hbm": mv_gbs / hbm,
         "matvec_frac_of_8tbs": mv_gbs / 8000.0,
@@ -356,8 +388,8 @@ def main():
                 "h2d_bytes_per_step": B * K * 4 + M * K * 4,
                 "d2h_bytes_per_step": B * N * 4 + M * N * 4,
                 "mmq_tops": e2e_mm * ws,
-                "note": "matvec: pinned H2D of x + matvec + D2H of y; prefill: H2D of x + "
-                        "quantise + MMQ + D2H of y, per step, events on the stream"},
+                "note": "eager calls through the public API; matvec: pinned H2D of x + matvec + "
+                        "D2H of y; prefill: H2D of x + quantise + MMQ + D2H of y; medians"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
@@ -365,7 +397,7 @@ def main():
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line))
-    for w in Ws:
+    for w in Wd + Wp:
         w.free()
     if ws > 1:
         torch.distributed.destroy_process_group()
