@@ -221,6 +221,39 @@ def graph_time_ms(fn, calls, trials=5):
     return statistics.median(out)
 
 
+def profile_calls(kernel: str, calls: int):
+    """Run `calls` launches of one hot-path kernel on the bench workload and exit: the
+    program that ncu captures are taken of (one kernel, few launches, ~0.3 GB on device)."""
+    import torch
+
+    import gguf_block_quantized_q4_gb300 as mq
+    from gguf_block_quantized_q4_gb300 import build as mqbuild
+    import synth
+    mqbuild.build()
+    mq.init(0)
+    Wb = synth.weights(QTYPE, N, K, W_SEED)
+    flags = mq.REG_NO_MMQ_PLANE if kernel == "matvec" else mq.REG_DEFAULT
+    W = mq.register_weight(QTYPE, Wb, N, K, flags)
+    if kernel == "matvec":
+        x = torch.from_numpy(synth.activations(B, K, XD_SEED)).cuda()
+        y = torch.empty((B, N), device="cuda")
+        for _ in range(calls):
+            mq.matvec(W, x, y)
+    else:
+        x = torch.from_numpy(synth.activations(M, K, XA_SEED)).cuda()
+        xq = mq.quantize_act(x)
+        y = torch.empty((M, N), device="cuda")
+        for _ in range(calls):
+            if kernel == "quantize":
+                mq.quantize_act(x, xq)
+            else:
+                mq.mmq(W, xq, M, y)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    W.free()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -228,7 +261,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
+                    help="profiling mode: only run --calls launches of this kernel")
+    ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args()
+    if args.kernel:
+        return profile_calls(args.kernel, args.calls)
     if args.impl == "reference":
         return run_reference(args)
     args.warmup = max(args.warmup, 3)
