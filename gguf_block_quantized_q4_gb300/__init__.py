@@ -167,7 +167,9 @@ def act_layout(M: int, K: int):
     o["op"] = al(o["bsum"] + M * nb * 4)
     o["scaleT"] = al(o["op"] + M * K * 2)
     o["minT"] = al(o["scaleT"] + mt * nb * 4)
-    o["total"] = al(o["minT"] + mt * nb * 4)
+    o["amin"] = al(o["minT"] + mt * nb * 4)
+    o["urow"] = al(o["amin"] + M * 3 * nb * 2)
+    o["total"] = al(o["urow"] + mt * 4)
     o["mt"] = mt
     return o
 
@@ -193,6 +195,16 @@ def act_views_transposed(xq, M: int, K: int):
     st = xq[o["scaleT"]:o["scaleT"] + mt * nb * 4].view(torch.float32).view(nb, mt)[:, :M]
     tt = xq[o["minT"]:o["minT"] + mt * nb * 4].view(torch.float32).view(nb, mt)[:, :M]
     return st, tt
+
+
+def act_views_min(xq, M: int, K: int):
+    """Views (amin f16 [M][3*K/32], urow f32 [M]) of the min-term operand sections."""
+    import torch
+    o = act_layout(M, K)
+    nb = K // 32
+    am = xq[o["amin"]:o["amin"] + M * 3 * nb * 2].view(torch.float16).view(M, 3 * nb)
+    ur = xq[o["urow"]:o["urow"] + M * 4].view(torch.float32)
+    return am, ur
 
 
 def quantize_act(x, xq=None, stream=None):

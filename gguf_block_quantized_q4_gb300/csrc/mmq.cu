@@ -21,19 +21,30 @@
 //               blocks, 1-D bulk copies of the tile's row scales s and s*S and
 //               column scales d and dmin*m_j into a 2-slot ring.
 //     warps 1,2 MMA issuers (warp 1 also owns TMEM: 512 columns = two pairs of
-//               128-column f32 accumulators).  Issuer i takes the pairs p with
-//               p % 2 == i and accumulator pair i: 4 (Q6_K: 8) tcgen05.mma M=128
-//               N=128 K=16, one block per accumulator, then tcgen05.commit to the
-//               stage's "empty" and the accumulator pair's "full" barrier.  Two
-//               issuers keep the tensor pipe fed while the other one waits.
+//               128-column f32 accumulators).  The accumulator uses alternate
+//               between them (issuer i, accumulator pair i): per pair of blocks
+//               4 (Q6_K: 8) tcgen05.mma M=128 N=128 K=16, one block per
+//               accumulator, then tcgen05.commit to the stage's "empty" and the
+//               accumulator pair's "full" barrier.  Two issuers keep the tensor
+//               pipe fed while the other one waits.  Each issuer owns half of the
+//               ring (stages i, i+2, ...) and the producer fills the stages in the
+//               order of the uses, so every stage is consumed by one issuer, round
+//               after round: a parity wait never sees a phase two rounds old.
 //   warpgroups 1-2 (registers raised to 240): 8 epilogue warps.  Warp w reads
 //               TMEM lanes 32*(w%4).. (its 32 rows) and 64 of the 128 columns;
 //               per block it loads the accumulator (tcgen05.ld, both halves in
 //               flight, one wait) and promotes it in registers:
 //                 Q8_0: y += (s_m * d_n) * D
-//                 Q4_K: a += s_m * D;  y -= (s_m * S_m) * (dmin*m_j)_n; per super-block y += d_n * a
-//                 Q6_K: a += s_m * D;  per super-block y += d_n * a
+//                 Q4_K, Q6_K: a = s_m * D (first block of a super-block), then
+//                             a += s_m * D; per super-block y += d_n * a
 //               and frees the accumulator pair after its second block.
+// Q4_K min term.  sum_b (s*S)_m,b * (dmin*m_j)_n,b is a product of rank K/32;
+// the tensor cores form it once per tile, after the main loop, from three f16
+// products per block (row side hi | hi | lo of (s*S)/u_m, column side
+// hi | lo | hi of (dmin*m_j)/v_n, u and v powers of two that keep both in f16
+// range; 22 significant bits), staged through the same ring as the last
+// accumulator use.  The epilogue adds y -= u_m * v_n * C_min before the store,
+// so the per-block work is a single multiply-add.
 // All mbarrier waits are bounded (2 s by %globaltimer); an expired wait writes
 // MQ_ERR_TIMEOUT into the device status word read by mq_stream_status.
 // Grid: m-tiles fastest, so concurrently running CTAs share each weight tile
@@ -49,16 +60,19 @@ namespace {
 
 constexpr int TM = 128, TN = 128, TK = 32;
 constexpr int PK = 2 * TK;              // K per pipeline stage (a pair of blocks)
-constexpr int NEPI = 8;                 // epilogue warps
-constexpr int NTHR = 32 * (4 + NEPI);   // 384 threads
+constexpr int NEPI = 16;                // epilogue warps: 4 per TMEM lane quarter
+constexpr int EC = TN * 4 / NEPI;       // accumulator columns per epilogue thread (32)
+constexpr int NTHR = 32 * (4 + NEPI);   // 640 threads
 constexpr uint32_t TMEM_COLS = 512;     // accumulator pair i at columns 256*i .. +256
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kTestWaitNs = 1000000ull;
 constexpr int kTileBytes = TM * PK * 2;  // 16 KB per operand tile and stage
-// launch: 384 threads x 168 registers = 64512; after setmaxnreg the control
-// warpgroup holds 128 x 24 and the epilogue warpgroups 256 x 240 = 64512.
-constexpr int kRegCtl = 24, kRegEpi = 240;
-static_assert(128 * kRegCtl + 256 * kRegEpi <= 384 * 168, "register split exceeds the launch");
+// launch: 640 threads x 96 registers = 61440; after setmaxnreg the control
+// warpgroup holds 128 x 24 and the four epilogue warpgroups 512 x 112 = 60416.
+constexpr int kRegLaunch = 96, kRegCtl = 24, kRegEpi = 112;
+static_assert(128 * kRegCtl + 512 * kRegEpi <= NTHR * kRegLaunch,
+              "register split exceeds the launch");
+static_assert(NTHR * kRegLaunch <= 65536, "launch registers exceed the SM");
 
 template <int TYPE>
 constexpr int stages() {  // 192 KB of operand ring
@@ -67,13 +81,14 @@ constexpr int stages() {  // 192 KB of operand ring
 
 struct TcArgs {
   const float *st;      // [nb][mt] activation block scales, transposed
-  const float *tt;      // [nb][mt] s*S, transposed
   const float *td;      // [nb][np] weight block scale d, transposed
-  const float *tm;      // [nb][np] Q4_K dmin*m_j, transposed
+  const float *urow;    // [mt] Q4_K min-term row factors u_m
+  const float *vcol;    // [np] Q4_K min-term column factors v_n
   float *y;             // [M][N]
   int32_t *D;           // [M][N][nb] (block-dot mode)
   int64_t M, N, mt, np;
   int nb;
+  int nms;              // Q4_K: ring stages of the min-term GEMM (3*nb/64 rounded up)
   int *status;
   int debug_expire;
 };
@@ -99,8 +114,6 @@ struct __align__(1024) TcSmem {
   Slots<__half, ODD ? NST : 0, TN * PK> b2;
   alignas(128) float gsx[2][8][TM];     // per group slot: row scales s
   alignas(128) float gd[2][8][TN];      // column scales d
-  Slots<float, MIN ? 16 : 0, TM> gt;    // row factors s*S (Q4_K), [slot*8 + block]
-  Slots<float, MIN ? 16 : 0, TN> gm;    // column dmin*m_j (Q4_K), [slot*8 + block]
   uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], never;
   uint32_t tmem;
 };
@@ -110,8 +123,7 @@ constexpr bool smem_layout_ok() {
   using S = TcSmem<TYPE>;
   return offsetof(S, a) % 1024 == 0 && offsetof(S, b) % 1024 == 0 &&
          offsetof(S, b2) % 1024 == 0 && offsetof(S, gsx) % 128 == 0 &&
-         offsetof(S, gd) % 128 == 0 && offsetof(S, gt) % 128 == 0 &&
-         offsetof(S, gm) % 128 == 0 && offsetof(S, full) % 8 == 0;
+         offsetof(S, gd) % 128 == 0 && offsetof(S, full) % 8 == 0;
 }
 static_assert(smem_layout_ok<MQ_Q8_0>() && smem_layout_ok<MQ_Q4_K>() &&
                   smem_layout_ok<MQ_Q6_K>(),
@@ -136,29 +148,28 @@ __device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// A probe that may suspend the thread until the phase completes (or a hardware
-// time limit passes), so a waiting warp does not take issue slots from others.
+// A probe that suspends the thread until the phase completes or about 0.1 ms
+// pass, so a waiting warp takes no issue slots from the others.
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(a), "r"(parity)
+      : "r"(a), "r"(parity), "r"(100000)
       : "memory");
   return ok != 0;
 }
 // Bounded wait on an mbarrier phase.  On expiry: record (timeout, site) in the
 // status word and return false; the caller carries on so the kernel ends.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *status, int site,
-                                          uint64_t limit_ns, unsigned sleep_ns = 0) {
+                                          uint64_t limit_ns) {
   if (mbar_probe(a, parity)) return true;
   const uint64_t t0 = gtime();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i) {
       if (mbar_try(a, parity)) return true;
-      if (sleep_ns) __nanosleep(sleep_ns);
     }
     if (gtime() - t0 > limit_ns) {
       if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
@@ -210,6 +221,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -232,9 +256,11 @@ __device__ __forceinline__ void tc_fence_after() {
 template <int TYPE, bool DOTS>
 __global__ void __launch_bounds__(NTHR, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
-                  const __grid_constant__ CUtensorMap tW2, const TcArgs p) {
+                  const __grid_constant__ CUtensorMap tW2, const __grid_constant__ CUtensorMap tAm,
+                  const __grid_constant__ CUtensorMap tBm, const TcArgs p) {
   using Sm = TcSmem<TYPE>;
-  constexpr int NST = Sm::NST;
+  constexpr int NST = Sm::NST, SR = NST / 2;  // SR ring stages per MMA issuer
+  static_assert(NST % 2 == 0, "the ring is split between two issuers");
   constexpr bool ODD = Sm::ODD, MIN = Sm::MIN;
   extern __shared__ uint8_t smem_raw[];
   Sm &sm = *reinterpret_cast<Sm *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -242,6 +268,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = int64_t(blockIdx.x) * TM, n0 = int64_t(blockIdx.y) * TN;
   const int nb = p.nb, npairs = (nb + 1) / 2;
+  // accumulator uses in order: pair pr = use pr, then the Q4_K min-term GEMM (use npairs)
+  const int nms = (MIN && !DOTS) ? p.nms : 0, nuse = npairs + (nms > 0 ? 1 : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -272,26 +300,31 @@ __global__ void __launch_bounds__(NTHR, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
-      for (int pr = 0; pr < npairs; ++pr) {
-        if (!DOTS && (pr & 3) == 0) {  // group g = pr/4 of 8 blocks
+      // Fills in the order of the accumulator uses: use pr = pair pr, then use npairs
+      // = the nms min-term stages (Q4_K).  Use u belongs to issuer u % 2, whose c-th
+      // stage is ring stage (u % 2) + 2 * (c % SR), round c / SR.
+      int c0 = 0, c1 = 0;
+      for (int f = 0; f < npairs + nms; ++f) {
+        const int pr = f < npairs ? f : -1, u = f < npairs ? f : npairs, i = u & 1;
+        const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
+        if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group g = pr/4 of 8 blocks
           const int g = pr >> 2, slot = g & 1, nbl = min(8, nb - 8 * g);
           if (g >= 2)
-            mbar_wait(sa(&sm.gempty[slot]), ((g >> 1) - 1) & 1, p.status, 5, kWaitNs, 64);
-          mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * (MIN ? 4u : 2u));
+            mbar_wait(sa(&sm.gempty[slot]), ((g >> 1) - 1) & 1, p.status, 5, kWaitNs);
+          mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * 2u);
           for (int bi = 0; bi < nbl; ++bi) {
             const int64_t b = 8 * g + bi;
             bulk_1d(sa(sm.gsx[slot][bi]), p.st + b * p.mt + m0, 512, sa(&sm.gfull[slot]));
             bulk_1d(sa(sm.gd[slot][bi]), p.td + b * p.np + n0, 512, sa(&sm.gfull[slot]));
-            if constexpr (MIN) {
-              bulk_1d(sa(sm.gt.v[MIN ? 8 * slot + bi : 0]), p.tt + b * p.mt + m0, 512,
-                      sa(&sm.gfull[slot]));
-              bulk_1d(sa(sm.gm.v[MIN ? 8 * slot + bi : 0]), p.tm + b * p.np + n0, 512,
-                      sa(&sm.gfull[slot]));
-            }
           }
         }
-        const int s = pr % NST;
-        if (pr >= NST) mbar_wait(sa(&sm.empty[s]), ((pr / NST) - 1) & 1, p.status, 1, kWaitNs, 64);
+        if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 1, kWaitNs);
+        if (pr < 0) {  // min-term operands: 64 columns of the [hi|hi|lo] x [hi|lo|hi] planes
+          mbar_expect_tx(sa(&sm.full[s]), 2 * kTileBytes);
+          tma_2d(sa(sm.a[s]), &tAm, (f - npairs) * PK, (int)m0, sa(&sm.full[s]));
+          tma_2d(sa(sm.b[s]), &tBm, (f - npairs) * PK, (int)n0, sa(&sm.full[s]));
+          continue;
+        }
         mbar_expect_tx(sa(&sm.full[s]), bytes);
         tma_2d(sa(sm.a[s]), &tA, pr * PK, (int)m0, sa(&sm.full[s]));
         tma_2d(sa(sm.b[s]), &tW, pr * PK, (int)n0, sa(&sm.full[s]));
@@ -301,10 +334,27 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int i = warp - 1;
       const uint32_t idesc = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
       const uint32_t acc0 = tmem + (uint32_t)(256 * i);
-      for (int pr = i; pr < npairs; pr += 2) {
-        const int s = pr % NST, use = pr >> 1;  // use: this issuer's pair count
-        mbar_wait(sa(&sm.full[s]), (pr / NST) & 1, p.status, 2, kWaitNs);
-        if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs, 32);
+      int c = 0;  // this issuer's stage count (its half of the ring)
+      for (int u = i; u < nuse; u += 2) {  // accumulator slot i, uses u = i, i+2, ...
+        const int use = u >> 1;             // this issuer's use count
+        if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs);
+        if (u == npairs) {  // the min-term GEMM over nms ring stages into columns acc0 .. +128
+          for (int k = 0; k < nms; ++k, ++c) {
+            const int s = i + 2 * (c % SR);
+            mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
+            tc_fence_after();
+            const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16(acc0, ad + 2 * kk, bd + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(sa(&sm.empty[s]));
+          }
+          mma_commit(sa(&sm.tfull[i]));
+          continue;
+        }
+        const int pr = u, s = i + 2 * (c % SR);
+        mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
+        ++c;
         tc_fence_after();
         const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
 #pragma unroll
@@ -325,102 +375,117 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {  // ---- epilogue warps
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
-    const int e = warp - 4, q = warp & 3, hcol = e >> 2;
+    const int e = warp - 4, q = warp & 3, hcol = e >> 2;  // rows 32q.., columns EC*hcol..
     const int rl = 32 * q + lane;
     const int64_t m = m0 + rl;
     const bool mok = m < p.M;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * hcol);
-    float acc[64], y[64];
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
+    float acc[EC], y[EC];
 #pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = y[j] = 0.f;
-    for (int pr = 0; pr < npairs; ++pr) {
-      const int i = pr & 1, use = pr >> 1;
-      const int g = pr >> 2, slot = g & 1;
-      if (!DOTS && (pr & 3) == 0)
-        mbar_wait(sa(&sm.gfull[slot]), (g >> 1) & 1, p.status, 6, kWaitNs);
-      if (pr == 0 && p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
-      mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
-      tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int b = 2 * pr + h;
-        if (b >= nb) break;
-        const int bi = b & 7;
-        uint32_t r[64];
-        TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
-        TC_LD32(trow + (uint32_t)(256 * i + 128 * h + 32), (r + 32));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if constexpr (DOTS) {
-          if (mok) {
+    for (int j = 0; j < EC; ++j) acc[j] = y[j] = 0.f;
+    // Groups of 8 blocks (4 pairs; a Q4_K / Q6_K super-block), unrolled so that the
+    // accumulator slot, the block's place in the group and every shared-memory
+    // offset are compile-time constants.
+    const int ngroups = (nb + 7) >> 3;
+    const uint32_t gsx0 = sa(&sm.gsx[0][0][rl]), gd0 = sa(&sm.gd[0][0][EC * hcol]);
+    for (int g = 0; g < ngroups; ++g) {
+      const int slot = g & 1;
+      if (!DOTS) mbar_wait(sa(&sm.gfull[slot]), (g >> 1) & 1, p.status, 6, kWaitNs);
+      const uint32_t gsx = gsx0 + (uint32_t)(slot * 8 * TM * 4);
+      const uint32_t gd = gd0 + (uint32_t)(slot * 8 * TN * 4);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int64_t n = n0 + 64 * hcol + j;
-              if (n < p.N) p.D[(m * p.N + n) * nb + b] = __float2int_rn(__uint_as_float(r[j]));
-            }
-          }
-        } else {
-          const float sxv = sm.gsx[slot][bi][rl];
-          const float4 *cd4 = reinterpret_cast<const float4 *>(&sm.gd[slot][bi][64 * hcol]);
-          if constexpr (TYPE == MQ_Q8_0) {
+      for (int pp = 0; pp < 4; ++pp) {
+        const int pr = 4 * g + pp;
+        if (TYPE == MQ_Q8_0 && pr >= npairs) break;  // K % 256 == 0 for the K-quants
+        const int i = pp & 1, use = pr >> 1;
+        if (pr == 0 && p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
+        mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
+        tc_fence_after();
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 c = cd4[j4];
-              y[4 * j4 + 0] = fmaf(sxv * c.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
-              y[4 * j4 + 1] = fmaf(sxv * c.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
-              y[4 * j4 + 2] = fmaf(sxv * c.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
-              y[4 * j4 + 3] = fmaf(sxv * c.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
+        for (int h = 0; h < 2; ++h) {
+          const int bi = 2 * pp + h, b = 8 * g + bi;
+          if (TYPE == MQ_Q8_0 && b >= nb) break;
+          uint32_t r[EC];
+          TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if constexpr (DOTS) {
+            if (mok) {
+#pragma unroll
+              for (int j = 0; j < EC; ++j) {
+                const int64_t n = n0 + EC * hcol + j;
+                if (n < p.N) p.D[(m * p.N + n) * nb + b] = __float2int_rn(__uint_as_float(r[j]));
+              }
             }
           } else {
-            const float tv = MIN ? -sm.gt.v[MIN ? 8 * slot + bi : 0][MIN ? rl : 0] : 0.f;
-            const float4 *cm4 = reinterpret_cast<const float4 *>(
-                &sm.gm.v[MIN ? 8 * slot + bi : 0][MIN ? 64 * hcol : 0]);
+            const float sxv = lds_f32(gsx + (uint32_t)(bi * TM * 4));
+            if constexpr (TYPE == MQ_Q8_0) {  // y += (s_m * d_n) * D per block
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {  // columns 4*j4 .. 4*j4+3
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                acc[4 * j4 + u] = fmaf(sxv, __uint_as_float(r[4 * j4 + u]), acc[4 * j4 + u]);
-              if constexpr (MIN) {
-                const float4 c = cm4[j4];
-                y[4 * j4 + 0] = fmaf(tv, c.x, y[4 * j4 + 0]);
-                y[4 * j4 + 1] = fmaf(tv, c.y, y[4 * j4 + 1]);
-                y[4 * j4 + 2] = fmaf(tv, c.z, y[4 * j4 + 2]);
-                y[4 * j4 + 3] = fmaf(tv, c.w, y[4 * j4 + 3]);
+              for (int j4 = 0; j4 < EC / 4; ++j4) {
+                const float4 c = lds_f4(gd + (uint32_t)((bi * TN + 4 * j4) * 4));
+                y[4 * j4 + 0] = fmaf(sxv * c.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
+                y[4 * j4 + 1] = fmaf(sxv * c.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
+                y[4 * j4 + 2] = fmaf(sxv * c.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
+                y[4 * j4 + 3] = fmaf(sxv * c.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
               }
-            }
-            if (bi == 7 || b == nb - 1) {  // end of a super-block: y += d * a
+            } else {
+              if (bi == 0) {  // first block of the super-block
 #pragma unroll
-              for (int j4 = 0; j4 < 16; ++j4) {
-                const float4 c = cd4[j4];
-                y[4 * j4 + 0] = fmaf(c.x, acc[4 * j4 + 0], y[4 * j4 + 0]);
-                y[4 * j4 + 1] = fmaf(c.y, acc[4 * j4 + 1], y[4 * j4 + 1]);
-                y[4 * j4 + 2] = fmaf(c.z, acc[4 * j4 + 2], y[4 * j4 + 2]);
-                y[4 * j4 + 3] = fmaf(c.w, acc[4 * j4 + 3], y[4 * j4 + 3]);
+                for (int j = 0; j < EC; ++j) acc[j] = sxv * __uint_as_float(r[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < EC; ++j) acc[j] = fmaf(sxv, __uint_as_float(r[j]), acc[j]);
               }
+              if (bi == 7) {  // end of the super-block: y += d * a
 #pragma unroll
-              for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+                for (int j4 = 0; j4 < EC / 4; ++j4) {
+                  const float4 c = lds_f4(gd + (uint32_t)((7 * TN + 4 * j4) * 4));
+                  y[4 * j4 + 0] = fmaf(c.x, acc[4 * j4 + 0], y[4 * j4 + 0]);
+                  y[4 * j4 + 1] = fmaf(c.y, acc[4 * j4 + 1], y[4 * j4 + 1]);
+                  y[4 * j4 + 2] = fmaf(c.z, acc[4 * j4 + 2], y[4 * j4 + 2]);
+                  y[4 * j4 + 3] = fmaf(c.w, acc[4 * j4 + 3], y[4 * j4 + 3]);
+                }
+              }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
-      if (!DOTS && ((pr & 3) == 3 || pr == npairs - 1)) {
+      if (!DOTS) {
         __syncwarp();
         if (lane == 0) mbar_arrive(sa(&sm.gempty[slot]));
       }
     }
+    if (nuse > npairs) {  // y -= u_m * v_n * C_min (the last accumulator use)
+      const int i = npairs & 1;
+      mbar_wait(sa(&sm.tfull[i]), (npairs >> 1) & 1, p.status, 7, kWaitNs);
+      tc_fence_after();
+      uint32_t r[EC];
+      TC_LD32(trow + (uint32_t)(256 * i), r);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const float um = mok ? -p.urow[m] : 0.f;
+      const float4 *v4 = reinterpret_cast<const float4 *>(p.vcol + n0 + EC * hcol);
+#pragma unroll
+      for (int j4 = 0; j4 < EC / 4; ++j4) {
+        const float4 v = __ldg(v4 + j4);
+        y[4 * j4 + 0] = fmaf(um * v.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
+        y[4 * j4 + 1] = fmaf(um * v.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
+        y[4 * j4 + 2] = fmaf(um * v.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
+        y[4 * j4 + 3] = fmaf(um * v.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
+      }
+    }
     if constexpr (!DOTS) {
       if (mok) {
-        float *dst = p.y + m * p.N + n0 + 64 * hcol;
-        const int64_t left = p.N - (n0 + 64 * hcol);
-        if (left >= 64 && (p.N & 3) == 0) {
+        float *dst = p.y + m * p.N + n0 + EC * hcol;
+        const int64_t left = p.N - (n0 + EC * hcol);
+        if (left >= EC && (p.N & 3) == 0) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 4)
+          for (int j = 0; j < EC; j += 4)
             *reinterpret_cast<float4 *>(dst + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
+          for (int j = 0; j < EC; ++j)
             if (j < left) dst[j] = y[j];
         }
       }
@@ -490,8 +555,8 @@ mq_status optin_t(const DeviceState *st, const char *name) {
 }
 
 template <int TYPE, bool DOTS>
-mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const TcArgs &a, cudaStream_t s,
-                   const char *name) {
+mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap &tAm,
+                   const TcArgs &a, cudaStream_t s, const char *name) {
   dim3 grid((unsigned)((a.M + TM - 1) / TM), (unsigned)((a.N + TN - 1) / TN));
   if (grid.y > 65535)
     return fail(MQ_ERR_SHAPE, "%s: N=%lld needs more than 65535 column tiles", name,
@@ -499,7 +564,9 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const TcArgs &a, c
   const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
   const CUtensorMap &tW2 = *reinterpret_cast<const CUtensorMap *>(
       TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);
-  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, a);
+  const CUtensorMap &tBm = *reinterpret_cast<const CUtensorMap *>(
+      TYPE == MQ_Q4_K && !DOTS ? W->tmap_mb : W->tmap_w);
+  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, a);
   MQ_LAUNCH_CHECK(name);
   return MQ_OK;
 }
@@ -514,6 +581,9 @@ mq_status encode_weight_maps(mq_weight *w) {
   if (w->mw2)
     s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w2), w->mw2, w->N, w->K,
                        "weight odd-part");
+  if (s == MQ_OK && w->mb)
+    s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_mb), w->mb, w->np,
+                       3 * (w->K / 32), "weight min-term");
   return s;
 }
 
@@ -533,14 +603,20 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
                      cudaStream_t s, const DeviceState *st, int debug_expire) {
   const ActLayout L = act_layout(M, W->K);
   const uint8_t *base = reinterpret_cast<const uint8_t *>(xq);
-  alignas(64) CUtensorMap tA;
+  alignas(64) CUtensorMap tA, tAm;
   mq_status r = encode_f16_map(&tA, base + L.op, M, W->K, "activation");
   if (r != MQ_OK) return r;
+  const bool mins = W->type == MQ_Q4_K && D == nullptr;
+  if (mins && (r = encode_f16_map(&tAm, base + L.amin, M, 3 * (W->K / 32), "activation min-term")) !=
+                  MQ_OK)
+    return r;
+  if (!mins) tAm = tA;
   TcArgs a;
   a.st = reinterpret_cast<const float *>(base + L.st);
-  a.tt = reinterpret_cast<const float *>(base + L.tt);
   a.td = W->td;
-  a.tm = W->tm;
+  a.urow = reinterpret_cast<const float *>(base + L.urow);
+  a.vcol = W->vcol;
+  a.nms = mins ? (int)((3 * (W->K / 32) + PK - 1) / PK) : 0;
   a.y = y;
   a.D = D;
   a.M = M;
@@ -553,14 +629,14 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
-      return dots ? launch_t<MQ_Q4_K, true>(W, tA, a, s, "mmq_tc_kernel<Q4_K,dots>")
-                  : launch_t<MQ_Q4_K, false>(W, tA, a, s, "mmq_tc_kernel<Q4_K>");
+      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q4_K,dots>")
+                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q4_K>");
     case MQ_Q6_K:
-      return dots ? launch_t<MQ_Q6_K, true>(W, tA, a, s, "mmq_tc_kernel<Q6_K,dots>")
-                  : launch_t<MQ_Q6_K, false>(W, tA, a, s, "mmq_tc_kernel<Q6_K>");
+      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q6_K,dots>")
+                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q6_K>");
     default:
-      return dots ? launch_t<MQ_Q8_0, true>(W, tA, a, s, "mmq_tc_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q8_0, false>(W, tA, a, s, "mmq_tc_kernel<Q8_0>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q8_0>");
   }
 }
 

@@ -139,11 +139,11 @@ static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t
 }
 
 static mq_status free_planes(mq_weight *w) {
-  void *ps[] = {w->q, w->d, w->mw, w->mw2, w->td, w->tm};
+  void *ps[] = {w->q, w->d, w->mw, w->mw2, w->td, w->tm, w->mb, w->vcol};
   for (void *p : ps)
     if (p) cudaFree(p);
   w->q = nullptr; w->d = nullptr; w->mw = nullptr;
-  w->mw2 = nullptr; w->td = nullptr; w->tm = nullptr;
+  w->mw2 = nullptr; w->td = nullptr; w->tm = nullptr; w->mb = nullptr; w->vcol = nullptr;
   return MQ_OK;
 }
 
@@ -224,6 +224,12 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
     // the padding columns of the transposed planes must read as zero
     cudaMemsetAsync(w->td, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
     if (w->tm) cudaMemsetAsync(w->tm, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
+    if (type == MQ_Q4_K) {
+      if ((s = zalloc(&w->mb, size_t(w->np) * 3 * (K / 32) * 2, "prefill min operand")) != MQ_OK)
+        return cleanup(s);
+      if ((s = zalloc(&w->vcol, size_t(w->np) * 4, "prefill min scale")) != MQ_OK)
+        return cleanup(s);
+    }
   }
   w->device_bytes = total;
 

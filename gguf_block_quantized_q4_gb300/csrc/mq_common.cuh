@@ -32,6 +32,10 @@
 //   td     f32  [K/32][Np] block scale d of each 32-element block (transposed;
 //                          Np = N rounded up to 128, the padding is zero)
 //   tm     f32  [K/32][Np] Q4_K only: dmin*m_j of each block (transposed)
+//   mb     f16  [Np][3*K/32] Q4_K only: min-term operand, row n holds hi | lo | hi over
+//                          the blocks of m~ = dmin*m_j / v_n (hi = f16(m~), lo = f16(m~ - hi))
+//   vcol   f32  [Np]       Q4_K only: v_n, a power of two with max_b |dmin*m_j| / v_n in
+//                          [2^13, 2^14) (0 for the padding rows)
 #pragma once
 
 #include <cstddef>
@@ -58,8 +62,11 @@ struct mq_weight {
   __half *mw2 = nullptr;
   float *td = nullptr;
   float *tm = nullptr;
+  __half *mb = nullptr;
+  float *vcol = nullptr;
   alignas(64) unsigned char tmap_w[128];   // TMA descriptors of w and w2 (CUtensorMap)
   alignas(64) unsigned char tmap_w2[128];
+  alignas(64) unsigned char tmap_mb[128];
 };
 
 namespace mq {
@@ -99,9 +106,11 @@ mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 // xq buffer layout (mq_act_bytes): q int8 [M][K], s f32 [M][K/32], S int32
 // [M][K/32], q as f16 [M][K], then the transposed block scales sT f32
 // [K/32][Mt] and the min-term factors tT = s*S f32 [K/32][Mt], Mt = M rounded up
-// to 128 (the epilogue's tile rows are one contiguous 512-byte run per block).
+// to 128 (the epilogue's tile rows are one contiguous 512-byte run per block);
+// then the min-term operand f16 [M][3*K/32] (row m: t~hi | t~hi | t~lo over the
+// blocks, t~ = s*S/u_m) and the row factors u_m f32 [Mt] (powers of two).
 struct ActLayout {
-  size_t qs, scale, bsum, op, st, tt, total;
+  size_t qs, scale, bsum, op, st, tt, amin, urow, total;
   int64_t mt;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -115,7 +124,9 @@ inline ActLayout act_layout(int64_t M, int64_t K) {
   L.op = align256(L.bsum + size_t(M) * (K / 32) * 4);
   L.st = align256(L.op + size_t(M) * K * 2);
   L.tt = align256(L.st + size_t(L.mt) * (K / 32) * 4);
-  L.total = align256(L.tt + size_t(L.mt) * (K / 32) * 4);
+  L.amin = align256(L.tt + size_t(L.mt) * (K / 32) * 4);
+  L.urow = align256(L.amin + size_t(M) * 3 * (K / 32) * 2);
+  L.total = align256(L.urow + size_t(L.mt) * 4);
   return L;
 }
 

@@ -8,70 +8,103 @@
 //   q = round_half_even(x / s) clamped to [-127, 127], or 0 when s == 0;
 //   S = sum q.
 // Writes every section of the xq buffer (mq_act_bytes): q as int8, s as f32,
-// S as int32, q as f16 (the tensor-core operand of mq_mmq), and the transposed
-// s and s*S planes the MMQ epilogue stages per 128-row tile.
+// S as int32, q as f16 (the tensor-core operand of mq_mmq), the transposed s and
+// s*S planes the MMQ epilogue stages per 128-row tile, and the min-term operand:
+// per row a power of two u_m with max_b |s*S| / u_m in [2^13, 2^14) and the f16
+// pair (hi, lo) of t~ = s*S / u_m per block (hi + lo carries 22 bits), laid out as
+// [hi | hi | lo] so that the MMQ's tensor cores form the min term
+// sum_b t~ * (dmin*m_j~) from three exact f16 products per block.
 //
-// Memory-bound: 8 threads per block, 4 elements (one float4) per thread; the
-// block's max and sum reduce over the 8 lanes with shuffles.
+// One CTA per row: 8 threads per block, 4 elements (one float4) per thread, 32
+// blocks per pass; the block's max and sum reduce over the 8 lanes with
+// shuffles, the row maximum of |s*S| over the CTA.
 #include "mq_common.cuh"
 
 namespace mq {
 namespace {
 
+constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared memory
+
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x,
                                                            uint8_t *__restrict__ xq, int64_t M,
                                                            int64_t K, ActLayout L) {
-  const int64_t nblk = M * (K / 32);
-  const int64_t gt = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-  const int64_t blk = gt >> 3;  // global block index m*(K/32) + b
-  const int sub = threadIdx.x & 7;
-  const bool ok = blk < nblk;
-  // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (ok) v = __ldg(reinterpret_cast<const float4 *>(x + blk * 32) + sub);
-  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-  const float s = __fdiv_rn(m, 127.0f);
-  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-  if (s != 0.0f) {
-    q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
-    q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
-    q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
-    q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
+  __shared__ float ttc[kTtCache];
+  __shared__ float wmax[8];
+  const int64_t m = blockIdx.x;
+  const int64_t nb = K / 32;
+  const int tb = threadIdx.x >> 3, sub = threadIdx.x & 7;
+  float rowmax = 0.f;
+  for (int64_t b0 = 0; b0 < nb; b0 += 32) {
+    const int64_t b = b0 + tb;
+    const bool ok = b < nb;
+    const int64_t blk = m * nb + b;  // global block index
+    // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) v = __ldg(reinterpret_cast<const float4 *>(x + blk * 32) + sub);
+    float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    const float s = __fdiv_rn(mx, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    if (s != 0.0f) {
+      q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
+      q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
+      q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
+      q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
+    }
+    int S = q0 + q1 + q2 + q3;
+    S += __shfl_xor_sync(0xffffffffu, S, 1);
+    S += __shfl_xor_sync(0xffffffffu, S, 2);
+    S += __shfl_xor_sync(0xffffffffu, S, 4);
+    if (!ok) continue;
+    const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
+                            ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+    reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
+    __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+    __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+    uint2 hv;
+    hv.x = *reinterpret_cast<uint32_t *>(&h01);
+    hv.y = *reinterpret_cast<uint32_t *>(&h23);
+    reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
+    if (sub == 0) {
+      const float t = s * (float)S;
+      reinterpret_cast<float *>(xq + L.scale)[blk] = s;
+      reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
+      reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
+      reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
+      if (b < kTtCache) ttc[b] = t;
+      rowmax = fmaxf(rowmax, fabsf(t));
+    }
   }
-  int S = q0 + q1 + q2 + q3;
-  S += __shfl_xor_sync(0xffffffffu, S, 1);
-  S += __shfl_xor_sync(0xffffffffu, S, 2);
-  S += __shfl_xor_sync(0xffffffffu, S, 4);
-  if (!ok) return;
-  const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                          ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-  reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-  __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-  __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-  uint2 hv;
-  hv.x = *reinterpret_cast<uint32_t *>(&h01);
-  hv.y = *reinterpret_cast<uint32_t *>(&h23);
-  reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
-  if (sub == 0) {
-    reinterpret_cast<float *>(xq + L.scale)[blk] = s;
-    reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
-    const int64_t nb = K / 32, m = blk / nb, b = blk - m * nb;
-    reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
-    reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = s * (float)S;
+  // row maximum of |s*S| -> u_m = 2^k with max / u_m in [2^13, 2^14)
+  rowmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(rowmax)));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = rowmax;
+  __syncthreads();
+  float mxr = wmax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mxr = fmaxf(mxr, wmax[w]);
+  const int E = (int)((__float_as_uint(mxr) >> 23) & 255);
+  int k = mxr == 0.f ? 0 : E - 140;
+  k = min(max(k, -100), 100);
+  const float inv_u = __int_as_float((127 - k) << 23);
+  if (threadIdx.x == 0) reinterpret_cast<float *>(xq + L.urow)[m] = __int_as_float((127 + k) << 23);
+  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * 3 * nb;
+  for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
+    const float t = (b < kTtCache ? ttc[b] : reinterpret_cast<const float *>(xq + L.tt)[b * L.mt + m]) * inv_u;
+    const __half hi = __float2half_rn(t);
+    const __half lo = __float2half_rn(t - __half2float(hi));
+    arow[b] = hi;
+    arow[nb + b] = hi;
+    arow[2 * nb + b] = lo;
   }
 }
 
 }  // namespace
 
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s) {
-  const int64_t threads = M * (K / 32) * 8;
-  const int T = 256;
-  const int64_t grid = (threads + T - 1) / T;
-  if (grid > 0x7fffffff) return fail(MQ_ERR_SHAPE, "mq_quantize_act: M*K too large");
-  quantize_act_kernel<<<(unsigned)grid, T, 0, s>>>(x, (uint8_t *)xq, M, K, act_layout(M, K));
+  if (M > 0x7fffffff) return fail(MQ_ERR_SHAPE, "mq_quantize_act: M too large");
+  quantize_act_kernel<<<(unsigned)M, 256, 0, s>>>(x, (uint8_t *)xq, M, K, act_layout(M, K));
   MQ_LAUNCH_CHECK("quantize_act_kernel");
   return MQ_OK;
 }

@@ -209,6 +209,32 @@ __global__ void unpack_q6_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
   dst[209] = tile[kRowGroup * 208 + 2 * r + 1];
 }
 
+// Q4_K min-term operand (one thread per weight row n): v_n = 2^k with
+// max_b |dmin*m_j| / v_n in [2^13, 2^14), and m~ = dmin*m_j / v_n split into
+// f16 hi and lo, stored as hi | lo | hi over the blocks (paired with the
+// activation side's hi | hi | lo, the three products hi*hi + hi*lo + lo*hi).
+__global__ void minplane_q4_k(const float *__restrict__ tm, int64_t N, int64_t nb, int64_t NP,
+                              __half *__restrict__ mb, float *__restrict__ vcol) {
+  const int64_t n = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (n >= N) return;
+  float mx = 0.f;
+  for (int64_t b = 0; b < nb; ++b) mx = fmaxf(mx, fabsf(tm[b * NP + n]));
+  const int E = (int)((__float_as_uint(mx) >> 23) & 255);
+  int k = mx == 0.f ? 0 : E - 140;
+  k = min(max(k, -100), 100);
+  const float inv_v = __int_as_float((127 - k) << 23);
+  vcol[n] = __int_as_float((127 + k) << 23);
+  __half *row = mb + n * 3 * nb;
+  for (int64_t b = 0; b < nb; ++b) {
+    const float t = tm[b * NP + n] * inv_v;
+    const __half hi = __float2half_rn(t);
+    const __half lo = __float2half_rn(t - __half2float(hi));
+    row[b] = hi;
+    row[nb + b] = lo;
+    row[2 * nb + b] = hi;
+  }
+}
+
 inline unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
 
 }  // namespace
@@ -226,6 +252,10 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
     repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr, w->td,
                                               w->tm);
     MQ_LAUNCH_CHECK("repack_q4_k");
+    if (mmq) {
+      minplane_q4_k<<<grid_for(N, T), T, 0, s>>>(w->tm, N, K / 32, w->np, w->mb, w->vcol);
+      MQ_LAUNCH_CHECK("minplane_q4_k");
+    }
   } else {
     const int64_t n = N * (K / 256);
     repack_q6_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,

@@ -56,8 +56,8 @@ def test_act_bytes_layout(L):
     M, K = 3, 96
     al = lambda v: (v + 255) & ~255
     mt = 128
-    expect = al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2) + mt * 3 * 4)
-                + mt * 3 * 4)
+    expect = al(al(al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2) + mt * 3 * 4)
+                      + mt * 3 * 4) + M * 3 * 3 * 2) + mt * 4)
     assert L.mq_act_bytes(M, K) == expect == mq.act_layout(M, K)["total"]
     assert L.mq_act_bytes(512, 3584) % 256 == 0
 
