@@ -221,6 +221,10 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+// columns j, j+1 of a tcgen05.ld result as an f32 pair
+__device__ __forceinline__ float2 pair(const uint32_t *r, int j) {
+  return make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+}
 __device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
@@ -380,9 +384,10 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int64_t m = m0 + rl;
     const bool mok = m < p.M;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
-    float acc[EC], y[EC];
+    // accumulators as f32 pairs: one packed fma.rn.f32x2 per two columns
+    float2 acc[EC / 2], y[EC / 2];
 #pragma unroll
-    for (int j = 0; j < EC; ++j) acc[j] = y[j] = 0.f;
+    for (int j = 0; j < EC / 2; ++j) acc[j] = y[j] = make_float2(0.f, 0.f);
     // Groups of 8 blocks (4 pairs; a Q4_K / Q6_K super-block), unrolled so that the
     // accumulator slot, the block's place in the group and every shared-memory
     // offset are compile-time constants.
@@ -418,31 +423,30 @@ __global__ void __launch_bounds__(NTHR, 1)
             }
           } else {
             const float sxv = lds_f32(gsx + (uint32_t)(bi * TM * 4));
+            const float2 sx2 = make_float2(sxv, sxv);
             if constexpr (TYPE == MQ_Q8_0) {  // y += (s_m * d_n) * D per block
 #pragma unroll
               for (int j4 = 0; j4 < EC / 4; ++j4) {
                 const float4 c = lds_f4(gd + (uint32_t)((bi * TN + 4 * j4) * 4));
-                y[4 * j4 + 0] = fmaf(sxv * c.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
-                y[4 * j4 + 1] = fmaf(sxv * c.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
-                y[4 * j4 + 2] = fmaf(sxv * c.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
-                y[4 * j4 + 3] = fmaf(sxv * c.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
+                y[2 * j4] = __ffma2_rn(__fmul2_rn(sx2, make_float2(c.x, c.y)), pair(r, 4 * j4),
+                                       y[2 * j4]);
+                y[2 * j4 + 1] = __ffma2_rn(__fmul2_rn(sx2, make_float2(c.z, c.w)),
+                                           pair(r, 4 * j4 + 2), y[2 * j4 + 1]);
               }
             } else {
               if (bi == 0) {  // first block of the super-block
 #pragma unroll
-                for (int j = 0; j < EC; ++j) acc[j] = sxv * __uint_as_float(r[j]);
+                for (int j = 0; j < EC / 2; ++j) acc[j] = __fmul2_rn(sx2, pair(r, 2 * j));
               } else {
 #pragma unroll
-                for (int j = 0; j < EC; ++j) acc[j] = fmaf(sxv, __uint_as_float(r[j]), acc[j]);
+                for (int j = 0; j < EC / 2; ++j) acc[j] = __ffma2_rn(sx2, pair(r, 2 * j), acc[j]);
               }
               if (bi == 7) {  // end of the super-block: y += d * a
 #pragma unroll
                 for (int j4 = 0; j4 < EC / 4; ++j4) {
                   const float4 c = lds_f4(gd + (uint32_t)((7 * TN + 4 * j4) * 4));
-                  y[4 * j4 + 0] = fmaf(c.x, acc[4 * j4 + 0], y[4 * j4 + 0]);
-                  y[4 * j4 + 1] = fmaf(c.y, acc[4 * j4 + 1], y[4 * j4 + 1]);
-                  y[4 * j4 + 2] = fmaf(c.z, acc[4 * j4 + 2], y[4 * j4 + 2]);
-                  y[4 * j4 + 3] = fmaf(c.w, acc[4 * j4 + 3], y[4 * j4 + 3]);
+                  y[2 * j4] = __ffma2_rn(make_float2(c.x, c.y), acc[2 * j4], y[2 * j4]);
+                  y[2 * j4 + 1] = __ffma2_rn(make_float2(c.z, c.w), acc[2 * j4 + 1], y[2 * j4 + 1]);
                 }
               }
             }
@@ -466,13 +470,13 @@ __global__ void __launch_bounds__(NTHR, 1)
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       const float um = mok ? -p.urow[m] : 0.f;
       const float4 *v4 = reinterpret_cast<const float4 *>(p.vcol + n0 + EC * hcol);
+      const float2 um2 = make_float2(um, um);
 #pragma unroll
       for (int j4 = 0; j4 < EC / 4; ++j4) {
         const float4 v = __ldg(v4 + j4);
-        y[4 * j4 + 0] = fmaf(um * v.x, __uint_as_float(r[4 * j4 + 0]), y[4 * j4 + 0]);
-        y[4 * j4 + 1] = fmaf(um * v.y, __uint_as_float(r[4 * j4 + 1]), y[4 * j4 + 1]);
-        y[4 * j4 + 2] = fmaf(um * v.z, __uint_as_float(r[4 * j4 + 2]), y[4 * j4 + 2]);
-        y[4 * j4 + 3] = fmaf(um * v.w, __uint_as_float(r[4 * j4 + 3]), y[4 * j4 + 3]);
+        y[2 * j4] = __ffma2_rn(__fmul2_rn(um2, make_float2(v.x, v.y)), pair(r, 4 * j4), y[2 * j4]);
+        y[2 * j4 + 1] =
+            __ffma2_rn(__fmul2_rn(um2, make_float2(v.z, v.w)), pair(r, 4 * j4 + 2), y[2 * j4 + 1]);
       }
     }
     if constexpr (!DOTS) {
@@ -481,12 +485,13 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int64_t left = p.N - (n0 + EC * hcol);
         if (left >= EC && (p.N & 3) == 0) {
 #pragma unroll
-          for (int j = 0; j < EC; j += 4)
-            *reinterpret_cast<float4 *>(dst + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+          for (int j = 0; j < EC / 2; j += 2)
+            *reinterpret_cast<float4 *>(dst + 2 * j) =
+                make_float4(y[j].x, y[j].y, y[j + 1].x, y[j + 1].y);
         } else {
 #pragma unroll
           for (int j = 0; j < EC; ++j)
-            if (j < left) dst[j] = y[j];
+            if (j < left) dst[j] = (j & 1) ? y[j >> 1].y : y[j >> 1].x;
         }
       }
     }
