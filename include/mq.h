@@ -139,8 +139,10 @@ mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, 
  *   minT    f32   [K/32][Mt]   s * S transposed, the min-term factor (rows >= M unspecified)
  *   amin    f16   [M][3*K/32]  min-term operand: row m holds hi | hi | lo over the
  *                              blocks b of t = s*S / u_m, hi = f16(t), lo = f16(t - hi)
- *   urow    f32   [Mt]         u_m: a power of two with max_b |s*S| / u_m in [2^13, 2^14)
- *                              (1 when the row's s*S are all 0; rows >= M unspecified)
+ *   urow    f32   [Mt]         u_m = 2^k, k = E - 140 clamped to [-100, 100], E the biased
+ *                              binary32 exponent of max_b |s*S| (so max_b |s*S| / u_m is in
+ *                              [2^13, 2^14) for a normal maximum); k = 0 when the row's s*S
+ *                              are all 0 (rows >= M unspecified)
  * Returns 0 if K is not a positive multiple of 32 or M < 1. */
 size_t mq_act_bytes(int64_t M, int64_t K);
 

@@ -157,6 +157,32 @@ def assert_quant_exact(x):
     st, tt = (v.cpu().numpy() for v in mq.act_views_transposed(xq, *x.shape))
     assert np.array_equal(st.T.view(np.uint32), rs.view(np.uint32))
     assert np.array_equal(tt.T, rs * rb.astype(np.float32))
+    assert_min_operand(xq, rs, rb)
+
+
+def assert_min_operand(xq, rs, rb):
+    """The min-term operand sections against their definition (mq.h, mq_act_bytes):
+    u_m = 2^k, k = E - 140 clamped to [-100, 100] with E the biased binary32 exponent of
+    max_b |s*S| (so max/u_m is in [2^13, 2^14) for a normal maximum; k = 0 for an all-zero
+    row and 100 for an infinite one); t = s*S / u_m; hi = f16(t); lo = f16(t - hi);
+    row = hi | hi | lo.  Operand bytes are compared on rows whose s*S are all finite."""
+    M, nb = rs.shape
+    am, ur = (v.cpu().numpy() for v in mq.act_views_min(xq, M, nb * 32))
+    with np.errstate(over="ignore", invalid="ignore"):
+        t = (rs * rb.astype(np.float32)).astype(np.float32)
+        mx = np.abs(t).max(axis=1).astype(np.float32)
+        E = ((mx.view(np.uint32) >> 23) & 255).astype(np.int64)
+        k = np.where(mx == 0, 0, np.clip(E - 140, -100, 100))
+        u = np.ldexp(np.float32(1), k).astype(np.float32)
+        assert np.array_equal(ur.view(np.uint32), u.view(np.uint32))
+        fin = np.isfinite(mx)
+        ts = (t / u[:, None]).astype(np.float32)[fin]
+        hi = ts.astype(np.float16)
+        lo = (ts - hi.astype(np.float32)).astype(np.float16)
+    am = am.view(np.uint16)[fin]
+    assert np.array_equal(am[:, :nb], hi.view(np.uint16))
+    assert np.array_equal(am[:, nb:2 * nb], hi.view(np.uint16))
+    assert np.array_equal(am[:, 2 * nb:], lo.view(np.uint16))
 
 
 @pytest.mark.parametrize("name,M", [("q4_k_mmq_512x18944x3584", 512),
@@ -214,6 +240,19 @@ def test_blockdots_bit_exact_workload_tiles(name):
     ref = oracle.blockdots(qtype, Wt, 256, K, qs)
     assert np.array_equal(D.cpu().numpy(), ref.astype(np.int32))
     W.free()
+
+
+@pytest.mark.parametrize("N,K,M", [(19, 256, 9), (70, 8192, 5), (130, 3584, 130)])
+def test_mmq_q4_k_min_term_stages(N, K, M):
+    """Q4_K min-term GEMM over 1, 12 (two rounds of the operand ring) and 6 stages."""
+    W = registered(12, N, K, 23)
+    x = synth.activations(M, K, seed=K + M)
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    y = mq.mmq(W, xq, M)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    yref, bnd = oracle.mmq(12, weights(12, N, K, 23), N, K, qs, sc)
+    assert_bound(y.cpu().numpy(), yref, bnd, f"mmq Q4_K {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
