@@ -68,8 +68,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kTestWaitNs = 1000000ull;
 constexpr int kTileBytes = TM * PK * 2;  // 16 KB per operand tile and stage
 // launch: 640 threads x 96 registers = 61440; after setmaxnreg the control
-// warpgroup holds 128 x 24 and the four epilogue warpgroups 512 x 112 = 60416.
-constexpr int kRegLaunch = 96, kRegCtl = 24, kRegEpi = 112;
+// warpgroup holds 128 x 32 and the four epilogue warpgroups 512 x 112 = 61440.
+constexpr int kRegLaunch = 96, kRegCtl = 32, kRegEpi = 112;
 static_assert(128 * kRegCtl + 512 * kRegEpi <= NTHR * kRegLaunch,
               "register split exceeds the launch");
 static_assert(NTHR * kRegLaunch <= 65536, "launch registers exceed the SM");
@@ -88,6 +88,7 @@ struct TcArgs {
   int32_t *D;           // [M][N][nb] (block-dot mode)
   int64_t M, N, mt, np;
   int nb;
+  int ntm, ntiles;      // output tiles: ntm along M (fastest), ntiles in all
   int nms;              // Q4_K: ring stages of the min-term GEMM (3*nb/64 rounded up)
   int *status;
   int debug_expire;
@@ -270,9 +271,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   Sm &sm = *reinterpret_cast<Sm *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                    ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = int64_t(blockIdx.x) * TM, n0 = int64_t(blockIdx.y) * TN;
-  const int nb = p.nb, npairs = (nb + 1) / 2;
-  // accumulator uses in order: pair pr = use pr, then the Q4_K min-term GEMM (use npairs)
+  const int nb = p.nb, npairs = (nb + 1) / 2, ngroups = (nb + 7) >> 3;
+  // Accumulator uses of a tile, in order: pair pr = use pr, then the Q4_K min-term GEMM
+  // (use npairs).  The CTA is persistent: it takes tiles blockIdx.x, + gridDim.x, ...
+  // and every ring, accumulator and group phase counts on across its tiles (global use
+  // U = tl * nuse + u, global group G = tl * ngroups + g for the CTA's tl-th tile).
   const int nms = (MIN && !DOTS) ? p.nms : 0, nuse = npairs + (nms > 0 ? 1 : 0);
 
   if (threadIdx.x == 0) {
@@ -304,106 +307,114 @@ __global__ void __launch_bounds__(NTHR, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
-      // Fills in the order of the accumulator uses: use pr = pair pr, then use npairs
-      // = the nms min-term stages (Q4_K).  Use u belongs to issuer u % 2, whose c-th
-      // stage is ring stage (u % 2) + 2 * (c % SR), round c / SR.
+      // Fills in the order of the accumulator uses.  Global use U belongs to issuer U % 2,
+      // whose c-th stage is ring stage (U % 2) + 2 * (c % SR), round c / SR.
       int c0 = 0, c1 = 0;
-      for (int f = 0; f < npairs + nms; ++f) {
-        const int pr = f < npairs ? f : -1, u = f < npairs ? f : npairs, i = u & 1;
-        const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
-        if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group g = pr/4 of 8 blocks
-          const int g = pr >> 2, slot = g & 1, nbl = min(8, nb - 8 * g);
-          if (g >= 2)
-            mbar_wait(sa(&sm.gempty[slot]), ((g >> 1) - 1) & 1, p.status, 5, kWaitNs);
-          mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * 2u);
-          for (int bi = 0; bi < nbl; ++bi) {
-            const int64_t b = 8 * g + bi;
-            bulk_1d(sa(sm.gsx[slot][bi]), p.st + b * p.mt + m0, 512, sa(&sm.gfull[slot]));
-            bulk_1d(sa(sm.gd[slot][bi]), p.td + b * p.np + n0, 512, sa(&sm.gfull[slot]));
+      for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
+        const int m0 = (t % p.ntm) * TM, n0 = (t / p.ntm) * TN;
+        for (int f = 0; f < npairs + nms; ++f) {
+          const int pr = f < npairs ? f : -1;
+          const int i = (tl * nuse + (f < npairs ? f : npairs)) & 1;
+          const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
+          if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group of 8 blocks
+            const int g = pr >> 2, G = tl * ngroups + g, slot = G & 1, nbl = min(8, nb - 8 * g);
+            if (G >= 2)
+              mbar_wait(sa(&sm.gempty[slot]), ((G >> 1) - 1) & 1, p.status, 5, kWaitNs);
+            mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * 2u);
+            for (int bi = 0; bi < nbl; ++bi) {
+              const int64_t b = 8 * g + bi;
+              bulk_1d(sa(sm.gsx[slot][bi]), p.st + b * p.mt + m0, 512, sa(&sm.gfull[slot]));
+              bulk_1d(sa(sm.gd[slot][bi]), p.td + b * p.np + n0, 512, sa(&sm.gfull[slot]));
+            }
           }
+          if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 1, kWaitNs);
+          if (pr < 0) {  // min-term operands: 64 columns of the [hi|hi|lo] x [hi|lo|hi] planes
+            mbar_expect_tx(sa(&sm.full[s]), 2 * kTileBytes);
+            tma_2d(sa(sm.a[s]), &tAm, (f - npairs) * PK, m0, sa(&sm.full[s]));
+            tma_2d(sa(sm.b[s]), &tBm, (f - npairs) * PK, n0, sa(&sm.full[s]));
+            continue;
+          }
+          mbar_expect_tx(sa(&sm.full[s]), bytes);
+          tma_2d(sa(sm.a[s]), &tA, pr * PK, m0, sa(&sm.full[s]));
+          tma_2d(sa(sm.b[s]), &tW, pr * PK, n0, sa(&sm.full[s]));
+          if constexpr (ODD) tma_2d(sa(sm.b2.v[ODD ? s : 0]), &tW2, pr * PK, n0, sa(&sm.full[s]));
         }
-        if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 1, kWaitNs);
-        if (pr < 0) {  // min-term operands: 64 columns of the [hi|hi|lo] x [hi|lo|hi] planes
-          mbar_expect_tx(sa(&sm.full[s]), 2 * kTileBytes);
-          tma_2d(sa(sm.a[s]), &tAm, (f - npairs) * PK, (int)m0, sa(&sm.full[s]));
-          tma_2d(sa(sm.b[s]), &tBm, (f - npairs) * PK, (int)n0, sa(&sm.full[s]));
-          continue;
-        }
-        mbar_expect_tx(sa(&sm.full[s]), bytes);
-        tma_2d(sa(sm.a[s]), &tA, pr * PK, (int)m0, sa(&sm.full[s]));
-        tma_2d(sa(sm.b[s]), &tW, pr * PK, (int)n0, sa(&sm.full[s]));
-        if constexpr (ODD) tma_2d(sa(sm.b2.v[ODD ? s : 0]), &tW2, pr * PK, (int)n0, sa(&sm.full[s]));
       }
     } else if ((warp == 1 || warp == 2) && lane == 0) {  // ---- MMA issuers
       const int i = warp - 1;
       const uint32_t idesc = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
       const uint32_t acc0 = tmem + (uint32_t)(256 * i);
       int c = 0;  // this issuer's stage count (its half of the ring)
-      for (int u = i; u < nuse; u += 2) {  // accumulator slot i, uses u = i, i+2, ...
-        const int use = u >> 1;             // this issuer's use count
-        if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs);
-        if (u == npairs) {  // the min-term GEMM over nms ring stages into columns acc0 .. +128
-          for (int k = 0; k < nms; ++k, ++c) {
-            const int s = i + 2 * (c % SR);
-            mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
-            tc_fence_after();
-            const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
+      for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
+        // this issuer's uses of the tile: U = tl * nuse + u with U % 2 == i
+        for (int u = (i - tl * nuse) & 1; u < nuse; u += 2) {
+          const int use = (tl * nuse + u) >> 1;  // this issuer's use count
+          if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs);
+          if (u == npairs) {  // the min-term GEMM over nms ring stages into columns acc0 .. +128
+            for (int k = 0; k < nms; ++k, ++c) {
+              const int s = i + 2 * (c % SR);
+              mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
+              tc_fence_after();
+              const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16(acc0, ad + 2 * kk, bd + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(sa(&sm.empty[s]));
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16(acc0, ad + 2 * kk, bd + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(sa(&sm.empty[s]));
+            }
+            mma_commit(sa(&sm.tfull[i]));
+            continue;
           }
+          const int s = i + 2 * (c % SR);
+          mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
+          ++c;
+          tc_fence_after();
+          const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // block 2*pr + h -> columns acc0 + 128*h
+            const uint32_t dt = acc0 + (uint32_t)(128 * h);
+            // +2 in the descriptor = +32 bytes = the next 16-element K slice
+            mma_f16(dt, ad + 4 * h, bd + 4 * h, idesc, 0u);
+            mma_f16(dt, ad + 4 * h + 2, bd + 4 * h + 2, idesc, 1u);
+            if constexpr (ODD) {
+              const uint64_t od = sdesc(sa(sm.b2.v[ODD ? s : 0]));
+              mma_f16(dt, ad + 4 * h, od + 4 * h, idesc, 1u);
+              mma_f16(dt, ad + 4 * h + 2, od + 4 * h + 2, idesc, 1u);
+            }
+          }
+          mma_commit(sa(&sm.empty[s]));
           mma_commit(sa(&sm.tfull[i]));
-          continue;
         }
-        const int pr = u, s = i + 2 * (c % SR);
-        mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
-        ++c;
-        tc_fence_after();
-        const uint64_t ad = sdesc(sa(sm.a[s])), bd = sdesc(sa(sm.b[s]));
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // block 2*pr + h -> columns acc0 + 128*h
-          const uint32_t dt = acc0 + (uint32_t)(128 * h);
-          // +2 in the descriptor = +32 bytes = the next 16-element K slice
-          mma_f16(dt, ad + 4 * h, bd + 4 * h, idesc, 0u);
-          mma_f16(dt, ad + 4 * h + 2, bd + 4 * h + 2, idesc, 1u);
-          if constexpr (ODD) {
-            const uint64_t od = sdesc(sa(sm.b2.v[ODD ? s : 0]));
-            mma_f16(dt, ad + 4 * h, od + 4 * h, idesc, 1u);
-            mma_f16(dt, ad + 4 * h + 2, od + 4 * h + 2, idesc, 1u);
-          }
-        }
-        mma_commit(sa(&sm.empty[s]));
-        mma_commit(sa(&sm.tfull[i]));
       }
     }
   } else {  // ---- epilogue warps
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
     const int e = warp - 4, q = warp & 3, hcol = e >> 2;  // rows 32q.., columns EC*hcol..
     const int rl = 32 * q + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
+    const uint32_t gsx0 = sa(&sm.gsx[0][0][rl]), gd0 = sa(&sm.gd[0][0][EC * hcol]);
+    for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
+    const int64_t m0 = int64_t(t % p.ntm) * TM, n0 = int64_t(t / p.ntm) * TN;
     const int64_t m = m0 + rl;
     const bool mok = m < p.M;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
     // accumulators as f32 pairs: one packed fma.rn.f32x2 per two columns
     float2 acc[EC / 2], y[EC / 2];
 #pragma unroll
     for (int j = 0; j < EC / 2; ++j) acc[j] = y[j] = make_float2(0.f, 0.f);
     // Groups of 8 blocks (4 pairs; a Q4_K / Q6_K super-block), unrolled so that the
-    // accumulator slot, the block's place in the group and every shared-memory
-    // offset are compile-time constants.
-    const int ngroups = (nb + 7) >> 3;
-    const uint32_t gsx0 = sa(&sm.gsx[0][0][rl]), gd0 = sa(&sm.gd[0][0][EC * hcol]);
+    // block's place in the group and every shared-memory offset are compile-time
+    // constants.
     for (int g = 0; g < ngroups; ++g) {
-      const int slot = g & 1;
-      if (!DOTS) mbar_wait(sa(&sm.gfull[slot]), (g >> 1) & 1, p.status, 6, kWaitNs);
+      const int G = tl * ngroups + g, slot = G & 1;
+      if (!DOTS) mbar_wait(sa(&sm.gfull[slot]), (G >> 1) & 1, p.status, 6, kWaitNs);
       const uint32_t gsx = gsx0 + (uint32_t)(slot * 8 * TM * 4);
       const uint32_t gd = gd0 + (uint32_t)(slot * 8 * TN * 4);
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
         const int pr = 4 * g + pp;
         if (TYPE == MQ_Q8_0 && pr >= npairs) break;  // K % 256 == 0 for the K-quants
-        const int i = pp & 1, use = pr >> 1;
-        if (pr == 0 && p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
+        const int U = tl * nuse + pr, i = U & 1, use = U >> 1;
+        if (tl == 0 && pr == 0 && p.debug_expire)
+          mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
         mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
         tc_fence_after();
 #pragma unroll
@@ -413,6 +424,11 @@ __global__ void __launch_bounds__(NTHR, 1)
           uint32_t r[EC];
           TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (h == 1 || b == nb - 1) {  // the pair's accumulators are in registers: free them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
+          }
           if constexpr (DOTS) {
             if (mok) {
 #pragma unroll
@@ -452,22 +468,22 @@ __global__ void __launch_bounds__(NTHR, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
       }
       if (!DOTS) {
         __syncwarp();
         if (lane == 0) mbar_arrive(sa(&sm.gempty[slot]));
       }
     }
-    if (nuse > npairs) {  // y -= u_m * v_n * C_min (the last accumulator use)
-      const int i = npairs & 1;
-      mbar_wait(sa(&sm.tfull[i]), (npairs >> 1) & 1, p.status, 7, kWaitNs);
+    if (nuse > npairs) {  // y -= u_m * v_n * C_min (the tile's last accumulator use)
+      const int U = tl * nuse + npairs, i = U & 1;
+      mbar_wait(sa(&sm.tfull[i]), (U >> 1) & 1, p.status, 7, kWaitNs);
       tc_fence_after();
       uint32_t r[EC];
       TC_LD32(trow + (uint32_t)(256 * i), r);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
       const float um = mok ? -p.urow[m] : 0.f;
       const float4 *v4 = reinterpret_cast<const float4 *>(p.vcol + n0 + EC * hcol);
       const float2 um2 = make_float2(um, um);
@@ -495,6 +511,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       }
     }
+    }  // tiles
   }
   tc_fence_before();
   __syncthreads();
@@ -561,11 +578,9 @@ mq_status optin_t(const DeviceState *st, const char *name) {
 
 template <int TYPE, bool DOTS>
 mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap &tAm,
-                   const TcArgs &a, cudaStream_t s, const char *name) {
-  dim3 grid((unsigned)((a.M + TM - 1) / TM), (unsigned)((a.N + TN - 1) / TN));
-  if (grid.y > 65535)
-    return fail(MQ_ERR_SHAPE, "%s: N=%lld needs more than 65535 column tiles", name,
-                (long long)a.N);
+                   const TcArgs &a, cudaStream_t s, int sms, const char *name) {
+  // persistent: one CTA per SM (shared memory allows no more), tiles strided over them
+  dim3 grid((unsigned)(a.ntiles < sms ? a.ntiles : sms));
   const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
   const CUtensorMap &tW2 = *reinterpret_cast<const CUtensorMap *>(
       TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);
@@ -629,19 +644,25 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   a.mt = L.mt;
   a.np = W->np;
   a.nb = (int)(W->K / 32);
+  const int64_t ntm = (M + TM - 1) / TM, ntn = (W->N + TN - 1) / TN;
+  if (ntm * ntn > 0x7fffffff / 2)
+    return fail(MQ_ERR_SHAPE, "mq_mmq: %lld x %lld output tiles are too many", (long long)ntm,
+                (long long)ntn);
+  a.ntm = (int)ntm;
+  a.ntiles = (int)(ntm * ntn);
   a.status = st->status;
   a.debug_expire = debug_expire;
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
-      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q4_K,dots>")
-                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q4_K>");
+      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
+                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
     case MQ_Q6_K:
-      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q6_K,dots>")
-                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q6_K>");
+      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
+                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q6_K>");
     default:
-      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, a, s, "mmq_tc_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, a, s, "mmq_tc_kernel<Q8_0>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q8_0>");
   }
 }
 
