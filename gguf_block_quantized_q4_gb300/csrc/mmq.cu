@@ -80,8 +80,6 @@ constexpr int stages() {  // 192 KB of operand ring
 }
 
 struct TcArgs {
-  const float *st;      // [nb][mt] activation block scales, transposed
-  const float *td;      // [nb][np] weight block scale d, transposed
   const float *urow;    // [mt] Q4_K min-term row factors u_m
   const float *vcol;    // [np] Q4_K min-term column factors v_n
   float *y;             // [M][N]
@@ -196,14 +194,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
-                                        uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // K-major operand in the 128-byte swizzle layout TMA writes: 8-row groups of
 // 1024 bytes (SBO), leading offset unused (16), descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
@@ -262,7 +252,8 @@ template <int TYPE, bool DOTS>
 __global__ void __launch_bounds__(NTHR, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
                   const __grid_constant__ CUtensorMap tW2, const __grid_constant__ CUtensorMap tAm,
-                  const __grid_constant__ CUtensorMap tBm, const TcArgs p) {
+                  const __grid_constant__ CUtensorMap tBm, const __grid_constant__ CUtensorMap tSx,
+                  const __grid_constant__ CUtensorMap tD, const TcArgs p) {
   using Sm = TcSmem<TYPE>;
   constexpr int NST = Sm::NST, SR = NST / 2;  // SR ring stages per MMA issuer
   static_assert(NST % 2 == 0, "the ring is split between two issuers");
@@ -317,15 +308,14 @@ __global__ void __launch_bounds__(NTHR, 1)
           const int i = (tl * nuse + (f < npairs ? f : npairs)) & 1;
           const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
           if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group of 8 blocks
-            const int g = pr >> 2, G = tl * ngroups + g, slot = G & 1, nbl = min(8, nb - 8 * g);
+            const int g = pr >> 2, G = tl * ngroups + g, slot = G & 1;
             if (G >= 2)
               mbar_wait(sa(&sm.gempty[slot]), ((G >> 1) - 1) & 1, p.status, 5, kWaitNs);
-            mbar_expect_tx(sa(&sm.gfull[slot]), (uint32_t)nbl * 512u * 2u);
-            for (int bi = 0; bi < nbl; ++bi) {
-              const int64_t b = 8 * g + bi;
-              bulk_1d(sa(sm.gsx[slot][bi]), p.st + b * p.mt + m0, 512, sa(&sm.gfull[slot]));
-              bulk_1d(sa(sm.gd[slot][bi]), p.td + b * p.np + n0, 512, sa(&sm.gfull[slot]));
-            }
+            // the group's 8 x 128 row scales and 8 x 128 column scales, one box each
+            // (blocks past the last read as 0)
+            mbar_expect_tx(sa(&sm.gfull[slot]), 2u * 8u * 128u * 4u);
+            tma_2d(sa(sm.gsx[slot][0]), &tSx, m0, 8 * g, sa(&sm.gfull[slot]));
+            tma_2d(sa(sm.gd[slot][0]), &tD, n0, 8 * g, sa(&sm.gfull[slot]));
           }
           if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 1, kWaitNs);
           if (pr < 0) {  // min-term operands: 64 columns of the [hi|hi|lo] x [hi|lo|hi] planes
@@ -557,6 +547,25 @@ mq_status encode_f16_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_
   return MQ_OK;
 }
 
+// f32 [rows][cols] row-major (a transposed block-scale plane: row = block, column =
+// matrix row), box 128 columns x 8 rows, no swizzle; rows past the plane read as 0.
+mq_status encode_scale_map(CUtensorMap *map, const void *ptr, int64_t cols, int64_t rows,
+                           const char *what) {
+  mq_status s = get_encode();
+  if (s != MQ_OK) return s;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {128, 8};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MQ_ERR_CUDA, "TMA descriptor for the %s plane (%lld x %lld f32 at %p) refused: %d",
+                what, (long long)rows, (long long)cols, ptr, (int)r);
+  return MQ_OK;
+}
+
 template <int TYPE>
 constexpr size_t smem_bytes() {
   return sizeof(TcSmem<TYPE>) + 1024;
@@ -578,7 +587,8 @@ mq_status optin_t(const DeviceState *st, const char *name) {
 
 template <int TYPE, bool DOTS>
 mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap &tAm,
-                   const TcArgs &a, cudaStream_t s, int sms, const char *name) {
+                   const CUtensorMap &tSx, const TcArgs &a, cudaStream_t s, int sms,
+                   const char *name) {
   // persistent: one CTA per SM (shared memory allows no more), tiles strided over them
   dim3 grid((unsigned)(a.ntiles < sms ? a.ntiles : sms));
   const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
@@ -586,7 +596,9 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
       TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);
   const CUtensorMap &tBm = *reinterpret_cast<const CUtensorMap *>(
       TYPE == MQ_Q4_K && !DOTS ? W->tmap_mb : W->tmap_w);
-  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, a);
+  const CUtensorMap &tD = *reinterpret_cast<const CUtensorMap *>(DOTS ? W->tmap_w : W->tmap_td);
+  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, tSx, tD,
+                                                                    a);
   MQ_LAUNCH_CHECK(name);
   return MQ_OK;
 }
@@ -604,6 +616,9 @@ mq_status encode_weight_maps(mq_weight *w) {
   if (s == MQ_OK && w->mb)
     s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_mb), w->mb, w->np,
                        3 * (w->K / 32), "weight min-term");
+  if (s == MQ_OK)
+    s = encode_scale_map(reinterpret_cast<CUtensorMap *>(w->tmap_td), w->td, w->np, w->K / 32,
+                         "weight block scale");
   return s;
 }
 
@@ -631,9 +646,15 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
                   MQ_OK)
     return r;
   if (!mins) tAm = tA;
+  alignas(64) CUtensorMap tSx;
+  if (D == nullptr) {
+    if ((r = encode_scale_map(&tSx, base + L.st, L.mt, W->K / 32, "activation block scale")) !=
+        MQ_OK)
+      return r;
+  } else {
+    tSx = tA;  // unused by the block-dot kernels
+  }
   TcArgs a;
-  a.st = reinterpret_cast<const float *>(base + L.st);
-  a.td = W->td;
   a.urow = reinterpret_cast<const float *>(base + L.urow);
   a.vcol = W->vcol;
   a.nms = mins ? (int)((3 * (W->K / 32) + PK - 1) / PK) : 0;
@@ -655,14 +676,14 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
-      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
-                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
+      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
+                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
     case MQ_Q6_K:
-      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
-                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q6_K>");
+      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
+                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K>");
     default:
-      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, a, s, st->sms, "mmq_tc_kernel<Q8_0>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0>");
   }
 }
 

@@ -67,6 +67,7 @@ struct mq_weight {
   alignas(64) unsigned char tmap_w[128];   // TMA descriptors of w and w2 (CUtensorMap)
   alignas(64) unsigned char tmap_w2[128];
   alignas(64) unsigned char tmap_mb[128];
+  alignas(64) unsigned char tmap_td[128];  // td as 8-block x 128-row boxes
 };
 
 namespace mq {
