@@ -264,10 +264,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p.nb, npairs = (nb + 1) / 2, ngroups = (nb + 7) >> 3;
   // Accumulator uses of a tile, in order: pair pr = use pr, then the Q4_K min-term GEMM
-  // (use npairs).  The CTA is persistent: it takes tiles blockIdx.x, + gridDim.x, ...
-  // and every ring, accumulator and group phase counts on across its tiles (global use
-  // U = tl * nuse + u, global group G = tl * ngroups + g for the CTA's tl-th tile).
-  const int nms = (MIN && !DOTS) ? p.nms : 0, nuse = npairs + (nms > 0 ? 1 : 0);
+  // as nmu uses (npairs + j, j < nmu), one per issuer when there are two, use j taking
+  // min-term stages j, j + nmu, ...  The CTA is persistent: it takes tiles blockIdx.x,
+  // + gridDim.x, ... and every ring, accumulator and group phase counts on across its
+  // tiles (global use U = tl * nuse + u, global group G = tl * ngroups + g for the CTA's
+  // tl-th tile).
+  const int nms = (MIN && !DOTS) ? p.nms : 0, nmu = nms >= 2 ? 2 : nms, nuse = npairs + nmu;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -305,7 +307,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int m0 = (t % p.ntm) * TM, n0 = (t / p.ntm) * TN;
         for (int f = 0; f < npairs + nms; ++f) {
           const int pr = f < npairs ? f : -1;
-          const int i = (tl * nuse + (f < npairs ? f : npairs)) & 1;
+          const int i =
+              (tl * nuse + (f < npairs ? f : npairs + (nmu == 2 ? (f - npairs) & 1 : 0))) & 1;
           const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
           if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group of 8 blocks
             const int g = pr >> 2, G = tl * ngroups + g, slot = G & 1;
@@ -340,8 +343,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         for (int u = (i - tl * nuse) & 1; u < nuse; u += 2) {
           const int use = (tl * nuse + u) >> 1;  // this issuer's use count
           if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs);
-          if (u == npairs) {  // the min-term GEMM over nms ring stages into columns acc0 .. +128
-            for (int k = 0; k < nms; ++k, ++c) {
+          if (u >= npairs) {  // min-term use j: stages j, j + nmu, ... into columns acc0 .. +128
+            const int ks = nmu == 2 ? (nms - (u - npairs) + 1) >> 1 : nms;
+            for (int k = 0; k < ks; ++k, ++c) {
               const int s = i + 2 * (c % SR);
               mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
               tc_fence_after();
@@ -464,8 +468,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (lane == 0) mbar_arrive(sa(&sm.gempty[slot]));
       }
     }
-    if (nuse > npairs) {  // y -= u_m * v_n * C_min (the tile's last accumulator use)
-      const int U = tl * nuse + npairs, i = U & 1;
+    for (int j = 0; j < nmu; ++j) {  // y -= u_m * v_n * C_min, C_min summed over the min uses
+      const int U = tl * nuse + npairs + j, i = U & 1;
       mbar_wait(sa(&sm.tfull[i]), (U >> 1) & 1, p.status, 7, kWaitNs);
       tc_fence_after();
       uint32_t r[EC];
