@@ -12,14 +12,16 @@
 // no integer tcgen05 kind, and f16 integers are exact, so this is the int8
 // contraction on the tensor pipe.
 //
-// Structure (one 128 x 128 output tile per CTA, 12 warps = 3 warpgroups).  The
-// K loop runs over pairs of 32-element blocks (64 K per pipeline stage):
-//   warpgroup 0 (registers lowered to 24 with setmaxnreg):
+// Structure.  Output tiles of 128 x 128; one persistent CTA per SM takes tiles
+// blockIdx.x, + gridDim.x, ... (m-tiles fastest, so CTAs running together share
+// each weight tile through L2 and the weights stream from HBM about once).  The K
+// loop runs over pairs of 32-element blocks (64 K per pipeline stage).  20 warps:
+//   warpgroup 0 (registers lowered to 32 with setmaxnreg):
 //     warp 0    TMA producer: per pair, the activation tile (128 x 64 f16) and the
 //               weight tile(s) (128 x 64 f16; Q6_K also the odd part) into a
 //               shared-memory ring (128-byte swizzle), mbarrier tx-count; per 8
-//               blocks, 1-D bulk copies of the tile's row scales s and s*S and
-//               column scales d and dmin*m_j into a 2-slot ring.
+//               blocks, one 2-D box each of the tile's row scales s and column
+//               scales d (8 blocks x 128) into a 2-slot ring.
 //     warps 1,2 MMA issuers (warp 1 also owns TMEM: 512 columns = two pairs of
 //               128-column f32 accumulators).  The accumulator uses alternate
 //               between them (issuer i, accumulator pair i): per pair of blocks
@@ -30,10 +32,10 @@
 //               ring (stages i, i+2, ...) and the producer fills the stages in the
 //               order of the uses, so every stage is consumed by one issuer, round
 //               after round: a parity wait never sees a phase two rounds old.
-//   warpgroups 1-2 (registers raised to 240): 8 epilogue warps.  Warp w reads
-//               TMEM lanes 32*(w%4).. (its 32 rows) and 64 of the 128 columns;
-//               per block it loads the accumulator (tcgen05.ld, both halves in
-//               flight, one wait) and promotes it in registers:
+//   warpgroups 1-4 (registers raised to 112): 16 epilogue warps.  Warp w reads
+//               TMEM lanes 32*(w%4).. (its 32 rows) and 32 of the 128 columns;
+//               per block it loads the accumulator (tcgen05.ld) and promotes it
+//               in registers with packed f32x2 multiply-adds:
 //                 Q8_0: y += (s_m * d_n) * D
 //                 Q4_K, Q6_K: a = s_m * D (first block of a super-block), then
 //                             a += s_m * D; per super-block y += d_n * a
@@ -42,13 +44,11 @@
 // the tensor cores form it once per tile, after the main loop, from three f16
 // products per block (row side hi | hi | lo of (s*S)/u_m, column side
 // hi | lo | hi of (dmin*m_j)/v_n, u and v powers of two that keep both in f16
-// range; 22 significant bits), staged through the same ring as the last
-// accumulator use.  The epilogue adds y -= u_m * v_n * C_min before the store,
-// so the per-block work is a single multiply-add.
+// range; 22 significant bits), staged through the same ring as two accumulator
+// uses, one per issuer.  The epilogue adds y -= u_m * v_n * C_min before the
+// store, so the per-block work is a single multiply-add.
 // All mbarrier waits are bounded (2 s by %globaltimer); an expired wait writes
 // MQ_ERR_TIMEOUT into the device status word read by mq_stream_status.
-// Grid: m-tiles fastest, so concurrently running CTAs share each weight tile
-// through L2 and the weights stream from HBM about once.
 #include <cstddef>
 #include <cuda.h>
 #include <cudaTypedefs.h>
