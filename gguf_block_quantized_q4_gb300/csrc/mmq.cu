@@ -136,26 +136,15 @@ __device__ __forceinline__ uint64_t gtime() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// One non-suspending probe of an mbarrier phase (cheap when it has completed).
-__device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(a), "r"(parity), "r"(0)
-      : "memory");
-  return ok != 0;
-}
-// A probe that suspends the thread until the phase completes or about 0.1 ms
-// pass, so a waiting warp takes no issue slots from the others.
+// A probe that may suspend the thread for the system-dependent time limit while
+// the phase is incomplete.
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(a), "r"(parity), "r"(100000)
+      : "r"(a), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -163,7 +152,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
 // status word and return false; the caller carries on so the kernel ends.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *status, int site,
                                           uint64_t limit_ns) {
-  if (mbar_probe(a, parity)) return true;
+  if (mbar_try(a, parity)) return true;
   const uint64_t t0 = gtime();
   for (;;) {
 #pragma unroll 1
@@ -278,9 +267,10 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(sa(&sm.tfull[t]), 1);
-      mbar_init(sa(&sm.tempty[t]), NEPI);
+      // every epilogue thread arrives on its own: no election or warp sync on the way
+      mbar_init(sa(&sm.tempty[t]), 32 * NEPI);
       mbar_init(sa(&sm.gfull[t]), 1);
-      mbar_init(sa(&sm.gempty[t]), NEPI);
+      mbar_init(sa(&sm.gempty[t]), 32 * NEPI);
     }
     mbar_init(sa(&sm.never), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -386,6 +376,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int rl = 32 * q + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
     const uint32_t gsx0 = sa(&sm.gsx[0][0][rl]), gd0 = sa(&sm.gd[0][0][EC * hcol]);
+    // test hook: a wait that never completes, before the first accumulator use
+    if (p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
     for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
     const int64_t m0 = int64_t(t % p.ntm) * TM, n0 = int64_t(t / p.ntm) * TN;
     const int64_t m = m0 + rl;
@@ -407,8 +399,6 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int pr = 4 * g + pp;
         if (TYPE == MQ_Q8_0 && pr >= npairs) break;  // K % 256 == 0 for the K-quants
         const int U = tl * nuse + pr, i = U & 1, use = U >> 1;
-        if (tl == 0 && pr == 0 && p.debug_expire)
-          mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
         mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
         tc_fence_after();
 #pragma unroll
@@ -418,10 +408,9 @@ __global__ void __launch_bounds__(NTHR, 1)
           uint32_t r[EC];
           TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (h == 1 || b == nb - 1) {  // the pair's accumulators are in registers: free them
+          if (h == 1 || (TYPE == MQ_Q8_0 && b == nb - 1)) {  // accumulators in registers: free them
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
+            mbar_arrive(sa(&sm.tempty[i]));
           }
           if constexpr (DOTS) {
             if (mok) {
@@ -464,8 +453,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       }
       if (!DOTS) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sa(&sm.gempty[slot]));
+        mbar_arrive(sa(&sm.gempty[slot]));
       }
     }
     for (int j = 0; j < nmu; ++j) {  // y -= u_m * v_n * C_min, C_min summed over the min uses
@@ -476,8 +464,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       TC_LD32(trow + (uint32_t)(256 * i), r);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sa(&sm.tempty[i]));
+      mbar_arrive(sa(&sm.tempty[i]));
       const float um = mok ? -p.urow[m] : 0.f;
       const float4 *v4 = reinterpret_cast<const float4 *>(p.vcol + n0 + EC * hcol);
       const float2 um2 = make_float2(um, um);
