@@ -601,8 +601,10 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = MvSmem<TYPE, NT>;
   constexpr int NS = Smem::NS;
-  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                       ~uintptr_t(127));
+  // aligned by an offset into the __shared__ array, so the compiler keeps knowing that
+  // every member lives in shared memory (plain loads become LDS, addresses stay 32-bit)
+  Smem &sm = *reinterpret_cast<Smem *>(
+      smem_raw + ((128u - (uint32_t)__cvta_generic_to_shared(smem_raw)) & 127u));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int rank = blockIdx.x % p.S;

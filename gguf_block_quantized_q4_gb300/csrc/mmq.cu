@@ -205,19 +205,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ float2 pair(const uint32_t *r, int j) {
   return make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
 }
-__device__ __forceinline__ float lds_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 lds_f4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -248,8 +235,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   static_assert(NST % 2 == 0, "the ring is split between two issuers");
   constexpr bool ODD = Sm::ODD, MIN = Sm::MIN;
   extern __shared__ uint8_t smem_raw[];
-  Sm &sm = *reinterpret_cast<Sm *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                   ~uintptr_t(1023));
+  // aligned by an offset into the __shared__ array, so the compiler keeps knowing that
+  // every member lives in shared memory (plain loads become LDS, addresses stay 32-bit)
+  Sm &sm = *reinterpret_cast<Sm *>(
+      smem_raw + ((1024u - (uint32_t)__cvta_generic_to_shared(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p.nb, npairs = (nb + 1) / 2, ngroups = (nb + 7) >> 3;
   // Accumulator uses of a tile, in order: pair pr = use pr, then the Q4_K min-term GEMM
@@ -375,7 +364,9 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int e = warp - 4, q = warp & 3, hcol = e >> 2;  // rows 32q.., columns EC*hcol..
     const int rl = 32 * q + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
-    const uint32_t gsx0 = sa(&sm.gsx[0][0][rl]), gd0 = sa(&sm.gd[0][0][EC * hcol]);
+    // Scale reads are plain C++ shared loads (ordered after the group's mbarrier wait,
+    // whose asm clobbers memory), so the compiler folds their constant offsets.
+    const float *gsx0 = &sm.gsx[0][0][rl], *gd0 = &sm.gd[0][0][EC * hcol];
     // test hook: a wait that never completes, before the first accumulator use
     if (p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
     for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
@@ -392,8 +383,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int g = 0; g < ngroups; ++g) {
       const int G = tl * ngroups + g, slot = G & 1;
       if (!DOTS) mbar_wait(sa(&sm.gfull[slot]), (G >> 1) & 1, p.status, 6, kWaitNs);
-      const uint32_t gsx = gsx0 + (uint32_t)(slot * 8 * TM * 4);
-      const uint32_t gd = gd0 + (uint32_t)(slot * 8 * TN * 4);
+      const float *gsx = gsx0 + slot * 8 * TM, *gd = gd0 + slot * 8 * TN;
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
         const int pr = 4 * g + pp;
@@ -421,12 +411,12 @@ __global__ void __launch_bounds__(NTHR, 1)
               }
             }
           } else {
-            const float sxv = lds_f32(gsx + (uint32_t)(bi * TM * 4));
+            const float sxv = gsx[bi * TM];
             const float2 sx2 = make_float2(sxv, sxv);
             if constexpr (TYPE == MQ_Q8_0) {  // y += (s_m * d_n) * D per block
 #pragma unroll
               for (int j4 = 0; j4 < EC / 4; ++j4) {
-                const float4 c = lds_f4(gd + (uint32_t)((bi * TN + 4 * j4) * 4));
+                const float4 c = *reinterpret_cast<const float4 *>(gd + bi * TN + 4 * j4);
                 y[2 * j4] = __ffma2_rn(__fmul2_rn(sx2, make_float2(c.x, c.y)), pair(r, 4 * j4),
                                        y[2 * j4]);
                 y[2 * j4 + 1] = __ffma2_rn(__fmul2_rn(sx2, make_float2(c.z, c.w)),
@@ -443,7 +433,7 @@ __global__ void __launch_bounds__(NTHR, 1)
               if (bi == 7) {  // end of the super-block: y += d * a
 #pragma unroll
                 for (int j4 = 0; j4 < EC / 4; ++j4) {
-                  const float4 c = lds_f4(gd + (uint32_t)((7 * TN + 4 * j4) * 4));
+                  const float4 c = *reinterpret_cast<const float4 *>(gd + 7 * TN + 4 * j4);
                   y[2 * j4] = __ffma2_rn(make_float2(c.x, c.y), acc[2 * j4], y[2 * j4]);
                   y[2 * j4 + 1] = __ffma2_rn(make_float2(c.z, c.w), acc[2 * j4 + 1], y[2 * j4 + 1]);
                 }
