@@ -242,12 +242,13 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p.nb, npairs = (nb + 1) / 2, ngroups = (nb + 7) >> 3;
   // Accumulator uses of a tile, in order: pair pr = use pr, then the Q4_K min-term GEMM
-  // as nmu uses (npairs + j, j < nmu), one per issuer when there are two, use j taking
-  // min-term stages j, j + nmu, ...  The CTA is persistent: it takes tiles blockIdx.x,
-  // + gridDim.x, ... and every ring, accumulator and group phase counts on across its
-  // tiles (global use U = tl * nuse + u, global group G = tl * ngroups + g for the CTA's
-  // tl-th tile).
-  const int nms = (MIN && !DOTS) ? p.nms : 0, nmu = nms >= 2 ? 2 : nms, nuse = npairs + nmu;
+  // as two uses (npairs + j, j < 2), one per issuer, use j taking min-term stages j,
+  // j + 2, ... (use 1 has none when there is one stage).  The CTA is persistent: it
+  // takes tiles blockIdx.x, + gridDim.x, ... and every ring, accumulator and group phase
+  // counts on across its tiles (global use U = tl * nuse + u, global group
+  // G = tl * ngroups + g for the CTA's tl-th tile).  For the K-quants npairs is a
+  // multiple of 4, so nuse is even and pair pr of every tile uses accumulator pr % 2.
+  const int nms = (MIN && !DOTS) ? p.nms : 0, nmu = nms > 0 ? 2 : 0, nuse = npairs + nmu;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -286,8 +287,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int m0 = (t % p.ntm) * TM, n0 = (t / p.ntm) * TN;
         for (int f = 0; f < npairs + nms; ++f) {
           const int pr = f < npairs ? f : -1;
-          const int i =
-              (tl * nuse + (f < npairs ? f : npairs + (nmu == 2 ? (f - npairs) & 1 : 0))) & 1;
+          const int i = (tl * nuse + (f < npairs ? f : npairs + ((f - npairs) & 1))) & 1;
           const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
           if (!DOTS && pr >= 0 && (pr & 3) == 0) {  // group of 8 blocks
             const int g = pr >> 2, G = tl * ngroups + g, slot = G & 1;
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           const int use = (tl * nuse + u) >> 1;  // this issuer's use count
           if (use >= 1) mbar_wait(sa(&sm.tempty[i]), (use - 1) & 1, p.status, 3, kWaitNs);
           if (u >= npairs) {  // min-term use j: stages j, j + nmu, ... into columns acc0 .. +128
-            const int ks = nmu == 2 ? (nms - (u - npairs) + 1) >> 1 : nms;
+            const int ks = (nms - (u - npairs) + 1) >> 1;
             for (int k = 0; k < ks; ++k, ++c) {
               const int s = i + 2 * (c % SR);
               mbar_wait(sa(&sm.full[s]), (c / SR) & 1, p.status, 2, kWaitNs);
@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     // Groups of 8 blocks (4 pairs; a Q4_K / Q6_K super-block), unrolled so that the
     // block's place in the group and every shared-memory offset are compile-time
     // constants.
+    const uint32_t ub = (uint32_t)(tl * nuse) >> 1;  // accumulator uses per issuer before this tile
     for (int g = 0; g < ngroups; ++g) {
       const int G = tl * ngroups + g, slot = G & 1;
       if (!DOTS) mbar_wait(sa(&sm.gfull[slot]), (G >> 1) & 1, p.status, 6, kWaitNs);
@@ -388,8 +389,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int pp = 0; pp < 4; ++pp) {
         const int pr = 4 * g + pp;
         if (TYPE == MQ_Q8_0 && pr >= npairs) break;  // K % 256 == 0 for the K-quants
-        const int U = tl * nuse + pr, i = U & 1, use = U >> 1;
-        mbar_wait(sa(&sm.tfull[i]), use & 1, p.status, 4, kWaitNs);
+        // accumulator i and its phase; compile-time i for the K-quants (even nuse)
+        const int U = tl * nuse + pr;
+        const int i = TYPE == MQ_Q8_0 ? U & 1 : pp & 1;
+        const uint32_t par = TYPE == MQ_Q8_0 ? (U >> 1) & 1 : (ub + (pp >> 1)) & 1;
+        mbar_wait(sa(&sm.tfull[i]), par, p.status, 4, kWaitNs);
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -450,6 +454,10 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int U = tl * nuse + npairs + j, i = U & 1;
       mbar_wait(sa(&sm.tfull[i]), (U >> 1) & 1, p.status, 7, kWaitNs);
       tc_fence_after();
+      if (nms - j <= 0) {  // an empty use (one min-term stage): nothing to read
+        mbar_arrive(sa(&sm.tempty[i]));
+        continue;
+      }
       uint32_t r[EC];
       TC_LD32(trow + (uint32_t)(256 * i), r);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
