@@ -254,6 +254,55 @@ def profile_calls(kernel: str, calls: int):
     return 0
 
 
+def chain_timing(links: int, reps: int = 200):
+    """Per-link time of a decode chain of `links` Q8_0 896x896 matvecs (B = 1), issued
+    eagerly and as one captured CUDA graph (a side measurement, not the bench line)."""
+    import torch
+
+    import gguf_block_quantized_q4_gb300 as mq
+    from gguf_block_quantized_q4_gb300 import build as mqbuild
+    import synth
+    mqbuild.build()
+    mq.init(0)
+    Ws = [mq.register_weight(synth.Q8_0, synth.weights(synth.Q8_0, 896, 896, 300 + l), 896, 896,
+                             mq.REG_NO_MMQ_PLANE) for l in range(links)]
+    x = torch.from_numpy(synth.activations(1, 896, 7)).cuda()
+    ys = [torch.empty((1, 896), device="cuda") for _ in range(links)]
+
+    def chain():
+        h = x
+        for W, y in zip(Ws, ys):
+            mq.matvec(W, h, y)
+            h = y
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            chain()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    for name, fn in (("eager", chain), ("graph", g.replay)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name + "_us_per_link"] = e0.elapsed_time(e1) * 1e3 / (reps * links)
+    mq.stream_status()
+    for W in Ws:
+        W.free()
+    print(json.dumps({"chain": f"{links} x Q8_0 896x896 matvec, B=1", **out}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -264,9 +313,13 @@ def main():
     ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
                     help="profiling mode: only run --calls launches of this kernel")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--chain", type=int, default=0,
+                    help="time a decode chain of this many small matvecs, eager and graphed")
     args = ap.parse_args()
     if args.kernel:
         return profile_calls(args.kernel, args.calls)
+    if args.chain:
+        return chain_timing(args.chain)
     if args.impl == "reference":
         return run_reference(args)
     args.warmup = max(args.warmup, 3)
