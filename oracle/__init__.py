@@ -156,3 +156,44 @@ def mmq(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, scale: np.nda
     _check(lib().oracle_mmq(qtype, _ptr(W), N, K, _ptr(qs), _ptr(scale), M, _ptr(mrows),
                             len(mrows), n0, n1, _ptr(y), _ptr(bnd)), "mmq")
     return y, bnd
+
+
+# ---- fused FFN gate/up with SwiGLU ("minfer CUDA Backend Design" §4.3 FusedFFN and
+# SwiGLU ops, §4.6 the ffn_gu concat of the gate and up weights).  The pages name the
+# operation but do not write it out; the reading used here is the usual one,
+# h = silu(g) * u with silu(v) = v / (1 + exp(-v)), g = W_gate x, u = W_up x.
+
+SILU_SLOPE = 1.1  # max |silu'(v)| = 1.0998... (at v ~ 2.4), rounded up
+
+
+def silu(v) -> np.ndarray:
+    """silu(v) = v / (1 + e^-v) in float64 (e^-v overflows to inf for v << 0: -0)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def swiglu_bound(g, u, bg, bu, rel):
+    """Bound on |silu(g') u' - silu(g) u| given |g' - g| <= rel*bg, |u' - u| <= rel*bu:
+    |silu(g')-silu(g)| <= SILU_SLOPE*|g'-g| (mean value theorem), so the error is at most
+    SILU_SLOPE*rel*bg*(|u| + rel*bu) + |silu(g)|*rel*bu."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    return SILU_SLOPE * rel * bg * (np.abs(u) + rel * bu) + np.abs(silu(g)) * rel * bu
+
+
+def ffn_gu_matvec(qtype: int, Wg: np.ndarray, Wu: np.ndarray, N: int, K: int, x: np.ndarray,
+                  rel: float = 1e-4):
+    """h = silu(W_gate x) * (W_up x) for N x K gate and up weights (raw GGUF bytes).
+    Returns (h, bound) float64 [B][N]; bound is swiglu_bound of the two matvec bounds."""
+    g, bg = matvec(qtype, Wg, N, K, x)
+    u, bu = matvec(qtype, Wu, N, K, x)
+    return silu(g) * u, swiglu_bound(g, u, bg, bu, rel)
+
+
+def ffn_gu_mmq(qtype: int, Wg: np.ndarray, Wu: np.ndarray, N: int, K: int, qs: np.ndarray,
+               scale: np.ndarray, mrows=None, rel: float = 1e-4):
+    """The MMQ form: g, u from the quantised activations (qs, scale) as in mmq()."""
+    g, bg = mmq(qtype, Wg, N, K, qs, scale, mrows)
+    u, bu = mmq(qtype, Wu, N, K, qs, scale, mrows)
+    return silu(g) * u, swiglu_bound(g, u, bg, bu, rel)

@@ -3,6 +3,7 @@ hand-worked golden blocks (tests/golden/), IEEE binary16 as numpy decodes it,
 invariants of the block formats and of the activation quantiser, special cases
 that reduce to a plain float64 matrix product, Python big-integer brute force, and
 a second, vectorised decoder.  CPU only."""
+import math
 import os
 
 import numpy as np
@@ -361,3 +362,60 @@ def test_power_of_two_scaled_blocks_roundtrip():
         qs, sc, bs = oracle.quantize_act(x.reshape(1, 128))
         assert np.all(sc == np.float32(2.0 ** e))
         assert np.array_equal(qs.reshape(4, 32), q)
+
+
+# ---- fused FFN gate/up (SwiGLU) ----------------------------------------------------
+
+def test_silu_closed_forms():
+    """silu(v) = v * sigma(v): silu(0) = 0, silu(1) = e/(1+e), silu(-1) = -1/(1+e), and
+    silu(v) - silu(-v) = v (sigma(v) + sigma(-v) = 1); far tails -> v and -0."""
+    e = math.e
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - e / (1 + e)) < 1e-15
+    assert abs(oracle.silu(-1.0) + 1 / (1 + e)) < 1e-15
+    v = np.linspace(-30, 30, 601)
+    assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=0, atol=1e-12)
+    assert oracle.silu(800.0) == 800.0
+    big_neg = oracle.silu(-800.0)
+    assert big_neg == 0.0 and math.copysign(1, big_neg) < 0
+
+
+def test_silu_matches_tanh_form_and_slope_bound():
+    """Independent formulas for sigma, and the slope bound used by
+    swiglu_bound: max |silu'| on a fine grid stays below SILU_SLOPE."""
+    v = np.linspace(-40, 40, 160001)
+    # tanh form for v >= 0; e^v / (1 + e^v) below 0, where 1 + tanh(v/2) cancels
+    ref = np.where(v >= 0, v * (1 + np.tanh(v / 2)) / 2, v * np.exp(v) / (1 + np.exp(v)))
+    assert np.allclose(oracle.silu(v), ref, rtol=1e-13, atol=1e-300)
+    slope = np.abs(np.diff(oracle.silu(v)) / np.diff(v))
+    assert slope.max() < oracle.SILU_SLOPE
+    assert slope.max() > 1.09  # the bound is tight, not arbitrary
+
+
+def test_swiglu_bound_covers_perturbations():
+    """Random g, u and perturbations inside their bounds never leave swiglu_bound."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    g = rng.standard_normal(20000) * 4
+    u = rng.standard_normal(20000) * 4
+    bg = np.abs(rng.standard_normal(20000)) * 50
+    bu = np.abs(rng.standard_normal(20000)) * 50
+    rel = 1e-4
+    dg = (rng.random(20000) * 2 - 1) * rel * bg
+    du = (rng.random(20000) * 2 - 1) * rel * bu
+    err = np.abs(oracle.silu(g + dg) * (u + du) - oracle.silu(g) * u)
+    assert (err <= oracle.swiglu_bound(g, u, bg, bu, rel) * (1 + 1e-12)).all()
+
+
+@pytest.mark.parametrize("qtype", [synth.Q8_0, synth.Q4_K, synth.Q6_K])
+def test_ffn_gu_matvec_is_silu_gate_times_up(qtype):
+    """The fused oracle against an explicit float64 dequantise + matmul + tanh-form silu."""
+    N, K, B = 5, 512, 3
+    Wg = synth.weights(qtype, N, K, 41)
+    Wu = synth.weights(qtype, N, K, 42)
+    x = synth.activations(B, K, 43)
+    h, bnd = oracle.ffn_gu_matvec(qtype, Wg, Wu, N, K, x)
+    g = x.astype(np.float64) @ oracle.dequant(qtype, Wg, N, K).T
+    u = x.astype(np.float64) @ oracle.dequant(qtype, Wu, N, K).T
+    ref = g * (1 + np.tanh(g / 2)) / 2 * u
+    assert np.allclose(h, ref, rtol=1e-12, atol=1e-12)
+    assert (bnd > 0).all()
