@@ -303,6 +303,63 @@ def chain_timing(links: int, reps: int = 200):
     return 0
 
 
+def ffn_gu_timing(reps: int = 20):
+    """Fused gate/up (one matvec or MMQ over both weights, SwiGLU in the store) against
+    the two plain calls, on the Q4_K 18944 x 3584 pair: a side measurement, not the bench
+    line.  Graph replays of back-to-back calls on rotating buffers, CUDA events."""
+    import torch
+
+    import gguf_block_quantized_q4_gb300 as mq
+    from gguf_block_quantized_q4_gb300 import build as mqbuild
+    import synth
+    mqbuild.build()
+    mq.init(0)
+    g, u = synth.weights(QTYPE, N, K, W_SEED), synth.weights(QTYPE, N, K, W_SEED + 1)
+    rot = 4  # weight copies rotated so the decode weights come from HBM
+    fused = [mq.register_ffn_gu(QTYPE, g, u, N, K) for _ in range(rot)]
+    gates = [mq.register_weight(QTYPE, g, N, K) for _ in range(rot)]
+    ups = [mq.register_weight(QTYPE, u, N, K) for _ in range(rot)]
+    x = torch.from_numpy(synth.activations(B, K, XD_SEED)).cuda()
+    xa = torch.from_numpy(synth.activations(M, K, XA_SEED)).cuda()
+    xq = mq.quantize_act(xa)
+    hy = torch.empty((M, N), device="cuda")
+    gy, uy = torch.empty((M, N), device="cuda"), torch.empty((M, N), device="cuda")
+    out = {}
+    cases = {
+        "matvec_fused_us": lambda i: mq.ffn_gu_matvec(fused[i % rot], x, hy[:B]),
+        "matvec_two_calls_us": lambda i: (mq.matvec(gates[i % rot], x, gy[:B]),
+                                          mq.matvec(ups[i % rot], x, uy[:B])),
+        "mmq_fused_us": lambda i: mq.ffn_gu_mmq(fused[i % rot], xq, M, hy),
+        "mmq_two_calls_us": lambda i: (mq.mmq(gates[i % rot], xq, M, gy),
+                                       mq.mmq(ups[i % rot], xq, M, uy)),
+    }
+    for name, fn in cases.items():
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(3):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(reps):
+                fn(i)
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) * 1e3 / reps
+    mq.stream_status()
+    for w in fused + gates + ups:
+        w.free()
+    print(json.dumps({"ffn_gu": f"Q4_K gate+up {N}x{K} each, decode B={B}, prefill M={M}",
+                      **out}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -315,11 +372,15 @@ def main():
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--chain", type=int, default=0,
                     help="time a decode chain of this many small matvecs, eager and graphed")
+    ap.add_argument("--ffn-gu", action="store_true",
+                    help="time the fused gate/up matvec and MMQ against two plain calls")
     args = ap.parse_args()
     if args.kernel:
         return profile_calls(args.kernel, args.calls)
     if args.chain:
         return chain_timing(args.chain)
+    if args.ffn_gu:
+        return ffn_gu_timing()
     if args.impl == "reference":
         return run_reference(args)
     args.warmup = max(args.warmup, 3)

@@ -45,6 +45,10 @@ ABI = {
     "mq_quantize_act": (_ST, [_P, _P, _I64, _I64, _P]),
     "mq_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_blockdots": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_register_ffn_gu": (_ST, [ctypes.c_int, _P, _P, _SZ, _I64, _I64, ctypes.c_uint32,
+                                 ctypes.POINTER(_P)]),
+    "mq_ffn_gu_matvec": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "mq_ffn_gu_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_stream_status": (_ST, [_P]),
     "mq_last_error": (ctypes.c_char_p, []),
     "mq_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -138,6 +142,53 @@ class Weight:
 
 def register_weight(qtype, data, N, K, flags=REG_DEFAULT) -> Weight:
     return Weight(qtype, data, N, K, flags)
+
+
+class FfnGuWeight(Weight):
+    """A fused gate/up weight (mq_register_ffn_gu): N gate rows and N up rows."""
+
+    def __init__(self, qtype: int, gate, up, N: int, K: int, flags: int = REG_DEFAULT):
+        import numpy as np
+
+        def as_u8(d):
+            return np.ascontiguousarray(np.frombuffer(memoryview(d), dtype=np.uint8)
+                                        if not isinstance(d, np.ndarray) else d.view(np.uint8))
+        g, u = as_u8(gate), as_u8(up)
+        if g.nbytes != u.nbytes:
+            raise ValueError("gate and up payloads differ in size")
+        h = ctypes.c_void_p()
+        _check(lib().mq_register_ffn_gu(qtype, g.ctypes.data_as(ctypes.c_void_p),
+                                        u.ctypes.data_as(ctypes.c_void_p), g.nbytes, N, K, flags,
+                                        ctypes.byref(h)))
+        self.handle = h
+        self.qtype, self.N, self.K = qtype, N, K
+        self.nbytes = 2 * g.nbytes
+
+
+def register_ffn_gu(qtype, gate, up, N, K, flags=REG_DEFAULT) -> FfnGuWeight:
+    return FfnGuWeight(qtype, gate, up, N, K, flags)
+
+
+def ffn_gu_matvec(W: FfnGuWeight, x, h=None, stream=None):
+    """h[B][N] = silu(W_gate x) * (W_up x) (x: CUDA f32 [B][K] or [K])."""
+    import torch
+    x2 = x.reshape(-1, W.K)
+    B = x2.shape[0]
+    if h is None:
+        h = torch.empty((B, W.N), dtype=torch.float32, device=x.device)
+    _check(lib().mq_ffn_gu_matvec(W.qtype, W.handle, _ptr(x2), _ptr(h), W.N, W.K, B,
+                                  _stream(stream)))
+    return h
+
+
+def ffn_gu_mmq(W: FfnGuWeight, xq, M: int, h=None, stream=None):
+    """h[M][N] = silu(W_gate a) * (W_up a) for the quantised activations xq."""
+    import torch
+    if h is None:
+        h = torch.empty((M, W.N), dtype=torch.float32, device=xq.device)
+    _check(lib().mq_ffn_gu_mmq(W.qtype, W.handle, _ptr(xq), _ptr(h), M, W.N, W.K,
+                               _stream(stream)))
+    return h
 
 
 def matvec(W: Weight, x, y=None, stream=None):

@@ -80,6 +80,7 @@ struct MvArgs {
   int B;
   int nchunk;  // ceil(K / 256)
   int S;       // K slices (cluster size)
+  int swiglu;  // fused gate/up weight: y[b][n] = silu(gate row) * (its up row), N / 2 wide
   int *status;
 };
 
@@ -596,6 +597,23 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int 
   }
 }
 
+// Results of the thread's row pair (rA, rA + 8) for batch row b.  A fused gate/up
+// weight has rows in units of 16 (8 gate rows, then the same 8 rows of the up
+// weight), so rA is a gate row and rA + 8 its up row: one SwiGLU output,
+// silu(g) * u with silu(v) = v / (1 + e^-v), at output row 8 * (rA / 16) + rA % 8.
+__device__ __forceinline__ void store_rows(const MvArgs &p, int b, int64_t rA, float vA,
+                                           float vB) {
+  if (p.swiglu) {
+    if (rA < p.N) {
+      const int64_t nout = p.N >> 1;
+      p.y[int64_t(b) * nout + (rA >> 4) * 8 + (rA & 7)] = vA / (1.f + expf(-vA)) * vB;
+    }
+    return;
+  }
+  if (rA < p.N) p.y[int64_t(b) * p.N + rA] = vA;
+  if (rA + 8 < p.N) p.y[int64_t(b) * p.N + rA + 8] = vB;
+}
+
 template <int TYPE, int NT>
 __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -668,17 +686,13 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
     }
   }
 
-  const int64_t rA = group * kRows + 16 * warp + g, rB = rA + 8;
-  const bool okA = rA < p.N, okB = rB < p.N;
+  const int64_t rA = group * kRows + 16 * warp + g;
   if (p.S == 1) {
     if (warp < kCompute) {
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         const int b = t + 4 * i;
-        if (b < p.B) {
-          if (okA) p.y[int64_t(b) * p.N + rA] = tot[0][i];
-          if (okB) p.y[int64_t(b) * p.N + rB] = tot[1][i];
-        }
+        if (b < p.B) store_rows(p, b, rA, tot[0][i], tot[1][i]);
       }
     }
     return;
@@ -705,10 +719,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
         sA += rp[16 * warp + g][b];
         sB += rp[16 * warp + g + 8][b];
       }
-      if (b < p.B) {
-        if (okA) p.y[int64_t(b) * p.N + rA] = sA;
-        if (okB) p.y[int64_t(b) * p.N + rB] = sB;
-      }
+      if (b < p.B) store_rows(p, b, rA, sA, sB);
     }
   }
   cluster.sync();
@@ -794,6 +805,7 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.B = B;
   a.nchunk = (int)((W->K + kChunk - 1) / kChunk);
   a.S = choose_split(W->N, W->K, st->sms);
+  a.swiglu = W->ffn_gu;
   a.status = st->status;
   const bool two = B > 4;
   switch (W->type) {

@@ -90,6 +90,7 @@ struct TcArgs {
   int nms;              // Q4_K: ring stages of the min-term GEMM (3*nb/64 rounded up)
   int *status;
   int debug_expire;
+  int swiglu;           // fused gate/up weight: y[m][n'] = silu(gate col) * (its up col), N / 2 wide
 };
 
 // Arrays that some block types do not need take (almost) no space; every slot
@@ -475,7 +476,29 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
     }
     if constexpr (!DOTS) {
-      if (mok) {
+      if (mok && p.swiglu) {
+        // columns in units of 16: 8 gate columns, then the same 8 columns of the up
+        // weight; the thread's 32 columns give 16 outputs silu(g) * u
+        const int64_t nout = p.N >> 1, c0 = n0 + EC * hcol, left = p.N - c0;
+        float h[EC / 2];
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int cg = 16 * v + j, cu = cg + 8;
+            const float gv = (cg & 1) ? y[cg >> 1].y : y[cg >> 1].x;
+            const float uv = (cu & 1) ? y[cu >> 1].y : y[cu >> 1].x;
+            h[8 * v + j] = gv / (1.f + expf(-gv)) * uv;
+          }
+        float *dst = p.y + m * nout + (c0 >> 1);
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          if (left >= 16 * (v + 1))
+#pragma unroll
+            for (int j = 0; j < 8; j += 4)
+              *reinterpret_cast<float4 *>(dst + 8 * v + j) =
+                  make_float4(h[8 * v + j], h[8 * v + j + 1], h[8 * v + j + 2], h[8 * v + j + 3]);
+      } else if (mok) {
         float *dst = p.y + m * p.N + n0 + EC * hcol;
         const int64_t left = p.N - (n0 + EC * hcol);
         if (left >= EC && (p.N & 3) == 0) {
@@ -662,6 +685,7 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   a.ntiles = (int)(ntm * ntn);
   a.status = st->status;
   a.debug_expire = debug_expire;
+  a.swiglu = W->ffn_gu;
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:

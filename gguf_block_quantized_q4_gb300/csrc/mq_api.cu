@@ -158,9 +158,9 @@ static mq_status alloc_plane(T **p, size_t bytes, size_t *total, const char *wha
   return MQ_OK;
 }
 
-extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, size_t nbytes,
-                                        int64_t N, int64_t K, uint32_t flags, mq_weight **out) {
-  const char *site = "mq_register_weight";
+static mq_status register_impl(const char *site, mq_type type, const void *host_bytes,
+                               size_t nbytes, int64_t N, int64_t K, uint32_t flags, int ffn_gu,
+                               mq_weight **out) {
   if (!out) return fail(MQ_ERR_ARG, "%s: out is NULL", site);
   *out = nullptr;
   mq_status s = check_type_shape(site, type, N, K);
@@ -180,6 +180,7 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
 
   mq_weight *w = new mq_weight();
   w->type = type;
+  w->ffn_gu = ffn_gu;
   w->N = N;
   w->K = K;
   w->np = round_up(N, 128);
@@ -250,6 +251,39 @@ extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, si
   return MQ_OK;
 }
 
+extern "C" mq_status mq_register_weight(mq_type type, const void *host_bytes, size_t nbytes,
+                                        int64_t N, int64_t K, uint32_t flags, mq_weight **out) {
+  return register_impl("mq_register_weight", type, host_bytes, nbytes, N, K, flags, 0, out);
+}
+
+// Rows of a fused gate/up weight, in units of 16: 8 gate rows, then the same 8 rows of
+// the up weight (a kernel thread then holds a gate result and its up result).
+extern "C" mq_status mq_register_ffn_gu(mq_type type, const void *gate_bytes,
+                                        const void *up_bytes, size_t nbytes_each, int64_t N,
+                                        int64_t K, uint32_t flags, mq_weight **out) {
+  const char *site = "mq_register_ffn_gu";
+  if (!out) return fail(MQ_ERR_ARG, "%s: out is NULL", site);
+  *out = nullptr;
+  mq_status s = check_type_shape(site, type, 2 * N, K);
+  if (s != MQ_OK) return s;
+  if (N % 8)
+    return fail(MQ_ERR_SHAPE, "%s: N=%lld gate rows must be a multiple of 8", site, (long long)N);
+  const size_t row = size_t(K / block_elems(type)) * size_t(block_bytes(type));
+  if (nbytes_each != size_t(N) * row)
+    return fail(MQ_ERR_PAYLOAD,
+                "%s: nbytes_each is %zu but a type-%d %lld x %lld tensor is exactly %zu bytes",
+                site, nbytes_each, type, (long long)N, (long long)K, size_t(N) * row);
+  if (!gate_bytes || !up_bytes) return fail(MQ_ERR_ARG, "%s: gate_bytes or up_bytes is NULL", site);
+  std::vector<uint8_t> fused(2 * nbytes_each);
+  const uint8_t *g = static_cast<const uint8_t *>(gate_bytes);
+  const uint8_t *u = static_cast<const uint8_t *>(up_bytes);
+  for (int64_t k = 0; k < N / 8; ++k) {
+    memcpy(fused.data() + size_t(16 * k) * row, g + size_t(8 * k) * row, 8 * row);
+    memcpy(fused.data() + size_t(16 * k + 8) * row, u + size_t(8 * k) * row, 8 * row);
+  }
+  return register_impl(site, type, fused.data(), fused.size(), 2 * N, K, flags, 1, out);
+}
+
 extern "C" mq_status mq_weight_free(mq_weight *w) {
   if (!w) return MQ_OK;
   int cur = 0;
@@ -294,6 +328,16 @@ extern "C" mq_status mq_weight_unpack(const mq_weight *w, void *host_bytes, size
   if (s != MQ_OK) return s;
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync", site);
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamSynchronize", site);
+  if (w->ffn_gu) {  // back from the interleaved row order to gate rows, then up rows
+    const size_t row = nbytes / size_t(w->N), half = nbytes / 2;
+    std::vector<uint8_t> tmp(static_cast<uint8_t *>(host_bytes),
+                             static_cast<uint8_t *>(host_bytes) + nbytes);
+    uint8_t *dst = static_cast<uint8_t *>(host_bytes);
+    for (int64_t k = 0; k < w->N / 16; ++k) {
+      memcpy(dst + size_t(8 * k) * row, tmp.data() + size_t(16 * k) * row, 8 * row);
+      memcpy(dst + half + size_t(8 * k) * row, tmp.data() + size_t(16 * k + 8) * row, 8 * row);
+    }
+  }
   return MQ_OK;
 }
 
@@ -320,8 +364,15 @@ static mq_status check_dev_ptr(const char *site, const char *name, const void *p
 }
 
 static mq_status check_weight(const char *site, int type, const mq_weight *W, int64_t N,
-                              int64_t K) {
+                              int64_t K, int ffn_gu = 0) {
   if (!W) return fail(MQ_ERR_ARG, "%s: W is NULL", site);
+  if (W->ffn_gu != ffn_gu)
+    return fail(MQ_ERR_ARG,
+                ffn_gu ? "%s: the weight is not a fused gate/up weight (mq_register_ffn_gu)"
+                       : "%s: the weight is a fused gate/up weight; use mq_ffn_gu_matvec or "
+                         "mq_ffn_gu_mmq",
+                site);
+  if (ffn_gu) N *= 2;  // the fused weight holds the gate and the up rows
   mq_status s = check_type_shape(site, type, N, K);
   if (s != MQ_OK) return s;
   if (W->type != type)
@@ -338,10 +389,10 @@ static mq_status check_weight(const char *site, int type, const mq_weight *W, in
   return MQ_OK;
 }
 
-extern "C" mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y,
-                               int64_t N, int64_t K, int B, mq_stream stream) {
-  const char *site = "mq_matvec";
-  mq_status s = check_weight(site, type, W, N, K);
+static mq_status matvec_impl(const char *site, int ffn_gu, mq_type type, const mq_weight *W,
+                             const float *x, float *y, int64_t N, int64_t K, int B,
+                             mq_stream stream) {
+  mq_status s = check_weight(site, type, W, N, K, ffn_gu);
   if (s != MQ_OK) return s;
   if (B < 1 || B > kMaxB)
     return fail(MQ_ERR_ARG, "%s: B=%d outside [1, %d]", site, B, kMaxB);
@@ -350,6 +401,16 @@ extern "C" mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x,
   if ((s = check_dev_ptr(site, "x", x, W->device, 16)) != MQ_OK) return s;
   if ((s = check_dev_ptr(site, "y", y, W->device, 16)) != MQ_OK) return s;
   return launch_matvec(W, x, y, B, (cudaStream_t)stream, st);
+}
+
+extern "C" mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y,
+                               int64_t N, int64_t K, int B, mq_stream stream) {
+  return matvec_impl("mq_matvec", 0, type, W, x, y, N, K, B, stream);
+}
+
+extern "C" mq_status mq_ffn_gu_matvec(mq_type type, const mq_weight *W, const float *x, float *h,
+                                      int64_t N, int64_t K, int B, mq_stream stream) {
+  return matvec_impl("mq_ffn_gu_matvec", 1, type, W, x, h, N, K, B, stream);
 }
 
 extern "C" size_t mq_act_bytes(int64_t M, int64_t K) {
@@ -386,8 +447,9 @@ static int test_expire_wait() {
 }
 
 static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, const void *xq,
-                            const void *out, int64_t M, int64_t N, int64_t K, DeviceState **st) {
-  mq_status s = check_weight(site, type, W, N, K);
+                            const void *out, int64_t M, int64_t N, int64_t K, DeviceState **st,
+                            int ffn_gu = 0) {
+  mq_status s = check_weight(site, type, W, N, K, ffn_gu);
   if (s != MQ_OK) return s;
   if (!W->mw)
     return fail(MQ_ERR_ARG, "%s: the weight was registered with MQ_REG_NO_MMQ_PLANE", site);
@@ -405,6 +467,14 @@ extern "C" mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, fl
   mq_status s = mmq_common("mq_mmq", type, W, xq, y, M, N, K, &st);
   if (s != MQ_OK) return s;
   return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait());
+}
+
+extern "C" mq_status mq_ffn_gu_mmq(mq_type type, const mq_weight *W, const void *xq, float *h,
+                                   int64_t M, int64_t N, int64_t K, mq_stream stream) {
+  DeviceState *st = nullptr;
+  mq_status s = mmq_common("mq_ffn_gu_mmq", type, W, xq, h, M, N, K, &st, 1);
+  if (s != MQ_OK) return s;
+  return launch_mmq(W, xq, h, nullptr, M, (cudaStream_t)stream, st, test_expire_wait());
 }
 
 extern "C" mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const void *xq,

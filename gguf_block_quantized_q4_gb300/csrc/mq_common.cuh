@@ -53,6 +53,8 @@ struct mq_weight {
   int nchunk;            // decode-plane K chunks (K / 256 rounded up)
   int device;
   size_t payload;        // GGUF bytes
+  int ffn_gu = 0;        // fused gate/up weight: rows in units of 16 = 8 gate rows, then
+                         // the same 8 rows of the up weight (N = 2 x the gate rows)
   size_t device_bytes;   // all planes
   // decode planes
   uint8_t *q = nullptr;  // Q8_0 qs / Q4_K and Q6_K tiles

@@ -174,6 +174,38 @@ mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int
 mq_status mq_mmq_blockdots(mq_type type, const mq_weight *W, const void *xq, int32_t *D,
                            int64_t M, int64_t N, int64_t K, mq_stream stream);
 
+/* ---- fused FFN gate/up with SwiGLU ("minfer CUDA Backend Design" §4.3: the FusedFFN
+ * and SwiGLU ops; §4.6: the loader's ffn_gu concat of the gate and up weights).  The
+ * pages name the operation without writing it out; it is read as the usual
+ * h = silu(W_gate x) * (W_up x), silu(v) = v / (1 + e^-v), elementwise. */
+
+/* mq_register_ffn_gu -- register the gate and up weights of one FFN as a single fused
+ * weight of 2N rows.  gate_bytes, up_bytes: raw GGUF bytes of an N x K tensor each
+ * (host memory, read only during the call), nbytes_each = the exact size of one of
+ * them; N % 8 == 0.  The rows are stored in units of 16 (8 gate rows, then the same 8
+ * rows of the up weight), so one kernel thread holds a gate result and its up result.
+ * flags as for mq_register_weight.  mq_weight_unpack returns the gate bytes followed by
+ * the up bytes.  A fused weight is used only through mq_ffn_gu_matvec / mq_ffn_gu_mmq
+ * (the plain calls return MQ_ERR_ARG, and vice versa).  mq_weight_info reports 2N rows.
+ * Errors as for mq_register_weight; MQ_ERR_SHAPE if N % 8 != 0. */
+mq_status mq_register_ffn_gu(mq_type type, const void *gate_bytes, const void *up_bytes,
+                             size_t nbytes_each, int64_t N, int64_t K, uint32_t flags,
+                             mq_weight **out);
+
+/* mq_ffn_gu_matvec -- decode form: h[b][n] = silu(g[b][n]) * u[b][n] with
+ * g = W_gate x, u = W_up x computed as by mq_matvec (same kernels, one launch).
+ * x: device f32 [B][K]; h: device f32 [B][N] (N = gate rows); 1 <= B <= 8.
+ * Within silu's slope (<= 1.1) times the matvec bound of g, times |u|, plus
+ * |silu(g)| times the bound of u. */
+mq_status mq_ffn_gu_matvec(mq_type type, const mq_weight *W, const float *x, float *h,
+                           int64_t N, int64_t K, int B, mq_stream stream);
+
+/* mq_ffn_gu_mmq -- prefill form: h[m][n] = silu(g[m][n]) * u[m][n] with g, u computed
+ * as by mq_mmq from xq (mq_quantize_act(M, K)).  h: device f32 [M][N]; the weight must
+ * have its MMQ planes.  Bound as for mq_ffn_gu_matvec with the MMQ bounds of g and u. */
+mq_status mq_ffn_gu_mmq(mq_type type, const mq_weight *W, const void *xq, float *h, int64_t M,
+                        int64_t N, int64_t K, mq_stream stream);
+
 /* mq_stream_status -- synchronise `stream`, then read and clear the current
  * device's status word written by bounded device-side waits.  Returns MQ_OK,
  * or MQ_ERR_TIMEOUT if a wait expired since the last call (the message names

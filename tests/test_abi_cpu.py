@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("mq_init", "mq_register_weight", "mq_matvec", "mq_quantize_act", "mq_mmq",
-                 "mq_mmq_blockdots", "mq_weight_unpack", "mq_stream_status", "mq_last_error"):
+                 "mq_mmq_blockdots", "mq_weight_unpack", "mq_stream_status", "mq_last_error",
+                 "mq_register_ffn_gu", "mq_ffn_gu_matvec", "mq_ffn_gu_mmq"):
         assert must in names
 
 
@@ -140,3 +141,27 @@ def test_last_error_is_per_thread(L):
     th.join()
     assert seen["msg"] == "no error"
     assert "W is NULL" in L.mq_last_error().decode()
+
+
+def _reg_gu(L, qtype, gate, up, nbytes_each, N, K, flags=0):
+    h = ctypes.c_void_p()
+    g = np.ascontiguousarray(gate, dtype=np.uint8)
+    u = np.ascontiguousarray(up, dtype=np.uint8)
+    st = L.mq_register_ffn_gu(qtype, g.ctypes.data_as(ctypes.c_void_p),
+                              u.ctypes.data_as(ctypes.c_void_p), nbytes_each, N, K, flags,
+                              ctypes.byref(h))
+    return st, L.mq_last_error().decode()
+
+
+def test_ffn_gu_registration_validates_before_device_work(L):
+    row = 256 // 256 * 144
+    z = np.zeros(16 * row, np.uint8)
+    st, msg = _reg_gu(L, mq.Q4_K, z, z, 12 * row, 12, 256)  # N not a multiple of 8
+    assert mq.STATUS[st] == "MQ_ERR_SHAPE" and "multiple of 8" in msg
+    st, msg = _reg_gu(L, mq.Q4_K, z, z, 16 * row - 1, 16, 256)
+    assert mq.STATUS[st] == "MQ_ERR_PAYLOAD" and str(16 * row) in msg
+    st, msg = _reg_gu(L, 3, z, z, 16 * row, 16, 256)
+    assert mq.STATUS[st] == "MQ_ERR_TYPE"
+    h = ctypes.c_void_p()
+    st = L.mq_register_ffn_gu(mq.Q4_K, None, None, 16 * row, 16, 256, 0, ctypes.byref(h))
+    assert mq.STATUS[st] == "MQ_ERR_ARG" and "NULL" in L.mq_last_error().decode()
