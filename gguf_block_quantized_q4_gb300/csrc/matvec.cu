@@ -89,10 +89,11 @@ template <int TYPE>
 __host__ __device__ constexpr int tile_bytes() {
   return kRows * (TYPE == MQ_Q4_K ? 144 : (TYPE == MQ_Q6_K ? 210 : 256 + 16));
 }
-// Weight-ring depth: two CTAs per SM must fit in shared memory.
+// Weight-ring depth: two CTAs per SM must fit in shared memory; within that, the depth
+// that measured fastest (Q4_K B <= 4: 2 stages beat 3 and 4).
 template <int TYPE, int NT>
 __host__ __device__ constexpr int ring_stages() {
-  return TYPE == MQ_Q4_K ? (NT == 1 ? 4 : 3) : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
+  return TYPE == MQ_Q4_K ? (NT == 1 ? 2 : 3) : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
 }
 // Fragment-ring depth.
 template <int TYPE>
