@@ -17,7 +17,9 @@
  *    included (the block scales d and dmin are binary16).
  *  - dequantisation of one weight row, per the GGUF block layouts whose byte
  *    ratios the minfer "CUDA Backend Design" page gives in §2.3 (q8_0 34 bytes
- *    per 32 elements, q4_K 144 per 256, q6_K 210 per 256) and whose field
+ *    per 32 elements, q4_K 144 per 256, q6_K 210 per 256; q4_0 and q5_K, among
+ *    the types the page's weight gate admits in §4.6, 18 per 32 and 176 per 256)
+ *    and whose field
  *    layout is the public ggml block format, restated in prose in the header
  *    of each function below.
  *  - the decode matvec reference y[b][n] = sum_k w[n][k] * x[b][k] in double,
@@ -41,8 +43,10 @@
 #include <stdlib.h>
 #include <string.h>
 
+#define OR_Q4_0 2
 #define OR_Q8_0 8
 #define OR_Q4_K 12
+#define OR_Q5_K 13
 #define OR_Q6_K 14
 
 /* ---- IEEE binary16 -> double ------------------------------------------ */
@@ -69,8 +73,10 @@ static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); 
 int oracle_block_elems(int type)
 {
     switch (type) {
+    case OR_Q4_0: return 32;
     case OR_Q8_0: return 32;
     case OR_Q4_K: return 256;
+    case OR_Q5_K: return 256;
     case OR_Q6_K: return 256;
     default: return 0;
     }
@@ -79,8 +85,10 @@ int oracle_block_elems(int type)
 int oracle_block_bytes(int type)
 {
     switch (type) {
+    case OR_Q4_0: return 18;
     case OR_Q8_0: return 34;
     case OR_Q4_K: return 144;
+    case OR_Q5_K: return 176;
     case OR_Q6_K: return 210;
     default: return 0;
     }
@@ -102,9 +110,15 @@ void oracle_q4_k_scale_min(const uint8_t *s12, int j, int *sc, int *mn)
 
 /* Integer weight of element e of one block, and the block-level scales.
  * The dequantised weight is  w = dscale * wint - dmin_term, where
+ *   q4_0: wint = nib(e) - 8,           dscale = d, dmin_term = 0
  *   q8_0: wint = q[e],                 dscale = d, dmin_term = 0
  *   q4_K: wint = sc_j * nib(e),        dscale = d, dmin_term = dmin * m_j
+ *   q5_K: wint = sc_j * q5(e),         dscale = d, dmin_term = dmin * m_j
  *   q6_K: wint = sc[16-group] * (q-32), dscale = d, dmin_term = 0
+ * q4_0 (d f16 at 0, 16 quant bytes at 2): element e = 16h + j, nib = (qs[j] >> 4h) & 15.
+ * q5_K (d, dmin f16 at 0 and 2, 12 scale bytes at 4 packed as in q4_K, 32 high-bit
+ *   bytes at 16, 128 quant bytes at 48): element e = 64c + 32h + l,
+ *   q5 = ((qs[32c+l] >> 4h) & 15) | ((qh[l] >> (2c + h)) & 1) << 4, j = 2c + h.
  * q4_K element e = 64c + 32h + l: nib = (qs[32c+l] >> 4h) & 15, j = 2c + h.
  * q6_K element e = 128h + 32r + l:
  *   lo4 = ql[64h + 32(r%2) + l], low nibble for r < 2, high nibble for r >= 2
@@ -115,6 +129,16 @@ static void block_elem(int type, const uint8_t *blk, int e, int64_t *wint, int *
     *mterm = 0;
     if (type == OR_Q8_0) {
         *wint = (int8_t)blk[2 + e];
+    } else if (type == OR_Q4_0) {
+        int h = e / 16, j = e % 16;
+        *wint = ((blk[2 + j] >> (4 * h)) & 15) - 8;
+    } else if (type == OR_Q5_K) {
+        int c = e / 64, h = (e / 32) % 2, l = e % 32;
+        int q5 = ((blk[48 + 32 * c + l] >> (4 * h)) & 15) | (((blk[16 + l] >> (2 * c + h)) & 1) << 4);
+        int sc, mn;
+        oracle_q4_k_scale_min(blk + 4, 2 * c + h, &sc, &mn);
+        *wint = (int64_t)sc * q5;
+        *mterm = mn;
     } else if (type == OR_Q4_K) {
         int c = e / 64, h = (e / 32) % 2, l = e % 32;
         int nib = (blk[16 + 32 * c + l] >> (4 * h)) & 15;
@@ -135,14 +159,14 @@ static void block_elem(int type, const uint8_t *blk, int e, int64_t *wint, int *
 
 static double block_d(int type, const uint8_t *blk)
 {
-    if (type == OR_Q8_0) return oracle_f16_to_double(rd16(blk));
-    if (type == OR_Q4_K) return oracle_f16_to_double(rd16(blk));
+    if (type == OR_Q8_0 || type == OR_Q4_0) return oracle_f16_to_double(rd16(blk));
+    if (type == OR_Q4_K || type == OR_Q5_K) return oracle_f16_to_double(rd16(blk));
     return oracle_f16_to_double(rd16(blk + 208));
 }
 
 static double block_dmin(int type, const uint8_t *blk)
 {
-    return type == OR_Q4_K ? oracle_f16_to_double(rd16(blk + 2)) : 0.0;
+    return (type == OR_Q4_K || type == OR_Q5_K) ? oracle_f16_to_double(rd16(blk + 2)) : 0.0;
 }
 
 static int valid_shape(int type, int64_t K)

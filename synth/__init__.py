@@ -17,6 +17,11 @@ Field distributions follow the five hot-path workloads (Qwen2.5-0.5B/7B shaped):
 * Q6_K (256 elements, 210 bytes): ``ql`` (128) and ``qh`` (64) bytes uniform on
   [0, 255] (so each 6-bit quant is uniform on [0, 63]), 16 int8 sub-scales uniform on
   [-128, 127], f16 ``d = |N| * 0.005``.
+* Q4_0 (32 elements, 18 bytes): f16 ``d = |N| * 0.02`` then 16 quant bytes uniform on
+  [0, 255] (each 4-bit quant uniform on [0, 15]).
+* Q5_K (256 elements, 176 bytes): as Q4_K (f16 ``d = |N| * 0.02``, ``dmin = |N| * 0.01``,
+  12 scale bytes) then 32 high-bit bytes and 128 quant bytes, all uniform on [0, 255]
+  (each 5-bit quant uniform on [0, 31]).
 * activations: f32 ``N(0,1) * x_scale``.
 
 Random draws use ``numpy.random.Generator(PCG64(seed))``; within a weight the
@@ -26,11 +31,12 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K = 8, 12, 14  # GGUF type ids
+Q4_0, Q8_0, Q4_K, Q5_K, Q6_K = 2, 8, 12, 13, 14  # GGUF type ids
 
 # type id -> (elements per block, bytes per block)
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
-TYPE_NAME = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
+BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176),
+         Q6_K: (256, 210)}
+TYPE_NAME = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
 
 
 def nbytes(qtype: int, N: int, K: int) -> int:
@@ -76,8 +82,34 @@ def q6_k_weights(N: int, K: int, seed: int, d_scale: float = 0.005) -> np.ndarra
     return out.reshape(-1)
 
 
+def q4_0_weights(N: int, K: int, seed: int, d_scale: float = 0.02) -> np.ndarray:
+    nb = N * (K // 32)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty((nb, 18), dtype=np.uint8)
+    out[:, 0:2] = _absnormal_f16(rng, nb, d_scale).view(np.uint8).reshape(nb, 2)
+    out[:, 2:18] = rng.integers(0, 256, size=(nb, 16), dtype=np.uint8)
+    return out.reshape(-1)
+
+
+def q5_k_weights(N: int, K: int, seed: int, d_scale: float = 0.02,
+                 dmin_scale: float = 0.01) -> np.ndarray:
+    nb = N * (K // 256)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty((nb, 176), dtype=np.uint8)
+    out[:, 0:2] = _absnormal_f16(rng, nb, d_scale).view(np.uint8).reshape(nb, 2)
+    out[:, 2:4] = _absnormal_f16(rng, nb, dmin_scale).view(np.uint8).reshape(nb, 2)
+    out[:, 4:16] = rng.integers(0, 256, size=(nb, 12), dtype=np.uint8)
+    out[:, 16:48] = rng.integers(0, 256, size=(nb, 32), dtype=np.uint8)
+    out[:, 48:176] = rng.integers(0, 256, size=(nb, 128), dtype=np.uint8)
+    return out.reshape(-1)
+
+
 def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
     """Raw GGUF bytes of an N x K weight, rows contiguous, blocks along K."""
+    if qtype == Q4_0:
+        return q4_0_weights(N, K, seed)
+    if qtype == Q5_K:
+        return q5_k_weights(N, K, seed)
     if qtype == Q8_0:
         return q8_0_weights(N, K, seed)
     if qtype == Q4_K:

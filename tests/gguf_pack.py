@@ -1,6 +1,6 @@
 """Test-side block encoders: build GGUF block bytes from chosen integer fields.
 
-These are the inverse of the block layouts (GGUF q8_0 / q4_K / q6_K), written
+These are the inverse of the block layouts (GGUF q4_0 / q8_0 / q4_K / q5_K / q6_K), written
 independently of the oracle so that the oracle's decoders can be checked
 against blocks whose field values the tests choose.  Also a vectorised numpy
 decoder: a second, loop-free formulation used to cross-check the oracle.
@@ -68,6 +68,33 @@ def pack_q6_k(d_bits: int, scales, q) -> bytes:
                                                                         d_bits >> 8])
 
 
+def pack_q4_0(d_bits: int, q) -> bytes:
+    """q[e] in -8..7 for e in 0..31; element j < 16 is the low nibble of quant byte j,
+    element 16 + j its high nibble (stored value q + 8)."""
+    q = np.asarray(q, dtype=np.int64)
+    assert q.shape == (32,) and q.min() >= -8 and q.max() <= 7
+    qs = bytes(int(q[j] + 8) | (int(q[16 + j] + 8) << 4) for j in range(16))
+    return bytes([d_bits & 255, d_bits >> 8]) + qs
+
+
+def pack_q5_k(d_bits: int, dmin_bits: int, sc, mn, q5) -> bytes:
+    """q5[e] in 0..31 for e in 0..255; element 64c + 32h + l: low 4 bits in quant byte
+    32c + l (low nibble for h = 0, high for h = 1), fifth bit at bit 2c + h of high-bit
+    byte l."""
+    q5 = np.asarray(q5, dtype=np.int64)
+    assert q5.shape == (256,) and q5.min() >= 0 and q5.max() <= 31
+    qh = bytearray(32)
+    qs = bytearray(128)
+    for c in range(4):
+        for h in range(2):
+            for l in range(32):
+                v = int(q5[64 * c + 32 * h + l])
+                qs[32 * c + l] |= (v & 15) << (4 * h)
+                qh[l] |= (v >> 4) << (2 * c + h)
+    return (bytes([d_bits & 255, d_bits >> 8, dmin_bits & 255, dmin_bits >> 8]) +
+            pack_q4_k_scales(sc, mn) + bytes(qh) + bytes(qs))
+
+
 # ---- second formulation: vectorised numpy decoders ------------------------
 
 def _f16(u8pair: np.ndarray) -> np.ndarray:
@@ -94,6 +121,28 @@ def np_dequant(qtype: int, W: np.ndarray, N: int, K: int) -> np.ndarray:
         nib = np.stack([qs & 15, qs >> 4], axis=3)  # [N, nb, c, h, l]
         nib = nib.reshape(N, K // 256, 8, 32)  # sub-block j = 2c + h
         w = d[..., None, None] * sc[..., None] * nib - dmin[..., None, None] * mn[..., None]
+        return w.reshape(N, K)
+    if qtype == 2:
+        blk = W.reshape(N, K // 32, 18)
+        d = _f16(blk[:, :, 0:2])
+        qs = blk[:, :, 2:18].astype(np.int64)
+        q = np.concatenate([qs & 15, qs >> 4], axis=-1) - 8  # elements 0..15, 16..31
+        return (d[:, :, None] * q).reshape(N, K)
+    if qtype == 13:
+        blk = W.reshape(N, K // 256, 176)
+        d = _f16(blk[:, :, 0:2])
+        dmin = _f16(blk[:, :, 2:4])
+        s = blk[:, :, 4:16].astype(np.int64)
+        sc = np.concatenate([s[..., 0:4] & 63,
+                             (s[..., 8:12] & 15) | ((s[..., 0:4] >> 6) << 4)], axis=-1)
+        mn = np.concatenate([s[..., 4:8] & 63,
+                             (s[..., 8:12] >> 4) | ((s[..., 4:8] >> 6) << 4)], axis=-1)
+        qh = blk[:, :, 16:48].astype(np.int64)[:, :, None, :]  # [N, nb, 1, l]
+        qs = blk[:, :, 48:176].astype(np.int64).reshape(N, K // 256, 4, 32)
+        nib = np.stack([qs & 15, qs >> 4], axis=3).reshape(N, K // 256, 8, 32)  # j = 2c + h
+        hib = (qh >> np.arange(8)[None, None, :, None]) & 1  # bit j of byte l
+        q = nib | (hib << 4)
+        w = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
         return w.reshape(N, K)
     if qtype == 14:
         blk = W.reshape(N, K // 256, 210)
