@@ -21,9 +21,10 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmq.so")
 
-Q8_0, Q4_K, Q6_K = 8, 12, 14
+Q4_0, Q8_0, Q4_K, Q5_K, Q6_K = 2, 8, 12, 13, 14
 REG_DEFAULT, REG_NO_MMQ_PLANE = 0, 1
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176),
+         Q6_K: (256, 210)}
 
 STATUS = ["MQ_OK", "MQ_ERR_ARG", "MQ_ERR_TYPE", "MQ_ERR_SHAPE", "MQ_ERR_PAYLOAD",
           "MQ_ERR_ALIGN", "MQ_ERR_CUDA", "MQ_ERR_OOM", "MQ_ERR_LAUNCH", "MQ_ERR_TIMEOUT",

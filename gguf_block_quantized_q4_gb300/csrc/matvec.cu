@@ -87,18 +87,33 @@ struct MvArgs {
 // Bytes of one (128-row group, chunk) tile of the decode plane.
 template <int TYPE>
 __host__ __device__ constexpr int tile_bytes() {
-  return kRows * (TYPE == MQ_Q4_K ? 144 : (TYPE == MQ_Q6_K ? 210 : 256 + 16));
+  return kRows * (TYPE == MQ_Q4_K   ? 144
+                  : TYPE == MQ_Q5_K ? 176
+                  : TYPE == MQ_Q6_K ? 210
+                  : TYPE == MQ_Q4_0 ? 128 + 16
+                                    : 256 + 16);
 }
 // Weight-ring depth: two CTAs per SM must fit in shared memory; within that, the depth
 // that measured fastest (Q4_K B <= 4: 2 stages beat 3 and 4).
 template <int TYPE, int NT>
 __host__ __device__ constexpr int ring_stages() {
-  return TYPE == MQ_Q4_K ? (NT == 1 ? 2 : 3) : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
+  return (TYPE == MQ_Q4_K || TYPE == MQ_Q5_K) ? (NT == 1 ? 2 : 3)
+                                              : (TYPE == MQ_Q6_K && NT == 1 ? 3 : 2);
 }
 // Fragment-ring depth.
 template <int TYPE>
 __host__ __device__ constexpr int frag_slots() {
-  return TYPE == MQ_Q4_K ? 3 : 2;
+  return (TYPE == MQ_Q4_K || TYPE == MQ_Q5_K) ? 3 : 2;
+}
+// The super-block types with a sub-block min term (their x warp also stages sub-block sums).
+template <int TYPE>
+__host__ __device__ constexpr bool kmin_type() {
+  return TYPE == MQ_Q4_K || TYPE == MQ_Q5_K;
+}
+// Bytes per 32-element block and tile row of the per-32-block types' quant plane.
+template <int TYPE>
+__host__ __device__ constexpr int q32_bytes() {
+  return TYPE == MQ_Q4_0 ? 16 : 32;
 }
 
 // Per-warp tables decoded from the tile headers of the warp's 16 rows.
@@ -118,12 +133,16 @@ template <>
 struct WarpTab<MQ_Q8_0> {
   float2 s[8][8];  // [32-element block][g]: d of rows g, g+8
 };
+template <>
+struct WarpTab<MQ_Q4_0> : WarpTab<MQ_Q8_0> {};
+template <>
+struct WarpTab<MQ_Q5_K> : WarpTab<MQ_Q4_K> {};
 
 template <int TYPE, int NT>
 struct MvSmem {
   static constexpr int NS = ring_stages<TYPE, NT>();
   static constexpr int FS = frag_slots<TYPE>();
-  static constexpr int FG = TYPE == MQ_Q4_K ? 17 : 16;  // 16 groups (+ the Q4_K min group)
+  static constexpr int FG = kmin_type<TYPE>() ? 17 : 16;  // 16 groups (+ the min group)
   union {
     alignas(128) uint8_t w[NS][tile_bytes<TYPE>()];  // weight tiles
     float part[kRows][8];  // split-K partial sums (after the ring has drained)
@@ -238,16 +257,18 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
     const int c = c_begin + i, s = i % NS;
     const int cw = chunk_width(p.K, c);
     const uint32_t bar = sa(&sm.wfull[s]);
-    const uint32_t wbytes =
-        TYPE == MQ_Q8_0 ? (uint32_t)(kRows * cw + kRows * 16) : (uint32_t)tile_bytes<TYPE>();
+    constexpr bool Q32 = TYPE == MQ_Q8_0 || TYPE == MQ_Q4_0;  // per-32-block scales
+    constexpr int QB = q32_bytes<TYPE>();                       // quant bytes per block row
+    const uint32_t wbytes = Q32 ? (uint32_t)(kRows * (cw / 32) * QB + kRows * 16)
+                                : (uint32_t)tile_bytes<TYPE>();
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"(wbytes + (uint32_t)(p.B * cw * 4))
                  : "memory");
     uint8_t *w = sm.w[s];
-    if constexpr (TYPE == MQ_Q8_0) {
-      bulk_1d(sa(w), p.q + (group * p.K + int64_t(c) * kChunk) * kRows, (uint32_t)(kRows * cw),
-              bar);
-      bulk_1d(sa(w + kRows * 256), p.d + (group * p.nchunk + c) * kRows * 8, kRows * 16, bar);
+    if constexpr (Q32) {
+      bulk_1d(sa(w), p.q + (group * (p.K / 32) + int64_t(c) * 8) * kRows * QB,
+              (uint32_t)(kRows * (cw / 32) * QB), bar);
+      bulk_1d(sa(w + kRows * 8 * QB), p.d + (group * p.nchunk + c) * kRows * 8, kRows * 16, bar);
     } else {
       bulk_1d(sa(w), p.q + (group * p.nchunk + c) * int64_t(tile_bytes<TYPE>()),
               (uint32_t)tile_bytes<TYPE>(), bar);
@@ -311,7 +332,7 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
         const uint32_t lo23 = pack_f16x2(v2 - f16_lo(hi23), v3 - f16_hi(hi23));
         sm.frag[fs][g16][b >> 2][col * 4 + t] = make_uint2(hi01, hi23);
         sm.frag[fs][g16][b >> 2][(col + 1) * 4 + t] = make_uint2(lo01, lo23);
-        if constexpr (TYPE == MQ_Q4_K) {
+        if constexpr (kmin_type<TYPE>()) {
           // sum of sub-block j = f >> 3 (8 consecutive items), scaled by 1/32 so
           // that |sum| < 2^15 fits f16
           float ps = (v0 + v1) + (v2 + v3);
@@ -321,7 +342,7 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
           if ((lane & 7) == 0) sm.xs[f >> 3] = ps * 0.03125f;
         }
       }
-      if constexpr (TYPE == MQ_Q4_K) {
+      if constexpr (kmin_type<TYPE>()) {
         // min-term B fragment: lane (col', t') holds sums 2t', 2t'+1 (hi or lo part)
         __syncwarp();
         if (lane < 8) {
@@ -353,17 +374,30 @@ __device__ __forceinline__ void release_and_wait(uint64_t &wempty, uint64_t &ffu
 // ---------------------------------------------------------------------------
 // Compute warps.  Thread (g, t) of warp w covers tile rows ra = 16w + g and
 // rb = ra + 8; tot[0/1][i] accumulates rows ra/rb for batch row 4i + t.
-template <int NT>
-__device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s, int fs,
+// Shift left by sh (right by -sh when negative); sh is a constant once the loops that
+// compute it are unrolled, so the branch folds away.
+__device__ __forceinline__ uint32_t shl(uint32_t v, int sh) {
+  return sh >= 0 ? v << sh : v >> (-sh);
+}
+
+// Q4_K and Q5_K (rows of RS = 144 / 176 bytes; Q5_K's fifth bits follow the quants).
+// For Q5_K the fifth bit of each element goes to bit 4 (low-nibble path: 1024 + q) or
+// bit 8 (high-nibble path: 1024 + 16q) of its f16 half before the magic exponent is
+// OR-ed in, so q in [0, 31] takes the same exact multiply-add by sc (or sc/16): sc*q is
+// at most 63*31 = 1953 < 2048, exact in f16.
+template <int TYPE, int NT>
+__device__ __forceinline__ void compute_chunk_q4k(MvSmem<TYPE, NT> &sm, int s, int fs,
                                                   uint32_t fpar, int warp, int lane, int *status,
                                                   const int (&fl)[NT], float (&tot)[2][NT]) {
+  constexpr bool Q5 = TYPE == MQ_Q5_K;
+  constexpr int RS = Q5 ? 176 : 144;
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
   WarpTab<MQ_Q4_K> &tb = sm.tab[warp];
   {  // lane c'*8 + r decodes sub-blocks 2c', 2c'+1 of rows r and r+8 (entry = lane)
     const int cp = lane >> 3, r = lane & 7;
-    const uint4 ha = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r) * 144);
-    const uint4 hb = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r + 8) * 144);
+    const uint4 ha = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r) * RS);
+    const uint4 hb = *reinterpret_cast<const uint4 *>(tile + (16 * warp + r + 8) * RS);
     // 6-bit scales / mins of sub-blocks 4q..4q+3 as bytes (q = cp >> 1)
     uint32_t sa4, sb4, ma4, mb4;
     if (cp < 2) {
@@ -396,12 +430,17 @@ __device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s
   }
   __syncwarp();
   const int ra = 16 * warp + g, rb = ra + 8;
-  const uint4 a0 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 16 + 32 * t);
-  const uint4 a1 = *reinterpret_cast<const uint4 *>(tile + ra * 144 + 32 + 32 * t);
-  const uint4 b0 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 16 + 32 * t);
-  const uint4 b1 = *reinterpret_cast<const uint4 *>(tile + rb * 144 + 32 + 32 * t);
+  const uint4 a0 = *reinterpret_cast<const uint4 *>(tile + ra * RS + 16 + 32 * t);
+  const uint4 a1 = *reinterpret_cast<const uint4 *>(tile + ra * RS + 32 + 32 * t);
+  const uint4 b0 = *reinterpret_cast<const uint4 *>(tile + rb * RS + 16 + 32 * t);
+  const uint4 b1 = *reinterpret_cast<const uint4 *>(tile + rb * RS + 32 + 32 * t);
   const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
   const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  uint2 qha = make_uint2(0u, 0u), qhb = make_uint2(0u, 0u);  // Q5_K fifth-bit words (u = 0, 1)
+  if constexpr (Q5) {
+    qha = *reinterpret_cast<const uint2 *>(tile + ra * RS + 144 + 8 * t);
+    qhb = *reinterpret_cast<const uint2 *>(tile + rb * RS + 144 + 8 * t);
+  }
   release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
   // min term first: its MMA latency hides under the main loop
   float cm[NT][4];
@@ -428,14 +467,31 @@ __device__ __forceinline__ void compute_chunk_q4k(MvSmem<MQ_Q4_K, NT> &sm, int s
     for (int u = 0; u < 2; ++u) {
       const uint32_t xa = wa[2 * cp + u], xb = wb[2 * cp + u];
       const uint32_t xa8 = xa >> 8, xb8 = xb >> 8;
-      const uint32_t l0 = hfma2(and_or(xa, kLo, kMagic), slo.x, slo.y);
-      const uint32_t l1 = hfma2(and_or(xb, kLo, kMagic), slo.z, slo.w);
-      const uint32_t l2 = hfma2(and_or(xa8, kLo, kMagic), slo.x, slo.y);
-      const uint32_t l3 = hfma2(and_or(xb8, kLo, kMagic), slo.z, slo.w);
-      const uint32_t h0 = hfma2(and_or(xa, kHi, kMagic), shi.x, shi.y);
-      const uint32_t h1 = hfma2(and_or(xb, kHi, kMagic), shi.z, shi.w);
-      const uint32_t h2 = hfma2(and_or(xa8, kHi, kMagic), shi.x, shi.y);
-      const uint32_t h3 = hfma2(and_or(xb8, kHi, kMagic), shi.z, shi.w);
+      // the OR-ed exponent word of each register: the magic, plus the fifth bits for Q5_K
+      // (bit 2c' of bytes 0/2 or 1/3 of the fifth-bit word for the low nibbles, bit
+      // 2c' + 1 for the high nibbles)
+      uint32_t mla = kMagic, mlb = kMagic, mla8 = kMagic, mlb8 = kMagic;
+      uint32_t mha = kMagic, mhb = kMagic, mha8 = kMagic, mhb8 = kMagic;
+      if constexpr (Q5) {
+        constexpr uint32_t kB4 = 0x00100010u, kB8 = 0x01000100u;
+        const uint32_t qa = u ? qha.y : qha.x, qb = u ? qhb.y : qhb.x;
+        mla = and_or(shl(qa, 4 - 2 * cp), kB4, kMagic);
+        mlb = and_or(shl(qb, 4 - 2 * cp), kB4, kMagic);
+        mla8 = and_or(shl(qa, -4 - 2 * cp), kB4, kMagic);
+        mlb8 = and_or(shl(qb, -4 - 2 * cp), kB4, kMagic);
+        mha = and_or(shl(qa, 7 - 2 * cp), kB8, kMagic);
+        mhb = and_or(shl(qb, 7 - 2 * cp), kB8, kMagic);
+        mha8 = and_or(shl(qa, -1 - 2 * cp), kB8, kMagic);
+        mhb8 = and_or(shl(qb, -1 - 2 * cp), kB8, kMagic);
+      }
+      const uint32_t l0 = hfma2(and_or(xa, kLo, mla), slo.x, slo.y);
+      const uint32_t l1 = hfma2(and_or(xb, kLo, mlb), slo.z, slo.w);
+      const uint32_t l2 = hfma2(and_or(xa8, kLo, mla8), slo.x, slo.y);
+      const uint32_t l3 = hfma2(and_or(xb8, kLo, mlb8), slo.z, slo.w);
+      const uint32_t h0 = hfma2(and_or(xa, kHi, mha), shi.x, shi.y);
+      const uint32_t h1 = hfma2(and_or(xb, kHi, mhb), shi.z, shi.w);
+      const uint32_t h2 = hfma2(and_or(xa8, kHi, mha8), shi.x, shi.y);
+      const uint32_t h3 = hfma2(and_or(xb8, kHi, mhb8), shi.z, shi.w);
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         const uint2 bl = sm.frag[fs][4 * cp + u][i][fl[i]];      // sub-block 2c', K half u
@@ -529,17 +585,23 @@ __device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s
   }
 }
 
-template <int NT>
-__device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int s, int fs,
+// Q8_0 and Q4_0: one scale d per 32-element block, applied after the block's two MMAs.
+// Q4_0's word of a (block, row) holds the block's quant bytes 4t..4t+3 (order 0, 2, 1, 3):
+// its low nibbles are elements 4t..4t+3 of the first 16-element half, its high nibbles
+// those of the second; (1024 + n) - 1032 and (1024 + 16n)/16 - 72 give n - 8 exactly.
+template <int TYPE, int NT>
+__device__ __forceinline__ void compute_chunk_q8_0(MvSmem<TYPE, NT> &sm, int s, int fs,
                                                    uint32_t fpar, int warp, int lane,
                                                    int *status, int nblk, const int (&fl)[NT],
                                                    float (&tot)[2][NT]) {
+  constexpr bool Q4 = TYPE == MQ_Q4_0;
+  constexpr int QB = q32_bytes<TYPE>();
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
   WarpTab<MQ_Q8_0> &tb = sm.tab[warp];
   {  // lane (r, h): blocks 4h..4h+3 of row r (slots past the chunk's blocks hold 0)
     const int r = lane & 15, h = lane >> 4, row = 16 * warp + r;
-    const uint2 dv = *reinterpret_cast<const uint2 *>(tile + kRows * 256 + row * 16 + 8 * h);
+    const uint2 dv = *reinterpret_cast<const uint2 *>(tile + kRows * 8 * QB + row * 16 + 8 * h);
     float *dst = reinterpret_cast<float *>(&tb.s[4 * h][r & 7]) + (r >> 3);
     dst[0] = f16_lo(dv.x);
     dst[16] = f16_hi(dv.x);
@@ -551,8 +613,14 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int 
   uint2 va[8], vb[8];  // blocks past the chunk's end hold stale but finite bytes
 #pragma unroll
   for (int blk = 0; blk < 8; ++blk) {
-    va[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + ra) * 32 + 8 * t);
-    vb[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + rb) * 32 + 8 * t);
+    if constexpr (Q4) {
+      va[blk].x = *reinterpret_cast<const uint32_t *>(tile + (blk * kRows + ra) * 16 + 4 * t);
+      vb[blk].x = *reinterpret_cast<const uint32_t *>(tile + (blk * kRows + rb) * 16 + 4 * t);
+      va[blk].y = vb[blk].y = 0u;
+    } else {
+      va[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + ra) * 32 + 8 * t);
+      vb[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + rb) * 32 + 8 * t);
+    }
   }
   release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
   float acc[2][NT];
@@ -571,11 +639,30 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<MQ_Q8_0, NT> &sm, int 
         for (int r = 0; r < 4; ++r) c4[i][r] = 0.f;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint32_t qA = wa[u] ^ 0x80808080u, qB = wb[u] ^ 0x80808080u;
-        const uint32_t a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
-        const uint32_t a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
-        const uint32_t a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
-        const uint32_t a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (Q4) {
+          constexpr uint32_t kM = 0x64006400u, kLo = 0x000f000fu, kHi = 0x00f000f0u;
+          constexpr uint32_t k1032 = 0x64086408u;                  // f16x2 (1032, 1032)
+          constexpr uint32_t kSixteenth = 0x2C002C00u, kM72 = 0xD480D480u;  // 1/16, -72
+          const uint32_t xA = wa[0], xB = wb[0], xA8 = xA >> 8, xB8 = xB >> 8;
+          if (u == 0) {
+            a0 = hsub2(and_or(xA, kLo, kM), k1032);
+            a2 = hsub2(and_or(xA8, kLo, kM), k1032);
+            a1 = hsub2(and_or(xB, kLo, kM), k1032);
+            a3 = hsub2(and_or(xB8, kLo, kM), k1032);
+          } else {
+            a0 = hfma2(and_or(xA, kHi, kM), kSixteenth, kM72);
+            a2 = hfma2(and_or(xA8, kHi, kM), kSixteenth, kM72);
+            a1 = hfma2(and_or(xB, kHi, kM), kSixteenth, kM72);
+            a3 = hfma2(and_or(xB8, kHi, kM), kSixteenth, kM72);
+          }
+        } else {
+          const uint32_t qA = wa[u] ^ 0x80808080u, qB = wb[u] ^ 0x80808080u;
+          a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
+          a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
+          a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
+          a3 = hsub2(__byte_perm(qB, magic, 0x5342), bias);
+        }
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           const uint2 bf = sm.frag[fs][2 * blk + u][i][fl[i]];
@@ -675,13 +762,13 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
       const int s = i % NS, fs = i % Smem::FS;
       const uint32_t fpar = (i / Smem::FS) & 1;
       mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 22);
-      if constexpr (TYPE == MQ_Q4_K)
-        compute_chunk_q4k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
+      if constexpr (kmin_type<TYPE>())
+        compute_chunk_q4k<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else if constexpr (TYPE == MQ_Q6_K)
         compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else
-        compute_chunk_q8_0<NT>(sm, s, fs, fpar, warp, lane, p.status,
-                               chunk_width(p.K, c_begin + i) / 32, fl, tot);
+        compute_chunk_q8_0<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status,
+                                     chunk_width(p.K, c_begin + i) / 32, fl, tot);
       __syncwarp();
       if (lane == 0) mbar_arrive(sa(&sm.fempty[fs]));  // this warp is done with the slot
     }
@@ -779,6 +866,10 @@ mq_status init_matvec(DeviceState *st) {
   if ((s = optin_mv<MQ_Q4_K, 2>(st, "matvec_kernel<Q4_K,NT=2>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q6_K, 1>(st, "matvec_kernel<Q6_K,NT=1>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q6_K, 2>(st, "matvec_kernel<Q6_K,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_0, 1>(st, "matvec_kernel<Q4_0,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_0, 2>(st, "matvec_kernel<Q4_0,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_K, 1>(st, "matvec_kernel<Q5_K,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_K, 2>(st, "matvec_kernel<Q5_K,NT=2>")) != MQ_OK) return s;
   return MQ_OK;
 }
 
@@ -816,6 +907,12 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
     case MQ_Q6_K:
       return two ? launch_one<MQ_Q6_K, 2>(a, s, "matvec_kernel<Q6_K,NT=2>")
                  : launch_one<MQ_Q6_K, 1>(a, s, "matvec_kernel<Q6_K,NT=1>");
+    case MQ_Q4_0:
+      return two ? launch_one<MQ_Q4_0, 2>(a, s, "matvec_kernel<Q4_0,NT=2>")
+                 : launch_one<MQ_Q4_0, 1>(a, s, "matvec_kernel<Q4_0,NT=1>");
+    case MQ_Q5_K:
+      return two ? launch_one<MQ_Q5_K, 2>(a, s, "matvec_kernel<Q5_K,NT=2>")
+                 : launch_one<MQ_Q5_K, 1>(a, s, "matvec_kernel<Q5_K,NT=1>");
     default:
       return two ? launch_one<MQ_Q8_0, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
                  : launch_one<MQ_Q8_0, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");

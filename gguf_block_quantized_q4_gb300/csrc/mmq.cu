@@ -653,7 +653,9 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   alignas(64) CUtensorMap tA, tAm;
   mq_status r = encode_f16_map(&tA, base + L.op, M, W->K, "activation");
   if (r != MQ_OK) return r;
-  const bool mins = W->type == MQ_Q4_K && D == nullptr;
+  // Q5_K runs the Q4_K kernel (integer weight sc*q, same min term) and Q4_0 the Q8_0
+  // kernel (integer weight q - 8, one scale per 32-element block)
+  const bool mins = (W->type == MQ_Q4_K || W->type == MQ_Q5_K) && D == nullptr;
   if (mins && (r = encode_f16_map(&tAm, base + L.amin, M, 3 * (W->K / 32), "activation min-term")) !=
                   MQ_OK)
     return r;
@@ -689,6 +691,7 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
+    case MQ_Q5_K:
       return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
                   : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
     case MQ_Q6_K:

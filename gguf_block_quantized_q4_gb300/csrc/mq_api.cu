@@ -122,8 +122,11 @@ extern "C" mq_status mq_init(int device) {
 }
 
 static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t K) {
-  if (type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q6_K)
-    return fail(MQ_ERR_TYPE, "%s: unsupported GGUF type %d (supported: 8 Q8_0, 12 Q4_K, 14 Q6_K)",
+  if (type != MQ_Q4_0 && type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q5_K &&
+      type != MQ_Q6_K)
+    return fail(MQ_ERR_TYPE,
+                "%s: unsupported GGUF type %d (supported: 2 Q4_0, 8 Q8_0, 12 Q4_K, 13 Q5_K, "
+                "14 Q6_K)",
                 site, type);
   if (N < 1 || K < 1)
     return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld must both be >= 1", site, (long long)N,
@@ -205,8 +208,13 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
   if (type == MQ_Q8_0) {
     if ((s = zalloc(&w->q, npad * K, "q8_0 qs")) != MQ_OK) return cleanup(s);
     if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q8_0 d")) != MQ_OK) return cleanup(s);
+  } else if (type == MQ_Q4_0) {
+    if ((s = zalloc(&w->q, npad * K / 2, "q4_0 qs")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q4_0 d")) != MQ_OK) return cleanup(s);
   } else if (type == MQ_Q4_K) {
     if ((s = zalloc(&w->q, npad * nsb * 144, "q4_K")) != MQ_OK) return cleanup(s);
+  } else if (type == MQ_Q5_K) {
+    if ((s = zalloc(&w->q, npad * nsb * 176, "q5_K")) != MQ_OK) return cleanup(s);
   } else {
     if ((s = zalloc(&w->q, npad * nsb * 210, "q6_K")) != MQ_OK) return cleanup(s);
   }
@@ -219,13 +227,14 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
       return cleanup(s);
     if ((s = alloc_plane(&w->td, size_t(w->np) * (K / 32) * 4, &total, "prefill d")) != MQ_OK)
       return cleanup(s);
-    if (type == MQ_Q4_K &&
+    const bool mins = type == MQ_Q4_K || type == MQ_Q5_K;
+    if (mins &&
         (s = alloc_plane(&w->tm, size_t(w->np) * (K / 32) * 4, &total, "prefill min")) != MQ_OK)
       return cleanup(s);
     // the padding columns of the transposed planes must read as zero
     cudaMemsetAsync(w->td, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
     if (w->tm) cudaMemsetAsync(w->tm, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
-    if (type == MQ_Q4_K) {
+    if (mins) {
       if ((s = zalloc(&w->mb, size_t(w->np) * 3 * (K / 32) * 2, "prefill min operand")) != MQ_OK)
         return cleanup(s);
       if ((s = zalloc(&w->vcol, size_t(w->np) * 4, "prefill min scale")) != MQ_OK)

@@ -133,9 +133,15 @@ inline ActLayout act_layout(int64_t M, int64_t K) {
   return L;
 }
 
-inline int block_elems(int type) { return type == MQ_Q8_0 ? 32 : 256; }
+inline int block_elems(int type) { return (type == MQ_Q8_0 || type == MQ_Q4_0) ? 32 : 256; }
 inline int block_bytes(int type) {
-  return type == MQ_Q8_0 ? 34 : (type == MQ_Q4_K ? 144 : 210);
+  switch (type) {
+    case MQ_Q4_0: return 18;
+    case MQ_Q8_0: return 34;
+    case MQ_Q4_K: return 144;
+    case MQ_Q5_K: return 176;
+    default: return 210;
+  }
 }
 
 // Checked launch: reads the launch's own error at the site ("CUDA Backend

@@ -9,12 +9,17 @@
 //           j<4 : sc = s[j]&63,                    m = s[j+4]&63
 //           j>=4: sc = (s[j+4]&15) | (s[j-4]>>6)<<4, m = (s[j+4]>>4) | (s[j]>>6)<<4
 //         element 64c + 32h + l is nibble h of qs[32c + l];  w = d*sc_j*nib - dmin*m_j
+//   Q4_0  18 B / 32 el : f16 d, u8 qs[16]; element j < 16 = low nibble of qs[j],
+//         element 16 + j = its high nibble;                  w = d*(nib - 8)
+//   Q5_K 176 B / 256 el: as Q4_K (d, dmin, scales[12]), u8 qh[32], u8 qs[128];
+//         element 64c + 32h + l: nibble h of qs[32c + l] plus bit 2c + h of qh[l] << 4
 //   Q6_K 210 B / 256 el: u8 ql[128], u8 qh[64], int8 sc[16], f16 d
 //         element 128h + 32r + l: low 4 bits from ql[64h + 32(r%2) + l] (low nibble
 //         for r<2, high for r>=2), high 2 bits = (qh[32h + l] >> 2r) & 3;
 //         w = d * sc[e/16] * (q - 32)
-// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_K sc_j*nib, at
-// most 945, exact in f16; Q6_K v = sc*(q-32), |v| <= 4096, stored as its even
+// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_0 nib - 8; Q4_K sc_j*nib,
+// at most 945, and Q5_K sc_j*q, at most 1953, exact in f16; Q6_K v = sc*(q-32),
+// |v| <= 4096, stored as its even
 // part 2*floor(v/2) plus its odd part in {0,1}, both exact in f16) and the
 // transposed f32 block-scale planes td (d) and tm (Q4_K dmin*m_j).
 #include "mq_common.cuh"
@@ -145,6 +150,108 @@ __global__ void unpack_q4_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
           dst[16 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]] = src[16 + 32 * t + 4 * (2 * c + u) + e];
 }
 
+// Q4_0 decode plane: per (row group, chunk), [8 blocks][128 rows][16 bytes]; word t of a
+// (block, row) holds quant bytes 4t + kQ4kPerm[e] (the block's elements 4t..4t+3 in its low
+// nibbles, elements 16 + 4t.. in its high nibbles).  The d plane is laid out as Q8_0's.
+__device__ __forceinline__ int64_t q4_0_off(int64_t n, int64_t b, int64_t K) {
+  const int64_t g = n / kRowGroup, r = n % kRowGroup, c = b / 8, j = b % 8;
+  return (g * (K / 2) + int64_t(kChunk / 2) * c) * kRowGroup + (j * kRowGroup + r) * 16;
+}
+
+__global__ void repack_q4_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
+                            uint8_t *__restrict__ q, uint16_t *__restrict__ d,
+                            __half *__restrict__ mw, float *__restrict__ td) {
+  const int64_t nb = K / 32;
+  const int nchunk = (int)((K + kChunk - 1) / kChunk);
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nb) return;
+  const int64_t n = i / nb, b = i % nb;
+  const uint8_t *src = raw + i * 18;
+  const uint16_t dbits = rd16(src);
+  d[q8_0_doff(n, b, nchunk)] = dbits;
+  uint8_t *dst = q + q4_0_off(n, b, K);
+  for (int t = 0; t < 4; ++t)
+    for (int e = 0; e < 4; ++e) dst[4 * t + e] = src[2 + 4 * t + kQ4kPerm[e]];
+  if (mw) {
+    for (int e = 0; e < 32; ++e) {
+      const int nib = (src[2 + (e & 15)] >> (4 * (e >> 4))) & 15;
+      mw[n * K + b * 32 + e] = __int2half_rn(nib - 8);
+    }
+    td[b * NP + n] = f16bits(dbits);
+  }
+}
+
+__global__ void unpack_q4_0(const uint8_t *__restrict__ q, const uint16_t *__restrict__ d,
+                            int64_t N, int64_t K, uint8_t *__restrict__ raw) {
+  const int64_t nb = K / 32;
+  const int nchunk = (int)((K + kChunk - 1) / kChunk);
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nb) return;
+  const int64_t n = i / nb, b = i % nb;
+  uint8_t *dst = raw + i * 18;
+  const uint16_t dv = d[q8_0_doff(n, b, nchunk)];
+  dst[0] = dv & 255;
+  dst[1] = dv >> 8;
+  const uint8_t *src = q + q4_0_off(n, b, K);
+  for (int t = 0; t < 4; ++t)
+    for (int e = 0; e < 4; ++e) dst[2 + 4 * t + kQ4kPerm[e]] = src[4 * t + e];
+}
+
+// Q5_K decode tile: 128 rows x 176 bytes, row = 16-byte header (d, dmin, scales), the
+// 128 quant bytes regrouped as Q4_K's, then the 32 fifth-bit bytes regrouped per
+// fragment thread: bytes 8t + 4u + e hold bits byte 16u + 4t + kQ4kPerm[e].
+__global__ void repack_q5_k(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
+                            uint8_t *__restrict__ q, __half *__restrict__ mw,
+                            float *__restrict__ td, float *__restrict__ tm) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = raw + i * 176;
+  uint8_t *dst = q + tile_row(i / nsb, i % nsb, (int)nsb) * 176;
+  for (int e = 0; e < 16; ++e) dst[e] = src[e];
+  for (int t = 0; t < 4; ++t)
+    for (int c = 0; c < 4; ++c)
+      for (int u = 0; u < 2; ++u)
+        for (int e = 0; e < 4; ++e)
+          dst[16 + 32 * t + 4 * (2 * c + u) + e] = src[48 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]];
+  for (int t = 0; t < 4; ++t)
+    for (int u = 0; u < 2; ++u)
+      for (int e = 0; e < 4; ++e) dst[144 + 8 * t + 4 * u + e] = src[16 + 16 * u + 4 * t + kQ4kPerm[e]];
+  if (mw) {
+    const int64_t n = i / nsb, s = i % nsb;
+    const float dd = f16bits(rd16(src)), dmin = f16bits(rd16(src + 2));
+    for (int j = 0; j < 8; ++j) {
+      int sc, m;
+      q4k_scale_min(src + 4, j, sc, m);
+      const int c = j / 2, h = j % 2;
+      for (int l = 0; l < 32; ++l) {
+        const int q5 = ((src[48 + 32 * c + l] >> (4 * h)) & 15) | (((src[16 + l] >> j) & 1) << 4);
+        mw[n * K + s * 256 + 32 * j + l] = __int2half_rn(sc * q5);
+      }
+      td[(s * 8 + j) * NP + n] = dd;
+      tm[(s * 8 + j) * NP + n] = dmin * (float)m;
+    }
+  }
+}
+
+__global__ void unpack_q5_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
+                            uint8_t *__restrict__ raw) {
+  const int64_t nsb = K / 256;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * nsb) return;
+  const uint8_t *src = q + tile_row(i / nsb, i % nsb, (int)nsb) * 176;
+  uint8_t *dst = raw + i * 176;
+  for (int e = 0; e < 16; ++e) dst[e] = src[e];
+  for (int t = 0; t < 4; ++t)
+    for (int c = 0; c < 4; ++c)
+      for (int u = 0; u < 2; ++u)
+        for (int e = 0; e < 4; ++e)
+          dst[48 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]] = src[16 + 32 * t + 4 * (2 * c + u) + e];
+  for (int t = 0; t < 4; ++t)
+    for (int u = 0; u < 2; ++u)
+      for (int e = 0; e < 4; ++e) dst[16 + 16 * u + 4 * t + kQ4kPerm[e]] = src[144 + 8 * t + 4 * u + e];
+}
+
 // Byte offset in the raw Q6_K block of word w (0: ql low pair, 1: ql high pair,
 // 2: qh) of fragment thread t for half h and 16-element half v.
 __device__ __forceinline__ int q6k_src(int t, int h, int v, int w) {
@@ -247,11 +354,22 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
     repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
                                               w->td);
     MQ_LAUNCH_CHECK("repack_q8_0");
-  } else if (w->type == MQ_Q4_K) {
+  } else if (w->type == MQ_Q4_0) {
+    const int64_t n = N * (K / 32);
+    repack_q4_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
+                                              w->td);
+    MQ_LAUNCH_CHECK("repack_q4_0");
+  } else if (w->type == MQ_Q4_K || w->type == MQ_Q5_K) {
     const int64_t n = N * (K / 256);
-    repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr, w->td,
-                                              w->tm);
-    MQ_LAUNCH_CHECK("repack_q4_k");
+    if (w->type == MQ_Q4_K) {
+      repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,
+                                                w->td, w->tm);
+      MQ_LAUNCH_CHECK("repack_q4_k");
+    } else {
+      repack_q5_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,
+                                                w->td, w->tm);
+      MQ_LAUNCH_CHECK("repack_q5_k");
+    }
     if (mmq) {
       minplane_q4_k<<<grid_for(N, T), T, 0, s>>>(w->tm, N, K / 32, w->np, w->mb, w->vcol);
       MQ_LAUNCH_CHECK("minplane_q4_k");
@@ -271,9 +389,15 @@ mq_status unpack_weight(const mq_weight *w, uint8_t *raw, cudaStream_t s) {
   if (w->type == MQ_Q8_0) {
     unpack_q8_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q8_0");
+  } else if (w->type == MQ_Q4_0) {
+    unpack_q4_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_q4_0");
   } else if (w->type == MQ_Q4_K) {
     unpack_q4_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q4_k");
+  } else if (w->type == MQ_Q5_K) {
+    unpack_q5_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_q5_k");
   } else {
     unpack_q6_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q6_k");

@@ -42,15 +42,23 @@ extern "C" {
 #endif
 
 /* GGUF tensor type ids of the supported block formats.
+ *   MQ_Q4_0: 32-element blocks of 18 bytes: f16 d, 16 bytes of 4-bit quants
+ *            (element j < 16 the low nibble of byte j, element 16 + j its high
+ *            nibble);  w = d*(q - 8).
  *   MQ_Q8_0: 32-element blocks of 34 bytes: f16 d, 32 x int8 q;  w = d*q.
  *   MQ_Q4_K: 256-element super-blocks of 144 bytes: f16 d, f16 dmin, 12 bytes
  *            of packed 6-bit sub-block scales/mins, 128 bytes of 4-bit quants;
  *            w = d*sc_j*q - dmin*m_j.
+ *   MQ_Q5_K: 256-element super-blocks of 176 bytes: as MQ_Q4_K (f16 d, f16 dmin,
+ *            12 bytes of scales/mins) then 32 bytes of fifth bits (bit 2c + h of
+ *            byte l for element 64c + 32h + l) and 128 bytes of low 4 bits;
+ *            w = d*sc_j*q - dmin*m_j with q in [0, 31].
  *   MQ_Q6_K: 256-element super-blocks of 210 bytes: 128 bytes low 4 bits,
  *            64 bytes high 2 bits, 16 int8 sub-scales, f16 d;
  *            w = d*sc*(q - 32).
- * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256). */
-typedef enum { MQ_Q8_0 = 8, MQ_Q4_K = 12, MQ_Q6_K = 14 } mq_type;
+ * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256); Q4_0 and
+ * Q5_K are among the types its weight gate admits (§4.6). */
+typedef enum { MQ_Q4_0 = 2, MQ_Q8_0 = 8, MQ_Q4_K = 12, MQ_Q5_K = 13, MQ_Q6_K = 14 } mq_type;
 
 typedef enum {
     MQ_OK = 0,

@@ -72,8 +72,8 @@ def _reg(L, qtype, data, N, K, flags=0):
 
 
 def test_register_rejects_bad_type(L):
-    st, msg = _reg(L, 2, np.zeros(18 * 8, np.uint8), 1, 256)
-    assert mq.STATUS[st] == "MQ_ERR_TYPE" and "unsupported GGUF type 2" in msg
+    st, msg = _reg(L, 3, np.zeros(20 * 8, np.uint8), 1, 256)  # Q4_1: not supported
+    assert mq.STATUS[st] == "MQ_ERR_TYPE" and "unsupported GGUF type 3" in msg
 
 
 def test_register_rejects_bad_shape(L):

@@ -62,7 +62,9 @@ def gpu_matvec(W, x):
 # ---- decode planes -----------------------------------------------------------
 
 @pytest.mark.parametrize("qtype,N,K", [(8, 37, 96), (8, 896, 896), (12, 19, 512),
-                                       (12, 18944, 3584), (14, 21, 768), (14, 3584, 18944)])
+                                       (12, 18944, 3584), (14, 21, 768), (14, 3584, 18944),
+                                       (2, 37, 96), (2, 4864, 896), (13, 19, 512),
+                                       (13, 18944, 3584)])
 def test_decode_plane_roundtrip_is_byte_exact(qtype, N, K):
     W = registered(qtype, N, K, 7)
     assert np.array_equal(W.unpack(), weights(qtype, N, K, 7))
@@ -74,7 +76,9 @@ def test_decode_plane_roundtrip_is_byte_exact(qtype, N, K):
 
 SMALL = [(8, 1, 32), (8, 37, 96), (8, 130, 288), (8, 64, 896),
          (12, 1, 256), (12, 19, 512), (12, 100, 768), (12, 257, 2560),
-         (14, 1, 256), (14, 21, 768), (14, 130, 512), (14, 64, 4608)]
+         (14, 1, 256), (14, 21, 768), (14, 130, 512), (14, 64, 4608),
+         (2, 1, 32), (2, 37, 96), (2, 130, 288), (2, 64, 896), (2, 300, 4864),
+         (13, 1, 256), (13, 19, 512), (13, 100, 768), (13, 257, 2560)]
 
 
 @pytest.mark.parametrize("qtype,N,K", SMALL)
@@ -118,7 +122,8 @@ def test_matvec_batch_columns_equal_single_calls_bitwise():
     assert np.array_equal(y3.view(np.uint32), y8[2:5].view(np.uint32))
 
 
-@pytest.mark.parametrize("qtype,N,K", [(8, 70, 288), (12, 70, 768), (14, 70, 768)])
+@pytest.mark.parametrize("qtype,N,K", [(8, 70, 288), (12, 70, 768), (14, 70, 768),
+                                       (2, 70, 288), (13, 70, 768)])
 def test_matvec_extreme_magnitudes(qtype, N, K):
     W = registered(qtype, N, K, 13)
     rng = np.random.default_rng(5)
@@ -209,7 +214,8 @@ def test_quantize_small_and_edge_blocks(M, K):
 # ---- MMQ -------------------------------------------------------------------
 
 SMALL_MMQ = [(8, 37, 96, 5), (8, 130, 288, 70), (12, 19, 512, 9), (12, 200, 768, 65),
-             (14, 21, 768, 3), (14, 130, 512, 129)]
+             (14, 21, 768, 3), (14, 130, 512, 129),
+             (2, 37, 96, 5), (2, 130, 288, 70), (13, 19, 512, 9), (13, 200, 768, 65)]
 
 
 @pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
@@ -337,3 +343,29 @@ def test_errors_are_reported_not_fallen_back():
     assert e.value.name == "MQ_ERR_ARG"
     Wn.free()
     mq.stream_status()
+
+
+# ---- the Q4_0 and Q5_K types at model-sized shapes ---------------------------
+
+@pytest.mark.parametrize("qtype,N,K,B", [(2, 4864, 896, 1), (2, 18944, 3584, 4),
+                                         (13, 18944, 3584, 1), (13, 3584, 18944, 8)])
+def test_matvec_new_types_ffn_shapes(qtype, N, K, B):
+    W = registered(qtype, N, K, 41, mq.REG_NO_MMQ_PLANE)
+    x = synth.activations(B, K, seed=42)
+    y = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 41), N, K, x)
+    assert_bound(y, yref, bnd, f"type {qtype} {N}x{K} B={B}")
+
+
+@pytest.mark.parametrize("qtype", [2, 13])
+def test_mmq_new_types_prefill_shape_sampled(qtype):
+    N, K, M = 18944, 3584, 512
+    W = registered(qtype, N, K, 43)
+    x = synth.activations(M, K, seed=44)
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    y = mq.mmq(W, xq, M)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    rows = np.array([0, 127, 128, 300, 511])
+    yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 43), N, K, qs, sc, mrows=rows)
+    assert_bound(y.cpu().numpy()[rows], yref, bnd, f"mmq type {qtype} 512x18944x3584")
