@@ -44,6 +44,9 @@
 #include <string.h>
 
 #define OR_Q4_0 2
+#define OR_Q4_1 3
+#define OR_Q5_0 6
+#define OR_Q5_1 7
 #define OR_Q8_0 8
 #define OR_Q4_K 12
 #define OR_Q5_K 13
@@ -74,6 +77,9 @@ int oracle_block_elems(int type)
 {
     switch (type) {
     case OR_Q4_0: return 32;
+    case OR_Q4_1: return 32;
+    case OR_Q5_0: return 32;
+    case OR_Q5_1: return 32;
     case OR_Q8_0: return 32;
     case OR_Q4_K: return 256;
     case OR_Q5_K: return 256;
@@ -86,6 +92,9 @@ int oracle_block_bytes(int type)
 {
     switch (type) {
     case OR_Q4_0: return 18;
+    case OR_Q4_1: return 20;
+    case OR_Q5_0: return 22;
+    case OR_Q5_1: return 24;
     case OR_Q8_0: return 34;
     case OR_Q4_K: return 144;
     case OR_Q5_K: return 176;
@@ -111,11 +120,18 @@ void oracle_q4_k_scale_min(const uint8_t *s12, int j, int *sc, int *mn)
 /* Integer weight of element e of one block, and the block-level scales.
  * The dequantised weight is  w = dscale * wint - dmin_term, where
  *   q4_0: wint = nib(e) - 8,           dscale = d, dmin_term = 0
+ *   q4_1: wint = nib(e),               dscale = d, dmin_term = -m   (w = d*nib + m)
+ *   q5_0: wint = q5(e) - 16,           dscale = d, dmin_term = 0
+ *   q5_1: wint = q5(e),                dscale = d, dmin_term = -m   (w = d*q5 + m)
  *   q8_0: wint = q[e],                 dscale = d, dmin_term = 0
  *   q4_K: wint = sc_j * nib(e),        dscale = d, dmin_term = dmin * m_j
  *   q5_K: wint = sc_j * q5(e),         dscale = d, dmin_term = dmin * m_j
  *   q6_K: wint = sc[16-group] * (q-32), dscale = d, dmin_term = 0
  * q4_0 (d f16 at 0, 16 quant bytes at 2): element e = 16h + j, nib = (qs[j] >> 4h) & 15.
+ * q4_1 (d, m f16 at 0 and 2, 16 quant bytes at 4): nibbles as q4_0.
+ * q5_0 (d f16 at 0, fifth-bit word qh (u32, little-endian) at 2, 16 quant bytes at 6):
+ *   q5 = nib(e) | ((qh >> e) & 1) << 4, nibbles as q4_0.
+ * q5_1 (d, m f16 at 0 and 2, qh at 4, 16 quant bytes at 8): as q5_0.
  * q5_K (d, dmin f16 at 0 and 2, 12 scale bytes at 4 packed as in q4_K, 32 high-bit
  *   bytes at 16, 128 quant bytes at 48): element e = 64c + 32h + l,
  *   q5 = ((qs[32c+l] >> 4h) & 15) | ((qh[l] >> (2c + h)) & 1) << 4, j = 2c + h.
@@ -132,6 +148,17 @@ static void block_elem(int type, const uint8_t *blk, int e, int64_t *wint, int *
     } else if (type == OR_Q4_0) {
         int h = e / 16, j = e % 16;
         *wint = ((blk[2 + j] >> (4 * h)) & 15) - 8;
+    } else if (type == OR_Q4_1) {
+        int h = e / 16, j = e % 16;
+        *wint = (blk[4 + j] >> (4 * h)) & 15;
+        *mterm = -1;
+    } else if (type == OR_Q5_0 || type == OR_Q5_1) {
+        int h = e / 16, j = e % 16, qo = type == OR_Q5_0 ? 6 : 8, ho = type == OR_Q5_0 ? 2 : 4;
+        uint32_t qh = (uint32_t)blk[ho] | ((uint32_t)blk[ho + 1] << 8) |
+                      ((uint32_t)blk[ho + 2] << 16) | ((uint32_t)blk[ho + 3] << 24);
+        int q5 = ((blk[qo + j] >> (4 * h)) & 15) | (int)(((qh >> e) & 1) << 4);
+        *wint = type == OR_Q5_0 ? q5 - 16 : q5;
+        *mterm = type == OR_Q5_0 ? 0 : -1;
     } else if (type == OR_Q5_K) {
         int c = e / 64, h = (e / 32) % 2, l = e % 32;
         int q5 = ((blk[48 + 32 * c + l] >> (4 * h)) & 15) | (((blk[16 + l] >> (2 * c + h)) & 1) << 4);
@@ -159,14 +186,19 @@ static void block_elem(int type, const uint8_t *blk, int e, int64_t *wint, int *
 
 static double block_d(int type, const uint8_t *blk)
 {
-    if (type == OR_Q8_0 || type == OR_Q4_0) return oracle_f16_to_double(rd16(blk));
+    if (type == OR_Q8_0 || type == OR_Q4_0 || type == OR_Q4_1 || type == OR_Q5_0 ||
+        type == OR_Q5_1)
+        return oracle_f16_to_double(rd16(blk));
     if (type == OR_Q4_K || type == OR_Q5_K) return oracle_f16_to_double(rd16(blk));
     return oracle_f16_to_double(rd16(blk + 208));
 }
 
 static double block_dmin(int type, const uint8_t *blk)
 {
-    return (type == OR_Q4_K || type == OR_Q5_K) ? oracle_f16_to_double(rd16(blk + 2)) : 0.0;
+    /* q4_K, q5_K: dmin; q4_1, q5_1: the additive min m (paired with mterm = -1) */
+    return (type == OR_Q4_K || type == OR_Q5_K || type == OR_Q4_1 || type == OR_Q5_1)
+               ? oracle_f16_to_double(rd16(blk + 2))
+               : 0.0;
 }
 
 static int valid_shape(int type, int64_t K)

@@ -19,6 +19,12 @@ Field distributions follow the five hot-path workloads (Qwen2.5-0.5B/7B shaped):
   [-128, 127], f16 ``d = |N| * 0.005``.
 * Q4_0 (32 elements, 18 bytes): f16 ``d = |N| * 0.02`` then 16 quant bytes uniform on
   [0, 255] (each 4-bit quant uniform on [0, 15]).
+* Q4_1 (32 elements, 20 bytes): f16 ``d = |N| * 0.02``, f16 ``m = -|N| * 0.1`` then 16
+  quant bytes uniform on [0, 255].
+* Q5_0 (32 elements, 22 bytes): f16 ``d = |N| * 0.01``, 4 fifth-bit bytes and 16 quant
+  bytes uniform on [0, 255] (each 5-bit quant uniform on [0, 31]).
+* Q5_1 (32 elements, 24 bytes): f16 ``d = |N| * 0.01``, f16 ``m = -|N| * 0.1``, then 4 + 16
+  bytes as Q5_0.
 * Q5_K (256 elements, 176 bytes): as Q4_K (f16 ``d = |N| * 0.02``, ``dmin = |N| * 0.01``,
   12 scale bytes) then 32 high-bit bytes and 128 quant bytes, all uniform on [0, 255]
   (each 5-bit quant uniform on [0, 31]).
@@ -31,12 +37,13 @@ from __future__ import annotations
 
 import numpy as np
 
-Q4_0, Q8_0, Q4_K, Q5_K, Q6_K = 2, 8, 12, 13, 14  # GGUF type ids
+Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14  # GGUF type ids
 
 # type id -> (elements per block, bytes per block)
-BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176),
-         Q6_K: (256, 210)}
-TYPE_NAME = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34),
+         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210)}
+TYPE_NAME = {Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q5_1: "Q5_1", Q8_0: "Q8_0",
+             Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
 
 
 def nbytes(qtype: int, N: int, K: int) -> int:
@@ -91,6 +98,21 @@ def q4_0_weights(N: int, K: int, seed: int, d_scale: float = 0.02) -> np.ndarray
     return out.reshape(-1)
 
 
+def q32_min_weights(N: int, K: int, seed: int, nbytes: int, with_min: bool, qh: bool,
+                    d_scale: float) -> np.ndarray:
+    """Q4_1 / Q5_0 / Q5_1: f16 d, [f16 m], [4 fifth-bit bytes], 16 quant bytes."""
+    nb = N * (K // 32)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty((nb, nbytes), dtype=np.uint8)
+    out[:, 0:2] = _absnormal_f16(rng, nb, d_scale).view(np.uint8).reshape(nb, 2)
+    o = 2
+    if with_min:
+        out[:, 2:4] = (-_absnormal_f16(rng, nb, 0.1)).view(np.uint8).reshape(nb, 2)
+        o = 4
+    out[:, o:] = rng.integers(0, 256, size=(nb, nbytes - o), dtype=np.uint8)
+    return out.reshape(-1)
+
+
 def q5_k_weights(N: int, K: int, seed: int, d_scale: float = 0.02,
                  dmin_scale: float = 0.01) -> np.ndarray:
     nb = N * (K // 256)
@@ -108,6 +130,12 @@ def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
     """Raw GGUF bytes of an N x K weight, rows contiguous, blocks along K."""
     if qtype == Q4_0:
         return q4_0_weights(N, K, seed)
+    if qtype == Q4_1:
+        return q32_min_weights(N, K, seed, 20, True, False, 0.02)
+    if qtype == Q5_0:
+        return q32_min_weights(N, K, seed, 22, False, True, 0.01)
+    if qtype == Q5_1:
+        return q32_min_weights(N, K, seed, 24, True, True, 0.01)
     if qtype == Q5_K:
         return q5_k_weights(N, K, seed)
     if qtype == Q8_0:

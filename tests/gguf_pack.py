@@ -77,6 +77,20 @@ def pack_q4_0(d_bits: int, q) -> bytes:
     return bytes([d_bits & 255, d_bits >> 8]) + qs
 
 
+def pack_q32(qtype: int, d_bits: int, m_bits: int, q) -> bytes:
+    """Q4_1 (q in 0..15), Q5_0 / Q5_1 (q in 0..31; the stored quant, before Q5_0's -16):
+    f16 d, [f16 m], [fifth-bit word: bit e = bit 4 of q[e]], then the nibbles as Q4_0."""
+    q = np.asarray(q, dtype=np.int64)
+    assert q.shape == (32,) and q.min() >= 0 and q.max() <= (15 if qtype == 3 else 31)
+    out = bytes([d_bits & 255, d_bits >> 8])
+    if qtype in (3, 7):
+        out += bytes([m_bits & 255, m_bits >> 8])
+    if qtype in (6, 7):
+        qh = sum(int((q[e] >> 4) & 1) << e for e in range(32))
+        out += qh.to_bytes(4, "little")
+    return out + bytes(int(q[j] & 15) | (int(q[16 + j] & 15) << 4) for j in range(16))
+
+
 def pack_q5_k(d_bits: int, dmin_bits: int, sc, mn, q5) -> bytes:
     """q5[e] in 0..31 for e in 0..255; element 64c + 32h + l: low 4 bits in quant byte
     32c + l (low nibble for h = 0, high for h = 1), fifth bit at bit 2c + h of high-bit
@@ -128,6 +142,22 @@ def np_dequant(qtype: int, W: np.ndarray, N: int, K: int) -> np.ndarray:
         qs = blk[:, :, 2:18].astype(np.int64)
         q = np.concatenate([qs & 15, qs >> 4], axis=-1) - 8  # elements 0..15, 16..31
         return (d[:, :, None] * q).reshape(N, K)
+    if qtype in (3, 6, 7):
+        bb = {3: 20, 6: 22, 7: 24}[qtype]
+        blk = W.reshape(N, K // 32, bb)
+        d = _f16(blk[:, :, 0:2])
+        m = _f16(blk[:, :, 2:4]) if qtype in (3, 7) else np.zeros_like(d)
+        qo = {3: 4, 6: 6, 7: 8}[qtype]
+        qs = blk[:, :, qo:qo + 16].astype(np.int64)
+        q = np.concatenate([qs & 15, qs >> 4], axis=-1)  # elements 0..15, 16..31
+        if qtype in (6, 7):
+            ho = qo - 4
+            qh = blk[:, :, ho:ho + 4].astype(np.int64)
+            word = qh[..., 0] | (qh[..., 1] << 8) | (qh[..., 2] << 16) | (qh[..., 3] << 24)
+            q = q | (((word[..., None] >> np.arange(32)) & 1) << 4)
+        if qtype == 6:
+            q = q - 16
+        return (d[:, :, None] * q + m[:, :, None]).reshape(N, K)
     if qtype == 13:
         blk = W.reshape(N, K // 256, 176)
         d = _f16(blk[:, :, 0:2])

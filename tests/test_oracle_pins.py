@@ -83,6 +83,16 @@ def test_q4_0_ramp_block():
     assert y[0, 0] == int(kv["dot_ones"])
 
 
+@pytest.mark.parametrize("fname", ["q4_1_as_q4_0.txt", "q5_0_ramp.txt", "q5_1_halves.txt"])
+def test_q32_min_and_fifth_bit_blocks(fname):
+    kv, _ = _read(fname)
+    qtype = int(kv["type"])
+    blk = np.frombuffer(bytes.fromhex(kv["hex"]), dtype=np.uint8)
+    assert oracle.dequant_row(qtype, blk, 32).tolist() == [float(v) for v in kv["w"].split()]
+    y, _ = oracle.matvec(qtype, blk, 1, 32, np.ones(32, np.float32))
+    assert y[0, 0] == float(kv["dot_ones"])
+
+
 def test_q5_k_high_bits_block():
     kv, _ = _read("q5_k_high_bits.txt")
     blk = np.frombuffer(bytes.fromhex(kv["hex"]), dtype=np.uint8)
@@ -217,7 +227,7 @@ def test_linearity_in_d_and_dmin():
 
 # ---- special cases that reduce to a plain float64 product --------------------
 
-@pytest.mark.parametrize("qtype", [2, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
 def test_unit_scales_reduce_to_integer_matrix_product(qtype):
     rng = np.random.default_rng(4 + qtype)
     N, K, B = 5, 512, 3
@@ -225,7 +235,7 @@ def test_unit_scales_reduce_to_integer_matrix_product(qtype):
     one = gp.f16_bits(1.0)
     for n in range(N):
         row = b""
-        for blk in range(K // (32 if qtype in (2, 8) else 256)):
+        for blk in range(K // (32 if qtype in (2, 3, 6, 7, 8) else 256)):
             if qtype == 8:
                 q = rng.integers(-128, 128, 32)
                 row += gp.pack_q8_0(one, q)
@@ -234,6 +244,10 @@ def test_unit_scales_reduce_to_integer_matrix_product(qtype):
                 q = rng.integers(-8, 8, 32)
                 row += gp.pack_q4_0(one, q)
                 ints[n, 32 * blk:32 * blk + 32] = q
+            elif qtype in (3, 6, 7):
+                q = rng.integers(0, 16 if qtype == 3 else 32, 32)
+                row += gp.pack_q32(qtype, one, 0, q)
+                ints[n, 32 * blk:32 * blk + 32] = q - (16 if qtype == 6 else 0)
             elif qtype == 13:
                 q = rng.integers(0, 32, 256)
                 row += gp.pack_q5_k(one, 0, [1] * 8, [0] * 8, q)
@@ -257,14 +271,14 @@ def test_unit_scales_reduce_to_integer_matrix_product(qtype):
 
 # ---- second formulation (vectorised numpy) and brute force ----------------
 
-@pytest.mark.parametrize("qtype", [2, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
 def test_dequant_matches_vectorised_numpy_decoder(qtype):
     N, K = 7, 512
     W = synth.weights(qtype, N, K, seed=11)
     assert np.array_equal(oracle.dequant(qtype, W, N, K), gp.np_dequant(qtype, W, N, K))
 
 
-@pytest.mark.parametrize("qtype", [2, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
 @pytest.mark.parametrize("N,K,B", [(1, 256, 1), (2, 256, 8), (3, 512, 4), (3, 512, 2)])
 def test_brute_force_tiny_matvec(qtype, N, K, B):
     W = synth.weights(qtype, N, K, seed=N * 100 + K + B)
@@ -277,7 +291,7 @@ def test_brute_force_tiny_matvec(qtype, N, K, B):
             assert abs(y[b, n] - exact) <= 1e-12 * bnd[b, n] + 1e-300
 
 
-@pytest.mark.parametrize("qtype", [2, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
 def test_blockdots_python_big_integers(qtype):
     N, K, M = 3, 512, 4
     W = synth.weights(qtype, N, K, seed=21)
@@ -289,16 +303,19 @@ def test_blockdots_python_big_integers(qtype):
     for n in range(N):
         wi = oracle.int_weights_row(qtype, W[n * rowbytes:(n + 1) * rowbytes], K)
         # the integer weight times the block scale (minus the q4_K min term) is the weight
-        be = 32 if qtype in (2, 8) else 256
+        be = 32 if qtype in (2, 3, 6, 7, 8) else 256
         blk = W[n * rowbytes:(n + 1) * rowbytes].reshape(-1, rowbytes // (K // be))
         for k in range(K):
             b = blk[k // be]
             if qtype == 14:
                 d = np.frombuffer(bytes(b[208:210]), np.float16)[0].astype(np.float64)
                 assert wf[n, k] == d * wi[k]
-            elif qtype in (2, 8):
+            elif qtype in (2, 6, 8):
                 d = np.frombuffer(bytes(b[0:2]), np.float16)[0].astype(np.float64)
                 assert wf[n, k] == d * wi[k]
+            elif qtype in (3, 7):
+                d, m = np.frombuffer(bytes(b[0:4]), np.float16).astype(np.float64)
+                assert wf[n, k] == d * wi[k] + m
         for m in range(M):
             for blk_i in range(K // 32):
                 ref = sum(int(wi[k]) * int(qs[m, k]) for k in range(32 * blk_i, 32 * blk_i + 32))
@@ -306,7 +323,7 @@ def test_blockdots_python_big_integers(qtype):
     assert np.abs(D).max() < 2 ** 24  # exact in f32 partial sums
 
 
-@pytest.mark.parametrize("qtype", [2, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
 def test_mmq_reference_equals_block_structured_sum(qtype):
     """The plain definition sum_k w * (s q) equals the block-structured form
     sum_b s_b * (d * D_b - dmin * m_j * S_b) built from the block dots."""
@@ -316,7 +333,7 @@ def test_mmq_reference_equals_block_structured_sum(qtype):
     qs, sc, bs = oracle.quantize_act(x)
     y, bnd = oracle.mmq(qtype, W, N, K, qs, sc)
     D = oracle.blockdots(qtype, W, N, K, qs)
-    be = 32 if qtype in (2, 8) else 256
+    be = 32 if qtype in (2, 3, 6, 7, 8) else 256
     rowbytes = len(W) // N
     for n in range(N):
         blocks = W[n * rowbytes:(n + 1) * rowbytes].reshape(K // be, -1)
@@ -324,9 +341,12 @@ def test_mmq_reference_equals_block_structured_sum(qtype):
             acc = 0.0
             for b in range(K // 32):
                 blk = blocks[b * 32 // be]
-                if qtype in (2, 8):
+                if qtype in (2, 6, 8):
                     d = float(np.frombuffer(bytes(blk[0:2]), np.float16)[0])
                     acc += float(sc[m, b]) * d * float(D[m, n, b])
+                elif qtype in (3, 7):
+                    d, mm = (float(v) for v in np.frombuffer(bytes(blk[0:4]), np.float16))
+                    acc += float(sc[m, b]) * (d * float(D[m, n, b]) + mm * float(bs[m, b]))
                 elif qtype in (12, 13):
                     d = float(np.frombuffer(bytes(blk[0:2]), np.float16)[0])
                     dmin = float(np.frombuffer(bytes(blk[2:4]), np.float16)[0])
