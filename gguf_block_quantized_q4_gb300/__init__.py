@@ -21,10 +21,10 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmq.so")
 
-Q4_0, Q8_0, Q4_K, Q5_K, Q6_K = 2, 8, 12, 13, 14
+Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14
 REG_DEFAULT, REG_NO_MMQ_PLANE = 0, 1
-BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176),
-         Q6_K: (256, 210)}
+BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34),
+         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210)}
 
 STATUS = ["MQ_OK", "MQ_ERR_ARG", "MQ_ERR_TYPE", "MQ_ERR_SHAPE", "MQ_ERR_PAYLOAD",
           "MQ_ERR_ALIGN", "MQ_ERR_CUDA", "MQ_ERR_OOM", "MQ_ERR_LAUNCH", "MQ_ERR_TIMEOUT",
@@ -207,6 +207,11 @@ def act_bytes(M: int, K: int) -> int:
     return lib().mq_act_bytes(M, K)
 
 
+def min_ld(nb: int) -> int:
+    """Row stride (f16 elements) of the min-term operand: 3*nb rounded up to 8."""
+    return (3 * nb + 7) // 8 * 8
+
+
 def act_layout(M: int, K: int):
     """Byte offsets of the xq sections (see mq_act_bytes in mq.h)."""
     def al(v):
@@ -220,7 +225,7 @@ def act_layout(M: int, K: int):
     o["scaleT"] = al(o["op"] + M * K * 2)
     o["minT"] = al(o["scaleT"] + mt * nb * 4)
     o["amin"] = al(o["minT"] + mt * nb * 4)
-    o["urow"] = al(o["amin"] + M * 3 * nb * 2)
+    o["urow"] = al(o["amin"] + M * min_ld(nb) * 2)
     o["total"] = al(o["urow"] + mt * 4)
     o["mt"] = mt
     return o
@@ -254,7 +259,8 @@ def act_views_min(xq, M: int, K: int):
     import torch
     o = act_layout(M, K)
     nb = K // 32
-    am = xq[o["amin"]:o["amin"] + M * 3 * nb * 2].view(torch.float16).view(M, 3 * nb)
+    ld = min_ld(nb)
+    am = xq[o["amin"]:o["amin"] + M * ld * 2].view(torch.float16).view(M, ld)[:, :3 * nb]
     ur = xq[o["urow"]:o["urow"] + M * 4].view(torch.float32)
     return am, ur
 

@@ -1,6 +1,7 @@
-// matvec.cu -- decode matvec y[b][n] = sum_k w[n][k] x[b][k] for GGUF Q8_0 /
-// Q4_K / Q6_K weights and f32 activations, B <= 8 ("minfer CUDA Backend Design"
-// §4.4: the nt == 1 matvec and the _multi variants for nt 2..8).
+// matvec.cu -- decode matvec y[b][n] = sum_k w[n][k] x[b][k] for GGUF Q4_0 / Q4_1 /
+// Q5_0 / Q5_1 / Q8_0 / Q4_K / Q5_K / Q6_K weights and f32 activations, B <= 8
+// ("minfer CUDA Backend Design" §4.4: the nt == 1 matvec and the _multi variants for
+// nt 2..8).
 //
 // GB300 design.  The weights are streamed once from HBM and dequantised in
 // registers straight into tensor-core fragments; the dot products run on the
@@ -74,6 +75,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 struct MvArgs {
   const uint8_t *q;
   const uint16_t *d;
+  const uint16_t *dm;  // Q4_1 / Q5_1 block m
+  const uint32_t *qh;  // Q5_0 / Q5_1 fifth-bit words
   const float *x;
   float *y;
   int64_t N, K;
@@ -84,14 +87,48 @@ struct MvArgs {
   int *status;
 };
 
+// The per-32-element-block types, those among them with an additive min m (w = d*q + m),
+// and those with a fifth bit per element.
+template <int TYPE>
+__host__ __device__ constexpr bool q32_type() {
+  return TYPE == MQ_Q8_0 || TYPE == MQ_Q4_0 || TYPE == MQ_Q4_1 || TYPE == MQ_Q5_0 ||
+         TYPE == MQ_Q5_1;
+}
+template <int TYPE>
+__host__ __device__ constexpr bool addmin_type() {
+  return TYPE == MQ_Q4_1 || TYPE == MQ_Q5_1;
+}
+template <int TYPE>
+__host__ __device__ constexpr bool fifth_type() {
+  return TYPE == MQ_Q5_0 || TYPE == MQ_Q5_1;
+}
+// Bytes per 32-element block and tile row of the per-32-block types' quant plane.
+template <int TYPE>
+__host__ __device__ constexpr int q32_bytes() {
+  return TYPE == MQ_Q8_0 ? 32 : 16;
+}
+// Stage layout of the per-32-block types: quants [8 blocks][128 rows][q32_bytes], then
+// the f16 d [128 rows][8 blocks], then (additive-min types) m as d, then (fifth-bit
+// types) the fifth-bit words [8 blocks][128 rows].
+template <int TYPE>
+__host__ __device__ constexpr int q32_off_d() {
+  return kRows * 8 * q32_bytes<TYPE>();
+}
+template <int TYPE>
+__host__ __device__ constexpr int q32_off_m() {
+  return q32_off_d<TYPE>() + kRows * 16;
+}
+template <int TYPE>
+__host__ __device__ constexpr int q32_off_h() {
+  return q32_off_d<TYPE>() + kRows * 16 * (addmin_type<TYPE>() ? 2 : 1);
+}
 // Bytes of one (128-row group, chunk) tile of the decode plane.
 template <int TYPE>
 __host__ __device__ constexpr int tile_bytes() {
-  return kRows * (TYPE == MQ_Q4_K   ? 144
-                  : TYPE == MQ_Q5_K ? 176
-                  : TYPE == MQ_Q6_K ? 210
-                  : TYPE == MQ_Q4_0 ? 128 + 16
-                                    : 256 + 16);
+  return TYPE == MQ_Q4_K   ? kRows * 144
+         : TYPE == MQ_Q5_K ? kRows * 176
+         : TYPE == MQ_Q6_K ? kRows * 210
+                           : q32_off_h<TYPE>() + (fifth_type<TYPE>() ? kRows * 32 : 0);
 }
 // Weight-ring depth: two CTAs per SM must fit in shared memory; within that, the depth
 // that measured fastest (Q4_K B <= 4: 2 stages beat 3 and 4).
@@ -110,12 +147,6 @@ template <int TYPE>
 __host__ __device__ constexpr bool kmin_type() {
   return TYPE == MQ_Q4_K || TYPE == MQ_Q5_K;
 }
-// Bytes per 32-element block and tile row of the per-32-block types' quant plane.
-template <int TYPE>
-__host__ __device__ constexpr int q32_bytes() {
-  return TYPE == MQ_Q4_0 ? 16 : 32;
-}
-
 // Per-warp tables decoded from the tile headers of the warp's 16 rows.
 template <int TYPE>
 struct WarpTab;
@@ -136,6 +167,15 @@ struct WarpTab<MQ_Q8_0> {
 template <>
 struct WarpTab<MQ_Q4_0> : WarpTab<MQ_Q8_0> {};
 template <>
+struct WarpTab<MQ_Q5_0> : WarpTab<MQ_Q8_0> {};
+template <>
+struct WarpTab<MQ_Q4_1> {
+  float2 s[8][8];  // [32-element block][g]: d of rows g, g+8
+  float2 m[8][8];  // the blocks' m
+};
+template <>
+struct WarpTab<MQ_Q5_1> : WarpTab<MQ_Q4_1> {};
+template <>
 struct WarpTab<MQ_Q5_K> : WarpTab<MQ_Q4_K> {};
 
 template <int TYPE, int NT>
@@ -152,6 +192,7 @@ struct MvSmem {
   float unscale[FS][8];                       // 2^-e per batch row of the slot's chunk
   WarpTab<TYPE> tab[kCompute];
   float xs[8];  // x-warp scratch: sub-block sums of one batch row
+  float xb[addmin_type<TYPE>() ? FS : 1][8][8];  // per slot: [block][batch row] sums of x
   // weight stage: copied (wfull) / read into registers by all warps (wempty);
   // fragment slot: written (ffull) / used by the compute warps (fempty)
   uint64_t wfull[NS], wempty[NS], ffull[FS], fempty[FS];
@@ -257,9 +298,10 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
     const int c = c_begin + i, s = i % NS;
     const int cw = chunk_width(p.K, c);
     const uint32_t bar = sa(&sm.wfull[s]);
-    constexpr bool Q32 = TYPE == MQ_Q8_0 || TYPE == MQ_Q4_0;  // per-32-block scales
-    constexpr int QB = q32_bytes<TYPE>();                       // quant bytes per block row
-    const uint32_t wbytes = Q32 ? (uint32_t)(kRows * (cw / 32) * QB + kRows * 16)
+    constexpr bool Q32 = q32_type<TYPE>();  // per-32-block scales
+    constexpr int QB = q32_bytes<TYPE>();  // quant bytes per block row
+    constexpr int HB = fifth_type<TYPE>() ? 4 : 0, MB = addmin_type<TYPE>() ? 16 : 0;
+    const uint32_t wbytes = Q32 ? (uint32_t)(kRows * (cw / 32) * (QB + HB) + kRows * (16 + MB))
                                 : (uint32_t)tile_bytes<TYPE>();
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"(wbytes + (uint32_t)(p.B * cw * 4))
@@ -268,7 +310,14 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
     if constexpr (Q32) {
       bulk_1d(sa(w), p.q + (group * (p.K / 32) + int64_t(c) * 8) * kRows * QB,
               (uint32_t)(kRows * (cw / 32) * QB), bar);
-      bulk_1d(sa(w + kRows * 8 * QB), p.d + (group * p.nchunk + c) * kRows * 8, kRows * 16, bar);
+      bulk_1d(sa(w + q32_off_d<TYPE>()), p.d + (group * p.nchunk + c) * kRows * 8, kRows * 16,
+              bar);
+      if constexpr (addmin_type<TYPE>())
+        bulk_1d(sa(w + q32_off_m<TYPE>()), p.dm + (group * p.nchunk + c) * kRows * 8, kRows * 16,
+                bar);
+      if constexpr (fifth_type<TYPE>())
+        bulk_1d(sa(w + q32_off_h<TYPE>()), p.qh + (group * (p.K / 32) + int64_t(c) * 8) * kRows,
+                (uint32_t)(kRows * (cw / 32) * 4), bar);
     } else {
       bulk_1d(sa(w), p.q + (group * p.nchunk + c) * int64_t(tile_bytes<TYPE>()),
               (uint32_t)tile_bytes<TYPE>(), bar);
@@ -292,7 +341,8 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
   }
 }
 
-// x warp: staged x chunk -> hi/lo B fragments (+ Q4_K sub-block sums).
+// x warp: staged x chunk -> hi/lo B fragments (+ the Q4_K / Q5_K sub-block sums, the
+// Q4_1 / Q5_1 block sums).
 template <int TYPE, int NT>
 __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, int c_begin,
                                         int nch, int lane) {
@@ -332,6 +382,14 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
         const uint32_t lo23 = pack_f16x2(v2 - f16_lo(hi23), v3 - f16_hi(hi23));
         sm.frag[fs][g16][b >> 2][col * 4 + t] = make_uint2(hi01, hi23);
         sm.frag[fs][g16][b >> 2][(col + 1) * 4 + t] = make_uint2(lo01, lo23);
+        if constexpr (addmin_type<TYPE>()) {
+          // block f >> 3 (8 consecutive items) sum of the scaled x, in f32
+          float ps = (v0 + v1) + (v2 + v3);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+          if ((lane & 7) == 0) sm.xb[fs][f >> 3][b] = ps;
+        }
         if constexpr (kmin_type<TYPE>()) {
           // sum of sub-block j = f >> 3 (8 consecutive items), scaled by 1/32 so
           // that |sum| < 2^15 fits f16
@@ -585,41 +643,65 @@ __device__ __forceinline__ void compute_chunk_q6k(MvSmem<MQ_Q6_K, NT> &sm, int s
   }
 }
 
-// Q8_0 and Q4_0: one scale d per 32-element block, applied after the block's two MMAs.
-// Q4_0's word of a (block, row) holds the block's quant bytes 4t..4t+3 (order 0, 2, 1, 3):
-// its low nibbles are elements 4t..4t+3 of the first 16-element half, its high nibbles
-// those of the second; (1024 + n) - 1032 and (1024 + 16n)/16 - 72 give n - 8 exactly.
+// The per-32-block types: one scale d per block, applied after the block's two MMAs.
+// A nibble type's word of a (block, row) holds the block's quant bytes 4t..4t+3 (order
+// 0, 2, 1, 3): its low nibbles are elements 4t..4t+3 of the first 16-element half, its
+// high nibbles those of the second.  A low nibble n masked into the mantissa of 1024
+// gives 1024 + n, a high one 1024 + 16n; one f16x2 subtraction or fma (by 1/16) turns
+// them into the exact integer weight: n - 8 (Q4_0), n (Q4_1).  For Q5_0 / Q5_1 the
+// fifth bit of each element is OR-ed in beside the nibble first (bit 4 of the half:
+// 1024 + q, or bit 8: 1024 + 16q), giving q - 16 (Q5_0) or q (Q5_1).  The fifth-bit
+// word of a (block, row) holds the pair of elements of register r of thread t at bits
+// 4r + t and 16 + 4r + t, so one shift and one mask move both to their halves.  The
+// additive min m of Q4_1 / Q5_1 adds m times the block's sum of x (staged by the x warp).
 template <int TYPE, int NT>
-__device__ __forceinline__ void compute_chunk_q8_0(MvSmem<TYPE, NT> &sm, int s, int fs,
-                                                   uint32_t fpar, int warp, int lane,
-                                                   int *status, int nblk, const int (&fl)[NT],
-                                                   float (&tot)[2][NT]) {
-  constexpr bool Q4 = TYPE == MQ_Q4_0;
+__device__ __forceinline__ void compute_chunk_q32(MvSmem<TYPE, NT> &sm, int s, int fs,
+                                                  uint32_t fpar, int warp, int lane, int *status,
+                                                  int nblk, const int (&fl)[NT],
+                                                  float (&tot)[2][NT]) {
+  constexpr bool NIB = TYPE != MQ_Q8_0, Q5 = fifth_type<TYPE>(), MADD = addmin_type<TYPE>();
   constexpr int QB = q32_bytes<TYPE>();
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *tile = sm.w[s];
-  WarpTab<MQ_Q8_0> &tb = sm.tab[warp];
+  WarpTab<TYPE> &tb = sm.tab[warp];
   {  // lane (r, h): blocks 4h..4h+3 of row r (slots past the chunk's blocks hold 0)
     const int r = lane & 15, h = lane >> 4, row = 16 * warp + r;
-    const uint2 dv = *reinterpret_cast<const uint2 *>(tile + kRows * 8 * QB + row * 16 + 8 * h);
+    const uint2 dv = *reinterpret_cast<const uint2 *>(tile + q32_off_d<TYPE>() + row * 16 + 8 * h);
     float *dst = reinterpret_cast<float *>(&tb.s[4 * h][r & 7]) + (r >> 3);
     dst[0] = f16_lo(dv.x);
     dst[16] = f16_hi(dv.x);
     dst[32] = f16_lo(dv.y);
     dst[48] = f16_hi(dv.y);
+    if constexpr (MADD) {
+      const uint2 mv =
+          *reinterpret_cast<const uint2 *>(tile + q32_off_m<TYPE>() + row * 16 + 8 * h);
+      float *dm = reinterpret_cast<float *>(&tb.m[4 * h][r & 7]) + (r >> 3);
+      dm[0] = f16_lo(mv.x);
+      dm[16] = f16_hi(mv.x);
+      dm[32] = f16_lo(mv.y);
+      dm[48] = f16_hi(mv.y);
+    }
   }
   __syncwarp();
   const int ra = 16 * warp + g, rb = ra + 8;
+  // nibble types: .x the quant word, .y the fifth-bit word (0 without fifth bits)
   uint2 va[8], vb[8];  // blocks past the chunk's end hold stale but finite bytes
 #pragma unroll
   for (int blk = 0; blk < 8; ++blk) {
-    if constexpr (Q4) {
+    if constexpr (NIB) {
       va[blk].x = *reinterpret_cast<const uint32_t *>(tile + (blk * kRows + ra) * 16 + 4 * t);
       vb[blk].x = *reinterpret_cast<const uint32_t *>(tile + (blk * kRows + rb) * 16 + 4 * t);
-      va[blk].y = vb[blk].y = 0u;
+      if constexpr (Q5) {
+        va[blk].y = *reinterpret_cast<const uint32_t *>(tile + q32_off_h<TYPE>() +
+                                                        (blk * kRows + ra) * 4);
+        vb[blk].y = *reinterpret_cast<const uint32_t *>(tile + q32_off_h<TYPE>() +
+                                                        (blk * kRows + rb) * 4);
+      } else {
+        va[blk].y = vb[blk].y = 0u;
+      }
     } else {
-      va[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + ra) * 32 + 8 * t);
-      vb[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + rb) * 32 + 8 * t);
+      va[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + ra) * QB + 8 * t);
+      vb[blk] = *reinterpret_cast<const uint2 *>(tile + (blk * kRows + rb) * QB + 8 * t);
     }
   }
   release_and_wait(sm.wempty[s], sm.ffull[fs], fpar, lane, status);
@@ -628,10 +710,16 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<TYPE, NT> &sm, int s, 
   for (int i = 0; i < NT; ++i) acc[0][i] = acc[1][i] = 0.f;
   const uint32_t magic = 0x64646464u;
   const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152): 1024 + 128
+  // nibble types: (1024 + n) - kSub and (1024 + 16n)/16 + kAdd give the integer weight
+  constexpr uint32_t kSub = TYPE == MQ_Q4_0   ? 0x64086408u   // 1032: n - 8
+                            : TYPE == MQ_Q5_0 ? 0x64106410u   // 1040: q - 16
+                                              : 0x64006400u;  // 1024: n or q
+  constexpr uint32_t kAdd = TYPE == MQ_Q4_0   ? 0xD480D480u   // -72
+                            : TYPE == MQ_Q5_0 ? 0xD500D500u   // -80
+                                              : 0xD400D400u;  // -64
 #pragma unroll
   for (int blk = 0; blk < 8; ++blk) {
     if (blk < nblk) {
-      const uint32_t wa[2] = {va[blk].x, va[blk].y}, wb[2] = {vb[blk].x, vb[blk].y};
       float c4[NT][4];
 #pragma unroll
       for (int i = 0; i < NT; ++i)
@@ -640,24 +728,41 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<TYPE, NT> &sm, int s, 
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         uint32_t a0, a1, a2, a3;
-        if constexpr (Q4) {
+        if constexpr (NIB) {
           constexpr uint32_t kM = 0x64006400u, kLo = 0x000f000fu, kHi = 0x00f000f0u;
-          constexpr uint32_t k1032 = 0x64086408u;                  // f16x2 (1032, 1032)
-          constexpr uint32_t kSixteenth = 0x2C002C00u, kM72 = 0xD480D480u;  // 1/16, -72
-          const uint32_t xA = wa[0], xB = wb[0], xA8 = xA >> 8, xB8 = xB >> 8;
+          constexpr uint32_t kSixteenth = 0x2C002C00u;  // 1/16
+          const uint32_t xA = va[blk].x, xB = vb[blk].x, xA8 = xA >> 8, xB8 = xB >> 8;
+          const uint32_t hA = va[blk].y, hB = vb[blk].y;
+          // exponent words OR-ed beside the nibbles: the magic, plus the fifth bits
+          uint32_t mA0 = kM, mA2 = kM, mB0 = kM, mB2 = kM;
           if (u == 0) {
-            a0 = hsub2(and_or(xA, kLo, kM), k1032);
-            a2 = hsub2(and_or(xA8, kLo, kM), k1032);
-            a1 = hsub2(and_or(xB, kLo, kM), k1032);
-            a3 = hsub2(and_or(xB8, kLo, kM), k1032);
+            if constexpr (Q5) {  // pairs of registers r = 0, 1 to bits 4 and 20
+              constexpr uint32_t kB4 = 0x00100010u;
+              mA0 = and_or(hA << (4 - t), kB4, kM);
+              mB0 = and_or(hB << (4 - t), kB4, kM);
+              mA2 = and_or(hA >> t, kB4, kM);
+              mB2 = and_or(hB >> t, kB4, kM);
+            }
+            a0 = hsub2(and_or(xA, kLo, mA0), kSub);
+            a2 = hsub2(and_or(xA8, kLo, mA2), kSub);
+            a1 = hsub2(and_or(xB, kLo, mB0), kSub);
+            a3 = hsub2(and_or(xB8, kLo, mB2), kSub);
           } else {
-            a0 = hfma2(and_or(xA, kHi, kM), kSixteenth, kM72);
-            a2 = hfma2(and_or(xA8, kHi, kM), kSixteenth, kM72);
-            a1 = hfma2(and_or(xB, kHi, kM), kSixteenth, kM72);
-            a3 = hfma2(and_or(xB8, kHi, kM), kSixteenth, kM72);
+            if constexpr (Q5) {  // registers r = 2, 3 to bits 8 and 24
+              constexpr uint32_t kB8 = 0x01000100u;
+              mA0 = and_or(hA >> t, kB8, kM);
+              mB0 = and_or(hB >> t, kB8, kM);
+              mA2 = and_or(hA >> (4 + t), kB8, kM);
+              mB2 = and_or(hB >> (4 + t), kB8, kM);
+            }
+            a0 = hfma2(and_or(xA, kHi, mA0), kSixteenth, kAdd);
+            a2 = hfma2(and_or(xA8, kHi, mA2), kSixteenth, kAdd);
+            a1 = hfma2(and_or(xB, kHi, mB0), kSixteenth, kAdd);
+            a3 = hfma2(and_or(xB8, kHi, mB2), kSixteenth, kAdd);
           }
         } else {
-          const uint32_t qA = wa[u] ^ 0x80808080u, qB = wb[u] ^ 0x80808080u;
+          const uint32_t qA = (u ? va[blk].y : va[blk].x) ^ 0x80808080u;
+          const uint32_t qB = (u ? vb[blk].y : vb[blk].x) ^ 0x80808080u;
           a0 = hsub2(__byte_perm(qA, magic, 0x5140), bias);
           a2 = hsub2(__byte_perm(qA, magic, 0x5342), bias);
           a1 = hsub2(__byte_perm(qB, magic, 0x5140), bias);
@@ -674,6 +779,15 @@ __device__ __forceinline__ void compute_chunk_q8_0(MvSmem<TYPE, NT> &sm, int s, 
       for (int i = 0; i < NT; ++i) {
         acc[0][i] = fmaf(dv.x, c4[i][0] + c4[i][1], acc[0][i]);
         acc[1][i] = fmaf(dv.y, c4[i][2] + c4[i][3], acc[1][i]);
+      }
+      if constexpr (MADD) {
+        const float2 mv = tb.m[blk][g];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const float xs = sm.xb[fs][blk][4 * i + t];
+          acc[0][i] = fmaf(mv.x, xs, acc[0][i]);
+          acc[1][i] = fmaf(mv.y, xs, acc[1][i]);
+        }
       }
     }
   }
@@ -725,6 +839,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
     constexpr int n16 = (int)(sizeof(sm.frag) / 16);
     for (int i = tid; i < n16; i += kThreads) f[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < Smem::FS * 8) (&sm.unscale[0][0])[tid] = 0.f;
+    constexpr int nxb = (int)(sizeof(sm.xb) / 4);
+    for (int i = tid; i < nxb; i += kThreads) (&sm.xb[0][0][0])[i] = 0.f;
   }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -767,8 +883,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
       else if constexpr (TYPE == MQ_Q6_K)
         compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else
-        compute_chunk_q8_0<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status,
-                                     chunk_width(p.K, c_begin + i) / 32, fl, tot);
+        compute_chunk_q32<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status,
+                                    chunk_width(p.K, c_begin + i) / 32, fl, tot);
       __syncwarp();
       if (lane == 0) mbar_arrive(sa(&sm.fempty[fs]));  // this warp is done with the slot
     }
@@ -870,6 +986,12 @@ mq_status init_matvec(DeviceState *st) {
   if ((s = optin_mv<MQ_Q4_0, 2>(st, "matvec_kernel<Q4_0,NT=2>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q5_K, 1>(st, "matvec_kernel<Q5_K,NT=1>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q5_K, 2>(st, "matvec_kernel<Q5_K,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_1, 1>(st, "matvec_kernel<Q4_1,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q4_1, 2>(st, "matvec_kernel<Q4_1,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_0, 1>(st, "matvec_kernel<Q5_0,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_0, 2>(st, "matvec_kernel<Q5_0,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_1, 1>(st, "matvec_kernel<Q5_1,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_Q5_1, 2>(st, "matvec_kernel<Q5_1,NT=2>")) != MQ_OK) return s;
   return MQ_OK;
 }
 
@@ -890,6 +1012,8 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   MvArgs a;
   a.q = W->q;
   a.d = W->d;
+  a.dm = W->dm;
+  a.qh = W->qh;
   a.x = x;
   a.y = y;
   a.N = W->N;
@@ -913,6 +1037,15 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
     case MQ_Q5_K:
       return two ? launch_one<MQ_Q5_K, 2>(a, s, "matvec_kernel<Q5_K,NT=2>")
                  : launch_one<MQ_Q5_K, 1>(a, s, "matvec_kernel<Q5_K,NT=1>");
+    case MQ_Q4_1:
+      return two ? launch_one<MQ_Q4_1, 2>(a, s, "matvec_kernel<Q4_1,NT=2>")
+                 : launch_one<MQ_Q4_1, 1>(a, s, "matvec_kernel<Q4_1,NT=1>");
+    case MQ_Q5_0:
+      return two ? launch_one<MQ_Q5_0, 2>(a, s, "matvec_kernel<Q5_0,NT=2>")
+                 : launch_one<MQ_Q5_0, 1>(a, s, "matvec_kernel<Q5_0,NT=1>");
+    case MQ_Q5_1:
+      return two ? launch_one<MQ_Q5_1, 2>(a, s, "matvec_kernel<Q5_1,NT=2>")
+                 : launch_one<MQ_Q5_1, 1>(a, s, "matvec_kernel<Q5_1,NT=1>");
     default:
       return two ? launch_one<MQ_Q8_0, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
                  : launch_one<MQ_Q8_0, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");

@@ -5,8 +5,8 @@
 // for the per-block epilogue).
 //
 // Exactness.  Both operands are integers carried in f16 (q in [-127, 127];
-// W_int = Q8_0 q, Q4_K sc_j*nib <= 945, Q6_K v = sc*(q-32) as even part +
-// odd part, each exact).  Every product is exact and every partial sum of a
+// W_int = Q8_0 q, Q4_0 n - 8, Q5_0 q - 16, Q4_1 / Q5_1 q, Q4_K sc_j*nib <= 945,
+// Q5_K sc_j*q <= 1953, Q6_K v = sc*(q-32) as even part + odd part, each exact).  Every product is exact and every partial sum of a
 // block stays below 2^24 (|D| <= 32*127*4097 < 16.7M), so tcgen05.mma kind::f16
 // accumulating one block in f32 yields the integer dot exactly.  sm_103a has
 // no integer tcgen05 kind, and f16 integers are exact, so this is the int8
@@ -36,11 +36,12 @@
 //               TMEM lanes 32*(w%4).. (its 32 rows) and 32 of the 128 columns;
 //               per block it loads the accumulator (tcgen05.ld) and promotes it
 //               in registers with packed f32x2 multiply-adds:
-//                 Q8_0: y += (s_m * d_n) * D
+//                 Q8_0, Q4_1: y += (s_m * d_n) * D
 //                 Q4_K, Q6_K: a = s_m * D (first block of a super-block), then
 //                             a += s_m * D; per super-block y += d_n * a
 //               and frees the accumulator pair after its second block.
-// Q4_K min term.  sum_b (s*S)_m,b * (dmin*m_j)_n,b is a product of rank K/32;
+// Min term (Q4_K: dmin*m_j per sub-block, subtracted; Q4_1: the block min m, added, so
+// its plane holds -m).  sum_b (s*S)_m,b * (dmin*m_j)_n,b is a product of rank K/32;
 // the tensor cores form it once per tile, after the main loop, from three f16
 // products per block (row side hi | hi | lo of (s*S)/u_m, column side
 // hi | lo | hi of (dmin*m_j)/v_n, u and v powers of two that keep both in f16
@@ -80,14 +81,14 @@ constexpr int stages() {  // 192 KB of operand ring
 }
 
 struct TcArgs {
-  const float *urow;    // [mt] Q4_K min-term row factors u_m
-  const float *vcol;    // [np] Q4_K min-term column factors v_n
+  const float *urow;    // [mt] min-term row factors u_m
+  const float *vcol;    // [np] min-term column factors v_n
   float *y;             // [M][N]
   int32_t *D;           // [M][N][nb] (block-dot mode)
   int64_t M, N, mt, np;
   int nb;
   int ntm, ntiles;      // output tiles: ntm along M (fastest), ntiles in all
-  int nms;              // Q4_K: ring stages of the min-term GEMM (3*nb/64 rounded up)
+  int nms;              // ring stages of the min-term GEMM (3*nb/64 rounded up), or 0
   int *status;
   int debug_expire;
   int swiglu;           // fused gate/up weight: y[m][n'] = silu(gate col) * (its up col), N / 2 wide
@@ -108,7 +109,7 @@ template <int TYPE>
 struct __align__(1024) TcSmem {
   static constexpr int NST = stages<TYPE>();
   static constexpr bool ODD = TYPE == MQ_Q6_K;
-  static constexpr bool MIN = TYPE == MQ_Q4_K;
+  static constexpr bool MIN = TYPE == MQ_Q4_K || TYPE == MQ_Q4_1;
   __half a[NST][TM * PK];
   __half b[NST][TN * PK];
   Slots<__half, ODD ? NST : 0, TN * PK> b2;
@@ -126,7 +127,7 @@ constexpr bool smem_layout_ok() {
          offsetof(S, gd) % 128 == 0 && offsetof(S, full) % 8 == 0;
 }
 static_assert(smem_layout_ok<MQ_Q8_0>() && smem_layout_ok<MQ_Q4_K>() &&
-                  smem_layout_ok<MQ_Q6_K>(),
+                  smem_layout_ok<MQ_Q6_K>() && smem_layout_ok<MQ_Q4_1>(),
               "TMA tiles need 1024-byte, bulk copies and float4 reads 16-byte alignment");
 
 __device__ __forceinline__ uint32_t sa(const void *p) {
@@ -235,6 +236,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   constexpr int NST = Sm::NST, SR = NST / 2;  // SR ring stages per MMA issuer
   static_assert(NST % 2 == 0, "the ring is split between two issuers");
   constexpr bool ODD = Sm::ODD, MIN = Sm::MIN;
+  // per-block epilogue (a scale d per 32-element block): Q8_0, and Q4_1 with its min term
+  constexpr bool PB = TYPE == MQ_Q8_0 || TYPE == MQ_Q4_1;
   extern __shared__ uint8_t smem_raw[];
   // aligned by an offset into the __shared__ array, so the compiler keeps knowing that
   // every member lives in shared memory (plain loads become LDS, addresses stay 32-bit)
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       smem_raw + ((1024u - (uint32_t)__cvta_generic_to_shared(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p.nb, npairs = (nb + 1) / 2, ngroups = (nb + 7) >> 3;
-  // Accumulator uses of a tile, in order: pair pr = use pr, then the Q4_K min-term GEMM
+  // Accumulator uses of a tile, in order: pair pr = use pr, then the min-term GEMM
   // as two uses (npairs + j, j < 2), one per issuer, use j taking min-term stages j,
   // j + 2, ... (use 1 has none when there is one stage).  The CTA is persistent: it
   // takes tiles blockIdx.x, + gridDim.x, ... and every ring, accumulator and group phase
@@ -389,21 +392,21 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
         const int pr = 4 * g + pp;
-        if (TYPE == MQ_Q8_0 && pr >= npairs) break;  // K % 256 == 0 for the K-quants
+        if (PB && pr >= npairs) break;  // K % 256 == 0 for the K-quants
         // accumulator i and its phase; compile-time i for the K-quants (even nuse)
         const int U = tl * nuse + pr;
-        const int i = TYPE == MQ_Q8_0 ? U & 1 : pp & 1;
-        const uint32_t par = TYPE == MQ_Q8_0 ? (U >> 1) & 1 : (ub + (pp >> 1)) & 1;
+        const int i = PB ? U & 1 : pp & 1;
+        const uint32_t par = PB ? (U >> 1) & 1 : (ub + (pp >> 1)) & 1;
         mbar_wait(sa(&sm.tfull[i]), par, p.status, 4, kWaitNs);
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int bi = 2 * pp + h, b = 8 * g + bi;
-          if (TYPE == MQ_Q8_0 && b >= nb) break;
+          if (PB && b >= nb) break;
           uint32_t r[EC];
           TC_LD32(trow + (uint32_t)(256 * i + 128 * h), r);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (h == 1 || (TYPE == MQ_Q8_0 && b == nb - 1)) {  // accumulators in registers: free them
+          if (h == 1 || (PB && b == nb - 1)) {  // accumulators in registers: free them
             tc_fence_before();
             mbar_arrive(sa(&sm.tempty[i]));
           }
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           } else {
             const float sxv = gsx[bi * TM];
             const float2 sx2 = make_float2(sxv, sxv);
-            if constexpr (TYPE == MQ_Q8_0) {  // y += (s_m * d_n) * D per block
+            if constexpr (PB) {  // y += (s_m * d_n) * D per block
 #pragma unroll
               for (int j4 = 0; j4 < EC / 4; ++j4) {
                 const float4 c = *reinterpret_cast<const float4 *>(gd + bi * TN + 4 * j4);
@@ -540,14 +543,14 @@ mq_status get_encode() {
   return MQ_OK;
 }
 
-// f16 [rows][K] K-major, box 64 x 128, 128-byte swizzle (rows beyond the tensor and
-// columns beyond K read as 0).
+// f16 [rows][K] K-major with row stride ld elements (K when 0), box 64 x 128, 128-byte
+// swizzle (rows beyond the tensor and columns beyond K read as 0).
 mq_status encode_f16_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K,
-                         const char *what) {
+                         const char *what, int64_t ld = 0) {
   mq_status s = get_encode();
   if (s != MQ_OK) return s;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld ? ld : K) * 2};
   cuuint32_t box[2] = {PK, 128};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
@@ -607,7 +610,7 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
   const CUtensorMap &tW2 = *reinterpret_cast<const CUtensorMap *>(
       TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);
   const CUtensorMap &tBm = *reinterpret_cast<const CUtensorMap *>(
-      TYPE == MQ_Q4_K && !DOTS ? W->tmap_mb : W->tmap_w);
+      TcSmem<TYPE>::MIN && !DOTS ? W->tmap_mb : W->tmap_w);
   const CUtensorMap &tD = *reinterpret_cast<const CUtensorMap *>(DOTS ? W->tmap_w : W->tmap_td);
   mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, tSx, tD,
                                                                     a);
@@ -627,7 +630,7 @@ mq_status encode_weight_maps(mq_weight *w) {
                        "weight odd-part");
   if (s == MQ_OK && w->mb)
     s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_mb), w->mb, w->np,
-                       3 * (w->K / 32), "weight min-term");
+                       3 * (w->K / 32), "weight min-term", min_ld(w->K / 32));
   if (s == MQ_OK)
     s = encode_scale_map(reinterpret_cast<CUtensorMap *>(w->tmap_td), w->td, w->np, w->K / 32,
                          "weight block scale");
@@ -640,6 +643,7 @@ mq_status init_kernels(DeviceState *st) {
   if ((s = optin_t<MQ_Q8_0, false>(st, "mmq_tc_kernel<Q8_0>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q4_K, false>(st, "mmq_tc_kernel<Q4_K>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q6_K, false>(st, "mmq_tc_kernel<Q6_K>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_1, false>(st, "mmq_tc_kernel<Q4_1>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q8_0, true>(st, "mmq_tc_kernel<Q8_0,dots>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q4_K, true>(st, "mmq_tc_kernel<Q4_K,dots>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q6_K, true>(st, "mmq_tc_kernel<Q6_K,dots>")) != MQ_OK) return s;
@@ -653,11 +657,14 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   alignas(64) CUtensorMap tA, tAm;
   mq_status r = encode_f16_map(&tA, base + L.op, M, W->K, "activation");
   if (r != MQ_OK) return r;
-  // Q5_K runs the Q4_K kernel (integer weight sc*q, same min term) and Q4_0 the Q8_0
-  // kernel (integer weight q - 8, one scale per 32-element block)
-  const bool mins = (W->type == MQ_Q4_K || W->type == MQ_Q5_K) && D == nullptr;
-  if (mins && (r = encode_f16_map(&tAm, base + L.amin, M, 3 * (W->K / 32), "activation min-term")) !=
-                  MQ_OK)
+  // Q5_K runs the Q4_K kernel (integer weight sc*q, same min term); Q4_0 and Q5_0 the
+  // Q8_0 kernel (integer weight n - 8 / q - 16, one scale per 32-element block); Q5_1 the
+  // Q4_1 kernel (one scale per block plus the min term of m)
+  const bool mins = (W->type == MQ_Q4_K || W->type == MQ_Q5_K || W->type == MQ_Q4_1 ||
+                     W->type == MQ_Q5_1) &&
+                    D == nullptr;
+  if (mins && (r = encode_f16_map(&tAm, base + L.amin, M, 3 * (W->K / 32), "activation min-term",
+                                  min_ld(W->K / 32))) != MQ_OK)
     return r;
   if (!mins) tAm = tA;
   alignas(64) CUtensorMap tSx;
@@ -694,6 +701,10 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
     case MQ_Q5_K:
       return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
                   : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
+    case MQ_Q4_1:
+    case MQ_Q5_1:  // block dots need no min term: the Q8_0 block-dot kernel
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q4_1, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_1>");
     case MQ_Q6_K:
       return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
                   : launch_t<MQ_Q6_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K>");

@@ -122,11 +122,11 @@ extern "C" mq_status mq_init(int device) {
 }
 
 static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t K) {
-  if (type != MQ_Q4_0 && type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q5_K &&
-      type != MQ_Q6_K)
+  if (type != MQ_Q4_0 && type != MQ_Q4_1 && type != MQ_Q5_0 && type != MQ_Q5_1 &&
+      type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q5_K && type != MQ_Q6_K)
     return fail(MQ_ERR_TYPE,
-                "%s: unsupported GGUF type %d (supported: 2 Q4_0, 8 Q8_0, 12 Q4_K, 13 Q5_K, "
-                "14 Q6_K)",
+                "%s: unsupported GGUF type %d (supported: 2 Q4_0, 3 Q4_1, 6 Q5_0, 7 Q5_1, "
+                "8 Q8_0, 12 Q4_K, 13 Q5_K, 14 Q6_K)",
                 site, type);
   if (N < 1 || K < 1)
     return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld must both be >= 1", site, (long long)N,
@@ -142,10 +142,10 @@ static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t
 }
 
 static mq_status free_planes(mq_weight *w) {
-  void *ps[] = {w->q, w->d, w->mw, w->mw2, w->td, w->tm, w->mb, w->vcol};
+  void *ps[] = {w->q, w->d, w->qh, w->dm, w->mw, w->mw2, w->td, w->tm, w->mb, w->vcol};
   for (void *p : ps)
     if (p) cudaFree(p);
-  w->q = nullptr; w->d = nullptr; w->mw = nullptr;
+  w->q = nullptr; w->d = nullptr; w->qh = nullptr; w->dm = nullptr; w->mw = nullptr;
   w->mw2 = nullptr; w->td = nullptr; w->tm = nullptr; w->mb = nullptr; w->vcol = nullptr;
   return MQ_OK;
 }
@@ -208,9 +208,15 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
   if (type == MQ_Q8_0) {
     if ((s = zalloc(&w->q, npad * K, "q8_0 qs")) != MQ_OK) return cleanup(s);
     if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q8_0 d")) != MQ_OK) return cleanup(s);
-  } else if (type == MQ_Q4_0) {
-    if ((s = zalloc(&w->q, npad * K / 2, "q4_0 qs")) != MQ_OK) return cleanup(s);
-    if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q4_0 d")) != MQ_OK) return cleanup(s);
+  } else if (block_elems(type) == 32) {  // Q4_0, Q4_1, Q5_0, Q5_1
+    if ((s = zalloc(&w->q, npad * K / 2, "4-bit quants")) != MQ_OK) return cleanup(s);
+    if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "block d")) != MQ_OK) return cleanup(s);
+    if ((type == MQ_Q4_1 || type == MQ_Q5_1) &&
+        (s = zalloc(&w->dm, npad * w->nchunk * 8 * 2, "block m")) != MQ_OK)
+      return cleanup(s);
+    if ((type == MQ_Q5_0 || type == MQ_Q5_1) &&
+        (s = zalloc(&w->qh, npad * (K / 32) * 4, "fifth bits")) != MQ_OK)
+      return cleanup(s);
   } else if (type == MQ_Q4_K) {
     if ((s = zalloc(&w->q, npad * nsb * 144, "q4_K")) != MQ_OK) return cleanup(s);
   } else if (type == MQ_Q5_K) {
@@ -227,7 +233,8 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
       return cleanup(s);
     if ((s = alloc_plane(&w->td, size_t(w->np) * (K / 32) * 4, &total, "prefill d")) != MQ_OK)
       return cleanup(s);
-    const bool mins = type == MQ_Q4_K || type == MQ_Q5_K;
+    const bool mins =
+        type == MQ_Q4_K || type == MQ_Q5_K || type == MQ_Q4_1 || type == MQ_Q5_1;
     if (mins &&
         (s = alloc_plane(&w->tm, size_t(w->np) * (K / 32) * 4, &total, "prefill min")) != MQ_OK)
       return cleanup(s);
@@ -235,7 +242,7 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
     cudaMemsetAsync(w->td, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
     if (w->tm) cudaMemsetAsync(w->tm, 0, size_t(w->np) * (K / 32) * 4, st->reg_stream);
     if (mins) {
-      if ((s = zalloc(&w->mb, size_t(w->np) * 3 * (K / 32) * 2, "prefill min operand")) != MQ_OK)
+      if ((s = zalloc(&w->mb, size_t(w->np) * min_ld(K / 32) * 2, "prefill min operand")) != MQ_OK)
         return cleanup(s);
       if ((s = zalloc(&w->vcol, size_t(w->np) * 4, "prefill min scale")) != MQ_OK)
         return cleanup(s);

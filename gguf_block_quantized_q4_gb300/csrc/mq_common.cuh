@@ -24,17 +24,26 @@
 //   Q8_0  qs  tile (g,c) at (g*K + 256c)*128 bytes, [block j][row r][32 bytes]:
 //             stored byte 8t + 4u + i  <-  block byte 16u + 4t + i (u = 16-element half)
 //         d   u16 at ((g*nchunk + c)*128 + r)*8 + j (8 slots per chunk; unused ones 0)
+//   Q4_0, Q4_1, Q5_0, Q5_1  q  tile (g,c) at (g*K/2 + 128c)*128 bytes, [block j][row r]
+//             [16 bytes]: stored byte 4t + i  <-  qs byte 4t + {0,2,1,3}[i]; d as Q8_0's;
+//         dm  (Q4_1, Q5_1) u16 m, laid out as d
+//         qh  (Q5_0, Q5_1) u32 at (g*K/32 + 8c + j)*128 + r: the fifth bits regrouped,
+//             bit 4r' + t and 16 + 4r' + t = the two elements of fragment register r'
+//             of thread t (r' = 0, 1: elements 4t + 2r', +1; r' = 2, 3: 16 + 4t + 2(r'-2), +1)
 // Prefill operand planes (MQ_REG_NO_MMQ_PLANE skips them), K-major for TMA:
-//   w      f16  [N][K]    integer weight W_int: Q8_0 q; Q4_K sc_j*nib (<= 945);
+//   w      f16  [N][K]    integer weight W_int: Q8_0 q; Q4_0 n - 8; Q5_0 q - 16; Q4_1 / Q5_1
+//                         q; Q4_K sc_j*nib (<= 945); Q5_K sc_j*q (<= 1953);
 //                         Q6_K the even part 2*floor(v/2) of v = sc*(q-32) (|v| <= 4096)
 //   w2     f16  [N][K]    Q6_K only: the odd part v - 2*floor(v/2) in {0, 1}
 //                         (every value exact in f16; w + w2 = v)
 //   td     f32  [K/32][Np] block scale d of each 32-element block (transposed;
 //                          Np = N rounded up to 128, the padding is zero)
-//   tm     f32  [K/32][Np] Q4_K only: dmin*m_j of each block (transposed)
-//   mb     f16  [Np][3*K/32] Q4_K only: min-term operand, row n holds hi | lo | hi over
-//                          the blocks of m~ = dmin*m_j / v_n (hi = f16(m~), lo = f16(m~ - hi))
-//   vcol   f32  [Np]       Q4_K only: v_n, a power of two with max_b |dmin*m_j| / v_n in
+//   tm     f32  [K/32][Np] min types only: dmin*m_j (Q4_K, Q5_K) or -m (Q4_1, Q5_1) of each
+//                          block (transposed)
+//   mb     f16  [Np][min_ld] min-term operand (Q4_K, Q5_K: dmin*m_j; Q4_1, Q5_1: -m),
+//                          row n holds hi | lo | hi over the blocks of m~ = tm / v_n
+//                          (hi = f16(m~), lo = f16(m~ - hi))
+//   vcol   f32  [Np]       min types only: v_n, a power of two with max_b |tm| / v_n in
 //                          [2^13, 2^14) (0 for the padding rows)
 #pragma once
 
@@ -57,8 +66,10 @@ struct mq_weight {
                          // the same 8 rows of the up weight (N = 2 x the gate rows)
   size_t device_bytes;   // all planes
   // decode planes
-  uint8_t *q = nullptr;  // Q8_0 qs / Q4_K and Q6_K tiles
-  uint16_t *d = nullptr; // Q8_0 block d
+  uint8_t *q = nullptr;  // Q8_0 / Q4_0 / Q4_1 / Q5_x quants, Q4_K / Q5_K / Q6_K tiles
+  uint16_t *d = nullptr; // per-32-block types: block d
+  uint32_t *qh = nullptr; // Q5_0 / Q5_1: fifth-bit words, one per (block, row)
+  uint16_t *dm = nullptr; // Q4_1 / Q5_1: block m (the additive min)
   // prefill operand planes
   __half *mw = nullptr;
   __half *mw2 = nullptr;
@@ -110,7 +121,7 @@ mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 // [M][K/32], q as f16 [M][K], then the transposed block scales sT f32
 // [K/32][Mt] and the min-term factors tT = s*S f32 [K/32][Mt], Mt = M rounded up
 // to 128 (the epilogue's tile rows are one contiguous 512-byte run per block);
-// then the min-term operand f16 [M][3*K/32] (row m: t~hi | t~hi | t~lo over the
+// then the min-term operand f16 [M][min_ld] (row m: t~hi | t~hi | t~lo over the
 // blocks, t~ = s*S/u_m) and the row factors u_m f32 [Mt] (powers of two).
 struct ActLayout {
   size_t qs, scale, bsum, op, st, tt, amin, urow, total;
@@ -118,6 +129,10 @@ struct ActLayout {
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+// Row stride (elements) of the min-term operands [rows][3*K/32]: rounded up to 8 so that
+// every row starts on a 16-byte boundary (a TMA stride rule); the columns past 3*K/32 are
+// never read (the tensor maps end at 3*K/32 and fill beyond it with zeros).
+__host__ __device__ inline int64_t min_ld(int64_t nb) { return (3 * nb + 7) / 8 * 8; }
 inline ActLayout act_layout(int64_t M, int64_t K) {
   ActLayout L;
   L.mt = round_up(M, 128);
@@ -128,15 +143,20 @@ inline ActLayout act_layout(int64_t M, int64_t K) {
   L.st = align256(L.op + size_t(M) * K * 2);
   L.tt = align256(L.st + size_t(L.mt) * (K / 32) * 4);
   L.amin = align256(L.tt + size_t(L.mt) * (K / 32) * 4);
-  L.urow = align256(L.amin + size_t(M) * 3 * (K / 32) * 2);
+  L.urow = align256(L.amin + size_t(M) * min_ld(K / 32) * 2);
   L.total = align256(L.urow + size_t(L.mt) * 4);
   return L;
 }
 
-inline int block_elems(int type) { return (type == MQ_Q8_0 || type == MQ_Q4_0) ? 32 : 256; }
+inline int block_elems(int type) {
+  return (type == MQ_Q4_K || type == MQ_Q5_K || type == MQ_Q6_K) ? 256 : 32;
+}
 inline int block_bytes(int type) {
   switch (type) {
     case MQ_Q4_0: return 18;
+    case MQ_Q4_1: return 20;
+    case MQ_Q5_0: return 22;
+    case MQ_Q5_1: return 24;
     case MQ_Q8_0: return 34;
     case MQ_Q4_K: return 144;
     case MQ_Q5_K: return 176;

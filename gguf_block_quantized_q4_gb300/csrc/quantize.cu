@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
   k = min(max(k, -100), 100);
   const float inv_u = __int_as_float((127 - k) << 23);
   if (threadIdx.x == 0) reinterpret_cast<float *>(xq + L.urow)[m] = __int_as_float((127 + k) << 23);
-  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * 3 * nb;
+  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * min_ld(nb);
   for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
     const float t = (b < kTtCache ? ttc[b] : reinterpret_cast<const float *>(xq + L.tt)[b * L.mt + m]) * inv_u;
     const __half hi = __float2half_rn(t);

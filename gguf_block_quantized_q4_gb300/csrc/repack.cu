@@ -11,13 +11,15 @@
 //         element 64c + 32h + l is nibble h of qs[32c + l];  w = d*sc_j*nib - dmin*m_j
 //   Q4_0  18 B / 32 el : f16 d, u8 qs[16]; element j < 16 = low nibble of qs[j],
 //         element 16 + j = its high nibble;                  w = d*(nib - 8)
+//   Q4_1, Q5_0, Q5_1: as Q4_0 with an additive min and / or a fifth-bit word (below)
 //   Q5_K 176 B / 256 el: as Q4_K (d, dmin, scales[12]), u8 qh[32], u8 qs[128];
 //         element 64c + 32h + l: nibble h of qs[32c + l] plus bit 2c + h of qh[l] << 4
 //   Q6_K 210 B / 256 el: u8 ql[128], u8 qh[64], int8 sc[16], f16 d
 //         element 128h + 32r + l: low 4 bits from ql[64h + 32(r%2) + l] (low nibble
 //         for r<2, high for r>=2), high 2 bits = (qh[32h + l] >> 2r) & 3;
 //         w = d * sc[e/16] * (q - 32)
-// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_0 nib - 8; Q4_K sc_j*nib,
+// The prefill planes hold the integer weight W_int (Q8_0 q; Q4_0 nib - 8; Q5_0 q - 16;
+// Q4_1 / Q5_1 the unsigned q, their min m entering through tm = -m; Q4_K sc_j*nib,
 // at most 945, and Q5_K sc_j*q, at most 1953, exact in f16; Q6_K v = sc*(q-32),
 // |v| <= 4096, stored as its even
 // part 2*floor(v/2) plus its odd part in {0,1}, both exact in f16) and the
@@ -150,51 +152,122 @@ __global__ void unpack_q4_k(const uint8_t *__restrict__ q, int64_t N, int64_t K,
           dst[16 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]] = src[16 + 32 * t + 4 * (2 * c + u) + e];
 }
 
-// Q4_0 decode plane: per (row group, chunk), [8 blocks][128 rows][16 bytes]; word t of a
-// (block, row) holds quant bytes 4t + kQ4kPerm[e] (the block's elements 4t..4t+3 in its low
-// nibbles, elements 16 + 4t.. in its high nibbles).  The d plane is laid out as Q8_0's.
+// Per-32-block nibble types.  Decode plane per (row group, chunk): [8 blocks][128 rows]
+// [16 bytes]; word t of a (block, row) holds quant bytes 4t + kQ4kPerm[e] (the block's
+// elements 4t..4t+3 in its low nibbles, elements 16 + 4t.. in its high nibbles).  The d
+// plane (and, for Q4_1 / Q5_1, the m plane) is laid out as Q8_0's d.  Q5_0 / Q5_1 add one
+// 32-bit fifth-bit word per (block, row), [8 blocks][128 rows] per (row group, chunk),
+// whose bits are regrouped so that fragment thread t finds the pair of elements of its
+// register r (r = 0, 1: elements 4t + 2r, +1; r = 2, 3: elements 16 + 4t + 2(r - 2), +1)
+// at bits 4r + t and 16 + 4r + t.
+//   Q4_0  18 B: f16 d, qs[16];                        w = d*(nib - 8)
+//   Q4_1  20 B: f16 d, f16 m, qs[16];                 w = d*nib + m
+//   Q5_0  22 B: f16 d, u32 qh, qs[16];                w = d*(q - 16), q = nib | bit e of qh << 4
+//   Q5_1  24 B: f16 d, f16 m, u32 qh, qs[16];         w = d*q + m
 __device__ __forceinline__ int64_t q4_0_off(int64_t n, int64_t b, int64_t K) {
   const int64_t g = n / kRowGroup, r = n % kRowGroup, c = b / 8, j = b % 8;
   return (g * (K / 2) + int64_t(kChunk / 2) * c) * kRowGroup + (j * kRowGroup + r) * 16;
 }
+// index of the fifth-bit word of (row n, block b)
+__device__ __forceinline__ int64_t qh_idx(int64_t n, int64_t b, int64_t K) {
+  return (n / kRowGroup * (K / 32) + b) * kRowGroup + n % kRowGroup;
+}
+// raw element of the low bit of the pair at stored bit 4r + t
+__device__ __forceinline__ int qh_elem(int r, int t) { return 16 * (r >> 1) + 4 * t + 2 * (r & 1); }
+__device__ __forceinline__ uint32_t qh_regroup(uint32_t h) {
+  uint32_t o = 0;
+  for (int r = 0; r < 4; ++r)
+    for (int t = 0; t < 4; ++t) {
+      const int e = qh_elem(r, t);
+      o |= ((h >> e) & 1u) << (4 * r + t);
+      o |= ((h >> (e + 1)) & 1u) << (16 + 4 * r + t);
+    }
+  return o;
+}
+__device__ __forceinline__ uint32_t qh_restore(uint32_t o) {
+  uint32_t h = 0;
+  for (int r = 0; r < 4; ++r)
+    for (int t = 0; t < 4; ++t) {
+      const int e = qh_elem(r, t);
+      h |= ((o >> (4 * r + t)) & 1u) << e;
+      h |= ((o >> (16 + 4 * r + t)) & 1u) << (e + 1);
+    }
+  return h;
+}
+template <int TYPE>
+struct Nib32 {
+  static constexpr bool MADD = TYPE == MQ_Q4_1 || TYPE == MQ_Q5_1;  // additive min m
+  static constexpr bool Q5 = TYPE == MQ_Q5_0 || TYPE == MQ_Q5_1;    // fifth bits
+  static constexpr int BB = 18 + (MADD ? 2 : 0) + (Q5 ? 4 : 0);      // block bytes
+  static constexpr int QO = BB - 16;                                // quant bytes offset
+  static constexpr int HO = MADD ? 4 : 2;                           // fifth-bit word offset
+};
 
-__global__ void repack_q4_0(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
-                            uint8_t *__restrict__ q, uint16_t *__restrict__ d,
-                            __half *__restrict__ mw, float *__restrict__ td) {
+// One thread per block.  Prefill planes: W_int = nib - 8 (Q4_0), q - 16 (Q5_0) or the
+// unsigned q (Q4_1, Q5_1); td = d; tm = -m (the min term enters as y -= sum tm * s * S).
+template <int TYPE>
+__global__ void repack_nib32(const uint8_t *__restrict__ raw, int64_t N, int64_t K, int64_t NP,
+                             uint8_t *__restrict__ q, uint16_t *__restrict__ d,
+                             uint16_t *__restrict__ dm, uint32_t *__restrict__ qh,
+                             __half *__restrict__ mw, float *__restrict__ td,
+                             float *__restrict__ tm) {
+  using T = Nib32<TYPE>;
   const int64_t nb = K / 32;
   const int nchunk = (int)((K + kChunk - 1) / kChunk);
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nb) return;
   const int64_t n = i / nb, b = i % nb;
-  const uint8_t *src = raw + i * 18;
+  const uint8_t *src = raw + i * T::BB;
   const uint16_t dbits = rd16(src);
   d[q8_0_doff(n, b, nchunk)] = dbits;
+  if (T::MADD) dm[q8_0_doff(n, b, nchunk)] = rd16(src + 2);
+  uint32_t h = 0;
+  if (T::Q5) {
+    h = (uint32_t)src[T::HO] | ((uint32_t)src[T::HO + 1] << 8) | ((uint32_t)src[T::HO + 2] << 16) |
+        ((uint32_t)src[T::HO + 3] << 24);
+    qh[qh_idx(n, b, K)] = qh_regroup(h);
+  }
   uint8_t *dst = q + q4_0_off(n, b, K);
   for (int t = 0; t < 4; ++t)
-    for (int e = 0; e < 4; ++e) dst[4 * t + e] = src[2 + 4 * t + kQ4kPerm[e]];
+    for (int e = 0; e < 4; ++e) dst[4 * t + e] = src[T::QO + 4 * t + kQ4kPerm[e]];
   if (mw) {
     for (int e = 0; e < 32; ++e) {
-      const int nib = (src[2 + (e & 15)] >> (4 * (e >> 4))) & 15;
-      mw[n * K + b * 32 + e] = __int2half_rn(nib - 8);
+      const int nib = (src[T::QO + (e & 15)] >> (4 * (e >> 4))) & 15;
+      const int qv = T::Q5 ? nib | (int)(((h >> e) & 1u) << 4) : nib;
+      const int wint = T::MADD ? qv : (T::Q5 ? qv - 16 : qv - 8);
+      mw[n * K + b * 32 + e] = __int2half_rn(wint);
     }
     td[b * NP + n] = f16bits(dbits);
+    if (T::MADD) tm[b * NP + n] = -f16bits(rd16(src + 2));
   }
 }
 
-__global__ void unpack_q4_0(const uint8_t *__restrict__ q, const uint16_t *__restrict__ d,
-                            int64_t N, int64_t K, uint8_t *__restrict__ raw) {
+template <int TYPE>
+__global__ void unpack_nib32(const uint8_t *__restrict__ q, const uint16_t *__restrict__ d,
+                             const uint16_t *__restrict__ dm, const uint32_t *__restrict__ qh,
+                             int64_t N, int64_t K, uint8_t *__restrict__ raw) {
+  using T = Nib32<TYPE>;
   const int64_t nb = K / 32;
   const int nchunk = (int)((K + kChunk - 1) / kChunk);
   const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   if (i >= N * nb) return;
   const int64_t n = i / nb, b = i % nb;
-  uint8_t *dst = raw + i * 18;
+  uint8_t *dst = raw + i * T::BB;
   const uint16_t dv = d[q8_0_doff(n, b, nchunk)];
   dst[0] = dv & 255;
   dst[1] = dv >> 8;
+  if (T::MADD) {
+    const uint16_t mv = dm[q8_0_doff(n, b, nchunk)];
+    dst[2] = mv & 255;
+    dst[3] = mv >> 8;
+  }
+  if (T::Q5) {
+    const uint32_t h = qh_restore(qh[qh_idx(n, b, K)]);
+    for (int k = 0; k < 4; ++k) dst[T::HO + k] = (uint8_t)(h >> (8 * k));
+  }
   const uint8_t *src = q + q4_0_off(n, b, K);
   for (int t = 0; t < 4; ++t)
-    for (int e = 0; e < 4; ++e) dst[2 + 4 * t + kQ4kPerm[e]] = src[4 * t + e];
+    for (int e = 0; e < 4; ++e) dst[T::QO + 4 * t + kQ4kPerm[e]] = src[4 * t + e];
 }
 
 // Q5_K decode tile: 128 rows x 176 bytes, row = 16-byte header (d, dmin, scales), the
@@ -331,7 +404,7 @@ __global__ void minplane_q4_k(const float *__restrict__ tm, int64_t N, int64_t n
   k = min(max(k, -100), 100);
   const float inv_v = __int_as_float((127 - k) << 23);
   vcol[n] = __int_as_float((127 + k) << 23);
-  __half *row = mb + n * 3 * nb;
+  __half *row = mb + n * min_ld(nb);
   for (int64_t b = 0; b < nb; ++b) {
     const float t = tm[b * NP + n] * inv_v;
     const __half hi = __float2half_rn(t);
@@ -354,11 +427,31 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
     repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
                                               w->td);
     MQ_LAUNCH_CHECK("repack_q8_0");
-  } else if (w->type == MQ_Q4_0) {
+  } else if (block_elems(w->type) == 32) {
     const int64_t n = N * (K / 32);
-    repack_q4_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
-                                              w->td);
-    MQ_LAUNCH_CHECK("repack_q4_0");
+    __half *mw = mmq ? w->mw : nullptr;
+    switch (w->type) {
+      case MQ_Q4_0:
+        repack_nib32<MQ_Q4_0><<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, w->dm,
+                                                           w->qh, mw, w->td, w->tm);
+        break;
+      case MQ_Q4_1:
+        repack_nib32<MQ_Q4_1><<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, w->dm,
+                                                           w->qh, mw, w->td, w->tm);
+        break;
+      case MQ_Q5_0:
+        repack_nib32<MQ_Q5_0><<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, w->dm,
+                                                           w->qh, mw, w->td, w->tm);
+        break;
+      default:
+        repack_nib32<MQ_Q5_1><<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, w->dm,
+                                                           w->qh, mw, w->td, w->tm);
+    }
+    MQ_LAUNCH_CHECK("repack_nib32");
+    if (mmq && w->tm) {
+      minplane_q4_k<<<grid_for(N, T), T, 0, s>>>(w->tm, N, K / 32, w->np, w->mb, w->vcol);
+      MQ_LAUNCH_CHECK("minplane_q4_k");
+    }
   } else if (w->type == MQ_Q4_K || w->type == MQ_Q5_K) {
     const int64_t n = N * (K / 256);
     if (w->type == MQ_Q4_K) {
@@ -389,9 +482,22 @@ mq_status unpack_weight(const mq_weight *w, uint8_t *raw, cudaStream_t s) {
   if (w->type == MQ_Q8_0) {
     unpack_q8_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q8_0");
-  } else if (w->type == MQ_Q4_0) {
-    unpack_q4_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
-    MQ_LAUNCH_CHECK("unpack_q4_0");
+  } else if (block_elems(w->type) == 32) {
+    const unsigned g = grid_for(N * (K / 32), T);
+    switch (w->type) {
+      case MQ_Q4_0:
+        unpack_nib32<MQ_Q4_0><<<g, T, 0, s>>>(w->q, w->d, w->dm, w->qh, N, K, raw);
+        break;
+      case MQ_Q4_1:
+        unpack_nib32<MQ_Q4_1><<<g, T, 0, s>>>(w->q, w->d, w->dm, w->qh, N, K, raw);
+        break;
+      case MQ_Q5_0:
+        unpack_nib32<MQ_Q5_0><<<g, T, 0, s>>>(w->q, w->d, w->dm, w->qh, N, K, raw);
+        break;
+      default:
+        unpack_nib32<MQ_Q5_1><<<g, T, 0, s>>>(w->q, w->d, w->dm, w->qh, N, K, raw);
+    }
+    MQ_LAUNCH_CHECK("unpack_nib32");
   } else if (w->type == MQ_Q4_K) {
     unpack_q4_k<<<grid_for(N * (K / 256), T), T, 0, s>>>(w->q, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q4_k");

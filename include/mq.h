@@ -45,6 +45,13 @@ extern "C" {
  *   MQ_Q4_0: 32-element blocks of 18 bytes: f16 d, 16 bytes of 4-bit quants
  *            (element j < 16 the low nibble of byte j, element 16 + j its high
  *            nibble);  w = d*(q - 8).
+ *   MQ_Q4_1: 32-element blocks of 20 bytes: f16 d, f16 m, 16 quant bytes (nibbles as
+ *            MQ_Q4_0);  w = d*q + m.
+ *   MQ_Q5_0: 32-element blocks of 22 bytes: f16 d, a 32-bit little-endian word whose
+ *            bit e is the fifth bit of element e, 16 quant bytes (low four bits as
+ *            MQ_Q4_0);  w = d*(q - 16), q in [0, 31].
+ *   MQ_Q5_1: 32-element blocks of 24 bytes: f16 d, f16 m, the fifth-bit word, 16 quant
+ *            bytes;  w = d*q + m.
  *   MQ_Q8_0: 32-element blocks of 34 bytes: f16 d, 32 x int8 q;  w = d*q.
  *   MQ_Q4_K: 256-element super-blocks of 144 bytes: f16 d, f16 dmin, 12 bytes
  *            of packed 6-bit sub-block scales/mins, 128 bytes of 4-bit quants;
@@ -56,9 +63,13 @@ extern "C" {
  *   MQ_Q6_K: 256-element super-blocks of 210 bytes: 128 bytes low 4 bits,
  *            64 bytes high 2 bits, 16 int8 sub-scales, f16 d;
  *            w = d*sc*(q - 32).
- * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256); Q4_0 and
- * Q5_K are among the types its weight gate admits (§4.6). */
-typedef enum { MQ_Q4_0 = 2, MQ_Q8_0 = 8, MQ_Q4_K = 12, MQ_Q5_K = 13, MQ_Q6_K = 14 } mq_type;
+ * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256); Q4_0, Q4_1,
+ * Q5_0, Q5_1 and Q5_K are among the types its matmul whitelist and weight gate admit
+ * (§4.3, §4.6). */
+typedef enum {
+    MQ_Q4_0 = 2, MQ_Q4_1 = 3, MQ_Q5_0 = 6, MQ_Q5_1 = 7, MQ_Q8_0 = 8,
+    MQ_Q4_K = 12, MQ_Q5_K = 13, MQ_Q6_K = 14
+} mq_type;
 
 typedef enum {
     MQ_OK = 0,
@@ -145,8 +156,9 @@ mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, 
  *   operand f16   [M][K]       q as f16 (exact), the tensor-core operand
  *   scaleT  f32   [K/32][Mt]   s transposed (rows >= M unspecified)
  *   minT    f32   [K/32][Mt]   s * S transposed, the min-term factor (rows >= M unspecified)
- *   amin    f16   [M][3*K/32]  min-term operand: row m holds hi | hi | lo over the
- *                              blocks b of t = s*S / u_m, hi = f16(t), lo = f16(t - hi)
+ *   amin    f16   [M][L]       min-term operand, L = 3*K/32 rounded up to a multiple of 8:
+ *                              row m holds hi | hi | lo over the blocks b of t = s*S / u_m,
+ *                              hi = f16(t), lo = f16(t - hi) (columns 3*K/32..L-1 unspecified)
  *   urow    f32   [Mt]         u_m = 2^k, k = E - 140 clamped to [-100, 100], E the biased
  *                              binary32 exponent of max_b |s*S| (so max_b |s*S| / u_m is in
  *                              [2^13, 2^14) for a normal maximum); k = 0 when the row's s*S

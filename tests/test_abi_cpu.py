@@ -54,12 +54,14 @@ def test_status_names(L):
 def test_act_bytes_layout(L):
     assert L.mq_act_bytes(0, 64) == 0
     assert L.mq_act_bytes(4, 48) == 0
-    M, K = 3, 96
     al = lambda v: (v + 255) & ~255
     mt = 128
-    expect = al(al(al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2) + mt * 3 * 4)
-                      + mt * 3 * 4) + M * 3 * 3 * 2) + mt * 4)
-    assert L.mq_act_bytes(M, K) == expect == mq.act_layout(M, K)["total"]
+    # the min-term operand row of 3 blocks x 3 parts is padded to 16 f16 (16-byte rows)
+    for M, K in ((3, 96), (20, 96)):
+        expect = al(al(al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2)
+                                 + mt * 3 * 4) + mt * 3 * 4) + M * 16 * 2) + mt * 4)
+        assert L.mq_act_bytes(M, K) == expect == mq.act_layout(M, K)["total"]
+    assert mq.min_ld(3) == 16 and mq.min_ld(112) == 336
     assert L.mq_act_bytes(512, 3584) % 256 == 0
 
 
@@ -72,8 +74,8 @@ def _reg(L, qtype, data, N, K, flags=0):
 
 
 def test_register_rejects_bad_type(L):
-    st, msg = _reg(L, 3, np.zeros(20 * 8, np.uint8), 1, 256)  # Q4_1: not supported
-    assert mq.STATUS[st] == "MQ_ERR_TYPE" and "unsupported GGUF type 3" in msg
+    st, msg = _reg(L, 10, np.zeros(84, np.uint8), 1, 256)  # Q2_K: not supported
+    assert mq.STATUS[st] == "MQ_ERR_TYPE" and "unsupported GGUF type 10" in msg
 
 
 def test_register_rejects_bad_shape(L):
@@ -160,7 +162,7 @@ def test_ffn_gu_registration_validates_before_device_work(L):
     assert mq.STATUS[st] == "MQ_ERR_SHAPE" and "multiple of 8" in msg
     st, msg = _reg_gu(L, mq.Q4_K, z, z, 16 * row - 1, 16, 256)
     assert mq.STATUS[st] == "MQ_ERR_PAYLOAD" and str(16 * row) in msg
-    st, msg = _reg_gu(L, 3, z, z, 16 * row, 16, 256)
+    st, msg = _reg_gu(L, 10, z, z, 16 * row, 16, 256)
     assert mq.STATUS[st] == "MQ_ERR_TYPE"
     h = ctypes.c_void_p()
     st = L.mq_register_ffn_gu(mq.Q4_K, None, None, 16 * row, 16, 256, 0, ctypes.byref(h))

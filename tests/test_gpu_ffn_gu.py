@@ -39,7 +39,8 @@ def pair(qtype, N, K, s):
 
 @pytest.mark.parametrize("qtype,N,K", [
     (synth.Q8_0, 8, 96), (synth.Q8_0, 136, 288), (synth.Q4_K, 8, 256), (synth.Q4_K, 72, 512),
-    (synth.Q4_K, 200, 768), (synth.Q6_K, 24, 256), (synth.Q6_K, 136, 512)])
+    (synth.Q4_K, 200, 768), (synth.Q6_K, 24, 256), (synth.Q6_K, 136, 512),
+    (synth.Q4_1, 72, 288), (synth.Q5_0, 136, 96), (synth.Q5_1, 8, 512)])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_ffn_gu_matvec_small_shapes(qtype, N, K, B):
     g, u = pair(qtype, N, K, 500 + N)
@@ -69,7 +70,8 @@ def test_ffn_gu_matvec_ffn_shapes(qtype, N, K, B):
 
 @pytest.mark.parametrize("qtype,N,K,M", [
     (synth.Q8_0, 8, 96, 5), (synth.Q8_0, 136, 320, 130), (synth.Q4_K, 8, 256, 19),
-    (synth.Q4_K, 200, 768, 140), (synth.Q6_K, 72, 512, 64)])
+    (synth.Q4_K, 200, 768, 140), (synth.Q6_K, 72, 512, 64), (synth.Q4_1, 136, 288, 70),
+    (synth.Q5_0, 8, 96, 5), (synth.Q5_1, 72, 512, 129)])
 def test_ffn_gu_mmq_small_shapes(qtype, N, K, M):
     g, u = pair(qtype, N, K, 700 + N)
     W = mq.register_ffn_gu(qtype, g, u, N, K)

@@ -64,7 +64,9 @@ def gpu_matvec(W, x):
 @pytest.mark.parametrize("qtype,N,K", [(8, 37, 96), (8, 896, 896), (12, 19, 512),
                                        (12, 18944, 3584), (14, 21, 768), (14, 3584, 18944),
                                        (2, 37, 96), (2, 4864, 896), (13, 19, 512),
-                                       (13, 18944, 3584)])
+                                       (13, 18944, 3584), (3, 37, 96), (3, 4864, 896),
+                                       (6, 37, 96), (6, 18944, 3584), (7, 37, 96),
+                                       (7, 3584, 18944)])
 def test_decode_plane_roundtrip_is_byte_exact(qtype, N, K):
     W = registered(qtype, N, K, 7)
     assert np.array_equal(W.unpack(), weights(qtype, N, K, 7))
@@ -78,7 +80,10 @@ SMALL = [(8, 1, 32), (8, 37, 96), (8, 130, 288), (8, 64, 896),
          (12, 1, 256), (12, 19, 512), (12, 100, 768), (12, 257, 2560),
          (14, 1, 256), (14, 21, 768), (14, 130, 512), (14, 64, 4608),
          (2, 1, 32), (2, 37, 96), (2, 130, 288), (2, 64, 896), (2, 300, 4864),
-         (13, 1, 256), (13, 19, 512), (13, 100, 768), (13, 257, 2560)]
+         (13, 1, 256), (13, 19, 512), (13, 100, 768), (13, 257, 2560),
+         (3, 1, 32), (3, 37, 96), (3, 130, 288), (3, 300, 4864),
+         (6, 1, 32), (6, 37, 96), (6, 130, 288), (6, 300, 4864),
+         (7, 1, 32), (7, 37, 96), (7, 130, 288), (7, 300, 4864)]
 
 
 @pytest.mark.parametrize("qtype,N,K", SMALL)
@@ -123,7 +128,8 @@ def test_matvec_batch_columns_equal_single_calls_bitwise():
 
 
 @pytest.mark.parametrize("qtype,N,K", [(8, 70, 288), (12, 70, 768), (14, 70, 768),
-                                       (2, 70, 288), (13, 70, 768)])
+                                       (2, 70, 288), (13, 70, 768), (3, 70, 288), (6, 70, 288),
+                                       (7, 70, 288)])
 def test_matvec_extreme_magnitudes(qtype, N, K):
     W = registered(qtype, N, K, 13)
     rng = np.random.default_rng(5)
@@ -215,7 +221,9 @@ def test_quantize_small_and_edge_blocks(M, K):
 
 SMALL_MMQ = [(8, 37, 96, 5), (8, 130, 288, 70), (12, 19, 512, 9), (12, 200, 768, 65),
              (14, 21, 768, 3), (14, 130, 512, 129),
-             (2, 37, 96, 5), (2, 130, 288, 70), (13, 19, 512, 9), (13, 200, 768, 65)]
+             (2, 37, 96, 5), (2, 130, 288, 70), (13, 19, 512, 9), (13, 200, 768, 65),
+             (3, 37, 96, 5), (3, 130, 288, 70), (6, 37, 96, 5), (6, 130, 288, 70),
+             (7, 37, 96, 5), (7, 130, 288, 70), (7, 200, 800, 131)]
 
 
 @pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
@@ -248,17 +256,19 @@ def test_blockdots_bit_exact_workload_tiles(name):
     W.free()
 
 
+@pytest.mark.parametrize("qtype", [12, 3])
 @pytest.mark.parametrize("N,K,M", [(19, 256, 9), (70, 8192, 5), (130, 3584, 130)])
-def test_mmq_q4_k_min_term_stages(N, K, M):
-    """Q4_K min-term GEMM over 1, 12 (two rounds of the operand ring) and 6 stages."""
-    W = registered(12, N, K, 23)
+def test_mmq_min_term_stages(qtype, N, K, M):
+    """Min-term GEMM (Q4_K sub-block mins, Q4_1 block mins) over 1, 12 (two rounds of the
+    operand ring) and 6 stages."""
+    W = registered(qtype, N, K, 23)
     x = synth.activations(M, K, seed=K + M)
     xq, qs, sc, _, _ = gpu_quantize(x)
     y = mq.mmq(W, xq, M)
     torch.cuda.synchronize()
     mq.stream_status()
-    yref, bnd = oracle.mmq(12, weights(12, N, K, 23), N, K, qs, sc)
-    assert_bound(y.cpu().numpy(), yref, bnd, f"mmq Q4_K {M}x{N}x{K}")
+    yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 23), N, K, qs, sc)
+    assert_bound(y.cpu().numpy(), yref, bnd, f"mmq type {qtype} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("qtype,N,K,M", SMALL_MMQ)
@@ -345,10 +355,13 @@ def test_errors_are_reported_not_fallen_back():
     mq.stream_status()
 
 
-# ---- the Q4_0 and Q5_K types at model-sized shapes ---------------------------
+# ---- the Q4_0, Q4_1, Q5_0, Q5_1 and Q5_K types at model-sized shapes -----------
 
 @pytest.mark.parametrize("qtype,N,K,B", [(2, 4864, 896, 1), (2, 18944, 3584, 4),
-                                         (13, 18944, 3584, 1), (13, 3584, 18944, 8)])
+                                         (13, 18944, 3584, 1), (13, 3584, 18944, 8),
+                                         (3, 18944, 3584, 1), (3, 4864, 896, 8),
+                                         (6, 18944, 3584, 2), (6, 3584, 18944, 1),
+                                         (7, 18944, 3584, 1), (7, 3584, 18944, 5)])
 def test_matvec_new_types_ffn_shapes(qtype, N, K, B):
     W = registered(qtype, N, K, 41, mq.REG_NO_MMQ_PLANE)
     x = synth.activations(B, K, seed=42)
@@ -357,7 +370,7 @@ def test_matvec_new_types_ffn_shapes(qtype, N, K, B):
     assert_bound(y, yref, bnd, f"type {qtype} {N}x{K} B={B}")
 
 
-@pytest.mark.parametrize("qtype", [2, 13])
+@pytest.mark.parametrize("qtype", [2, 13, 3, 6, 7])
 def test_mmq_new_types_prefill_shape_sampled(qtype):
     N, K, M = 18944, 3584, 512
     W = registered(qtype, N, K, 43)
