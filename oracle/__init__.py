@@ -41,6 +41,8 @@ def lib():
         L = ctypes.CDLL(build())
         L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         L.oracle_f16_to_double.restype = ctypes.c_double
+        L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_double.restype = ctypes.c_double
         L.oracle_q4_k_scale_min.argtypes = [_P, ctypes.c_int, _P, _P]
         L.oracle_q4_k_scale_min.restype = None
         L.oracle_dequant_row.argtypes = [ctypes.c_int, _P, _I64, _P]
@@ -71,6 +73,10 @@ def _check(rc, what):
 
 def f16_to_double(bits: int) -> float:
     return lib().oracle_f16_to_double(bits)
+
+
+def bf16_to_double(bits: int) -> float:
+    return lib().oracle_bf16_to_double(bits)
 
 
 def q4_k_scale_min(s12: bytes, j: int):

@@ -14,7 +14,9 @@
  * What it computes, and the passage each function follows:
  *
  *  - f16 -> double: IEEE 754 binary16 decoding, subnormals and signed zero
- *    included (the block scales d and dmin are binary16).
+ *    included (the block scales d and dmin are binary16); bf16 -> double likewise
+ *    (the upper half of a binary32).  f16 and bf16 weight rows (the f16/bf16 kernels
+ *    of "CUDA Backend Design" §4.4) are K such elements, with no integer form.
  *  - dequantisation of one weight row, per the GGUF block layouts whose byte
  *    ratios the minfer "CUDA Backend Design" page gives in §2.3 (q8_0 34 bytes
  *    per 32 elements, q4_K 144 per 256, q6_K 210 per 256; q4_0 and q5_K, among
@@ -43,6 +45,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#define OR_F16 1
+#define OR_BF16 30
 #define OR_Q4_0 2
 #define OR_Q4_1 3
 #define OR_Q5_0 6
@@ -71,11 +75,35 @@ double oracle_f16_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* ---- bfloat16 -> double --------------------------------------------------
+ * sign 1 bit, exponent 8 bits (bias 127), fraction 7 bits (the upper half of a
+ * binary32).  exponent 0: subnormal fraction * 2^-133; exponent 255: inf / NaN. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 255;
+    int f = h & 127;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);
+    } else if (e == 255) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + f), e - 134);
+    }
+    return sign ? -v : v;
+}
+
 static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* f16 / bf16 weights: one 2-byte little-endian element per "block", no integer form */
+static int is_float_type(int type) { return type == OR_F16 || type == OR_BF16; }
 
 int oracle_block_elems(int type)
 {
     switch (type) {
+    case OR_F16: return 1;
+    case OR_BF16: return 1;
     case OR_Q4_0: return 32;
     case OR_Q4_1: return 32;
     case OR_Q5_0: return 32;
@@ -91,6 +119,8 @@ int oracle_block_elems(int type)
 int oracle_block_bytes(int type)
 {
     switch (type) {
+    case OR_F16: return 2;
+    case OR_BF16: return 2;
     case OR_Q4_0: return 18;
     case OR_Q4_1: return 20;
     case OR_Q5_0: return 22;
@@ -211,6 +241,12 @@ static int valid_shape(int type, int64_t K)
 int oracle_dequant_row(int type, const uint8_t *row, int64_t K, double *out)
 {
     if (!valid_shape(type, K)) return -1;
+    if (is_float_type(type)) {
+        for (int64_t k = 0; k < K; ++k)
+            out[k] = type == OR_F16 ? oracle_f16_to_double(rd16(row + 2 * k))
+                                    : oracle_bf16_to_double(rd16(row + 2 * k));
+        return 0;
+    }
     int be = oracle_block_elems(type), bb = oracle_block_bytes(type);
     for (int64_t b = 0; b < K / be; ++b) {
         const uint8_t *blk = row + b * bb;
@@ -228,7 +264,7 @@ int oracle_dequant_row(int type, const uint8_t *row, int64_t K, double *out)
 /* Integer weights of one row (the W_int of the block dots). */
 int oracle_int_weights_row(int type, const uint8_t *row, int64_t K, int64_t *out)
 {
-    if (!valid_shape(type, K)) return -1;
+    if (!valid_shape(type, K) || is_float_type(type)) return -1;
     int be = oracle_block_elems(type), bb = oracle_block_bytes(type);
     for (int64_t b = 0; b < K / be; ++b) {
         for (int e = 0; e < be; ++e) {
@@ -314,7 +350,8 @@ int oracle_blockdots(int type, const uint8_t *W, int64_t N, int64_t K, const int
                      int64_t M, const int64_t *mrows, int64_t nm, int64_t n0, int64_t n1,
                      int64_t *D)
 {
-    if (!valid_shape(type, K) || n0 < 0 || n1 > N || n0 > n1) return -1;
+    if (!valid_shape(type, K) || is_float_type(type) || K % 32 || n0 < 0 || n1 > N || n0 > n1)
+        return -1;
     int64_t rowbytes = K / oracle_block_elems(type) * oracle_block_bytes(type);
     int64_t nb = K / 32;
     int64_t *wi = (int64_t *)malloc((size_t)K * sizeof(int64_t));
@@ -342,7 +379,7 @@ int oracle_mmq(int type, const uint8_t *W, int64_t N, int64_t K, const int8_t *q
                const float *scale, int64_t M, const int64_t *mrows, int64_t nm, int64_t n0,
                int64_t n1, double *y, double *bound)
 {
-    if (!valid_shape(type, K) || n0 < 0 || n1 > N || n0 > n1 || nm < 0) return -1;
+    if (!valid_shape(type, K) || K % 32 || n0 < 0 || n1 > N || n0 > n1 || nm < 0) return -1;
     int64_t rowbytes = K / oracle_block_elems(type) * oracle_block_bytes(type);
     int64_t nb = K / 32;
     for (int64_t i = 0; i < nm; ++i)

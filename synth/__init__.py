@@ -28,6 +28,9 @@ Field distributions follow the five hot-path workloads (Qwen2.5-0.5B/7B shaped):
 * Q5_K (256 elements, 176 bytes): as Q4_K (f16 ``d = |N| * 0.02``, ``dmin = |N| * 0.01``,
   12 scale bytes) then 32 high-bit bytes and 128 quant bytes, all uniform on [0, 255]
   (each 5-bit quant uniform on [0, 31]).
+* F16 (one element, 2 bytes): ``N(0,1) * 0.02`` rounded to f16.
+* BF16 (one element, 2 bytes): the upper 16 bits of the f32 ``N(0,1) * 0.02`` (the value
+  truncated toward zero to bfloat16).
 * activations: f32 ``N(0,1) * x_scale``.
 
 Random draws use ``numpy.random.Generator(PCG64(seed))``; within a weight the
@@ -38,12 +41,13 @@ from __future__ import annotations
 import numpy as np
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14  # GGUF type ids
+F16, BF16 = 1, 30
 
 # type id -> (elements per block, bytes per block)
 BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34),
-         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210)}
+         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), F16: (1, 2), BF16: (1, 2)}
 TYPE_NAME = {Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q5_1: "Q5_1", Q8_0: "Q8_0",
-             Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+             Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", F16: "F16", BF16: "BF16"}
 
 
 def nbytes(qtype: int, N: int, K: int) -> int:
@@ -126,8 +130,18 @@ def q5_k_weights(N: int, K: int, seed: int, d_scale: float = 0.02,
     return out.reshape(-1)
 
 
+def float_weights(N: int, K: int, seed: int, bf16: bool, w_scale: float = 0.02) -> np.ndarray:
+    """F16 or BF16: N x K elements, row-major, little-endian."""
+    rng = np.random.default_rng(seed)
+    v = (rng.standard_normal(N * K) * w_scale).astype(np.float32)
+    bits = (v.view(np.uint32) >> 16).astype(np.uint16) if bf16 else v.astype(np.float16).view(np.uint16)
+    return bits.astype("<u2").view(np.uint8).copy()
+
+
 def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
     """Raw GGUF bytes of an N x K weight, rows contiguous, blocks along K."""
+    if qtype in (F16, BF16):
+        return float_weights(N, K, seed, qtype == BF16)
     if qtype == Q4_0:
         return q4_0_weights(N, K, seed)
     if qtype == Q4_1:

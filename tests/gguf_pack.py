@@ -117,6 +117,11 @@ def _f16(u8pair: np.ndarray) -> np.ndarray:
 
 def np_dequant(qtype: int, W: np.ndarray, N: int, K: int) -> np.ndarray:
     W = np.asarray(W, dtype=np.uint8)
+    if qtype == 1:  # f16, little-endian
+        return W.view("<f2").astype(np.float64).reshape(N, K)
+    if qtype == 30:  # bf16: the upper half of a binary32
+        bits = W.view("<u2").astype(np.uint32) << 16
+        return bits.view(np.float32).astype(np.float64).reshape(N, K)
     if qtype == 8:
         blk = W.reshape(N, K // 32, 34)
         d = _f16(blk[:, :, 0:2])

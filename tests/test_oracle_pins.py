@@ -55,6 +55,41 @@ def test_f16_golden_values():
         assert got == float(v) and np.signbit(got) == np.signbit(float(v)), (b, v, got)
 
 
+def test_bf16_all_bit_patterns_match_binary32():
+    """bfloat16 is the upper half of a binary32: numpy's f32 decoding of bits << 16."""
+    bits = np.arange(65536, dtype=np.uint32)
+    ref = (bits << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_golden_values():
+    for line in open(os.path.join(GOLD, "bf16_values.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        b, v = line.split()
+        got = oracle.bf16_to_double(int(b, 16))
+        assert got == float(v) and np.signbit(got) == np.signbit(float(v)), (b, v, got)
+
+
+def test_float_weight_rows_worked_by_hand():
+    """f16 row (1, 2, -0.5, 65504) and bf16 row (1, -123.5, 0.25, 10) against x = (1, 1, 2, 1/4):
+    1 + 2 - 1 + 16376 = 16378 and 1 - 123.5 + 0.5 + 2.5 = -119.5."""
+    x = np.array([[1.0, 1.0, 2.0, 0.25]], np.float32)
+    wf = np.array([0x3C00, 0x4000, 0xB800, 0x7BFF], "<u2").view(np.uint8)
+    y, bnd = oracle.matvec(1, wf, 1, 4, x)
+    assert y[0, 0] == 16378.0 and bnd[0, 0] == 1 + 2 + 1 + 16376.0
+    wb = np.array([0x3F80, 0xC2F7, 0x3E80, 0x4120], "<u2").view(np.uint8)
+    y, bnd = oracle.matvec(30, wb, 1, 4, x)
+    assert y[0, 0] == -119.5 and bnd[0, 0] == 1 + 123.5 + 0.5 + 2.5
+    # no integer form: the block-dot reference refuses float weights
+    with pytest.raises(ValueError):
+        oracle.blockdots(1, np.zeros(64, np.uint8), 1, 32, np.zeros((1, 32), np.int8))
+
+
 # ---- hand-worked blocks ----------------------------------------------------
 
 def test_q8_0_ramp_block():
@@ -271,14 +306,14 @@ def test_unit_scales_reduce_to_integer_matrix_product(qtype):
 
 # ---- second formulation (vectorised numpy) and brute force ----------------
 
-@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [1, 30, 2, 3, 6, 7, 8, 12, 13, 14])
 def test_dequant_matches_vectorised_numpy_decoder(qtype):
     N, K = 7, 512
     W = synth.weights(qtype, N, K, seed=11)
     assert np.array_equal(oracle.dequant(qtype, W, N, K), gp.np_dequant(qtype, W, N, K))
 
 
-@pytest.mark.parametrize("qtype", [2, 3, 6, 7, 8, 12, 13, 14])
+@pytest.mark.parametrize("qtype", [1, 30, 2, 3, 6, 7, 8, 12, 13, 14])
 @pytest.mark.parametrize("N,K,B", [(1, 256, 1), (2, 256, 8), (3, 512, 4), (3, 512, 2)])
 def test_brute_force_tiny_matvec(qtype, N, K, B):
     W = synth.weights(qtype, N, K, seed=N * 100 + K + B)
