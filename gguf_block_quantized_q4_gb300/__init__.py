@@ -22,9 +22,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmq.so")
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14
+F16, BF16 = 1, 30  # unquantised weights: decode matvec only
 REG_DEFAULT, REG_NO_MMQ_PLANE = 0, 1
+# (elements, bytes) per block; f16 / bf16 rows count in units of 32 elements (K % 32 == 0)
 BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34),
-         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210)}
+         Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), F16: (32, 64), BF16: (32, 64)}
 
 STATUS = ["MQ_OK", "MQ_ERR_ARG", "MQ_ERR_TYPE", "MQ_ERR_SHAPE", "MQ_ERR_PAYLOAD",
           "MQ_ERR_ALIGN", "MQ_ERR_CUDA", "MQ_ERR_OOM", "MQ_ERR_LAUNCH", "MQ_ERR_TIMEOUT",

@@ -57,6 +57,7 @@
 // rank order (deterministic, and independent of B, so every column of a batched
 // call equals the B = 1 call bitwise).  All mbarrier waits are bounded.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include "mq_common.cuh"
 
@@ -122,10 +123,16 @@ template <int TYPE>
 __host__ __device__ constexpr int q32_off_h() {
   return q32_off_d<TYPE>() + kRows * 16 * (addmin_type<TYPE>() ? 2 : 1);
 }
+// Unquantised f16 / bf16 weights.
+template <int TYPE>
+__host__ __device__ constexpr bool float_w() {
+  return TYPE == MQ_F16 || TYPE == MQ_BF16;
+}
 // Bytes of one (128-row group, chunk) tile of the decode plane.
 template <int TYPE>
 __host__ __device__ constexpr int tile_bytes() {
-  return TYPE == MQ_Q4_K   ? kRows * 144
+  return float_w<TYPE>()   ? kRows * kChunk * 2
+         : TYPE == MQ_Q4_K ? kRows * 144
          : TYPE == MQ_Q5_K ? kRows * 176
          : TYPE == MQ_Q6_K ? kRows * 210
                            : q32_off_h<TYPE>() + (fifth_type<TYPE>() ? kRows * 32 : 0);
@@ -176,6 +183,12 @@ struct WarpTab<MQ_Q4_1> {
 template <>
 struct WarpTab<MQ_Q5_1> : WarpTab<MQ_Q4_1> {};
 template <>
+struct WarpTab<MQ_F16> {
+  float unused;  // no scales: the weights are the f16 operand itself
+};
+template <>
+struct WarpTab<MQ_BF16> : WarpTab<MQ_F16> {};
+template <>
 struct WarpTab<MQ_Q5_K> : WarpTab<MQ_Q4_K> {};
 
 template <int TYPE, int NT>
@@ -202,6 +215,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 operands (unquantised bf16 weights, bf16 hi/lo activation parts)
+__device__ __forceinline__ void mma16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -240,6 +264,12 @@ __device__ __forceinline__ float f16_lo(uint32_t v) {
 __device__ __forceinline__ float f16_hi(uint32_t v) {
   return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __device__ __forceinline__ int chunk_width(int64_t K, int c) {
   const int64_t left = K - int64_t(c) * kChunk;
@@ -301,8 +331,9 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
     constexpr bool Q32 = q32_type<TYPE>();  // per-32-block scales
     constexpr int QB = q32_bytes<TYPE>();  // quant bytes per block row
     constexpr int HB = fifth_type<TYPE>() ? 4 : 0, MB = addmin_type<TYPE>() ? 16 : 0;
-    const uint32_t wbytes = Q32 ? (uint32_t)(kRows * (cw / 32) * (QB + HB) + kRows * (16 + MB))
-                                : (uint32_t)tile_bytes<TYPE>();
+    const uint32_t wbytes = Q32            ? (uint32_t)(kRows * (cw / 32) * (QB + HB) + kRows * (16 + MB))
+                            : float_w<TYPE>() ? (uint32_t)(kRows * cw * 2)
+                                              : (uint32_t)tile_bytes<TYPE>();
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"(wbytes + (uint32_t)(p.B * cw * 4))
                  : "memory");
@@ -318,6 +349,8 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
       if constexpr (fifth_type<TYPE>())
         bulk_1d(sa(w + q32_off_h<TYPE>()), p.qh + (group * (p.K / 32) + int64_t(c) * 8) * kRows,
                 (uint32_t)(kRows * (cw / 32) * 4), bar);
+    } else if constexpr (float_w<TYPE>()) {  // a partial last chunk is a shorter run
+      bulk_1d(sa(w), p.q + (group * p.K + int64_t(c) * kChunk) * kRows * 2, wbytes, bar);
     } else {
       bulk_1d(sa(w), p.q + (group * p.nchunk + c) * int64_t(tile_bytes<TYPE>()),
               (uint32_t)tile_bytes<TYPE>(), bar);
@@ -377,9 +410,18 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
         const int f = lane + 32 * k, g16 = f >> 2, t = f & 3;
         const float v0 = v[k].x * scale, v1 = v[k].y * scale, v2 = v[k].z * scale,
                     v3 = v[k].w * scale;
-        const uint32_t hi01 = pack_f16x2(v0, v1), hi23 = pack_f16x2(v2, v3);
-        const uint32_t lo01 = pack_f16x2(v0 - f16_lo(hi01), v1 - f16_hi(hi01));
-        const uint32_t lo23 = pack_f16x2(v2 - f16_lo(hi23), v3 - f16_hi(hi23));
+        uint32_t hi01, hi23, lo01, lo23;
+        if constexpr (TYPE == MQ_BF16) {  // bf16 parts: 16 significant bits of x
+          hi01 = pack_bf16x2(v0, v1);
+          hi23 = pack_bf16x2(v2, v3);
+          lo01 = pack_bf16x2(v0 - bf16_lo(hi01), v1 - bf16_hi(hi01));
+          lo23 = pack_bf16x2(v2 - bf16_lo(hi23), v3 - bf16_hi(hi23));
+        } else {
+          hi01 = pack_f16x2(v0, v1);
+          hi23 = pack_f16x2(v2, v3);
+          lo01 = pack_f16x2(v0 - f16_lo(hi01), v1 - f16_hi(hi01));
+          lo23 = pack_f16x2(v2 - f16_lo(hi23), v3 - f16_hi(hi23));
+        }
         sm.frag[fs][g16][b >> 2][col * 4 + t] = make_uint2(hi01, hi23);
         sm.frag[fs][g16][b >> 2][(col + 1) * 4 + t] = make_uint2(lo01, lo23);
         if constexpr (addmin_type<TYPE>()) {
@@ -799,6 +841,49 @@ __device__ __forceinline__ void compute_chunk_q32(MvSmem<TYPE, NT> &sm, int s, i
   }
 }
 
+// F16 / BF16: the weights are the A operand as stored (thread t's 8 bytes of a 16-element
+// group and row hold elements 4t..4t+3, the two registers of a row).  Nothing to decode,
+// so the warp reads its words straight from the stage inside the MMA loop and releases
+// the stage after it.  Against bf16 weights the x warp stages bf16 hi/lo parts.
+template <int TYPE, int NT>
+__device__ __forceinline__ void compute_chunk_float(MvSmem<TYPE, NT> &sm, int s, int fs,
+                                                    uint32_t fpar, int warp, int lane,
+                                                    int *status, int ngrp, const int (&fl)[NT],
+                                                    float (&tot)[2][NT]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t *tile = sm.w[s];
+  const int ra = 16 * warp + g, rb = ra + 8;
+  mbar_wait(sa(&sm.ffull[fs]), fpar, status, 24);
+  float c4[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) c4[i][r] = 0.f;
+#pragma unroll
+  for (int grp = 0; grp < 16; ++grp) {
+    if (grp < ngrp) {
+      const uint2 wa = *reinterpret_cast<const uint2 *>(tile + (grp * kRows + ra) * 32 + 8 * t);
+      const uint2 wb = *reinterpret_cast<const uint2 *>(tile + (grp * kRows + rb) * 32 + 8 * t);
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const uint2 bf = sm.frag[fs][grp][i][fl[i]];
+        if constexpr (TYPE == MQ_BF16)
+          mma16816_bf16(c4[i], wa.x, wb.x, wa.y, wb.y, bf.x, bf.y);
+        else
+          mma16816(c4[i], wa.x, wb.x, wa.y, wb.y, bf.x, bf.y);
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const float us = sm.unscale[fs][4 * i + t];
+    tot[0][i] = fmaf(us, c4[i][0] + c4[i][1], tot[0][i]);
+    tot[1][i] = fmaf(us, c4[i][2] + c4[i][3], tot[1][i]);
+  }
+}
+
 // Results of the thread's row pair (rA, rA + 8) for batch row b.  A fused gate/up
 // weight has rows in units of 16 (8 gate rows, then the same 8 rows of the up
 // weight), so rA is a gate row and rA + 8 its up row: one SwiGLU output,
@@ -882,6 +967,9 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
         compute_chunk_q4k<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
       else if constexpr (TYPE == MQ_Q6_K)
         compute_chunk_q6k<NT>(sm, s, fs, fpar, warp, lane, p.status, fl, tot);
+      else if constexpr (float_w<TYPE>())
+        compute_chunk_float<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status,
+                                      chunk_width(p.K, c_begin + i) / 16, fl, tot);
       else
         compute_chunk_q32<TYPE, NT>(sm, s, fs, fpar, warp, lane, p.status,
                                     chunk_width(p.K, c_begin + i) / 32, fl, tot);
@@ -992,16 +1080,20 @@ mq_status init_matvec(DeviceState *st) {
   if ((s = optin_mv<MQ_Q5_0, 2>(st, "matvec_kernel<Q5_0,NT=2>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q5_1, 1>(st, "matvec_kernel<Q5_1,NT=1>")) != MQ_OK) return s;
   if ((s = optin_mv<MQ_Q5_1, 2>(st, "matvec_kernel<Q5_1,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_F16, 1>(st, "matvec_kernel<F16,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_F16, 2>(st, "matvec_kernel<F16,NT=2>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_BF16, 1>(st, "matvec_kernel<BF16,NT=1>")) != MQ_OK) return s;
+  if ((s = optin_mv<MQ_BF16, 2>(st, "matvec_kernel<BF16,NT=2>")) != MQ_OK) return s;
   return MQ_OK;
 }
 
 // K-split: as many slices as keep every CTA of the grid resident in one wave
-// of two CTAs per SM (at most 8, a portable cluster).  Depends only on (N, K),
-// never on B, so batched columns reproduce the B = 1 result bitwise.
-static int choose_split(int64_t N, int64_t K, int sms) {
+// of cps CTAs per SM (at most 8, a portable cluster).  Depends only on (N, K) and the
+// type, never on B, so batched columns reproduce the B = 1 result bitwise.
+static int choose_split(int64_t N, int64_t K, int sms, int cps) {
   const int64_t groups = (N + kRows - 1) / kRows;
   const int nchunk = (int)((K + kChunk - 1) / kChunk);
-  const int64_t fit = 2 * int64_t(sms) / groups;
+  const int64_t fit = cps * int64_t(sms) / groups;
   int S = (int)(fit < 8 ? fit : 8);
   S = min(S, nchunk);
   return max(S, 1);
@@ -1020,7 +1112,8 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.K = W->K;
   a.B = B;
   a.nchunk = (int)((W->K + kChunk - 1) / kChunk);
-  a.S = choose_split(W->N, W->K, st->sms);
+  // the f16 / bf16 stages (64 KB) leave room for one CTA per SM, the others for two
+  a.S = choose_split(W->N, W->K, st->sms, float_type(W->type) ? 1 : 2);
   a.swiglu = W->ffn_gu;
   a.status = st->status;
   const bool two = B > 4;
@@ -1046,6 +1139,12 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
     case MQ_Q5_1:
       return two ? launch_one<MQ_Q5_1, 2>(a, s, "matvec_kernel<Q5_1,NT=2>")
                  : launch_one<MQ_Q5_1, 1>(a, s, "matvec_kernel<Q5_1,NT=1>");
+    case MQ_F16:
+      return two ? launch_one<MQ_F16, 2>(a, s, "matvec_kernel<F16,NT=2>")
+                 : launch_one<MQ_F16, 1>(a, s, "matvec_kernel<F16,NT=1>");
+    case MQ_BF16:
+      return two ? launch_one<MQ_BF16, 2>(a, s, "matvec_kernel<BF16,NT=2>")
+                 : launch_one<MQ_BF16, 1>(a, s, "matvec_kernel<BF16,NT=1>");
     default:
       return two ? launch_one<MQ_Q8_0, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
                  : launch_one<MQ_Q8_0, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");

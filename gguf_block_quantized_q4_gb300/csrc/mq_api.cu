@@ -123,10 +123,11 @@ extern "C" mq_status mq_init(int device) {
 
 static mq_status check_type_shape(const char *site, int type, int64_t N, int64_t K) {
   if (type != MQ_Q4_0 && type != MQ_Q4_1 && type != MQ_Q5_0 && type != MQ_Q5_1 &&
-      type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q5_K && type != MQ_Q6_K)
+      type != MQ_Q8_0 && type != MQ_Q4_K && type != MQ_Q5_K && type != MQ_Q6_K &&
+      !float_type(type))
     return fail(MQ_ERR_TYPE,
-                "%s: unsupported GGUF type %d (supported: 2 Q4_0, 3 Q4_1, 6 Q5_0, 7 Q5_1, "
-                "8 Q8_0, 12 Q4_K, 13 Q5_K, 14 Q6_K)",
+                "%s: unsupported GGUF type %d (supported: 1 F16, 2 Q4_0, 3 Q4_1, 6 Q5_0, "
+                "7 Q5_1, 8 Q8_0, 12 Q4_K, 13 Q5_K, 14 Q6_K, 30 BF16)",
                 site, type);
   if (N < 1 || K < 1)
     return fail(MQ_ERR_SHAPE, "%s: N=%lld K=%lld must both be >= 1", site, (long long)N,
@@ -205,7 +206,9 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
     if (r == MQ_OK) cudaMemsetAsync(*pp, 0, bytes, st->reg_stream);
     return r;
   };
-  if (type == MQ_Q8_0) {
+  if (float_type(type)) {
+    if ((s = zalloc(&w->q, npad * K * 2, "f16/bf16 weights")) != MQ_OK) return cleanup(s);
+  } else if (type == MQ_Q8_0) {
     if ((s = zalloc(&w->q, npad * K, "q8_0 qs")) != MQ_OK) return cleanup(s);
     if ((s = zalloc(&w->d, npad * w->nchunk * 8 * 2, "q8_0 d")) != MQ_OK) return cleanup(s);
   } else if (block_elems(type) == 32) {  // Q4_0, Q4_1, Q5_0, Q5_1
@@ -224,7 +227,8 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
   } else {
     if ((s = zalloc(&w->q, npad * nsb * 210, "q6_K")) != MQ_OK) return cleanup(s);
   }
-  const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE);
+  // f16 / bf16 weights have no integer form and no prefill planes
+  const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE) && !float_type(type);
   if (mmq) {
     if ((s = alloc_plane(&w->mw, size_t(N) * K * 2, &total, "prefill operand")) != MQ_OK)
       return cleanup(s);
@@ -467,6 +471,9 @@ static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, 
                             int ffn_gu = 0) {
   mq_status s = check_weight(site, type, W, N, K, ffn_gu);
   if (s != MQ_OK) return s;
+  if (float_type(type))
+    return fail(MQ_ERR_TYPE, "%s: type %d is an unquantised (f16/bf16) weight: it has no "
+                "integer MMQ form; use the matvec", site, type);
   if (!W->mw)
     return fail(MQ_ERR_ARG, "%s: the weight was registered with MQ_REG_NO_MMQ_PLANE", site);
   if (M < 1 || M > (int64_t(1) << 31))

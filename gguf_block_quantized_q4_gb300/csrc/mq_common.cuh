@@ -24,6 +24,8 @@
 //   Q8_0  qs  tile (g,c) at (g*K + 256c)*128 bytes, [block j][row r][32 bytes]:
 //             stored byte 8t + 4u + i  <-  block byte 16u + 4t + i (u = 16-element half)
 //         d   u16 at ((g*nchunk + c)*128 + r)*8 + j (8 slots per chunk; unused ones 0)
+//   F16, BF16 q  tile (g,c) at (g*K + 256c)*128*2 bytes, [16-element group j][row r]
+//             [16 elements]: thread t's four elements 4t..4t+3 of a group are 8 contiguous bytes
 //   Q4_0, Q4_1, Q5_0, Q5_1  q  tile (g,c) at (g*K/2 + 128c)*128 bytes, [block j][row r]
 //             [16 bytes]: stored byte 4t + i  <-  qs byte 4t + {0,2,1,3}[i]; d as Q8_0's;
 //         dm  (Q4_1, Q5_1) u16 m, laid out as d
@@ -148,6 +150,7 @@ inline ActLayout act_layout(int64_t M, int64_t K) {
   return L;
 }
 
+inline bool float_type(int type) { return type == MQ_F16 || type == MQ_BF16; }
 inline int block_elems(int type) {
   return (type == MQ_Q4_K || type == MQ_Q5_K || type == MQ_Q6_K) ? 256 : 32;
 }
@@ -160,6 +163,8 @@ inline int block_bytes(int type) {
     case MQ_Q8_0: return 34;
     case MQ_Q4_K: return 144;
     case MQ_Q5_K: return 176;
+    case MQ_F16: return 64;   // 32 elements of 2 bytes (the K % 32 unit)
+    case MQ_BF16: return 64;
     default: return 210;
   }
 }

@@ -270,6 +270,36 @@ __global__ void unpack_nib32(const uint8_t *__restrict__ q, const uint16_t *__re
     for (int e = 0; e < 4; ++e) dst[T::QO + 4 * t + kQ4kPerm[e]] = src[4 * t + e];
 }
 
+// F16 / BF16 decode plane: per (row group, chunk), [16-element group j][128 rows][32 bytes],
+// the group's elements in their natural order (thread t's elements 4t..4t+3 are bytes
+// 8t..8t+7).  One thread per (row, group): 32 bytes, as two 16-byte words.
+__device__ __forceinline__ int64_t float_off(int64_t n, int64_t grp, int64_t K) {
+  const int64_t g = n / kRowGroup, r = n % kRowGroup, c = grp / 16, j = grp % 16;
+  return (g * K + int64_t(kChunk) * c) * kRowGroup * 2 + (j * kRowGroup + r) * 32;
+}
+
+__global__ void repack_float(const uint8_t *__restrict__ raw, int64_t N, int64_t K,
+                             uint8_t *__restrict__ q) {
+  const int64_t ng = K / 16;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * ng) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(raw + i * 32);
+  uint4 *dst = reinterpret_cast<uint4 *>(q + float_off(i / ng, i % ng, K));
+  dst[0] = src[0];
+  dst[1] = src[1];
+}
+
+__global__ void unpack_float(const uint8_t *__restrict__ q, int64_t N, int64_t K,
+                             uint8_t *__restrict__ raw) {
+  const int64_t ng = K / 16;
+  const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (i >= N * ng) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(q + float_off(i / ng, i % ng, K));
+  uint4 *dst = reinterpret_cast<uint4 *>(raw + i * 32);
+  dst[0] = src[0];
+  dst[1] = src[1];
+}
+
 // Q5_K decode tile: 128 rows x 176 bytes, row = 16-byte header (d, dmin, scales), the
 // 128 quant bytes regrouped as Q4_K's, then the 32 fifth-bit bytes regrouped per
 // fragment thread: bytes 8t + 4u + e hold bits byte 16u + 4t + kQ4kPerm[e].
@@ -422,7 +452,10 @@ inline unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + thread
 mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t s) {
   const int T = 128;
   const int64_t N = w->N, K = w->K;
-  if (w->type == MQ_Q8_0) {
+  if (float_type(w->type)) {
+    repack_float<<<grid_for(N * (K / 16), T), T, 0, s>>>(raw, N, K, w->q);
+    MQ_LAUNCH_CHECK("repack_float");
+  } else if (w->type == MQ_Q8_0) {
     const int64_t n = N * (K / 32);
     repack_q8_0<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, w->d, mmq ? w->mw : nullptr,
                                               w->td);
@@ -479,7 +512,10 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
 mq_status unpack_weight(const mq_weight *w, uint8_t *raw, cudaStream_t s) {
   const int T = 128;
   const int64_t N = w->N, K = w->K;
-  if (w->type == MQ_Q8_0) {
+  if (float_type(w->type)) {
+    unpack_float<<<grid_for(N * (K / 16), T), T, 0, s>>>(w->q, N, K, raw);
+    MQ_LAUNCH_CHECK("unpack_float");
+  } else if (w->type == MQ_Q8_0) {
     unpack_q8_0<<<grid_for(N * (K / 32), T), T, 0, s>>>(w->q, w->d, N, K, raw);
     MQ_LAUNCH_CHECK("unpack_q8_0");
   } else if (block_elems(w->type) == 32) {

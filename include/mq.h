@@ -63,12 +63,17 @@ extern "C" {
  *   MQ_Q6_K: 256-element super-blocks of 210 bytes: 128 bytes low 4 bits,
  *            64 bytes high 2 bits, 16 int8 sub-scales, f16 d;
  *            w = d*sc*(q - 32).
+ *   MQ_F16, MQ_BF16: unquantised weights, one little-endian IEEE binary16 (or bfloat16,
+ *            the upper half of a binary32) per element, rows of K elements; K must be a
+ *            multiple of 32.  Decode matvec only ("CUDA Backend Design" §4.4: the f16 and
+ *            bf16 kernels); they have no integer form, so mq_mmq, mq_mmq_blockdots and
+ *            mq_ffn_gu_mmq return MQ_ERR_TYPE, and registration builds no prefill planes.
  * Byte ratios as in "CUDA Backend Design" §2.3 (34/32, 144/256, 210/256); Q4_0, Q4_1,
  * Q5_0, Q5_1 and Q5_K are among the types its matmul whitelist and weight gate admit
  * (§4.3, §4.6). */
 typedef enum {
-    MQ_Q4_0 = 2, MQ_Q4_1 = 3, MQ_Q5_0 = 6, MQ_Q5_1 = 7, MQ_Q8_0 = 8,
-    MQ_Q4_K = 12, MQ_Q5_K = 13, MQ_Q6_K = 14
+    MQ_F16 = 1, MQ_Q4_0 = 2, MQ_Q4_1 = 3, MQ_Q5_0 = 6, MQ_Q5_1 = 7, MQ_Q8_0 = 8,
+    MQ_Q4_K = 12, MQ_Q5_K = 13, MQ_Q6_K = 14, MQ_BF16 = 30
 } mq_type;
 
 typedef enum {

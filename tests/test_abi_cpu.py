@@ -102,6 +102,14 @@ def test_register_payload_is_an_equality(L, qtype, K, wrong):
     assert str(expect) in msg
 
 
+@pytest.mark.parametrize("qtype", [mq.F16, mq.BF16])
+def test_float_weights_validate_shape_and_payload(L, qtype):
+    st, msg = _reg(L, qtype, np.zeros(2 * 48, np.uint8), 1, 48)
+    assert mq.STATUS[st] == "MQ_ERR_SHAPE" and "multiple of the type" in msg
+    st, msg = _reg(L, qtype, np.zeros(2 * 64 * 3 - 1, np.uint8), 3, 64)
+    assert mq.STATUS[st] == "MQ_ERR_PAYLOAD" and str(2 * 64 * 3) in msg
+
+
 def test_q4_0_payload_with_q4_k_ratio_is_refused(L):
     # 2 rows x 512: q4_K expects 2*2*144 = 576 bytes; a q4_0 tensor of 1 row x 1024 has
     # 32 blocks of 18 = 576 bytes, but N=2, K=512 as q4_K would accept 576 -- so the

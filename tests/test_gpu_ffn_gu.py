@@ -40,7 +40,8 @@ def pair(qtype, N, K, s):
 @pytest.mark.parametrize("qtype,N,K", [
     (synth.Q8_0, 8, 96), (synth.Q8_0, 136, 288), (synth.Q4_K, 8, 256), (synth.Q4_K, 72, 512),
     (synth.Q4_K, 200, 768), (synth.Q6_K, 24, 256), (synth.Q6_K, 136, 512),
-    (synth.Q4_1, 72, 288), (synth.Q5_0, 136, 96), (synth.Q5_1, 8, 512)])
+    (synth.Q4_1, 72, 288), (synth.Q5_0, 136, 96), (synth.Q5_1, 8, 512),
+    (synth.F16, 72, 288), (synth.BF16, 136, 512)])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_ffn_gu_matvec_small_shapes(qtype, N, K, B):
     g, u = pair(qtype, N, K, 500 + N)

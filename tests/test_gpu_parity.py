@@ -66,7 +66,8 @@ def gpu_matvec(W, x):
                                        (2, 37, 96), (2, 4864, 896), (13, 19, 512),
                                        (13, 18944, 3584), (3, 37, 96), (3, 4864, 896),
                                        (6, 37, 96), (6, 18944, 3584), (7, 37, 96),
-                                       (7, 3584, 18944)])
+                                       (7, 3584, 18944), (1, 37, 96), (1, 130, 800),
+                                       (30, 37, 96), (30, 4864, 896)])
 def test_decode_plane_roundtrip_is_byte_exact(qtype, N, K):
     W = registered(qtype, N, K, 7)
     assert np.array_equal(W.unpack(), weights(qtype, N, K, 7))
@@ -83,7 +84,9 @@ SMALL = [(8, 1, 32), (8, 37, 96), (8, 130, 288), (8, 64, 896),
          (13, 1, 256), (13, 19, 512), (13, 100, 768), (13, 257, 2560),
          (3, 1, 32), (3, 37, 96), (3, 130, 288), (3, 300, 4864),
          (6, 1, 32), (6, 37, 96), (6, 130, 288), (6, 300, 4864),
-         (7, 1, 32), (7, 37, 96), (7, 130, 288), (7, 300, 4864)]
+         (7, 1, 32), (7, 37, 96), (7, 130, 288), (7, 300, 4864),
+         (1, 1, 32), (1, 37, 96), (1, 130, 288), (1, 300, 4864),
+         (30, 1, 32), (30, 37, 96), (30, 130, 288), (30, 300, 4864)]
 
 
 @pytest.mark.parametrize("qtype,N,K", SMALL)
@@ -129,7 +132,7 @@ def test_matvec_batch_columns_equal_single_calls_bitwise():
 
 @pytest.mark.parametrize("qtype,N,K", [(8, 70, 288), (12, 70, 768), (14, 70, 768),
                                        (2, 70, 288), (13, 70, 768), (3, 70, 288), (6, 70, 288),
-                                       (7, 70, 288)])
+                                       (7, 70, 288), (1, 70, 288), (30, 70, 288)])
 def test_matvec_extreme_magnitudes(qtype, N, K):
     W = registered(qtype, N, K, 13)
     rng = np.random.default_rng(5)
@@ -361,7 +364,9 @@ def test_errors_are_reported_not_fallen_back():
                                          (13, 18944, 3584, 1), (13, 3584, 18944, 8),
                                          (3, 18944, 3584, 1), (3, 4864, 896, 8),
                                          (6, 18944, 3584, 2), (6, 3584, 18944, 1),
-                                         (7, 18944, 3584, 1), (7, 3584, 18944, 5)])
+                                         (7, 18944, 3584, 1), (7, 3584, 18944, 5),
+                                         (1, 4864, 896, 1), (1, 3584, 18944, 8),
+                                         (30, 18944, 3584, 1), (30, 896, 4864, 3)])
 def test_matvec_new_types_ffn_shapes(qtype, N, K, B):
     W = registered(qtype, N, K, 41, mq.REG_NO_MMQ_PLANE)
     x = synth.activations(B, K, seed=42)
@@ -382,3 +387,18 @@ def test_mmq_new_types_prefill_shape_sampled(qtype):
     rows = np.array([0, 127, 128, 300, 511])
     yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 43), N, K, qs, sc, mrows=rows)
     assert_bound(y.cpu().numpy()[rows], yref, bnd, f"mmq type {qtype} 512x18944x3584")
+
+
+@pytest.mark.parametrize("qtype", [1, 30])
+def test_float_weights_have_no_mmq_form(qtype):
+    N, K = 40, 96
+    W = mq.register_weight(qtype, weights(qtype, N, K, 3), N, K)
+    xq = mq.quantize_act(torch.zeros((4, K), device="cuda"))
+    with pytest.raises(mq.MQError) as e:
+        mq.mmq(W, xq, 4)
+    assert e.value.name == "MQ_ERR_TYPE"
+    with pytest.raises(mq.MQError) as e:
+        mq.mmq_blockdots(W, xq, 4)
+    assert e.value.name == "MQ_ERR_TYPE"
+    W.free()
+    mq.stream_status()
