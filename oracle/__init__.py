@@ -35,29 +35,34 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 
 
+def load(path: str):
+    """A ctypes handle on a compiled oracle library, its signatures declared."""
+    L = ctypes.CDLL(path)
+    L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_f16_to_double.restype = ctypes.c_double
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_q4_k_scale_min.argtypes = [_P, ctypes.c_int, _P, _P]
+    L.oracle_q4_k_scale_min.restype = None
+    L.oracle_dequant_row.argtypes = [ctypes.c_int, _P, _I64, _P]
+    L.oracle_int_weights_row.argtypes = [ctypes.c_int, _P, _I64, _P]
+    L.oracle_matvec.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, ctypes.c_int, _I64, _I64,
+                                _P, _P]
+    L.oracle_quantize_act.argtypes = [_P, _I64, _I64, _P, _P, _P]
+    L.oracle_blockdots.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _I64, _P, _I64, _I64,
+                                   _I64, _P]
+    L.oracle_mmq.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _P, _I64, _P, _I64, _I64,
+                             _I64, _P, _P]
+    for f in ("oracle_dequant_row", "oracle_int_weights_row", "oracle_matvec",
+              "oracle_quantize_act", "oracle_blockdots", "oracle_mmq"):
+        getattr(L, f).restype = ctypes.c_int
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
-        L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
-        L.oracle_f16_to_double.restype = ctypes.c_double
-        L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-        L.oracle_bf16_to_double.restype = ctypes.c_double
-        L.oracle_q4_k_scale_min.argtypes = [_P, ctypes.c_int, _P, _P]
-        L.oracle_q4_k_scale_min.restype = None
-        L.oracle_dequant_row.argtypes = [ctypes.c_int, _P, _I64, _P]
-        L.oracle_int_weights_row.argtypes = [ctypes.c_int, _P, _I64, _P]
-        L.oracle_matvec.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, ctypes.c_int, _I64, _I64,
-                                    _P, _P]
-        L.oracle_quantize_act.argtypes = [_P, _I64, _I64, _P, _P, _P]
-        L.oracle_blockdots.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _I64, _P, _I64, _I64,
-                                       _I64, _P]
-        L.oracle_mmq.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _P, _I64, _P, _I64, _I64,
-                                 _I64, _P, _P]
-        for f in ("oracle_dequant_row", "oracle_int_weights_row", "oracle_matvec",
-                  "oracle_quantize_act", "oracle_blockdots", "oracle_mmq"):
-            getattr(L, f).restype = ctypes.c_int
-        _lib = L
+        _lib = load(build())
     return _lib
 
 

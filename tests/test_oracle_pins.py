@@ -58,7 +58,8 @@ def test_f16_golden_values():
 def test_bf16_all_bit_patterns_match_binary32():
     """bfloat16 is the upper half of a binary32: numpy's f32 decoding of bits << 16."""
     bits = np.arange(65536, dtype=np.uint32)
-    ref = (bits << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).view(np.float32).astype(np.float64)
     got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(got), nan)
@@ -311,6 +312,18 @@ def test_dequant_matches_vectorised_numpy_decoder(qtype):
     N, K = 7, 512
     W = synth.weights(qtype, N, K, seed=11)
     assert np.array_equal(oracle.dequant(qtype, W, N, K), gp.np_dequant(qtype, W, N, K))
+
+
+@pytest.mark.parametrize("qtype", [1, 30, 2, 3, 6, 7, 8, 12, 13, 14])
+def test_matvec_bound_is_sum_of_absolute_products(qtype):
+    """The per-row bound is sum_k |w||x| with w from the independent numpy decoder."""
+    N, K, B = 3, 512, 2
+    W = synth.weights(qtype, N, K, seed=31)
+    x = synth.activations(B, K, seed=32)
+    _, bnd = oracle.matvec(qtype, W, N, K, x)
+    w = gp.np_dequant(qtype, W, N, K)
+    ref = np.abs(x.astype(np.float64)) @ np.abs(w).T
+    assert np.allclose(bnd, ref, rtol=1e-12, atol=0.0)
 
 
 @pytest.mark.parametrize("qtype", [1, 30, 2, 3, 6, 7, 8, 12, 13, 14])
