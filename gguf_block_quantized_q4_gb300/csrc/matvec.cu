@@ -1026,7 +1026,7 @@ template <int TYPE, int NT>
 mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   const int64_t groups = (a.N + kRows - 1) / kRows;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(groups * a.S), 1, 1);
+  cfg.gridDim = dim3(test_fail_launch() ? 0u : (unsigned)(groups * a.S), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = mv_smem_bytes<TYPE, NT>();
   cfg.stream = s;
@@ -1040,9 +1040,11 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   cfg.attrs = attr;
   cfg.numAttrs = a.S > 1 ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, NT>, a);
-  if (e != cudaSuccess)
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
     return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u, cluster %d) failed: %s", name,
                 cfg.gridDim.x, a.S, cudaGetErrorName(e));
+  }
   return MQ_OK;
 }
 

@@ -605,7 +605,7 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
                    const CUtensorMap &tSx, const TcArgs &a, cudaStream_t s, int sms,
                    const char *name) {
   // persistent: one CTA per SM (shared memory allows no more), tiles strided over them
-  dim3 grid((unsigned)(a.ntiles < sms ? a.ntiles : sms));
+  dim3 grid(test_fail_launch() ? 0u : (unsigned)(a.ntiles < sms ? a.ntiles : sms));
   const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
   const CUtensorMap &tW2 = *reinterpret_cast<const CUtensorMap *>(
       TYPE == MQ_Q6_K ? W->tmap_w2 : W->tmap_w);

@@ -457,6 +457,11 @@ extern "C" mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_
   return launch_quantize(x, xq, M, K, (cudaStream_t)stream);
 }
 
+int mq::test_fail_launch() {
+  const char *v = getenv("MQ_TEST_FAIL_LAUNCH");
+  return (v && v[0] == '1') ? 1 : 0;
+}
+
 // Failure-injection seam for the bounded-wait test: with MQ_TEST_EXPIRE_WAIT=1 the
 // MMQ epilogue first waits on a barrier nothing arrives on; the wait expires
 // after about a millisecond, records MQ_ERR_TIMEOUT in the status word and the

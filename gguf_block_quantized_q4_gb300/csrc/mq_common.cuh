@@ -116,6 +116,10 @@ mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaSt
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
                      cudaStream_t s, const DeviceState *st, int debug_expire);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
+// Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 the matvec
+// and MMQ launches are configured with an empty grid, which the runtime refuses before any
+// kernel runs.  Read at every launch.
+int test_fail_launch();
 mq_status init_kernels(DeviceState *st);  // smem opt-ins of the MMQ kernels
 mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 

@@ -170,7 +170,8 @@ def assert_quant_exact(x):
     assert np.array_equal(op.astype(np.float32), rq.astype(np.float32))
     st, tt = (v.cpu().numpy() for v in mq.act_views_transposed(xq, *x.shape))
     assert np.array_equal(st.T.view(np.uint32), rs.view(np.uint32))
-    assert np.array_equal(tt.T, rs * rb.astype(np.float32))
+    with np.errstate(over="ignore"):
+        assert np.array_equal(tt.T, rs * rb.astype(np.float32))
     assert_min_operand(xq, rs, rb)
 
 
@@ -402,3 +403,47 @@ def test_float_weights_have_no_mmq_form(qtype):
     assert e.value.name == "MQ_ERR_TYPE"
     W.free()
     mq.stream_status()
+
+
+def test_refused_launches_are_reported_and_leave_no_error(monkeypatch):
+    """With the failure-injection seam the matvec and MMQ launches get an empty grid, which
+    the runtime refuses before any kernel runs: the call returns MQ_ERR_LAUNCH naming the
+    kernel, and the next calls run normally and stay within the oracle's bound."""
+    qtype, N, K, M = 12, 200, 768, 9
+    W = registered(qtype, N, K, 17)
+    x = synth.activations(2, K, seed=3)
+    xa = synth.activations(M, K, seed=4)
+    xq, qs, sc, _, _ = gpu_quantize(xa)
+    monkeypatch.setenv("MQ_TEST_FAIL_LAUNCH", "1")
+    with pytest.raises(mq.MQError) as e:
+        mq.matvec(W, torch.from_numpy(x).cuda())
+    assert e.value.name == "MQ_ERR_LAUNCH" and "matvec_kernel<Q4_K" in str(e.value)
+    with pytest.raises(mq.MQError) as e:
+        mq.mmq(W, xq, M)
+    assert e.value.name == "MQ_ERR_LAUNCH" and "mmq_tc_kernel<Q4_K>" in str(e.value)
+    monkeypatch.delenv("MQ_TEST_FAIL_LAUNCH")
+    y = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 17), N, K, x)
+    assert_bound(y, yref, bnd, "matvec after a refused launch")
+    ym = mq.mmq(W, xq, M)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    yref, bnd = oracle.mmq(qtype, weights(qtype, N, K, 17), N, K, qs, sc)
+    assert_bound(ym.cpu().numpy(), yref, bnd, "mmq after a refused launch")
+
+
+@pytest.mark.parametrize("qtype,N,K", [(1, 700, 2080), (30, 700, 2080), (2, 700, 2080),
+                                       (3, 700, 2080), (6, 700, 2080), (7, 700, 2080),
+                                       (8, 700, 2080), (12, 700, 2048), (13, 700, 2048),
+                                       (14, 700, 2048)])
+def test_batch_columns_equal_single_calls_bitwise_every_type(qtype, N, K):
+    """Every column of a B = 8 (two-tile kernel) and a B = 3 call equals the B = 1 call bit for
+    bit: the K split and the accumulation order depend on (N, K) only."""
+    W = registered(qtype, N, K, 51, mq.REG_NO_MMQ_PLANE)
+    x = synth.activations(8, K, seed=52)
+    y8 = gpu_matvec(W, x)
+    y3 = gpu_matvec(W, x[3:6])
+    for b in range(8):
+        y1 = gpu_matvec(W, x[b:b + 1])
+        assert np.array_equal(y1[0].view(np.uint32), y8[b].view(np.uint32)), (qtype, b)
+    assert np.array_equal(y3.view(np.uint32), y8[3:6].view(np.uint32))
