@@ -52,6 +52,23 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(values, ws, device):
+    """Each rank's timings replaced by their maximum over the ranks (the slowest rank sets
+    the job's time); any process-group backend, tensors on `device`."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job(per_rank_rate, ws):
+    """Replicas (weak scaling): every rank processes the same units in the common (maximum)
+    time, so the whole job's rate is the per-rank rate times the number of ranks."""
+    return per_rank_rate * ws
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -454,10 +471,7 @@ def main():
     t_q = graph_time_ms(lambda j: mq.quantize_act(xa[j % ROT], xq[j % ROT]), 4 * ROT)
     t_mm = graph_time_ms(lambda j: mq.mmq(Wp[j % ROT], xq[j % ROT], M, ym[j % ROT]), 2 * ROT)
     mq.stream_status()
-    times = torch.tensor([total_ms, t_mv, t_q, t_mm], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    total_ms, t_mv, t_q, t_mm = times.tolist()
+    total_ms, t_mv, t_q, t_mm = max_over_ranks([total_ms, t_mv, t_q, t_mm], ws, dev)
 
     # end to end through the public API, eager: pinned host inputs in, results back out
     stream = torch.cuda.current_stream()
@@ -488,10 +502,7 @@ def main():
     torch.cuda.synchronize()
     te_mv = statistics.median(e[0].elapsed_time(e[1]) for e in eev)
     te_mm = statistics.median(e[1].elapsed_time(e[2]) for e in eev)
-    te = torch.tensor([te_mv, te_mm], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    te_mv, te_mm = te.tolist()
+    te_mv, te_mm = max_over_ranks([te_mv, te_mm], ws, dev)
     assert np.isfinite(yd_p.numpy()).all() and np.isfinite(ym_p.numpy()).all()
 
     hbm, bf16, peak_src = peaks()
@@ -521,7 +532,7 @@ def main():
     e2e_mv = MV_BYTES / (te_mv * 1e-3) / 1e9
     e2e_mm = MMQ_OPS / (te_mm * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": mv_gbs * ws, "unit": "GB/s", "n_gpus": ws,
+        "metric": METRIC, "value": whole_job(mv_gbs, ws), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
         "data": "synthetic (seeded, Qwen2.5-7B FFN-shaped Q4_K weights, N(0,1) activations)",
@@ -531,15 +542,15 @@ def main():
                    "timing": ("steps: one CUDA graph of K steps; per-kernel: graph replays of "
                               "back-to-back calls on rotating buffers, median of 5"),
                    "parallelism": f"replicas x{ws}"},
-        "matvec_gbs": mv_gbs * ws, "matvec_frac_of_hbm": mv_gbs / hbm,
+        "matvec_gbs": whole_job(mv_gbs, ws), "matvec_frac_of_hbm": mv_gbs / hbm,
         "matvec_frac_of_8tbs": mv_gbs / 8000.0,
-        "mmq_tops": mm_tops * ws, "mmq_frac_of_f16_peak": mm_tops / bf16,
-        "quantize_gbs": q_gbs * ws,
+        "mmq_tops": whole_job(mm_tops, ws), "mmq_frac_of_f16_peak": mm_tops / bf16,
+        "quantize_gbs": whole_job(q_gbs, ws),
         "roofline": roof, "kernels": kern,
-        "e2e": {"value": e2e_mv * ws, "unit": "GB/s",
+        "e2e": {"value": whole_job(e2e_mv, ws), "unit": "GB/s",
                 "h2d_bytes_per_step": B * K * 4 + M * K * 4,
                 "d2h_bytes_per_step": B * N * 4 + M * N * 4,
-                "mmq_tops": e2e_mm * ws,
+                "mmq_tops": whole_job(e2e_mm, ws),
                 "note": "eager calls through the public API; matvec: pinned H2D of x + matvec + "
                         "D2H of y; prefill: H2D of x + quantise + MMQ + D2H of y; medians"},
         "gpu_launches": 3 * args.steps,
