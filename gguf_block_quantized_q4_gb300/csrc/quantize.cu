@@ -34,47 +34,59 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
   const int64_t nb = K / 32;
   const int tb = threadIdx.x >> 3, sub = threadIdx.x & 7;
   float rowmax = 0.f;
-  for (int64_t b0 = 0; b0 < nb; b0 += 32) {
-    const int64_t b = b0 + tb;
-    const bool ok = b < nb;
-    const int64_t blk = m * nb + b;  // global block index
-    // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok) v = __ldg(reinterpret_cast<const float4 *>(x + blk * 32) + sub);
-    float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    const float s = __fdiv_rn(mx, 127.0f);
-    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-    if (s != 0.0f) {
-      q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
-      q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
-      q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
-      q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
+  // passes of 32 blocks, kPre of them loaded before any is processed (one load latency
+  // per kPre passes)
+  constexpr int kPre = 4;
+  for (int64_t p0 = 0; p0 < nb; p0 += 32 * kPre) {
+    float4 vp[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+      const int64_t b = p0 + 32 * k + tb;
+      vp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < nb) vp[k] = __ldg(reinterpret_cast<const float4 *>(x + (m * nb + b) * 32) + sub);
     }
-    int S = q0 + q1 + q2 + q3;
-    S += __shfl_xor_sync(0xffffffffu, S, 1);
-    S += __shfl_xor_sync(0xffffffffu, S, 2);
-    S += __shfl_xor_sync(0xffffffffu, S, 4);
-    if (!ok) continue;
-    const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                            ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-    reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-    __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-    __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-    uint2 hv;
-    hv.x = *reinterpret_cast<uint32_t *>(&h01);
-    hv.y = *reinterpret_cast<uint32_t *>(&h23);
-    reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
-    if (sub == 0) {
-      const float t = s * (float)S;
-      reinterpret_cast<float *>(xq + L.scale)[blk] = s;
-      reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
-      reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
-      reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
-      if (b < kTtCache) ttc[b] = t;
-      rowmax = fmaxf(rowmax, fabsf(t));
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+      const int64_t b = p0 + 32 * k + tb;
+      const bool ok = b < nb;
+      const int64_t blk = m * nb + b;  // global block index
+      // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
+      const float4 v = vp[k];
+      float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      const float s = __fdiv_rn(mx, 127.0f);
+      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+      if (s != 0.0f) {
+        q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
+        q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
+        q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
+        q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
+      }
+      int S = q0 + q1 + q2 + q3;
+      S += __shfl_xor_sync(0xffffffffu, S, 1);
+      S += __shfl_xor_sync(0xffffffffu, S, 2);
+      S += __shfl_xor_sync(0xffffffffu, S, 4);
+      if (!ok) continue;
+      const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
+                              ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+      reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
+      __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+      __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+      uint2 hv;
+      hv.x = *reinterpret_cast<uint32_t *>(&h01);
+      hv.y = *reinterpret_cast<uint32_t *>(&h23);
+      reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
+      if (sub == 0) {
+        const float t = s * (float)S;
+        reinterpret_cast<float *>(xq + L.scale)[blk] = s;
+        reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
+        reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
+        reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
+        if (b < kTtCache) ttc[b] = t;
+        rowmax = fmaxf(rowmax, fabsf(t));
+      }
     }
   }
   // row maximum of |s*S| -> u_m = 2^k with max / u_m in [2^13, 2^14)
