@@ -47,6 +47,7 @@ ABI = {
     "mq_act_bytes": (_SZ, [_I64, _I64]),
     "mq_quantize_act": (_ST, [_P, _P, _I64, _I64, _P]),
     "mq_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_mmq_fused": (_ST, [ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_blockdots": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_register_ffn_gu": (_ST, [ctypes.c_int, _P, _P, _SZ, _I64, _I64, ctypes.c_uint32,
                                  ctypes.POINTER(_P)]),
@@ -228,7 +229,8 @@ def act_layout(M: int, K: int):
     o["minT"] = al(o["scaleT"] + mt * nb * 4)
     o["amin"] = al(o["minT"] + mt * nb * 4)
     o["urow"] = al(o["amin"] + M * min_ld(nb) * 2)
-    o["total"] = al(o["urow"] + mt * 4)
+    o["sync"] = al(o["urow"] + mt * 4)
+    o["total"] = al(o["sync"] + 8)
     o["mt"] = mt
     return o
 
@@ -283,6 +285,27 @@ def mmq(W: Weight, xq, M: int, y=None, stream=None):
         y = torch.empty((M, W.N), dtype=torch.float32, device=xq.device)
     _check(lib().mq_mmq(W.qtype, W.handle, _ptr(xq), _ptr(y), M, W.N, W.K, _stream(stream)))
     return y
+
+
+def act_buffer(M: int, K: int, device=None):
+    """An xq buffer of mq_act_bytes(M, K) bytes, zero-filled (so the fused call's barrier
+    count starts at zero), ready for mmq_fused as well as quantize_act."""
+    import torch
+    return torch.zeros(act_bytes(M, K), dtype=torch.uint8, device=device or "cuda")
+
+
+def mmq_fused(W: Weight, x, xq=None, y=None, stream=None):
+    """Quantise x (f32 [M][K] on the device) into xq and run the MMQ, in one kernel.
+    Returns (y, xq); xq then holds what quantize_act writes."""
+    import torch
+    M = x.shape[0]
+    if xq is None:
+        xq = act_buffer(M, W.K, x.device)
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.float32, device=x.device)
+    _check(lib().mq_mmq_fused(W.qtype, W.handle, _ptr(x), _ptr(xq), _ptr(y), M, W.N, W.K,
+                              _stream(stream)))
+    return y, xq
 
 
 def mmq_blockdots(W: Weight, xq, M: int, D=None, stream=None):

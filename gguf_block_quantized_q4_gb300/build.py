@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmq.so")
 SOURCES = ["mq_api.cu", "repack.cu", "matvec.cu", "quantize.cu", "mmq.cu"]
-HEADERS = [os.path.join(CSRC, "mq_common.cuh"), os.path.join(ROOT, "include", "mq.h")]
+HEADERS = [os.path.join(CSRC, "mq_common.cuh"), os.path.join(CSRC, "quant_row.cuh"),
+           os.path.join(ROOT, "include", "mq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]

@@ -54,7 +54,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "mq_common.cuh"
+#include "quant_row.cuh"
 
 namespace mq {
 namespace {
@@ -92,6 +92,13 @@ struct TcArgs {
   int *status;
   int debug_expire;
   int swiglu;           // fused gate/up weight: y[m][n'] = silu(gate col) * (its up col), N / 2 wide
+};
+
+// Fused quantisation (x non-null): the CTAs first quantise the rows of x into xq.
+struct QfArgs {
+  const float *x;
+  uint8_t *xq;
+  unsigned *sync;       // the grid barrier's two words inside xq
 };
 
 // Arrays that some block types do not need take (almost) no space; every slot
@@ -167,6 +174,43 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *stat
     }
   }
 }
+// Grid-wide barrier of the fused quantise + MMQ (all CTAs co-resident: cooperative launch),
+// run by one thread per CTA after the CTA's writers have fenced their writes and met at a
+// CTA barrier.  sync[0] counts arrivals, sync[1] is the generation; the last CTA to arrive
+// resets the count and advances the generation, so the count is zero again when the
+// barrier opens.  The wait is bounded (expiry: status site 8, and the kernel carries on).
+__device__ __forceinline__ void grid_wait(unsigned *sync, unsigned G, int *status) {
+  unsigned *cnt = sync, *gen = sync + 1;
+  unsigned g;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(gen) : "memory");
+  __threadfence();
+  if (atomicAdd(cnt, 1u) == G - 1) {
+    atomicExch(cnt, 0u);
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gen), "r"(g + 1u) : "memory");
+  } else {
+    const uint64_t t0 = gtime();
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gen) : "memory");
+      if (v != g) break;
+      if (gtime() - t0 > kWaitNs) {
+        if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, 8);
+        break;
+      }
+    }
+  }
+  __threadfence();
+}
+
+// Fused prologue: the 512 epilogue threads form kQGroups groups of kQThreads, each
+// quantising its own rows (row group * gridDim.x + blockIdx.x, then + gridDim.x * kQGroups,
+// ...: the rows are dealt to the CTAs first); named barriers: 1..kQGroups per group,
+// kBarEpi among the epilogue threads, kBarAll for the whole CTA (the control warps wait
+// there until the grid barrier has opened).
+constexpr int kQThreads = 128, kQGroups = 4;
+constexpr int kBarEpi = 14, kBarAll = 15;
+
 __device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count));
 }
@@ -226,12 +270,12 @@ __device__ __forceinline__ void tc_fence_after() {
         "=r"(r[31])                                                                           \
       : "r"(taddr))
 
-template <int TYPE, bool DOTS>
+template <int TYPE, bool DOTS, bool QF = false>
 __global__ void __launch_bounds__(NTHR, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
                   const __grid_constant__ CUtensorMap tW2, const __grid_constant__ CUtensorMap tAm,
                   const __grid_constant__ CUtensorMap tBm, const __grid_constant__ CUtensorMap tSx,
-                  const __grid_constant__ CUtensorMap tD, const TcArgs p) {
+                  const __grid_constant__ CUtensorMap tD, const TcArgs p, const QfArgs qf) {
   using Sm = TcSmem<TYPE>;
   constexpr int NST = Sm::NST, SR = NST / 2;  // SR ring stages per MMA issuer
   static_assert(NST % 2 == 0, "the ring is split between two issuers");
@@ -253,6 +297,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   // G = tl * ngroups + g for the CTA's tl-th tile).  For the K-quants npairs is a
   // multiple of 4, so nuse is even and pair pr of every tile uses accumulator pr % 2.
   const int nms = (MIN && !DOTS) ? p.nms : 0, nmu = nms > 0 ? 2 : 0, nuse = npairs + nmu;
+
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -282,6 +327,10 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+    if constexpr (QF) {  // wait until every CTA's rows are in xq (epilogue warps, below)
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NTHR) : "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads of xq
+    }
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
       // Fills in the order of the accumulator uses.  Global use U belongs to issuer U % 2,
@@ -365,6 +414,28 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {  // ---- epilogue warps
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
+    if constexpr (QF) {
+      // Fused quantisation, with the activation ring (not in use yet) as scratch, then the
+      // grid barrier: every row of x is in xq before any CTA's producer reads it.
+      static_assert(sizeof(sm.a) >= (kQGroups * kTtCache + NEPI) * sizeof(float),
+                    "prologue scratch fits in the activation ring");
+      static_assert(kQGroups * kQThreads == 32 * NEPI, "the epilogue threads form the groups");
+      const int et = threadIdx.x - 128, grp = et / kQThreads, tid = et % kQThreads;
+      float *scratch = reinterpret_cast<float *>(&sm.a[0][0]);
+      float *ttc = scratch + grp * kTtCache, *wmax = scratch + kQGroups * kTtCache + grp * 4;
+      const int64_t K = int64_t(nb) * 32;
+      const ActLayout L = act_layout(p.M, K);
+      for (int64_t m = int64_t(grp) * gridDim.x + blockIdx.x; m < p.M;
+           m += int64_t(gridDim.x) * kQGroups) {
+        quantize_row<kQThreads, 8>(qf.x, qf.xq, m, K, L, ttc, wmax, tid, 1 + grp);
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kQThreads) : "memory");
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __threadfence();
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarEpi), "n"(32 * NEPI) : "memory");
+      if (et == 0) grid_wait(qf.sync, gridDim.x, p.status);
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NTHR) : "memory");
+    }
     const int e = warp - 4, q = warp & 3, hcol = e >> 2;  // rows 32q.., columns EC*hcol..
     const int rl = 32 * q + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(EC * hcol);
@@ -586,13 +657,13 @@ constexpr size_t smem_bytes() {
   return sizeof(TcSmem<TYPE>) + 1024;
 }
 
-template <int TYPE, bool DOTS>
+template <int TYPE, bool DOTS, bool QF = false>
 mq_status optin_t(const DeviceState *st, const char *name) {
   const size_t smem = smem_bytes<TYPE>();
   if ((int)smem > st->smem_optin)
     return fail(MQ_ERR_LAUNCH, "%s needs %zu bytes of shared memory; the device allows %d", name,
                 smem, st->smem_optin);
-  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<TYPE, DOTS>,
+  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<TYPE, DOTS, QF>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
@@ -602,8 +673,8 @@ mq_status optin_t(const DeviceState *st, const char *name) {
 
 template <int TYPE, bool DOTS>
 mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap &tAm,
-                   const CUtensorMap &tSx, const TcArgs &a, cudaStream_t s, int sms,
-                   const char *name) {
+                   const CUtensorMap &tSx, const TcArgs &a, const QfArgs &qf, cudaStream_t s,
+                   int sms, const char *name) {
   // persistent: one CTA per SM (shared memory allows no more), tiles strided over them
   dim3 grid(test_fail_launch() ? 0u : (unsigned)(a.ntiles < sms ? a.ntiles : sms));
   const CUtensorMap &tW = *reinterpret_cast<const CUtensorMap *>(W->tmap_w);
@@ -612,9 +683,32 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
   const CUtensorMap &tBm = *reinterpret_cast<const CUtensorMap *>(
       TcSmem<TYPE>::MIN && !DOTS ? W->tmap_mb : W->tmap_w);
   const CUtensorMap &tD = *reinterpret_cast<const CUtensorMap *>(DOTS ? W->tmap_w : W->tmap_td);
-  mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, tSx, tD,
-                                                                    a);
-  MQ_LAUNCH_CHECK(name);
+  if (DOTS || qf.x == nullptr) {
+    mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, tSx,
+                                                                      tD, a, qf);
+    MQ_LAUNCH_CHECK(name);
+    return MQ_OK;
+  }
+  // fused quantisation: a cooperative launch, so that every CTA of the grid barrier is
+  // resident (the runtime refuses the launch otherwise)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHR, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<TYPE>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, false, true>, tA, tW, tW2, tAm, tBm, tSx, tD, a,
+                         qf);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
+    return fail(MQ_ERR_LAUNCH, "cooperative launch of %s (grid %u) failed: %s", name, grid.x,
+                cudaGetErrorName(e));
+  }
   return MQ_OK;
 }
 
@@ -647,11 +741,15 @@ mq_status init_kernels(DeviceState *st) {
   if ((s = optin_t<MQ_Q8_0, true>(st, "mmq_tc_kernel<Q8_0,dots>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q4_K, true>(st, "mmq_tc_kernel<Q4_K,dots>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q6_K, true>(st, "mmq_tc_kernel<Q6_K,dots>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q8_0, false, true>(st, "mmq_tc_kernel<Q8_0,fused>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_K, false, true>(st, "mmq_tc_kernel<Q4_K,fused>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q6_K, false, true>(st, "mmq_tc_kernel<Q6_K,fused>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_1, false, true>(st, "mmq_tc_kernel<Q4_1,fused>")) != MQ_OK) return s;
   return MQ_OK;
 }
 
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
-                     cudaStream_t s, const DeviceState *st, int debug_expire) {
+                     cudaStream_t s, const DeviceState *st, int debug_expire, const float *x) {
   const ActLayout L = act_layout(M, W->K);
   const uint8_t *base = reinterpret_cast<const uint8_t *>(xq);
   alignas(64) CUtensorMap tA, tAm;
@@ -695,22 +793,26 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   a.status = st->status;
   a.debug_expire = debug_expire;
   a.swiglu = W->ffn_gu;
+  QfArgs qf;
+  qf.x = D == nullptr ? x : nullptr;  // the block-dot export is never fused
+  qf.xq = const_cast<uint8_t *>(base);
+  qf.sync = reinterpret_cast<unsigned *>(const_cast<uint8_t *>(base) + L.sync);
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
     case MQ_Q5_K:
-      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
-                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_K>");
+      return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
+                  : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q4_K>");
     case MQ_Q4_1:
     case MQ_Q5_1:  // block dots need no min term: the Q8_0 block-dot kernel
-      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q4_1, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q4_1>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q4_1, false>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q4_1>");
     case MQ_Q6_K:
-      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
-                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q6_K>");
+      return dots ? launch_t<MQ_Q6_K, true>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q6_K,dots>")
+                  : launch_t<MQ_Q6_K, false>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q6_K>");
     default:
-      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
-                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, tSx, a, s, st->sms, "mmq_tc_kernel<Q8_0>");
+      return dots ? launch_t<MQ_Q8_0, true>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q8_0,dots>")
+                  : launch_t<MQ_Q8_0, false>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q8_0>");
   }
 }
 

@@ -497,6 +497,15 @@ extern "C" mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, fl
   return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait());
 }
 
+extern "C" mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float *x, void *xq,
+                                  float *y, int64_t M, int64_t N, int64_t K, mq_stream stream) {
+  DeviceState *st = nullptr;
+  mq_status s = mmq_common("mq_mmq_fused", type, W, xq, y, M, N, K, &st);
+  if (s != MQ_OK) return s;
+  if ((s = check_dev_ptr("mq_mmq_fused", "x", x, W->device, 16)) != MQ_OK) return s;
+  return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait(), x);
+}
+
 extern "C" mq_status mq_ffn_gu_mmq(mq_type type, const mq_weight *W, const void *xq, float *h,
                                    int64_t M, int64_t N, int64_t K, mq_stream stream) {
   DeviceState *st = nullptr;

@@ -113,8 +113,10 @@ mq_status unpack_weight(const mq_weight *w, uint8_t *raw_dev, cudaStream_t s);
 mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
                         const DeviceState *st);
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
+// x non-null: the fused form (the kernel quantises x into xq first; cooperative launch)
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
-                     cudaStream_t s, const DeviceState *st, int debug_expire);
+                     cudaStream_t s, const DeviceState *st, int debug_expire,
+                     const float *x = nullptr);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
 // Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 the matvec
 // and MMQ launches are configured with an empty grid, which the runtime refuses before any
@@ -128,18 +130,20 @@ mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 // [K/32][Mt] and the min-term factors tT = s*S f32 [K/32][Mt], Mt = M rounded up
 // to 128 (the epilogue's tile rows are one contiguous 512-byte run per block);
 // then the min-term operand f16 [M][min_ld] (row m: t~hi | t~hi | t~lo over the
-// blocks, t~ = s*S/u_m) and the row factors u_m f32 [Mt] (powers of two).
+// blocks, t~ = s*S/u_m) and the row factors u_m f32 [Mt] (powers of two); last, the two
+// u32 words of the grid barrier of the fused quantise + MMQ (arrival count, zero between
+// its calls; generation).
 struct ActLayout {
-  size_t qs, scale, bsum, op, st, tt, amin, urow, total;
+  size_t qs, scale, bsum, op, st, tt, amin, urow, sync, total;
   int64_t mt;
 };
-inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
-inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+__host__ __device__ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 // Row stride (elements) of the min-term operands [rows][3*K/32]: rounded up to 8 so that
 // every row starts on a 16-byte boundary (a TMA stride rule); the columns past 3*K/32 are
 // never read (the tensor maps end at 3*K/32 and fill beyond it with zeros).
 __host__ __device__ inline int64_t min_ld(int64_t nb) { return (3 * nb + 7) / 8 * 8; }
-inline ActLayout act_layout(int64_t M, int64_t K) {
+__host__ __device__ inline ActLayout act_layout(int64_t M, int64_t K) {
   ActLayout L;
   L.mt = round_up(M, 128);
   L.qs = 0;
@@ -150,7 +154,8 @@ inline ActLayout act_layout(int64_t M, int64_t K) {
   L.tt = align256(L.st + size_t(L.mt) * (K / 32) * 4);
   L.amin = align256(L.tt + size_t(L.mt) * (K / 32) * 4);
   L.urow = align256(L.amin + size_t(M) * min_ld(K / 32) * 2);
-  L.total = align256(L.urow + size_t(L.mt) * 4);
+  L.sync = align256(L.urow + size_t(L.mt) * 4);
+  L.total = align256(L.sync + 8);
   return L;
 }
 

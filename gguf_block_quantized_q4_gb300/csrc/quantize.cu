@@ -3,113 +3,22 @@
 // Architecture Execution Plan" C4 S2b design decision 4: amax/127 and round
 // half to even, the same steps on every backend so the bytes agree exactly).
 //
-// Per row m and 32-element block b, in IEEE binary32:
-//   amax = max |x|;  s = amax / 127 (correctly rounded division);
-//   q = round_half_even(x / s) clamped to [-127, 127], or 0 when s == 0;
-//   S = sum q.
-// Writes every section of the xq buffer (mq_act_bytes): q as int8, s as f32,
-// S as int32, q as f16 (the tensor-core operand of mq_mmq), the transposed s and
-// s*S planes the MMQ epilogue stages per 128-row tile, and the min-term operand:
-// per row a power of two u_m with max_b |s*S| / u_m in [2^13, 2^14) and the f16
-// pair (hi, lo) of t~ = s*S / u_m per block (hi + lo carries 22 bits), laid out as
-// [hi | hi | lo] so that the MMQ's tensor cores form the min term
-// sum_b t~ * (dmin*m_j~) from three exact f16 products per block.
-//
-// One CTA per row: 8 threads per block, 4 elements (one float4) per thread, 32
-// blocks per pass; the block's max and sum reduce over the 8 lanes with
-// shuffles, the row maximum of |s*S| over the CTA.
-#include "mq_common.cuh"
+// The per-row arithmetic and the sections written are in quant_row.cuh.  One CTA of 256
+// threads per row: 8 threads per block, 4 elements (one float4) per thread, 32 blocks per
+// pass; the block's max and sum reduce over the 8 lanes with shuffles, the row maximum
+// of |s*S| over the CTA.  The min-term operand lets the MMQ's tensor cores form the min
+// term sum_b t~ * (dmin*m_j~) from three exact f16 products per block.
+#include "quant_row.cuh"
 
 namespace mq {
 namespace {
-
-constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared memory
 
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x,
                                                            uint8_t *__restrict__ xq, int64_t M,
                                                            int64_t K, ActLayout L) {
   __shared__ float ttc[kTtCache];
   __shared__ float wmax[8];
-  const int64_t m = blockIdx.x;
-  const int64_t nb = K / 32;
-  const int tb = threadIdx.x >> 3, sub = threadIdx.x & 7;
-  float rowmax = 0.f;
-  // passes of 32 blocks, kPre of them loaded before any is processed (one load latency
-  // per kPre passes)
-  constexpr int kPre = 4;
-  for (int64_t p0 = 0; p0 < nb; p0 += 32 * kPre) {
-    float4 vp[kPre];
-#pragma unroll
-    for (int k = 0; k < kPre; ++k) {
-      const int64_t b = p0 + 32 * k + tb;
-      vp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b < nb) vp[k] = __ldg(reinterpret_cast<const float4 *>(x + (m * nb + b) * 32) + sub);
-    }
-#pragma unroll
-    for (int k = 0; k < kPre; ++k) {
-      const int64_t b = p0 + 32 * k + tb;
-      const bool ok = b < nb;
-      const int64_t blk = m * nb + b;  // global block index
-      // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
-      const float4 v = vp[k];
-      float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      const float s = __fdiv_rn(mx, 127.0f);
-      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-      if (s != 0.0f) {
-        q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
-        q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
-        q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
-        q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
-      }
-      int S = q0 + q1 + q2 + q3;
-      S += __shfl_xor_sync(0xffffffffu, S, 1);
-      S += __shfl_xor_sync(0xffffffffu, S, 2);
-      S += __shfl_xor_sync(0xffffffffu, S, 4);
-      if (!ok) continue;
-      const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                              ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-      reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-      __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-      __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-      uint2 hv;
-      hv.x = *reinterpret_cast<uint32_t *>(&h01);
-      hv.y = *reinterpret_cast<uint32_t *>(&h23);
-      reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
-      if (sub == 0) {
-        const float t = s * (float)S;
-        reinterpret_cast<float *>(xq + L.scale)[blk] = s;
-        reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
-        reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
-        reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
-        if (b < kTtCache) ttc[b] = t;
-        rowmax = fmaxf(rowmax, fabsf(t));
-      }
-    }
-  }
-  // row maximum of |s*S| -> u_m = 2^k with max / u_m in [2^13, 2^14)
-  rowmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(rowmax)));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = rowmax;
-  __syncthreads();
-  float mxr = wmax[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) mxr = fmaxf(mxr, wmax[w]);
-  const int E = (int)((__float_as_uint(mxr) >> 23) & 255);
-  int k = mxr == 0.f ? 0 : E - 140;
-  k = min(max(k, -100), 100);
-  const float inv_u = __int_as_float((127 - k) << 23);
-  if (threadIdx.x == 0) reinterpret_cast<float *>(xq + L.urow)[m] = __int_as_float((127 + k) << 23);
-  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * min_ld(nb);
-  for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
-    const float t = (b < kTtCache ? ttc[b] : reinterpret_cast<const float *>(xq + L.tt)[b * L.mt + m]) * inv_u;
-    const __half hi = __float2half_rn(t);
-    const __half lo = __float2half_rn(t - __half2float(hi));
-    arow[b] = hi;
-    arow[nb + b] = hi;
-    arow[2 * nb + b] = lo;
-  }
+  quantize_row<256>(x, xq, blockIdx.x, K, L, ttc, wmax, threadIdx.x, -1);
 }
 
 }  // namespace

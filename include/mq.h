@@ -168,6 +168,11 @@ mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, 
  *                              binary32 exponent of max_b |s*S| (so max_b |s*S| / u_m is in
  *                              [2^13, 2^14) for a normal maximum); k = 0 when the row's s*S
  *                              are all 0 (rows >= M unspecified)
+ *   sync    u32   [2]          the grid barrier of mq_mmq_fused: an arrival count, which
+ *                              must be zero before the buffer's first mq_mmq_fused call
+ *                              and which every call leaves zero, and a generation word
+ *                              (any value; each call advances it).  mq_quantize_act and
+ *                              mq_mmq neither read nor write them.
  * Returns 0 if K is not a positive multiple of 32 or M < 1. */
 size_t mq_act_bytes(int64_t M, int64_t K);
 
@@ -189,6 +194,21 @@ mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_t K, mq_str
  * product of W with the dequantised activations. */
 mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int64_t M,
                  int64_t N, int64_t K, mq_stream stream);
+
+/* mq_mmq_fused -- mq_quantize_act followed by mq_mmq in one kernel: every CTA of the
+ * persistent MMQ first quantises a slice of the rows of x into xq, a grid-wide barrier
+ * follows, then the contraction runs as in mq_mmq ("CUDA Backend Design" §3 and §8: the
+ * quantisation fused into the GEMM's prologue, named there as the open step change; §4:
+ * the quantised activations stay valid for the next matmul on the same rows).
+ * x: device f32 [M][K]; xq: device buffer of mq_act_bytes(M, K) bytes (256-byte aligned)
+ * whose sync count is zero before its first fused call (each call leaves it zero; one
+ * call in flight per buffer); on return xq holds exactly what mq_quantize_act writes and y
+ * equals the result of mq_quantize_act + mq_mmq bit for bit.  The launch is cooperative
+ * (all CTAs co-resident, or MQ_ERR_LAUNCH); the barrier wait is bounded (an expiry is
+ * reported by mq_stream_status).  Quantised weights with MMQ planes only (MQ_ERR_TYPE for
+ * F16 / BF16, MQ_ERR_ARG for a fused gate/up weight or one registered without planes). */
+mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float *x, void *xq, float *y,
+                       int64_t M, int64_t N, int64_t K, mq_stream stream);
 
 /* mq_mmq_blockdots -- test export of the contraction's integer part:
  * D[(m*N + n)*(K/32) + b] = sum_{k in block b} W_int[n][k] * q[m][k], int32,

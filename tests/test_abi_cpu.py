@@ -58,8 +58,8 @@ def test_act_bytes_layout(L):
     mt = 128
     # the min-term operand row of 3 blocks x 3 parts is padded to 16 f16 (16-byte rows)
     for M, K in ((3, 96), (20, 96)):
-        expect = al(al(al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2)
-                                 + mt * 3 * 4) + mt * 3 * 4) + M * 16 * 2) + mt * 4)
+        expect = al(al(al(al(al(al(al(al(al(M * K) + M * 3 * 4) + M * 3 * 4) + M * K * 2)
+                                    + mt * 3 * 4) + mt * 3 * 4) + M * 16 * 2) + mt * 4) + 8)
         assert L.mq_act_bytes(M, K) == expect == mq.act_layout(M, K)["total"]
     assert mq.min_ld(3) == 16 and mq.min_ld(112) == 336
     assert L.mq_act_bytes(512, 3584) % 256 == 0
