@@ -48,6 +48,7 @@ ABI = {
     "mq_quantize_act": (_ST, [_P, _P, _I64, _I64, _P]),
     "mq_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_fused": (_ST, [ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_mmq_fused_static": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_blockdots": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_register_ffn_gu": (_ST, [ctypes.c_int, _P, _P, _SZ, _I64, _I64, ctypes.c_uint32,
                                  ctypes.POINTER(_P)]),
@@ -306,6 +307,21 @@ def mmq_fused(W: Weight, x, xq=None, y=None, stream=None):
     _check(lib().mq_mmq_fused(W.qtype, W.handle, _ptr(x), _ptr(xq), _ptr(y), M, W.N, W.K,
                               _stream(stream)))
     return y, xq
+
+
+STATIC_XQ_BYTES = 16 << 20  # the library's scratch for mmq_fused_static (MQ_STATIC_XQ_BYTES)
+
+
+def mmq_fused_static(W: Weight, x, y=None, stream=None):
+    """mmq_fused with the library's static scratch in place of an xq buffer (allocates
+    nothing on the device; one call in flight at a time).  Returns y."""
+    import torch
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.float32, device=x.device)
+    _check(lib().mq_mmq_fused_static(W.qtype, W.handle, _ptr(x), _ptr(y), M, W.N, W.K,
+                                     _stream(stream)))
+    return y
 
 
 def mmq_blockdots(W: Weight, xq, M: int, D=None, stream=None):

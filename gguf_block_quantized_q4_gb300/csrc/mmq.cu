@@ -749,7 +749,8 @@ mq_status init_kernels(DeviceState *st) {
 }
 
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
-                     cudaStream_t s, const DeviceState *st, int debug_expire, const float *x) {
+                     cudaStream_t s, const DeviceState *st, int debug_expire, const float *x,
+                     unsigned *sync) {
   const ActLayout L = act_layout(M, W->K);
   const uint8_t *base = reinterpret_cast<const uint8_t *>(xq);
   alignas(64) CUtensorMap tA, tAm;
@@ -796,7 +797,7 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   QfArgs qf;
   qf.x = D == nullptr ? x : nullptr;  // the block-dot export is never fused
   qf.xq = const_cast<uint8_t *>(base);
-  qf.sync = reinterpret_cast<unsigned *>(const_cast<uint8_t *>(base) + L.sync);
+  qf.sync = sync ? sync : reinterpret_cast<unsigned *>(const_cast<uint8_t *>(base) + L.sync);
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:

@@ -506,6 +506,53 @@ extern "C" mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float 
   return launch_mmq(W, xq, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait(), x);
 }
 
+// Scratch of mq_mmq_fused_static: one file-scope device array per device (zero at module
+// load), its first 256 bytes the grid barrier's words (at a fixed place, so that calls of
+// different shapes find the count at zero), the rest an xq buffer.  Its address is looked
+// up once per device; nothing is allocated.
+static __device__ __align__(256) uint8_t g_static_xq[MQ_STATIC_XQ_BYTES];
+static std::mutex g_static_mu;
+
+static mq_status static_scratch(DeviceState *st, uint8_t **out, const char *site) {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!st->static_xq) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_xq);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)", site);
+    st->static_xq = static_cast<uint8_t *>(p);
+  }
+  *out = st->static_xq;
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_mmq_fused_static(mq_type type, const mq_weight *W, const float *x,
+                                         float *y, int64_t M, int64_t N, int64_t K,
+                                         mq_stream stream) {
+  const char *site = "mq_mmq_fused_static";
+  DeviceState *st = nullptr;
+  mq_status s;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  if (!W) return fail(MQ_ERR_ARG, "%s: W is NULL", site);
+  int dev = -1;
+  CK(cudaGetDevice(&dev), site);
+  if (dev != W->device)
+    return fail(MQ_ERR_ARG, "%s: the weight lives on device %d, the current device is %d", site,
+                W->device, dev);
+  if (M >= 1 && K >= 32 && K % 32 == 0 && M <= (int64_t(1) << 31)) {
+    const size_t need = act_layout(M, K).total, room = MQ_STATIC_XQ_BYTES - 256;
+    if (need > room)
+      return fail(MQ_ERR_SHAPE,
+                  "%s: M=%lld K=%lld needs %zu bytes of scratch; the static scratch holds %zu",
+                  site, (long long)M, (long long)K, need, room);
+  }
+  uint8_t *base = nullptr;
+  if ((s = static_scratch(st, &base, site)) != MQ_OK) return s;
+  if ((s = mmq_common(site, type, W, base + 256, y, M, N, K, &st)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "x", x, W->device, 16)) != MQ_OK) return s;
+  return launch_mmq(W, base + 256, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait(), x,
+                    reinterpret_cast<unsigned *>(base));
+}
+
 extern "C" mq_status mq_ffn_gu_mmq(mq_type type, const mq_weight *W, const void *xq, float *h,
                                    int64_t M, int64_t N, int64_t K, mq_stream stream) {
   DeviceState *st = nullptr;

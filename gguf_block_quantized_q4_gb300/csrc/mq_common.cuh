@@ -103,6 +103,7 @@ struct DeviceState {
   int smem_optin = 0;
   int *status = nullptr;  // device status word for bounded waits (code, kernel id)
   cudaStream_t reg_stream = nullptr;
+  uint8_t *static_xq = nullptr;  // mq_mmq_fused_static's scratch (device symbol address)
 };
 DeviceState *device_state(int dev);  // nullptr if mq_init(dev) was not called
 mq_status current_state(DeviceState **st, const char *site);
@@ -114,9 +115,10 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
                         const DeviceState *st);
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
 // x non-null: the fused form (the kernel quantises x into xq first; cooperative launch)
+// sync non-null: the grid barrier's words there instead of inside xq
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
                      cudaStream_t s, const DeviceState *st, int debug_expire,
-                     const float *x = nullptr);
+                     const float *x = nullptr, unsigned *sync = nullptr);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
 // Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 the matvec
 // and MMQ launches are configured with an empty grid, which the runtime refuses before any

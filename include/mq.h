@@ -210,6 +210,23 @@ mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int
 mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float *x, void *xq, float *y,
                        int64_t M, int64_t N, int64_t K, mq_stream stream);
 
+/* mq_mmq_fused_static -- mq_mmq_fused with its scratch in the library instead of a caller
+ * buffer, so that the call allocates nothing (no counterpart in the pages, which always
+ * hand the quantised activations over in a buffer).  The scratch is one file-scope static
+ * device array of MQ_STATIC_XQ_BYTES per device, created by the driver with the library's
+ * device code (with lazy module loading, when the first call looks it up); its address is
+ * looked up once per device (cudaGetSymbolAddress, checked).  Its first 256 bytes hold the
+ * grid barrier's words, the rest an xq buffer: mq_act_bytes(M, K) must not exceed
+ * MQ_STATIC_XQ_BYTES - 256 (else MQ_ERR_SHAPE, before any device work).  After a call the
+ * scratch holds that call's quantised activations in the mq_act_bytes layout (there is no
+ * accessor; the next call overwrites them).  Calls that overlap in time (on different
+ * streams, or from different host threads) share the scratch and race: their results, and
+ * the barrier, are then undefined (an expired barrier wait is reported by
+ * mq_stream_status).  y and x as for mq_mmq_fused; y equals mq_mmq_fused's bit for bit. */
+#define MQ_STATIC_XQ_BYTES (16u << 20)
+mq_status mq_mmq_fused_static(mq_type type, const mq_weight *W, const float *x, float *y,
+                              int64_t M, int64_t N, int64_t K, mq_stream stream);
+
 /* mq_mmq_blockdots -- test export of the contraction's integer part:
  * D[(m*N + n)*(K/32) + b] = sum_{k in block b} W_int[n][k] * q[m][k], int32,
  * where W_int is the weight's integer value: Q8_0 the int8 quant; Q4_K the
