@@ -470,8 +470,12 @@ def main():
     t_mv = graph_time_ms(lambda j: mq.matvec(Wd[j % rmv], xd[j % ROT], yd[j % rmv]), 5 * rmv)
     t_q = graph_time_ms(lambda j: mq.quantize_act(xa[j % ROT], xq[j % ROT]), 4 * ROT)
     t_mm = graph_time_ms(lambda j: mq.mmq(Wp[j % ROT], xq[j % ROT], M, ym[j % ROT]), 2 * ROT)
+    # the prefill with the quantisation inside the MMQ kernel (one cooperative launch)
+    xqf = [mq.act_buffer(M, K, dev) for _ in range(ROT)]
+    t_fu = graph_time_ms(lambda j: mq.mmq_fused(Wp[j % ROT], xa[j % ROT], xqf[j % ROT],
+                                                ym[j % ROT]), 2 * ROT)
     mq.stream_status()
-    total_ms, t_mv, t_q, t_mm = max_over_ranks([total_ms, t_mv, t_q, t_mm], ws, dev)
+    total_ms, t_mv, t_q, t_mm, t_fu = max_over_ranks([total_ms, t_mv, t_q, t_mm, t_fu], ws, dev)
 
     # end to end through the public API, eager: pinned host inputs in, results back out
     stream = torch.cuda.current_stream()
@@ -547,6 +551,12 @@ def main():
         "mmq_tops": whole_job(mm_tops, ws), "mmq_frac_of_f16_peak": mm_tops / bf16,
         "quantize_gbs": whole_job(q_gbs, ws),
         "roofline": roof, "kernels": kern,
+        "prefill_incl_quantise": {
+            "two_kernels_ms": t_q + t_mm, "fused_ms": t_fu,
+            "two_kernels_tops": whole_job(MMQ_OPS / ((t_q + t_mm) * 1e-3) / 1e12, ws),
+            "fused_tops": whole_job(MMQ_OPS / (t_fu * 1e-3) / 1e12, ws),
+            "note": "quantise + MMQ as two launches, and as mq_mmq_fused (one cooperative "
+                    "launch); graph replays of back-to-back calls"},
         "e2e": {"value": whole_job(e2e_mv, ws), "unit": "GB/s",
                 "h2d_bytes_per_step": B * K * 4 + M * K * 4,
                 "d2h_bytes_per_step": B * N * 4 + M * N * 4,

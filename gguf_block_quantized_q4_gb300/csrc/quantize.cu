@@ -13,7 +13,7 @@
 namespace mq {
 namespace {
 
-__global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x,
+__global__ void __launch_bounds__(256, 4) quantize_act_kernel(const float *__restrict__ x,
                                                            uint8_t *__restrict__ xq, int64_t M,
                                                            int64_t K, ActLayout L) {
   __shared__ float ttc[kTtCache];
