@@ -486,15 +486,11 @@ def main():
 
     def e2e_step(i, ev):
         r = i % ROT
+        # one C-ABI call each: H2D of x from pinned host memory, the kernel(s), D2H of y
         ev[0].record(stream)
-        xd[r].copy_(xd_p, non_blocking=True)
-        mq.matvec(Wd[i % rmv], xd[r], yd[i % rmv], stream)
-        yd_p.copy_(yd[i % rmv], non_blocking=True)
+        mq.matvec_host(Wd[i % rmv], xd_p, yd_p, xd[r], yd[i % rmv], stream)
         ev[1].record(stream)
-        xa[r].copy_(xa_p, non_blocking=True)
-        mq.quantize_act(xa[r], xq[r], stream)
-        mq.mmq(Wp[r], xq[r], M, ym[r], stream)
-        ym_p.copy_(ym[r], non_blocking=True)
+        mq.mmq_host(Wp[r], xa_p, ym_p, xa[r], xq[r], ym[r], stream)
         ev[2].record(stream)
 
     eev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -561,8 +557,9 @@ def main():
                 "h2d_bytes_per_step": B * K * 4 + M * K * 4,
                 "d2h_bytes_per_step": B * N * 4 + M * N * 4,
                 "mmq_tops": whole_job(e2e_mm, ws),
-                "note": "eager calls through the public API; matvec: pinned H2D of x + matvec + "
-                        "D2H of y; prefill: H2D of x + quantise + MMQ + D2H of y; medians"},
+                "note": "eager calls of the C ABI with host buffers (mq_matvec_host: pinned "
+                        "H2D of x + matvec + D2H of y; mq_mmq_host: H2D of x + quantise + MMQ "
+                        "+ D2H of y), device time per step between events, medians"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }

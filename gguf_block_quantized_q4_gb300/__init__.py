@@ -49,6 +49,8 @@ ABI = {
     "mq_mmq": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_fused": (_ST, [ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_fused_static": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mq_matvec_host": (_ST, [ctypes.c_int, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int, _P]),
+    "mq_mmq_host": (_ST, [ctypes.c_int, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_mmq_blockdots": (_ST, [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _P]),
     "mq_register_ffn_gu": (_ST, [ctypes.c_int, _P, _P, _SZ, _I64, _I64, ctypes.c_uint32,
                                  ctypes.POINTER(_P)]),
@@ -307,6 +309,22 @@ def mmq_fused(W: Weight, x, xq=None, y=None, stream=None):
     _check(lib().mq_mmq_fused(W.qtype, W.handle, _ptr(x), _ptr(xq), _ptr(y), M, W.N, W.K,
                               _stream(stream)))
     return y, xq
+
+
+def matvec_host(W: Weight, x_host, y_host, x_dev, y_dev, stream=None):
+    """Decode matvec from host buffers (torch CPU tensors, pinned for asynchronous copies):
+    x_host [B][K] -> x_dev, the matvec into y_dev, y_dev -> y_host [B][N], all enqueued on
+    the stream by one C call.  y_host is complete when the stream is."""
+    B = x_host.shape[0]
+    _check(lib().mq_matvec_host(W.qtype, W.handle, _ptr(x_host), _ptr(y_host), _ptr(x_dev),
+                                _ptr(y_dev), W.N, W.K, B, _stream(stream)))
+
+
+def mmq_host(W: Weight, x_host, y_host, x_dev, xq_dev, y_dev, stream=None):
+    """Prefill (quantise + MMQ) from host buffers, as matvec_host."""
+    M = x_host.shape[0]
+    _check(lib().mq_mmq_host(W.qtype, W.handle, _ptr(x_host), _ptr(y_host), _ptr(x_dev),
+                             _ptr(xq_dev), _ptr(y_dev), M, W.N, W.K, _stream(stream)))
 
 
 STATIC_XQ_BYTES = 16 << 20  # the library's scratch for mmq_fused_static (MQ_STATIC_XQ_BYTES)

@@ -433,6 +433,44 @@ extern "C" mq_status mq_ffn_gu_matvec(mq_type type, const mq_weight *W, const fl
   return matvec_impl("mq_ffn_gu_matvec", 1, type, W, x, h, N, K, B, stream);
 }
 
+// Host buffers of the host-buffer calls: any non-null pointer CUDA does not report as device
+// memory (pinned memory keeps the copies asynchronous; pageable memory works, but its
+// copies then wait for the host).
+static mq_status check_host_ptr(const char *site, const char *name, const void *p) {
+  if (!p) return fail(MQ_ERR_ARG, "%s: %s is NULL", site, name);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MQ_ERR_ARG, "%s: %s=%p: cudaPointerGetAttributes failed (%s)", site, name, p,
+                cudaGetErrorName(e));
+  }
+  if (a.type == cudaMemoryTypeDevice)
+    return fail(MQ_ERR_ARG, "%s: %s=%p is device memory; a host buffer is required", site, name,
+                p);
+  return MQ_OK;
+}
+
+extern "C" mq_status mq_matvec_host(mq_type type, const mq_weight *W, const float *x_host,
+                                    float *y_host, float *x_dev, float *y_dev, int64_t N,
+                                    int64_t K, int B, mq_stream stream) {
+  const char *site = "mq_matvec_host";
+  mq_status s = check_weight(site, type, W, N, K);
+  if (s != MQ_OK) return s;
+  if (B < 1 || B > kMaxB) return fail(MQ_ERR_ARG, "%s: B=%d outside [1, %d]", site, B, kMaxB);
+  DeviceState *st = nullptr;
+  if ((s = current_state(&st, site)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "x_dev", x_dev, W->device, 16)) != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "y_dev", y_dev, W->device, 16)) != MQ_OK) return s;
+  if ((s = check_host_ptr(site, "x_host", x_host)) != MQ_OK) return s;
+  if ((s = check_host_ptr(site, "y_host", y_host)) != MQ_OK) return s;
+  cudaStream_t cs = (cudaStream_t)stream;
+  CK(cudaMemcpyAsync(x_dev, x_host, size_t(B) * K * 4, cudaMemcpyHostToDevice, cs), site);
+  if ((s = launch_matvec(W, x_dev, y_dev, B, cs, st)) != MQ_OK) return s;
+  CK(cudaMemcpyAsync(y_host, y_dev, size_t(B) * N * 4, cudaMemcpyDeviceToHost, cs), site);
+  return MQ_OK;
+}
+
 extern "C" size_t mq_act_bytes(int64_t M, int64_t K) {
   if (M < 1 || K < 32 || K % 32) return 0;
   return act_layout(M, K).total;
@@ -551,6 +589,25 @@ extern "C" mq_status mq_mmq_fused_static(mq_type type, const mq_weight *W, const
   if ((s = check_dev_ptr(site, "x", x, W->device, 16)) != MQ_OK) return s;
   return launch_mmq(W, base + 256, y, nullptr, M, (cudaStream_t)stream, st, test_expire_wait(), x,
                     reinterpret_cast<unsigned *>(base));
+}
+
+extern "C" mq_status mq_mmq_host(mq_type type, const mq_weight *W, const float *x_host,
+                                 float *y_host, float *x_dev, void *xq_dev, float *y_dev,
+                                 int64_t M, int64_t N, int64_t K, mq_stream stream) {
+  const char *site = "mq_mmq_host";
+  DeviceState *st = nullptr;
+  mq_status s = mmq_common(site, type, W, xq_dev, y_dev, M, N, K, &st);
+  if (s != MQ_OK) return s;
+  if ((s = check_dev_ptr(site, "x_dev", x_dev, W->device, 16)) != MQ_OK) return s;
+  if ((s = check_host_ptr(site, "x_host", x_host)) != MQ_OK) return s;
+  if ((s = check_host_ptr(site, "y_host", y_host)) != MQ_OK) return s;
+  cudaStream_t cs = (cudaStream_t)stream;
+  CK(cudaMemcpyAsync(x_dev, x_host, size_t(M) * K * 4, cudaMemcpyHostToDevice, cs), site);
+  if ((s = launch_quantize(x_dev, xq_dev, M, K, cs)) != MQ_OK) return s;
+  if ((s = launch_mmq(W, xq_dev, y_dev, nullptr, M, cs, st, test_expire_wait())) != MQ_OK)
+    return s;
+  CK(cudaMemcpyAsync(y_host, y_dev, size_t(M) * N * 4, cudaMemcpyDeviceToHost, cs), site);
+  return MQ_OK;
 }
 
 extern "C" mq_status mq_ffn_gu_mmq(mq_type type, const mq_weight *W, const void *xq, float *h,

@@ -195,6 +195,23 @@ mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_t K, mq_str
 mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int64_t M,
                  int64_t N, int64_t K, mq_stream stream);
 
+/* mq_matvec_host, mq_mmq_host -- the decode matvec and the prefill (mq_quantize_act +
+ * mq_mmq) from host buffers: each call enqueues on `stream` the copy of x from x_host
+ * (f32 [B][K] / [M][K]) into the caller's device buffer x_dev, the kernel(s), and the copy of
+ * y from the caller's device buffer y_dev into y_host (f32 [B][N] / [M][N]); xq_dev is the
+ * caller's quantised-activation buffer (mq_act_bytes(M, K)).  Nothing is allocated.  Like
+ * every call here they return once the work is enqueued: y_host is complete when `stream`
+ * is.  Pinned host buffers keep the copies asynchronous.  Host pointers that CUDA reports
+ * as device memory are refused (MQ_ERR_ARG); the rest is validated as mq_matvec / mq_mmq,
+ * all before anything is enqueued.  The device reads the activations as f32, as in the
+ * decisions listed on "CUDA Backend Design" (ADR-0013). */
+mq_status mq_matvec_host(mq_type type, const mq_weight *W, const float *x_host, float *y_host,
+                         float *x_dev, float *y_dev, int64_t N, int64_t K, int B,
+                         mq_stream stream);
+mq_status mq_mmq_host(mq_type type, const mq_weight *W, const float *x_host, float *y_host,
+                      float *x_dev, void *xq_dev, float *y_dev, int64_t M, int64_t N, int64_t K,
+                      mq_stream stream);
+
 /* mq_mmq_fused -- mq_quantize_act followed by mq_mmq in one kernel: every CTA of the
  * persistent MMQ first quantises a slice of the rows of x into xq, a grid-wide barrier
  * follows, then the contraction runs as in mq_mmq ("CUDA Backend Design" §3 and §8: the

@@ -447,3 +447,28 @@ def test_batch_columns_equal_single_calls_bitwise_every_type(qtype, N, K):
         y1 = gpu_matvec(W, x[b:b + 1])
         assert np.array_equal(y1[0].view(np.uint32), y8[b].view(np.uint32)), (qtype, b)
     assert np.array_equal(y3.view(np.uint32), y8[3:6].view(np.uint32))
+
+
+def test_host_buffer_calls_equal_the_device_calls():
+    """mq_matvec_host / mq_mmq_host (copies in, kernels, copies out, one call each) give the
+    device-pointer calls' results bit for bit, and refuse a device pointer as a host buffer."""
+    qtype, N, K, B, M = 12, 700, 2048, 3, 70
+    W = registered(qtype, N, K, 17)
+    xh = torch.from_numpy(synth.activations(B, K, seed=81)).pin_memory()
+    ah = torch.from_numpy(synth.activations(M, K, seed=82)).pin_memory()
+    yh = torch.empty((B, N)).pin_memory()
+    mh = torch.empty((M, N)).pin_memory()
+    xd, yd = torch.empty((B, K), device="cuda"), torch.empty((B, N), device="cuda")
+    ad, md = torch.empty((M, K), device="cuda"), torch.empty((M, N), device="cuda")
+    xq = torch.empty(mq.act_bytes(M, K), dtype=torch.uint8, device="cuda")
+    mq.matvec_host(W, xh, yh, xd, yd)
+    mq.mmq_host(W, ah, mh, ad, xq, md)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    yref = mq.matvec(W, xh.cuda()).cpu()
+    mref = mq.mmq(W, mq.quantize_act(ah.cuda()), M).cpu()
+    assert torch.equal(yh.view(torch.int32), yref.view(torch.int32))
+    assert torch.equal(mh.view(torch.int32), mref.view(torch.int32))
+    with pytest.raises(mq.MQError) as e:
+        mq.matvec_host(W, xd, yh, xd, yd)  # x_host is device memory
+    assert e.value.name == "MQ_ERR_ARG" and "host buffer" in str(e.value)
