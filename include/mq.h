@@ -4,8 +4,9 @@
  *
  * The operation is the quantised MatMul of the minfer engine ("minfer CUDA
  * Backend Design", §4.4 Execution dispatch): weights stay in their GGUF block
- * encoding (Q8_0 / Q4_K / Q6_K), activations and outputs are f32 ("CUDA
- * Backend Design" §1.3: activations stay f32).  Two forms:
+ * encoding (Q8_0 / Q4_K / Q6_K, and Q4_0, Q4_1, Q5_0, Q5_1, Q5_K; unquantised F16 and
+ * BF16 for the matvec), activations and outputs are f32 ("CUDA Backend Design" §1.3:
+ * activations stay f32).  Two forms:
  *
  *   decode matvec   y[b][n] = sum_k w[n][k] * x[b][k],  b < B <= 8
  *                   ("CUDA Backend Design" §4.4: nt == 1 and the _multi
@@ -13,7 +14,8 @@
  *   prefill MMQ     activations quantised per 32-element block to int8 with an
  *                   f32 scale (mq_quantize_act), then an exact integer
  *                   contraction per block and a per-block scale epilogue
- *                   (mq_mmq) ("CUDA Backend Design" §4.4: the int8 MMQ path).
+ *                   (mq_mmq) ("CUDA Backend Design" §4.4: the int8 MMQ path);
+ *                   mq_mmq_fused does both in one kernel.
  *
  * Conventions ("CUDA Backend Design" §4.9 GPU safety; "GPU Safety" CUDA
  * rules): every invariant violation returns an error status and never falls
