@@ -384,15 +384,36 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
     const int c = c_begin + i, s = i % NS, fs = i % FS;
     const int cw = chunk_width(p.K, c);
     mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 23);
+    // lane handles float4 items f = lane and lane + 32 of each batch row.  In the two-tile
+    // kernel (B = 5..8) the conversion takes long enough that the chunk's x goes to
+    // registers first and the weight stage is released before it (the copy warp refills
+    // the stage meanwhile); the one-tile kernel releases it after the conversion.
+    constexpr bool early = NT == 2;
+    float4 xv[4 * NT][2];
+    if (early) {
+#pragma unroll
+      for (int b = 0; b < 4 * NT; ++b)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int f = lane + 32 * k;
+          xv[b][k] = b < p.B && 4 * f < cw
+                         ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
+    }
     if (i >= FS) mbar_wait(sa(&sm.fempty[fs]), ((i / FS) - 1) & 1, p.status, 25);
-    // lane handles float4 items f = lane and lane + 32 of each batch row
-    for (int b = 0; b < p.B; ++b) {
+#pragma unroll
+    for (int b = 0; b < 4 * NT; ++b) {
+      if (b >= p.B) break;
       float4 v[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int f = lane + 32 * k;
-        v[k] = 4 * f < cw ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[k] = early ? xv[b][k]
+                     : (4 * f < cw ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f));
       }
       float m = 0.f;
 #pragma unroll
@@ -456,8 +477,10 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
       }
     }
     mbar_arrive(sa(&sm.ffull[fs]));  // each lane, after its own fragment stores
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
+    if (!early) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
+    }
   }
 }
 
