@@ -375,8 +375,10 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
 }
 
 // x warp: staged x chunk -> hi/lo B fragments (+ the Q4_K / Q5_K sub-block sums, the
-// Q4_1 / Q5_1 block sums).
-template <int TYPE, int NT>
+// Q4_1 / Q5_1 block sums).  XE: the chunk's x goes to registers first and the weight stage
+// is released before the conversion (the copy warp refills it meanwhile), which pays from
+// three batch rows on; otherwise the stage is released after the conversion.
+template <int TYPE, int NT, bool XE>
 __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, int c_begin,
                                         int nch, int lane) {
   constexpr int NS = MvSmem<TYPE, NT>::NS, FS = MvSmem<TYPE, NT>::FS;
@@ -384,11 +386,8 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
     const int c = c_begin + i, s = i % NS, fs = i % FS;
     const int cw = chunk_width(p.K, c);
     mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 23);
-    // lane handles float4 items f = lane and lane + 32 of each batch row.  In the two-tile
-    // kernel (B = 5..8) the conversion takes long enough that the chunk's x goes to
-    // registers first and the weight stage is released before it (the copy warp refills
-    // the stage meanwhile); the one-tile kernel releases it after the conversion.
-    constexpr bool early = NT == 2;
+    // lane handles float4 items f = lane and lane + 32 of each batch row
+    constexpr bool early = XE;
     float4 xv[4 * NT][2];
     if (early) {
 #pragma unroll
@@ -924,7 +923,7 @@ __device__ __forceinline__ void store_rows(const MvArgs &p, int b, int64_t rA, f
   if (rA + 8 < p.N) p.y[int64_t(b) * p.N + rA + 8] = vB;
 }
 
-template <int TYPE, int NT>
+template <int TYPE, int NT, bool XE>
 __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = MvSmem<TYPE, NT>;
@@ -973,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   if (warp == kCopyWarp) {
     if (lane == 0) issue_copies<TYPE, NT>(sm, p, group, c_begin, nch);
   } else if (warp == kXWarp) {
-    stage_x<TYPE, NT>(sm, p, c_begin, nch, lane);
+    stage_x<TYPE, NT, XE>(sm, p, c_begin, nch, lane);
   } else {
     // Lane (g, t) feeds column g of each n8 tile, i.e. batch row 4i + g/2.  Lanes
     // of absent batch rows read lane (g mod 2, t)'s fragment instead: the copy
@@ -1045,7 +1044,7 @@ constexpr size_t mv_smem_bytes() {
   return sizeof(MvSmem<TYPE, NT>) + 128;
 }
 
-template <int TYPE, int NT>
+template <int TYPE, int NT, bool XE>
 mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   const int64_t groups = (a.N + kRows - 1) / kRows;
   cudaLaunchConfig_t cfg = {};
@@ -1062,7 +1061,7 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.S > 1 ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, NT>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<TYPE, NT, XE>, a);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
     return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u, cluster %d) failed: %s", name,
@@ -1071,13 +1070,13 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   return MQ_OK;
 }
 
-template <int TYPE, int NT>
+template <int TYPE, int NT, bool XE>
 mq_status optin_mv(const DeviceState *st, const char *name) {
   const size_t smem = mv_smem_bytes<TYPE, NT>();
   if ((int)smem > st->smem_optin)
     return fail(MQ_ERR_LAUNCH, "%s needs %zu bytes of shared memory; the device allows %d", name,
                 smem, st->smem_optin);
-  cudaError_t e = cudaFuncSetAttribute(matvec_kernel<TYPE, NT>,
+  cudaError_t e = cudaFuncSetAttribute(matvec_kernel<TYPE, NT, XE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
@@ -1087,29 +1086,28 @@ mq_status optin_mv(const DeviceState *st, const char *name) {
 
 }  // namespace
 
+// The three kernels of a type: one n8 tile (B <= 2; B = 3, 4 with the early x release) and
+// two tiles (B = 5..8, early x release).
+template <int TYPE>
+mq_status optin_type(const DeviceState *st, const char *name) {
+  mq_status s;
+  if ((s = optin_mv<TYPE, 1, false>(st, name)) != MQ_OK) return s;
+  if ((s = optin_mv<TYPE, 1, true>(st, name)) != MQ_OK) return s;
+  return optin_mv<TYPE, 2, true>(st, name);
+}
+
 mq_status init_matvec(DeviceState *st) {
   mq_status s;
-  if ((s = optin_mv<MQ_Q8_0, 1>(st, "matvec_kernel<Q8_0,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q8_0, 2>(st, "matvec_kernel<Q8_0,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_K, 1>(st, "matvec_kernel<Q4_K,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_K, 2>(st, "matvec_kernel<Q4_K,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q6_K, 1>(st, "matvec_kernel<Q6_K,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q6_K, 2>(st, "matvec_kernel<Q6_K,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_0, 1>(st, "matvec_kernel<Q4_0,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_0, 2>(st, "matvec_kernel<Q4_0,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_K, 1>(st, "matvec_kernel<Q5_K,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_K, 2>(st, "matvec_kernel<Q5_K,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_1, 1>(st, "matvec_kernel<Q4_1,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q4_1, 2>(st, "matvec_kernel<Q4_1,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_0, 1>(st, "matvec_kernel<Q5_0,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_0, 2>(st, "matvec_kernel<Q5_0,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_1, 1>(st, "matvec_kernel<Q5_1,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_Q5_1, 2>(st, "matvec_kernel<Q5_1,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_F16, 1>(st, "matvec_kernel<F16,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_F16, 2>(st, "matvec_kernel<F16,NT=2>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_BF16, 1>(st, "matvec_kernel<BF16,NT=1>")) != MQ_OK) return s;
-  if ((s = optin_mv<MQ_BF16, 2>(st, "matvec_kernel<BF16,NT=2>")) != MQ_OK) return s;
-  return MQ_OK;
+  if ((s = optin_type<MQ_Q8_0>(st, "matvec_kernel<Q8_0>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q4_K>(st, "matvec_kernel<Q4_K>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q6_K>(st, "matvec_kernel<Q6_K>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q4_0>(st, "matvec_kernel<Q4_0>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q5_K>(st, "matvec_kernel<Q5_K>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q4_1>(st, "matvec_kernel<Q4_1>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q5_0>(st, "matvec_kernel<Q5_0>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q5_1>(st, "matvec_kernel<Q5_1>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_F16>(st, "matvec_kernel<F16>")) != MQ_OK) return s;
+  return optin_type<MQ_BF16>(st, "matvec_kernel<BF16>");
 }
 
 // K-split: as many slices as keep every CTA of the grid resident in one wave
@@ -1122,6 +1120,13 @@ static int choose_split(int64_t N, int64_t K, int sms, int cps) {
   int S = (int)(fit < 8 ? fit : 8);
   S = min(S, nchunk);
   return max(S, 1);
+}
+
+template <int TYPE>
+mq_status launch_type(const MvArgs &a, int B, cudaStream_t s, const char *name) {
+  if (B > 4) return launch_one<TYPE, 2, true>(a, s, name);
+  if (B > 2) return launch_one<TYPE, 1, true>(a, s, name);
+  return launch_one<TYPE, 1, false>(a, s, name);
 }
 
 mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
@@ -1141,38 +1146,17 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.S = choose_split(W->N, W->K, st->sms, float_type(W->type) ? 1 : 2);
   a.swiglu = W->ffn_gu;
   a.status = st->status;
-  const bool two = B > 4;
   switch (W->type) {
-    case MQ_Q4_K:
-      return two ? launch_one<MQ_Q4_K, 2>(a, s, "matvec_kernel<Q4_K,NT=2>")
-                 : launch_one<MQ_Q4_K, 1>(a, s, "matvec_kernel<Q4_K,NT=1>");
-    case MQ_Q6_K:
-      return two ? launch_one<MQ_Q6_K, 2>(a, s, "matvec_kernel<Q6_K,NT=2>")
-                 : launch_one<MQ_Q6_K, 1>(a, s, "matvec_kernel<Q6_K,NT=1>");
-    case MQ_Q4_0:
-      return two ? launch_one<MQ_Q4_0, 2>(a, s, "matvec_kernel<Q4_0,NT=2>")
-                 : launch_one<MQ_Q4_0, 1>(a, s, "matvec_kernel<Q4_0,NT=1>");
-    case MQ_Q5_K:
-      return two ? launch_one<MQ_Q5_K, 2>(a, s, "matvec_kernel<Q5_K,NT=2>")
-                 : launch_one<MQ_Q5_K, 1>(a, s, "matvec_kernel<Q5_K,NT=1>");
-    case MQ_Q4_1:
-      return two ? launch_one<MQ_Q4_1, 2>(a, s, "matvec_kernel<Q4_1,NT=2>")
-                 : launch_one<MQ_Q4_1, 1>(a, s, "matvec_kernel<Q4_1,NT=1>");
-    case MQ_Q5_0:
-      return two ? launch_one<MQ_Q5_0, 2>(a, s, "matvec_kernel<Q5_0,NT=2>")
-                 : launch_one<MQ_Q5_0, 1>(a, s, "matvec_kernel<Q5_0,NT=1>");
-    case MQ_Q5_1:
-      return two ? launch_one<MQ_Q5_1, 2>(a, s, "matvec_kernel<Q5_1,NT=2>")
-                 : launch_one<MQ_Q5_1, 1>(a, s, "matvec_kernel<Q5_1,NT=1>");
-    case MQ_F16:
-      return two ? launch_one<MQ_F16, 2>(a, s, "matvec_kernel<F16,NT=2>")
-                 : launch_one<MQ_F16, 1>(a, s, "matvec_kernel<F16,NT=1>");
-    case MQ_BF16:
-      return two ? launch_one<MQ_BF16, 2>(a, s, "matvec_kernel<BF16,NT=2>")
-                 : launch_one<MQ_BF16, 1>(a, s, "matvec_kernel<BF16,NT=1>");
-    default:
-      return two ? launch_one<MQ_Q8_0, 2>(a, s, "matvec_kernel<Q8_0,NT=2>")
-                 : launch_one<MQ_Q8_0, 1>(a, s, "matvec_kernel<Q8_0,NT=1>");
+    case MQ_Q4_K: return launch_type<MQ_Q4_K>(a, B, s, "matvec_kernel<Q4_K>");
+    case MQ_Q6_K: return launch_type<MQ_Q6_K>(a, B, s, "matvec_kernel<Q6_K>");
+    case MQ_Q4_0: return launch_type<MQ_Q4_0>(a, B, s, "matvec_kernel<Q4_0>");
+    case MQ_Q5_K: return launch_type<MQ_Q5_K>(a, B, s, "matvec_kernel<Q5_K>");
+    case MQ_Q4_1: return launch_type<MQ_Q4_1>(a, B, s, "matvec_kernel<Q4_1>");
+    case MQ_Q5_0: return launch_type<MQ_Q5_0>(a, B, s, "matvec_kernel<Q5_0>");
+    case MQ_Q5_1: return launch_type<MQ_Q5_1>(a, B, s, "matvec_kernel<Q5_1>");
+    case MQ_F16: return launch_type<MQ_F16>(a, B, s, "matvec_kernel<F16>");
+    case MQ_BF16: return launch_type<MQ_BF16>(a, B, s, "matvec_kernel<BF16>");
+    default: return launch_type<MQ_Q8_0>(a, B, s, "matvec_kernel<Q8_0>");
   }
 }
 
