@@ -115,3 +115,20 @@ def test_fused_rejects_what_the_mmq_rejects():
     Wf.free()
     Wn.free()
     mq.stream_status()
+
+
+@pytest.mark.parametrize("qtype,N,K,M", [(synth.Q8_0, 1, 32, 1), (synth.Q4_0, 3, 32, 2),
+                                         (synth.Q5_1, 1, 64, 1), (synth.Q4_K, 1, 256, 1),
+                                         (synth.Q6_K, 2, 256, 1)])
+def test_fused_minimal_shapes(qtype, N, K, M):
+    """One output tile that is almost all padding, a single activation row, K one block."""
+    W = mq.register_weight(qtype, synth.weights(qtype, N, K, 69), N, K)
+    x = synth.activations(M, K, seed=70)
+    fused_vs_separate(W, x)
+    xd = torch.from_numpy(x).cuda()
+    ys = mq.mmq_fused_static(W, xd)
+    yf, _ = mq.mmq_fused(W, xd)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    assert torch.equal(ys.view(torch.int32), yf.view(torch.int32))
+    W.free()
