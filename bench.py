@@ -557,9 +557,11 @@ def main():
                 "h2d_bytes_per_step": B * K * 4 + M * K * 4,
                 "d2h_bytes_per_step": B * N * 4 + M * N * 4,
                 "mmq_tops": whole_job(e2e_mm, ws),
-                "note": "eager calls of the C ABI with host buffers (mq_matvec_host: pinned "
-                        "H2D of x + matvec + D2H of y; mq_mmq_host: H2D of x + quantise + MMQ "
-                        "+ D2H of y), device time per step between events, medians"},
+                "note": "eager calls of the C ABI with pinned host buffers (mq_matvec_host: "
+                        "x pulled over the host link by a copy kernel that the matvec overlaps, "
+                        "y stored by the matvec into host memory; mq_mmq_host: the quantiser "
+                        "reads x from host memory, MMQ, D2H copy of y), device time per step "
+                        "between events, medians"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }

@@ -312,16 +312,19 @@ def mmq_fused(W: Weight, x, xq=None, y=None, stream=None):
 
 
 def matvec_host(W: Weight, x_host, y_host, x_dev, y_dev, stream=None):
-    """Decode matvec from host buffers (torch CPU tensors, pinned for asynchronous copies):
-    x_host [B][K] -> x_dev, the matvec into y_dev, y_dev -> y_host [B][N], all enqueued on
-    the stream by one C call.  y_host is complete when the stream is."""
+    """Decode matvec from host buffers (torch CPU tensors x_host [B][K], y_host [B][N]), all
+    enqueued on the stream by one C call.  Pinned, 16-byte aligned host tensors are read and
+    written by the kernels directly (x through x_dev, y straight into y_host); others are
+    copied through x_dev / y_dev.  y_host is complete when the stream is."""
     B = x_host.shape[0]
     _check(lib().mq_matvec_host(W.qtype, W.handle, _ptr(x_host), _ptr(y_host), _ptr(x_dev),
                                 _ptr(y_dev), W.N, W.K, B, _stream(stream)))
 
 
 def mmq_host(W: Weight, x_host, y_host, x_dev, xq_dev, y_dev, stream=None):
-    """Prefill (quantise + MMQ) from host buffers, as matvec_host."""
+    """Prefill (quantise + MMQ) from host buffers, as matvec_host: a pinned, 16-byte aligned
+    x_host is read by the quantiser directly (else copied through x_dev); y goes out through
+    y_dev and a copy."""
     M = x_host.shape[0]
     _check(lib().mq_mmq_host(W.qtype, W.handle, _ptr(x_host), _ptr(y_host), _ptr(x_dev),
                              _ptr(xq_dev), _ptr(y_dev), M, W.N, W.K, _stream(stream)))

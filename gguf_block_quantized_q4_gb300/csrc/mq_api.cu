@@ -465,9 +465,19 @@ extern "C" mq_status mq_matvec_host(mq_type type, const mq_weight *W, const floa
   if ((s = check_host_ptr(site, "x_host", x_host)) != MQ_OK) return s;
   if ((s = check_host_ptr(site, "y_host", y_host)) != MQ_OK) return s;
   cudaStream_t cs = (cudaStream_t)stream;
-  CK(cudaMemcpyAsync(x_dev, x_host, size_t(B) * K * 4, cudaMemcpyHostToDevice, cs), site);
-  if ((s = launch_matvec(W, x_dev, y_dev, B, cs, st)) != MQ_OK) return s;
-  CK(cudaMemcpyAsync(y_host, y_dev, size_t(B) * N * 4, cudaMemcpyDeviceToHost, cs), site);
+  // page-locked host buffers are read and written by the kernels through their device
+  // views; other host memory goes through copies into and out of x_dev / y_dev
+  if (const void *xv = host_device_view(x_host, 16)) {
+    if ((s = launch_copy_in(static_cast<const float *>(xv), x_dev, int64_t(B) * K, cs,
+                            st->sms)) != MQ_OK)
+      return s;
+  } else {
+    CK(cudaMemcpyAsync(x_dev, x_host, size_t(B) * K * 4, cudaMemcpyHostToDevice, cs), site);
+  }
+  float *yv = static_cast<float *>(const_cast<void *>(host_device_view(y_host, 16)));
+  if ((s = launch_matvec(W, x_dev, yv ? yv : y_dev, B, cs, st)) != MQ_OK) return s;
+  if (!yv)
+    CK(cudaMemcpyAsync(y_host, y_dev, size_t(B) * N * 4, cudaMemcpyDeviceToHost, cs), site);
   return MQ_OK;
 }
 
@@ -602,8 +612,14 @@ extern "C" mq_status mq_mmq_host(mq_type type, const mq_weight *W, const float *
   if ((s = check_host_ptr(site, "x_host", x_host)) != MQ_OK) return s;
   if ((s = check_host_ptr(site, "y_host", y_host)) != MQ_OK) return s;
   cudaStream_t cs = (cudaStream_t)stream;
-  CK(cudaMemcpyAsync(x_dev, x_host, size_t(M) * K * 4, cudaMemcpyHostToDevice, cs), site);
-  if ((s = launch_quantize(x_dev, xq_dev, M, K, cs)) != MQ_OK) return s;
+  // a page-locked x_host is read by the quantiser through its device view, other host
+  // memory is copied into x_dev.  y always goes out through y_dev and a copy: the MMQ's
+  // stores (one row's 32-column piece per thread) would cross the host link as 16-byte
+  // writes, about a fifth of the copy engine's rate.
+  const float *xv = static_cast<const float *>(host_device_view(x_host, 16));
+  if (!xv)
+    CK(cudaMemcpyAsync(x_dev, x_host, size_t(M) * K * 4, cudaMemcpyHostToDevice, cs), site);
+  if ((s = launch_quantize(xv ? xv : x_dev, xq_dev, M, K, cs)) != MQ_OK) return s;
   if ((s = launch_mmq(W, xq_dev, y_dev, nullptr, M, cs, st, test_expire_wait())) != MQ_OK)
     return s;
   CK(cudaMemcpyAsync(y_host, y_dev, size_t(M) * N * 4, cudaMemcpyDeviceToHost, cs), site);

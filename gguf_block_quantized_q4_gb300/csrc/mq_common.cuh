@@ -120,6 +120,13 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
                      cudaStream_t s, const DeviceState *st, int debug_expire,
                      const float *x = nullptr, unsigned *sync = nullptr);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
+// Host-buffer transfers (host_io.cu).  host_device_view: the device view of p if p is
+// page-locked host memory that this device can map and both p and its view are aligned to
+// `align` bytes, else nullptr.  launch_copy_in: dst[0..n) = src_view[0..n) by SM loads of
+// the view (n a multiple of 4, both 16-byte aligned); the next launch, if it carries the
+// programmatic-serialisation attribute, overlaps it and waits for it before reading dst.
+const void *host_device_view(const void *p, size_t align);
+mq_status launch_copy_in(const float *src_view, float *dst, int64_t n, cudaStream_t s, int sms);
 // Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 the matvec
 // and MMQ launches are configured with an empty grid, which the runtime refuses before any
 // kernel runs.  Read at every launch.

@@ -198,15 +198,24 @@ mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int
                  int64_t N, int64_t K, mq_stream stream);
 
 /* mq_matvec_host, mq_mmq_host -- the decode matvec and the prefill (mq_quantize_act +
- * mq_mmq) from host buffers: each call enqueues on `stream` the copy of x from x_host
- * (f32 [B][K] / [M][K]) into the caller's device buffer x_dev, the kernel(s), and the copy of
- * y from the caller's device buffer y_dev into y_host (f32 [B][N] / [M][N]); xq_dev is the
- * caller's quantised-activation buffer (mq_act_bytes(M, K)).  Nothing is allocated.  Like
- * every call here they return once the work is enqueued: y_host is complete when `stream`
- * is.  Pinned host buffers keep the copies asynchronous.  Host pointers that CUDA reports
- * as device memory are refused (MQ_ERR_ARG); the rest is validated as mq_matvec / mq_mmq,
- * all before anything is enqueued.  The device reads the activations as f32, as in the
- * decisions listed on "CUDA Backend Design" (ADR-0013). */
+ * mq_mmq) from host buffers x_host (f32 [B][K] / [M][K]) and y_host (f32 [B][N] / [M][N]);
+ * x_dev, y_dev are the caller's device buffers of the same shapes and xq_dev its
+ * quantised-activation buffer (mq_act_bytes(M, K)).  Nothing is allocated.  Like every call
+ * here they return once the work is enqueued on `stream`: y_host is complete when `stream`
+ * is.  Transfers:
+ *   - a host buffer that is page-locked (cudaHostAlloc, cudaHostRegister, a pinned tensor)
+ *     and 16-byte aligned is accessed by the kernels through its device view, over the
+ *     host link: the matvec's x is pulled into x_dev by a small copy kernel that the
+ *     matvec overlaps (its weight stream starts at once; x is read after the grid
+ *     dependency wait), the matvec stores y into y_host (y_dev is not written), and the
+ *     prefill's quantiser reads x_host itself (x_dev is not written);
+ *   - any other host buffer, and the prefill's y always, goes through x_dev / y_dev with
+ *     cudaMemcpyAsync copies (synchronous with the host for pageable memory, as CUDA
+ *     defines them).
+ * The results are identical on both routes.  Host pointers that CUDA reports as device
+ * memory are refused (MQ_ERR_ARG); the rest is validated as mq_matvec / mq_mmq, all before
+ * anything is enqueued.  The device reads the activations as f32, as in the decisions
+ * listed on "CUDA Backend Design" (ADR-0013). */
 mq_status mq_matvec_host(mq_type type, const mq_weight *W, const float *x_host, float *y_host,
                          float *x_dev, float *y_dev, int64_t N, int64_t K, int B,
                          mq_stream stream);

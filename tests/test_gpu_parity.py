@@ -450,25 +450,61 @@ def test_batch_columns_equal_single_calls_bitwise_every_type(qtype, N, K):
 
 
 def test_host_buffer_calls_equal_the_device_calls():
-    """mq_matvec_host / mq_mmq_host (copies in, kernels, copies out, one call each) give the
-    device-pointer calls' results bit for bit, and refuse a device pointer as a host buffer."""
+    """mq_matvec_host / mq_mmq_host give the device-pointer calls' results bit for bit on both
+    transfer routes: page-locked aligned buffers (the kernels read and write them through
+    their device views, so the matvec's y_dev and the prefill's x_dev stay untouched) and
+    pageable or misaligned ones (copies through x_dev / y_dev).  A device pointer is refused as a host
+    buffer."""
     qtype, N, K, B, M = 12, 700, 2048, 3, 70
     W = registered(qtype, N, K, 17)
-    xh = torch.from_numpy(synth.activations(B, K, seed=81)).pin_memory()
-    ah = torch.from_numpy(synth.activations(M, K, seed=82)).pin_memory()
-    yh = torch.empty((B, N)).pin_memory()
-    mh = torch.empty((M, N)).pin_memory()
-    xd, yd = torch.empty((B, K), device="cuda"), torch.empty((B, N), device="cuda")
-    ad, md = torch.empty((M, K), device="cuda"), torch.empty((M, N), device="cuda")
+    x, a = synth.activations(B, K, seed=81), synth.activations(M, K, seed=82)
+    yref = mq.matvec(W, torch.from_numpy(x).cuda()).cpu()
+    mref = mq.mmq(W, mq.quantize_act(torch.from_numpy(a).cuda()), M).cpu()
     xq = torch.empty(mq.act_bytes(M, K), dtype=torch.uint8, device="cuda")
+    nan = float("nan")
+
+    def bits_equal(u, v):
+        return torch.equal(u.contiguous().view(torch.int32), v.contiguous().view(torch.int32))
+
+    # page-locked, aligned: direct access
+    xh, ah = torch.from_numpy(x).pin_memory(), torch.from_numpy(a).pin_memory()
+    yh, mh = torch.full((B, N), nan).pin_memory(), torch.full((M, N), nan).pin_memory()
+    xd, yd = torch.empty((B, K), device="cuda"), torch.full((B, N), nan, device="cuda")
+    ad, md = torch.full((M, K), nan, device="cuda"), torch.full((M, N), nan, device="cuda")
     mq.matvec_host(W, xh, yh, xd, yd)
     mq.mmq_host(W, ah, mh, ad, xq, md)
     torch.cuda.synchronize()
     mq.stream_status()
-    yref = mq.matvec(W, xh.cuda()).cpu()
-    mref = mq.mmq(W, mq.quantize_act(ah.cuda()), M).cpu()
-    assert torch.equal(yh.view(torch.int32), yref.view(torch.int32))
-    assert torch.equal(mh.view(torch.int32), mref.view(torch.int32))
+    assert bits_equal(yh, yref) and bits_equal(mh, mref)
+    assert torch.equal(xd.cpu(), xh)  # the matvec's x is pulled into x_dev
+    assert torch.isnan(yd).all() and torch.isnan(ad).all()  # y and the prefill's x go direct
+    assert bits_equal(md.cpu(), mref)  # the prefill's y goes out through y_dev
+
+    # pageable: copies through the device buffers
+    yp, mp = torch.full((B, N), nan), torch.full((M, N), nan)
+    mq.matvec_host(W, torch.from_numpy(x.copy()), yp, xd, yd)
+    mq.mmq_host(W, torch.from_numpy(a.copy()), mp, ad, xq, md)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    assert bits_equal(yp, yref) and bits_equal(mp, mref)
+    assert bits_equal(yd.cpu(), yref) and bits_equal(md.cpu(), mref)
+
+    # page-locked but 4 bytes off a 16-byte boundary: copies as well
+    xbig, ybig = torch.empty(B * K + 1).pin_memory(), torch.full((B * N + 1,), nan).pin_memory()
+    abig, mbig = torch.empty(M * K + 1).pin_memory(), torch.full((M * N + 1,), nan).pin_memory()
+    xm, ym = xbig[1:].view(B, K), ybig[1:].view(B, N)
+    am, mm = abig[1:].view(M, K), mbig[1:].view(M, N)
+    xm.copy_(torch.from_numpy(x))
+    am.copy_(torch.from_numpy(a))
+    yd.fill_(nan)
+    md.fill_(nan)
+    mq.matvec_host(W, xm, ym, xd, yd)
+    mq.mmq_host(W, am, mm, ad, xq, md)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    assert bits_equal(ym, yref) and bits_equal(mm, mref)
+    assert bits_equal(yd.cpu(), yref) and bits_equal(md.cpu(), mref)
+
     with pytest.raises(mq.MQError) as e:
         mq.matvec_host(W, xd, yh, xd, yd)  # x_host is device memory
     assert e.value.name == "MQ_ERR_ARG" and "host buffer" in str(e.value)
