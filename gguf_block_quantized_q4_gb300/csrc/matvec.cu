@@ -68,9 +68,25 @@ namespace {
 
 constexpr int kRows = kRowGroup;               // rows per CTA
 constexpr int kCompute = kRows / 16;           // compute warps, 16 rows each
-constexpr int kXWarp = kCompute;               // x-fragment warp
-constexpr int kCopyWarp = kCompute + 1;        // bulk-copy warp
-constexpr int kThreads = 32 * (kCompute + 2);
+// x-fragment warps: one in the kernel for B <= 2; in the kernels for more batch rows two
+// (x warp j converts rows [j * 2NT, (j + 1) * 2NT) of the chunk), except for Q6_K, whose
+// single x warp converts all rows step by step over the rows (stage_x_rows); the bulk-copy
+// warp comes last.  Measured at B = 4 / 8 against one row-by-row x warp: Q4_K 18944 x 3584
+// 15.6 -> 13.8 / 22.0 -> 18.4 us, Q5_K 17.4 -> 15.9 / 25.2 -> 21.4 us, Q4_1 B = 8 26.4 ->
+// 23.8 us, Q8_0 B = 8 22.7 -> 21.6 us; Q6_K 3584 x 18944 B = 8 took 23.9 us with two x warps
+// (either form) and 23.3 us with the one row-batched warp.
+template <int TYPE, bool XE>
+__host__ __device__ constexpr int x_warps() {
+  return XE && TYPE != MQ_Q6_K ? 2 : 1;
+}
+template <int TYPE, bool XE>
+__host__ __device__ constexpr int copy_warp() {
+  return kCompute + x_warps<TYPE, XE>();
+}
+template <int TYPE, bool XE>
+__host__ __device__ constexpr int mv_threads() {
+  return 32 * (kCompute + 1 + x_warps<TYPE, XE>());
+}
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct MvArgs {
@@ -381,13 +397,14 @@ __device__ __forceinline__ void issue_copies(MvSmem<TYPE, NT> &sm, const MvArgs 
 // min-term fragments), so the rows' dependency chains (warp reductions, shuffles) overlap
 // instead of running one row after another.  Rows beyond B are computed on zeros and not
 // stored.  Per row the arithmetic is that of stage_x below, so the fragments are the same.
-// Measured per type at B = 8: Q6_K 3584 x 18944 25.1 -> 23.3 us; Q8_0 and Q4_1 2% slower,
-// Q4_0, Q5_0 unchanged, Q4_K and Q5_K 1-9% slower (their min-term sums), so only Q6_K uses
-// it.  The function is written for every type.
-template <int TYPE, int NT>
+// With one x warp, measured per type at B = 8: Q6_K 3584 x 18944 25.1 -> 23.3 us; Q8_0 and
+// Q4_1 2% slower, Q4_0, Q5_0 level, Q4_K and Q5_K 1-9% slower (their min-term sums).  The
+// other types take two row-by-row x warps instead.  The function is written for every type.
+template <int TYPE, int NT, int XI>
 __device__ __forceinline__ void stage_x_rows(MvSmem<TYPE, NT> &sm, const MvArgs &p,
                                              int c_begin, int nch, int lane) {
-  constexpr int NS = MvSmem<TYPE, NT>::NS, FS = MvSmem<TYPE, NT>::FS, R = 4 * NT;
+  constexpr int NS = MvSmem<TYPE, NT>::NS, FS = MvSmem<TYPE, NT>::FS;
+  constexpr int R = 4 * NT / x_warps<TYPE, true>(), R0 = XI * R;  // rows R0 .. R0 + R - 1
   for (int i = 0; i < nch; ++i) {
     const int c = c_begin + i, s = i % NS, fs = i % FS;
     const int cw = chunk_width(p.K, c);
@@ -399,8 +416,9 @@ __device__ __forceinline__ void stage_x_rows(MvSmem<TYPE, NT> &sm, const MvArgs 
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int f = lane + 32 * k;
-        xv[b][k] = b < p.B && 4 * f < cw ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[b][k] = R0 + b < p.B && 4 * f < cw
+                       ? *reinterpret_cast<const float4 *>(&sm.xr[s][R0 + b][4 * f])
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     __syncwarp();
     if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
@@ -418,17 +436,18 @@ __device__ __forceinline__ void stage_x_rows(MvSmem<TYPE, NT> &sm, const MvArgs 
       int e = mb == 0 ? 0 : 141 - max(E, 1);
       e = min(max(e, -100), 126);
       scale[b] = __int_as_float((e + 127) << 23);
-      if (lane == 0 && b < p.B) sm.unscale[fs][b] = __int_as_float((127 - e) << 23);
+      if (lane == 0 && R0 + b < p.B) sm.unscale[fs][R0 + b] = __int_as_float((127 - e) << 23);
     }
 #pragma unroll
-    for (int b = 0; b < R; ++b) {
+    for (int bl = 0; bl < R; ++bl) {
+      const int b = R0 + bl;  // batch row
       const int col = 2 * (b & 3);
       const bool live = b < p.B;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int f = lane + 32 * k, g16 = f >> 2, t = f & 3;
-        const float v0 = xv[b][k].x * scale[b], v1 = xv[b][k].y * scale[b],
-                    v2 = xv[b][k].z * scale[b], v3 = xv[b][k].w * scale[b];
+        const float v0 = xv[bl][k].x * scale[bl], v1 = xv[bl][k].y * scale[bl],
+                    v2 = xv[bl][k].z * scale[bl], v3 = xv[bl][k].w * scale[bl];
         uint32_t hi01, hi23, lo01, lo23;
         if constexpr (TYPE == MQ_BF16) {  // bf16 parts: 16 significant bits of x
           hi01 = pack_bf16x2(v0, v1);
@@ -466,7 +485,7 @@ __device__ __forceinline__ void stage_x_rows(MvSmem<TYPE, NT> &sm, const MvArgs 
       if (lane < 8) {
         const int part = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int b = 0; b < R; ++b) {
+        for (int b = R0; b < R0 + R; ++b) {
           if (b < p.B) {
             const float s0 = sm.xs[b][2 * t], s1 = sm.xs[b][2 * t + 1];
             const uint32_t h = pack_f16x2(s0, s1);
@@ -485,39 +504,41 @@ __device__ __forceinline__ void stage_x_rows(MvSmem<TYPE, NT> &sm, const MvArgs 
 // Q4_1 / Q5_1 block sums).  XE: the chunk's x goes to registers first and the weight stage
 // is released before the conversion (the copy warp refills it meanwhile), which pays from
 // three batch rows on; otherwise the stage is released after the conversion.
-template <int TYPE, int NT, bool XE>
+template <int TYPE, int NT, bool XE, int XI>
 __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, int c_begin,
                                         int nch, int lane) {
   constexpr int NS = MvSmem<TYPE, NT>::NS, FS = MvSmem<TYPE, NT>::FS;
+  constexpr int R = 4 * NT / x_warps<TYPE, XE>(), R0 = XI * R;  // rows R0 .. R0 + R - 1
   for (int i = 0; i < nch; ++i) {
     const int c = c_begin + i, s = i % NS, fs = i % FS;
     const int cw = chunk_width(p.K, c);
     mbar_wait(sa(&sm.wfull[s]), (i / NS) & 1, p.status, 23);
     // lane handles float4 items f = lane and lane + 32 of each batch row
     constexpr bool early = XE;
-    float4 xv[4 * NT][2];
+    float4 xv[R][2];
     if (early) {
 #pragma unroll
-      for (int b = 0; b < 4 * NT; ++b)
+      for (int bl = 0; bl < R; ++bl)
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int f = lane + 32 * k;
-          xv[b][k] = b < p.B && 4 * f < cw
-                         ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          xv[bl][k] = R0 + bl < p.B && 4 * f < cw
+                          ? *reinterpret_cast<const float4 *>(&sm.xr[s][R0 + bl][4 * f])
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       __syncwarp();
       if (lane == 0) mbar_arrive(sa(&sm.wempty[s]));  // done reading the staged x
     }
     if (i >= FS) mbar_wait(sa(&sm.fempty[fs]), ((i / FS) - 1) & 1, p.status, 25);
 #pragma unroll
-    for (int b = 0; b < 4 * NT; ++b) {
+    for (int bl = 0; bl < R; ++bl) {
+      const int b = R0 + bl;  // batch row
       if (b >= p.B) break;
       float4 v[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int f = lane + 32 * k;
-        v[k] = early ? xv[b][k]
+        v[k] = early ? xv[bl][k]
                      : (4 * f < cw ? *reinterpret_cast<const float4 *>(&sm.xr[s][b][4 * f])
                                    : make_float4(0.f, 0.f, 0.f, 0.f));
       }
@@ -566,7 +587,7 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
           ps += __shfl_xor_sync(0xffffffffu, ps, 1);
           ps += __shfl_xor_sync(0xffffffffu, ps, 2);
           ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-          if ((lane & 7) == 0) sm.xs[0][f >> 3] = ps * 0.03125f;
+          if ((lane & 7) == 0) sm.xs[b][f >> 3] = ps * 0.03125f;
         }
       }
       if constexpr (kmin_type<TYPE>()) {
@@ -574,7 +595,7 @@ __device__ __forceinline__ void stage_x(MvSmem<TYPE, NT> &sm, const MvArgs &p, i
         __syncwarp();
         if (lane < 8) {
           const int part = lane >> 2, t = lane & 3;
-          const float s0 = sm.xs[0][2 * t], s1 = sm.xs[0][2 * t + 1];
+          const float s0 = sm.xs[b][2 * t], s1 = sm.xs[b][2 * t + 1];
           const uint32_t h = pack_f16x2(s0, s1);
           const uint32_t word = part == 0 ? h : pack_f16x2(s0 - f16_lo(h), s1 - f16_hi(h));
           sm.frag[fs][16][b >> 2][(col + part) * 4 + t] = make_uint2(word, 0u);
@@ -1031,7 +1052,7 @@ __device__ __forceinline__ void store_rows(const MvArgs &p, int b, int64_t rA, f
 }
 
 template <int TYPE, int NT, bool XE>
-__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
+__global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const MvArgs p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = MvSmem<TYPE, NT>;
   constexpr int NS = Smem::NS;
@@ -1051,19 +1072,20 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
   {
     uint4 *f = reinterpret_cast<uint4 *>(&sm.frag[0][0][0][0]);
     constexpr int n16 = (int)(sizeof(sm.frag) / 16);
-    for (int i = tid; i < n16; i += kThreads) f[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < n16; i += mv_threads<TYPE, XE>()) f[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < Smem::FS * 8) (&sm.unscale[0][0])[tid] = 0.f;
     constexpr int nxb = (int)(sizeof(sm.xb) / 4);
-    for (int i = tid; i < nxb; i += kThreads) (&sm.xb[0][0][0])[i] = 0.f;
+    for (int i = tid; i < nxb; i += mv_threads<TYPE, XE>()) (&sm.xb[0][0][0])[i] = 0.f;
   }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.wfull[s])), "r"(1));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.wempty[s])),
-                   "r"(kCompute + 1));
+                   "r"(kCompute + x_warps<TYPE, XE>()));
     }
     for (int f = 0; f < Smem::FS; ++f) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.ffull[f])), "r"(32));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.ffull[f])),
+                   "r"(32 * x_warps<TYPE, XE>()));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.fempty[f])),
                    "r"(kCompute));
     }
@@ -1076,13 +1098,15 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvArgs p) {
 #pragma unroll
   for (int i = 0; i < NT; ++i) tot[0][i] = tot[1][i] = 0.f;
 
-  if (warp == kCopyWarp) {
+  if (warp == copy_warp<TYPE, XE>()) {
     if (lane == 0) issue_copies<TYPE, NT>(sm, p, group, c_begin, nch);
-  } else if (warp == kXWarp) {
+  } else if (warp == kCompute) {
     if constexpr (XE && TYPE == MQ_Q6_K)
-      stage_x_rows<TYPE, NT>(sm, p, c_begin, nch, lane);
+      stage_x_rows<TYPE, NT, 0>(sm, p, c_begin, nch, lane);
     else
-      stage_x<TYPE, NT, XE>(sm, p, c_begin, nch, lane);
+      stage_x<TYPE, NT, XE, 0>(sm, p, c_begin, nch, lane);
+  } else if (x_warps<TYPE, XE>() == 2 && warp == kCompute + 1) {
+    if constexpr (x_warps<TYPE, XE>() == 2) stage_x<TYPE, NT, XE, 1>(sm, p, c_begin, nch, lane);
   } else {
     // Lane (g, t) feeds column g of each n8 tile, i.e. batch row 4i + g/2.  Lanes
     // of absent batch rows read lane (g mod 2, t)'s fragment instead: the copy
@@ -1164,7 +1188,7 @@ mq_status launch_one(const MvArgs &a, cudaStream_t s, const char *name) {
   const int64_t groups = (a.N + kRows - 1) / kRows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(test_fail_launch() ? 0u : (unsigned)(groups * a.S), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(mv_threads<TYPE, XE>(), 1, 1);
   cfg.dynamicSmemBytes = mv_smem_bytes<TYPE, NT>();
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
