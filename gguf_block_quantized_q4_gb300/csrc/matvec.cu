@@ -34,13 +34,15 @@
 // (repack.cu) store each thread's words contiguously.
 //
 // Data movement and roles.  A CTA owns one 128-row group of the decode plane
-// and a K-slice, and runs 10 warps around a shared-memory ring of chunk stages:
+// and a K-slice, and runs 10 warps (11 in most kernels for three or more batch rows,
+// see x_warps) around a shared-memory ring of chunk stages:
 //  * the copy warp (one lane) streams, per 256-element chunk, the group's weight
 //    tile (one contiguous run of the tiled decode plane) and the x chunk of every
 //    batch row into the stage with 1-D bulk copies (cp.async.bulk, counted by the
 //    stage's transaction barrier);
-//  * the x warp turns the staged x chunk into B fragments (and the sub-block
-//    sums for Q4_K) in a second, smaller ring of fragment slots;
+//  * the x warp (or two, each with half of the batch rows) turns the staged x
+//    chunk into B fragments (and the sub-block sums for Q4_K) in a second,
+//    smaller ring of fragment slots;
 //  * eight compute warps, 16 rows each, wait for a weight stage, decode their
 //    rows' scales into a warp-private table and copy their quant words into
 //    registers, release the weight stage at once (so the next chunk's copy is
