@@ -132,8 +132,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def src_sha(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def src_sha(paths):
+    """sha256[:16] of a source file, or of several files' bytes in the order given."""
+    if isinstance(paths, str):
+        paths = [paths]
+    h = hashlib.sha256()
+    for path in paths:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel_key, src):
@@ -517,7 +523,8 @@ def main():
                    "ms": t_mv, "algorithmic_bytes": MV_BYTES},
         "quantize": {"kernel": "quantize_act_kernel", "bound": "hbm", "achieved": q_gbs,
                      "peak": hbm, "unit": "GB/s", "frac": q_gbs / hbm,
-                     "traffic": traffic_for("quantize_m512", os.path.join(csrc, "quantize.cu")),
+                     "traffic": traffic_for("quantize_m512", [os.path.join(csrc, "quantize.cu"),
+                                                              os.path.join(csrc, "quant_row.cuh")]),
                      "ms": t_q, "algorithmic_bytes": Q_BYTES},
         "mmq": {"kernel": "mmq_tc_kernel<Q4_K>", "bound": "tensor", "achieved": mm_tops,
                 "peak": bf16, "unit": "TFLOP/s", "frac": mm_tops / bf16,
