@@ -244,7 +244,7 @@ def graph_time_ms(fn, calls, trials=5):
     return statistics.median(out)
 
 
-def profile_calls(kernel: str, calls: int):
+def profile_calls(kernel: str, calls: int, batch=None):
     """Run `calls` launches of one hot-path kernel on the bench workload and exit: the
     program that ncu captures are taken of (one kernel, few launches, ~0.3 GB on device)."""
     import torch
@@ -258,8 +258,9 @@ def profile_calls(kernel: str, calls: int):
     flags = mq.REG_NO_MMQ_PLANE if kernel == "matvec" else mq.REG_DEFAULT
     W = mq.register_weight(QTYPE, Wb, N, K, flags)
     if kernel == "matvec":
-        x = torch.from_numpy(synth.activations(B, K, XD_SEED)).cuda()
-        y = torch.empty((B, N), device="cuda")
+        nb = batch or B
+        x = torch.from_numpy(synth.activations(nb, K, XD_SEED)).cuda()
+        y = torch.empty((nb, N), device="cuda")
         for _ in range(calls):
             mq.matvec(W, x, y)
     else:
@@ -393,13 +394,15 @@ def main():
     ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
                     help="profiling mode: only run --calls launches of this kernel")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--batch", type=int, choices=range(1, 9), default=None,
+                    help="profiling mode, matvec: batch rows (default: the bench's decode batch)")
     ap.add_argument("--chain", type=int, default=0,
                     help="time a decode chain of this many small matvecs, eager and graphed")
     ap.add_argument("--ffn-gu", action="store_true",
                     help="time the fused gate/up matvec and MMQ against two plain calls")
     args = ap.parse_args()
     if args.kernel:
-        return profile_calls(args.kernel, args.calls)
+        return profile_calls(args.kernel, args.calls, args.batch)
     if args.chain:
         return chain_timing(args.chain)
     if args.ffn_gu:
