@@ -9,7 +9,13 @@ Prints one JSON line.  `value` is the decode matvec's HBM throughput (algorithmi
 bytes / kernel time, whole job = all ranks), timed over back-to-back calls on
 rotating weight copies (> 3x the 135 MB L2) replayed from a CUDA graph; the
 MMQ's int-op rate and the per-kernel rooflines are in the same line.  The K
-timed steps (matvec + quantise + MMQ each) are one captured CUDA graph.
+timed steps (matvec + quantise + MMQ each) are one captured CUDA graph, replayed
+once at the end of a sustained busy period of untimed replays of the same graph
+(clocks are sampled over all of it).  `configs` holds every configuration of the
+five workloads (Q8_0 896 x 896; Q4_K 18944 x 3584; Q6_K 3584 x 18944 at B = 1, 2,
+4, 8; the Q4_K prefill at M = 512; the Q6_K 151936 x 3584 LM head at M = 1 and
+M = 2048), each with its roofline.  `cpu_baseline` times the oracle on one core
+and on all cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mq|reference]
 """
@@ -25,6 +31,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -34,6 +42,7 @@ QTYPE, N, K, B, M = 12, 18944, 3584, 1, 512
 W_SEED, XD_SEED, XA_SEED = 102, 202, 204
 ROT = 4  # prefill buffer sets rotated between steps (4 x ~220 MB >> L2)
 L2_BYTES = 135e6
+SOAK_S = 1.5  # seconds of sustained replays ending with the timed region
 
 # algorithmic bytes / ops per launch (what the method must move or compute)
 MV_BYTES = N * (K // 256) * 144 + B * K * 4 + B * N * 4
@@ -156,68 +165,137 @@ def traffic_for(kernel_key, src):
     return None
 
 
-def cpu_baseline(budget_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the same workload (1 thread)."""
-    import numpy as np
+def _host_cpus():
+    """(usable cores, CPU model line) of this host: os.sched_getaffinity and lscpu."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = "unknown"
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return cores, model
 
+
+def _timed(fn, min_s):
+    """(seconds per call, calls) of fn() repeated until at least min_s seconds have passed."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        t = time.perf_counter() - t0
+        if t >= min_s:
+            return t / n, n
+
+
+def cpu_baseline(budget_s: float = 16.0):
+    """The oracle, as it stands, on the bench workload's own inputs: the decode matvec
+    (GB/s, the value metric) and the prefill MMQ (TOPS), each on one core and on all
+    cores (the OpenMP build of the same oracle.c: rows in parallel, per-row arithmetic
+    unchanged).  One-core figures come from a sample of the call, extrapolated linearly
+    (the work per row is fixed); all-core figures time the full decode call and a
+    16-row slice of the prefill."""
     import oracle
     import synth
     Wb = synth.weights(QTYPE, N, K, W_SEED)
     xd = synth.activations(B, K, XD_SEED)
     xa = synth.activations(M, K, XA_SEED)
-    # decode matvec sample: the first `rows` weight rows
-    rows, t = 256, 0.0
+    qs, sc, _ = oracle.quantize_act(xa)
+    cores, model = _host_cpus()
+    threads = oracle.threads(True)
+    q = budget_s / 4
+    # decode matvec, one core: the first `rows` weight rows
+    rows = 64
     while True:
-        t0 = time.perf_counter()
-        oracle.matvec(QTYPE, Wb, N, K, xd, 0, rows)
-        t = time.perf_counter() - t0
-        if t > budget_s / 4 or rows >= N:
+        t1, _ = _timed(lambda: oracle.matvec(QTYPE, Wb, N, K, xd, 0, rows), 0.0)
+        if t1 > q / 4 or rows >= N:
             break
-        rows = min(N, rows * 2)
-    mv_bytes = rows * (K // 256) * 144 + B * K * 4 + B * rows * 4
-    mv_gbs = mv_bytes / t / 1e9
-    # prefill sample: quantise 1 activation row, MMQ against `nrow` weight rows
-    qs, sc, _ = oracle.quantize_act(xa[:1])
-    nrow, tm = 256, 0.0
+        rows = min(N, rows * 4)
+    t1, _ = _timed(lambda: oracle.matvec(QTYPE, Wb, N, K, xd, 0, rows), q)
+    mv1 = (rows * (K // 256) * 144 + B * K * 4 + B * rows * 4) / t1 / 1e9
+    # decode matvec, all cores: the whole call
+    tall, nall = _timed(lambda: oracle.matvec(QTYPE, Wb, N, K, xd, parallel=True), q)
+    mvall = MV_BYTES / tall / 1e9
+    # prefill MMQ, 16 activation rows: one core against `nrow` weight rows, all cores
+    # against all N rows
+    mrows = list(range(16))
+    nrow = 16
     while True:
-        t0 = time.perf_counter()
-        oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=[0], n0=0, n1=nrow)
-        tm = time.perf_counter() - t0
-        if tm > budget_s / 4 or nrow >= N:
+        tm1, _ = _timed(lambda: oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=mrows, n1=nrow), 0.0)
+        if tm1 > q / 4 or nrow >= N:
             break
-        nrow = min(N, nrow * 2)
-    mmq_tops = 2 * 1 * nrow * K / tm / 1e12
-    return {"value": mv_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"decode matvec over weight rows 0..{rows} of {N} (B=1), "
-                       f"{t:.2f} s; MMQ of 1 activation row x {nrow} weight rows, {tm:.2f} s; "
-                       "single-threaded plain C, fp64 accumulation"),
-            "mmq_tops": mmq_tops, "seconds": t + tm}
+        nrow = min(N, nrow * 4)
+    tm1, _ = _timed(lambda: oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=mrows, n1=nrow), q)
+    tmall, _ = _timed(lambda: oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=mrows, parallel=True), q)
+    mm1 = 2 * 16 * nrow * K / tm1 / 1e12
+    mmall = 2 * 16 * N * K / tmall / 1e12
+    return {
+        "value": mvall, "unit": "GB/s", "cores": threads, "kind": "oracle",
+        "sample": (f"decode matvec {N}x{K} B={B}: the full call on {threads} threads "
+                   f"({nall} calls); prefill MMQ: activation rows 0..15 x all {N} weight "
+                   f"rows on {threads} threads; plain C, fp64 accumulation"),
+        "mmq_tops": mmall,
+        "one_core": {"value": mv1, "unit": "GB/s", "mmq_tops": mm1, "cores": 1,
+                     "sample": (f"decode matvec over weight rows 0..{rows} of {N}; MMQ of "
+                                f"activation rows 0..15 x weight rows 0..{nrow}; rates per "
+                                "row extrapolated linearly to the full calls")},
+        "host": {"affinity_cpus": cores, "lscpu_model": model, "openmp_threads": threads},
+    }
+
+
+def workload_config(ws: int):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": WORKLOAD, "N": N, "K": K, "decode_B": B, "prefill_M": M,
+            "qtype": "Q4_K", "seeds": {"W": W_SEED, "x_decode": XD_SEED, "x_prefill": XA_SEED},
+            "l2": ("inputs larger than L2: decode weight copies rotated (> 3x L2 together); "
+                   "each step's prefill moves ~180 MB between decode calls"),
+            "parallelism": f"replicas x{ws}"}
 
 
 def run_reference(args):
+    """The reference arm: the oracle (all host cores), as it stands, on the same workload;
+    each step one full decode matvec call (the value metric) plus a 16-row slice of the
+    prefill MMQ.  Rank 0 alone runs it."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    cb = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    import oracle
+    import synth
+    Wb = synth.weights(QTYPE, N, K, W_SEED)
+    xd = synth.activations(B, K, XD_SEED)
+    qs, sc, _ = oracle.quantize_act(synth.activations(M, K, XA_SEED))
+    threads = oracle.threads(True)
+    cores, model = _host_cpus()
+
+    def step():
+        t0 = time.perf_counter()
+        oracle.matvec(QTYPE, Wb, N, K, xd, parallel=True)
+        t1 = time.perf_counter()
+        oracle.mmq(QTYPE, Wb, N, K, qs, sc, mrows=list(range(16)), parallel=True)
+        return t1 - t0, time.perf_counter() - t1
+
     for _ in range(args.warmup):
-        pass  # the oracle has no warm state; each step below is timed
-    vals = []
-    t_all = 0.0
-    for _ in range(args.steps):
-        c = cpu_baseline(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-        vals.append(c["value"])
-        t_all += c["seconds"]
-    v = statistics.median(vals) if vals else cb["value"]
+        step()
+    tm = [step() for _ in range(args.steps)]
+    t_mv = statistics.median(a for a, _ in tm)
+    t_mm = statistics.median(b for _, b in tm)
+    v = MV_BYTES / t_mv / 1e9
+    sample = (f"each step: the full decode matvec {N}x{K} B={B} and activation rows 0..15 of "
+              f"the prefill MMQ (all {N} weight rows), on {threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000 * t_all / max(1, args.steps), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": cb["sample"]},
+            "ms_per_step": 1000 * sum(a + b for a, b in tm) / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(ws),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample,
+                             "host": {"affinity_cpus": cores, "lscpu_model": model}},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
-            "mmq_tops": cb["mmq_tops"]}
+            "mmq_tops": 2 * 16 * N * K / t_mm / 1e12}
     print(json.dumps(line))
     return 0
 
@@ -384,34 +462,135 @@ def ffn_gu_timing(reps: int = 20):
     return 0
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
-                    help="profiling mode: only run --calls launches of this kernel")
-    ap.add_argument("--calls", type=int, default=3)
-    ap.add_argument("--batch", type=int, choices=range(1, 9), default=None,
-                    help="profiling mode, matvec: batch rows (default: the bench's decode batch)")
-    ap.add_argument("--chain", type=int, default=0,
-                    help="time a decode chain of this many small matvecs, eager and graphed")
-    ap.add_argument("--ffn-gu", action="store_true",
-                    help="time the fused gate/up matvec and MMQ against two plain calls")
-    args = ap.parse_args()
-    if args.kernel:
-        return profile_calls(args.kernel, args.calls, args.batch)
-    if args.chain:
-        return chain_timing(args.chain)
-    if args.ffn_gu:
-        return ffn_gu_timing()
-    if args.impl == "reference":
-        return run_reference(args)
-    args.warmup = max(args.warmup, 3)
+def rotation(nbytes: float) -> int:
+    """Copies of an input that together exceed 3x L2, so back-to-back calls read HBM."""
+    return max(1, int(np.ceil(3 * L2_BYTES / nbytes)))
 
-    import numpy as np
+
+def roof(kernel, bound, achieved, peak, unit, ms, algorithmic, traffic=None, note=None):
+    r = {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+         "frac": achieved / peak, "traffic": traffic, "ms": ms}
+    r["algorithmic_bytes" if bound == "hbm" else "algorithmic_ops"] = algorithmic
+    if note:
+        r["note"] = note
+    return r
+
+
+MMQ_PEAK_NOTE = ("the integer contraction runs exactly on the f16 tensor pipe (integer-valued "
+                 "f16 operands, f32 accumulation): sm_103a has no tcgen05 kind::i8, and the "
+                 "legacy int8 mma.sync path measured 151 TOPS on this GPU; frac is against the "
+                 "measured bf16 burst peak (f16 runs at the bf16 rate)")
+
+
+def measure_configs(mq, dev, hbm, bf16):
+    """Every configuration of the five hot-path workloads: device time per call from graph
+    replays of back-to-back calls on rotating inputs (median of 5), with its roofline."""
+    import torch
+
+    import synth
+    WL = synth.WORKLOADS
+    out = {}
+    csrc = os.path.join(ROOT, "gguf_block_quantized_q4_gb300", "csrc")
+
+    def mv_bytes(qtype, n, k, b):
+        be, bb = synth.BLOCK[qtype]
+        return n * (k // be) * bb + b * k * 4 + b * n * 4
+
+    def matvec_case(name, batches, rotate=True):
+        c = WL[name]
+        qt, n, k = c["qtype"], c["N"], c["K"]
+        wb = synth.weights(qt, n, k, c["w_seed"])
+        rot = rotation(len(wb)) if rotate else 1
+        Ws = [mq.register_weight(qt, wb, n, k, mq.REG_NO_MMQ_PLANE) for _ in range(rot)]
+        res = {}
+        for b in batches:
+            x = torch.from_numpy(synth.activations(b, k, c["x_seed"], c["x_scale"])).to(dev)
+            ys = [torch.empty((b, n), device=dev) for _ in range(rot)]
+            t = graph_time_ms(lambda j: mq.matvec(Ws[j % rot], x, ys[j % rot]),
+                              max(8, 2 * rot) if rot > 1 else 20)
+            by = mv_bytes(qt, n, k, b)
+            res[b] = roof(f"matvec_kernel<{synth.TYPE_NAME[qt]}>", "hbm", by / (t * 1e-3) / 1e9,
+                          hbm, "GB/s", t, by)
+            res[b]["weight_copies_rotated"] = rot
+        return Ws, res
+
+    # C1: Q8_0 896 x 896, B = 1 (L2-resident; launch-bound): us per call, eager and graphed
+    Ws, r = matvec_case("q8_0_matvec_896x896", [1])
+    c1 = r[1]
+    x = torch.from_numpy(synth.activations(1, 896, 0)).to(dev)
+    ys = [torch.empty((1, 896), device=dev) for _ in range(len(Ws))]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for j in range(20):
+        mq.matvec(Ws[j % len(Ws)], x, ys[j % len(Ws)])
+    reps = 2000
+    torch.cuda.synchronize()
+    e0.record()
+    for j in range(reps):
+        mq.matvec(Ws[j % len(Ws)], x, ys[j % len(Ws)])
+    e1.record()
+    torch.cuda.synchronize()
+    eager_us = e0.elapsed_time(e1) * 1e3 / reps
+    g1000 = graph_time_ms(lambda j: mq.matvec(Ws[j % len(Ws)], x, ys[j % len(Ws)]), 1000, 3)
+    c1.update({"us_per_call_graph": c1["ms"] * 1e3, "us_per_call_eager": eager_us,
+               "us_per_call_graph_1000": g1000 * 1e3,
+               "note": ("0.86 MB, L2-resident when repeated: launch-bound, reported in us per "
+                        "call; eager = back-to-back host launches through the Python binding")})
+    out["c1_q8_0_matvec_896x896_b1"] = c1
+    for W in Ws:
+        W.free()
+    # C2: Q4_K 18944 x 3584, B = 1
+    Ws, r = matvec_case("q4_k_matvec_18944x3584", [1])
+    out["c2_q4_k_matvec_18944x3584_b1"] = r[1]
+    for W in Ws:
+        W.free()
+    # C3: Q6_K 3584 x 18944, B = 1, 2, 4, 8
+    Ws, r = matvec_case("q6_k_matvec_3584x18944", [1, 2, 4, 8])
+    for b in (1, 2, 4, 8):
+        out[f"c3_q6_k_matvec_3584x18944_b{b}"] = r[b]
+    for W in Ws:
+        W.free()
+
+    def prefill_case(name, key, rot):
+        c = WL[name]
+        qt, n, k, m = c["qtype"], c["N"], c["K"], c["M"][0]
+        wb = synth.weights(qt, n, k, c["w_seed"])
+        Ws = [mq.register_weight(qt, wb, n, k) for _ in range(rot)]
+        xs = [torch.from_numpy(synth.activations(m, k, c["x_seed"], c["x_scale"])).to(dev)
+              for _ in range(rot)]
+        xq = [mq.act_buffer(m, k, dev) for _ in range(rot)]
+        ys = [torch.empty((m, n), device=dev) for _ in range(rot)]
+        tq = graph_time_ms(lambda j: mq.quantize_act(xs[j % rot], xq[j % rot]), 4 * rot)
+        tm = graph_time_ms(lambda j: mq.mmq(Ws[j % rot], xq[j % rot], m, ys[j % rot]), 2 * rot)
+        tf = graph_time_ms(lambda j: mq.mmq_fused(Ws[j % rot], xs[j % rot], xq[j % rot],
+                                                  ys[j % rot]), 2 * rot)
+        qbytes = m * k * 4 + m * k + 2 * m * (k // 32) * 4 + m * k * 2
+        ops = 2 * m * n * k
+        out[f"{key}_quantize"] = roof("quantize_act_kernel", "hbm", qbytes / (tq * 1e-3) / 1e9,
+                                      hbm, "GB/s", tq, qbytes)
+        out[f"{key}_mmq"] = roof(f"mmq_tc_kernel<{synth.TYPE_NAME[qt]}>", "tensor",
+                                 ops / (tm * 1e-3) / 1e12, bf16, "TFLOP/s", tm, ops,
+                                 note=MMQ_PEAK_NOTE)
+        out[f"{key}_prefill_incl_quantise"] = {
+            "two_kernels_ms": tq + tm, "fused_ms": tf,
+            "two_kernels_tops": ops / ((tq + tm) * 1e-3) / 1e12,
+            "fused_tops": ops / (tf * 1e-3) / 1e12}
+        for W in Ws:
+            W.free()
+
+    # C4: Q4_K prefill, M = 512
+    prefill_case("q4_k_mmq_512x18944x3584", "c4_q4_k_m512", 4)
+    # C5: Q6_K LM head 151936 x 3584: M = 1 decode matvec, M = 2048 prefill
+    Ws, r = matvec_case("q6_k_lm_head_151936x3584", [1], rotate=False)
+    out["c5_q6_k_lm_head_151936x3584_m1"] = r[1]
+    for W in Ws:
+        W.free()
+    prefill_case("q6_k_lm_head_151936x3584", "c5_q6_k_lm_head_m2048", 1)
+    torch.cuda.synchronize()
+    mq.stream_status()
+    return out
+
+
+def run_mq(args):
     import torch
 
     import gguf_block_quantized_q4_gb300 as mq
@@ -426,10 +605,11 @@ def main():
     mqbuild.build()
     mq.init(local)
     dev = torch.device("cuda", local)
+    hbm, bf16, peak_src = peaks()
 
     Wb = synth.weights(QTYPE, N, K, W_SEED)
     # decode: RMV weight copies, > 3x L2 together, so back-to-back calls read HBM
-    rmv = int(np.ceil(3 * L2_BYTES / len(Wb)))
+    rmv = rotation(len(Wb))
     Wd = [mq.register_weight(QTYPE, Wb, N, K, mq.REG_NO_MMQ_PLANE) for _ in range(rmv)]
     Wp = [mq.register_weight(QTYPE, Wb, N, K) for _ in range(ROT)]
     xd_h = synth.activations(B, K, XD_SEED)
@@ -461,14 +641,24 @@ def main():
     g_steps.replay()  # untimed warm replay
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Clocks are sampled over a sustained busy period that ends with the timed region: the
+    # same step graph replayed (untimed) for >= SOAK_S seconds, then the K timed steps.
+    t0 = time.perf_counter()
+    g_steps.replay()
+    torch.cuda.synchronize()
+    soak_reps = max(1, int(np.ceil(SOAK_S / max(1e-6, time.perf_counter() - t0))))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        t_soak = time.perf_counter()
+        for _ in range(soak_reps):
+            g_steps.replay()
         e0.record()
         g_steps.replay()
         e1.record()
         torch.cuda.synchronize()
+        t_soak = time.perf_counter() - t_soak
     if ws > 1:
         torch.distributed.barrier()
     mq.stream_status()
@@ -513,50 +703,55 @@ def main():
     te_mm = statistics.median(e[1].elapsed_time(e[2]) for e in eev)
     te_mv, te_mm = max_over_ranks([te_mv, te_mm], ws, dev)
     assert np.isfinite(yd_p.numpy()).all() and np.isfinite(ym_p.numpy()).all()
+    for w in Wd + Wp:
+        w.free()
+    del xq, xqf, ym
+    torch.cuda.empty_cache()
 
-    hbm, bf16, peak_src = peaks()
+    # every configuration of the five workloads (the step above covers two of them)
+    configs = measure_configs(mq, dev, hbm, bf16) if not args.no_configs else None
+
     mv_gbs = MV_BYTES / (t_mv * 1e-3) / 1e9
     q_gbs = Q_BYTES / (t_q * 1e-3) / 1e9
     mm_tops = MMQ_OPS / (t_mm * 1e-3) / 1e12
     csrc = os.path.join(ROOT, "gguf_block_quantized_q4_gb300", "csrc")
     kern = {
-        "matvec": {"kernel": "matvec_kernel<Q4_K,NT=1>", "bound": "hbm", "achieved": mv_gbs,
-                   "peak": hbm, "unit": "GB/s", "frac": mv_gbs / hbm,
-                   "traffic": traffic_for("matvec_q4_k_b1", os.path.join(csrc, "matvec.cu")),
-                   "ms": t_mv, "algorithmic_bytes": MV_BYTES},
-        "quantize": {"kernel": "quantize_act_kernel", "bound": "hbm", "achieved": q_gbs,
-                     "peak": hbm, "unit": "GB/s", "frac": q_gbs / hbm,
-                     "traffic": traffic_for("quantize_m512", [os.path.join(csrc, "quantize.cu"),
-                                                              os.path.join(csrc, "quant_row.cuh")]),
-                     "ms": t_q, "algorithmic_bytes": Q_BYTES},
-        "mmq": {"kernel": "mmq_tc_kernel<Q4_K>", "bound": "tensor", "achieved": mm_tops,
-                "peak": bf16, "unit": "TFLOP/s", "frac": mm_tops / bf16,
-                "traffic": traffic_for("mmq_q4_k_m512", os.path.join(csrc, "mmq.cu")),
-                "ms": t_mm, "algorithmic_ops": MMQ_OPS},
+        "matvec": roof("matvec_kernel<Q4_K,NT=1>", "hbm", mv_gbs, hbm, "GB/s", t_mv, MV_BYTES,
+                       traffic_for("matvec_q4_k_b1", os.path.join(csrc, "matvec.cu"))),
+        "quantize": roof("quantize_act_kernel", "hbm", q_gbs, hbm, "GB/s", t_q, Q_BYTES,
+                         traffic_for("quantize_m512", [os.path.join(csrc, "quantize.cu"),
+                                                       os.path.join(csrc, "quant_row.cuh")])),
+        "mmq": roof("mmq_tc_kernel<Q4_K>", "tensor", mm_tops, bf16, "TFLOP/s", t_mm, MMQ_OPS,
+                    traffic_for("mmq_q4_k_m512", os.path.join(csrc, "mmq.cu")),
+                    note=MMQ_PEAK_NOTE),
     }
     dom = max(kern, key=lambda k: kern[k]["ms"])
-    roof = {k: kern[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
-    roof["kernel"] = kern[dom]["kernel"]
-    roof["peak_source"] = (f"{peak_src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'}"
-                           " burst; f16 runs at the bf16 rate)")
+    roofl = {k: kern[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roofl["kernel"] = kern[dom]["kernel"]
+    roofl["peak_source"] = (f"{peak_src} ({'hbm_gbs' if roofl['bound'] == 'hbm' else 'bf16_tflops'}"
+                            " burst)")
+    if "note" in kern[dom]:
+        roofl["peak_note"] = kern[dom]["note"]
     e2e_mv = MV_BYTES / (te_mv * 1e-3) / 1e9
     e2e_mm = MMQ_OPS / (te_mm * 1e-3) / 1e12
+    config = workload_config(ws)
+    config["timing"] = (f"steps: one CUDA graph of K steps, timed once (exactly K steps) at the "
+                        f"end of a sustained busy period of {soak_reps} untimed replays of the "
+                        f"same graph ({t_soak:.2f} s in all, clocks sampled throughout); "
+                        "per-kernel and per-config: graph replays of back-to-back calls on "
+                        "rotating buffers, median of 5")
     line = {
         "metric": METRIC, "value": whole_job(mv_gbs, ws), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
         "data": "synthetic (seeded, Qwen2.5-7B FFN-shaped Q4_K weights, N(0,1) activations)",
-        "config": {"workload": WORKLOAD, "N": N, "K": K, "decode_B": B, "prefill_M": M,
-                   "l2": (f"inputs larger than L2: {rmv} decode weight copies rotated; each timed "
-                          f"step's prefill moves ~180 MB between decode calls"),
-                   "timing": ("steps: one CUDA graph of K steps; per-kernel: graph replays of "
-                              "back-to-back calls on rotating buffers, median of 5"),
-                   "parallelism": f"replicas x{ws}"},
+        "config": config,
         "matvec_gbs": whole_job(mv_gbs, ws), "matvec_frac_of_hbm": mv_gbs / hbm,
         "matvec_frac_of_8tbs": mv_gbs / 8000.0,
         "mmq_tops": whole_job(mm_tops, ws), "mmq_frac_of_f16_peak": mm_tops / bf16,
         "quantize_gbs": whole_job(q_gbs, ws),
-        "roofline": roof, "kernels": kern,
+        "roofline": roofl, "kernels": kern,
+        "configs": configs,
         "prefill_incl_quantise": {
             "two_kernels_ms": t_q + t_mm, "fused_ms": t_fu,
             "two_kernels_tops": whole_job(MMQ_OPS / ((t_q + t_mm) * 1e-3) / 1e12, ws),
@@ -579,11 +774,40 @@ def main():
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line))
-    for w in Wd + Wp:
-        w.free()
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements of the five workloads")
+    ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
+                    help="profiling mode: only run --calls launches of this kernel")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--batch", type=int, choices=range(1, 9), default=None,
+                    help="profiling mode, matvec: batch rows (default: the bench's decode batch)")
+    ap.add_argument("--chain", type=int, default=0,
+                    help="time a decode chain of this many small matvecs, eager and graphed")
+    ap.add_argument("--ffn-gu", action="store_true",
+                    help="time the fused gate/up matvec and MMQ against two plain calls")
+    args = ap.parse_args()
+    if args.kernel:
+        return profile_calls(args.kernel, args.calls, args.batch)
+    if args.chain:
+        return chain_timing(args.chain)
+    if args.ffn_gu:
+        return ffn_gu_timing()
+    if args.impl == "reference":
+        return run_reference(args)
+    args.warmup = max(args.warmup, 3)
+    return run_mq(args)
 
 
 if __name__ == "__main__":

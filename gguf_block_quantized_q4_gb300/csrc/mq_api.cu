@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -80,8 +81,29 @@ extern "C" const char *mq_status_name(mq_status s) {
   return "MQ_ERR_UNKNOWN";
 }
 
+// Failure-injection seams of the tests, read from the environment by mq_init (every call,
+// including those that find the device ready), never on a hot-path call:
+//   MQ_TEST_FAIL_LAUNCH=1  the matvec and MMQ launches are configured with an empty grid,
+//                          which the runtime refuses before any kernel runs;
+//   MQ_TEST_EXPIRE_WAIT=1  the MMQ epilogue first waits on a barrier nothing arrives on;
+//                          the wait expires after about a millisecond, records
+//                          MQ_ERR_TIMEOUT in the status word and the kernel carries on.
+static std::atomic<int> g_test_fail_launch{0}, g_test_expire_wait{0};
+
+static int env_flag(const char *name) {
+  const char *v = getenv(name);
+  return (v && v[0] == '1') ? 1 : 0;
+}
+
+int mq::test_fail_launch() { return g_test_fail_launch.load(std::memory_order_relaxed); }
+static int test_expire_wait() { return g_test_expire_wait.load(std::memory_order_relaxed); }
+
+static mq_status static_scratch(DeviceState *st, uint8_t **out, const char *site);
+
 extern "C" mq_status mq_init(int device) {
   const char *site = "mq_init";
+  g_test_fail_launch.store(env_flag("MQ_TEST_FAIL_LAUNCH"), std::memory_order_relaxed);
+  g_test_expire_wait.store(env_flag("MQ_TEST_EXPIRE_WAIT"), std::memory_order_relaxed);
   int ndev = 0;
   CK(cudaGetDeviceCount(&ndev), site);
   if (device < 0 || device >= ndev)
@@ -106,6 +128,10 @@ extern "C" mq_status mq_init(int device) {
   CK(cudaStreamCreateWithFlags(&st->reg_stream, cudaStreamNonBlocking), site);
   mq_status s = init_kernels(st);
   if (s == MQ_OK) s = init_matvec(st);
+  // the static scratch of mq_mmq_fused_static: looking its address up here loads this file's
+  // device code (and with it the array) now, outside any stream capture of the caller
+  uint8_t *scratch = nullptr;
+  if (s == MQ_OK) s = static_scratch(st, &scratch, site);
   if (s != MQ_OK) return s;
   CK(cudaDeviceSynchronize(), site);
   st->ready = true;
@@ -505,20 +531,6 @@ extern "C" mq_status mq_quantize_act(const float *x, void *xq, int64_t M, int64_
   return launch_quantize(x, xq, M, K, (cudaStream_t)stream);
 }
 
-int mq::test_fail_launch() {
-  const char *v = getenv("MQ_TEST_FAIL_LAUNCH");
-  return (v && v[0] == '1') ? 1 : 0;
-}
-
-// Failure-injection seam for the bounded-wait test: with MQ_TEST_EXPIRE_WAIT=1 the
-// MMQ epilogue first waits on a barrier nothing arrives on; the wait expires
-// after about a millisecond, records MQ_ERR_TIMEOUT in the status word and the
-// kernel carries on (results stay correct).  Read at every call.
-static int test_expire_wait() {
-  const char *v = getenv("MQ_TEST_EXPIRE_WAIT");
-  return (v && v[0] == '1') ? 1 : 0;
-}
-
 static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, const void *xq,
                             const void *out, int64_t M, int64_t N, int64_t K, DeviceState **st,
                             int ffn_gu = 0) {
@@ -557,7 +569,7 @@ extern "C" mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float 
 // Scratch of mq_mmq_fused_static: one file-scope device array per device (zero at module
 // load), its first 256 bytes the grid barrier's words (at a fixed place, so that calls of
 // different shapes find the count at zero), the rest an xq buffer.  Its address is looked
-// up once per device; nothing is allocated.
+// up once per device, by mq_init; nothing is allocated.
 static __device__ __align__(256) uint8_t g_static_xq[MQ_STATIC_XQ_BYTES];
 static std::mutex g_static_mu;
 

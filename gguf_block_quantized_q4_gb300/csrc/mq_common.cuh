@@ -127,9 +127,9 @@ mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill p
 // programmatic-serialisation attribute, overlaps it and waits for it before reading dst.
 const void *host_device_view(const void *p, size_t align);
 mq_status launch_copy_in(const float *src_view, float *dst, int64_t n, cudaStream_t s, int sms);
-// Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 the matvec
-// and MMQ launches are configured with an empty grid, which the runtime refuses before any
-// kernel runs.  Read at every launch.
+// Failure-injection seam for the launch-failure test: with MQ_TEST_FAIL_LAUNCH=1 in the
+// environment of the last mq_init call, the matvec and MMQ launches are configured with an
+// empty grid, which the runtime refuses before any kernel runs.
 int test_fail_launch();
 mq_status init_kernels(DeviceState *st);  // smem opt-ins of the MMQ kernels
 mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels

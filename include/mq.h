@@ -107,9 +107,12 @@ typedef void *mq_stream;
  * the calling thread).  Queries the SM count and the shared-memory opt-in
  * limit, opts every kernel that needs more than 48 KiB of dynamic shared
  * memory in (once per device, outside any stream capture: "CUDA Backend
- * Design" §2.4, the eager pre-warm), and allocates the per-device status word
- * used by bounded waits.  Idempotent.  Must precede every other call for that
- * device.  Errors: MQ_ERR_CUDA, MQ_ERR_LAUNCH (an opt-in refused). */
+ * Design" §2.4, the eager pre-warm), allocates the per-device status word
+ * used by bounded waits and looks up the address of mq_mmq_fused_static's
+ * scratch.  Idempotent.  Must precede every other call for that device.  Each
+ * call also reads the tests' failure-injection switches MQ_TEST_FAIL_LAUNCH and
+ * MQ_TEST_EXPIRE_WAIT from the environment (no hot-path call reads it).
+ * Errors: MQ_ERR_CUDA, MQ_ERR_LAUNCH (an opt-in refused). */
 mq_status mq_init(int device);
 
 /* mq_register_weight -- copy an N x K GGUF tensor (rows contiguous, blocks
@@ -242,8 +245,8 @@ mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float *x, void *x
  * buffer, so that the call allocates nothing (no counterpart in the pages, which always
  * hand the quantised activations over in a buffer).  The scratch is one file-scope static
  * device array of MQ_STATIC_XQ_BYTES per device, created by the driver with the library's
- * device code (with lazy module loading, when the first call looks it up); its address is
- * looked up once per device (cudaGetSymbolAddress, checked).  Its first 256 bytes hold the
+ * device code; mq_init looks its address up (cudaGetSymbolAddress, checked), which loads
+ * that code, so the array exists once mq_init has returned and a call allocates nothing.  Its first 256 bytes hold the
  * grid barrier's words, the rest an xq buffer: mq_act_bytes(M, K) must not exceed
  * MQ_STATIC_XQ_BYTES - 256 (else MQ_ERR_SHAPE, before any device work).  After a call the
  * scratch holds that call's quantised activations in the mq_act_bytes layout (there is no

@@ -16,21 +16,36 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 
-CFLAGS = ["-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off", "-Wall", "-shared",
-          "-fPIC"]
+CFLAGS = ["-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off", "-Wall",
+          "-Wno-unknown-pragmas", "-shared", "-fPIC"]
+
+
+def _compile(target: str, extra, force: bool) -> str:
+    if force or not os.path.exists(target) or \
+            os.path.getmtime(target) < os.path.getmtime(_SRC):
+        tmp = target + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, *extra, _SRC, "-o", tmp, "-lm"], check=True,
+                       capture_output=True)
+        os.replace(tmp, target)
+    return target
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so next to it (gcc, no FMA contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
-        os.replace(tmp, _LIB)
-    return _LIB
+    """Compile oracle.c into liboracle.so next to it (gcc, no FMA contraction), and the
+    same source with -fopenmp into liboracle_omp.so when the compiler has OpenMP (the
+    all-cores build: rows in parallel, each row's arithmetic unchanged)."""
+    lib_path = _compile(_LIB, [], force)
+    try:
+        _compile(_LIB_OMP, ["-fopenmp"], force)
+    except (subprocess.CalledProcessError, OSError):
+        pass  # no OpenMP here: the all-cores build is absent, lib_omp() returns None
+    return lib_path
 
 
 _lib = None
+_lib_omp = None
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 
@@ -56,6 +71,10 @@ def load(path: str):
     for f in ("oracle_dequant_row", "oracle_int_weights_row", "oracle_matvec",
               "oracle_quantize_act", "oracle_blockdots", "oracle_mmq"):
         getattr(L, f).restype = ctypes.c_int
+    L.oracle_threads.argtypes = []
+    L.oracle_threads.restype = ctypes.c_int
+    L.oracle_set_threads.argtypes = [ctypes.c_int]
+    L.oracle_set_threads.restype = None
     return L
 
 
@@ -64,6 +83,31 @@ def lib():
     if _lib is None:
         _lib = load(build())
     return _lib
+
+
+def lib_omp():
+    """The OpenMP build of the same oracle.c (rows over all cores), or None if this host's
+    compiler has no OpenMP."""
+    global _lib_omp
+    if _lib_omp is None:
+        build()
+        if os.path.exists(_LIB_OMP):
+            _lib_omp = load(_LIB_OMP)
+    return _lib_omp
+
+
+def threads(parallel: bool = True) -> int:
+    """Threads the row loops run on: 1 for the plain build, the OpenMP build's count else."""
+    L = lib_omp() if parallel else lib()
+    return L.oracle_threads() if L is not None else 1
+
+
+def _rows_lib(parallel: bool):
+    if parallel:
+        L = lib_omp()
+        if L is not None:
+            return L
+    return lib()
 
 
 def _ptr(a: np.ndarray):
@@ -112,16 +156,17 @@ def int_weights_row(qtype: int, row: np.ndarray, K: int) -> np.ndarray:
 
 
 def matvec(qtype: int, W: np.ndarray, N: int, K: int, x: np.ndarray, n0: int = 0,
-           n1: int | None = None):
-    """Returns (y, bound), each float64 [B][n1-n0]."""
+           n1: int | None = None, parallel: bool = False):
+    """Returns (y, bound), each float64 [B][n1-n0].  parallel: rows on all cores (the
+    OpenMP build of the same source; the same bits)."""
     n1 = N if n1 is None else n1
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
     B = x.shape[0]
     W = np.ascontiguousarray(W, dtype=np.uint8)
     y = np.empty((B, n1 - n0), dtype=np.float64)
     bnd = np.empty_like(y)
-    _check(lib().oracle_matvec(qtype, _ptr(W), N, K, _ptr(x), B, n0, n1, _ptr(y), _ptr(bnd)),
-           "matvec")
+    _check(_rows_lib(parallel).oracle_matvec(qtype, _ptr(W), N, K, _ptr(x), B, n0, n1, _ptr(y),
+                                             _ptr(bnd)), "matvec")
     return y, bnd
 
 
@@ -138,7 +183,7 @@ def quantize_act(x: np.ndarray):
 
 
 def blockdots(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, mrows=None,
-              n0: int = 0, n1: int | None = None) -> np.ndarray:
+              n0: int = 0, n1: int | None = None, parallel: bool = False) -> np.ndarray:
     """Returns int64 D [len(mrows)][n1-n0][K/32]."""
     n1 = N if n1 is None else n1
     qs = np.ascontiguousarray(qs, dtype=np.int8)
@@ -147,13 +192,13 @@ def blockdots(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, mrows=N
         np.ascontiguousarray(mrows, dtype=np.int64)
     W = np.ascontiguousarray(W, dtype=np.uint8)
     D = np.empty((len(mrows), n1 - n0, K // 32), dtype=np.int64)
-    _check(lib().oracle_blockdots(qtype, _ptr(W), N, K, _ptr(qs), M, _ptr(mrows), len(mrows),
-                                  n0, n1, _ptr(D)), "blockdots")
+    _check(_rows_lib(parallel).oracle_blockdots(qtype, _ptr(W), N, K, _ptr(qs), M, _ptr(mrows),
+                                                len(mrows), n0, n1, _ptr(D)), "blockdots")
     return D
 
 
 def mmq(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, scale: np.ndarray,
-        mrows=None, n0: int = 0, n1: int | None = None):
+        mrows=None, n0: int = 0, n1: int | None = None, parallel: bool = False):
     """Returns (y, bound), float64 [len(mrows)][n1-n0]."""
     n1 = N if n1 is None else n1
     qs = np.ascontiguousarray(qs, dtype=np.int8)
@@ -164,8 +209,9 @@ def mmq(qtype: int, W: np.ndarray, N: int, K: int, qs: np.ndarray, scale: np.nda
     W = np.ascontiguousarray(W, dtype=np.uint8)
     y = np.empty((len(mrows), n1 - n0), dtype=np.float64)
     bnd = np.empty_like(y)
-    _check(lib().oracle_mmq(qtype, _ptr(W), N, K, _ptr(qs), _ptr(scale), M, _ptr(mrows),
-                            len(mrows), n0, n1, _ptr(y), _ptr(bnd)), "mmq")
+    _check(_rows_lib(parallel).oracle_mmq(qtype, _ptr(W), N, K, _ptr(qs), _ptr(scale), M,
+                                          _ptr(mrows), len(mrows), n0, n1, _ptr(y), _ptr(bnd)),
+           "mmq")
     return y, bnd
 
 

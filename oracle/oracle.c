@@ -10,6 +10,10 @@
  * Build: gcc -std=c99 -O2 -fno-fast-math -ffp-contract=off -shared -fPIC
  * (no FMA contraction, no fast-math: the activation quantiser below is
  * defined in IEEE binary32 arithmetic and must be computed exactly so).
+ * The same file built with -fopenmp runs the output rows of the matvec, the
+ * block dots and the MMQ reference on all cores (one thread per row at a time,
+ * each row's arithmetic and summation order exactly as in the plain build, so
+ * both builds return the same bits); without -fopenmp the pragmas are ignored.
  *
  * What it computes, and the passage each function follows:
  *
@@ -44,6 +48,29 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the row loops below use: 1 in the plain build. */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Sets the thread count of the row loops (OpenMP build; a no-op otherwise). */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
 
 #define OR_F16 1
 #define OR_BF16 30
@@ -282,23 +309,32 @@ int oracle_matvec(int type, const uint8_t *W, int64_t N, int64_t K, const float 
 {
     if (!valid_shape(type, K) || n0 < 0 || n1 > N || n0 > n1 || B < 1) return -1;
     int64_t rowbytes = K / oracle_block_elems(type) * oracle_block_bytes(type);
-    double *w = (double *)malloc((size_t)K * sizeof(double));
-    if (!w) return -2;
-    for (int64_t n = n0; n < n1; ++n) {
-        oracle_dequant_row(type, W + n * rowbytes, K, w);
-        for (int b = 0; b < B; ++b) {
-            double acc = 0.0, bnd = 0.0;
-            for (int64_t k = 0; k < K; ++k) {
-                double xv = (double)x[(int64_t)b * K + k];
-                acc += w[k] * xv;
-                bnd += fabs(w[k]) * fabs(xv);
-            }
-            y[(int64_t)b * (n1 - n0) + (n - n0)] = acc;
-            bound[(int64_t)b * (n1 - n0) + (n - n0)] = bnd;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *w = (double *)malloc((size_t)K * sizeof(double));
+        if (!w) {
+#pragma omp atomic write
+            err = -2;
         }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t n = n0; n < n1; ++n) {
+            if (!w) continue;
+            oracle_dequant_row(type, W + n * rowbytes, K, w);
+            for (int b = 0; b < B; ++b) {
+                double acc = 0.0, bnd = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double xv = (double)x[(int64_t)b * K + k];
+                    acc += w[k] * xv;
+                    bnd += fabs(w[k]) * fabs(xv);
+                }
+                y[(int64_t)b * (n1 - n0) + (n - n0)] = acc;
+                bound[(int64_t)b * (n1 - n0) + (n - n0)] = bnd;
+            }
+        }
+        free(w);
     }
-    free(w);
-    return 0;
+    return err;
 }
 
 /* Activation quantiser, binary32 throughout.  For row m and 32-element block
@@ -354,22 +390,32 @@ int oracle_blockdots(int type, const uint8_t *W, int64_t N, int64_t K, const int
         return -1;
     int64_t rowbytes = K / oracle_block_elems(type) * oracle_block_bytes(type);
     int64_t nb = K / 32;
-    int64_t *wi = (int64_t *)malloc((size_t)K * sizeof(int64_t));
-    if (!wi) return -2;
-    for (int64_t n = n0; n < n1; ++n) {
-        oracle_int_weights_row(type, W + n * rowbytes, K, wi);
-        for (int64_t i = 0; i < nm; ++i) {
-            int64_t m = mrows[i];
-            if (m < 0 || m >= M) { free(wi); return -1; }
-            for (int64_t b = 0; b < nb; ++b) {
-                int64_t acc = 0;
-                for (int64_t k = 32 * b; k < 32 * b + 32; ++k) acc += wi[k] * (int64_t)qs[m * K + k];
-                D[(i * (n1 - n0) + (n - n0)) * nb + b] = acc;
+    for (int64_t i = 0; i < nm; ++i)
+        if (mrows[i] < 0 || mrows[i] >= M) return -1;
+    int err = 0;
+#pragma omp parallel
+    {
+        int64_t *wi = (int64_t *)malloc((size_t)K * sizeof(int64_t));
+        if (!wi) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t n = n0; n < n1; ++n) {
+            if (!wi) continue;
+            oracle_int_weights_row(type, W + n * rowbytes, K, wi);
+            for (int64_t i = 0; i < nm; ++i) {
+                int64_t m = mrows[i];
+                for (int64_t b = 0; b < nb; ++b) {
+                    int64_t acc = 0;
+                    for (int64_t k = 32 * b; k < 32 * b + 32; ++k) acc += wi[k] * (int64_t)qs[m * K + k];
+                    D[(i * (n1 - n0) + (n - n0)) * nb + b] = acc;
+                }
             }
         }
+        free(wi);
     }
-    free(wi);
-    return 0;
+    return err;
 }
 
 /* Prefill MMQ reference for activation rows mrows[0..nm) and weight rows
@@ -384,26 +430,36 @@ int oracle_mmq(int type, const uint8_t *W, int64_t N, int64_t K, const int8_t *q
     int64_t nb = K / 32;
     for (int64_t i = 0; i < nm; ++i)
         if (mrows[i] < 0 || mrows[i] >= M) return -1;
-    double *w = (double *)malloc((size_t)K * sizeof(double));
     double *xh = (double *)malloc((size_t)(nm > 0 ? nm : 1) * (size_t)K * sizeof(double));
-    if (!w || !xh) { free(w); free(xh); return -2; }
+    if (!xh) return -2;
     /* the dequantised activations x^ = scale * q, one row per listed m */
     for (int64_t i = 0; i < nm; ++i)
         for (int64_t k = 0; k < K; ++k)
             xh[i * K + k] = (double)scale[mrows[i] * nb + k / 32] * (double)qs[mrows[i] * K + k];
-    for (int64_t n = n0; n < n1; ++n) {
-        oracle_dequant_row(type, W + n * rowbytes, K, w);
-        for (int64_t i = 0; i < nm; ++i) {
-            double acc = 0.0, bnd = 0.0;
-            for (int64_t k = 0; k < K; ++k) {
-                acc += w[k] * xh[i * K + k];
-                bnd += fabs(w[k]) * fabs(xh[i * K + k]);
-            }
-            y[i * (n1 - n0) + (n - n0)] = acc;
-            bound[i * (n1 - n0) + (n - n0)] = bnd;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *w = (double *)malloc((size_t)K * sizeof(double));
+        if (!w) {
+#pragma omp atomic write
+            err = -2;
         }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t n = n0; n < n1; ++n) {
+            if (!w) continue;
+            oracle_dequant_row(type, W + n * rowbytes, K, w);
+            for (int64_t i = 0; i < nm; ++i) {
+                double acc = 0.0, bnd = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    acc += w[k] * xh[i * K + k];
+                    bnd += fabs(w[k]) * fabs(xh[i * K + k]);
+                }
+                y[i * (n1 - n0) + (n - n0)] = acc;
+                bound[i * (n1 - n0) + (n - n0)] = bnd;
+            }
+        }
+        free(w);
     }
-    free(w);
     free(xh);
-    return 0;
+    return err;
 }

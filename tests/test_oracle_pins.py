@@ -515,3 +515,25 @@ def test_ffn_gu_matvec_is_silu_gate_times_up(qtype):
     ref = g * (1 + np.tanh(g / 2)) / 2 * u
     assert np.allclose(h, ref, rtol=1e-12, atol=1e-12)
     assert (bnd > 0).all()
+
+
+@pytest.mark.parametrize("qtype", [synth.Q8_0, synth.Q4_K, synth.Q6_K, synth.Q5_1])
+def test_all_cores_build_returns_the_plain_builds_bits(qtype):
+    """The OpenMP build of oracle.c (rows on all cores; the full-output GPU parity checks
+    and the all-cores CPU baseline use it) returns exactly the plain build's bits: each
+    row's arithmetic and summation order are the same in both."""
+    if oracle.lib_omp() is None:
+        pytest.skip("no OpenMP in this host's compiler")
+    N, K = 301, 1024
+    W = synth.weights(qtype, N, K, 61)
+    x = synth.activations(3, K, 62)
+    for a, b in zip(oracle.matvec(qtype, W, N, K, x), oracle.matvec(qtype, W, N, K, x,
+                                                                    parallel=True)):
+        assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+    qs, sc, _ = oracle.quantize_act(synth.activations(5, K, 63))
+    rows = [4, 0, 2]
+    for a, b in zip(oracle.mmq(qtype, W, N, K, qs, sc, mrows=rows, n0=7, n1=290),
+                    oracle.mmq(qtype, W, N, K, qs, sc, mrows=rows, n0=7, n1=290, parallel=True)):
+        assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+    assert np.array_equal(oracle.blockdots(qtype, W, N, K, qs, mrows=rows),
+                          oracle.blockdots(qtype, W, N, K, qs, mrows=rows, parallel=True))

@@ -2,8 +2,8 @@
 place of a caller buffer.  Two consecutive calls of different shapes and weight types must
 each equal the buffer-based mq_mmq_fused bit for bit (the second call finds the barrier in
 its entry state although the first left quantised data of another shape in the scratch),
-the device's free memory must not change across them once the scratch exists (nothing is
-allocated), and a shape
+the device's free memory must not change across them, the first call on the device
+included (mq_init looked the scratch up; nothing is allocated), and a shape
 whose scratch would not fit is refused before any device work."""
 import pytest
 
@@ -36,9 +36,8 @@ def test_two_consecutive_calls_equal_the_buffered_entry_point():
         xs.append(x)
         ys.append(torch.empty((M, N), device="cuda"))
         refs.append(ref)
-    # one call first: with lazy module loading the driver creates the scratch (a module
-    # global) when the module first loads on the device, i.e. at the first call
-    mq.mmq_fused_static(Ws[1], xs[1], torch.empty_like(ys[1]))
+    # mq_init has looked the scratch up (which loads the module holding it), so even the
+    # first call on the device allocates nothing
     torch.cuda.synchronize()
     mq.stream_status()
     free_before = torch.cuda.mem_get_info()[0]
