@@ -509,7 +509,7 @@ def measure_configs(mq, dev, hbm, bf16):
             t = graph_time_ms(lambda j: mq.matvec(Ws[j % rot], x, ys[j % rot]),
                               max(8, 2 * rot) if rot > 1 else 20)
             by = mv_bytes(qt, n, k, b)
-            res[b] = roof(f"matvec_kernel<{synth.TYPE_NAME[qt]}>", "hbm", by / (t * 1e-3) / 1e9,
+            res[b] = roof(("matvec_kq_kernel" if qt in (12, 13, 14) else "matvec_kernel") + f"<{synth.TYPE_NAME[qt]}>", "hbm", by / (t * 1e-3) / 1e9,
                           hbm, "GB/s", t, by)
             res[b]["weight_copies_rotated"] = rot
         return Ws, res
@@ -716,7 +716,7 @@ def run_mq(args):
     mm_tops = MMQ_OPS / (t_mm * 1e-3) / 1e12
     csrc = os.path.join(ROOT, "gguf_block_quantized_q4_gb300", "csrc")
     kern = {
-        "matvec": roof("matvec_kernel<Q4_K,NT=1>", "hbm", mv_gbs, hbm, "GB/s", t_mv, MV_BYTES,
+        "matvec": roof("matvec_kq_kernel<Q4_K>", "hbm", mv_gbs, hbm, "GB/s", t_mv, MV_BYTES,
                        traffic_for("matvec_q4_k_b1", os.path.join(csrc, "matvec.cu"))),
         "quantize": roof("quantize_act_kernel", "hbm", q_gbs, hbm, "GB/s", t_q, Q_BYTES,
                          traffic_for("quantize_m512", [os.path.join(csrc, "quantize.cu"),

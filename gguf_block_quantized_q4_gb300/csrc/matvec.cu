@@ -61,12 +61,14 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
-#include "mq_common.cuh"
+#include "mv_device.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace mq {
 namespace {
+
+using namespace mvd;
 
 constexpr int kRows = kRowGroup;               // rows per CTA
 constexpr int kCompute = kRows / 16;           // compute warps, 16 rows each
@@ -89,7 +91,6 @@ template <int TYPE, bool XE>
 __host__ __device__ constexpr int mv_threads() {
   return 32 * (kCompute + 1 + x_warps<TYPE, XE>());
 }
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct MvArgs {
   const uint8_t *q;
@@ -234,113 +235,6 @@ struct MvSmem {
   uint64_t wfull[NS], wempty[NS], ffull[FS], fempty[FS];
 };
 
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// bf16 operands (unquantised bf16 weights, bf16 hi/lo activation parts)
-__device__ __forceinline__ void mma16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1,
-                                              uint32_t a2, uint32_t a3, uint32_t b0,
-                                              uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-// (a & b) | c as one three-input logic instruction (written out so that two
-// constant operands do not turn it into two instructions)
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ float f16_lo(uint32_t v) {
-  return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
-}
-__device__ __forceinline__ float f16_hi(uint32_t v) {
-  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-
-__device__ __forceinline__ int chunk_width(int64_t K, int c) {
-  const int64_t left = K - int64_t(c) * kChunk;
-  return left < kChunk ? (int)left : kChunk;
-}
-__device__ __forceinline__ uint32_t sa(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t gtime() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; on expiry records (timeout, site) in the status word and returns.
-__device__ __forceinline__ void mbar_wait(uint32_t a, uint32_t parity, int *status, int site) {
-  if (mbar_try(a, parity)) return;
-  const uint64_t t0 = gtime();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i)
-      if (mbar_try(a, parity)) return;
-    if (gtime() - t0 > kWaitNs) {
-      if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
-      return;
-    }
-  }
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
-                                        uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // ---------------------------------------------------------------------------
 // Copy warp (one lane): weight tile and x rows of each chunk into its stage.
 template <int TYPE, int NT>
@@ -630,11 +524,6 @@ __device__ __forceinline__ void release_and_wait(uint64_t &wempty, uint64_t &ffu
 // ---------------------------------------------------------------------------
 // Compute warps.  Thread (g, t) of warp w covers tile rows ra = 16w + g and
 // rb = ra + 8; tot[0/1][i] accumulates rows ra/rb for batch row 4i + t.
-// Shift left by sh (right by -sh when negative); sh is a constant once the loops that
-// compute it are unrolled, so the branch folds away.
-__device__ __forceinline__ uint32_t shl(uint32_t v, int sh) {
-  return sh >= 0 ? v << sh : v >> (-sh);
-}
 
 // Q4_K and Q5_K (rows of RS = 144 / 176 bytes; Q5_K's fifth bits follow the quants).
 // For Q5_K the fifth bit of each element goes to bit 4 (low-nibble path: 1024 + q) or
@@ -1243,11 +1132,12 @@ mq_status optin_type(const DeviceState *st, const char *name) {
 
 mq_status init_matvec(DeviceState *st) {
   mq_status s;
+  if ((s = init_matvec_kq(st)) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q8_0>(st, "matvec_kernel<Q8_0>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q4_K>(st, "matvec_kernel<Q4_K>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q6_K>(st, "matvec_kernel<Q6_K>")) != MQ_OK) return s;
-  if ((s = optin_type<MQ_Q4_0>(st, "matvec_kernel<Q4_0>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q5_K>(st, "matvec_kernel<Q5_K>")) != MQ_OK) return s;
+  if ((s = optin_type<MQ_Q4_0>(st, "matvec_kernel<Q4_0>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q4_1>(st, "matvec_kernel<Q4_1>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q5_0>(st, "matvec_kernel<Q5_0>")) != MQ_OK) return s;
   if ((s = optin_type<MQ_Q5_1>(st, "matvec_kernel<Q5_1>")) != MQ_OK) return s;
@@ -1291,11 +1181,13 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.S = choose_split(W->N, W->K, st->sms, float_type(W->type) ? 1 : 2);
   a.swiglu = W->ffn_gu;
   a.status = st->status;
+  const bool kq = W->type == MQ_Q4_K || W->type == MQ_Q5_K || W->type == MQ_Q6_K;
+  if (kq && matvec_kq_applies(W->N, st->sms)) return launch_matvec_kq(W, x, y, B, s, st);
   switch (W->type) {
     case MQ_Q4_K: return launch_type<MQ_Q4_K>(a, B, s, "matvec_kernel<Q4_K>");
     case MQ_Q6_K: return launch_type<MQ_Q6_K>(a, B, s, "matvec_kernel<Q6_K>");
-    case MQ_Q4_0: return launch_type<MQ_Q4_0>(a, B, s, "matvec_kernel<Q4_0>");
     case MQ_Q5_K: return launch_type<MQ_Q5_K>(a, B, s, "matvec_kernel<Q5_K>");
+    case MQ_Q4_0: return launch_type<MQ_Q4_0>(a, B, s, "matvec_kernel<Q4_0>");
     case MQ_Q4_1: return launch_type<MQ_Q4_1>(a, B, s, "matvec_kernel<Q4_1>");
     case MQ_Q5_0: return launch_type<MQ_Q5_0>(a, B, s, "matvec_kernel<Q5_0>");
     case MQ_Q5_1: return launch_type<MQ_Q5_1>(a, B, s, "matvec_kernel<Q5_1>");

@@ -113,6 +113,11 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw_dev, bool mmq, cudaStre
 mq_status unpack_weight(const mq_weight *w, uint8_t *raw_dev, cudaStream_t s);
 mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
                         const DeviceState *st);
+// the super-block types' persistent decode matvec (matvec_kq.cu), for weights of at least
+// SMs / 2 row groups of 128 (matvec_kq_applies); launch_matvec dispatches to it
+bool matvec_kq_applies(int64_t N, int sms);
+mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
+                           const DeviceState *st);
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
 // x non-null: the fused form (the kernel quantises x into xq first; cooperative launch)
 // sync non-null: the grid barrier's words there instead of inside xq
@@ -133,6 +138,7 @@ mq_status launch_copy_in(const float *src_view, float *dst, int64_t n, cudaStrea
 int test_fail_launch();
 mq_status init_kernels(DeviceState *st);  // smem opt-ins of the MMQ kernels
 mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
+mq_status init_matvec_kq(DeviceState *st);
 
 // xq buffer layout (mq_act_bytes): q int8 [M][K], s f32 [M][K/32], S int32
 // [M][K/32], q as f16 [M][K], then the transposed block scales sT f32

@@ -116,6 +116,22 @@ def test_matvec_workloads_full(name, B):
     assert_bound(y, yref, bnd, name)
 
 
+@pytest.mark.parametrize("qtype", [12, 13, 14])
+@pytest.mark.parametrize("B", [1, 2, 4, 5, 8])
+def test_matvec_persistent_kernel_several_groups_per_cta(qtype, B):
+    """Weights of at least SMs / 2 row groups run the persistent kernel; at 39000 rows each CTA
+    takes two or three 128-row groups in turn (the last one ragged), and every column of the
+    batch equals the B = 1 call bit for bit."""
+    N, K = 39000, 768
+    W = registered(qtype, N, K, 19)
+    x = synth.activations(B, K, seed=200 + B)
+    y = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 19), N, K, x, parallel=True)
+    assert_bound(y, yref, bnd, f"type {qtype} {N}x{K} B={B}")
+    y1 = gpu_matvec(W, x[B - 1:B])
+    assert np.array_equal(y1[0].view(np.uint32), y[B - 1].view(np.uint32))
+
+
 def test_matvec_batch_columns_equal_single_calls_bitwise():
     c = synth.WORKLOADS["q6_k_matvec_3584x18944"]
     W = registered(c["qtype"], c["N"], c["K"], c["w_seed"])
