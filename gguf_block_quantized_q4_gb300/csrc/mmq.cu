@@ -419,7 +419,6 @@ __global__ void __launch_bounds__(NTHR, 1)
       // grid barrier: every row of x is in xq before any CTA's producer reads it.
       static_assert(sizeof(sm.a) >= (kQGroups * kTtCache + NEPI) * sizeof(float),
                     "prologue scratch fits in the activation ring");
-      static_assert(kQGroups * kQThreads == 32 * NEPI, "the epilogue threads form the groups");
       const int et = threadIdx.x - 128, grp = et / kQThreads, tid = et % kQThreads;
       float *scratch = reinterpret_cast<float *>(&sm.a[0][0]);
       float *ttc = scratch + grp * kTtCache, *wmax = scratch + kQGroups * kTtCache + grp * 4;
@@ -427,9 +426,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       const ActLayout L = act_layout(p.M, K);
       for (int64_t m = int64_t(grp) * gridDim.x + blockIdx.x; m < p.M;
            m += int64_t(gridDim.x) * kQGroups) {
-        quantize_row<kQThreads, 8>(qf.x, qf.xq, m, K, L, ttc, wmax, tid, 1 + grp);
+        quantize_row<kQThreads, 8>(qf.x + m * K, qf.xq, m, K, L, ttc, wmax, tid, 1 + grp);
         asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kQThreads) : "memory");
       }
+      // the scratch in the activation ring is overwritten by the producer's TMA next
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
       __threadfence();
       asm volatile("bar.sync %0, %1;" ::"n"(kBarEpi), "n"(32 * NEPI) : "memory");

@@ -26,8 +26,41 @@ namespace mq {
 
 constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared memory
 
+// rint(fl(x / s)) for s > 0 (f32 division correctly rounded, then round half to even),
+// computed as w = fl(x * r) with r = fl(1 / s), and by the division itself only when w is
+// within 2^-14 of a half-integer (or not below 128 in magnitude, or not finite).  Why that
+// is exact: |r - 1/s| <= 2^-24 / s and |w - x r| <= 2^-24 |x r|, so with |x / s| <= 127
+// (|x| <= amax = 127 s, up to the rounding of s) |w - x/s| < 2^-16, and the quotient
+// v = fl(x / s) has |v - x/s| < 2^-17; so |w - v| < 2^-15.  If every half-integer is at
+// least 2^-14 from w, v lies on the same side of each as w and is not one itself, so both
+// round to the same integer.  (A subnormal s can make r infinite; then w is not finite and
+// the division runs.)
+__device__ __forceinline__ int quant_div_rint(float x, float s, float r) {
+  const float w = __fmul_rn(x, r);
+  const float a = fabsf(w);
+  const float f = a - floorf(a);  // exact: a < 2^24
+  const float v = (fabsf(f - 0.5f) < 0x1p-14f || !(a < 128.0f)) ? __fdiv_rn(x, s) : w;
+  return __float2int_rn(v);
+}
+
+// The loads of one round of a row (PRE passes of NT / 8 blocks from block p0 on): thread
+// tid's float4 of each pass, zeros past the row's end.  xrow: the row in global memory.
+template <int NT, int PRE>
+__device__ __forceinline__ void quant_row_load(const float *__restrict__ xrow, int64_t K,
+                                               int64_t p0, int tid, float4 (&vp)[PRE]) {
+  const int64_t nb = K / 32;
+  const int tb = tid >> 3, sub = tid & 7;
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int64_t b = p0 + (NT / 8) * k + tb;
+    vp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (b < nb) vp[k] = __ldg(reinterpret_cast<const float4 *>(xrow + b * 32) + sub);
+  }
+}
+
+// xrow: row m of x
 template <int NT, int PRE = 4>
-__device__ __forceinline__ void quantize_row(const float *__restrict__ x, uint8_t *__restrict__ xq,
+__device__ __forceinline__ void quantize_row(const float *__restrict__ xrow, uint8_t *__restrict__ xq,
                                              int64_t m, int64_t K, const ActLayout &L, float *ttc,
                                              float *wmax, int tid, int bar) {
   const int64_t nb = K / 32;
@@ -38,12 +71,7 @@ __device__ __forceinline__ void quantize_row(const float *__restrict__ x, uint8_
   constexpr int kPass = NT / 8, kPre = PRE;
   for (int64_t p0 = 0; p0 < nb; p0 += kPass * kPre) {
     float4 vp[kPre];
-#pragma unroll
-    for (int k = 0; k < kPre; ++k) {
-      const int64_t b = p0 + kPass * k + tb;
-      vp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b < nb) vp[k] = __ldg(reinterpret_cast<const float4 *>(x + (m * nb + b) * 32) + sub);
-    }
+    quant_row_load<NT, PRE>(xrow, K, p0, tid, vp);
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
       const int64_t b = p0 + kPass * k + tb;
@@ -58,10 +86,11 @@ __device__ __forceinline__ void quantize_row(const float *__restrict__ x, uint8_
       const float s = __fdiv_rn(mx, 127.0f);
       int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
       if (s != 0.0f) {
-        q0 = min(max(__float2int_rn(__fdiv_rn(v.x, s)), -127), 127);
-        q1 = min(max(__float2int_rn(__fdiv_rn(v.y, s)), -127), 127);
-        q2 = min(max(__float2int_rn(__fdiv_rn(v.z, s)), -127), 127);
-        q3 = min(max(__float2int_rn(__fdiv_rn(v.w, s)), -127), 127);
+        const float r = __frcp_rn(s);
+        q0 = min(max(quant_div_rint(v.x, s, r), -127), 127);
+        q1 = min(max(quant_div_rint(v.y, s, r), -127), 127);
+        q2 = min(max(quant_div_rint(v.z, s, r), -127), 127);
+        q3 = min(max(quant_div_rint(v.w, s, r), -127), 127);
       }
       int S = q0 + q1 + q2 + q3;
       S += __shfl_xor_sync(0xffffffffu, S, 1);
@@ -113,5 +142,6 @@ __device__ __forceinline__ void quantize_row(const float *__restrict__ x, uint8_
     arow[2 * nb + b] = lo;
   }
 }
+
 
 }  // namespace mq

@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(256, 4) quantize_act_kernel(const float *__res
                                                            int64_t K, ActLayout L) {
   __shared__ float ttc[kTtCache];
   __shared__ float wmax[8];
-  quantize_row<256>(x, xq, blockIdx.x, K, L, ttc, wmax, threadIdx.x, -1);
+  quantize_row<256>(x + int64_t(blockIdx.x) * K, xq, blockIdx.x, K, L, ttc, wmax, threadIdx.x, -1);
 }
 
 }  // namespace
