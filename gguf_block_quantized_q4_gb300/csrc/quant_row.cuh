@@ -13,11 +13,12 @@
 // [2^13, 2^14) and the f16 pair (hi, lo) of t~ = s*S / u_m per block, laid out as
 // [hi | hi | lo].
 //
-// A group of NT threads (PRE: passes loaded ahead) (tid = 0..NT-1 within the group) calls it for one row (8 threads per
-// block, 4 elements each, NT / 8 blocks per pass); it synchronises the group once, with
-// __syncthreads when bar < 0 (the group is the whole CTA) and otherwise with the named
-// barrier bar of NT threads.  ttc: shared scratch of kTtCache floats; wmax: shared scratch
-// of NT / 32 floats; both may be reused only after the group's next synchronisation.
+// quantize_row: a group of NT threads (tid = 0..NT-1 within the group) for one row (8
+// threads per block, 4 elements each, NT / 8 blocks per pass, PRE passes loaded at a time);
+// it synchronises the group once, with __syncthreads when bar < 0 (the group is the whole
+// CTA) and otherwise with the named barrier bar of NT threads.  ttc: shared scratch of
+// kTtCache floats; wmax: shared scratch of NT / 32 floats; both may be reused only after
+// the group's next synchronisation.
 #pragma once
 
 #include "mq_common.cuh"
@@ -58,7 +59,83 @@ __device__ __forceinline__ void quant_row_load(const float *__restrict__ xrow, i
   }
 }
 
-// xrow: row m of x
+// One 32-element block of row m: the 8 lanes sub = 0..7 of a group of 8 hold its elements
+// 4 sub .. 4 sub + 3 in v (every lane of the warp takes part in the shuffles; lanes of
+// blocks past the row's end carry zeros and store nothing).  Writes the block's q, f16 q,
+// s, S, and the transposed s and s*S; keeps s*S in ttc (blocks below TTC) and the
+// largest |s*S| in rowmax (lane sub == 0).
+template <int TTC = kTtCache>
+__device__ __forceinline__ void quant_block(const float4 v, int64_t b, bool ok, int64_t m,
+                                            int64_t nb, const ActLayout &L,
+                                            uint8_t *__restrict__ xq, float *ttc, int sub,
+                                            float &rowmax) {
+  const int64_t blk = m * nb + b;  // global block index
+  float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  const float s = __fdiv_rn(mx, 127.0f);
+  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+  if (s != 0.0f) {
+    const float r = __frcp_rn(s);
+    q0 = min(max(quant_div_rint(v.x, s, r), -127), 127);
+    q1 = min(max(quant_div_rint(v.y, s, r), -127), 127);
+    q2 = min(max(quant_div_rint(v.z, s, r), -127), 127);
+    q3 = min(max(quant_div_rint(v.w, s, r), -127), 127);
+  }
+  int S = q0 + q1 + q2 + q3;
+  S += __shfl_xor_sync(0xffffffffu, S, 1);
+  S += __shfl_xor_sync(0xffffffffu, S, 2);
+  S += __shfl_xor_sync(0xffffffffu, S, 4);
+  if (!ok) return;
+  const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
+                          ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+  reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
+  __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+  __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+  uint2 hv;
+  hv.x = *reinterpret_cast<uint32_t *>(&h01);
+  hv.y = *reinterpret_cast<uint32_t *>(&h23);
+  reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
+  if (sub == 0) {
+    const float t = s * (float)S;
+    reinterpret_cast<float *>(xq + L.scale)[blk] = s;
+    reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
+    reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
+    reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
+    if (b < TTC) ttc[b] = t;
+    rowmax = fmaxf(rowmax, fabsf(t));
+  }
+}
+
+// The row's min-term operand, once its maximum |s*S| (mxr) is known: a power of two u_m
+// with mxr / u_m in [2^13, 2^14), and the f16 pair (hi, lo) of s*S / u_m per block, laid out
+// [hi | hi | lo]; threads tid = 0 .. NT - 1 of the row's group share the blocks; s*S from
+// ttc for blocks below TTC, else read back from the xq buffer.
+template <int NT, int TTC = kTtCache>
+__device__ __forceinline__ void quant_row_finish(float mxr, int64_t m, int64_t nb,
+                                                 const ActLayout &L, uint8_t *__restrict__ xq,
+                                                 const float *ttc, int tid) {
+  const int E = (int)((__float_as_uint(mxr) >> 23) & 255);
+  int k = mxr == 0.f ? 0 : E - 140;
+  k = min(max(k, -100), 100);
+  const float inv_u = __int_as_float((127 - k) << 23);
+  if (tid == 0) reinterpret_cast<float *>(xq + L.urow)[m] = __int_as_float((127 + k) << 23);
+  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * min_ld(nb);
+  for (int64_t b = tid; b < nb; b += NT) {
+    const float t =
+        (b < TTC ? ttc[b] : reinterpret_cast<const float *>(xq + L.tt)[b * L.mt + m]) * inv_u;
+    const __half hi = __float2half_rn(t);
+    const __half lo = __float2half_rn(t - __half2float(hi));
+    arow[b] = hi;
+    arow[nb + b] = hi;
+    arow[2 * nb + b] = lo;
+  }
+}
+
+// xrow: row m of x; a group of NT threads (tid = 0 .. NT - 1), PRE passes of NT / 8 blocks
+// loaded at a time.  It synchronises the group once, with __syncthreads when bar < 0 (the
+// group is the whole CTA) and otherwise with the named barrier bar of NT threads.
 template <int NT, int PRE = 4>
 __device__ __forceinline__ void quantize_row(const float *__restrict__ xrow, uint8_t *__restrict__ xq,
                                              int64_t m, int64_t K, const ActLayout &L, float *ttc,
@@ -75,49 +152,10 @@ __device__ __forceinline__ void quantize_row(const float *__restrict__ xrow, uin
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
       const int64_t b = p0 + kPass * k + tb;
-      const bool ok = b < nb;
-      const int64_t blk = m * nb + b;  // global block index
-      // every lane of a warp takes part in the shuffles; out-of-range lanes carry zeros
-      const float4 v = vp[k];
-      float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      const float s = __fdiv_rn(mx, 127.0f);
-      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-      if (s != 0.0f) {
-        const float r = __frcp_rn(s);
-        q0 = min(max(quant_div_rint(v.x, s, r), -127), 127);
-        q1 = min(max(quant_div_rint(v.y, s, r), -127), 127);
-        q2 = min(max(quant_div_rint(v.z, s, r), -127), 127);
-        q3 = min(max(quant_div_rint(v.w, s, r), -127), 127);
-      }
-      int S = q0 + q1 + q2 + q3;
-      S += __shfl_xor_sync(0xffffffffu, S, 1);
-      S += __shfl_xor_sync(0xffffffffu, S, 2);
-      S += __shfl_xor_sync(0xffffffffu, S, 4);
-      if (!ok) continue;
-      const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                              ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-      reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-      __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-      __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-      uint2 hv;
-      hv.x = *reinterpret_cast<uint32_t *>(&h01);
-      hv.y = *reinterpret_cast<uint32_t *>(&h23);
-      reinterpret_cast<uint2 *>(xq + L.op)[blk * 8 + sub] = hv;
-      if (sub == 0) {
-        const float t = s * (float)S;
-        reinterpret_cast<float *>(xq + L.scale)[blk] = s;
-        reinterpret_cast<int32_t *>(xq + L.bsum)[blk] = S;
-        reinterpret_cast<float *>(xq + L.st)[b * L.mt + m] = s;
-        reinterpret_cast<float *>(xq + L.tt)[b * L.mt + m] = t;
-        if (b < kTtCache) ttc[b] = t;
-        rowmax = fmaxf(rowmax, fabsf(t));
-      }
+      quant_block(vp[k], b, b < nb, m, nb, L, xq, ttc, sub, rowmax);
     }
   }
-  // row maximum of |s*S| -> u_m = 2^k with max / u_m in [2^13, 2^14)
+  // row maximum of |s*S|
   rowmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(rowmax)));
   if ((tid & 31) == 0) wmax[tid >> 5] = rowmax;
   if (bar < 0)
@@ -127,21 +165,7 @@ __device__ __forceinline__ void quantize_row(const float *__restrict__ xrow, uin
   float mxr = wmax[0];
 #pragma unroll
   for (int w = 1; w < NT / 32; ++w) mxr = fmaxf(mxr, wmax[w]);
-  const int E = (int)((__float_as_uint(mxr) >> 23) & 255);
-  int k = mxr == 0.f ? 0 : E - 140;
-  k = min(max(k, -100), 100);
-  const float inv_u = __int_as_float((127 - k) << 23);
-  if (tid == 0) reinterpret_cast<float *>(xq + L.urow)[m] = __int_as_float((127 + k) << 23);
-  __half *arow = reinterpret_cast<__half *>(xq + L.amin) + m * min_ld(nb);
-  for (int64_t b = tid; b < nb; b += NT) {
-    const float t = (b < kTtCache ? ttc[b] : reinterpret_cast<const float *>(xq + L.tt)[b * L.mt + m]) * inv_u;
-    const __half hi = __float2half_rn(t);
-    const __half lo = __float2half_rn(t - __half2float(hi));
-    arow[b] = hi;
-    arow[nb + b] = hi;
-    arow[2 * nb + b] = lo;
-  }
+  quant_row_finish<NT>(mxr, m, nb, L, xq, ttc, tid);
 }
-
 
 }  // namespace mq

@@ -223,6 +223,10 @@ def test_quantize_workloads_bit_exact(name, M):
 
 @pytest.mark.parametrize("M,K", [(1, 32), (7, 96), (65, 288), (3, 4096)])
 def test_quantize_small_and_edge_blocks(M, K):
+    quantize_edge_blocks(M, K)
+
+
+def quantize_edge_blocks(M, K):
     x = synth.activations(M, K, seed=M * 7 + K)
     x[0, :32] = 0.0                                   # s = 0 block
     if K >= 64:
