@@ -88,6 +88,7 @@ struct TcArgs {
   int64_t M, N, mt, np;
   int nb;
   int ntm, ntiles;      // output tiles: ntm along M (fastest), ntiles in all
+  int mt0;              // first M-tile (a call over M-tiles mt0 .. mt0 + ntm - 1)
   int nms;              // ring stages of the min-term GEMM (3*nb/64 rounded up), or 0
   int *status;
   int debug_expire;
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       // whose c-th stage is ring stage (U % 2) + 2 * (c % SR), round c / SR.
       int c0 = 0, c1 = 0;
       for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
-        const int m0 = (t % p.ntm) * TM, n0 = (t / p.ntm) * TN;
+        const int m0 = (p.mt0 + t % p.ntm) * TM, n0 = (t / p.ntm) * TN;
         for (int f = 0; f < npairs + nms; ++f) {
           const int pr = f < npairs ? f : -1;
           const int i = (tl * nuse + (f < npairs ? f : npairs + ((f - npairs) & 1))) & 1;
@@ -446,7 +447,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     // test hook: a wait that never completes, before the first accumulator use
     if (p.debug_expire) mbar_wait(sa(&sm.never), 0, p.status, 9, kTestWaitNs);
     for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
-    const int64_t m0 = int64_t(t % p.ntm) * TM, n0 = int64_t(t / p.ntm) * TN;
+    const int64_t m0 = int64_t(p.mt0 + t % p.ntm) * TM, n0 = int64_t(t / p.ntm) * TN;
     const int64_t m = m0 + rl;
     const bool mok = m < p.M;
     // accumulators as f32 pairs: one packed fma.rn.f32x2 per two columns
@@ -751,7 +752,7 @@ mq_status init_kernels(DeviceState *st) {
 
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
                      cudaStream_t s, const DeviceState *st, int debug_expire, const float *x,
-                     unsigned *sync) {
+                     unsigned *sync, int64_t mt_begin, int64_t mt_count) {
   const ActLayout L = act_layout(M, W->K);
   const uint8_t *base = reinterpret_cast<const uint8_t *>(xq);
   alignas(64) CUtensorMap tA, tAm;
@@ -786,7 +787,13 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   a.mt = L.mt;
   a.np = W->np;
   a.nb = (int)(W->K / 32);
-  const int64_t ntm = (M + TM - 1) / TM, ntn = (W->N + TN - 1) / TN;
+  const int64_t mt_all = (M + TM - 1) / TM, ntn = (W->N + TN - 1) / TN;
+  const int64_t ntm = mt_count < 0 ? mt_all : mt_count;
+  if (mt_begin < 0 || ntm < 1 || mt_begin + ntm > mt_all || (x != nullptr && ntm != mt_all))
+    return fail(MQ_ERR_ARG, "mq_mmq: M-tiles %lld .. %lld outside the %lld of M=%lld",
+                (long long)mt_begin, (long long)(mt_begin + ntm), (long long)mt_all,
+                (long long)M);
+  a.mt0 = (int)mt_begin;
   if (ntm * ntn > 0x7fffffff / 2)
     return fail(MQ_ERR_SHAPE, "mq_mmq: %lld x %lld output tiles are too many", (long long)ntm,
                 (long long)ntn);

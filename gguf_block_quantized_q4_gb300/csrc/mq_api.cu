@@ -126,6 +126,9 @@ extern "C" mq_status mq_init(int device) {
   CK(cudaMalloc(&st->status, 64), site);
   CK(cudaMemset(st->status, 0, 64), site);
   CK(cudaStreamCreateWithFlags(&st->reg_stream, cudaStreamNonBlocking), site);
+  CK(cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking), site);
+  CK(cudaEventCreateWithFlags(&st->ev_rows, cudaEventDisableTiming), site);
+  CK(cudaEventCreateWithFlags(&st->ev_copied, cudaEventDisableTiming), site);
   mq_status s = init_kernels(st);
   if (s == MQ_OK) s = init_matvec(st);
   // the static scratch of mq_mmq_fused_static: looking its address up here loads this file's
@@ -140,6 +143,9 @@ extern "C" mq_status mq_init(int device) {
     // another thread finished first; keep its state
     cudaFree(st->status);
     cudaStreamDestroy(st->reg_stream);
+    cudaStreamDestroy(st->copy_stream);
+    cudaEventDestroy(st->ev_rows);
+    cudaEventDestroy(st->ev_copied);
     delete st;
   } else {
     g_devs[device] = st;
@@ -572,6 +578,7 @@ extern "C" mq_status mq_mmq_fused(mq_type type, const mq_weight *W, const float 
 // up once per device, by mq_init; nothing is allocated.
 static __device__ __align__(256) uint8_t g_static_xq[MQ_STATIC_XQ_BYTES];
 static std::mutex g_static_mu;
+static std::mutex g_host_mu;  // mq_mmq_host's enqueue sequence (shared events)
 
 static mq_status static_scratch(DeviceState *st, uint8_t **out, const char *site) {
   std::lock_guard<std::mutex> lk(g_static_mu);
@@ -632,9 +639,30 @@ extern "C" mq_status mq_mmq_host(mq_type type, const mq_weight *W, const float *
   if (!xv)
     CK(cudaMemcpyAsync(x_dev, x_host, size_t(M) * K * 4, cudaMemcpyHostToDevice, cs), site);
   if ((s = launch_quantize(xv ? xv : x_dev, xq_dev, M, K, cs)) != MQ_OK) return s;
-  if ((s = launch_mmq(W, xq_dev, y_dev, nullptr, M, cs, st, test_expire_wait())) != MQ_OK)
-    return s;
-  CK(cudaMemcpyAsync(y_host, y_dev, size_t(M) * N * 4, cudaMemcpyDeviceToHost, cs), site);
+  // The MMQ in chunks of M-tiles (128 rows) on the caller's stream; each chunk's rows of y
+  // go back to the host on the library's copy stream while the next chunk runs (the host
+  // link, not the MMQ, bounds the call: Q4_K 512 x 18944 x 3584, 361 -> 305 us).  The copy
+  // stream rejoins the caller's stream at the end, so the call stays asynchronous and
+  // ordered on `stream`.  One enqueue sequence at a time per device (the two events are
+  // shared).  Quantising per chunk as well measured slower (316 us): its reads of x then
+  // share the host link with the copies of y.
+  const int64_t mts = (M + 127) / 128;
+  const int64_t chunks = mts < 4 ? mts : 4, per = (mts + chunks - 1) / chunks;
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  for (int64_t c0 = 0; c0 < mts; c0 += per) {
+    const int64_t cn = mts - c0 < per ? mts - c0 : per;
+    const int64_t r0 = c0 * 128, r1 = (c0 + cn) * 128 < M ? (c0 + cn) * 128 : M;
+    if ((s = launch_mmq(W, xq_dev, y_dev, nullptr, M, cs, st, test_expire_wait(), nullptr,
+                        nullptr, c0, cn)) != MQ_OK)
+      return s;
+    CK(cudaEventRecord(st->ev_rows, cs), site);
+    CK(cudaStreamWaitEvent(st->copy_stream, st->ev_rows, 0), site);
+    CK(cudaMemcpyAsync(y_host + r0 * N, y_dev + r0 * N, size_t(r1 - r0) * N * 4,
+                       cudaMemcpyDeviceToHost, st->copy_stream),
+       site);
+  }
+  CK(cudaEventRecord(st->ev_copied, st->copy_stream), site);
+  CK(cudaStreamWaitEvent(cs, st->ev_copied, 0), site);
   return MQ_OK;
 }
 

@@ -104,6 +104,9 @@ struct DeviceState {
   int *status = nullptr;  // device status word for bounded waits (code, kernel id)
   cudaStream_t reg_stream = nullptr;
   uint8_t *static_xq = nullptr;  // mq_mmq_fused_static's scratch (device symbol address)
+  // mq_mmq_host: the stream that copies y back while the MMQ's next rows run, and its events
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_rows = nullptr, ev_copied = nullptr;
 };
 DeviceState *device_state(int dev);  // nullptr if mq_init(dev) was not called
 mq_status current_state(DeviceState **st, const char *site);
@@ -121,9 +124,12 @@ mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, 
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
 // x non-null: the fused form (the kernel quantises x into xq first; cooperative launch)
 // sync non-null: the grid barrier's words there instead of inside xq
+// mt_begin, mt_count: only the output rows of M-tiles (128 rows) mt_begin .. + mt_count - 1
+// (mt_count < 0: all; the fused form takes all)
 mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, int64_t M,
                      cudaStream_t s, const DeviceState *st, int debug_expire,
-                     const float *x = nullptr, unsigned *sync = nullptr);
+                     const float *x = nullptr, unsigned *sync = nullptr, int64_t mt_begin = 0,
+                     int64_t mt_count = -1);
 mq_status encode_weight_maps(mq_weight *w);  // TMA descriptors of the prefill planes
 // Host-buffer transfers (host_io.cu).  host_device_view: the device view of p if p is
 // page-locked host memory that this device can map and both p and its view are aligned to

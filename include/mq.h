@@ -214,7 +214,11 @@ mq_status mq_mmq(mq_type type, const mq_weight *W, const void *xq, float *y, int
  *     prefill's quantiser reads x_host itself (x_dev is not written);
  *   - any other host buffer, and the prefill's y always, goes through x_dev / y_dev with
  *     cudaMemcpyAsync copies (synchronous with the host for pageable memory, as CUDA
- *     defines them).
+ *     defines them).  The prefill's MMQ runs in up to four chunks of 128-row tiles, and
+ *     each chunk's rows of y are copied back on a stream the library owns (created by
+ *     mq_init) while the next chunk runs; that stream waits on events recorded on `stream`
+ *     and `stream` waits on it before the call returns, so the work stays ordered on
+ *     `stream` (also when `stream` is being captured into a CUDA graph).
  * The results are identical on both routes.  Host pointers that CUDA reports as device
  * memory are refused (MQ_ERR_ARG); the rest is validated as mq_matvec / mq_mmq, all before
  * anything is enqueued.  The device reads the activations as f32, as in the decisions
