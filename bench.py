@@ -151,6 +151,15 @@ def src_sha(paths):
     return h.hexdigest()[:16]
 
 
+def matvec_kernel_name(qtype, n, sms):
+    """The matvec kernel the library launches for a weight of this type and row count: the
+    persistent kernel for Q4_K / Q5_K / Q6_K weights of at least sms / 2 row groups of 128,
+    else the split-K kernel."""
+    import synth
+    persistent = qtype in (12, 13, 14) and (n + 127) // 128 * 2 >= sms
+    return ("matvec_kq_kernel" if persistent else "matvec_kernel") + f"<{synth.TYPE_NAME[qtype]}>"
+
+
 def traffic_for(kernel_key, src):
     """DRAM bytes per launch from a committed ncu summary (profiles/traffic.txt: lines of
     `key dram_bytes_per_launch source_sha`), if the kernel source is unchanged since the
@@ -496,6 +505,8 @@ def measure_configs(mq, dev, hbm, bf16):
         be, bb = synth.BLOCK[qtype]
         return n * (k // be) * bb + b * k * 4 + b * n * 4
 
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
     def matvec_case(name, batches, rotate=True):
         c = WL[name]
         qt, n, k = c["qtype"], c["N"], c["K"]
@@ -509,7 +520,7 @@ def measure_configs(mq, dev, hbm, bf16):
             t = graph_time_ms(lambda j: mq.matvec(Ws[j % rot], x, ys[j % rot]),
                               max(8, 2 * rot) if rot > 1 else 20)
             by = mv_bytes(qt, n, k, b)
-            res[b] = roof(("matvec_kq_kernel" if qt in (12, 13, 14) else "matvec_kernel") + f"<{synth.TYPE_NAME[qt]}>", "hbm", by / (t * 1e-3) / 1e9,
+            res[b] = roof(matvec_kernel_name(qt, n, sms), "hbm", by / (t * 1e-3) / 1e9,
                           hbm, "GB/s", t, by)
             res[b]["weight_copies_rotated"] = rot
         return Ws, res
@@ -717,12 +728,14 @@ def run_mq(args):
     csrc = os.path.join(ROOT, "gguf_block_quantized_q4_gb300", "csrc")
     kern = {
         "matvec": roof("matvec_kq_kernel<Q4_K>", "hbm", mv_gbs, hbm, "GB/s", t_mv, MV_BYTES,
-                       traffic_for("matvec_q4_k_b1", os.path.join(csrc, "matvec.cu"))),
+                       traffic_for("matvec_q4_k_b1", [os.path.join(csrc, "matvec_kq.cu"),
+                                                      os.path.join(csrc, "mv_device.cuh")])),
         "quantize": roof("quantize_act_kernel", "hbm", q_gbs, hbm, "GB/s", t_q, Q_BYTES,
                          traffic_for("quantize_m512", [os.path.join(csrc, "quantize.cu"),
                                                        os.path.join(csrc, "quant_row.cuh")])),
         "mmq": roof("mmq_tc_kernel<Q4_K>", "tensor", mm_tops, bf16, "TFLOP/s", t_mm, MMQ_OPS,
-                    traffic_for("mmq_q4_k_m512", os.path.join(csrc, "mmq.cu")),
+                    traffic_for("mmq_q4_k_m512", [os.path.join(csrc, "mmq.cu"),
+                                                  os.path.join(csrc, "quant_row.cuh")]),
                     note=MMQ_PEAK_NOTE),
     }
     dom = max(kern, key=lambda k: kern[k]["ms"])
