@@ -351,14 +351,15 @@ def profile_calls(kernel: str, calls: int, batch=None):
         for _ in range(calls):
             mq.matvec(W, x, y)
     else:
-        x = torch.from_numpy(synth.activations(M, K, XA_SEED)).cuda()
+        m = batch or M  # activation rows (the K = 3584 quantiser of C5 at --batch 2048)
+        x = torch.from_numpy(synth.activations(m, K, XA_SEED)).cuda()
         xq = mq.quantize_act(x)
-        y = torch.empty((M, N), device="cuda")
+        y = torch.empty((m, N), device="cuda")
         for _ in range(calls):
             if kernel == "quantize":
                 mq.quantize_act(x, xq)
             else:
-                mq.mmq(W, xq, M, y)
+                mq.mmq(W, xq, m, y)
     torch.cuda.synchronize()
     mq.stream_status()
     W.free()
@@ -778,7 +779,9 @@ def run_mq(args):
                 "note": "eager calls of the C ABI with pinned host buffers (mq_matvec_host: "
                         "x pulled over the host link by a copy kernel that the matvec overlaps, "
                         "y stored by the matvec into host memory; mq_mmq_host: the quantiser "
-                        "reads x from host memory, MMQ, D2H copy of y), device time per step "
+                        "reads x from host memory, then the MMQ in up to four chunks of 128-row "
+                        "tiles, each chunk's rows of y copied to the host while the next chunk "
+                        "runs), device time per step "
                         "between events, medians"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
@@ -804,14 +807,17 @@ def main():
     ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
                     help="profiling mode: only run --calls launches of this kernel")
     ap.add_argument("--calls", type=int, default=3)
-    ap.add_argument("--batch", type=int, choices=range(1, 9), default=None,
-                    help="profiling mode, matvec: batch rows (default: the bench's decode batch)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling mode: the matvec's batch rows (1..8), or the quantiser's and "
+                         "MMQ's activation rows (default: the bench's decode batch / prefill M)")
     ap.add_argument("--chain", type=int, default=0,
                     help="time a decode chain of this many small matvecs, eager and graphed")
     ap.add_argument("--ffn-gu", action="store_true",
                     help="time the fused gate/up matvec and MMQ against two plain calls")
     args = ap.parse_args()
     if args.kernel:
+        if args.batch is not None and not (1 <= args.batch <= (8 if args.kernel == "matvec" else 4096)):
+            ap.error("--batch: 1..8 for the matvec, 1..4096 for the quantiser and the MMQ")
         return profile_calls(args.kernel, args.calls, args.batch)
     if args.chain:
         return chain_timing(args.chain)
