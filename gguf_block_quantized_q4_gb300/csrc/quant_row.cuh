@@ -27,21 +27,27 @@ namespace mq {
 
 constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared memory
 
-// rint(fl(x / s)) for s > 0 (f32 division correctly rounded, then round half to even),
-// computed as w = fl(x * r) with r = fl(1 / s), and by the division itself only when w is
-// within 2^-14 of a half-integer (or not below 128 in magnitude, or not finite).  Why that
-// is exact: |r - 1/s| <= 2^-24 / s and |w - x r| <= 2^-24 |x r|, so with |x / s| <= 127
-// (|x| <= amax = 127 s, up to the rounding of s) |w - x/s| < 2^-16, and the quotient
+// q = clamp(rint(fl(x / s)), -127, 127) for s > 0 (f32 division correctly rounded, then
+// round half to even), returned as the binary32 value t = 1.5 * 2^23 + q: its low byte is q
+// as int8, its bits less those of 1.5 * 2^23 are q, and t - 1.5 * 2^23 is q as a float.
+// Computed as w = fl(x * r) with r = fl(1 / s), rounded to an integer by adding 1.5 * 2^23
+// (ties to even, exact for |w| < 2^22), and by the division itself only when w is within
+// 2^-14 of a half-integer (its residual d = w - rint(w), exact, has |d| >= 1/2 - 2^-14), or
+// |w| >= 127.25, or w is not finite.  Why that is exact: |r - 1/s| <= 2^-24 / s and
+// |w - x r| <= 2^-24 |x r|, so with |x / s| <= 127.25 |w - x/s| < 2^-16, and the quotient
 // v = fl(x / s) has |v - x/s| < 2^-17; so |w - v| < 2^-15.  If every half-integer is at
 // least 2^-14 from w, v lies on the same side of each as w and is not one itself, so both
-// round to the same integer.  (A subnormal s can make r infinite; then w is not finite and
-// the division runs.)
-__device__ __forceinline__ int quant_div_rint(float x, float s, float r) {
+// round to the same integer, which is within [-127, 127].  (A subnormal s can make r
+// infinite; then w is not finite and the division runs.)
+constexpr float kQuantMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kQuantMagicBits = 0x4B400000;
+__device__ __forceinline__ float quant_code(float x, float s, float r) {
   const float w = __fmul_rn(x, r);
-  const float a = fabsf(w);
-  const float f = a - floorf(a);  // exact: a < 2^24
-  const float v = (fabsf(f - 0.5f) < 0x1p-14f || !(a < 128.0f)) ? __fdiv_rn(x, s) : w;
-  return __float2int_rn(v);
+  const float t = __fadd_rn(w, kQuantMagic);
+  const float d = __fsub_rn(w, __fsub_rn(t, kQuantMagic));
+  if (fabsf(d) < 0.5f - 0x1p-14f && fabsf(w) < 127.25f) return t;
+  const int q = min(max(__float2int_rn(__fdiv_rn(x, s)), -127), 127);
+  return __fadd_rn((float)q, kQuantMagic);
 }
 
 // The loads of one round of a row (PRE passes of NT / 8 blocks from block p0 on): thread
@@ -75,24 +81,27 @@ __device__ __forceinline__ void quant_block(const float4 v, int64_t b, bool ok, 
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
   const float s = __fdiv_rn(mx, 127.0f);
-  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+  float t0 = kQuantMagic, t1 = kQuantMagic, t2 = kQuantMagic, t3 = kQuantMagic;  // q = 0
   if (s != 0.0f) {
     const float r = __frcp_rn(s);
-    q0 = min(max(quant_div_rint(v.x, s, r), -127), 127);
-    q1 = min(max(quant_div_rint(v.y, s, r), -127), 127);
-    q2 = min(max(quant_div_rint(v.z, s, r), -127), 127);
-    q3 = min(max(quant_div_rint(v.w, s, r), -127), 127);
+    t0 = quant_code(v.x, s, r);
+    t1 = quant_code(v.y, s, r);
+    t2 = quant_code(v.z, s, r);
+    t3 = quant_code(v.w, s, r);
   }
-  int S = q0 + q1 + q2 + q3;
+  const int i0 = __float_as_int(t0), i1 = __float_as_int(t1), i2 = __float_as_int(t2),
+            i3 = __float_as_int(t3);
+  int S = (i0 + i1) + (i2 + i3) - 4 * kQuantMagicBits;
   S += __shfl_xor_sync(0xffffffffu, S, 1);
   S += __shfl_xor_sync(0xffffffffu, S, 2);
   S += __shfl_xor_sync(0xffffffffu, S, 4);
   if (!ok) return;
-  const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                          ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+  // the low bytes of t0..t3 are q0..q3 as int8
+  const uint32_t packed =
+      __byte_perm(__byte_perm(i0, i1, 0x0040u), __byte_perm(i2, i3, 0x0040u), 0x5410u);
   reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-  __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-  __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+  __half2 h01 = __floats2half2_rn(__fsub_rn(t0, kQuantMagic), __fsub_rn(t1, kQuantMagic));
+  __half2 h23 = __floats2half2_rn(__fsub_rn(t2, kQuantMagic), __fsub_rn(t3, kQuantMagic));
   uint2 hv;
   hv.x = *reinterpret_cast<uint32_t *>(&h01);
   hv.y = *reinterpret_cast<uint32_t *>(&h23);
