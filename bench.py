@@ -331,9 +331,10 @@ def graph_time_ms(fn, calls, trials=5):
     return statistics.median(out)
 
 
-def profile_calls(kernel: str, calls: int, batch=None):
-    """Run `calls` launches of one hot-path kernel on the bench workload and exit: the
-    program that ncu captures are taken of (one kernel, few launches, ~0.3 GB on device)."""
+def profile_calls(kernel: str, calls: int, batch=None, workload=None):
+    """Run `calls` launches of one hot-path kernel on the bench workload (or on the weight
+    of another named workload) and exit: the program that ncu captures are taken of (one
+    kernel, few launches, ~0.3 GB on device)."""
     import torch
 
     import gguf_block_quantized_q4_gb300 as mq
@@ -341,20 +342,24 @@ def profile_calls(kernel: str, calls: int, batch=None):
     import synth
     mqbuild.build()
     mq.init(0)
-    Wb = synth.weights(QTYPE, N, K, W_SEED)
+    qt, n, k, ws, xs = QTYPE, N, K, W_SEED, XD_SEED
+    if workload:
+        c = synth.WORKLOADS[workload]
+        qt, n, k, ws, xs = c["qtype"], c["N"], c["K"], c["w_seed"], c["x_seed"]
+    Wb = synth.weights(qt, n, k, ws)
     flags = mq.REG_NO_MMQ_PLANE if kernel == "matvec" else mq.REG_DEFAULT
-    W = mq.register_weight(QTYPE, Wb, N, K, flags)
+    W = mq.register_weight(qt, Wb, n, k, flags)
     if kernel == "matvec":
         nb = batch or B
-        x = torch.from_numpy(synth.activations(nb, K, XD_SEED)).cuda()
-        y = torch.empty((nb, N), device="cuda")
+        x = torch.from_numpy(synth.activations(nb, k, xs)).cuda()
+        y = torch.empty((nb, n), device="cuda")
         for _ in range(calls):
             mq.matvec(W, x, y)
     else:
         m = batch or M  # activation rows (the K = 3584 quantiser of C5 at --batch 2048)
-        x = torch.from_numpy(synth.activations(m, K, XA_SEED)).cuda()
+        x = torch.from_numpy(synth.activations(m, k, XA_SEED)).cuda()
         xq = mq.quantize_act(x)
-        y = torch.empty((m, N), device="cuda")
+        y = torch.empty((m, n), device="cuda")
         for _ in range(calls):
             if kernel == "quantize":
                 mq.quantize_act(x, xq)
@@ -807,6 +812,9 @@ def main():
     ap.add_argument("--kernel", choices=["matvec", "quantize", "mmq"],
                     help="profiling mode: only run --calls launches of this kernel")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--workload", default=None,
+                    help="profiling mode: the weight of this named workload instead of the "
+                         "bench's (e.g. q6_k_matvec_3584x18944)")
     ap.add_argument("--batch", type=int, default=None,
                     help="profiling mode: the matvec's batch rows (1..8), or the quantiser's and "
                          "MMQ's activation rows (default: the bench's decode batch / prefill M)")
@@ -818,7 +826,11 @@ def main():
     if args.kernel:
         if args.batch is not None and not (1 <= args.batch <= (8 if args.kernel == "matvec" else 4096)):
             ap.error("--batch: 1..8 for the matvec, 1..4096 for the quantiser and the MMQ")
-        return profile_calls(args.kernel, args.calls, args.batch)
+        if args.workload is not None:
+            import synth
+            if args.workload not in synth.WORKLOADS:
+                ap.error(f"--workload: one of {', '.join(synth.WORKLOADS)}")
+        return profile_calls(args.kernel, args.calls, args.batch, args.workload)
     if args.chain:
         return chain_timing(args.chain)
     if args.ffn_gu:

@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmq.so")
-SOURCES = ["mq_api.cu", "repack.cu", "matvec.cu", "matvec_kq.cu", "quantize.cu", "mmq.cu",
-           "host_io.cu"]
+SOURCES = ["mq_api.cu", "repack.cu", "matvec.cu", "matvec_kq.cu", "xplane.cu", "quantize.cu",
+           "mmq.cu", "host_io.cu"]
 HEADERS = [os.path.join(CSRC, "mq_common.cuh"), os.path.join(CSRC, "quant_row.cuh"),
            os.path.join(CSRC, "mv_device.cuh"),
            os.path.join(ROOT, "include", "mq.h")]

@@ -93,6 +93,9 @@ struct KqArgs {
   int64_t groups;
   int swiglu;
   int *status;
+  // the activation fragment plane of this call (xplane.cu), or nullptr: the x warps convert
+  // x themselves
+  const uint8_t *xp;
 };
 
 template <int TYPE>
@@ -119,12 +122,14 @@ struct KqSmem {
   alignas(128) uint8_t w[NS][kq_tile_bytes<TYPE>()];  // weight tiles
   // B fragments, each group padded by 8 words (consecutive groups 8 banks apart)
   alignas(16) uint2 frag[kFS][FG][NT][32 + (NT == 1 ? 4 : 2)];
-  float unscale[kFS][8];                  // 2^-e per batch row of the slot's chunk
+  alignas(16) float unscale[kFS][8];      // 2^-e per batch row of the slot's chunk
   alignas(16) float xr[kq_xwarps<NT>()][kXS][kq_xrows<NT>()][kChunk];  // x staging rings
   KqTab<TYPE> tab[kCompute];
   float xs[kq_xwarps<NT>()][kq_xrows<NT>()][8];  // x-warp scratch: sub-block sums
   float xch[2][kTeam][32][2 * NT];         // team 1 -> team 0 partial sums, by unit parity
   uint64_t wfull[NS], wempty[NS], ffull[kFS], fempty[kFS], pfull[kTeam][2], pempty[kTeam][2];
+  static_assert(sizeof(frag[0]) == FG * xp_group_bytes(NT),
+                "a fragment slot must have the activation fragment plane's layout");
 };
 
 template <int TYPE, int NT>
@@ -305,6 +310,29 @@ __device__ __noinline__ void kq_stage_x(KqSmem<TYPE, NT> &sm, const KqArgs &p, i
     advance(cq);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// With an activation fragment plane: lane 0 of the x warp of row slice 0 and chunk parity
+// par copies the fragments and unscale factors of this parity's chunks into their fragment
+// slots (one bulk-copy transaction per slot), once the team is done with the slot.
+template <int TYPE, int NT>
+__device__ __noinline__ void kq_copy_plane(KqSmem<TYPE, NT> &sm, const KqArgs &p, int par) {
+  constexpr uint32_t FB = KqSmem<TYPE, NT>::FG * xp_group_bytes(NT);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the plane comes from the previous kernel
+  int i = 0;
+  Unit un;
+  for (int u = 0; unit_at(p, u, un); ++u) {
+    for (int c = un.cb; c < un.ce; ++c, ++i) {
+      if ((i & 1) != par) continue;
+      const int fs = i % kFS;
+      if (i >= kFS) mbar_wait(sa(&sm.fempty[fs]), ((i / kFS) - 1) & 1, p.status, 38);
+      const uint32_t bar = sa(&sm.ffull[fs]);
+      mbar_arrive_tx(bar, FB + 32u);
+      const uint8_t *src = p.xp + int64_t(c) * xp_chunk_bytes(NT);
+      bulk_1d(sa(&sm.frag[fs][0][0][0]), src, FB, bar);
+      bulk_1d(sa(&sm.unscale[fs][0]), src + xp_off_unscale(NT), 32u, bar);
+    }
+  }
 }
 
 // Every lane releases the weight stage after its own reads of it (the stage's "empty"
@@ -556,8 +584,9 @@ __global__ void __launch_bounds__(kq_threads<NT>(), 1) matvec_kq_kernel(const Kq
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
-  // fragment columns of absent batch rows stay zero (never read for stored outputs)
-  {
+  // fragment columns of absent batch rows stay zero (never read for stored outputs); with an
+  // activation fragment plane the slots are filled by bulk copies alone (zeros included)
+  if (!p.xp) {
     uint4 *f = reinterpret_cast<uint4 *>(&sm.frag[0][0][0][0]);
     constexpr int n16 = (int)(sizeof(sm.frag) / 16);
     for (int i = tid; i < n16; i += kq_threads<NT>()) f[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -570,11 +599,11 @@ __global__ void __launch_bounds__(kq_threads<NT>(), 1) matvec_kq_kernel(const Kq
                    "r"(32 * kTeam));  // every lane of the consuming team
     }
     // a slot is filled by the x warps of its chunk parity that have batch rows (the others
-    // return at once)
+    // return at once); with a plane, by one bulk-copy transaction
     const int xlive = min((p.B + kq_xrows<NT>() - 1) / kq_xrows<NT>(), kq_xwarps<NT>() / 2);
     for (int f = 0; f < kFS; ++f) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.ffull[f])),
-                   "r"(32 * xlive));
+                   "r"(p.xp ? 1 : 32 * xlive));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.fempty[f])),
                    "r"(32 * kTeam));
     }
@@ -593,7 +622,10 @@ __global__ void __launch_bounds__(kq_threads<NT>(), 1) matvec_kq_kernel(const Kq
     if (lane == 0) kq_copies<TYPE, NT>(sm, p);
   } else if (warp >= kCompute) {  // x warp (row slice, chunk parity)
     const int xw = kq_xwarp_index(warp);
-    kq_stage_x<TYPE, NT>(sm, p, lane, xw >> 1, xw & 1);
+    if (!p.xp)
+      kq_stage_x<TYPE, NT>(sm, p, lane, xw >> 1, xw & 1);
+    else if ((xw >> 1) == 0 && lane == 0)
+      kq_copy_plane<TYPE, NT>(sm, p, xw & 1);
   } else {
     const int team = warp / kTeam, wq = warp % kTeam;
     // Lane (g, t) feeds column g of each n8 tile, i.e. batch row 4i + g/2.  Lanes of absent
@@ -717,6 +749,7 @@ bool matvec_kq_applies(int64_t N, int sms) { return (N + kRows - 1) / kRows * 2 
 mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
                            const DeviceState *st) {
   KqArgs a;
+  a.xp = nullptr;
   a.q = W->q;
   a.x = x;
   a.y = y;
@@ -729,17 +762,52 @@ mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, 
   a.swiglu = W->ffn_gu;
   a.status = st->status;
   const bool two = B > 4;
-  switch (W->type) {
-    case MQ_Q4_K:
-      return two ? kq_launch_one<MQ_Q4_K, 2>(a, grid, s, "matvec_kq_kernel<Q4_K>")
-                 : kq_launch_one<MQ_Q4_K, 1>(a, grid, s, "matvec_kq_kernel<Q4_K>");
-    case MQ_Q5_K:
-      return two ? kq_launch_one<MQ_Q5_K, 2>(a, grid, s, "matvec_kq_kernel<Q5_K>")
-                 : kq_launch_one<MQ_Q5_K, 1>(a, grid, s, "matvec_kq_kernel<Q5_K>");
-    default:
-      return two ? kq_launch_one<MQ_Q6_K, 2>(a, grid, s, "matvec_kq_kernel<Q6_K>")
-                 : kq_launch_one<MQ_Q6_K, 1>(a, grid, s, "matvec_kq_kernel<Q6_K>");
+  if (!two) {
+    switch (W->type) {
+      case MQ_Q4_K: return kq_launch_one<MQ_Q4_K, 1>(a, grid, s, "matvec_kq_kernel<Q4_K>");
+      case MQ_Q5_K: return kq_launch_one<MQ_Q5_K, 1>(a, grid, s, "matvec_kq_kernel<Q5_K>");
+      default: return kq_launch_one<MQ_Q6_K, 1>(a, grid, s, "matvec_kq_kernel<Q6_K>");
+    }
   }
+  // Q4_K / Q5_K with two tiles (B = 5..8): x converted once into the activation fragment
+  // plane, a per-call buffer from the device's stream-ordered pool (freed in stream order
+  // after the matvec; in a captured graph, an allocation node and a free node), instead of by
+  // the four x warps of every CTA, which also form the min-term sums of these types.
+  // Measured at 18944 x 3584: Q4_K B = 5 / 8 16.6 / 17.9 -> 15.0 / 15.0 us, Q5_K 18.9 / 20.3
+  // -> 17.9 / 18.0 us.  Where the x warps' work is lighter, the plane's extra launch costs
+  // more than it saves: Q6_K B = 5 / 8 17.5 / 18.6 -> 19.0 / 19.0 us; with one tile (B <= 4)
+  // Q4_K B = 3 / 4 11.9 / 12.6 -> 13.4 / 13.0 us; the split-K kernel of narrow weights
+  // (Q6_K 3584 x 18944) B = 3..5 1.5-1.9 us slower, B = 8 23.6 -> 23.3 us.  Without the
+  // pool, or if the allocation is refused, the x warps convert x themselves (the same
+  // fragments).
+  uint8_t *xp = nullptr;
+  if (st->xpool && W->type != MQ_Q6_K) {
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&xp), xplane_bytes(B, W->K), st->xpool,
+                                s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      xp = nullptr;
+    } else {
+      const mq_status r = launch_xplane(x, B, W->K, xp, s);
+      if (r != MQ_OK) {
+        (void)cudaFreeAsync(xp, s);
+        return r;
+      }
+    }
+  }
+  a.xp = xp;
+  mq_status r;
+  switch (W->type) {
+    case MQ_Q4_K: r = kq_launch_one<MQ_Q4_K, 2>(a, grid, s, "matvec_kq_kernel<Q4_K>"); break;
+    case MQ_Q5_K: r = kq_launch_one<MQ_Q5_K, 2>(a, grid, s, "matvec_kq_kernel<Q5_K>"); break;
+    default: r = kq_launch_one<MQ_Q6_K, 2>(a, grid, s, "matvec_kq_kernel<Q6_K>"); break;
+  }
+  if (xp) {
+    const cudaError_t e = cudaFreeAsync(xp, s);
+    if (e != cudaSuccess && r == MQ_OK)
+      r = fail(MQ_ERR_CUDA, "release of the activation fragment plane failed: %s",
+               cudaGetErrorName(e));
+  }
+  return r;
 }
 
 }  // namespace mq

@@ -129,6 +129,22 @@ extern "C" mq_status mq_init(int device) {
   CK(cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking), site);
   CK(cudaEventCreateWithFlags(&st->ev_rows, cudaEventDisableTiming), site);
   CK(cudaEventCreateWithFlags(&st->ev_copied, cudaEventDisableTiming), site);
+  {
+    // the activation fragment planes of the persistent matvec's two-tile calls: a
+    // stream-ordered pool of this device that keeps up to 64 MB reserved between calls (a
+    // plane takes 36 bytes per element of K); without it the x warps convert x themselves
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    if (cudaMemPoolCreate(&st->xpool, &props) == cudaSuccess) {
+      uint64_t keep = 64ull << 20;
+      (void)cudaMemPoolSetAttribute(st->xpool, cudaMemPoolAttrReleaseThreshold, &keep);
+    } else {
+      (void)cudaGetLastError();
+      st->xpool = nullptr;
+    }
+  }
   mq_status s = init_kernels(st);
   if (s == MQ_OK) s = init_matvec(st);
   // the static scratch of mq_mmq_fused_static: looking its address up here loads this file's
@@ -146,6 +162,7 @@ extern "C" mq_status mq_init(int device) {
     cudaStreamDestroy(st->copy_stream);
     cudaEventDestroy(st->ev_rows);
     cudaEventDestroy(st->ev_copied);
+    if (st->xpool) cudaMemPoolDestroy(st->xpool);
     delete st;
   } else {
     g_devs[device] = st;

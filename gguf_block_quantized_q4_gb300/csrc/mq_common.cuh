@@ -107,6 +107,9 @@ struct DeviceState {
   // mq_mmq_host: the stream that copies y back while the MMQ's next rows run, and its events
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_rows = nullptr, ev_copied = nullptr;
+  // the stream-ordered pool of the per-call activation fragment planes of the persistent
+  // matvec's Q4_K / Q5_K two-tile calls (nullptr: its x warps convert x themselves)
+  cudaMemPool_t xpool = nullptr;
 };
 DeviceState *device_state(int dev);  // nullptr if mq_init(dev) was not called
 mq_status current_state(DeviceState **st, const char *site);
@@ -121,6 +124,11 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
 bool matvec_kq_applies(int64_t N, int sms);
 mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, cudaStream_t s,
                            const DeviceState *st);
+// The activation fragment plane of the persistent matvec's Q4_K / Q5_K two-tile calls
+// (xplane.cu): its
+// size for B rows of K, and the launch that converts x into it.
+size_t xplane_bytes(int B, int64_t K);
+mq_status launch_xplane(const float *x, int B, int64_t K, uint8_t *plane, cudaStream_t s);
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s);
 // x non-null: the fused form (the kernel quantises x into xq first; cooperative launch)
 // sync non-null: the grid barrier's words there instead of inside xq

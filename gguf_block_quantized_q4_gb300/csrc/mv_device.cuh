@@ -1,6 +1,7 @@
-// mv_device.cuh -- device helpers shared by the decode matvec kernels (matvec.cu and
-// matvec_kq.cu): the warp-level f16 tensor-core MMA, packed f16 arithmetic, f16 / bf16
-// packing, mbarrier waits bounded by %globaltimer, and 1-D bulk copies.
+// mv_device.cuh -- device helpers shared by the decode matvec kernels (matvec.cu,
+// matvec_kq.cu and xplane.cu): the warp-level f16 tensor-core MMA, packed f16 arithmetic,
+// f16 / bf16 packing, mbarrier waits bounded by %globaltimer, 1-D bulk copies, and the layout
+// of the activation fragment plane.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -11,6 +12,23 @@ namespace mq {
 namespace mvd {
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
+
+// The activation fragment plane of a Q4_K / Q5_K two-tile call (B = 5..8) of the persistent
+// matvec: x
+// converted once per call by xplane_kernel (xplane.cu) into the B fragments that the x warps
+// would otherwise form in every CTA; the kernel bulk-copies each chunk's part into a fragment
+// slot.  Per 256-element chunk, NT n8 tiles (4 batch rows each): the fragment groups
+// [kXpGroups][NT][32 + xp_pad(NT)] of uint2 (the kernel's shared-memory slot layout: 16
+// groups of 16 elements, then the Q4_K / Q5_K min-term group), then the unscale factor 2^-e
+// of each of the 4 NT rows (0 for rows past B), padded to 8 floats.  Both sections are
+// multiples of 16 bytes.
+constexpr int kXpGroups = 17;
+__host__ __device__ constexpr int xp_pad(int nt) { return nt == 1 ? 4 : 2; }
+__host__ __device__ constexpr int xp_group_bytes(int nt) { return nt * (32 + xp_pad(nt)) * 8; }
+__host__ __device__ constexpr int xp_off_unscale(int nt) { return kXpGroups * xp_group_bytes(nt); }
+__host__ __device__ constexpr int xp_chunk_bytes(int nt) { return xp_off_unscale(nt) + 32; }
+static_assert(xp_group_bytes(1) % 16 == 0 && xp_group_bytes(2) % 16 == 0,
+              "fragment groups must keep the bulk copies 16-byte aligned");
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -120,6 +138,11 @@ __device__ __forceinline__ void mbar_wait(uint32_t a, uint32_t parity, int *stat
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t a) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+// arrive, and expect `bytes` more of the transaction count (one arrival of the barrier)
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_1d(uint32_t dst, const void *src, uint32_t bytes,
                                         uint32_t bar) {

@@ -31,7 +31,13 @@
  * as global memory (cudaMalloc, torch CUDA tensors, managed memory).  Host
  * pointers passed where a device pointer is required are rejected with
  * MQ_ERR_ARG (checked with cudaPointerGetAttributes).  All hot-path calls are
- * asynchronous on the given stream and allocate nothing.
+ * asynchronous on the given stream.  They allocate nothing, with one exception:
+ * mq_matvec with B = 5..8 on a Q4_K / Q5_K weight of at least SMs / 2 row
+ * groups of 128 takes a per-call buffer of 36 bytes per element of K
+ * (the activation fragment plane) from a stream-ordered pool that mq_init
+ * creates for the device, and frees it in stream order after its kernels (in
+ * a captured graph: an allocation node and a free node).  If the pool cannot
+ * give it, the call computes the same result without it.
  */
 #ifndef MQ_H
 #define MQ_H
@@ -153,7 +159,9 @@ mq_status mq_weight_unpack(const mq_weight *w, void *host_bytes, size_t nbytes);
  * W.  x and y 16-byte aligned.  Every column b of a batched call is computed
  * exactly as the B = 1 call on x[b] (bitwise; "Architecture Execution Plan"
  * ADR-0010, the bitwise-by-default identity rule).  Float result within
- * 1e-4 * sum_k |w[n][k]| |x[b][k]| of the exact product. */
+ * 1e-4 * sum_k |w[n][k]| |x[b][k]| of the exact product.  The calls with
+ * B = 5..8 on wide Q4_K / Q5_K weights use a per-call buffer from the
+ * library's stream-ordered pool (see Pointers above). */
 mq_status mq_matvec(mq_type type, const mq_weight *W, const float *x, float *y, int64_t N,
                     int64_t K, int B, mq_stream stream);
 
