@@ -1053,14 +1053,30 @@ __global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   if (rank == 0 && warp < kCompute) {
+    // all ranks' partials are loaded first (the distributed-shared-memory loads overlap),
+    // then added in rank order
+    float pa[8][NT], pb[8][NT];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < p.S) {
+        float(*rp)[8] = cluster.map_shared_rank(sm.part, r);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          pa[r][i] = rp[16 * warp + g][t + 4 * i];
+          pb[r][i] = rp[16 * warp + g + 8][t + 4 * i];
+        }
+      }
+    }
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const int b = t + 4 * i;
       float sA = 0.f, sB = 0.f;
-      for (int r = 0; r < p.S; ++r) {
-        float(*rp)[8] = cluster.map_shared_rank(sm.part, r);
-        sA += rp[16 * warp + g][b];
-        sB += rp[16 * warp + g + 8][b];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < p.S) {
+          sA += pa[r][i];
+          sB += pb[r][i];
+        }
       }
       if (b < p.B) store_rows(p, b, rA, sA, sB);
     }
