@@ -41,13 +41,36 @@ constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared me
 // infinite; then w is not finite and the division runs.)
 constexpr float kQuantMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr int kQuantMagicBits = 0x4B400000;
-__device__ __forceinline__ float quant_code(float x, float s, float r) {
-  const float w = __fmul_rn(x, r);
-  const float t = __fadd_rn(w, kQuantMagic);
-  const float d = __fsub_rn(w, __fsub_rn(t, kQuantMagic));
-  if (fabsf(d) < 0.5f - 0x1p-14f && fabsf(w) < 127.25f) return t;
-  const int q = min(max(__float2int_rn(__fdiv_rn(x, s)), -127), 127);
-  return __fadd_rn((float)q, kQuantMagic);
+// max that propagates NaN (a NaN operand must send its lane's codes to the division)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float m;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(a), "f"(b));
+  return m;
+}
+// The codes of one lane's four elements v as above: t[k] = 1.5 * 2^23 + q_k, and q_k as a
+// float.  The arithmetic runs on f32 pairs (w - rint(w) as fma(rint(w), -1, w), exact), and
+// one test of the four residuals and magnitudes decides; if any fails, all four codes come
+// from the division (which gives every code, the passing ones included).
+__device__ __forceinline__ void quant_codes4(const float4 v, float s, float r, float (&t)[4],
+                                             float (&qf)[4]) {
+  const float2 r2 = make_float2(r, r), m2 = make_float2(kQuantMagic, kQuantMagic);
+  const float2 nm2 = make_float2(-kQuantMagic, -kQuantMagic), neg = make_float2(-1.f, -1.f);
+  const float2 w01 = __fmul2_rn(make_float2(v.x, v.y), r2);
+  const float2 w23 = __fmul2_rn(make_float2(v.z, v.w), r2);
+  const float2 t01 = __fadd2_rn(w01, m2), t23 = __fadd2_rn(w23, m2);
+  const float2 q01 = __fadd2_rn(t01, nm2), q23 = __fadd2_rn(t23, nm2);
+  const float2 d01 = __ffma2_rn(q01, neg, w01), d23 = __ffma2_rn(q23, neg, w23);
+  const float dm = max_nan(max_nan(fabsf(d01.x), fabsf(d01.y)), max_nan(fabsf(d23.x), fabsf(d23.y)));
+  const float wm = max_nan(max_nan(fabsf(w01.x), fabsf(w01.y)), max_nan(fabsf(w23.x), fabsf(w23.y)));
+  t[0] = t01.x, t[1] = t01.y, t[2] = t23.x, t[3] = t23.y;
+  qf[0] = q01.x, qf[1] = q01.y, qf[2] = q23.x, qf[3] = q23.y;
+  if (dm < 0.5f - 0x1p-14f && wm < 127.25f) return;
+  const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    qf[k] = (float)min(max(__float2int_rn(__fdiv_rn(x[k], s)), -127), 127);
+    t[k] = __fadd_rn(qf[k], kQuantMagic);
+  }
 }
 
 // The loads of one round of a row (PRE passes of NT / 8 blocks from block p0 on): thread
@@ -81,16 +104,10 @@ __device__ __forceinline__ void quant_block(const float4 v, int64_t b, bool ok, 
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
   const float s = __fdiv_rn(mx, 127.0f);
-  float t0 = kQuantMagic, t1 = kQuantMagic, t2 = kQuantMagic, t3 = kQuantMagic;  // q = 0
-  if (s != 0.0f) {
-    const float r = __frcp_rn(s);
-    t0 = quant_code(v.x, s, r);
-    t1 = quant_code(v.y, s, r);
-    t2 = quant_code(v.z, s, r);
-    t3 = quant_code(v.w, s, r);
-  }
-  const int i0 = __float_as_int(t0), i1 = __float_as_int(t1), i2 = __float_as_int(t2),
-            i3 = __float_as_int(t3);
+  float t[4] = {kQuantMagic, kQuantMagic, kQuantMagic, kQuantMagic}, qf[4] = {0.f, 0.f, 0.f, 0.f};
+  if (s != 0.0f) quant_codes4(v, s, __frcp_rn(s), t, qf);
+  const int i0 = __float_as_int(t[0]), i1 = __float_as_int(t[1]), i2 = __float_as_int(t[2]),
+            i3 = __float_as_int(t[3]);
   int S = (i0 + i1) + (i2 + i3) - 4 * kQuantMagicBits;
   S += __shfl_xor_sync(0xffffffffu, S, 1);
   S += __shfl_xor_sync(0xffffffffu, S, 2);
@@ -100,8 +117,8 @@ __device__ __forceinline__ void quant_block(const float4 v, int64_t b, bool ok, 
   const uint32_t packed =
       __byte_perm(__byte_perm(i0, i1, 0x0040u), __byte_perm(i2, i3, 0x0040u), 0x5410u);
   reinterpret_cast<uint32_t *>(xq + L.qs)[blk * 8 + sub] = packed;
-  __half2 h01 = __floats2half2_rn(__fsub_rn(t0, kQuantMagic), __fsub_rn(t1, kQuantMagic));
-  __half2 h23 = __floats2half2_rn(__fsub_rn(t2, kQuantMagic), __fsub_rn(t3, kQuantMagic));
+  __half2 h01 = __floats2half2_rn(qf[0], qf[1]);
+  __half2 h23 = __floats2half2_rn(qf[2], qf[3]);
   uint2 hv;
   hv.x = *reinterpret_cast<uint32_t *>(&h01);
   hv.y = *reinterpret_cast<uint32_t *>(&h23);
