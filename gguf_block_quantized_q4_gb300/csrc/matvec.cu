@@ -71,6 +71,7 @@ namespace {
 using namespace mvd;
 
 constexpr int kRows = kRowGroup;               // rows per CTA
+constexpr int kMaxSplit = 16;                  // K slices: a cluster of up to 16 CTAs
 constexpr int kCompute = kRows / 16;           // compute warps, 16 rows each
 // x-fragment warps: one in the kernel for B <= 2; in the kernels for more batch rows two
 // (x warp j converts rows [j * 2NT, (j + 1) * 2NT) of the chunk), except for Q6_K, whose
@@ -1055,9 +1056,9 @@ __global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const
   if (rank == 0 && warp < kCompute) {
     // all ranks' partials are loaded first (the distributed-shared-memory loads overlap),
     // then added in rank order
-    float pa[8][NT], pb[8][NT];
+    float pa[kMaxSplit][NT], pb[kMaxSplit][NT];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < kMaxSplit; ++r) {
       if (r < p.S) {
         float(*rp)[8] = cluster.map_shared_rank(sm.part, r);
 #pragma unroll
@@ -1072,7 +1073,7 @@ __global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const
       const int b = t + 4 * i;
       float sA = 0.f, sB = 0.f;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      for (int r = 0; r < kMaxSplit; ++r) {
         if (r < p.S) {
           sA += pa[r][i];
           sB += pb[r][i];
@@ -1128,22 +1129,55 @@ mq_status optin_mv(const DeviceState *st, const char *name) {
                 smem, st->smem_optin);
   cudaError_t e = cudaFuncSetAttribute(matvec_kernel<TYPE, NT, XE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)  // clusters of up to 16 CTAs (above the portable 8)
+    e = cudaFuncSetAttribute(matvec_kernel<TYPE, NT, XE>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess)
-    return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
+    return fail(MQ_ERR_LAUNCH, "smem / cluster opt-in of %s (%zu bytes) refused: %s", name, smem,
                 cudaGetErrorName(e));
   return MQ_OK;
+}
+
+// The most clusters of S CTAs of this kernel that the device holds at once (0 if none).
+template <int TYPE, int NT, bool XE>
+int max_clusters(int S) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)S, 1, 1);
+  cfg.blockDim = dim3(mv_threads<TYPE, XE>(), 1, 1);
+  cfg.dynamicSmemBytes = mv_smem_bytes<TYPE, NT>();
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = S;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, matvec_kernel<TYPE, NT, XE>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace
 
 // The three kernels of a type: one n8 tile (B <= 2; B = 3, 4 with the early x release) and
 // two tiles (B = 5..8, early x release).
+// Also records, per cluster size, the most clusters resident at once for every kernel of
+// the type (the least over the three).
 template <int TYPE>
-mq_status optin_type(const DeviceState *st, const char *name) {
+mq_status optin_type(DeviceState *st, const char *name) {
   mq_status s;
   if ((s = optin_mv<TYPE, 1, false>(st, name)) != MQ_OK) return s;
   if ((s = optin_mv<TYPE, 1, true>(st, name)) != MQ_OK) return s;
-  return optin_mv<TYPE, 2, true>(st, name);
+  if ((s = optin_mv<TYPE, 2, true>(st, name)) != MQ_OK) return s;
+  st->mv_clusters[TYPE][1] = 1 << 30;  // no cluster
+  for (int S = 2; S <= kMaxSplit; ++S)
+    st->mv_clusters[TYPE][S] = min(max_clusters<TYPE, 1, false>(S),
+                                   min(max_clusters<TYPE, 1, true>(S),
+                                       max_clusters<TYPE, 2, true>(S)));
+  return MQ_OK;
 }
 
 mq_status init_matvec(DeviceState *st) {
@@ -1161,16 +1195,25 @@ mq_status init_matvec(DeviceState *st) {
   return optin_type<MQ_BF16>(st, "matvec_kernel<BF16>");
 }
 
-// K-split: as many slices as keep every CTA of the grid resident in one wave
-// of cps CTAs per SM (at most 8, a portable cluster).  Depends only on (N, K) and the
-// type, never on B, so batched columns reproduce the B = 1 result bitwise.
-static int choose_split(int64_t N, int64_t K, int sms, int cps) {
+// K-split: as many slices as keep every CTA of the grid resident in one wave of cps CTAs
+// per SM, at most one per chunk; up to 8 (a portable cluster) by that count alone, and up to
+// 16 where the device also reports every cluster of that size co-resident for each of the
+// type's kernels (its count of resident clusters covers how clusters fit into the GPCs).
+// Depends only on (N, K), the type and the device, never on B, so batched columns
+// reproduce the B = 1 result bitwise.  Measured on Q6_K 3584 x 18944 (28 row groups, 74
+// chunks): S = 8 / 9 / 10 took 16.3 / 15.5 / 15.0 us at B = 1 and 23.3 / 22.0 / 23.1 us at
+// B = 8; 11 to 16 need two waves (20.6-22.9 us at B = 1).  The counts check alone would
+// lower f16 weights' 5-way split (whose clusters it does not count as all co-resident),
+// which measured slower at B = 8, so it only decides sizes above 8.
+static int choose_split(int64_t N, int64_t K, int type, const DeviceState *st, int cps) {
   const int64_t groups = (N + kRows - 1) / kRows;
   const int nchunk = (int)((K + kChunk - 1) / kChunk);
-  const int64_t fit = cps * int64_t(sms) / groups;
-  int S = (int)(fit < 8 ? fit : 8);
-  S = min(S, nchunk);
-  return max(S, 1);
+  const int64_t fit = cps * int64_t(st->sms) / groups;
+  int top = fit < kMaxSplit ? (int)fit : kMaxSplit;
+  if (top > nchunk) top = nchunk;
+  for (int S = top; S > 8; --S)
+    if (groups <= st->mv_clusters[type][S]) return S;
+  return top < 8 ? (top > 1 ? top : 1) : 8;
 }
 
 template <int TYPE>
@@ -1194,7 +1237,7 @@ mq_status launch_matvec(const mq_weight *W, const float *x, float *y, int B, cud
   a.B = B;
   a.nchunk = (int)((W->K + kChunk - 1) / kChunk);
   // the f16 / bf16 stages (64 KB) leave room for one CTA per SM, the others for two
-  a.S = choose_split(W->N, W->K, st->sms, float_type(W->type) ? 1 : 2);
+  a.S = choose_split(W->N, W->K, W->type, st, float_type(W->type) ? 1 : 2);
   a.swiglu = W->ffn_gu;
   a.status = st->status;
   const bool kq = W->type == MQ_Q4_K || W->type == MQ_Q5_K || W->type == MQ_Q6_K;

@@ -107,6 +107,10 @@ struct DeviceState {
   // mq_mmq_host: the stream that copies y back while the MMQ's next rows run, and its events
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_rows = nullptr, ev_copied = nullptr;
+  // split-K matvec (matvec.cu): the most clusters of S CTAs that can be resident at once
+  // for every kernel of a weight type, by type id (the GGUF number, < 32) and S = 1..16
+  // (0: that cluster size cannot run); filled by init_matvec
+  int mv_clusters[32][17] = {};
   // the stream-ordered pool of the per-call activation fragment planes of the persistent
   // matvec's Q4_K / Q5_K two-tile calls (nullptr: its x warps convert x themselves)
   cudaMemPool_t xpool = nullptr;
