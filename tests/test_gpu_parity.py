@@ -486,6 +486,22 @@ def test_batch_columns_equal_single_calls_bitwise_every_type(qtype, N, K):
     assert np.array_equal(y3.view(np.uint32), y8[3:6].view(np.uint32))
 
 
+@pytest.mark.parametrize("qtype,N,K", [(8, 300, 4864), (12, 300, 4864), (14, 300, 4864),
+                                       (3, 1000, 8192)])
+def test_wide_k_split_over_large_clusters(qtype, N, K):
+    """Few row groups and many chunks: the K split goes past the portable cluster size (up to
+    16 CTAs per cluster, where every cluster fits at once); the result stays within the bound
+    and every column of a B = 8 call equals its B = 1 call bit for bit."""
+    W = registered(qtype, N, K, 53, mq.REG_NO_MMQ_PLANE)
+    x = synth.activations(8, K, seed=54)
+    y8 = gpu_matvec(W, x)
+    yref, bnd = oracle.matvec(qtype, weights(qtype, N, K, 53), N, K, x)
+    assert_bound(y8, yref, bnd, f"type {qtype} {N}x{K} B=8")
+    for b in (0, 5, 7):
+        y1 = gpu_matvec(W, x[b:b + 1])
+        assert np.array_equal(y1[0].view(np.uint32), y8[b].view(np.uint32)), (qtype, b)
+
+
 def test_host_buffer_calls_equal_the_device_calls():
     """mq_matvec_host / mq_mmq_host give the device-pointer calls' results bit for bit on both
     transfer routes: page-locked aligned buffers (the kernels read and write them through
