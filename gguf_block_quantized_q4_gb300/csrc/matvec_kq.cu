@@ -781,7 +781,7 @@ mq_status launch_matvec_kq(const mq_weight *W, const float *x, float *y, int B, 
   // pool, or if the allocation is refused, the x warps convert x themselves (the same
   // fragments).
   uint8_t *xp = nullptr;
-  if (st->xpool && W->type != MQ_Q6_K) {
+  if (st->xpool && W->type != MQ_Q6_K && !test_no_xplane()) {
     if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&xp), xplane_bytes(B, W->K), st->xpool,
                                 s) != cudaSuccess) {
       (void)cudaGetLastError();

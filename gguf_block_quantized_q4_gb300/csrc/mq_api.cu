@@ -87,8 +87,11 @@ extern "C" const char *mq_status_name(mq_status s) {
 //                          which the runtime refuses before any kernel runs;
 //   MQ_TEST_EXPIRE_WAIT=1  the MMQ epilogue first waits on a barrier nothing arrives on;
 //                          the wait expires after about a millisecond, records
-//                          MQ_ERR_TIMEOUT in the status word and the kernel carries on.
-static std::atomic<int> g_test_fail_launch{0}, g_test_expire_wait{0};
+//                          MQ_ERR_TIMEOUT in the status word and the kernel carries on;
+//   MQ_TEST_NO_XPLANE=1    the persistent matvec's two-tile calls take no activation
+//                          fragment plane (as when the pool cannot give one): its x warps
+//                          convert x themselves.
+static std::atomic<int> g_test_fail_launch{0}, g_test_expire_wait{0}, g_test_no_xplane{0};
 
 static int env_flag(const char *name) {
   const char *v = getenv(name);
@@ -96,6 +99,7 @@ static int env_flag(const char *name) {
 }
 
 int mq::test_fail_launch() { return g_test_fail_launch.load(std::memory_order_relaxed); }
+int mq::test_no_xplane() { return g_test_no_xplane.load(std::memory_order_relaxed); }
 static int test_expire_wait() { return g_test_expire_wait.load(std::memory_order_relaxed); }
 
 static mq_status static_scratch(DeviceState *st, uint8_t **out, const char *site);
@@ -104,6 +108,7 @@ extern "C" mq_status mq_init(int device) {
   const char *site = "mq_init";
   g_test_fail_launch.store(env_flag("MQ_TEST_FAIL_LAUNCH"), std::memory_order_relaxed);
   g_test_expire_wait.store(env_flag("MQ_TEST_EXPIRE_WAIT"), std::memory_order_relaxed);
+  g_test_no_xplane.store(env_flag("MQ_TEST_NO_XPLANE"), std::memory_order_relaxed);
   int ndev = 0;
   CK(cudaGetDeviceCount(&ndev), site);
   if (device < 0 || device >= ndev)

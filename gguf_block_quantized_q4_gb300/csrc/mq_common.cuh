@@ -154,6 +154,10 @@ mq_status launch_copy_in(const float *src_view, float *dst, int64_t n, cudaStrea
 // environment of the last mq_init call, the matvec and MMQ launches are configured with an
 // empty grid, which the runtime refuses before any kernel runs.
 int test_fail_launch();
+// Test seam: with MQ_TEST_NO_XPLANE=1 at the last mq_init, the persistent matvec's two-tile
+// calls run without the activation fragment plane (the path taken when the pool cannot give
+// one), so that path is covered by the tests.
+int test_no_xplane();
 mq_status init_kernels(DeviceState *st);  // smem opt-ins of the MMQ kernels
 mq_status init_matvec(DeviceState *st);   // smem opt-ins of the matvec kernels
 mq_status init_matvec_kq(DeviceState *st);

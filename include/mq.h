@@ -116,8 +116,8 @@ typedef void *mq_stream;
  * Design" §2.4, the eager pre-warm), allocates the per-device status word
  * used by bounded waits and looks up the address of mq_mmq_fused_static's
  * scratch.  Idempotent.  Must precede every other call for that device.  Each
- * call also reads the tests' failure-injection switches MQ_TEST_FAIL_LAUNCH and
- * MQ_TEST_EXPIRE_WAIT from the environment (no hot-path call reads it).
+ * call also reads the tests' switches MQ_TEST_FAIL_LAUNCH, MQ_TEST_EXPIRE_WAIT and
+ * MQ_TEST_NO_XPLANE from the environment (no hot-path call reads it).
  * Errors: MQ_ERR_CUDA, MQ_ERR_LAUNCH (an opt-in refused). */
 mq_status mq_init(int device);
 

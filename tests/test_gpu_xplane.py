@@ -87,3 +87,30 @@ def test_two_streams_at_once_on_one_weight():
     assert (err <= 1e-4 * bnd + 1e-37).all()
     mq.stream_status()
     W.free()
+
+
+@pytest.mark.parametrize("qtype", [12, 13])
+def test_without_the_plane_the_same_bits(monkeypatch, qtype):
+    """With MQ_TEST_NO_XPLANE=1 at mq_init (the path taken when the pool cannot give a plane)
+    the x warps convert x themselves at two tiles: the result equals the plane's bit for bit
+    and stays within the oracle's bound."""
+    N, K, B = 18944, 1024, 8
+    wb = synth.weights(qtype, N, K, 67)
+    W = mq.register_weight(qtype, wb, N, K, mq.REG_NO_MMQ_PLANE)
+    x = torch.from_numpy(synth.activations(B, K, seed=68)).cuda()
+    with_plane = mq.matvec(W, x)
+    torch.cuda.synchronize()
+    monkeypatch.setenv("MQ_TEST_NO_XPLANE", "1")
+    mq.init(0)
+    try:
+        without = mq.matvec(W, x)
+        torch.cuda.synchronize()
+    finally:
+        monkeypatch.delenv("MQ_TEST_NO_XPLANE")
+        mq.init(0)
+    assert np.array_equal(bits(without), bits(with_plane))
+    yref, bnd = oracle.matvec(qtype, wb, N, K, x.cpu().numpy(), parallel=True)
+    err = np.abs(without.cpu().numpy().astype(np.float64) - yref)
+    assert (err <= 1e-4 * bnd + 1e-37).all()
+    mq.stream_status()
+    W.free()
