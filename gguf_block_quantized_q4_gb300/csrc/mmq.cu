@@ -325,6 +325,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
+  // (launched with programmatic stream serialisation outside the fused form) a following
+  // kernel may launch at once; the producer waits for the previous grid before its first
+  // load, and everything that reads xq or writes the outputs follows its loads
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
@@ -333,6 +337,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads of xq
     }
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // xq comes from the previous kernel
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
       // Fills in the order of the accumulator uses.  Global use U belongs to issuer U % 2,
       // whose c-th stage is ring stage (U % 2) + 2 * (c % SR), round c / SR.
@@ -688,9 +693,25 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
       TcSmem<TYPE>::MIN && !DOTS ? W->tmap_mb : W->tmap_w);
   const CUtensorMap &tD = *reinterpret_cast<const CUtensorMap *>(DOTS ? W->tmap_w : W->tmap_td);
   if (DOTS || qf.x == nullptr) {
-    mmq_tc_kernel<TYPE, DOTS><<<grid, NTHR, smem_bytes<TYPE>(), s>>>(tA, tW, tW2, tAm, tBm, tSx,
-                                                                      tD, a, qf);
-    MQ_LAUNCH_CHECK(name);
+    // programmatic stream serialisation: the CTAs' set-up (barriers, tensor memory) overlaps
+    // the previous kernel's tail; the producer waits for that kernel before its first load
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTHR, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<TYPE>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, DOTS>, tA, tW, tW2, tAm,
+                                             tBm, tSx, tD, a, qf);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
+      return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u) failed: %s", name, grid.x,
+                  cudaGetErrorName(e));
+    }
     return MQ_OK;
   }
   // fused quantisation: a cooperative launch, so that every CTA of the grid barrier is

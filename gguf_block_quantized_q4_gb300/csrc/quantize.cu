@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256, 4) quantize_act_kernel(const float *__res
                                                            int64_t K, ActLayout L) {
   __shared__ float ttc[kTtCache];
   __shared__ float wmax[8];
+  // launched with programmatic stream serialisation: the MMQ that follows may start its
+  // set-up at once, and this grid reads x and writes xq only after the previous one is done
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   quantize_row<256>(x + int64_t(blockIdx.x) * K, xq, blockIdx.x, K, L, ttc, wmax, threadIdx.x, -1);
 }
 
@@ -27,8 +31,22 @@ __global__ void __launch_bounds__(256, 4) quantize_act_kernel(const float *__res
 
 mq_status launch_quantize(const float *x, void *xq, int64_t M, int64_t K, cudaStream_t s) {
   if (M > 0x7fffffff) return fail(MQ_ERR_SHAPE, "mq_quantize_act: M too large");
-  quantize_act_kernel<<<(unsigned)M, 256, 0, s>>>(x, (uint8_t *)xq, M, K, act_layout(M, K));
-  MQ_LAUNCH_CHECK("quantize_act_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel, x, (uint8_t *)xq, M, K,
+                                           act_layout(M, K));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MQ_ERR_LAUNCH, "launch of quantize_act_kernel (grid %lld) failed: %s",
+                (long long)M, cudaGetErrorName(e));
+  }
   return MQ_OK;
 }
 
