@@ -337,8 +337,23 @@ __global__ void __launch_bounds__(NTHR, 1)
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads of xq
     }
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // xq comes from the previous kernel
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
+      // Registered weights are never written by a kernel: the weight tiles of the first
+      // tile's first NST fills (fill f of the first tile uses ring stage f) go out before the
+      // wait for the previous kernel, the activation tiles of those stages after it.
+      int pre = 0;
+      if constexpr (!QF) {
+        if (blockIdx.x < p.ntiles) {
+          const int n0 = (blockIdx.x / p.ntm) * TN;
+          pre = npairs < NST ? npairs : NST;
+          for (int f = 0; f < pre; ++f) {
+            mbar_expect_tx(sa(&sm.full[f]), bytes);
+            tma_2d(sa(sm.b[f]), &tW, f * PK, n0, sa(&sm.full[f]));
+            if constexpr (ODD) tma_2d(sa(sm.b2.v[ODD ? f : 0]), &tW2, f * PK, n0, sa(&sm.full[f]));
+          }
+        }
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // xq comes from the previous kernel
       // Fills in the order of the accumulator uses.  Global use U belongs to issuer U % 2,
       // whose c-th stage is ring stage (U % 2) + 2 * (c % SR), round c / SR.
       int c0 = 0, c1 = 0;
@@ -363,6 +378,10 @@ __global__ void __launch_bounds__(NTHR, 1)
             mbar_expect_tx(sa(&sm.full[s]), 2 * kTileBytes);
             tma_2d(sa(sm.a[s]), &tAm, (f - npairs) * PK, m0, sa(&sm.full[s]));
             tma_2d(sa(sm.b[s]), &tBm, (f - npairs) * PK, n0, sa(&sm.full[s]));
+            continue;
+          }
+          if (tl == 0 && f < pre) {  // its weight tiles are in flight already
+            tma_2d(sa(sm.a[s]), &tA, pr * PK, m0, sa(&sm.full[s]));
             continue;
           }
           mbar_expect_tx(sa(&sm.full[s]), bytes);
