@@ -1041,7 +1041,8 @@ __global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const
     }
     return;
   }
-  // split-K over the cluster: rank 0 sums the ranks' partials in rank order.
+  // split-K over the cluster: the ranks' partials are summed in rank order (the rows of
+  // compute warp w by rank w mod S).
   // part overlays the ring, so every warp must be past its last ring access.
   __syncthreads();
   if (warp < kCompute) {
@@ -1053,7 +1054,8 @@ __global__ void __launch_bounds__(mv_threads<TYPE, XE>(), 2) matvec_kernel(const
   }
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  if (rank == 0 && warp < kCompute) {
+  if (warp < kCompute && warp % p.S == rank) {
+    // the rows of compute warp w are summed by rank w mod S (the ranks share the reads);
     // all ranks' partials are loaded first (the distributed-shared-memory loads overlap),
     // then added in rank order
     float pa[kMaxSplit][NT], pb[kMaxSplit][NT];
