@@ -39,6 +39,20 @@ constexpr int kTtCache = 2048;  // s*S of a row's first blocks kept in shared me
 // least 2^-14 from w, v lies on the same side of each as w and is not one itself, so both
 // round to the same integer, which is within [-127, 127].  (A subnormal s can make r
 // infinite; then w is not finite and the division runs.)
+// s = fl(amax / 127) (correctly rounded) without the division: q0 = fl(amax * c) with
+// c = fl(1 / 127), the remainder amax - 127 q0 by one fma (exact), and one fma correction
+// fl(q0 + r c), the correction step of Markstein's division by a correctly rounded
+// reciprocal.  It gives the correctly rounded quotient for every non-negative finite binary32
+// amax (checked exhaustively, subnormals included, in tests/test_quant_rule_cpu.py); a
+// non-finite amax takes the division itself.
+__device__ __forceinline__ float div127(float a) {
+  constexpr float c = 0x1.020408p-7f;  // fl(1 / 127)
+  const float q0 = __fmul_rn(a, c);
+  const float r = __fmaf_rn(-q0, 127.0f, a);
+  const float q1 = __fmaf_rn(r, c, q0);
+  return a < INFINITY ? q1 : __fdiv_rn(a, 127.0f);
+}
+
 constexpr float kQuantMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr int kQuantMagicBits = 0x4B400000;
 // max that propagates NaN (a NaN operand must send its lane's codes to the division)
@@ -103,7 +117,7 @@ __device__ __forceinline__ void quant_block(const float4 v, int64_t b, bool ok, 
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-  const float s = __fdiv_rn(mx, 127.0f);
+  const float s = div127(mx);
   float t[4] = {kQuantMagic, kQuantMagic, kQuantMagic, kQuantMagic}, qf[4] = {0.f, 0.f, 0.f, 0.f};
   if (s != 0.0f) quant_codes4(v, s, __frcp_rn(s), t, qf);
   const int i0 = __float_as_int(t[0]), i1 = __float_as_int(t[1]), i2 = __float_as_int(t[2]),

@@ -80,3 +80,51 @@ def test_fallback_is_needed_and_codes_read_from_the_bits():
     bits = (q.astype(np.float32) + MAGIC).view(np.int32)
     assert np.array_equal(bits - np.int32(0x4B400000), q)
     assert np.array_equal((bits & 255).astype(np.uint8).view(np.int8), q.astype(np.int8))
+
+
+def div127_rule(bits):
+    """The kernels' s = amax / 127: q0 = fl(a c), r = fl(fma(-q0, 127, a)), fl(fma(r, c, q0)),
+    c = fl(1/127), emulated exactly in float64 (the products are exact there; the final sum is
+    rounded once to binary32, ties resolved by the exact error of the float64 sum)."""
+    a = bits.view(np.float32)
+    c = F(1) / F(127)
+    q0 = a * c
+    r = (a.astype(np.float64) - 127.0 * q0.astype(np.float64)).astype(np.float32)
+    q064 = q0.astype(np.float64)
+    rc = r.astype(np.float64) * np.float64(c)
+    s = q064 + rc
+    bb = s - q064
+    e = (q064 - (s - bb)) + (rc - bb)
+    t = s.astype(np.float32)
+    t64 = t.astype(np.float64)
+    up = np.nextafter(t, np.float32(np.inf))
+    dn = np.nextafter(t, np.float32(-np.inf))
+    res = t.copy()
+    m1 = (s == (t64 + up.astype(np.float64)) / 2) & (e > 0)
+    res[m1] = up[m1]
+    m2 = (s == (t64 + dn.astype(np.float64)) / 2) & (e < 0)
+    res[m2] = dn[m2]
+    return res
+
+
+def test_division_by_127_is_correctly_rounded():
+    """Every 61st non-negative finite binary32 bit pattern (35 M values from 0 to FLT_MAX,
+    subnormals included) and every pattern near powers of two and of 127: the kernels'
+    fma-corrected quotient equals the correctly rounded a / 127.  With MQ_EXHAUSTIVE=1 every
+    one of the 2^31 - 2^23 patterns is checked (a few minutes; it passes)."""
+    import os
+    top = int(np.float32(3.4028235e38).view(np.uint32))
+    stride = 1 if os.environ.get("MQ_EXHAUSTIVE") == "1" else 61
+    step = 1 << 24
+    for start in range(0, top + 1, step * stride):
+        bits = np.arange(start, min(start + step * stride, top + 1), stride,
+                         dtype=np.uint64).astype(np.uint32)
+        a = bits.view(np.float32)
+        assert np.array_equal(div127_rule(bits).view(np.uint32), (a / F(127)).view(np.uint32))
+    near = []
+    for e in range(-149, 128):
+        for base in (np.float32(2.0) ** e, np.float32(127.0) * np.float32(2.0) ** (e - 7)):
+            b = np.float32(base).view(np.uint32).astype(np.int64)
+            near.append(np.arange(b - 64, b + 64))
+    nb = np.unique(np.clip(np.concatenate(near), 0, top)).astype(np.uint32)
+    assert np.array_equal(div127_rule(nb).view(np.uint32), (nb.view(np.float32) / F(127)).view(np.uint32))
