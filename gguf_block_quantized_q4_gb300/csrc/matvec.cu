@@ -160,10 +160,11 @@ __host__ __device__ constexpr int tile_bytes() {
 // Weight-ring depth: two CTAs per SM must fit in shared memory (checked at each launch
 // site for the quantised types; the f16 / bf16 tiles take one CTA per SM); within that,
 // the depth that measured fastest (Q4_K B <= 4: 2 stages beat 3 and 4; a third stage for
-// the Q4_K / Q5_K two-tile kernel left one CTA per SM and doubled its time).
+// the Q4_K / Q5_K two-tile kernel left one CTA per SM and doubled its time; Q6_K 3584 x
+// 18944 in clusters of 10, B = 1..4: 2 stages 1.5-2% faster than 3).
 template <int TYPE, int NT>
 __host__ __device__ constexpr int ring_stages() {
-  return TYPE == MQ_Q6_K && NT == 1 ? 3 : 2;
+  return 2;
 }
 // Fragment-ring depth.
 template <int TYPE>
