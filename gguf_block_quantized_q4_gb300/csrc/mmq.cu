@@ -339,13 +339,17 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
       const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
       // Registered weights are never written by a kernel: the weight tiles of the first
-      // tile's first NST fills (fill f of the first tile uses ring stage f) go out before the
-      // wait for the previous kernel, the activation tiles of those stages after it.
+      // tile's first kRamp fills (fill f of the first tile uses ring stage f) go out before
+      // the wait for the previous kernel, the activation tiles of those stages after it.
+      // The rest of the first ring round is ramped: stage s is filled once stage s - kRamp
+      // has landed, so that every SM's first stages are not queued behind the whole first
+      // round of all SMs (Q4_K 512 x 18944 x 3584: 109.5 -> 108.9 us; a ramp of 2 109.3).
+      constexpr int kRamp = 3;
       int pre = 0;
       if constexpr (!QF) {
         if (blockIdx.x < p.ntiles) {
           const int n0 = (blockIdx.x / p.ntm) * TN;
-          pre = npairs < NST ? npairs : NST;
+          pre = npairs < kRamp ? npairs : kRamp;
           for (int f = 0; f < pre; ++f) {
             mbar_expect_tx(sa(&sm.full[f]), bytes);
             tma_2d(sa(sm.b[f]), &tW, f * PK, n0, sa(&sm.full[f]));
@@ -374,6 +378,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             tma_2d(sa(sm.gd[slot][0]), &tD, n0, 8 * g, sa(&sm.gfull[slot]));
           }
           if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 1, kWaitNs);
+          else if (tl == 0 && s >= kRamp)  // first round: after stage s - kRamp has landed
+            mbar_wait(sa(&sm.full[s - kRamp]), 0u, p.status, 10, kWaitNs);
           if (pr < 0) {  // min-term operands: 64 columns of the [hi|hi|lo] x [hi|lo|hi] planes
             mbar_expect_tx(sa(&sm.full[s]), 2 * kTileBytes);
             tma_2d(sa(sm.a[s]), &tAm, (f - npairs) * PK, m0, sa(&sm.full[s]));
