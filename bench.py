@@ -331,10 +331,11 @@ def graph_time_ms(fn, calls, trials=5):
     return statistics.median(out)
 
 
-def profile_calls(kernel: str, calls: int, batch=None, workload=None):
+def profile_calls(kernel: str, calls: int, batch=None, workload=None, from_decode_plane=False):
     """Run `calls` launches of one hot-path kernel on the bench workload (or on the weight
     of another named workload) and exit: the program that ncu captures are taken of (one
-    kernel, few launches, ~0.3 GB on device)."""
+    kernel, few launches, ~0.3 GB on device).  from_decode_plane: register the (Q4_K) weight
+    with MQ_REG_MMQ_FROM_DECODE_PLANE."""
     import torch
 
     import gguf_block_quantized_q4_gb300 as mq
@@ -348,6 +349,8 @@ def profile_calls(kernel: str, calls: int, batch=None, workload=None):
         qt, n, k, ws, xs = c["qtype"], c["N"], c["K"], c["w_seed"], c["x_seed"]
     Wb = synth.weights(qt, n, k, ws)
     flags = mq.REG_NO_MMQ_PLANE if kernel == "matvec" else mq.REG_DEFAULT
+    if from_decode_plane:
+        flags = mq.REG_MMQ_FROM_DECODE_PLANE
     W = mq.register_weight(qt, Wb, n, k, flags)
     if kernel == "matvec":
         nb = batch or B
@@ -818,6 +821,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="profiling mode: the matvec's batch rows (1..8), or the quantiser's and "
                          "MMQ's activation rows (default: the bench's decode batch / prefill M)")
+    ap.add_argument("--mmq-from-decode-plane", action="store_true",
+                    help="profiling mode: register the Q4_K weight without the f16 plane (the "
+                         "MMQ expands the decode-plane tiles in shared memory)")
     ap.add_argument("--chain", type=int, default=0,
                     help="time a decode chain of this many small matvecs, eager and graphed")
     ap.add_argument("--ffn-gu", action="store_true",
@@ -830,7 +836,8 @@ def main():
             import synth
             if args.workload not in synth.WORKLOADS:
                 ap.error(f"--workload: one of {', '.join(synth.WORKLOADS)}")
-        return profile_calls(args.kernel, args.calls, args.batch, args.workload)
+        return profile_calls(args.kernel, args.calls, args.batch, args.workload,
+                             args.mmq_from_decode_plane)
     if args.chain:
         return chain_timing(args.chain)
     if args.ffn_gu:

@@ -17,13 +17,14 @@ from __future__ import annotations
 
 import ctypes
 import os
+import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmq.so")
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14
 F16, BF16 = 1, 30  # unquantised weights: decode matvec only
-REG_DEFAULT, REG_NO_MMQ_PLANE = 0, 1
+REG_DEFAULT, REG_NO_MMQ_PLANE, REG_MMQ_FROM_DECODE_PLANE = 0, 1, 2
 # (elements, bytes) per block; f16 / bf16 rows count in units of 32 elements (K % 32 == 0)
 BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q5_1: (32, 24), Q8_0: (32, 34),
          Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), F16: (32, 64), BF16: (32, 64)}
@@ -136,18 +137,48 @@ class Weight:
 
     def free(self):
         if self.handle:
+            _free_deferred()
             _check(lib().mq_weight_free(self.handle))
             self.handle = None
 
     def __del__(self):
+        # mq_weight_free synchronises the device, which would invalidate a stream capture in
+        # progress (a weight kept alive by a reference cycle is collected whenever the
+        # garbage collector runs): during a capture the handle is kept and freed later
         try:
             if getattr(self, "handle", None) and _lib is not None:
-                _lib.mq_weight_free(self.handle)
+                if _capturing():
+                    _deferred_frees.append(self.handle)
+                else:
+                    _free_deferred()
+                    _lib.mq_weight_free(self.handle)
         except Exception:
             pass
 
 
+_deferred_frees = []
+
+
+def _capturing() -> bool:
+    torch = sys.modules.get("torch")
+    try:
+        return bool(torch is not None and torch.cuda.is_available()
+                    and torch.cuda.is_current_stream_capturing())
+    except Exception:
+        return False
+
+
+def _free_deferred():
+    """Free the weights whose collection fell inside a stream capture (none while one is
+    still in progress)."""
+    if not _deferred_frees or _capturing():
+        return
+    while _deferred_frees:
+        _lib.mq_weight_free(_deferred_frees.pop())
+
+
 def register_weight(qtype, data, N, K, flags=REG_DEFAULT) -> Weight:
+    _free_deferred()
     return Weight(qtype, data, N, K, flags)
 
 
@@ -173,6 +204,7 @@ class FfnGuWeight(Weight):
 
 
 def register_ffn_gu(qtype, gate, up, N, K, flags=REG_DEFAULT) -> FfnGuWeight:
+    _free_deferred()
     return FfnGuWeight(qtype, gate, up, N, K, flags)
 
 

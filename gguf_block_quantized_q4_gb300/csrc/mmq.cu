@@ -51,6 +51,7 @@
 // All mbarrier waits are bounded (2 s by %globaltimer); an expired wait writes
 // MQ_ERR_TIMEOUT into the device status word read by mq_stream_status.
 #include <cstddef>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -64,20 +65,43 @@ constexpr int PK = 2 * TK;              // K per pipeline stage (a pair of block
 constexpr int NEPI = 16;                // epilogue warps: 4 per TMEM lane quarter
 constexpr int EC = TN * 4 / NEPI;       // accumulator columns per epilogue thread (32)
 constexpr int NTHR = 32 * (4 + NEPI);   // 640 threads
+// Q4_K from its decode-plane tiles: a sixth warpgroup of four weight decoders, 768 threads
+constexpr int NTHR_PW = NTHR + 128;
+template <bool PW>
+__host__ __device__ constexpr int nthr() {
+  return PW ? NTHR_PW : NTHR;
+}
+constexpr int kPkBytes = 128 * 144;     // one Q4_K decode-plane tile: 128 rows, one 256-K chunk
 constexpr uint32_t TMEM_COLS = 512;     // accumulator pair i at columns 256*i .. +256
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kTestWaitNs = 1000000ull;
 constexpr int kTileBytes = TM * PK * 2;  // 16 KB per operand tile and stage
 // launch: 640 threads x 96 registers = 61440; after setmaxnreg the control
 // warpgroup holds 128 x 32 and the four epilogue warpgroups 512 x 112 = 61440.
-constexpr int kRegLaunch = 96, kRegCtl = 32, kRegEpi = 112;
-static_assert(128 * kRegCtl + 512 * kRegEpi <= NTHR * kRegLaunch,
+// With the decoder warpgroup: 768 x 80 = 61440 = 128 x 32 (control) + 512 x 104
+// (epilogue) + 128 x 32 (decoders).  setmaxnreg.inc waits until the registers are free, so
+// the split must fit the launch exactly as compiled: the host checks the kernel's register
+// count against reg_launch before the first launch.
+constexpr int kRegCtl = 32;
+template <bool PW>
+__host__ __device__ constexpr int reg_launch() {
+  return PW ? 80 : 96;
+}
+template <bool PW>
+__host__ __device__ constexpr int reg_epi() {
+  return PW ? 104 : 112;
+}
+static_assert(128 * kRegCtl + 512 * reg_epi<false>() <= NTHR * reg_launch<false>(),
               "register split exceeds the launch");
-static_assert(NTHR * kRegLaunch <= 65536, "launch registers exceed the SM");
+static_assert(128 * kRegCtl + 512 * reg_epi<true>() + 128 * kRegCtl <=
+                  NTHR_PW * reg_launch<true>(),
+              "register split exceeds the launch");
+static_assert(NTHR * reg_launch<false>() <= 65536 && NTHR_PW * reg_launch<true>() <= 65536,
+              "launch registers exceed the SM");
 
-template <int TYPE>
-constexpr int stages() {  // 192 KB of operand ring
-  return TYPE == MQ_Q6_K ? 4 : 6;
+template <int TYPE, bool PW = false>
+constexpr int stages() {  // 192 KB of operand ring (128 KB beside the decode-plane tiles)
+  return (TYPE == MQ_Q6_K || PW) ? 4 : 6;
 }
 
 struct TcArgs {
@@ -93,6 +117,8 @@ struct TcArgs {
   int *status;
   int debug_expire;
   int swiglu;           // fused gate/up weight: y[m][n'] = silu(gate col) * (its up col), N / 2 wide
+  const uint8_t *wq;    // Q4_K decode plane (tiles of 128 rows x 144 bytes per 256-K chunk)
+  int nchk;             // its chunks per row group (K / 256)
 };
 
 // Fused quantisation (x non-null): the CTAs first quantise the rows of x into xq.
@@ -113,9 +139,9 @@ struct __align__(128) Slots<T, 0, W> {
   T v[1][1];  // never indexed
 };
 
-template <int TYPE>
+template <int TYPE, bool PW = false>
 struct __align__(1024) TcSmem {
-  static constexpr int NST = stages<TYPE>();
+  static constexpr int NST = stages<TYPE, PW>();
   static constexpr bool ODD = TYPE == MQ_Q6_K;
   static constexpr bool MIN = TYPE == MQ_Q4_K || TYPE == MQ_Q4_1;
   __half a[NST][TM * PK];
@@ -123,19 +149,22 @@ struct __align__(1024) TcSmem {
   Slots<__half, ODD ? NST : 0, TN * PK> b2;
   alignas(128) float gsx[2][8][TM];     // per group slot: row scales s
   alignas(128) float gd[2][8][TN];      // column scales d
-  uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], never;
+  Slots<uint8_t, PW ? 2 : 0, kPkBytes> pk;  // Q4_K decode-plane tiles (two chunk slots)
+  uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], pfull[2], pempty[2],
+      never;
   uint32_t tmem;
 };
 
-template <int TYPE>
+template <int TYPE, bool PW = false>
 constexpr bool smem_layout_ok() {
-  using S = TcSmem<TYPE>;
+  using S = TcSmem<TYPE, PW>;
   return offsetof(S, a) % 1024 == 0 && offsetof(S, b) % 1024 == 0 &&
          offsetof(S, b2) % 1024 == 0 && offsetof(S, gsx) % 128 == 0 &&
-         offsetof(S, gd) % 128 == 0 && offsetof(S, full) % 8 == 0;
+         offsetof(S, gd) % 128 == 0 && offsetof(S, pk) % 128 == 0 && offsetof(S, full) % 8 == 0;
 }
 static_assert(smem_layout_ok<MQ_Q8_0>() && smem_layout_ok<MQ_Q4_K>() &&
-                  smem_layout_ok<MQ_Q6_K>() && smem_layout_ok<MQ_Q4_1>(),
+                  smem_layout_ok<MQ_Q6_K>() && smem_layout_ok<MQ_Q4_1>() &&
+                  smem_layout_ok<MQ_Q4_K, true>(),
               "TMA tiles need 1024-byte, bulk copies and float4 reads 16-byte alignment");
 
 __device__ __forceinline__ uint32_t sa(const void *p) {
@@ -159,7 +188,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait on an mbarrier phase.  On expiry: record (timeout, site) in the
-// status word and return false; the caller carries on so the kernel ends.
+// status word and return false; the caller carries on so the kernel ends.  A wait that has
+// lasted kAbandonNs while the status word already holds an error gives up at once, so that
+// after one expiry the kernel's remaining waits do not each run to the limit (no wait of a
+// working pipeline lasts that long; the test hook's 1 ms expiry delays the others by about
+// 1 ms, and they still complete).
+constexpr uint64_t kAbandonNs = 10000000ull;
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *status, int site,
                                           uint64_t limit_ns) {
   if (mbar_try(a, parity)) return true;
@@ -169,10 +203,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int *stat
     for (int i = 0; i < 8; ++i) {
       if (mbar_try(a, parity)) return true;
     }
-    if (gtime() - t0 > limit_ns) {
+    const uint64_t dt = gtime() - t0;
+    if (dt > limit_ns) {
       if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
       return false;
     }
+    if (dt > kAbandonNs && *reinterpret_cast<volatile int *>(status) != 0) return false;
   }
 }
 // Grid-wide barrier of the fused quantise + MMQ (all CTAs co-resident: cooperative launch),
@@ -230,6 +266,79 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// One integer weight pair sc * n_lo, sc * n_hi from the nibbles at bits sh and sh + 16 of
+// w: 1024 + n is an f16 formed by one bit operation, and fma(1024 + n, sc, -1024 sc) rounds
+// once, to the exact sc * n (<= 945).
+__device__ __forceinline__ uint32_t q4k_pair(uint32_t w, int sh, __half2 sc, __half2 msc) {
+  const uint32_t v = ((w >> sh) & 0x000F000Fu) | 0x64006400u;
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&v), sc, msc);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+// (sc, sc) and (-1024 sc, -1024 sc) as f16 pairs, sc the byte of scp at selector sel
+__device__ __forceinline__ void q4k_scale_pair(uint32_t scp, uint32_t sel, __half2 &sc,
+                                               __half2 &msc) {
+  const uint32_t v = __byte_perm(scp, 0u, sel) | 0x64006400u;  // 1024 + sc in both halves
+  sc = __hsub2(*reinterpret_cast<const __half2 *>(&v), __half2half2(__ushort_as_half(0x6400)));
+  msc = __hmul2(sc, __half2half2(__ushort_as_half(0xE400)));  // * -1024
+}
+// Weight tile of one pipeline stage from a Q4_K decode-plane tile in shared memory: quarter
+// qt of the 256-element chunk (elements 64 qt .. 64 qt + 63, sub-blocks 2 qt and 2 qt + 1)
+// for rows r0 .. r0 + 31, as the f16 integers sc_j * nib in the K-major 128-byte-swizzled
+// layout the MMA reads (the layout a TMA box of the f16 plane lands in: row r at 128 r,
+// 16-byte unit j of the row at unit j ^ (r % 8)).  A decode-plane row is the 16-byte block
+// header (d, dmin, 12 scale bytes), then four 32-byte groups t whose word 2 qt + u holds qs
+// bytes 32 qt + 16 u + 4 t + (0, 2, 1, 3): low nibbles are elements 16 u + 4 t .. + 3 of
+// the quarter (sub-block 2 qt), high nibbles the same + 32 (sub-block 2 qt + 1).
+// Lane (r8, u, rh): rows r0 + 8 (rh + 2 k) + r8 for k < 2; the 8 lanes of each store phase
+// write 8 rows' same unit, distinct banks after the swizzle.
+__device__ __forceinline__ void q4k_stage_decode(const uint8_t *pk, __half *b, int qt, int r0,
+                                                 int lane) {
+  const int r8 = lane & 7, u = (lane >> 3) & 1, rh = lane >> 4;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int r = r0 + 8 * (rh + 2 * k) + r8;
+    const uint8_t *row = pk + r * 144;
+    // the quarter's two 6-bit sub-block scales (scale bytes s0..s11 at row + 4): for
+    // j < 4, s_j & 63; for j >= 4, (s_{j+4} & 15) | (s_{j-4} >> 6) << 4
+    const uint32_t s03 = *reinterpret_cast<const uint32_t *>(row + 4);
+    uint32_t scp;
+    if (qt < 2) {
+      scp = (s03 >> (16 * qt)) & 0x3F3Fu;
+    } else {
+      const int sh = 16 * (qt - 2);
+      const uint32_t s811 = *reinterpret_cast<const uint32_t *>(row + 12);
+      scp = ((s811 >> sh) & 0x0F0Fu) | (((s03 >> sh) & 0xC0C0u) >> 2);
+    }
+    __half2 slo, mlo, shi, mhi;
+    q4k_scale_pair(scp, 0x4040u, slo, mlo);
+    q4k_scale_pair(scp, 0x4141u, shi, mhi);
+    const uint8_t *wp = row + 16 + 8 * qt + 4 * u;
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) w[t] = *reinterpret_cast<const uint32_t *>(wp + 32 * t);
+    uint8_t *brow = reinterpret_cast<uint8_t *>(b) + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int tp = 0; tp < 2; ++tp) {
+      const uint32_t wa = w[2 * tp], wb = w[2 * tp + 1];
+      // elements 16 u + 8 tp .. + 7 (unit 2 u + tp), then the same + 32 (unit 4 + 2 u + tp)
+      *reinterpret_cast<uint4 *>(brow + (((2 * u + tp) ^ sw) << 4)) =
+          make_uint4(q4k_pair(wa, 0, slo, mlo), q4k_pair(wa, 8, slo, mlo),
+                     q4k_pair(wb, 0, slo, mlo), q4k_pair(wb, 8, slo, mlo));
+      *reinterpret_cast<uint4 *>(brow + (((4 + 2 * u + tp) ^ sw) << 4)) =
+          make_uint4(q4k_pair(wa, 4, shi, mhi), q4k_pair(wa, 12, shi, mhi),
+                     q4k_pair(wb, 4, shi, mhi), q4k_pair(wb, 12, shi, mhi));
+    }
+  }
+}
 // K-major operand in the 128-byte swizzle layout TMA writes: 8-row groups of
 // 1024 bytes (SBO), leading offset unused (16), descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
@@ -271,13 +380,15 @@ __device__ __forceinline__ void tc_fence_after() {
         "=r"(r[31])                                                                           \
       : "r"(taddr))
 
-template <int TYPE, bool DOTS, bool QF = false>
-__global__ void __launch_bounds__(NTHR, 1)
+template <int TYPE, bool DOTS, bool QF = false, bool PW = false>
+__global__ void __launch_bounds__(nthr<PW>(), 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
                   const __grid_constant__ CUtensorMap tW2, const __grid_constant__ CUtensorMap tAm,
                   const __grid_constant__ CUtensorMap tBm, const __grid_constant__ CUtensorMap tSx,
                   const __grid_constant__ CUtensorMap tD, const TcArgs p, const QfArgs qf) {
-  using Sm = TcSmem<TYPE>;
+  using Sm = TcSmem<TYPE, PW>;
+  static_assert(!PW || TYPE == MQ_Q4_K, "decode-plane weight tiles are Q4_K's");
+  constexpr int NT = nthr<PW>();
   constexpr int NST = Sm::NST, SR = NST / 2;  // SR ring stages per MMA issuer
   static_assert(NST % 2 == 0, "the ring is split between two issuers");
   constexpr bool ODD = Sm::ODD, MIN = Sm::MIN;
@@ -302,8 +413,14 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(sa(&sm.full[s]), 1);
+      // with decode-plane weights a stage is full when its activation tile has landed and
+      // the four decoder warps have written its weight tile
+      mbar_init(sa(&sm.full[s]), PW ? 5 : 1);
       mbar_init(sa(&sm.empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sa(&sm.pfull[t]), 1);
+      mbar_init(sa(&sm.pempty[t]), 4);  // one arrival per decoder warp
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(sa(&sm.tfull[t]), 1);
@@ -330,14 +447,59 @@ __global__ void __launch_bounds__(NTHR, 1)
   // load, and everything that reads xq or writes the outputs follows its loads
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // ---- weight decoders (Q4_K from its decode plane): decoder warp dw writes rows
+  // 32 dw .. 32 dw + 31 of every stage's weight tile.  They follow the producer's fill order;
+  // a stage's tile is written once the MMA has released the stage (its previous round), and
+  // the chunk slot is released after the chunk's fourth quarter.  Min-term fills (TMA only)
+  // get the decoders' arrivals too, so that every fill completes the same count.
+  auto decode_weights = [&](int dw) {
+    int c0 = 0, c1 = 0;
+    for (int t = blockIdx.x, tl = 0; t < p.ntiles; t += gridDim.x, ++tl) {
+      for (int f = 0; f < npairs + nms; ++f) {
+        const int pr = f < npairs ? f : -1;
+        const int i = (tl * nuse + (f < npairs ? f : npairs + ((f - npairs) & 1))) & 1;
+        const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
+        if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 11, kWaitNs);
+        const int cg = tl * p.nchk + (pr >> 2);  // chunk in this CTA's sequence
+        if (pr >= 0) {
+          if ((pr & 3) == 0) mbar_wait(sa(&sm.pfull[cg & 1]), (cg >> 1) & 1, p.status, 12, kWaitNs);
+          q4k_stage_decode(sm.pk.v[PW ? (cg & 1) : 0], sm.b[s], pr & 3, 32 * dw, lane);
+          // the MMA (async proxy) reads what these generic stores wrote
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(sa(&sm.full[s]));
+          if (pr >= 0 && (pr & 3) == 3) mbar_arrive(sa(&sm.pempty[cg & 1]));
+        }
+      }
+    }
+  };
+
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
     if constexpr (QF) {  // wait until every CTA's rows are in xq (epilogue warps, below)
-      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NTHR) : "memory");
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NT) : "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads of xq
     }
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
-      const uint32_t bytes = (ODD ? 3 : 2) * kTileBytes;
+      const uint32_t bytes = (PW ? 1 : ODD ? 3 : 2) * kTileBytes;
+      // Decode-plane weights: chunk cg of this CTA's sequence (its tile cg / nchk, chunk
+      // cg % nchk of that tile's row group) goes to slot cg & 1 with one bulk copy; the first
+      // two go out before the wait for the previous kernel, chunk cg + 1 when the producer
+      // starts chunk cg, once chunk cg - 1 is decoded.
+      const int nchunks = PW && (int)blockIdx.x < p.ntiles
+                              ? ((p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * p.nchk
+                              : 0;
+      auto chunk_copy = [&](int cg) {
+        const int tt = (int)blockIdx.x + (cg / p.nchk) * (int)gridDim.x;
+        const uint8_t *src = p.wq + (int64_t(tt / p.ntm) * p.nchk + cg % p.nchk) * kPkBytes;
+        mbar_expect_tx(sa(&sm.pfull[cg & 1]), kPkBytes);
+        bulk_copy(sa(sm.pk.v[PW ? (cg & 1) : 0]), src, kPkBytes, sa(&sm.pfull[cg & 1]));
+      };
+      if constexpr (PW) {
+        for (int cg = 0; cg < 2 && cg < nchunks; ++cg) chunk_copy(cg);
+      }
       // Registered weights are never written by a kernel: the weight tiles of the first
       // tile's first kRamp fills (fill f of the first tile uses ring stage f) go out before
       // the wait for the previous kernel, the activation tiles of those stages after it.
@@ -346,7 +508,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       // round of all SMs (Q4_K 512 x 18944 x 3584: 109.5 -> 108.9 us; a ramp of 2 109.3).
       constexpr int kRamp = 3;
       int pre = 0;
-      if constexpr (!QF) {
+      if constexpr (!QF && !PW) {
         if (blockIdx.x < p.ntiles) {
           const int n0 = (blockIdx.x / p.ntm) * TN;
           pre = npairs < kRamp ? npairs : kRamp;
@@ -392,7 +554,16 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
           mbar_expect_tx(sa(&sm.full[s]), bytes);
           tma_2d(sa(sm.a[s]), &tA, pr * PK, m0, sa(&sm.full[s]));
-          tma_2d(sa(sm.b[s]), &tW, pr * PK, n0, sa(&sm.full[s]));
+          if constexpr (PW) {
+            const int cg = tl * p.nchk + (pr >> 2);
+            if ((pr & 3) == 0 && cg >= 1 && cg + 1 < nchunks) {
+              mbar_wait(sa(&sm.pempty[(cg + 1) & 1]), (((cg + 1) >> 1) - 1) & 1, p.status, 13,
+                        kWaitNs);
+              chunk_copy(cg + 1);
+            }
+          } else {
+            tma_2d(sa(sm.b[s]), &tW, pr * PK, n0, sa(&sm.full[s]));
+          }
           if constexpr (ODD) tma_2d(sa(sm.b2.v[ODD ? s : 0]), &tW2, pr * PK, n0, sa(&sm.full[s]));
         }
       }
@@ -443,8 +614,12 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       }
     }
+  } else if (PW && warp >= 4 + NEPI) {  // ---- weight decoders (warpgroup 5)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+    if constexpr (QF) asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NT) : "memory");
+    decode_weights(warp - (4 + NEPI));
   } else {  // ---- epilogue warps
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(reg_epi<PW>()));
     if constexpr (QF) {
       // Fused quantisation, with the activation ring (not in use yet) as scratch, then the
       // grid barrier: every row of x is in xq before any CTA's producer reads it.
@@ -468,7 +643,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       __threadfence();
       asm volatile("bar.sync %0, %1;" ::"n"(kBarEpi), "n"(32 * NEPI) : "memory");
       if (et == 0) grid_wait(qf.sync, gridDim.x, p.status);
-      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NTHR) : "memory");
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarAll), "n"(NT) : "memory");
     }
     const int e = warp - 4, q = warp & 3, hcol = e >> 2;  // rows 32q.., columns EC*hcol..
     const int rl = 32 * q + lane;
@@ -686,26 +861,35 @@ mq_status encode_scale_map(CUtensorMap *map, const void *ptr, int64_t cols, int6
   return MQ_OK;
 }
 
-template <int TYPE>
+template <int TYPE, bool PW = false>
 constexpr size_t smem_bytes() {
-  return sizeof(TcSmem<TYPE>) + 1024;
+  return sizeof(TcSmem<TYPE, PW>) + 1024;
 }
 
-template <int TYPE, bool DOTS, bool QF = false>
+template <int TYPE, bool DOTS, bool QF = false, bool PW = false>
 mq_status optin_t(const DeviceState *st, const char *name) {
-  const size_t smem = smem_bytes<TYPE>();
+  const size_t smem = smem_bytes<TYPE, PW>();
   if ((int)smem > st->smem_optin)
     return fail(MQ_ERR_LAUNCH, "%s needs %zu bytes of shared memory; the device allows %d", name,
                 smem, st->smem_optin);
-  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<TYPE, DOTS, QF>,
+  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<TYPE, DOTS, QF, PW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess)
     return fail(MQ_ERR_LAUNCH, "smem opt-in of %s (%zu bytes) refused: %s", name, smem,
                 cudaGetErrorName(e));
+  // the warpgroups' setmaxnreg split assumes this launch register count; with another one
+  // the epilogue's increase could never be granted, so the kernel is refused instead
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, mmq_tc_kernel<TYPE, DOTS, QF, PW>);
+  if (e != cudaSuccess)
+    return fail(MQ_ERR_LAUNCH, "attributes of %s: %s", name, cudaGetErrorName(e));
+  if (fa.numRegs != reg_launch<PW>())
+    return fail(MQ_ERR_LAUNCH, "%s was compiled with %d registers per thread; its register "
+                "split needs %d", name, fa.numRegs, reg_launch<PW>());
   return MQ_OK;
 }
 
-template <int TYPE, bool DOTS>
+template <int TYPE, bool DOTS, bool PW = false>
 mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap &tAm,
                    const CUtensorMap &tSx, const TcArgs &a, const QfArgs &qf, cudaStream_t s,
                    int sms, const char *name) {
@@ -722,16 +906,16 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
     // the previous kernel's tail; the producer waits for that kernel before its first load
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(NTHR, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<TYPE>();
+    cfg.blockDim = dim3(nthr<PW>(), 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<TYPE, PW>();
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, DOTS>, tA, tW, tW2, tAm,
-                                             tBm, tSx, tD, a, qf);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, DOTS, false, PW>, tA, tW,
+                                             tW2, tAm, tBm, tSx, tD, a, qf);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
       return fail(MQ_ERR_LAUNCH, "launch of %s (grid %u) failed: %s", name, grid.x,
@@ -743,8 +927,8 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
   // resident (the runtime refuses the launch otherwise)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(NTHR, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes<TYPE>();
+  cfg.blockDim = dim3(nthr<PW>(), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<TYPE, PW>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -752,8 +936,8 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e =
-      cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, false, true>, tA, tW, tW2, tAm, tBm, tSx, tD, a,
-                         qf);
+      cudaLaunchKernelEx(&cfg, mmq_tc_kernel<TYPE, false, true, PW>, tA, tW, tW2, tAm, tBm, tSx, tD,
+                         a, qf);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();  // the refused launch leaves no error behind for later calls
     return fail(MQ_ERR_LAUNCH, "cooperative launch of %s (grid %u) failed: %s", name, grid.x,
@@ -766,8 +950,10 @@ mq_status launch_t(const mq_weight *W, const CUtensorMap &tA, const CUtensorMap 
 
 mq_status encode_weight_maps(mq_weight *w) {
   static_assert(sizeof(CUtensorMap) <= sizeof(w->tmap_w), "tensor map storage");
-  mq_status s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w), w->mw, w->N, w->K,
-                               "weight");
+  // (a Q4_K weight registered with MQ_REG_MMQ_FROM_DECODE_PLANE has no f16 plane)
+  mq_status s = w->mw ? encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w), w->mw, w->N,
+                                       w->K, "weight")
+                      : MQ_OK;
   if (s != MQ_OK) return s;
   if (w->mw2)
     s = encode_f16_map(reinterpret_cast<CUtensorMap *>(w->tmap_w2), w->mw2, w->N, w->K,
@@ -778,6 +964,8 @@ mq_status encode_weight_maps(mq_weight *w) {
   if (s == MQ_OK)
     s = encode_scale_map(reinterpret_cast<CUtensorMap *>(w->tmap_td), w->td, w->np, w->K / 32,
                          "weight block scale");
+  // a valid (unused) map in the weight slot of the kernels that take none
+  if (s == MQ_OK && !w->mw) memcpy(w->tmap_w, w->tmap_td, sizeof(w->tmap_w));
   return s;
 }
 
@@ -795,6 +983,12 @@ mq_status init_kernels(DeviceState *st) {
   if ((s = optin_t<MQ_Q4_K, false, true>(st, "mmq_tc_kernel<Q4_K,fused>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q6_K, false, true>(st, "mmq_tc_kernel<Q6_K,fused>")) != MQ_OK) return s;
   if ((s = optin_t<MQ_Q4_1, false, true>(st, "mmq_tc_kernel<Q4_1,fused>")) != MQ_OK) return s;
+  if ((s = optin_t<MQ_Q4_K, false, false, true>(st, "mmq_tc_kernel<Q4_K,plane>")) != MQ_OK)
+    return s;
+  if ((s = optin_t<MQ_Q4_K, true, false, true>(st, "mmq_tc_kernel<Q4_K,plane,dots>")) != MQ_OK)
+    return s;
+  if ((s = optin_t<MQ_Q4_K, false, true, true>(st, "mmq_tc_kernel<Q4_K,plane,fused>")) != MQ_OK)
+    return s;
   return MQ_OK;
 }
 
@@ -850,6 +1044,8 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   a.status = st->status;
   a.debug_expire = debug_expire;
   a.swiglu = W->ffn_gu;
+  a.wq = W->q;
+  a.nchk = W->nchunk;
   QfArgs qf;
   qf.x = D == nullptr ? x : nullptr;  // the block-dot export is never fused
   qf.xq = const_cast<uint8_t *>(base);
@@ -857,6 +1053,12 @@ mq_status launch_mmq(const mq_weight *W, const void *xq, float *y, int32_t *D, i
   const bool dots = D != nullptr;
   switch (W->type) {
     case MQ_Q4_K:
+      if (!W->mw)  // registered without the f16 plane: the weight tiles come from the decode plane
+        return dots ? launch_t<MQ_Q4_K, true, true>(W, tA, tAm, tSx, a, qf, s, st->sms,
+                                                    "mmq_tc_kernel<Q4_K,plane,dots>")
+                    : launch_t<MQ_Q4_K, false, true>(W, tA, tAm, tSx, a, qf, s, st->sms,
+                                                     "mmq_tc_kernel<Q4_K,plane>");
+      [[fallthrough]];
     case MQ_Q5_K:
       return dots ? launch_t<MQ_Q4_K, true>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q4_K,dots>")
                   : launch_t<MQ_Q4_K, false>(W, tA, tAm, tSx, a, qf, s, st->sms, "mmq_tc_kernel<Q4_K>");

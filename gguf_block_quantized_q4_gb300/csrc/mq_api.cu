@@ -223,8 +223,12 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
   *out = nullptr;
   mq_status s = check_type_shape(site, type, N, K);
   if (s != MQ_OK) return s;
-  if (flags & ~MQ_REG_NO_MMQ_PLANE)
-    return fail(MQ_ERR_ARG, "%s: unknown flag bits 0x%x", site, flags & ~MQ_REG_NO_MMQ_PLANE);
+  const uint32_t known = MQ_REG_NO_MMQ_PLANE | MQ_REG_MMQ_FROM_DECODE_PLANE;
+  if (flags & ~known)
+    return fail(MQ_ERR_ARG, "%s: unknown flag bits 0x%x", site, flags & ~known);
+  if ((flags & MQ_REG_MMQ_FROM_DECODE_PLANE) && type != MQ_Q4_K)
+    return fail(MQ_ERR_ARG, "%s: MQ_REG_MMQ_FROM_DECODE_PLANE is for Q4_K weights (type %d)",
+                site, type);
   size_t expect = size_t(N) * size_t(K / block_elems(type)) * size_t(block_bytes(type));
   if (nbytes != expect)
     return fail(MQ_ERR_PAYLOAD,
@@ -284,7 +288,10 @@ static mq_status register_impl(const char *site, mq_type type, const void *host_
   // f16 / bf16 weights have no integer form and no prefill planes
   const bool mmq = !(flags & MQ_REG_NO_MMQ_PLANE) && !float_type(type);
   if (mmq) {
-    if ((s = alloc_plane(&w->mw, size_t(N) * K * 2, &total, "prefill operand")) != MQ_OK)
+    // with MQ_REG_MMQ_FROM_DECODE_PLANE the Q4_K MMQ expands the decode-plane tiles in
+    // shared memory instead of reading an f16 integer plane
+    if (!(flags & MQ_REG_MMQ_FROM_DECODE_PLANE) &&
+        (s = alloc_plane(&w->mw, size_t(N) * K * 2, &total, "prefill operand")) != MQ_OK)
       return cleanup(s);
     if (type == MQ_Q6_K &&
         (s = alloc_plane(&w->mw2, size_t(N) * K * 2, &total, "prefill odd part")) != MQ_OK)
@@ -567,7 +574,7 @@ static mq_status mmq_common(const char *site, mq_type type, const mq_weight *W, 
   if (float_type(type))
     return fail(MQ_ERR_TYPE, "%s: type %d is an unquantised (f16/bf16) weight: it has no "
                 "integer MMQ form; use the matvec", site, type);
-  if (!W->mw)
+  if (!W->td)
     return fail(MQ_ERR_ARG, "%s: the weight was registered with MQ_REG_NO_MMQ_PLANE", site);
   if (M < 1 || M > (int64_t(1) << 31))
     return fail(MQ_ERR_ARG, "%s: M=%lld outside [1, 2^31]", site, (long long)M);

@@ -120,16 +120,18 @@ __global__ void repack_q4_k(const uint8_t *__restrict__ raw, int64_t N, int64_t 
       for (int u = 0; u < 2; ++u)
         for (int e = 0; e < 4; ++e)
           dst[16 + 32 * t + 4 * (2 * c + u) + e] = src[16 + 32 * c + 16 * u + 4 * t + kQ4kPerm[e]];
-  if (mw) {
+  if (td) {  // the prefill planes; the f16 integer plane only where one is asked for
     const int64_t n = i / nsb, s = i % nsb;
     const float dd = f16bits(rd16(src)), dmin = f16bits(rd16(src + 2));
     for (int j = 0; j < 8; ++j) {
       int sc, m;
       q4k_scale_min(src + 4, j, sc, m);
       const int c = j / 2, h = j % 2;
-      for (int l = 0; l < 32; ++l) {
-        const int nib = (src[16 + 32 * c + l] >> (4 * h)) & 15;
-        mw[n * K + s * 256 + 32 * j + l] = __int2half_rn(sc * nib);
+      if (mw) {
+        for (int l = 0; l < 32; ++l) {
+          const int nib = (src[16 + 32 * c + l] >> (4 * h)) & 15;
+          mw[n * K + s * 256 + 32 * j + l] = __int2half_rn(sc * nib);
+        }
       }
       td[(s * 8 + j) * NP + n] = dd;
       tm[(s * 8 + j) * NP + n] = dmin * (float)m;
@@ -488,8 +490,9 @@ mq_status repack_weight(mq_weight *w, const uint8_t *raw, bool mmq, cudaStream_t
   } else if (w->type == MQ_Q4_K || w->type == MQ_Q5_K) {
     const int64_t n = N * (K / 256);
     if (w->type == MQ_Q4_K) {
+      // (no f16 integer plane when the MMQ expands the decode-plane tiles itself)
       repack_q4_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,
-                                                w->td, w->tm);
+                                                mmq ? w->td : nullptr, w->tm);
       MQ_LAUNCH_CHECK("repack_q4_k");
     } else {
       repack_q5_k<<<grid_for(n, T), T, 0, s>>>(raw, N, K, w->np, w->q, mmq ? w->mw : nullptr,

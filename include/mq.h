@@ -108,6 +108,12 @@ typedef void *mq_stream;
 #define MQ_REG_DEFAULT 0u
 /* Skip the prefill operand planes; mq_mmq then returns MQ_ERR_ARG for this weight. */
 #define MQ_REG_NO_MMQ_PLANE 1u
+/* Q4_K only (MQ_ERR_ARG for other types): build no f16 integer weight plane (2 bytes per
+ * element, 3.56x the GGUF payload); the MMQ calls copy the decode plane's 144-byte-per-row
+ * tiles and expand them to the same f16 integers sc_j * nib in shared memory.  Results are
+ * bit-identical to the default; the prefill MMQ takes longer (measured on 512 x 18944 x 3584:
+ * 152 against 109 us).  Device bytes fall from 5.3x to 1.8x the payload. */
+#define MQ_REG_MMQ_FROM_DECODE_PLANE 2u
 
 /* mq_init -- prepare the library for CUDA device `device` (makes it current on
  * the calling thread).  Queries the SM count and the shared-memory opt-in
@@ -129,7 +135,8 @@ mq_status mq_init(int device);
  *     tensor-core fragment reads 16-byte words (lossless: mq_weight_unpack
  *     restores the original bytes);
  *   - unless MQ_REG_NO_MMQ_PLANE: the prefill operand planes (integer-valued
- *     f16 weights [N][K] plus f32 block-scale planes).
+ *     f16 weights [N][K], none with MQ_REG_MMQ_FROM_DECODE_PLANE, plus f32
+ *     block-scale planes).
  * host_bytes: host pointer to nbytes bytes (read only during the call).
  * Validation before any device work: type supported (MQ_ERR_TYPE); N >= 1,
  * K >= 1, K a multiple of the block size (MQ_ERR_SHAPE); nbytes ==

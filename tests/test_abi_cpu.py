@@ -128,6 +128,15 @@ def test_register_rejects_unknown_flags_and_null(L):
     assert mq.STATUS[st] == "MQ_ERR_ARG"
 
 
+@pytest.mark.parametrize("qtype", [mq.Q8_0, mq.Q5_K, mq.Q6_K])
+def test_decode_plane_mmq_flag_is_for_q4_k_only(L, qtype):
+    """MQ_REG_MMQ_FROM_DECODE_PLANE (no f16 integer plane) exists for Q4_K alone; other
+    types are refused before any device work."""
+    blk, nb = {mq.Q8_0: (32, 34), mq.Q5_K: (256, 176), mq.Q6_K: (256, 210)}[qtype]
+    st, msg = _reg(L, qtype, np.zeros(nb, np.uint8), 1, blk, flags=mq.REG_MMQ_FROM_DECODE_PLANE)
+    assert mq.STATUS[st] == "MQ_ERR_ARG" and "Q4_K" in msg
+
+
 def test_quantize_rejects_bad_shape_before_device_work(L):
     assert mq.STATUS[L.mq_quantize_act(None, None, 4, 48, None)] == "MQ_ERR_SHAPE"
     assert mq.STATUS[L.mq_quantize_act(None, None, 0, 64, None)] == "MQ_ERR_ARG"
@@ -175,3 +184,30 @@ def test_ffn_gu_registration_validates_before_device_work(L):
     h = ctypes.c_void_p()
     st = L.mq_register_ffn_gu(mq.Q4_K, None, None, 16 * row, 16, 256, 0, ctypes.byref(h))
     assert mq.STATUS[st] == "MQ_ERR_ARG" and "NULL" in L.mq_last_error().decode()
+
+
+def test_weight_collected_during_a_capture_is_freed_after_it(monkeypatch):
+    """mq_weight_free synchronises the device, which would invalidate a stream capture in
+    progress; a Weight collected while the current stream is capturing keeps its handle
+    until the next free or registration outside the capture."""
+    freed = []
+
+    class FakeLib:
+        def mq_weight_free(self, h):
+            freed.append(h)
+            return 0
+
+    monkeypatch.setattr(mq, "_lib", FakeLib())
+    capturing = [True]
+    monkeypatch.setattr(mq, "_capturing", lambda: capturing[0])
+    w = mq.Weight.__new__(mq.Weight)
+    w.handle = 1234
+    del w
+    assert freed == [] and mq._deferred_frees == [1234]
+    mq._free_deferred()  # still capturing: nothing happens
+    assert freed == []
+    capturing[0] = False
+    w2 = mq.Weight.__new__(mq.Weight)
+    w2.handle = 99
+    del w2
+    assert freed == [1234, 99] and mq._deferred_frees == []

@@ -259,6 +259,37 @@ def test_blockdots_bit_exact_small(qtype, N, K, M):
     assert np.array_equal(D.cpu().numpy(), ref.astype(np.int32))
 
 
+# A Q4_K weight registered with MQ_REG_MMQ_FROM_DECODE_PLANE has no f16 integer plane: the
+# MMQ copies the decode-plane tiles (one 256-element chunk per bulk copy, two chunk slots)
+# and expands them in shared memory.  Shapes with one chunk per tile, one tile per CTA with
+# the in-loop chunk prefetch, and two or three tiles per CTA whose chunk sequence continues
+# across tiles; ragged N and M.  Block dots bit-exact against the oracle, y within its bound
+# and bit-identical to the default registration's (the same integers reach the MMA), also
+# through the fused quantise + MMQ.
+@pytest.mark.parametrize("N,K,M", [(25637, 256, 130), (2437, 768, 300), (12805, 768, 257)])
+def test_q4k_mmq_from_decode_plane_tiles(N, K, M):
+    qtype = 12
+    W = registered(qtype, N, K, 23, mq.REG_MMQ_FROM_DECODE_PLANE)
+    Wd = registered(qtype, N, K, 23)
+    assert W.info()[3] == Wd.info()[3] - N * K * 2  # the f16 plane alone is missing
+    x = synth.activations(M, K, seed=M + 3 * K)
+    xq, qs, sc, _, _ = gpu_quantize(x)
+    D = mq.mmq_blockdots(W, xq, M)
+    y = mq.mmq(W, xq, M)
+    yd = mq.mmq(Wd, xq, M)
+    yf, _ = mq.mmq_fused(W, torch.from_numpy(x).cuda(), mq.act_buffer(M, K))
+    torch.cuda.synchronize()
+    mq.stream_status()
+    assert np.array_equal(y.cpu().numpy(), yd.cpu().numpy())
+    assert np.array_equal(yf.cpu().numpy(), yd.cpu().numpy())
+    wb = weights(qtype, N, K, 23)
+    ref = oracle.blockdots(qtype, wb, N, K, qs)
+    assert np.array_equal(D.cpu().numpy(), ref.astype(np.int32))
+    if N * K * M <= 2437 * 768 * 300:
+        yref, bnd = oracle.mmq(qtype, wb, N, K, qs, sc)
+        assert_bound(y.cpu().numpy(), yref, bnd, f"Q4_K {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("name", ["q4_k_mmq_512x18944x3584", "q6_k_lm_head_151936x3584"])
 def test_blockdots_bit_exact_workload_tiles(name):
     """A 128 x 256 x (all blocks) tile of each prefill workload: the first 256 weight rows
@@ -456,7 +487,7 @@ def test_refused_launches_are_reported_and_leave_no_error(monkeypatch):
     assert e.value.name == "MQ_ERR_LAUNCH" and "matvec_kernel<Q4_K" in str(e.value)
     with pytest.raises(mq.MQError) as e:
         mq.mmq(W, xq, M)
-    assert e.value.name == "MQ_ERR_LAUNCH" and "mmq_tc_kernel<Q4_K>" in str(e.value)
+    assert e.value.name == "MQ_ERR_LAUNCH" and "mmq_tc_kernel<Q4_K" in str(e.value)
     monkeypatch.delenv("MQ_TEST_FAIL_LAUNCH")
     mq.init(0)
     y = gpu_matvec(W, x)
