@@ -72,6 +72,7 @@ __host__ __device__ constexpr int nthr() {
   return PW ? NTHR_PW : NTHR;
 }
 constexpr int kPkBytes = 128 * 144;     // one Q4_K decode-plane tile: 128 rows, one 256-K chunk
+constexpr int kPkSlots = 3;             // chunk slots: copies run two chunks ahead
 constexpr uint32_t TMEM_COLS = 512;     // accumulator pair i at columns 256*i .. +256
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kTestWaitNs = 1000000ull;
@@ -149,9 +150,9 @@ struct __align__(1024) TcSmem {
   Slots<__half, ODD ? NST : 0, TN * PK> b2;
   alignas(128) float gsx[2][8][TM];     // per group slot: row scales s
   alignas(128) float gd[2][8][TN];      // column scales d
-  Slots<uint8_t, PW ? 2 : 0, kPkBytes> pk;  // Q4_K decode-plane tiles (two chunk slots)
-  uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], pfull[2], pempty[2],
-      never;
+  Slots<uint8_t, PW ? kPkSlots : 0, kPkBytes> pk;  // Q4_K decode-plane tiles (chunk slots)
+  uint64_t full[NST], empty[NST], tfull[2], tempty[2], gfull[2], gempty[2], pfull[kPkSlots],
+      pempty[kPkSlots], never;
   uint32_t tmem;
 };
 
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(nthr<PW>(), 1)
       mbar_init(sa(&sm.full[s]), PW ? 5 : 1);
       mbar_init(sa(&sm.empty[s]), 1);
     }
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < kPkSlots; ++t) {
       mbar_init(sa(&sm.pfull[t]), 1);
       mbar_init(sa(&sm.pempty[t]), 4);  // one arrival per decoder warp
     }
@@ -461,16 +462,18 @@ __global__ void __launch_bounds__(nthr<PW>(), 1)
         const int c = i ? c1++ : c0++, s = i + 2 * (c % SR), q = c / SR;
         if (q >= 1) mbar_wait(sa(&sm.empty[s]), (q - 1) & 1, p.status, 11, kWaitNs);
         const int cg = tl * p.nchk + (pr >> 2);  // chunk in this CTA's sequence
+        const int ps = cg % kPkSlots;            // its slot, round cg / kPkSlots
         if (pr >= 0) {
-          if ((pr & 3) == 0) mbar_wait(sa(&sm.pfull[cg & 1]), (cg >> 1) & 1, p.status, 12, kWaitNs);
-          q4k_stage_decode(sm.pk.v[PW ? (cg & 1) : 0], sm.b[s], pr & 3, 32 * dw, lane);
+          if ((pr & 3) == 0)
+            mbar_wait(sa(&sm.pfull[ps]), (cg / kPkSlots) & 1, p.status, 12, kWaitNs);
+          q4k_stage_decode(sm.pk.v[PW ? ps : 0], sm.b[s], pr & 3, 32 * dw, lane);
           // the MMA (async proxy) reads what these generic stores wrote
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(sa(&sm.full[s]));
-          if (pr >= 0 && (pr & 3) == 3) mbar_arrive(sa(&sm.pempty[cg & 1]));
+          if (pr >= 0 && (pr & 3) == 3) mbar_arrive(sa(&sm.pempty[ps]));
         }
       }
     }
@@ -485,20 +488,21 @@ __global__ void __launch_bounds__(nthr<PW>(), 1)
     if (warp == 0 && lane == 0) {  // ---- TMA producer (operands and group scales)
       const uint32_t bytes = (PW ? 1 : ODD ? 3 : 2) * kTileBytes;
       // Decode-plane weights: chunk cg of this CTA's sequence (its tile cg / nchk, chunk
-      // cg % nchk of that tile's row group) goes to slot cg & 1 with one bulk copy; the first
-      // two go out before the wait for the previous kernel, chunk cg + 1 when the producer
-      // starts chunk cg, once chunk cg - 1 is decoded.
+      // cg % nchk of that tile's row group) goes to slot cg % kPkSlots with one bulk copy; the
+      // first kPkSlots go out before the wait for the previous kernel, chunk cg + 2 when the
+      // producer starts chunk cg, once chunk cg - 1 (the slot's previous chunk) is decoded.
       const int nchunks = PW && (int)blockIdx.x < p.ntiles
                               ? ((p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * p.nchk
                               : 0;
       auto chunk_copy = [&](int cg) {
         const int tt = (int)blockIdx.x + (cg / p.nchk) * (int)gridDim.x;
         const uint8_t *src = p.wq + (int64_t(tt / p.ntm) * p.nchk + cg % p.nchk) * kPkBytes;
-        mbar_expect_tx(sa(&sm.pfull[cg & 1]), kPkBytes);
-        bulk_copy(sa(sm.pk.v[PW ? (cg & 1) : 0]), src, kPkBytes, sa(&sm.pfull[cg & 1]));
+        const int ps = cg % kPkSlots;
+        mbar_expect_tx(sa(&sm.pfull[ps]), kPkBytes);
+        bulk_copy(sa(sm.pk.v[PW ? ps : 0]), src, kPkBytes, sa(&sm.pfull[ps]));
       };
       if constexpr (PW) {
-        for (int cg = 0; cg < 2 && cg < nchunks; ++cg) chunk_copy(cg);
+        for (int cg = 0; cg < kPkSlots && cg < nchunks; ++cg) chunk_copy(cg);
       }
       // Registered weights are never written by a kernel: the weight tiles of the first
       // tile's first kRamp fills (fill f of the first tile uses ring stage f) go out before
@@ -555,11 +559,12 @@ __global__ void __launch_bounds__(nthr<PW>(), 1)
           mbar_expect_tx(sa(&sm.full[s]), bytes);
           tma_2d(sa(sm.a[s]), &tA, pr * PK, m0, sa(&sm.full[s]));
           if constexpr (PW) {
-            const int cg = tl * p.nchk + (pr >> 2);
-            if ((pr & 3) == 0 && cg >= 1 && cg + 1 < nchunks) {
-              mbar_wait(sa(&sm.pempty[(cg + 1) & 1]), (((cg + 1) >> 1) - 1) & 1, p.status, 13,
+            // chunk cg + 2 into the slot of chunk cg - 1
+            const int cg = tl * p.nchk + (pr >> 2), cn = cg + kPkSlots - 1;
+            if ((pr & 3) == 0 && cg >= 1 && cn < nchunks) {
+              mbar_wait(sa(&sm.pempty[cn % kPkSlots]), (cn / kPkSlots - 1) & 1, p.status, 13,
                         kWaitNs);
-              chunk_copy(cg + 1);
+              chunk_copy(cn);
             }
           } else {
             tma_2d(sa(sm.b[s]), &tW, pr * PK, n0, sa(&sm.full[s]));

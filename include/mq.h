@@ -112,7 +112,7 @@ typedef void *mq_stream;
  * element, 3.56x the GGUF payload); the MMQ calls copy the decode plane's 144-byte-per-row
  * tiles and expand them to the same f16 integers sc_j * nib in shared memory.  Results are
  * bit-identical to the default; the prefill MMQ takes longer (measured on 512 x 18944 x 3584:
- * 152 against 109 us).  Device bytes fall from 5.3x to 1.8x the payload. */
+ * 151 against 110 us).  Device bytes fall from 5.3x to 1.8x the payload. */
 #define MQ_REG_MMQ_FROM_DECODE_PLANE 2u
 
 /* mq_init -- prepare the library for CUDA device `device` (makes it current on

@@ -260,7 +260,7 @@ def test_blockdots_bit_exact_small(qtype, N, K, M):
 
 
 # A Q4_K weight registered with MQ_REG_MMQ_FROM_DECODE_PLANE has no f16 integer plane: the
-# MMQ copies the decode-plane tiles (one 256-element chunk per bulk copy, two chunk slots)
+# MMQ copies the decode-plane tiles (one 256-element chunk per bulk copy, three chunk slots)
 # and expands them in shared memory.  Shapes with one chunk per tile, one tile per CTA with
 # the in-loop chunk prefetch, and two or three tiles per CTA whose chunk sequence continues
 # across tiles; ragged N and M.  Block dots bit-exact against the oracle, y within its bound
