@@ -40,6 +40,12 @@
 //                 Q4_K, Q6_K: a = s_m * D (first block of a super-block), then
 //                             a += s_m * D; per super-block y += d_n * a
 //               and frees the accumulator pair after its second block.
+//   Q4_K weights registered without the f16 plane (MQ_REG_MMQ_FROM_DECODE_PLANE) run a
+//   24-warp form: the producer bulk-copies the decode plane's 128-row x 144-byte tiles (one
+//   per 256-K chunk, two chunks ahead, three slots) instead of the weight tiles, and a sixth
+//   warpgroup of four decoder warps writes each stage's weight tile, the same f16 integers
+//   sc_j*nib, into the ring in the layout TMA gives the plane's tiles; 4 ring stages; registers
+//   80 at launch, 32 / 104 / 32 after setmaxnreg.
 // Min term (Q4_K: dmin*m_j per sub-block, subtracted; Q4_1: the block min m, added, so
 // its plane holds -m).  sum_b (s*S)_m,b * (dmin*m_j)_n,b is a product of rank K/32;
 // the tensor cores form it once per tile, after the main loop, from three f16
