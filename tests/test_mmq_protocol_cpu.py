@@ -8,49 +8,17 @@ deadlock) and every read must see the data meant for it: the MMA the stage's act
 weight tiles of its fill (at issue and at completion), the decoders the chunk of their fill,
 the epilogue the accumulator of its use and the scales of its group.  The index arithmetic
 of each role is the kernel's, restated.  Planted protocol mistakes must be caught."""
-import random
-
 import pytest
+
+from tests.protocol_model import Bar, Violation, run
 
 K_RAMP = 3
 PK_SLOTS = 3
 
 
-class Violation(Exception):
-    pass
-
-
-class Bar:
-    def __init__(self, count):
-        self.count, self.pending, self.tx, self.phase = count, count, 0, 0
-
-    def _check(self):
-        if self.pending == 0 and self.tx == 0:
-            self.phase += 1
-            self.pending = self.count
-
-    def arrive(self):
-        if self.pending == 0:  # the phase still waits for bytes: the count would underflow
-            raise Violation("arrival beyond the barrier's count")
-        self.pending -= 1
-        self._check()
-
-    def expect_tx(self, n):  # mbarrier.arrive.expect_tx
-        self.tx += n
-        self.arrive()
-
-    def complete_tx(self, n):
-        self.tx -= n
-        self._check()
-
-    def ready(self, parity):
-        return (self.phase & 1) != parity
-
-
 def run_cta(ntiles, grid, b, ntm, nb, dots, pw, seed, bug=None):
     """One CTA (blockIdx b of `grid`) of a Q4_K MMQ over ntiles output tiles (ntm along M),
     nb 32-element blocks along K.  Returns the number of scheduling steps."""
-    rnd = random.Random(seed)
     NST = 4 if pw else 6
     SR = NST // 2
     npairs, ngroups, nchk = (nb + 1) // 2, (nb + 7) >> 3, nb // 8
@@ -232,30 +200,7 @@ def run_cta(ntiles, grid, b, ntm, nb, dots, pw, seed, bug=None):
     agents = [producer(), issuer(0), issuer(1), epilogue()]
     if pw:
         agents += [decoder(d) for d in range(4)]
-    waits = [None] * len(agents)
-    alive = [True] * len(agents)
-    steps = 0
-    while True:
-        steps += 1
-        cands = [("a", k) for k in range(len(agents))
-                 if alive[k] and (waits[k] is None or waits[k][0].ready(waits[k][1]))]
-        cands += [("e", k) for k in range(len(events))]
-        cands += [("m", k) for k in range(2) if mma_q[k]]
-        if not cands:
-            if any(alive) or events:
-                raise Violation("deadlock")
-            return steps
-        kind, k = rnd.choice(cands)
-        if kind == "e":
-            events.pop(k)()
-        elif kind == "m":
-            mma_q[k].pop(0)()
-        else:
-            try:
-                waits[k] = next(agents[k])
-            except StopIteration:
-                alive[k] = False
-                waits[k] = None
+    return run(agents, events, mma_q, seed)
 
 
 SHAPES = [  # ntiles, grid, ntm, nb: one tile, several per CTA, one chunk per tile, many
