@@ -9,7 +9,8 @@ to the team-0 warp of the same rows through a buffer per unit parity.  Bulk copi
 any order.  Every run must finish and every read must see the chunk (or unit) it is meant
 for.  The index arithmetic is the kernel's, restated.  Planted mistakes must be caught: an
 odd ring depth and teams by the unit-local chunk parity (the two failures met while the
-kernel was built) and a copy warp that does not wait for a stage to be released."""
+kernel was built) and a copy warp that does not wait for a stage to be released.  The
+split-K kernel's simpler pipeline (csrc/matvec.cu) is modelled at the end."""
 import pytest
 
 from tests.protocol_model import Bar, Violation, run
@@ -135,6 +136,95 @@ def test_planted_protocol_mistakes_are_caught(bug, ns, nchunk):
     for seed in range(200):
         try:
             run_cta(4, 1, 0, nchunk, 1, False, seed=seed, ns=ns, bug=bug)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+# ---- the split-K matvec (csrc/matvec.cu): one CTA per (row group, K slice) -------------
+# The copy warp fills a stage with the weight tile and the x chunk of every batch row (one
+# transaction barrier; the first ring round's weights before the wait for the previous
+# kernel, its x after); the x warps convert the staged x into a fragment slot and release the
+# stage (before the conversion with x in registers, "early", or after it); the eight compute
+# warps read their weights, release the stage, wait for the slot, read it and release it.
+
+def run_split(nch, xwarps, early, seed, ns=2, fs_n=2, bug=None):
+    ncomp = 8
+    wfull, wempty = [Bar(1) for _ in range(ns)], [Bar(ncomp + xwarps) for _ in range(ns)]
+    ffull, fempty = [Bar(xwarps) for _ in range(fs_n)], [Bar(ncomp) for _ in range(fs_n)]
+    w_tag, x_tag = [None] * ns, [None] * ns
+    f_tag = [[None] * xwarps for _ in range(fs_n)]
+    events = []
+
+    def fill(i, weights=True, x=True):
+        s = i % ns
+        if weights:
+            wfull[s].expect_tx(2)
+            events.append(lambda s=s, i=i: (w_tag.__setitem__(s, i), wfull[s].complete_tx(1)))
+        if x:
+            events.append(lambda s=s, i=i: (x_tag.__setitem__(s, i), wfull[s].complete_tx(1)))
+
+    def copies():
+        pre = min(nch, ns)
+        for i in range(pre):
+            fill(i, x=False)
+        for i in range(pre):
+            fill(i, weights=False)
+        for i in range(pre, nch):
+            if bug != "copy_skips_empty":
+                yield wempty[i % ns], ((i // ns) - 1) & 1
+            fill(i)
+
+    def x_warp(xi):
+        for i in range(nch):
+            s, fs = i % ns, i % fs_n
+            yield wfull[s], (i // ns) & 1
+            if early:
+                if x_tag[s] != i:
+                    raise Violation(f"x warp {xi} read x of chunk {x_tag[s]} for {i}")
+                wempty[s].arrive()
+            if i >= fs_n:
+                yield fempty[fs], ((i // fs_n) - 1) & 1
+            if not early and x_tag[s] != i:
+                raise Violation(f"x warp {xi} read x of chunk {x_tag[s]} for {i}")
+            f_tag[fs][xi] = i
+            ffull[fs].arrive()
+            if not early:
+                wempty[s].arrive()
+
+    def compute(w):
+        for i in range(nch):
+            s, fs = i % ns, i % fs_n
+            yield wfull[s], (i // ns) & 1
+            if w_tag[s] != i:
+                raise Violation(f"compute warp {w} read weights of chunk {w_tag[s]} for {i}")
+            if bug == "release_slot_first":
+                fempty[fs].arrive()
+            wempty[s].arrive()
+            yield ffull[fs], (i // fs_n) & 1
+            if any(v != i for v in f_tag[fs]):
+                raise Violation(f"compute warp {w} read fragments {f_tag[fs]} for {i}")
+            if bug != "release_slot_first":
+                fempty[fs].arrive()
+
+    agents = [copies()] + [x_warp(k) for k in range(xwarps)] + [compute(w) for w in range(8)]
+    return run(agents, events, [], seed)
+
+
+@pytest.mark.parametrize("fs_n", [2, 3])  # fragment slots: 3 for Q4_K / Q5_K, else 2
+@pytest.mark.parametrize("xwarps,early", [(1, False), (1, True), (2, False), (2, True)])
+def test_split_k_random_schedules_finish_and_read_what_they_should(xwarps, early, fs_n):
+    for nch in (1, 2, 3, 5, 8, 14):
+        for seed in range(40):
+            run_split(nch, xwarps, early, seed=101 * nch + seed, fs_n=fs_n)
+
+
+@pytest.mark.parametrize("bug", ["copy_skips_empty", "release_slot_first"])
+def test_split_k_planted_mistakes_are_caught(bug):
+    caught = 0
+    for seed in range(200):
+        try:
+            run_split(8, 2, True, seed=seed, bug=bug)
         except Violation:
             caught += 1
     assert caught > 0
