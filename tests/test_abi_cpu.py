@@ -211,3 +211,23 @@ def test_weight_collected_during_a_capture_is_freed_after_it(monkeypatch):
     w2.handle = 99
     del w2
     assert freed == [1234, 99] and mq._deferred_frees == []
+
+
+def test_binding_constants_match_the_header():
+    """The binding's registration flags, type codes and static-scratch size are the values
+    include/mq.h defines."""
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "mq.h")).read()
+    defs = dict(re.findall(r"#define\s+(MQ_\w+)\s+\(?(\w+)u?\)?", src))
+
+    def val(name):
+        return int(defs[name].rstrip("uU"), 0)
+    assert val("MQ_REG_DEFAULT") == mq.REG_DEFAULT
+    assert val("MQ_REG_NO_MMQ_PLANE") == mq.REG_NO_MMQ_PLANE
+    assert val("MQ_REG_MMQ_FROM_DECODE_PLANE") == mq.REG_MMQ_FROM_DECODE_PLANE
+    assert len({mq.REG_NO_MMQ_PLANE, mq.REG_MMQ_FROM_DECODE_PLANE}) == 2
+    types = dict((k, int(v)) for k, v in re.findall(r"MQ_(\w+) = (\d+)", src))
+    for name in ("F16", "Q4_0", "Q4_1", "Q5_0", "Q5_1", "Q8_0", "Q4_K", "Q5_K", "Q6_K", "BF16"):
+        assert types[name] == getattr(mq, name), name
+    m = re.search(r"#define MQ_STATIC_XQ_BYTES \((\d+)u << (\d+)\)", src)
+    assert int(m.group(1)) << int(m.group(2)) == mq.STATIC_XQ_BYTES
